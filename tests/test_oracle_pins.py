@@ -1,0 +1,284 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test ties one part of the oracle to something other than itself: a
+size or a formula the pages print, a hand-packed block with hand-derived
+weights (tests/golden/), a library routine (numpy / torch conversions,
+numpy's float64 matmul), an exact-integer special case or a bijection.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from golden_io import all_fixtures, load
+
+pytestmark = pytest.mark.filterwarnings("ignore")
+
+T = {"Q4_K": 1, "Q6_K": 2, "Q8_0": 3, "Q5_0": 4, "Q4_0": 5}
+
+
+# ---------------------------------------------------------------- sizes --
+
+def test_block_sizes_and_bits_per_weight(oracle_mod):
+    o = oracle_mod
+    # "Hitchhiker's Guide", 11.2 / "12 -- llama.cpp / GGUF", bit layout:
+    # 256 weights -> 144 bytes = 4.5 bits per weight.
+    assert o.block_bytes(T["Q4_K"]) == 144 and o.block_elems(T["Q4_K"]) == 256
+    assert o.block_bytes(T["Q4_K"]) * 8 / 256 == 4.5
+    # "Hitchhiker's Guide", 11.1: Q4_0, 32 weights -> 18 bytes = 4.5 bits/weight.
+    assert o.block_bytes(T["Q4_0"]) == 18 and o.block_bytes(T["Q4_0"]) * 8 / 32 == 4.5
+    # "12 -- llama.cpp / GGUF", k-quants table: Q6_K at 6.6 bits/weight.
+    bpw6 = o.block_bytes(T["Q6_K"]) * 8 / o.block_elems(T["Q6_K"])
+    assert bpw6 == 6.5625 and round(bpw6, 1) == 6.6
+    # Q8_0: fp16 d + 32 int8 = 34 B; Q5_0: fp16 d + 4 B + 16 B = 22 B.
+    assert o.block_bytes(T["Q8_0"]) == 34 and o.block_elems(T["Q8_0"]) == 32
+    assert o.block_bytes(T["Q5_0"]) == 22 and o.block_elems(T["Q5_0"]) == 32
+    # Row bytes: cols / elems * block bytes (the workload's 9,030-byte rows).
+    assert o.row_bytes(T["Q6_K"], 11008) == 9030
+    assert o.row_bytes(T["Q4_K"], 1024) * 256 == 147456
+
+
+# ---------------------------------------------------- number formats --
+
+def test_half_decode_exhaustive(oracle_mod):
+    h = np.arange(65536, dtype=np.uint16)
+    ref = h.view(np.float16).astype(np.float32)
+    got = np.array([oracle_mod.half_to_float(int(v)) for v in h], np.float32)
+    fin = np.isfinite(ref)
+    assert np.array_equal(got[fin].view(np.uint32), ref[fin].view(np.uint32))
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(np.isinf(got), np.isinf(ref))
+
+
+def test_half_encode_matches_numpy(oracle_mod):
+    g = synth.rng(7)
+    vals = np.concatenate([
+        g.standard_normal(4000).astype(np.float32) * np.float32(10.0) ** g.integers(-9, 5, 4000),
+        np.arange(-2048, 2049, dtype=np.float32) * np.float32(2.0 ** -25),  # subnormal ties
+        np.array([65504, 65519.99, 65520, 1e6, -1e6, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26,
+                  1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11, 0.0, -0.0], np.float32)])
+    ref = vals.astype(np.float16).view(np.uint16)
+    got = np.array([oracle_mod.float_to_half(float(v)) for v in vals], np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_rounding_matches_torch(oracle_mod):
+    g = synth.rng(8)
+    bits = g.integers(0, 2 ** 32, 20000, dtype=np.uint64).astype(np.uint32)
+    vals = bits.view(np.float32)
+    vals = vals[np.isfinite(vals)]
+    ties = (np.arange(1, 2000, dtype=np.uint32) << 16 | 0x8000).view(np.float32)  # exact ties
+    vals = np.concatenate([vals, ties, -ties, np.array([0.0, -0.0, 3.4e38, 1e-40], np.float32)])
+    ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle_mod.float_to_bf16_array(vals)
+    assert np.array_equal(got, ref)
+    back = np.array([oracle_mod.bf16_to_float(int(b)) for b in ref[:100]], np.float32)
+    assert np.array_equal(back, torch.from_numpy(ref[:100].view(np.int16)).view(torch.bfloat16).float().numpy())
+
+
+# -------------------------------------------------- golden fixtures --
+
+@pytest.mark.parametrize("path", all_fixtures(), ids=lambda p: p.rsplit("/", 1)[-1])
+def test_golden_block(oracle_mod, path):
+    name, blk, expect = load(path)
+    t = T[name]
+    assert blk.size == oracle_mod.block_bytes(t)
+    w = oracle_mod.dequant(t, blk, 1, oracle_mod.block_elems(t))[0]
+    assert np.array_equal(w.astype(np.float64), expect), np.nonzero(w != expect)
+
+
+# --------------------------------------- nibble order: the Q4_0 routine --
+
+def _q4_0_as_printed(blocks: np.ndarray) -> np.ndarray:
+    """Q4_0 dequantization as "How LLM Inference Engines Work" ("Loading GGUF
+    Models") describes it: per 18-byte block an fp16 scale, then 16 bytes
+    whose low nibbles, minus 8, are the first 16 values and whose high
+    nibbles, minus 8, the last 16; everything times the scale."""
+    b = blocks.reshape(-1, 18)
+    scale = b[:, :2].copy().view(np.float16).astype(np.float32)
+    nib = b[:, 2:]
+    first = (nib & 15).astype(np.float32) - 8
+    second = (nib >> 4).astype(np.float32) - 8
+    return (np.concatenate([first, second], axis=1) * scale).reshape(-1)
+
+
+def test_q4_0_nibble_order_matches_page_routine(oracle_mod):
+    W = synth.rng(3).integers(0, 256, (64, 18), dtype=np.uint8)
+    W[:, :2] = (np.abs(synth.rng(4).standard_normal(64)) * 0.01).astype(np.float16).view(np.uint8).reshape(64, 2)
+    got = oracle_mod.dequant(T["Q4_0"], W.reshape(-1), 64, 32).reshape(-1)
+    assert np.array_equal(got, _q4_0_as_printed(W.reshape(-1)))
+
+
+def test_q5_0_low_nibbles_follow_q4_0_convention(oracle_mod):
+    # With every fifth bit clear, Q5_0 codes equal the Q4_0 codes of the same
+    # nibble bytes, so w_Q5_0 + 16d == w_Q4_0 + 8d element by element.
+    g = synth.rng(5)
+    nib = g.integers(0, 256, (32, 16), dtype=np.uint8)
+    d = np.full((32, 2), [0, 0x3C], np.uint8)  # d = 1.0
+    q5 = np.concatenate([d, np.zeros((32, 4), np.uint8), nib], axis=1).reshape(-1)
+    q4 = np.concatenate([d, nib], axis=1).reshape(-1)
+    w5 = oracle_mod.dequant(T["Q5_0"], q5, 32, 32)
+    w4 = oracle_mod.dequant(T["Q4_0"], q4, 32, 32)
+    assert np.array_equal(w5 + 16, w4 + 8)
+
+
+# ------------------------------------------------------ round trips --
+
+@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0"])
+def test_bytes_unpack_pack_bijection(oracle_mod, name):
+    # Every byte of these blocks is used, so unpack followed by pack must give
+    # back the same bytes (and unpack of that, the same fields).
+    t = T[name]
+    bb, nb = oracle_mod.block_bytes(t), 200
+    W = synth.rng(11).integers(0, 256, nb * bb, dtype=np.uint8)
+    codes, sc, mins, d, dmin = oracle_mod.unpack(t, W, nb)
+    dbits = np.array([oracle_mod.float_to_half(float(v)) for v in d], np.uint16)
+    dminbits = np.array([oracle_mod.float_to_half(float(v)) for v in dmin], np.uint16)
+    # fp16 NaN payloads do not survive a float round trip; restore raw bits.
+    off = {"Q4_K": 0, "Q6_K": 208, "Q8_0": 0, "Q5_0": 0, "Q4_0": 0}[name]
+    raw_d = W.reshape(nb, bb)[:, off:off + 2].copy().view(np.uint16).reshape(nb)
+    dbits = raw_d
+    if name == "Q4_K":
+        dminbits = W.reshape(nb, bb)[:, 2:4].copy().view(np.uint16).reshape(nb)
+    again = oracle_mod.pack(t, codes, sc, mins, dbits, dminbits)
+    assert np.array_equal(again, W)
+
+
+def test_q4k_every_6bit_value_in_every_slot(oracle_mod):
+    # 64 values x 8 scale slots and 64 x 8 min slots, others random.
+    g = synth.rng(12)
+    nb = 64 * 8
+    sc = np.zeros((nb, 16), np.int16)
+    mn = np.zeros((nb, 8), np.uint8)
+    sc[:, :8] = g.integers(0, 64, (nb, 8))
+    mn[:, :] = g.integers(0, 64, (nb, 8))
+    for i in range(nb):
+        v, slot = i % 64, i // 64
+        sc[i, slot] = v
+        mn[i, 7 - slot] = 63 - v
+    codes = g.integers(0, 16, (nb, 256)).astype(np.int16)
+    W = oracle_mod.pack(1, codes, sc, mn, np.full(nb, 0x3C00, np.uint16), np.full(nb, 0x3C00, np.uint16))
+    c2, sc2, mn2, d, dmin = oracle_mod.unpack(1, W, nb)
+    assert np.array_equal(c2, codes) and np.array_equal(sc2, sc) and np.array_equal(mn2, mn)
+    assert np.all(d == 1.0) and np.all(dmin == 1.0)
+
+
+def test_q6k_q8_q5_code_ranges_round_trip(oracle_mod):
+    g = synth.rng(13)
+    for name, lo, hi, be in (("Q6_K", 0, 64, 256), ("Q8_0", -128, 128, 32), ("Q5_0", 0, 32, 32)):
+        nb = 128
+        codes = g.integers(lo, hi, (nb, be)).astype(np.int16)
+        codes[0, :hi - lo if hi - lo <= be else be] = np.arange(lo, lo + min(hi - lo, be))
+        sc = np.zeros((nb, 16), np.int16)
+        if name == "Q6_K":
+            sc[:] = g.integers(-128, 128, (nb, 16))
+            sc[1, :] = [-128, 127] * 8
+        W = oracle_mod.pack(T[name], codes, sc, None, np.full(nb, 0x3800, np.uint16))
+        c2, sc2, _, d, _ = oracle_mod.unpack(T[name], W, nb)
+        assert np.array_equal(c2, codes)
+        if name == "Q6_K":
+            assert np.array_equal(sc2, sc)
+        assert np.all(d == 0.5)
+
+
+# --------------------------------------------- dequant formula checks --
+
+def test_q4k_formula_exact_in_fp32(oracle_mod):
+    # d*sc and dmin*m are exact products in fp32 (11 + 6 significant bits), so
+    # is (d*sc)*q (+ 4 bits); only the final subtraction rounds.  Hence the
+    # oracle's weight equals fl(fl64((d*sc)*q) - fl64(dmin*m)) computed in fp64.
+    W = synth.random_blocks("Q4_K", 8, 2048, 21)
+    codes, sc, mins, d, dmin = oracle_mod.unpack(1, W, 64)
+    ds = d[:, None].astype(np.float64) * sc[:, :8].astype(np.float64)
+    dm = dmin[:, None].astype(np.float64) * mins.astype(np.float64)
+    sub = np.repeat(np.arange(8), 32)
+    exact = ds[:, sub] * codes.astype(np.float64) - dm[:, sub]
+    got = oracle_mod.dequant(1, W, 8, 2048).reshape(64, 256)
+    assert np.array_equal(got, exact.astype(np.float32))
+
+
+def test_zero_scale_block_is_zero(oracle_mod):
+    for name in ("Q4_K", "Q6_K", "Q8_0", "Q5_0"):
+        W = synth.random_blocks(name, 2, 512, 22)
+        bb, be, doff, dmoff = synth.GEOMETRY[name]
+        B = W.reshape(-1, bb)
+        B[:, doff:doff + 2] = 0
+        if dmoff is not None:
+            B[:, dmoff:dmoff + 2] = 0
+        w = oracle_mod.dequant(T[name], W, 2, 512)
+        assert np.all(w == 0)
+
+
+# ------------------------------------------------------ dot products --
+
+@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q5_0"])
+@pytest.mark.parametrize("rows,cols,M", [(1, 256, 1), (3, 512, 2), (4, 1024, 3)])
+def test_gemv_matches_numpy_float64_matmul(oracle_mod, name, rows, cols, M):
+    t = T[name]
+    W = synth.random_blocks(name, rows, cols, 30 + rows)
+    x = synth.activations(M, cols, 31)
+    y, S = oracle_mod.gemv(t, W, rows, cols, x)
+    w = oracle_mod.dequant(t, W, rows, cols).astype(np.float64)
+    ref = x.astype(np.float64) @ w.T
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+    assert np.allclose(S, np.abs(x.astype(np.float64)) @ np.abs(w).T, rtol=1e-12)
+    assert np.all(S >= np.abs(y) - 1e-12)
+
+
+def test_gemv_exact_integer_case(oracle_mod):
+    # Q8_0 with d = 2^-3 and small-integer x: every product and partial sum is
+    # an exact binary fraction, so y equals (codes . x) * 2^-3 exactly, with
+    # the codes taken from the generator, not from the unpacker.
+    g = synth.rng(40)
+    rows, cols = 5, 256
+    codes = g.integers(-128, 128, (rows * cols // 32, 32)).astype(np.int16)
+    W = oracle_mod.pack(3, codes, None, None, np.full(rows * cols // 32, 0x3000, np.uint16))
+    x = g.integers(-8, 9, (2, cols)).astype(np.float32)
+    y, _ = oracle_mod.gemv(3, W, rows, cols, x)
+    expect = (x.astype(np.int64) @ codes.reshape(rows, cols).astype(np.int64).T) * 0.125
+    assert np.array_equal(y, expect)
+
+
+def test_gemm_bf16_is_gemv_on_rounded_activations(oracle_mod):
+    name, rows, cols, M = "Q4_K", 6, 512, 3
+    W = synth.random_blocks(name, rows, cols, 50)
+    Xb = synth.activations_bf16_bits(M, cols, 51)
+    Y, S = oracle_mod.gemm_bf16(1, W, rows, cols, Xb)
+    xf = torch.from_numpy(Xb.view(np.int16)).view(torch.bfloat16).float().numpy()
+    y2, S2 = oracle_mod.gemv(1, W, rows, cols, xf)
+    assert np.array_equal(Y, y2) and np.array_equal(S, S2)
+
+
+def test_entries_equal_full_products(oracle_mod):
+    name, rows, cols, M = "Q6_K", 9, 768, 4
+    W = synth.random_blocks(name, rows, cols, 60)
+    x = synth.activations(M, cols, 61)
+    Xb = synth.activations_bf16_bits(M, cols, 62)
+    y, S = oracle_mod.gemv(2, W, rows, cols, x)
+    Y, SY = oracle_mod.gemm_bf16(2, W, rows, cols, Xb)
+    mi = np.array([0, 3, 2, 1, 3]); ni = np.array([8, 0, 4, 4, 7])
+    ye, Se = oracle_mod.entries(2, W, rows, cols, mi, ni, x=x)
+    Ye, SYe = oracle_mod.entries(2, W, rows, cols, mi, ni, X_bits=Xb)
+    assert np.array_equal(ye, y[mi, ni]) and np.array_equal(Se, S[mi, ni])
+    assert np.array_equal(Ye, Y[mi, ni]) and np.array_equal(SYe, SY[mi, ni])
+
+
+# -------------------------------------------------------- quantizer --
+
+def test_quantizer_error_bounds(oracle_mod):
+    w = synth.normal_weights(16, 1024, 70)
+    # Q8_0: |w - wq| <= d/2 per block (the max element maps to +-127 exactly
+    # up to the fp16 rounding of d, which moves it by less than half a step).
+    W = oracle_mod.quantize(3, w)
+    dq = oracle_mod.dequant(3, W, 16, 1024)
+    _, _, _, d, _ = oracle_mod.unpack(3, W, 16 * 32)
+    err = np.abs(dq - w).reshape(-1, 32).max(axis=1)
+    assert np.all(err <= 0.5 * d * 1.01 + 1e-9)
+    # Q4_K: every weight within one code step (d*sc) of the input plus the
+    # min's rounding (dmin/2).
+    W = oracle_mod.quantize(1, w)
+    dq = oracle_mod.dequant(1, W, 16, 1024)
+    codes, sc, mins, d, dmin = oracle_mod.unpack(1, W, 64)
+    step = (d[:, None] * sc[:, :8]).repeat(32, axis=1).reshape(-1)
+    bound = step + np.repeat(dmin, 256) * 0.5 + 1e-6
+    assert np.all(np.abs(dq.reshape(-1) - w.reshape(-1)) <= bound)
