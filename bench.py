@@ -1,0 +1,405 @@
+"""Benchmark of the fused dequant-GEMV hot path on one Llama-7B-shaped decoder
+layer at decode batch 1 (q/k/v/o 4096x4096 Q4_K, gate/up 11008x4096 Q4_K,
+down 4096x11008 Q6_K; x fp32 ~ N(0, 1)).
+
+One step = the seven GEMVs of one layer through the C ABI (qk_gemv), i.e.
+one pass of the whole hot path: load packed blocks, unpack scales and codes,
+dequantize inside the dot product, accumulate, reduce.  The step cycles
+through distinct copies of the layer whose total exceeds the L2 cache, so
+every step streams its weights from HBM.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on
+the host cores instead (a bounded sample of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "Q4_K/Q6_K dequant-GEMV HBM GB/s (% of peak); dequant-GEMM TFLOP/s"
+L2_BYTES = 129 * 2 ** 20
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def layer_bytes(layer):
+    """Algorithmic bytes of one decode step of the layer: packed weights +
+    fp32 activations read + fp32 outputs written."""
+    import synth
+    tot = 0
+    for (_, name, rows, cols) in layer:
+        tot += rows * synth.row_bytes(name, cols) + 4 * cols + 4 * rows
+    return tot
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.f = None
+
+    def __enter__(self):
+        try:
+            self.f = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.f is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.f.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def build_layer_copies(dev, ncopies):
+    """ncopies distinct layers of packed weights on the device, plus one
+    activation vector, output and workspace per matrix."""
+    import torch
+    import gguf_quant_dequant_gb300 as qk
+    import synth
+    layer = synth.LLAMA7B_LAYER
+    Ws = [[synth.random_blocks_torch(name, rows, cols, 100 * c + i, dev)
+           for i, (_, name, rows, cols) in enumerate(layer)] for c in range(ncopies)]
+    g = torch.Generator(device=dev)
+    g.manual_seed(4242)
+    xs = [torch.randn((1, cols), device=dev, generator=g) for (_, _, _, cols) in layer]
+    ys = [torch.empty((1, rows), device=dev) for (_, _, rows, _) in layer]
+    ws_need = max(qk.gemv_workspace(synth.TYPE_IDS[name], rows, cols, 1) for (_, name, rows, cols) in layer)
+    ws = torch.empty(max(ws_need, 16), dtype=torch.uint8, device=dev)
+    return layer, Ws, xs, ys, ws
+
+
+def launches_per_step(layer):
+    import gguf_quant_dequant_gb300 as qk
+    import synth
+    n = 0
+    for (_, name, rows, cols) in layer:
+        n += 1 + (qk.gemv_workspace(synth.TYPE_IDS[name], rows, cols, 1) > 0)
+    return n
+
+
+def run_gpu(args):
+    import torch
+    import gguf_quant_dequant_gb300 as qk
+    import synth
+    from gguf_quant_dequant_gb300 import build as qkbuild
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    qkbuild.build()
+    qk.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    hbm_peak, peak_src = peaks()
+
+    wbytes = sum(rows * synth.row_bytes(name, cols) for (_, name, rows, cols) in synth.LLAMA7B_LAYER)
+    ncopies = max(2, -(-4 * L2_BYTES // wbytes))
+    layer, Ws, xs, ys, ws = build_layer_copies(dev, ncopies)
+    lb = layer_bytes(layer)
+
+    def step(c):
+        for i, (_, name, rows, cols) in enumerate(layer):
+            qk.gemv(synth.TYPE_IDS[name], Ws[c][i], rows, cols, xs[i], y=ys[i], ws=ws)
+
+    def sub_step(c, idx):
+        for i in idx:
+            (_, name, rows, cols) = layer[i]
+            qk.gemv(synth.TYPE_IDS[name], Ws[c][i], rows, cols, xs[i], y=ys[i], ws=ws)
+
+    # Warm the kernels up eagerly once (module load, attributes), then capture
+    # one CUDA graph per layer copy.
+    for c in range(ncopies):
+        step(c)
+    torch.cuda.synchronize()
+    graphs = []
+    for c in range(ncopies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(c)
+        graphs.append(g)
+    q4_idx = [i for i, l in enumerate(layer) if l[1] == "Q4_K"]
+    q4_graphs = []
+    for c in range(ncopies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            sub_step(c, q4_idx)
+        q4_graphs.append(g)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    K, W = args.steps, args.warmup
+    with Clocks(local) as clk:
+        t_end = time.time() + 1.0
+        i = 0
+        while i < W or time.time() < t_end:
+            graphs[i % ncopies].replay()
+            i += 1
+            if i % 64 == 0:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        _barrier(world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(K):
+            graphs[k % ncopies].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        _barrier(world)
+        torch.cuda.synchronize()
+        # Dominant kernel alone: the six Q4_K GEMVs of a layer, same rotation.
+        reps = max(K, 200)
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for k in range(reps):
+            q4_graphs[k % ncopies].replay()
+        f1.record(stream)
+        torch.cuda.synchronize()
+        q4_ms = f0.elapsed_time(f1)
+    clocks = clk.summary()
+    ms_max = _max_over_ranks(ms, world)
+    ms_step = ms_max / K
+    value = world * lb / (ms_step * 1e-3) / 1e9
+
+    q4_launch_bytes = sum(layer[i][2] * synth.row_bytes("Q4_K", layer[i][3]) + 4 * layer[i][3] + 4 * layer[i][2]
+                          for i in q4_idx) / len(q4_idx)
+    q4_launch_ms = q4_ms / (reps * len(q4_idx))
+    achieved = q4_launch_bytes / (q4_launch_ms * 1e-3) / 1e9
+
+    e2e = run_e2e(args, dev, layer, Ws[0], xs, lb) if rank == 0 else None
+    cpu = cpu_baseline(layer) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "q4_k/q6_k blocks, f32 activations and accumulation",
+            "data": "synthetic (seeded random blocks, x ~ N(0,1))",
+            "config": {"workload": "Llama-7B-shaped decoder layer, decode batch 1: q/k/v/o 4096x4096 Q4_K, "
+                                   "gate/up 11008x4096 Q4_K, down 4096x11008 Q6_K",
+                       "bytes_per_step": lb, "layer_copies_rotated": ncopies,
+                       "l2": f"inputs larger than L2: {ncopies} distinct layer copies "
+                             f"({ncopies * wbytes / 2**20:.0f} MiB) rotated per step",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "timing": "CUDA graph per layer copy, CUDA events on the launch stream"},
+            "frac_of_peak": round(value / world / hbm_peak, 4),
+            "roofline": {"bound": "hbm", "kernel": "gemv_kernel<Q4_K, MT=1>", "achieved": round(achieved, 2),
+                         "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s",
+                         "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                         "launch_bytes": int(q4_launch_bytes), "launch_us": round(q4_launch_ms * 1e3, 3)},
+            "gpu_launches": K * launches_per_step(layer),
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, dev, layer, Wd, xs, lb):
+    """Same step through the C ABI from pinned HOST buffers: every step copies
+    the layer's packed weights and activations host->device, runs the seven
+    GEMVs and copies the outputs back; all inside the timed region."""
+    import torch
+    import gguf_quant_dequant_gb300 as qk
+    import synth
+    Wh = [w.cpu().pin_memory() for w in Wd]
+    xh = [x.cpu().pin_memory() for x in xs]
+    yd = [torch.empty((1, rows), device=dev) for (_, _, rows, _) in layer]
+    yh = [torch.empty((1, rows)).pin_memory() for (_, _, rows, _) in layer]
+    xd = [torch.empty_like(x, device=dev) for x in xs]
+    Wdd = [torch.empty_like(w, device=dev) for w in Wd]
+    ws_need = max(qk.gemv_workspace(synth.TYPE_IDS[name], rows, cols, 1) for (_, name, rows, cols) in layer)
+    ws = torch.empty(max(ws_need, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for i, (_, name, rows, cols) in enumerate(layer):
+            Wdd[i].copy_(Wh[i], non_blocking=True)
+            xd[i].copy_(xh[i], non_blocking=True)
+            qk.gemv(synth.TYPE_IDS[name], Wdd[i], rows, cols, xd[i], y=yd[i], ws=ws)
+            yh[i].copy_(yd[i], non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    n = max(5, min(args.steps, 50))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    h2d = sum(w.numel() for w in Wh) + sum(4 * x.numel() for x in xh)
+    d2h = sum(4 * y.numel() for y in yh)
+    return {"value": round(lb / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n}
+
+
+def _oracle_layer_sample(row_div: int):
+    """Host inputs of the layer; with row_div > 1 only the first rows/row_div
+    rows of each matrix (a bounded sample of the same workload)."""
+    import synth
+    mats = []
+    for i, (nm, name, rows, cols) in enumerate(synth.LLAMA7B_LAYER):
+        r = max(1, rows // row_div)
+        W = synth.random_blocks(name, r, cols, 300 + i)
+        x = synth.activations(1, cols, 400 + i)
+        mats.append((synth.TYPE_IDS[name], W, r, cols, x, r * synth.row_bytes(name, cols) + 4 * cols + 4 * r))
+    return mats
+
+
+def cpu_baseline(layer, budget_s: float = 10.0):
+    """The oracle as it stands, single-threaded, on passes over one full layer
+    until about budget_s seconds have run."""
+    import oracle
+    oracle.build()
+    mats = _oracle_layer_sample(1)
+    t0 = time.perf_counter()
+    passes, nbytes = 0, 0
+    while True:
+        for (t, W, r, cols, x, b) in mats:
+            oracle.gemv(t, W, r, cols, x)
+            nbytes += b
+        passes += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{passes} full pass(es) of the layer's 7 GEMVs (batch 1), scalar C, fp64 accumulation",
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is the layer with every
+    matrix cut to its first 1/64 of rows (full K), timed on one host core."""
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    mats = _oracle_layer_sample(64)
+    sample_bytes = sum(m[5] for m in mats)
+    for _ in range(args.warmup):
+        for (t, W, r, cols, x, b) in mats:
+            oracle.gemv(t, W, r, cols, x)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for (t, W, r, cols, x, b) in mats:
+            oracle.gemv(t, W, r, cols, x)
+    dt = time.perf_counter() - t0
+    ms = dt / args.steps * 1e3
+    value = sample_bytes / (ms * 1e-3) / 1e9
+    sample = "Llama-7B layer at decode batch 1, first 1/64 of each matrix's rows, scalar C oracle"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "q4_k/q6_k blocks, f64 accumulation",
+        "data": "synthetic (seeded random blocks, x ~ N(0,1))",
+        "config": {"workload": "Llama-7B-shaped decoder layer, decode batch 1: q/k/v/o 4096x4096 Q4_K, "
+                               "gate/up 11008x4096 Q4_K, down 4096x11008 Q6_K",
+                   "bytes_per_step": sample_bytes, "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="qk", choices=["qk", "reference"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,163 @@
+"""Python binding of libqk (include/qk.h): argument marshalling only.
+
+Every computation runs in the library's CUDA kernels; this module passes
+device pointers, sizes and the current CUDA stream of PyTorch tensors, and
+raises QKError on a non-zero status.  There is no CPU fallback: if libqk.so
+has not been built, load() raises.
+
+Type ids: Q4_K = 1, Q6_K = 2, Q8_0 = 3, Q5_0 = 4.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+Q4_K, Q6_K, Q8_0, Q5_0 = 1, 2, 3, 4
+TYPES = {"Q4_K": Q4_K, "Q6_K": Q6_K, "Q8_0": Q8_0, "Q5_0": Q5_0}
+OUT_F32, OUT_BF16 = 0, 1
+STATUS = {0: "QK_OK", 1: "QK_ERR_TYPE", 2: "QK_ERR_SHAPE", 3: "QK_ERR_ALIGN", 4: "QK_ERR_NULL",
+          5: "QK_ERR_WORKSPACE", 6: "QK_ERR_CUDA", 7: "QK_ERR_TIMEOUT", 8: "QK_ERR_ARG"}
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqk.so")
+_lib = None
+_lock = threading.Lock()
+
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_sz = ctypes.c_size_t
+_int = ctypes.c_int
+
+# name: (restype, argtypes), exactly as declared in include/qk.h
+SIGNATURES = {
+    "qk_version": (_int, []),
+    "qk_block_bytes": (_sz, [_int]),
+    "qk_block_elems": (_int, [_int]),
+    "qk_row_bytes": (_sz, [_int, _i64]),
+    "qk_dequant": (_int, [_int, _p, _i64, _i64, _p, _int, _p]),
+    "qk_gemv_workspace": (_sz, [_int, _i64, _i64, _i64]),
+    "qk_gemv": (_int, [_int, _p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
+    "qk_gemm_workspace": (_sz, [_int, _i64, _i64, _i64]),
+    "qk_gemm": (_int, [_int, _p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
+    "qk_unpack": (_int, [_int, _p, _i64, _p, _p, _p, _p, _p, _p]),
+    "qk_device_status": (_int, [_p]),
+    "qk_last_error": (ctypes.c_char_p, []),
+}
+
+
+class QKError(RuntimeError):
+    def __init__(self, status: int, where: str, msg: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+def load() -> ctypes.CDLL:
+    """Load libqk.so (built in-tree by build.build()); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -m gguf_quant_dequant_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _check(st: int, where: str) -> None:
+    if st != 0:
+        raise QKError(st, where, load().qk_last_error().decode())
+
+
+def _stream(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def block_bytes(t: int) -> int:
+    return load().qk_block_bytes(t)
+
+
+def block_elems(t: int) -> int:
+    return load().qk_block_elems(t)
+
+
+def row_bytes(t: int, cols: int) -> int:
+    return load().qk_row_bytes(t, cols)
+
+
+def dequant(t: int, W, rows: int, cols: int, out=None, bf16: bool = False, stream=None):
+    """W: uint8 CUDA tensor of packed blocks -> out [rows, cols] fp32 / bf16."""
+    import torch
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.bfloat16 if bf16 else torch.float32, device=W.device)
+    _check(load().qk_dequant(t, _ptr(W), rows, cols, _ptr(out), OUT_BF16 if bf16 else OUT_F32,
+                             _stream(stream)), "qk_dequant")
+    return out
+
+
+def gemv_workspace(t: int, rows: int, cols: int, M: int) -> int:
+    return load().qk_gemv_workspace(t, rows, cols, M)
+
+
+def gemv(t: int, W, rows: int, cols: int, x, y=None, ws=None, stream=None):
+    """x fp32 CUDA [M, cols] -> y fp32 [M, rows]; ws allocated if needed."""
+    import torch
+    M = x.shape[0] if x.dim() == 2 else 1
+    if y is None:
+        y = torch.empty((M, rows), dtype=torch.float32, device=x.device)
+    need = gemv_workspace(t, rows, cols, M)
+    if ws is None and need:
+        ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load().qk_gemv(t, _ptr(W), rows, cols, _ptr(x), M, _ptr(y), _ptr(ws), nbytes, _stream(stream)),
+           "qk_gemv")
+    return y
+
+
+def gemm_workspace(t: int, rows: int, cols: int, M: int) -> int:
+    return load().qk_gemm_workspace(t, rows, cols, M)
+
+
+def gemm(t: int, W, rows: int, cols: int, X, Y=None, ws=None, stream=None):
+    """X bf16 CUDA [M, cols] -> Y fp32 [M, rows]."""
+    import torch
+    M = X.shape[0]
+    if Y is None:
+        Y = torch.empty((M, rows), dtype=torch.float32, device=X.device)
+    need = gemm_workspace(t, rows, cols, M)
+    if ws is None and need:
+        ws = torch.empty(need, dtype=torch.uint8, device=X.device)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load().qk_gemm(t, _ptr(W), rows, cols, _ptr(X), M, _ptr(Y), _ptr(ws), nbytes, _stream(stream)),
+           "qk_gemm")
+    return Y
+
+
+def unpack(t: int, W, nblocks: int, stream=None):
+    """-> (codes int16 [nblocks, elems], sc int16 [nblocks, 16], mins uint8
+    [nblocks, 8], d f32 [nblocks], dmin f32 [nblocks]) as CUDA tensors."""
+    import torch
+    dev = W.device
+    codes = torch.empty((nblocks, block_elems(t)), dtype=torch.int16, device=dev)
+    sc = torch.empty((nblocks, 16), dtype=torch.int16, device=dev)
+    mins = torch.empty((nblocks, 8), dtype=torch.uint8, device=dev)
+    d = torch.empty(nblocks, dtype=torch.float32, device=dev)
+    dmin = torch.empty(nblocks, dtype=torch.float32, device=dev)
+    _check(load().qk_unpack(t, _ptr(W), nblocks, _ptr(codes), _ptr(sc), _ptr(mins), _ptr(d), _ptr(dmin),
+                            _stream(stream)), "qk_unpack")
+    return codes, sc, mins, d, dmin
+
+
+def device_status(stream=None) -> None:
+    _check(load().qk_device_status(_stream(stream)), "qk_device_status")

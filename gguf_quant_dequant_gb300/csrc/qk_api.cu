@@ -1,0 +1,216 @@
+// qk_api.cu -- the extern "C" entry points of libqk (include/qk.h): argument
+// validation on the host, then a launch on the caller's stream.  Nothing here
+// allocates device memory; scratch comes from the caller's workspace.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/qk.h"
+#include "qk_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+// Kernel status word (bit 0: a bounded wait ran out).  One per device; its
+// address is looked up once per device and passed to the kernels.
+__device__ unsigned g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned* g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+qk_status fail(qk_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+qk_status fail(qk_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+qk_status cuda_fail(cudaError_t e, const char* where) {
+    return fail(QK_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool known_type(int t) { return t >= QK_Q4_K && t <= QK_Q5_0; }
+
+size_t block_bytes(int t) {
+    switch (t) {
+    case QK_Q4_K: return 144;
+    case QK_Q6_K: return 210;
+    case QK_Q8_0: return 34;
+    case QK_Q5_0: return 22;
+    }
+    return 0;
+}
+
+int block_elems(int t) {
+    switch (t) {
+    case QK_Q4_K: case QK_Q6_K: return 256;
+    case QK_Q8_0: case QK_Q5_0: return 32;
+    }
+    return 0;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Per-device state: status-word address and SM count, set up on first use.
+qk_status device_state(unsigned** status, int* sms) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(QK_ERR_ARG, "device %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_status_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        g_sm_count[dev] = n;
+        g_status_ptr[dev] = static_cast<unsigned*>(p);
+    }
+    if (status) *status = g_status_ptr[dev];
+    if (sms) *sms = g_sm_count[dev];
+    return QK_OK;
+}
+
+int sm_count_or_default() {
+    int sms = 0;
+    if (device_state(nullptr, &sms) != QK_OK || sms <= 0) return 148;
+    return sms;
+}
+
+// Shared validation of (type, rows, cols, W).
+qk_status check_matrix(int type, const void* W, int64_t rows, int64_t cols) {
+    if (!known_type(type)) return fail(QK_ERR_TYPE, "unknown quant type %d", type);
+    if (rows < 0 || cols < 0) return fail(QK_ERR_SHAPE, "negative shape rows=%lld cols=%lld", (long long)rows,
+                                          (long long)cols);
+    if (cols % block_elems(type) != 0)
+        return fail(QK_ERR_SHAPE, "cols=%lld is not a multiple of %d", (long long)cols, block_elems(type));
+    if (rows > 0 && cols > 0) {
+        if (!W) return fail(QK_ERR_NULL, "W is NULL");
+        if (!aligned(W, 16)) return fail(QK_ERR_ALIGN, "W is not 16-byte aligned");
+    }
+    return QK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qk_version(void) { return 1; }
+
+size_t qk_block_bytes(int type) { return block_bytes(type); }
+
+int qk_block_elems(int type) { return block_elems(type); }
+
+size_t qk_row_bytes(int type, int64_t cols) {
+    if (!known_type(type) || cols < 0 || cols % block_elems(type) != 0) return 0;
+    return (size_t)(cols / block_elems(type)) * block_bytes(type);
+}
+
+const char* qk_last_error(void) { return g_last_error.c_str(); }
+
+qk_status qk_dequant(int type, const void* W, int64_t rows, int64_t cols, void* out, int out_dtype, void* stream) {
+    qk_status st = check_matrix(type, W, rows, cols);
+    if (st != QK_OK) return st;
+    if (out_dtype != QK_OUT_F32 && out_dtype != QK_OUT_BF16) return fail(QK_ERR_ARG, "bad out_dtype %d", out_dtype);
+    if (rows == 0 || cols == 0) return QK_OK;
+    if (!out) return fail(QK_ERR_NULL, "out is NULL");
+    if (!aligned(out, 16)) return fail(QK_ERR_ALIGN, "out is not 16-byte aligned");
+    cudaError_t e = qk::launch_dequant(type, static_cast<const uint8_t*>(W), rows, cols, out,
+                                       out_dtype == QK_OUT_BF16, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "qk_dequant launch");
+    g_last_error.clear();
+    return QK_OK;
+}
+
+size_t qk_gemv_workspace(int type, int64_t rows, int64_t cols, int64_t M) {
+    if (!known_type(type) || rows <= 0 || cols <= 0 || M <= 0 || cols % block_elems(type) != 0) return 0;
+    return (size_t)qk::plan_gemv(type, rows, cols, M, sm_count_or_default()).ws_bytes;
+}
+
+qk_status qk_gemv(int type, const void* W, int64_t rows, int64_t cols, const float* x, int64_t M, float* y,
+                  void* ws, size_t ws_bytes, void* stream) {
+    qk_status st = check_matrix(type, W, rows, cols);
+    if (st != QK_OK) return st;
+    if (M < 0) return fail(QK_ERR_SHAPE, "negative M=%lld", (long long)M);
+    if (rows == 0 || M == 0) return QK_OK;
+    if (!y) return fail(QK_ERR_NULL, "y is NULL");
+    if (!aligned(y, 4)) return fail(QK_ERR_ALIGN, "y is not 4-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cols == 0) {
+        cudaError_t e = cudaMemsetAsync(y, 0, (size_t)(M * rows) * sizeof(float), s);
+        if (e != cudaSuccess) return cuda_fail(e, "qk_gemv zero fill");
+        return QK_OK;
+    }
+    if (!x) return fail(QK_ERR_NULL, "x is NULL");
+    if (!aligned(x, 16)) return fail(QK_ERR_ALIGN, "x is not 16-byte aligned");
+    unsigned* status = nullptr;
+    int sms = 0;
+    st = device_state(&status, &sms);
+    if (st != QK_OK) return st;
+    const qk::GemvPlan pl = qk::plan_gemv(type, rows, cols, M, sms);
+    if (pl.ws_bytes > 0) {
+        if (ws_bytes < (size_t)pl.ws_bytes)
+            return fail(QK_ERR_WORKSPACE, "workspace %zu bytes < %lld needed", ws_bytes, (long long)pl.ws_bytes);
+        if (!ws) return fail(QK_ERR_NULL, "workspace is NULL");
+        if (!aligned(ws, 16)) return fail(QK_ERR_ALIGN, "workspace is not 16-byte aligned");
+    }
+    cudaError_t e = qk::launch_gemv(type, pl, static_cast<const uint8_t*>(W), rows, cols, x, M, y,
+                                    static_cast<float*>(ws), status, s);
+    if (e != cudaSuccess) return cuda_fail(e, "qk_gemv launch");
+    g_last_error.clear();
+    return QK_OK;
+}
+
+size_t qk_gemm_workspace(int type, int64_t rows, int64_t cols, int64_t M) {
+    (void)type; (void)rows; (void)cols; (void)M;
+    return 0;
+}
+
+qk_status qk_gemm(int type, const void* W, int64_t rows, int64_t cols, const void* X_bf16, int64_t M, float* Y,
+                  void* ws, size_t ws_bytes, void* stream) {
+    (void)ws; (void)ws_bytes; (void)stream; (void)X_bf16; (void)Y;
+    qk_status st = check_matrix(type, W, rows, cols);
+    if (st != QK_OK) return st;
+    if (M < 0) return fail(QK_ERR_SHAPE, "negative M=%lld", (long long)M);
+    return fail(QK_ERR_ARG, "qk_gemm: tensor-core path not built yet");
+}
+
+qk_status qk_unpack(int type, const void* W, int64_t nblocks, int16_t* codes, int16_t* sc, uint8_t* mins, float* d,
+                    float* dmin, void* stream) {
+    if (!known_type(type)) return fail(QK_ERR_TYPE, "unknown quant type %d", type);
+    if (nblocks < 0) return fail(QK_ERR_SHAPE, "negative nblocks");
+    if (nblocks == 0) return QK_OK;
+    if (!W) return fail(QK_ERR_NULL, "W is NULL");
+    if (!aligned(W, 16)) return fail(QK_ERR_ALIGN, "W is not 16-byte aligned");
+    cudaError_t e = qk::launch_unpack(type, static_cast<const uint8_t*>(W), nblocks, codes, sc, mins, d, dmin,
+                                      static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "qk_unpack launch");
+    return QK_OK;
+}
+
+qk_status qk_device_status(void* stream) {
+    unsigned* status = nullptr;
+    qk_status st = device_state(&status, nullptr);
+    if (st != QK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, status, sizeof v, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof v, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "qk_device_status");
+    if (v & 1u) return fail(QK_ERR_TIMEOUT, "a bounded wait inside a kernel ran out (status 0x%x)", v);
+    return QK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,26 @@
+// qk_internal.h -- launchers shared between the C-ABI layer (qk_api.cu) and
+// the kernel translation units.  Host code only; no torch types anywhere.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qk {
+
+cudaError_t launch_dequant(int type, const uint8_t* W, int64_t rows, int64_t cols, void* out,
+                           int out_bf16, cudaStream_t s);
+
+cudaError_t launch_unpack(int type, const uint8_t* W, int64_t nblocks, int16_t* codes, int16_t* sc,
+                          uint8_t* mins, float* d, float* dmin, cudaStream_t s);
+
+// GEMV launch plan: how the [rows, cols] x [M] problem is cut into CTAs.
+struct GemvPlan {
+    int mt = 1;          // activation rows per CTA pass (template width)
+    int splits = 1;      // K splits (partials reduced by a second kernel)
+    int64_t ws_bytes = 0;
+};
+GemvPlan plan_gemv(int type, int64_t rows, int64_t cols, int64_t M, int sm_count);
+cudaError_t launch_gemv(int type, const GemvPlan& plan, const uint8_t* W, int64_t rows, int64_t cols,
+                        const float* x, int64_t M, float* y, float* ws, unsigned* status, cudaStream_t s);
+
+}  // namespace qk

@@ -1,0 +1,162 @@
+/*
+ * qk.h -- C ABI of libqk: matrix products over GGUF block-quantized weights
+ * on one GB300 (sm_103a), with the blocks unpacked inside the dot product.
+ *
+ * Block formats (one block = a fixed number of weights along a row):
+ *   Q4_K  256 weights in 144 bytes: fp16 d, fp16 dmin, 12 bytes holding eight
+ *         6-bit sub-block scales and eight 6-bit mins, 128 bytes of 4-bit
+ *         codes; weight = (d*sc)*q - dmin*m.  ("Hitchhiker's Guide -- Lab 01:
+ *         Air-Gapped LLM Serving", section 11.2, Q4_K super-block figure;
+ *         "12 -- llama.cpp / GGUF / Local Inference Mastery", "Q4_K_M -- bit
+ *         layout in exquisite detail", figure and dequantization pseudo-code.)
+ *   Q6_K  256 weights in 210 bytes: 128 bytes of low code nibbles, 64 bytes
+ *         of high code bit pairs, sixteen int8 scales (one per 16 weights),
+ *         fp16 d; weight = d*sc*(q - 32).  ("12 -- llama.cpp / GGUF", "Other
+ *         k-quants at a glance": 256-weight super-block, 6.6 bits/weight.)
+ *   Q8_0  32 weights in 34 bytes: fp16 d, 32 int8 codes; weight = d*q.
+ *         ("Hitchhiker's Guide", section 11.1: the Q4_0 structure with 8-bit
+ *         codes.)
+ *   Q5_0  32 weights in 22 bytes: fp16 d, a 32-bit word of fifth bits, 16
+ *         bytes of nibbles; weight = d*(q - 16).  ("Local LLM inference",
+ *         "The mmap backend": one of the block types of a Q4_K_M file.)
+ * The bit placement inside the Q4_K scale bytes, the Q6_K code bytes and the
+ * Q5_0 block is the k-quant / GGUF packing: low nibbles of a group of bytes
+ * are the first weights, high nibbles the next ("How LLM Inference Engines
+ * Work", "Loading GGUF Models").
+ *
+ * Matrix layout: a weight matrix W has `rows` output rows and `cols` inputs.
+ * Each row is cols / block_elems blocks laid back to back along cols; row r
+ * starts at byte r * qk_row_bytes(type, cols).  Rows follow each other with
+ * no padding (so Q6_K rows of 11008 weights start at 9030-byte steps, not on
+ * 16-byte boundaries).
+ *
+ * Ownership and memory: every pointer argument is DEVICE memory owned by the
+ * caller, except where a function says otherwise.  The library allocates no
+ * device memory; scratch space comes from the caller as a workspace.
+ *
+ * Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
+ * Every compute call is asynchronous on it and returns once the work is
+ * queued.  Argument errors are detected on the host before anything is
+ * queued; nothing is launched when a call returns an error.
+ *
+ * Errors: every call returns a qk_status; qk_last_error() gives a text for
+ * the last failure on the calling thread.  Waits inside the kernels are
+ * bounded; a wait that runs out sets a device status word instead of
+ * hanging, and qk_device_status() reports it as QK_ERR_TIMEOUT.
+ */
+#ifndef QK_H_
+#define QK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Quant types.  The numbers are this library's own. */
+typedef enum { QK_Q4_K = 1, QK_Q6_K = 2, QK_Q8_0 = 3, QK_Q5_0 = 4 } qk_type;
+
+typedef enum {
+    QK_OK = 0,
+    QK_ERR_TYPE = 1,      /* unknown quant type                                 */
+    QK_ERR_SHAPE = 2,     /* negative size, cols not a multiple of block_elems  */
+    QK_ERR_ALIGN = 3,     /* a pointer breaks its stated alignment              */
+    QK_ERR_NULL = 4,      /* a required pointer is NULL                         */
+    QK_ERR_WORKSPACE = 5, /* workspace smaller than the matching *_workspace()  */
+    QK_ERR_CUDA = 6,      /* the CUDA runtime reported an error                 */
+    QK_ERR_TIMEOUT = 7,   /* a bounded wait inside a kernel ran out             */
+    QK_ERR_ARG = 8        /* any other invalid argument                         */
+} qk_status;
+
+/* Output element types of qk_dequant. */
+enum { QK_OUT_F32 = 0, QK_OUT_BF16 = 1 };
+
+/* Version of this ABI. */
+int qk_version(void);
+
+/* Bytes per block (144, 210, 34, 22) and weights per block (256, 256, 32,
+ * 32); 0 for an unknown type.  ("Hitchhiker's Guide", 11.2: 144 bytes =
+ * 4.5 bits per weight.) */
+size_t qk_block_bytes(int type);
+int qk_block_elems(int type);
+
+/* Bytes of one row of `cols` weights; 0 for an unknown type or when cols is
+ * not a multiple of the block size. */
+size_t qk_row_bytes(int type, int64_t cols);
+
+/* Dequantize W [rows, cols] into out [rows, cols] row-major, as fp32
+ * (out_dtype QK_OUT_F32) or bf16 (QK_OUT_BF16, round to nearest even).
+ * Each weight is computed in fp32 by the type's formula above, in the order
+ * written ((d*sc)*q - dmin*m for Q4_K); fp32 results are exact except for
+ * the final subtraction of Q4_K.
+ * W: 16-byte aligned.  out: 16-byte aligned.  rows == 0 queues nothing. */
+qk_status qk_dequant(int type, const void* W, int64_t rows, int64_t cols,
+                     void* out, int out_dtype, void* stream);
+
+/* Workspace bytes qk_gemv needs for this problem on the current device (0
+ * when it needs none).  The value depends on the device's SM count. */
+size_t qk_gemv_workspace(int type, int64_t rows, int64_t cols, int64_t M);
+
+/* Fused dequant-GEMV for decode: y[m, n] = sum_k w[n, k] * x[m, k] for
+ * m < M, n < rows, with every weight unpacked in registers inside the dot
+ * product and never written out ("Local LLM inference", "The mmap backend":
+ * blocks dequantized inside the dot product; each weight decoded once per
+ * input batch and reused across its rows).  fp32 activations and
+ * accumulation.
+ *   W  [rows, cols] packed blocks, 16-byte aligned.
+ *   x  fp32 [M, cols] row-major, 16-byte aligned.
+ *   y  fp32 [M, rows] row-major, 4-byte aligned; fully overwritten.
+ *   ws workspace of ws_bytes >= qk_gemv_workspace(...) bytes, 16-byte
+ *      aligned (may be NULL when that is 0).  Its contents need no
+ *      initialisation and are garbage afterwards.
+ * Accuracy: |y - y_exact| <= 1e-4 * sum_k |w x| + 1e-6 per output.
+ * Results are deterministic run to run (fixed reduction order).
+ * rows == 0 or M == 0 queues nothing; cols == 0 zero-fills y. */
+qk_status qk_gemv(int type, const void* W, int64_t rows, int64_t cols,
+                  const float* x, int64_t M, float* y,
+                  void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes qk_gemm needs (0 when none). */
+size_t qk_gemm_workspace(int type, int64_t rows, int64_t cols, int64_t M);
+
+/* Tensor-core dequant-GEMM for prefill: Y[m, n] = sum_k w[n, k] * X[m, k]
+ * with X in bf16 and fp32 accumulation; weight tiles are unpacked to bf16 in
+ * shared memory and fed to the tensor cores.  ("12 -- llama.cpp / GGUF":
+ * prompt processing is big GEMMs of high arithmetic intensity.)
+ *   W  [rows, cols] packed blocks, 16-byte aligned.
+ *   X  bf16 [M, cols] row-major, 16-byte aligned; cols * 2 bytes must be a
+ *      multiple of 16 (always true: cols is a multiple of 32).
+ *   Y  fp32 [M, rows] row-major, 16-byte aligned; fully overwritten.
+ *   ws as for qk_gemv.
+ * Accuracy: |Y - Y_exact(bf16 X)| <= 5e-3 * sum_k |w x|; the weights are
+ * rounded to bf16 before the product (Q8_0, Q5_0 and Q6_K codes and most
+ * Q4_K weights are exact in bf16 up to the block scale).
+ * M == 0 or rows == 0 queues nothing; cols == 0 zero-fills Y. */
+qk_status qk_gemm(int type, const void* W, int64_t rows, int64_t cols,
+                  const void* X_bf16, int64_t M, float* Y,
+                  void* ws, size_t ws_bytes, void* stream);
+
+/* Test hook: unpack nblocks consecutive blocks into their integer fields.
+ *   codes int16 [nblocks * block_elems]: Q4_K 0..15, Q6_K 0..63,
+ *         Q8_0 -128..127, Q5_0 0..31.
+ *   sc    int16 [nblocks * 16]: Q4_K 6-bit scales in slots 0..7, Q6_K the
+ *         sixteen int8 scales; other slots and types 0.
+ *   mins  uint8 [nblocks * 8]: Q4_K 6-bit mins; 0 for other types.
+ *   d, dmin fp32 [nblocks]: the decoded binary16 fields (dmin 0 unless Q4_K).
+ * All outputs device memory, any may be NULL.  W 16-byte aligned. */
+qk_status qk_unpack(int type, const void* W, int64_t nblocks, int16_t* codes,
+                    int16_t* sc, uint8_t* mins, float* d, float* dmin, void* stream);
+
+/* Synchronize `stream`, then read and clear this device's kernel status
+ * word: QK_OK, or QK_ERR_TIMEOUT when a bounded wait ran out since the last
+ * call (the affected outputs are then invalid). */
+qk_status qk_device_status(void* stream);
+
+/* Text of the last error on the calling thread ("" if none). */
+const char* qk_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QK_H_ */

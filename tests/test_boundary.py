@@ -1,0 +1,99 @@
+"""The C-ABI boundary without a GPU: the library loads, exports every entry
+point include/qk.h declares, reports sizes, and rejects bad arguments on the
+host before any CUDA call (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gguf_quant_dequant_gb300 as qk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")]
+
+
+def _declared():
+    names = set()
+    for h in HEADERS:
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names |= set(re.findall(r"\b(qk_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gguf_quant_dequant_gb300 import build
+    build.build()
+    return qk.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert {"qk_dequant", "qk_gemv", "qk_gemm"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(qk.SIGNATURES) == names
+
+
+def test_sizes(lib):
+    assert [qk.block_bytes(t) for t in (1, 2, 3, 4)] == [144, 210, 34, 22]
+    assert [qk.block_elems(t) for t in (1, 2, 3, 4)] == [256, 256, 32, 32]
+    assert qk.block_bytes(9) == 0 and qk.block_elems(0) == 0
+    assert qk.row_bytes(qk.Q6_K, 11008) == 9030
+    assert qk.row_bytes(qk.Q4_K, 4096) == 2304
+    assert qk.row_bytes(qk.Q4_K, 100) == 0
+    assert lib.qk_version() == 1
+
+
+def _status(fn, *args):
+    return fn(*args)
+
+
+def test_argument_errors_are_caught_on_host(lib):
+    fake = ctypes.c_void_p(0x10000)          # 16-byte aligned, never dereferenced
+    odd = ctypes.c_void_p(0x10008)           # 8-byte aligned only
+    # bad type
+    assert lib.qk_gemv(7, fake, 4, 256, fake, 1, fake, None, 0, None) == 1
+    assert b"type" in lib.qk_last_error()
+    # cols not a multiple of the block
+    assert lib.qk_gemv(qk.Q4_K, fake, 4, 100, fake, 1, fake, None, 0, None) == 2
+    assert lib.qk_dequant(qk.Q8_0, fake, 4, 40, fake, 0, None) == 2
+    # negative sizes
+    assert lib.qk_gemv(qk.Q4_K, fake, -1, 256, fake, 1, fake, None, 0, None) == 2
+    assert lib.qk_gemv(qk.Q4_K, fake, 4, 256, fake, -2, fake, None, 0, None) == 2
+    # NULL weights / outputs / activations
+    assert lib.qk_gemv(qk.Q4_K, None, 4, 256, fake, 1, fake, None, 0, None) == 4
+    assert lib.qk_gemv(qk.Q4_K, fake, 4, 256, fake, 1, None, None, 0, None) == 4
+    assert lib.qk_gemv(qk.Q4_K, fake, 4, 256, None, 1, fake, None, 0, None) == 4
+    assert lib.qk_dequant(qk.Q4_K, fake, 4, 256, None, 0, None) == 4
+    # misaligned pointers
+    assert lib.qk_gemv(qk.Q4_K, odd, 4, 256, fake, 1, fake, None, 0, None) == 3
+    assert lib.qk_gemv(qk.Q4_K, fake, 4, 256, odd, 1, fake, None, 0, None) == 3
+    assert lib.qk_dequant(qk.Q4_K, fake, 4, 256, odd, 0, None) == 3
+    # bad output dtype
+    assert lib.qk_dequant(qk.Q4_K, fake, 4, 256, fake, 5, None) == 8
+    # unpack
+    assert lib.qk_unpack(0, fake, 1, None, None, None, None, None, None) == 1
+    assert lib.qk_unpack(qk.Q4_K, odd, 1, None, None, None, None, None, None) == 3
+    assert lib.qk_unpack(qk.Q4_K, fake, -1, None, None, None, None, None, None) == 2
+
+
+def test_empty_problems_queue_nothing(lib):
+    fake = ctypes.c_void_p(0x10000)
+    # rows == 0 or M == 0: success without touching the device.
+    assert lib.qk_gemv(qk.Q4_K, fake, 0, 256, fake, 1, fake, None, 0, None) == 0
+    assert lib.qk_gemv(qk.Q4_K, fake, 8, 256, fake, 0, fake, None, 0, None) == 0
+    assert lib.qk_dequant(qk.Q6_K, fake, 0, 256, fake, 0, None) == 0
+    assert lib.qk_unpack(qk.Q8_0, fake, 0, None, None, None, None, None, None) == 0
+
+
+def test_binding_refuses_to_run_without_library(monkeypatch, tmp_path):
+    import importlib
+    mod = importlib.reload(qk)
+    monkeypatch.setattr(mod, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(mod, "_lib", None)
+    with pytest.raises(RuntimeError):
+        mod.load()
+    importlib.reload(qk)

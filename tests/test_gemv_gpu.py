@@ -1,0 +1,132 @@
+"""qk_gemv against the oracle on small seeded problems that span several
+stages, ragged row tiles and tails, every activation-batch width, split and
+unsplit K, misaligned Q6_K rows; plus invariants and edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import gguf_quant_dequant_gb300 as qk
+import oracle
+import synth
+from gpu_helpers import assert_gemv_close, dev_f32, dev_u8, gpu, type_id  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+NAMES = ["Q4_K", "Q6_K", "Q8_0", "Q5_0"]
+
+
+def run(gpu, name, rows, cols, M, seed, W=None, x=None):
+    t = type_id(name)
+    if W is None:
+        W = synth.random_blocks(name, rows, cols, seed)
+    if x is None:
+        x = synth.activations(M, cols, seed + 1)
+    y = qk.gemv(t, dev_u8(W, gpu), rows, cols, dev_f32(x, gpu)).cpu().numpy()
+    y_ref, S = oracle.gemv(t, W, rows, cols, x)
+    return y, y_ref, S
+
+
+# Shapes: one block; one stage plus a one-block tail; many rows with a ragged
+# last CTA (rows % 16 != 0) and several stages; a 11008-wide Q6_K case whose
+# rows start 6 bytes off 16-byte alignment and whose total size is not a
+# multiple of 16 (the last bytes are not bulk-copyable).
+SHAPES = {
+    "Q4_K": [(1, 256), (5, 1280), (37, 3328), (300, 1024)],
+    "Q6_K": [(1, 256), (5, 1280), (37, 3328), (9, 11008)],
+    "Q8_0": [(1, 32), (5, 1056), (37, 3104), (300, 1024)],
+    "Q5_0": [(1, 32), (5, 1056), (37, 3104), (300, 1024)],
+}
+
+
+@pytest.mark.parametrize("name", NAMES)
+@pytest.mark.parametrize("shape_i", range(4))
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 9])
+def test_gemv_parity(gpu, name, shape_i, M):
+    rows, cols = SHAPES[name][shape_i]
+    y, y_ref, S = run(gpu, name, rows, cols, M, 1000 + 10 * shape_i + M)
+    assert y.shape == (M, rows)
+    assert_gemv_close(y, y_ref, S, what=f"{name} {rows}x{cols} M={M}")
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_gemv_quantized_codes(gpu, name):
+    # Codes from the plain quantizer applied to N(0, 0.02) weights.
+    rows, cols = 64, 2048
+    W = oracle.quantize(type_id(name), synth.normal_weights(rows, cols, 77))
+    y, y_ref, S = run(gpu, name, rows, cols, 2, 78, W=W)
+    assert_gemv_close(y, y_ref, S, what=name)
+
+
+def test_split_and_unsplit_paths(gpu):
+    # 16 rows -> one CTA -> the plan splits K; 4096 rows -> no split.
+    for rows in (16, 4096):
+        ws = qk.gemv_workspace(qk.Q4_K, rows, 4096, 1)
+        assert (ws > 0) == (rows == 16)
+        y, y_ref, S = run(gpu, "Q4_K", rows, 4096, 1, 2000 + rows)
+        assert_gemv_close(y, y_ref, S, what=f"rows={rows}")
+
+
+def test_exact_integer_case_is_bit_exact(gpu):
+    # Q8_0 with d = 2^-3 and integer x in [-8, 8]: every product and partial
+    # sum is a multiple of 2^-3 below 2^21, exact in fp32 in any order.
+    g = synth.rng(90)
+    rows, cols = 48, 4096
+    codes = g.integers(-128, 128, (rows * cols // 32, 32)).astype(np.int16)
+    W = oracle.pack(qk.Q8_0, codes, None, None, np.full(rows * cols // 32, 0x3000, np.uint16))
+    x = g.integers(-8, 9, (3, cols)).astype(np.float32)
+    y, y_ref, _ = run(gpu, "Q8_0", rows, cols, 3, 0, W=W, x=x)
+    assert np.array_equal(y.astype(np.float64), y_ref)
+
+
+def test_linearity_and_batch_rows(gpu):
+    name, rows, cols = "Q6_K", 40, 2048
+    t = type_id(name)
+    W = dev_u8(synth.random_blocks(name, rows, cols, 91), gpu)
+    x = synth.activations(4, cols, 92)
+    Y = qk.gemv(t, W, rows, cols, dev_f32(x, gpu)).cpu().numpy()
+    for m in range(4):
+        y1 = qk.gemv(t, W, rows, cols, dev_f32(x[m:m + 1], gpu)).cpu().numpy()[0]
+        assert np.allclose(Y[m], y1, rtol=1e-5, atol=1e-5)
+    a, b = 0.5, -2.0
+    yc = qk.gemv(t, W, rows, cols, dev_f32(a * x[0:1] + b * x[1:2], gpu)).cpu().numpy()[0]
+    assert np.allclose(yc, a * Y[0] + b * Y[1], rtol=1e-4, atol=1e-4)
+
+
+def test_deterministic(gpu):
+    name, rows, cols = "Q4_K", 64, 8192   # split-K path included
+    t = type_id(name)
+    W = dev_u8(synth.random_blocks(name, rows, cols, 93), gpu)
+    x = dev_f32(synth.activations(1, cols, 94), gpu)
+    y0 = qk.gemv(t, W, rows, cols, x).cpu().numpy()
+    for _ in range(3):
+        assert np.array_equal(qk.gemv(t, W, rows, cols, x).cpu().numpy(), y0)
+
+
+def test_output_canaries_and_empty(gpu):
+    name, rows, cols, M = "Q5_0", 21, 1024, 2
+    t = type_id(name)
+    W = synth.random_blocks(name, rows, cols, 95)
+    x = synth.activations(M, cols, 96)
+    buf = torch.full((M * rows + 8,), float("nan"), device=gpu)
+    y = buf[4:4 + M * rows].view(M, rows)
+    qk.gemv(t, dev_u8(W, gpu), rows, cols, dev_f32(x, gpu), y=y)
+    b = buf.cpu().numpy()
+    assert np.isnan(b[:4]).all() and np.isnan(b[-4:]).all() and not np.isnan(b[4:-4]).any()
+    # cols == 0 zero-fills, rows == 0 and M == 0 are no-ops
+    y0 = torch.full((2, 3), 7.0, device=gpu)
+    qk.gemv(t, torch.zeros(16, dtype=torch.uint8, device=gpu), 3, 0,
+            torch.zeros((2, 0), device=gpu), y=y0)
+    assert (y0 == 0).all()
+    qk.gemv(t, dev_u8(W, gpu), 0, cols, dev_f32(x, gpu), y=torch.empty((2, 0), device=gpu))
+    qk.device_status()
+
+
+def test_workspace_too_small_is_rejected(gpu):
+    t, rows, cols = qk.Q4_K, 16, 4096
+    need = qk.gemv_workspace(t, rows, cols, 1)
+    assert need > 0
+    W = dev_u8(synth.random_blocks("Q4_K", rows, cols, 97), gpu)
+    x = dev_f32(synth.activations(1, cols, 98), gpu)
+    small = torch.empty(need - 16, dtype=torch.uint8, device=gpu)
+    with pytest.raises(qk.QKError) as e:
+        qk.gemv(t, W, rows, cols, x, ws=small)
+    assert e.value.status == 5
