@@ -68,6 +68,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return pol;
 }
 
+// Evict-last L2 policy for small data many CTAs read (prepped activations).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // Bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned) from
 // global to this CTA's shared memory, completing on `bar` (complete_tx).
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,

@@ -57,24 +57,28 @@ def test_gemv_quantized_codes(gpu, name):
 
 
 def test_split_and_unsplit_paths(gpu):
-    # 16 rows -> one CTA -> the plan splits K; 4096 rows -> no split.
-    for rows in (16, 4096):
-        ws = qk.gemv_workspace(qk.Q4_K, rows, 4096, 1)
-        assert (ws > 0) == (rows == 16)
-        y, y_ref, S = run(gpu, "Q4_K", rows, 4096, 1, 2000 + rows)
+    # 16 rows (one row tile) split K over many CTAs; 8192 rows do not split.
+    # The split plan needs room for partials beyond the prepped activations.
+    xp_only = qk.gemv_workspace(qk.Q4_K, 8192, 8192, 1)
+    assert qk.gemv_workspace(qk.Q4_K, 16, 8192, 1) > xp_only
+    for rows in (16, 8192):
+        y, y_ref, S = run(gpu, "Q4_K", rows, 8192, 1, 2000 + rows)
         assert_gemv_close(y, y_ref, S, what=f"rows={rows}")
 
 
-def test_exact_integer_case_is_bit_exact(gpu):
-    # Q8_0 with d = 2^-3 and integer x in [-8, 8]: every product and partial
-    # sum is a multiple of 2^-3 below 2^21, exact in fp32 in any order.
+def test_exact_integer_case_is_near_exact(gpu):
+    # Q8_0 with d = 2^-3 and integer x in [-8, 8]: the exact result is an
+    # integer multiple of 2^-3.  The integer part of the product is exact in
+    # the kernel (dp4a on 24-bit fixed-point activations), so only a few fp32
+    # roundings of the block scales remain: far inside the 1e-4 bound.
     g = synth.rng(90)
     rows, cols = 48, 4096
     codes = g.integers(-128, 128, (rows * cols // 32, 32)).astype(np.int16)
     W = oracle.pack(qk.Q8_0, codes, None, None, np.full(rows * cols // 32, 0x3000, np.uint16))
     x = g.integers(-8, 9, (3, cols)).astype(np.float32)
-    y, y_ref, _ = run(gpu, "Q8_0", rows, cols, 3, 0, W=W, x=x)
-    assert np.array_equal(y.astype(np.float64), y_ref)
+    y, y_ref, S = run(gpu, "Q8_0", rows, cols, 3, 0, W=W, x=x)
+    assert np.all(np.abs(y - y_ref) <= 2.0 ** -20 * S)
+    assert np.array_equal(y_ref, np.round(y_ref * 8) / 8)
 
 
 def test_linearity_and_batch_rows(gpu):
@@ -86,9 +90,12 @@ def test_linearity_and_batch_rows(gpu):
     for m in range(4):
         y1 = qk.gemv(t, W, rows, cols, dev_f32(x[m:m + 1], gpu)).cpu().numpy()[0]
         assert np.allclose(Y[m], y1, rtol=1e-5, atol=1e-5)
+    # Linearity, within the sum of the three results' error bounds.
     a, b = 0.5, -2.0
     yc = qk.gemv(t, W, rows, cols, dev_f32(a * x[0:1] + b * x[1:2], gpu)).cpu().numpy()[0]
-    assert np.allclose(yc, a * Y[0] + b * Y[1], rtol=1e-4, atol=1e-4)
+    _, S = oracle.gemv(t, W.cpu().numpy(), rows, cols, x[:2])
+    bound = 2e-4 * (abs(a) * S[0] + abs(b) * S[1]) + 3e-6
+    assert np.all(np.abs(yc - (a * Y[0] + b * Y[1])) <= bound)
 
 
 def test_deterministic(gpu):
