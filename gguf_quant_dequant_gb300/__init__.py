@@ -37,6 +37,7 @@ SIGNATURES = {
     "qk_dequant": (_int, [_int, _p, _i64, _i64, _p, _int, _p]),
     "qk_gemv_workspace": (_sz, [_int, _i64, _i64, _i64]),
     "qk_gemv": (_int, [_int, _p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
+    "qk_gemv_noalloc": (_int, [_int, _p, _i64, _i64, _p, _i64, _p, _p]),
     "qk_gemm_workspace": (_sz, [_int, _i64, _i64, _i64]),
     "qk_gemm": (_int, [_int, _p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
     "qk_unpack": (_int, [_int, _p, _i64, _p, _p, _p, _p, _p, _p]),
@@ -122,6 +123,18 @@ def gemv(t: int, W, rows: int, cols: int, x, y=None, ws=None, stream=None):
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(load().qk_gemv(t, _ptr(W), rows, cols, _ptr(x), M, _ptr(y), _ptr(ws), nbytes, _stream(stream)),
            "qk_gemv")
+    return y
+
+
+def gemv_noalloc(t: int, W, rows: int, cols: int, x, y=None, stream=None):
+    """qk_gemv_noalloc: the GEMV with the library's fixed device scratch
+    instead of a workspace (for callers that cannot allocate)."""
+    import torch
+    M = x.shape[0] if x.dim() == 2 else 1
+    if y is None:
+        y = torch.empty((M, rows), dtype=torch.float32, device=x.device)
+    _check(load().qk_gemv_noalloc(t, _ptr(W), rows, cols, _ptr(x), M, _ptr(y), _stream(stream)),
+           "qk_gemv_noalloc")
     return y
 
 

@@ -104,6 +104,12 @@ qk_status check_matrix(int type, const void* W, int64_t rows, int64_t cols) {
 
 }  // namespace
 
+namespace qk {
+// Record `msg` as the calling thread's last error and return `st` (for entry
+// points defined in other translation units).
+qk_status set_error(qk_status st, const char* msg) { return fail(st, "%s", msg); }
+}  // namespace qk
+
 extern "C" {
 
 int qk_version(void) { return 1; }

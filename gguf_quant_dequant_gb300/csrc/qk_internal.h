@@ -5,7 +5,12 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "../../include/qk.h"
+
 namespace qk {
+
+// Sets the calling thread's qk_last_error() text; returns st.
+qk_status set_error(qk_status st, const char* msg);
 
 cudaError_t launch_dequant(int type, const uint8_t* W, int64_t rows, int64_t cols, void* out,
                            int out_bf16, cudaStream_t s);

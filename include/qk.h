@@ -117,6 +117,33 @@ qk_status qk_gemv(int type, const void* W, int64_t rows, int64_t cols,
                   const float* x, int64_t M, float* y,
                   void* ws, size_t ws_bytes, void* stream);
 
+/* Size of the fixed scratch array qk_gemv_noalloc uses: 8 MiB per device. */
+#define QK_GEMV_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/* qk_gemv for callers that cannot allocate device memory.  The pages have no
+ * counterpart; this is a convenience of this library.  Some callers of a
+ * decode GEMV are not allowed to allocate: plug-in code running inside a
+ * host runtime that owns every device allocation, code under a fixed memory
+ * budget that must not grow its footprint while serving, and paths that
+ * cannot afford the device-wide synchronization that cudaMalloc / cudaFree
+ * can cause.  They call this instead of qk_gemv and pass no workspace.
+ *   Arguments, results, accuracy and errors are those of qk_gemv.
+ *   Scratch: one array of QK_GEMV_NOALLOC_SCRATCH_BYTES that the library
+ *     holds in device memory on every GPU that loads it, until the process
+ *     exits.  Problems needing more scratch than that (qk_gemv_workspace()
+ *     larger than the array) are rejected with QK_ERR_WORKSPACE and nothing
+ *     is queued.  This call itself allocates nothing.
+ *   Set-up: the first call on each device, with that device current, looks
+ *     up the array's device address; make that first call before starting
+ *     any stream capture.
+ *   Sharing: every call on a device uses the same array and leaves its
+ *     contents behind; each call clears what must start at zero itself.
+ *     Calls whose kernels overlap on the GPU (different streams without an
+ *     ordering between them) race on the array and give wrong results;
+ *     order them on one stream or with events. */
+qk_status qk_gemv_noalloc(int type, const void* W, int64_t rows, int64_t cols,
+                          const float* x, int64_t M, float* y, void* stream);
+
 /* Workspace bytes qk_gemm needs (0 when none). */
 size_t qk_gemm_workspace(int type, int64_t rows, int64_t cols, int64_t M);
 
