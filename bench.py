@@ -260,7 +260,7 @@ def run_gpu(args):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "timing": "CUDA graph per layer copy, CUDA events on the launch stream"},
             "frac_of_peak": round(value / world / hbm_peak, 4),
-            "roofline": {"bound": "hbm", "kernel": "gemv_kernel<Q4_K, MT=1>", "achieved": round(achieved, 2),
+            "roofline": {"bound": "hbm", "kernel": "gemv4_kernel<Q4_K> (M=1 decode)", "achieved": round(achieved, 2),
                          "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s",
                          "frac": round(achieved / hbm_peak, 4), "traffic": None,
                          "launch_bytes": int(q4_launch_bytes), "launch_us": round(q4_launch_ms * 1e3, 3)},

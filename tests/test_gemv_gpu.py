@@ -57,13 +57,15 @@ def test_gemv_quantized_codes(gpu, name):
 
 
 def test_split_and_unsplit_paths(gpu):
-    # 16 rows (one row tile) split K over many CTAs; 8192 rows do not split.
-    # The split plan needs room for partials beyond the prepped activations.
-    xp_only = qk.gemv_workspace(qk.Q4_K, 8192, 8192, 1)
-    assert qk.gemv_workspace(qk.Q4_K, 16, 8192, 1) > xp_only
+    # Batched (M = 2) kernel: 16 rows (one row tile) split K over many CTAs,
+    # 8192 rows do not; the split plan needs room for partials beyond the
+    # prepped activations.  M = 1 uses the K-sliced decode kernel.
+    xp_only = qk.gemv_workspace(qk.Q4_K, 8192, 8192, 2)
+    assert qk.gemv_workspace(qk.Q4_K, 16, 8192, 2) > xp_only
     for rows in (16, 8192):
-        y, y_ref, S = run(gpu, "Q4_K", rows, 8192, 1, 2000 + rows)
-        assert_gemv_close(y, y_ref, S, what=f"rows={rows}")
+        for M in (1, 2):
+            y, y_ref, S = run(gpu, "Q4_K", rows, 8192, M, 2000 + rows)
+            assert_gemv_close(y, y_ref, S, what=f"rows={rows} M={M}")
 
 
 def test_exact_integer_case_is_near_exact(gpu):
