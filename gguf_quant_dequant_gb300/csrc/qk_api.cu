@@ -185,11 +185,30 @@ size_t qk_gemm_workspace(int type, int64_t rows, int64_t cols, int64_t M) {
 
 qk_status qk_gemm(int type, const void* W, int64_t rows, int64_t cols, const void* X_bf16, int64_t M, float* Y,
                   void* ws, size_t ws_bytes, void* stream) {
-    (void)ws; (void)ws_bytes; (void)stream; (void)X_bf16; (void)Y;
+    (void)ws; (void)ws_bytes;
     qk_status st = check_matrix(type, W, rows, cols);
     if (st != QK_OK) return st;
     if (M < 0) return fail(QK_ERR_SHAPE, "negative M=%lld", (long long)M);
-    return fail(QK_ERR_ARG, "qk_gemm: tensor-core path not built yet");
+    if (rows == 0 || M == 0) return QK_OK;
+    if (!Y) return fail(QK_ERR_NULL, "Y is NULL");
+    if (!aligned(Y, 4)) return fail(QK_ERR_ALIGN, "Y is not 4-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cols == 0) {
+        cudaError_t e = cudaMemsetAsync(Y, 0, (size_t)(M * rows) * sizeof(float), s);
+        if (e != cudaSuccess) return cuda_fail(e, "qk_gemm zero fill");
+        return QK_OK;
+    }
+    if (!X_bf16) return fail(QK_ERR_NULL, "X is NULL");
+    if (!aligned(X_bf16, 16)) return fail(QK_ERR_ALIGN, "X is not 16-byte aligned");
+    if (rows > (int64_t)1 << 31 || M > (int64_t)1 << 31 || cols > (int64_t)1 << 31)
+        return fail(QK_ERR_SHAPE, "qk_gemm: dimensions must be below 2^31");
+    unsigned* status = nullptr;
+    st = device_state(&status, nullptr);
+    if (st != QK_OK) return st;
+    cudaError_t e = qk::launch_gemm(type, static_cast<const uint8_t*>(W), rows, cols, X_bf16, M, Y, status, s);
+    if (e != cudaSuccess) return cuda_fail(e, "qk_gemm launch");
+    g_last_error.clear();
+    return QK_OK;
 }
 
 qk_status qk_unpack(int type, const void* W, int64_t nblocks, int16_t* codes, int16_t* sc, uint8_t* mins, float* d,

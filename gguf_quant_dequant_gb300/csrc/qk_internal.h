@@ -28,4 +28,8 @@ GemvPlan plan_gemv(int type, int64_t rows, int64_t cols, int64_t M, int sm_count
 cudaError_t launch_gemv(int type, const GemvPlan& plan, const uint8_t* W, int64_t rows, int64_t cols,
                         const float* x, int64_t M, float* y, float* ws, unsigned* status, cudaStream_t s);
 
+// Tensor-core dequant-GEMM (bf16 activations, fp32 output); no workspace.
+cudaError_t launch_gemm(int type, const uint8_t* W, int64_t rows, int64_t cols, const void* X, int64_t M, float* Y,
+                        unsigned* status, cudaStream_t s);
+
 }  // namespace qk

@@ -1,0 +1,69 @@
+"""qk_gemm (tcgen05 tensor-core dequant-GEMM) against the oracle fed the same
+bf16 activations: |Y - Y_ref| <= 5e-3 * sum|w x| per output.  Shapes cover
+one tile, ragged weight rows and token counts, a K whose last 64-block is
+half empty (32-weight blocks), every quant type, and M from 1 to 300."""
+import numpy as np
+import pytest
+import torch
+
+import gguf_quant_dequant_gb300 as qk
+import oracle
+import synth
+from gpu_helpers import GEMM_RTOL, assert_gemv_close, dev_u8, gpu, type_id  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    ("Q4_K", 128, 256, 256),
+    ("Q4_K", 200, 512, 300),
+    ("Q6_K", 136, 768, 64),
+    ("Q8_0", 130, 96, 17),
+    ("Q5_0", 256, 160, 1),
+    ("Q5_0", 64, 1024, 257),
+    ("Q8_0", 384, 2048, 512),
+]
+
+
+def run_gemm(gpu, name, rows, cols, M, seed):
+    t = type_id(name)
+    W = synth.random_blocks(name, rows, cols, seed)
+    Xb = synth.activations_bf16_bits(M, cols, seed + 1)
+    Xd = torch.from_numpy(Xb.view(np.int16)).to(gpu).view(torch.bfloat16)
+    Y = qk.gemm(t, dev_u8(W, gpu), rows, cols, Xd).cpu().numpy()
+    qk.device_status()
+    Y_ref, S = oracle.gemm_bf16(t, W, rows, cols, Xb)
+    return Y, Y_ref, S
+
+
+@pytest.mark.parametrize("name,rows,cols,M", CASES)
+def test_gemm_parity(gpu, name, rows, cols, M):
+    Y, Y_ref, S = run_gemm(gpu, name, rows, cols, M, 3000 + rows + M)
+    assert Y.shape == (M, rows)
+    assert_gemv_close(Y, Y_ref, S, rtol=GEMM_RTOL, atol=0.0, what=f"gemm {name} {rows}x{cols} M={M}")
+
+
+def test_gemm_matches_dequant_then_matmul(gpu):
+    # Same bf16 weights, fp32 accumulation on both sides: agreement far
+    # inside the GEMM tolerance.
+    name, rows, cols, M = "Q4_K", 256, 1024, 256
+    t = type_id(name)
+    W = synth.random_blocks(name, rows, cols, 4000)
+    Wd = dev_u8(W, gpu)
+    Xb = synth.activations_bf16_bits(M, cols, 4001)
+    Xd = torch.from_numpy(Xb.view(np.int16)).to(gpu).view(torch.bfloat16)
+    Y = qk.gemm(t, Wd, rows, cols, Xd)
+    Wbf = qk.dequant(t, Wd, rows, cols, bf16=True)
+    ref = (Xd.float() @ Wbf.float().t())
+    _, S = oracle.gemm_bf16(t, W, rows, cols, Xb)
+    assert np.all(np.abs((Y - ref).cpu().numpy()) <= 1e-4 * S + 1e-5)
+
+
+def test_gemm_empty_and_zero_k(gpu):
+    t = qk.Q4_K
+    Y = torch.full((4, 8), 3.0, device=gpu)
+    qk.gemm(t, torch.zeros(16, dtype=torch.uint8, device=gpu), 8, 0,
+            torch.zeros((4, 0), dtype=torch.bfloat16, device=gpu), Y=Y)
+    assert (Y == 0).all()
+    qk.gemm(t, torch.zeros(144, dtype=torch.uint8, device=gpu), 0, 256,
+            torch.zeros((4, 256), dtype=torch.bfloat16, device=gpu), Y=torch.empty((4, 0), device=gpu))
+    qk.device_status()
