@@ -245,6 +245,18 @@ def run_gpu(args):
     achieved = q4_launch_bytes / (q4_launch_ms * 1e-3) / 1e9
 
     e2e = run_e2e(args, dev, layer, Ws[0], xs, lb) if rank == 0 else None
+    del Ws, graphs, q4_graphs
+    torch.cuda.empty_cache()
+    gemm = None
+    if rank == 0 and not args.no_gemm:
+        gemm = run_gemm_bench(dev)
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                pk = json.load(f)
+            gemm["frac_of_bf16_peak"] = round(gemm["tflops"] / float(pk["bf16_tflops"]), 4)
+            gemm["frac_of_bf16_sustained"] = round(gemm["tflops"] / float(pk["bf16_tflops_sustained"]), 4)
+        except Exception:
+            pass
     cpu = cpu_baseline(layer) if (rank == 0 and world == 1 and not args.no_cpu) else None
     if rank == 0:
         out = {
@@ -268,11 +280,74 @@ def run_gpu(args):
             "clocks": clocks,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "gemm": gemm,
         }
         print(json.dumps(out))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_gemm_bench(dev, reps: int = 5):
+    """Prefill dequant-GEMM (M = 2048 bf16 activations) over the mixed recipe
+    of 4096x4096, 14336x4096 and 4096x14336 matrices in Q4_K / Q6_K / Q8_0
+    plus the 128256x4096 Q6_K vocabulary matrix.  TFLOP/s = 2*M*N*K / time
+    (CUDA events, median of `reps` launches per matrix), and the same flops
+    through qk_dequant -> bf16 + torch.matmul (cuBLAS) as a comparator."""
+    import torch
+    import gguf_quant_dequant_gb300 as qk
+    import synth
+    M = synth.PREFILL_M
+    g = torch.Generator(device=dev)
+    g.manual_seed(77)
+    stream = torch.cuda.current_stream()
+    per, tot_flop, tot_ms, cmp_flop, cmp_ms = {}, 0.0, 0.0, 0.0, 0.0
+    Xs = {}
+    for i, (nm, name, rows, cols) in enumerate(synth.PREFILL):
+        t = synth.TYPE_IDS[name]
+        W = synth.random_blocks_torch(name, rows, cols, 900 + i, dev)
+        if cols not in Xs:
+            Xs[cols] = torch.randn((M, cols), device=dev, generator=g).to(torch.bfloat16)
+        X = Xs[cols]
+        Y = torch.empty((M, rows), device=dev)
+        for _ in range(2):
+            qk.gemm(t, W, rows, cols, X, Y=Y)
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            qk.gemm(t, W, rows, cols, X, Y=Y)
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms = statistics.median(ts)
+        fl = 2.0 * M * rows * cols
+        per[nm] = round(fl / (ms * 1e-3) / 1e12, 1)
+        tot_flop += fl
+        tot_ms += ms
+        if nm != "vocab":
+            Wb = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev)
+            for _ in range(2):
+                qk.dequant(t, W, rows, cols, out=Wb, bf16=True)
+                torch.matmul(X, Wb.t())
+            ts = []
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                qk.dequant(t, W, rows, cols, out=Wb, bf16=True)
+                torch.matmul(X, Wb.t())
+                e1.record(stream)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            cmp_flop += fl
+            cmp_ms += statistics.median(ts)
+            del Wb
+        del W, Y
+    torch.cuda.synchronize()
+    return {"workload": "prefill dequant-GEMM, M=2048 bf16 activations, 9 recipe matrices + 128256x4096 Q6_K vocab",
+            "tflops": round(tot_flop / (tot_ms * 1e-3) / 1e12, 1), "per_matrix_tflops": per,
+            "comparator_dequant_then_cublas_tflops": round(cmp_flop / (cmp_ms * 1e-3) / 1e12, 1),
+            "comparator_note": "qk_dequant to bf16 then torch.matmul, same 9 matrices (vocab excluded)"}
 
 
 def run_e2e(args, dev, layer, Wd, xs, lb):
@@ -392,6 +467,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="qk", choices=["qk", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--no-gemm", action="store_true", help="skip the prefill GEMM leg")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -23,23 +23,59 @@
 #include "qk_tc.cuh"
 
 namespace qk {
+namespace gv {
+// (from qk_gemv.cu; shared-memory word loads at 2-byte alignment)
+template <int N>
+__device__ __forceinline__ void lds_words_a2(const uint8_t* p, uint32_t (&w)[N]) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint8_t* base = reinterpret_cast<const uint8_t*>(a & ~uintptr_t(3));
+    const uint32_t sh = (uint32_t)(a & 3) * 8;   // 0 or 16
+    uint32_t prev = *reinterpret_cast<const uint32_t*>(base);
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const uint32_t next = *reinterpret_cast<const uint32_t*>(base + 4 * (i + 1));
+        w[i] = __funnelshift_r(prev, next, sh);
+        prev = next;
+    }
+}
+}  // namespace gv
 namespace gm {
+
+__device__ __forceinline__ uint4 lds128_g(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
 
 constexpr int kBM = 128;          // weight rows per CTA (MMA M)
 constexpr int kBN = 256;          // tokens per CTA (MMA N)
 constexpr int kBK = 64;           // K per stage (one 128-byte swizzle row)
-constexpr int kNS = 4;            // pipeline stages
+constexpr int kNS = 3;            // bf16 operand stages
 constexpr int kA = kBM * kBK * 2; // 16 KB
 constexpr int kB = kBN * kBK * 2; // 32 KB
 constexpr int kStage = kA + kB;
-constexpr int kDeqWarps = 8;
+constexpr int kDeqWarps = 16;
+constexpr int kDeqThreads = kDeqWarps * 32;
+constexpr int kParts = kDeqThreads / kBM;            // threads per tile row (4): 16 weights each
 constexpr int kThreads = (2 + kDeqWarps) * 32;
 constexpr int kTmemCols = 256;
-constexpr int kSmem = 1024 + kNS * kStage + (3 * kNS + 1) * 8 + 16;
+constexpr int kMB = 256;          // weights per packed macro-block (one super-block / 8 small blocks)
+constexpr int kNSP = 2;           // packed macro-block stages
+
+// Packed macro-block geometry: bytes per row, and the per-row slot (the
+// aligned-down window can start up to 15 bytes early; slack for the
+// funnel-shifted reads past the end).
+template <int T> struct Pk {
+    static constexpr int BYTES = kMB / Fmt<T>::BE * Fmt<T>::BB;   // 144, 210, 272, 176
+    // Row slots are 16-byte multiples (cp.async) and an odd number of 16-byte
+    // units, so the 32 rows a warp reads spread over 8 bank groups.
+    static constexpr int SLOT0 = (BYTES + 32 + 15) / 16 * 16;
+    static constexpr int SLOT = (SLOT0 / 16) % 2 == 0 ? SLOT0 + 16 : SLOT0;
+    static constexpr int STAGE = kBM * SLOT;
+    static constexpr int OFF_P = 1024 + kNS * kStage;             // packed ring (after the operand stages)
+    static constexpr int OFF_BAR = OFF_P + kNSP * STAGE;
+    static constexpr int SMEM = OFF_BAR + (3 * kNS + 1) * 8 + 16;
+};
 
 struct Args {
     const uint8_t* W;
-    int64_t rows, cols, row_bytes, M;
+    int64_t rows, cols, row_bytes, M, total16;
     float* Y;
     unsigned* status;
     int nkb;
@@ -61,11 +97,14 @@ __device__ __forceinline__ void locate(int o, int& u, int& h) {
     }
 }
 
-// 32 bf16 weights of row `row`, k in [k0, k0 + 32), into 4 swizzled 16-byte
-// chunks of the A stage (chunks cbase..cbase+3 of the row).  Rows past the
-// matrix and k past cols are zero.
+// 32 bf16 weights, k in [k0, k0 + 32) of row `row`, decoded from the row's
+// packed macro-block in shared memory (`mb` points at its first byte; the
+// macro-block starts at k = kmb), into 4 swizzled 16-byte chunks of the A
+// stage (chunks cbase..cbase+3 of tile row r).  Rows past the matrix and k
+// past cols are zero.
 template <int T>
-__device__ __forceinline__ void dequant32(const Args& p, uint8_t* A, int r, int64_t row, int64_t k0, int cbase) {
+__device__ __forceinline__ void dequant32(const Args& p, uint8_t* A, int r, int64_t row, const uint8_t* mb,
+                                          int64_t kmb, int64_t k0, int cbase) {
     using F = Fmt<T>;
     uint32_t packed[16];
 #pragma unroll
@@ -73,10 +112,10 @@ __device__ __forceinline__ void dequant32(const Args& p, uint8_t* A, int r, int6
         const int64_t k = k0 + 16 * hf;
         float w[16];
         if (row < p.rows && k < p.cols) {
-            const int64_t b = k / F::BE;
+            const int o = (int)(k - kmb);               // offset inside the macro-block
             int u, h;
-            locate<T>((int)(k % F::BE), u, h);
-            dequant_half<T>(p.W + row * p.row_bytes + b * F::BB, u, h, w);
+            locate<T>(o % F::BE, u, h);
+            dequant_half<T>(mb + (o / F::BE) * F::BB, u, h, w);
         } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) w[i] = 0.0f;
@@ -96,13 +135,203 @@ __device__ __forceinline__ void dequant32(const Args& p, uint8_t* A, int r, int6
     }
 }
 
+// ---------------------------------------------------------------------------
+// Fast bf16 decoders (32 weights of one tile row for one 64-wide k-block,
+// half hh).  A code byte is placed into an fp32 mantissa by one byte permute
+// (exact: 128 + q with the code in bits 16-23 of 0x43000000, or 256 + u/128
+// with the byte in bits 8-15 of 0x43800000), then one packed fp32 FMA per two
+// weights applies scale and offset, and one convert packs two bf16.
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Four bytes of v (each < 128) -> 128 + byte as fp32, times a, plus c;
+// packed as two bf16x2 words.
+__device__ __forceinline__ void four_hi(uint32_t v, float2 a, float2 c, uint32_t& o0, uint32_t& o1) {
+    const float f0 = __uint_as_float(__byte_perm(v, 0x43000000u, 0x7044));
+    const float f1 = __uint_as_float(__byte_perm(v, 0x43000000u, 0x7144));
+    const float f2 = __uint_as_float(__byte_perm(v, 0x43000000u, 0x7244));
+    const float f3 = __uint_as_float(__byte_perm(v, 0x43000000u, 0x7344));
+    const float2 w01 = __ffma2_rn(a, make_float2(f0, f1), c);
+    const float2 w23 = __ffma2_rn(a, make_float2(f2, f3), c);
+    o0 = pack_bf16(w01.x, w01.y);
+    o1 = pack_bf16(w23.x, w23.y);
+}
+
+__device__ __forceinline__ void store_row_chunks(uint8_t* A, int r, int cbase, const uint32_t (&pk)[16]) {
+    uint8_t* rowp = A + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int chunk = (cbase + c) ^ (r & 7);
+        *reinterpret_cast<uint4*>(rowp + chunk * 16) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    }
+}
+
+// Q4_K: k-block c = kb % 4 of super-block `blk` (16-byte aligned in shared
+// memory), sub-block j = 2c + hh: codes are nibble hh of qs[32c .. 32c+31].
+// w = (d*sc)*q - dmin*m = ds*(128 + q) - (128 ds + dm).
+__device__ __forceinline__ void fast_q4k(const uint8_t* blk, int c, int hh, uint32_t (&pk)[16]) {
+    const uint4 h = lds128_g(blk);
+    const uint4 q0 = lds128_g(blk + 16 + 32 * c), q1 = lds128_g(blk + 32 + 32 * c);
+    uint32_t sc, m;
+    Fmt<T_Q4_K>::scale_min(blk, 2 * c + hh, sc, m);
+    const float ds = h2f(h.x & 0xFFFFu) * (float)sc, dm = h2f(h.x >> 16) * (float)m;
+    const float2 a = make_float2(ds, ds), cc = make_float2(-(128.0f * ds + dm), -(128.0f * ds + dm));
+    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) four_hi((w[i] >> (4 * hh)) & 0x0F0F0F0Fu, a, cc, pk[2 * i], pk[2 * i + 1]);
+}
+
+// Q8_0: one 34-byte block (2-byte aligned): w = d*q = 128d*(256 + u/128) - 32896d, u = q + 128.
+__device__ __forceinline__ void fast_q80(const uint8_t* blk, uint32_t (&pk)[16]) {
+    uint32_t q[8];
+    gv::lds_words_a2<8>(blk + 2, q);
+    const float d = h2f(ld_u16(blk));
+    const float2 a = make_float2(128.0f * d, 128.0f * d), cc = make_float2(-32896.0f * d, -32896.0f * d);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t u = q[i] ^ 0x80808080u;
+        const float f0 = __uint_as_float(__byte_perm(u, 0x43800000u, 0x7604));
+        const float f1 = __uint_as_float(__byte_perm(u, 0x43800000u, 0x7614));
+        const float f2 = __uint_as_float(__byte_perm(u, 0x43800000u, 0x7624));
+        const float f3 = __uint_as_float(__byte_perm(u, 0x43800000u, 0x7634));
+        const float2 w01 = __ffma2_rn(a, make_float2(f0, f1), cc);
+        const float2 w23 = __ffma2_rn(a, make_float2(f2, f3), cc);
+        pk[2 * i] = pack_bf16(w01.x, w01.y);
+        pk[2 * i + 1] = pack_bf16(w23.x, w23.y);
+    }
+}
+
+// Q6_K: 32 weights o = 64c + 32hh .. of super-block `blk` (2-byte aligned):
+// half t = o / 128, group g = (o % 128) / 32; w = d*sc*(q - 32) = ds*(128 + q) - 160 ds.
+__device__ __forceinline__ void fast_q6k(const uint8_t* blk, int c, int hh, uint32_t (&pk)[16]) {
+    const int o = 64 * c + 32 * hh, t = o >> 7, g = (o >> 5) & 3;
+    uint32_t ql[8], qh[8];
+    gv::lds_words_a2<8>(blk + 64 * t + 32 * (g & 1), ql);
+    gv::lds_words_a2<8>(blk + 128 + 32 * t, qh);
+    const uint32_t sw = ld_u16(blk + 192 + 8 * t + 2 * g);
+    const float d = h2f(ld_u16(blk + 208));
+    const float ds0 = d * (float)(int)(int8_t)(sw & 0xFFu), ds1 = d * (float)(int)(int8_t)(sw >> 8);
+    const int nsh = 4 * (g >> 1), hsh = 2 * g;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float ds = i < 4 ? ds0 : ds1;
+        const uint32_t v = ((ql[i] >> nsh) & 0x0F0F0F0Fu) | (((qh[i] >> hsh) & 0x03030303u) << 4);
+        four_hi(v, make_float2(ds, ds), make_float2(-160.0f * ds, -160.0f * ds), pk[2 * i], pk[2 * i + 1]);
+    }
+}
+
+// 16-weight variants: quarter qq (0..3) of the 64-wide k-block c.
+__device__ __forceinline__ void fast16_q4k(const uint8_t* blk, int c, int qq, uint32_t (&pk)[8]) {
+    const int hh = qq >> 1;   // sub-block 2c + hh, code bytes 16 (qq & 1) .. +16 of its 32
+    const uint4 h = lds128_g(blk);
+    const uint4 q = lds128_g(blk + 16 + 32 * c + 16 * (qq & 1));
+    uint32_t sc, m;
+    Fmt<T_Q4_K>::scale_min(blk, 2 * c + hh, sc, m);
+    const float ds = h2f(h.x & 0xFFFFu) * (float)sc, dm = h2f(h.x >> 16) * (float)m;
+    const float2 a = make_float2(ds, ds), cc = make_float2(-(128.0f * ds + dm), -(128.0f * ds + dm));
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) four_hi((w[i] >> (4 * hh)) & 0x0F0F0F0Fu, a, cc, pk[2 * i], pk[2 * i + 1]);
+}
+
+__device__ __forceinline__ void fast16_q80(const uint8_t* blk, int half, uint32_t (&pk)[8]) {
+    uint32_t q[4];
+    gv::lds_words_a2<4>(blk + 2 + 16 * half, q);
+    const float d = h2f(ld_u16(blk));
+    const float2 a = make_float2(128.0f * d, 128.0f * d), cc = make_float2(-32896.0f * d, -32896.0f * d);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t u = q[i] ^ 0x80808080u;
+        const float f0 = __uint_as_float(__byte_perm(u, 0x43800000u, 0x7604));
+        const float f1 = __uint_as_float(__byte_perm(u, 0x43800000u, 0x7614));
+        const float f2 = __uint_as_float(__byte_perm(u, 0x43800000u, 0x7624));
+        const float f3 = __uint_as_float(__byte_perm(u, 0x43800000u, 0x7634));
+        const float2 w01 = __ffma2_rn(a, make_float2(f0, f1), cc);
+        const float2 w23 = __ffma2_rn(a, make_float2(f2, f3), cc);
+        pk[2 * i] = pack_bf16(w01.x, w01.y);
+        pk[2 * i + 1] = pack_bf16(w23.x, w23.y);
+    }
+}
+
+__device__ __forceinline__ void fast16_q6k(const uint8_t* blk, int c, int qq, uint32_t (&pk)[8]) {
+    const int o = 64 * c + 16 * qq, t = o >> 7, g = (o >> 5) & 3, l0 = o & 31;
+    uint32_t ql[4], qh[4];
+    gv::lds_words_a2<4>(blk + 64 * t + 32 * (g & 1) + l0, ql);
+    gv::lds_words_a2<4>(blk + 128 + 32 * t + l0, qh);
+    const float d = h2f(ld_u16(blk + 208));
+    const float ds = d * (float)(int)(int8_t)blk[192 + 8 * t + 2 * g + (l0 >> 4)];
+    const int nsh = 4 * (g >> 1), hsh = 2 * g;
+    const float2 a = make_float2(ds, ds), cc = make_float2(-160.0f * ds, -160.0f * ds);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t v = ((ql[i] >> nsh) & 0x0F0F0F0Fu) | (((qh[i] >> hsh) & 0x03030303u) << 4);
+        four_hi(v, a, cc, pk[2 * i], pk[2 * i + 1]);
+    }
+}
+
+__device__ __forceinline__ void store_row_chunks2(uint8_t* A, int r, int cbase, const uint32_t (&pk)[8]) {
+    uint8_t* rowp = A + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const int chunk = (cbase + c) ^ (r & 7);
+        *reinterpret_cast<uint4*>(rowp + chunk * 16) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    }
+}
+
+// Generic (Q5_0) 16 weights via the shared decoders: k in [k0, k0 + 16).
+template <int T>
+__device__ __forceinline__ void generic16(const uint8_t* mb, int o, uint32_t (&pk)[8]) {
+    using F = Fmt<T>;
+    int u, h;
+    locate<T>(o % F::BE, u, h);
+    float w[16];
+    dequant_half<T>(mb + (o / F::BE) * F::BB, u, h, w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) pk[i] = pack_bf16(w[2 * i], w[2 * i + 1]);
+}
+
+// Copy macro-block `m` of the tile's 128 rows into packed slot `dst` with
+// 16-byte cp.async (aligned-down windows; thread t takes row t/2, every
+// other chunk).  Bytes past the last full 16 bytes of W are loaded by the
+// consumer of that row (tail_fix).
+template <int T>
+__device__ __forceinline__ void issue_packed(const Args& p, uint8_t* dst, int64_t row0, int64_t m, int r, int part) {
+    using K = Pk<T>;
+    const int64_t row = row0 + r;
+    if (row >= p.rows) return;
+    const int64_t kb0 = m * kMB;
+    const int64_t len = min((int64_t)kMB, p.cols - kb0) / Fmt<T>::BE * Fmt<T>::BB;
+    const int64_t st = row * p.row_bytes + m * K::BYTES;
+    const int64_t a = st & ~(int64_t)15;
+    const int64_t e = min((st + len + 15) & ~(int64_t)15, p.total16);
+    const int nch = e > a ? (int)((e - a) >> 4) : 0;
+    uint8_t* d = dst + r * K::SLOT;
+    for (int ch = part; ch < nch; ch += kParts) cp_async16(d + 16 * ch, p.W + a + 16 * ch);
+}
+
+template <int T>
+__device__ __forceinline__ void tail_fix(const Args& p, uint8_t* slot_row, int64_t row, int64_t m) {
+    using K = Pk<T>;
+    const int64_t kb0 = m * kMB;
+    const int64_t len = min((int64_t)kMB, p.cols - kb0) / Fmt<T>::BE * Fmt<T>::BB;
+    const int64_t st = row * p.row_bytes + m * K::BYTES;
+    if (st + len <= p.total16) return;
+    uint8_t* base = slot_row - (st & ~(int64_t)15);
+    for (int64_t b = max(st, p.total16); b < st + len; ++b) base[b] = p.W[b];
+}
+
 template <int T>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
+    using K = Pk<T>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base (the 128-byte swizzle atoms must be aligned).
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    uint64_t* full_x = reinterpret_cast<uint64_t*>(smem + kNS * kStage);
+    uint8_t* packed = smem_raw + K::OFF_P;
+    uint64_t* full_x = reinterpret_cast<uint64_t*>(smem_raw + K::OFF_BAR);
     uint64_t* full_w = full_x + kNS;
     uint64_t* empty = full_w + kNS;
     uint64_t* accum = empty + kNS;
@@ -139,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             int issued = 0;
             for (int kb = 0; kb < p.nkb; ++kb) {
                 const int s = kb % kNS;
-                if (kb >= kNS && !mbar_wait_bounded(&empty[s], (uint32_t)((kb / kNS - 1) & 1), p.status)) break;
+                if (kb >= kNS && !mbar_wait_sleep_bounded(&empty[s], (uint32_t)((kb / kNS - 1) & 1), p.status)) break;
                 mbar_arrive_expect_tx(&full_x[s], (uint32_t)kB);
                 tc::tma_load_2d(smem + s * kStage + kA, &xmap, kb * kBK, (int)tok0, &full_x[s]);
                 issued = kb + 1;
@@ -155,7 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             for (int kb = 0; kb < p.nkb; ++kb) {
                 const int s = kb % kNS;
                 const uint32_t par = (uint32_t)((kb / kNS) & 1);
-                if (!mbar_wait_bounded(&full_x[s], par, p.status) || !mbar_wait_bounded(&full_w[s], par, p.status))
+                if (!mbar_wait_sleep_bounded(&full_x[s], par, p.status) ||
+                    !mbar_wait_sleep_bounded(&full_w[s], par, p.status))
                     break;
                 tc::fence_after_sync();
                 const uint32_t a = smem_u32(smem + s * kStage), b = a + kA;
@@ -167,25 +397,69 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             }
             tc::commit(accum);   // fires once every MMA issued above has completed
             // Tensor memory may only be released after the MMAs are done.
-            mbar_wait_bounded(accum, 0, p.status);
+            mbar_wait_sleep_bounded(accum, 0, p.status);
         }
     } else {
-        // Dequant warps: thread -> (tile row r, half hh of the 64-wide k-block).
-        const int t = threadIdx.x - 64;
-        const int r = t & (kBM - 1), hh = t >> 7;
+        // Dequant warps.  Warp dw owns tile rows 8dw .. 8dw+7; lane -> (row
+        // 8dw + lane/4, 16-weight quarter lane%4 of each 64-wide k-block).  The
+        // warp streams its rows' packed macro-blocks (256 weights per row) into
+        // a 2-deep ring with cp.async and decodes them with no CTA barrier.
+        const int dw = warp - 2;
+        const int r = 8 * dw + (lane >> 2), qq = lane & 3;
         const int64_t row = row0 + r;
-        for (int kb = 0; kb < p.nkb; ++kb) {
-            const int s = kb % kNS;
-            if (kb >= kNS && !mbar_wait_bounded(&empty[s], (uint32_t)((kb / kNS - 1) & 1), p.status)) break;
-            dequant32<T>(p, smem + s * kStage, r, row, (int64_t)kb * kBK + 32 * hh, 4 * hh);
-            fence_proxy_async_smem();   // generic stores -> visible to the tensor core
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full_w[s]);
+        const int64_t nmb = (p.cols + kMB - 1) / kMB;
+        bool ok = true;
+#pragma unroll 1
+        for (int m = 0; m < kNSP - 1; ++m) {
+            if (m < nmb) issue_packed<T>(p, packed + m * K::STAGE, row0, m, r, qq);
+            cp_async_commit();
         }
+#pragma unroll 1
+        for (int64_t m = 0; m < nmb; ++m) {
+            if (m + kNSP - 1 < nmb)
+                issue_packed<T>(p, packed + ((m + kNSP - 1) % kNSP) * K::STAGE, row0, m + kNSP - 1, r, qq);
+            cp_async_commit();
+            cp_async_wait<kNSP - 1>();
+            uint8_t* pk = packed + (m % kNSP) * K::STAGE;
+            if (qq == 0 && row < p.rows) tail_fix<T>(p, pk + r * K::SLOT, row, m);
+            __syncwarp();   // this warp's rows of macro-block m are visible
+            const int64_t st = row * p.row_bytes + m * K::BYTES;
+            const uint8_t* mbp = pk + r * K::SLOT + (int)(st & 15);
+            for (int kk = 0; kk < kMB / kBK; ++kk) {
+                const int64_t kb = m * (kMB / kBK) + kk;
+                if (kb >= p.nkb) break;
+                const int s = (int)(kb % kNS);
+                if (ok && kb >= kNS) {   // one lane polls, the warp follows
+                    int good = 1;
+                    if (lane == 0) good = mbar_wait_bounded(&empty[s], (uint32_t)((kb / kNS - 1) & 1), p.status);
+                    ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+                }
+                if (ok) {
+                    uint32_t pk8[8];
+                    const int c = (int)(kb & 3);
+                    if (row < p.rows && kb * kBK + 16 * qq < p.cols) {
+                        if constexpr (T == T_Q4_K) fast16_q4k(mbp, c, qq, pk8);
+                        else if constexpr (T == T_Q6_K) fast16_q6k(mbp, c, qq, pk8);
+                        else if constexpr (T == T_Q8_0) fast16_q80(mbp + (2 * c + (qq >> 1)) * 34, qq & 1, pk8);
+                        else generic16<T>(mbp, (int)(kb * kBK + 16 * qq - m * kMB), pk8);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) pk8[i] = 0u;
+                    }
+                    store_row_chunks2(smem + s * kStage, r, 2 * qq, pk8);
+                }
+                fence_proxy_async_smem();   // generic stores -> visible to the tensor core
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full_w[s]);
+            }
+            __syncwarp();   // this warp is done reading slot m % kNSP
+        }
+        cp_async_wait<0>();
         // Epilogue: warps 2..5 cover the four 32-lane quarters of the accumulator.
         if (warp < 6) {
             const int q = warp & 3;
-            mbar_wait_bounded(accum, 0, p.status);
+            if (lane == 0) mbar_wait_sleep_bounded(accum, 0, p.status);
+            __syncwarp();
             tc::fence_after_sync();
             const int64_t orow = row0 + 32 * q + lane;
 #pragma unroll 1
@@ -233,12 +507,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 template <int T>
 static cudaError_t gemm_t(const gm::Args& a, const CUtensorMap& map, cudaStream_t s) {
     auto kern = gm::gemm_kernel<T>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, gm::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, gm::Pk<T>::SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((a.rows + gm::kBM - 1) / gm::kBM), (unsigned)((a.M + gm::kBN - 1) / gm::kBN));
     cfg.blockDim = dim3(gm::kThreads);
-    cfg.dynamicSmemBytes = gm::kSmem;
+    cfg.dynamicSmemBytes = gm::Pk<T>::SMEM;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -271,10 +545,18 @@ cudaError_t launch_gemm(int type, const uint8_t* W, int64_t rows, int64_t cols, 
     a.status = status;
     a.nkb = (int)((cols + gm::kBK - 1) / gm::kBK);
     switch (type) {
-    case T_Q4_K: a.row_bytes = cols / 256 * 144; return gemm_t<T_Q4_K>(a, map, s);
-    case T_Q6_K: a.row_bytes = cols / 256 * 210; return gemm_t<T_Q6_K>(a, map, s);
-    case T_Q8_0: a.row_bytes = cols / 32 * 34; return gemm_t<T_Q8_0>(a, map, s);
-    case T_Q5_0: a.row_bytes = cols / 32 * 22; return gemm_t<T_Q5_0>(a, map, s);
+    case T_Q4_K: a.row_bytes = cols / 256 * 144; break;
+    case T_Q6_K: a.row_bytes = cols / 256 * 210; break;
+    case T_Q8_0: a.row_bytes = cols / 32 * 34; break;
+    case T_Q5_0: a.row_bytes = cols / 32 * 22; break;
+    default: return cudaErrorInvalidValue;
+    }
+    a.total16 = (rows * a.row_bytes) & ~(int64_t)15;
+    switch (type) {
+    case T_Q4_K: return gemm_t<T_Q4_K>(a, map, s);
+    case T_Q6_K: return gemm_t<T_Q6_K>(a, map, s);
+    case T_Q8_0: return gemm_t<T_Q8_0>(a, map, s);
+    case T_Q5_0: return gemm_t<T_Q5_0>(a, map, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -61,6 +61,29 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return false;
 }
 
+// try_wait that lets the hardware suspend the thread for up to `ns`
+// nanoseconds while the phase is incomplete (it resumes when the phase
+// completes), for long waits by threads that should not spin.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait with suspension between checks (total bound about 2 s).
+__device__ __forceinline__ bool mbar_wait_sleep_bounded(uint64_t* bar, uint32_t parity, unsigned* status) {
+    for (uint32_t i = 0; i < (1u << 21); ++i)
+        if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
+    atomicOr(status, STATUS_TIMEOUT);
+    return false;
+}
+
 // Evict-first L2 policy for data streamed exactly once (weights of a GEMV).
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t pol;
