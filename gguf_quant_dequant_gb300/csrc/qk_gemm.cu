@@ -2,16 +2,20 @@
 //
 // Prefill turns the per-token GEMV into a real dense contraction ("12 --
 // llama.cpp / GGUF": prompt processing is big GEMMs of high arithmetic
-// intensity; decode is bandwidth-bound).  A CTA owns 128 weight rows x 256
+// intensity; decode is bandwidth-bound).  A CTA owns 128 weight rows x 512
 // tokens and walks K in blocks of 64:
-//   * 8 dequant warps unpack the packed blocks of the 128 weight rows, round
+//   * 16 dequant warps unpack the packed blocks of the 128 weight rows, round
 //     the fp32 weights to bf16 and store them straight into shared memory in
 //     the tensor core's K-major 128-byte-swizzled layout (operand A);
-//   * one thread loads the 256 x 64 bf16 activation tile with TMA (operand B);
+//   * one thread loads the two 256 x 64 bf16 activation tiles with TMA
+//     (operand B);
 //   * one thread issues tcgen05.mma (M = 128, N = 256, K = 16 per instruction)
-//     into an fp32 accumulator in tensor memory and releases each stage with
-//     tcgen05.commit;
-//   * four warps read the accumulator back (tcgen05.ld) and write Y.
+//     into two fp32 accumulators in tensor memory (tokens 0-255 and 256-511:
+//     all 512 columns) and releases each stage with tcgen05.commit;
+//   * the dequant warps then read the accumulators back (tcgen05.ld) and
+//     write Y.
+// Dequantizing a weight tile is the costly part; covering 512 tokens per
+// tile halves it per FLOP compared with one 256-column accumulator.
 // Every mbarrier wait is bounded; tensor memory is always released.
 #include <algorithm>
 #include <cuda_bf16.h>
@@ -44,28 +48,33 @@ namespace gm {
 __device__ __forceinline__ uint4 lds128_g(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
 
 constexpr int kBM = 128;          // weight rows per CTA (MMA M)
-constexpr int kBN = 256;          // tokens per CTA (MMA N)
+constexpr int kBNM = 256;         // tokens per MMA / accumulator (MMA N)
+constexpr int kNAcc = 2;          // accumulators per CTA
+constexpr int kBN = kBNM * kNAcc; // tokens per CTA
 constexpr int kBK = 64;           // K per stage (one 128-byte swizzle row)
-constexpr int kNS = 3;            // bf16 operand stages
+constexpr int kNS = 2;            // bf16 operand stages
 constexpr int kA = kBM * kBK * 2; // 16 KB
-constexpr int kB = kBN * kBK * 2; // 32 KB
+constexpr int kBsub = kBNM * kBK * 2;   // 32 KB per accumulator's activation tile
+constexpr int kB = kBsub * kNAcc; // 64 KB
 constexpr int kStage = kA + kB;
 constexpr int kDeqWarps = 16;
 constexpr int kDeqThreads = kDeqWarps * 32;
 constexpr int kParts = kDeqThreads / kBM;            // threads per tile row (4): 16 weights each
 constexpr int kThreads = (2 + kDeqWarps) * 32;
-constexpr int kTmemCols = 256;
-constexpr int kMB = 256;          // weights per packed macro-block (one super-block / 8 small blocks)
+constexpr int kTmemCols = kBNM * kNAcc;   // 512: all of tensor memory
 constexpr int kNSP = 2;           // packed macro-block stages
 
-// Packed macro-block geometry: bytes per row, and the per-row slot (the
-// aligned-down window can start up to 15 bytes early; slack for the
-// funnel-shifted reads past the end).
+// Packed macro-block geometry: weights and bytes per row (one super-block,
+// or four / eight 32-weight blocks), and the per-row slot: the aligned-down
+// window starts up to 14 bytes early and the funnel-shifted word reads run up
+// to 4 bytes past the end.
 template <int T> struct Pk {
-    static constexpr int BYTES = kMB / Fmt<T>::BE * Fmt<T>::BB;   // 144, 210, 272, 176
+    static constexpr int MB = T == T_Q8_0 ? 128 : 256;
+    static constexpr int KPM = MB / kBK;                         // k-blocks per macro-block
+    static constexpr int BYTES = MB / Fmt<T>::BE * Fmt<T>::BB;   // 144, 210, 136, 176
     // Row slots are 16-byte multiples (cp.async) and an odd number of 16-byte
     // units, so the 32 rows a warp reads spread over 8 bank groups.
-    static constexpr int SLOT0 = (BYTES + 32 + 15) / 16 * 16;
+    static constexpr int SLOT0 = (BYTES + 14 + 4 + 15) / 16 * 16;
     static constexpr int SLOT = (SLOT0 / 16) % 2 == 0 ? SLOT0 + 16 : SLOT0;
     static constexpr int STAGE = kBM * SLOT;
     static constexpr int OFF_P = 1024 + kNS * kStage;             // packed ring (after the operand stages)
@@ -302,8 +311,8 @@ __device__ __forceinline__ void issue_packed(const Args& p, uint8_t* dst, int64_
     using K = Pk<T>;
     const int64_t row = row0 + r;
     if (row >= p.rows) return;
-    const int64_t kb0 = m * kMB;
-    const int64_t len = min((int64_t)kMB, p.cols - kb0) / Fmt<T>::BE * Fmt<T>::BB;
+    const int64_t kb0 = m * K::MB;
+    const int64_t len = min((int64_t)K::MB, p.cols - kb0) / Fmt<T>::BE * Fmt<T>::BB;
     const int64_t st = row * p.row_bytes + m * K::BYTES;
     const int64_t a = st & ~(int64_t)15;
     const int64_t e = min((st + len + 15) & ~(int64_t)15, p.total16);
@@ -315,8 +324,8 @@ __device__ __forceinline__ void issue_packed(const Args& p, uint8_t* dst, int64_
 template <int T>
 __device__ __forceinline__ void tail_fix(const Args& p, uint8_t* slot_row, int64_t row, int64_t m) {
     using K = Pk<T>;
-    const int64_t kb0 = m * kMB;
-    const int64_t len = min((int64_t)kMB, p.cols - kb0) / Fmt<T>::BE * Fmt<T>::BB;
+    const int64_t kb0 = m * K::MB;
+    const int64_t len = min((int64_t)K::MB, p.cols - kb0) / Fmt<T>::BE * Fmt<T>::BB;
     const int64_t st = row * p.row_bytes + m * K::BYTES;
     if (st + len <= p.total16) return;
     uint8_t* base = slot_row - (st & ~(int64_t)15);
@@ -340,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row0 = (int64_t)blockIdx.x * kBM;
     const int64_t tok0 = (int64_t)blockIdx.y * kBN;
+    const int nacc = p.M - tok0 > kBNM ? 2 : 1;   // accumulators holding real tokens
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNS; ++s) {
@@ -369,8 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             for (int kb = 0; kb < p.nkb; ++kb) {
                 const int s = kb % kNS;
                 if (kb >= kNS && !mbar_wait_sleep_bounded(&empty[s], (uint32_t)((kb / kNS - 1) & 1), p.status)) break;
-                mbar_arrive_expect_tx(&full_x[s], (uint32_t)kB);
-                tc::tma_load_2d(smem + s * kStage + kA, &xmap, kb * kBK, (int)tok0, &full_x[s]);
+                mbar_arrive_expect_tx(&full_x[s], (uint32_t)(kBsub * nacc));
+                for (int j = 0; j < nacc; ++j)
+                    tc::tma_load_2d(smem + s * kStage + kA + j * kBsub, &xmap, kb * kBK, (int)tok0 + kBNM * j,
+                                    &full_x[s]);
                 issued = kb + 1;
             }
             // Every load issued must land before the CTA may exit.
@@ -380,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     } else if (warp == 1) {
         // MMA issuer.
         if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
+            constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBNM);
             for (int kb = 0; kb < p.nkb; ++kb) {
                 const int s = kb % kNS;
                 const uint32_t par = (uint32_t)((kb / kNS) & 1);
@@ -389,10 +401,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     break;
                 tc::fence_after_sync();
                 const uint32_t a = smem_u32(smem + s * kStage), b = a + kA;
+                for (int j = 0; j < nacc; ++j) {
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)
-                    tc::mma_bf16(tmem, tc::sdesc_k128(a + 32 * kk), tc::sdesc_k128(b + 32 * kk), idesc,
-                                 (kb | kk) != 0 ? 1u : 0u);
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        tc::mma_bf16(tmem + kBNM * j, tc::sdesc_k128(a + 32 * kk),
+                                     tc::sdesc_k128(b + kBsub * j + 32 * kk), idesc, (kb | kk) != 0 ? 1u : 0u);
+                }
                 tc::commit(&empty[s]);
             }
             tc::commit(accum);   // fires once every MMA issued above has completed
@@ -402,12 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     } else {
         // Dequant warps.  Warp dw owns tile rows 8dw .. 8dw+7; lane -> (row
         // 8dw + lane/4, 16-weight quarter lane%4 of each 64-wide k-block).  The
-        // warp streams its rows' packed macro-blocks (256 weights per row) into
-        // a 2-deep ring with cp.async and decodes them with no CTA barrier.
+        // warp streams its rows' packed macro-blocks into a 2-deep ring with
+        // cp.async and decodes them with no CTA barrier.
         const int dw = warp - 2;
         const int r = 8 * dw + (lane >> 2), qq = lane & 3;
         const int64_t row = row0 + r;
-        const int64_t nmb = (p.cols + kMB - 1) / kMB;
+        const int64_t nmb = (p.cols + K::MB - 1) / K::MB;
         bool ok = true;
 #pragma unroll 1
         for (int m = 0; m < kNSP - 1; ++m) {
@@ -425,8 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             __syncwarp();   // this warp's rows of macro-block m are visible
             const int64_t st = row * p.row_bytes + m * K::BYTES;
             const uint8_t* mbp = pk + r * K::SLOT + (int)(st & 15);
-            for (int kk = 0; kk < kMB / kBK; ++kk) {
-                const int64_t kb = m * (kMB / kBK) + kk;
+            for (int kk = 0; kk < K::KPM; ++kk) {
+                const int64_t kb = m * K::KPM + kk;
                 if (kb >= p.nkb) break;
                 const int s = (int)(kb % kNS);
                 if (ok && kb >= kNS) {   // one lane polls, the warp follows
@@ -436,12 +450,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 }
                 if (ok) {
                     uint32_t pk8[8];
-                    const int c = (int)(kb & 3);
+                    const int c = kk;
                     if (row < p.rows && kb * kBK + 16 * qq < p.cols) {
                         if constexpr (T == T_Q4_K) fast16_q4k(mbp, c, qq, pk8);
                         else if constexpr (T == T_Q6_K) fast16_q6k(mbp, c, qq, pk8);
                         else if constexpr (T == T_Q8_0) fast16_q80(mbp + (2 * c + (qq >> 1)) * 34, qq & 1, pk8);
-                        else generic16<T>(mbp, (int)(kb * kBK + 16 * qq - m * kMB), pk8);
+                        else generic16<T>(mbp, kk * kBK + 16 * qq, pk8);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 8; ++i) pk8[i] = 0u;
@@ -455,22 +469,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             __syncwarp();   // this warp is done reading slot m % kNSP
         }
         cp_async_wait<0>();
-        // Epilogue: warps 2..5 cover the four 32-lane quarters of the accumulator.
-        if (warp < 6) {
-            const int q = warp & 3;
+        // Epilogue: warp w may read tensor-memory lanes 32 (w % 4) .. +31 (its
+        // quarter of the weight rows); the four warps of a quarter split the
+        // 512 accumulator columns (tokens) into 128-column groups.
+        {
+            const int q = warp & 3, grp = dw >> 2;
             if (lane == 0) mbar_wait_sleep_bounded(accum, 0, p.status);
             __syncwarp();
             tc::fence_after_sync();
             const int64_t orow = row0 + 32 * q + lane;
 #pragma unroll 1
-            for (int j = 0; j < kBN / 16; ++j) {
+            for (int j = 0; j < 128 / 16; ++j) {
+                const int col = 128 * grp + 16 * j;
+                if (tok0 + col >= p.M) break;   // warp-uniform
                 uint32_t v[16];
-                tc::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 16 * j, v);
+                tc::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + col, v);
                 tc::tmem_wait_ld();
+                if (orow < p.rows) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int64_t tok = tok0 + 16 * j + i;
-                    if (tok < p.M && orow < p.rows) p.Y[tok * p.rows + orow] = __uint_as_float(v[i]);
+                    for (int i = 0; i < 16; ++i) {
+                        const int64_t tok = tok0 + col + i;
+                        if (tok < p.M) p.Y[tok * p.rows + orow] = __uint_as_float(v[i]);
+                    }
                 }
             }
         }
@@ -506,6 +526,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 template <int T>
 static cudaError_t gemm_t(const gm::Args& a, const CUtensorMap& map, cudaStream_t s) {
+    static_assert(gm::Pk<T>::SMEM <= 227 * 1024, "shared memory per CTA");
     auto kern = gm::gemm_kernel<T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, gm::Pk<T>::SMEM);
     if (e != cudaSuccess) return e;
@@ -530,7 +551,7 @@ cudaError_t launch_gemm(int type, const uint8_t* W, int64_t rows, int64_t cols, 
     CUtensorMap map;
     cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)M};
     cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {(cuuint32_t)gm::kBK, (cuuint32_t)gm::kBN};
+    cuuint32_t box[2] = {(cuuint32_t)gm::kBK, (cuuint32_t)gm::kBNM};
     cuuint32_t estride[2] = {1, 1};
     CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), gdim, gstride, box, estride,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

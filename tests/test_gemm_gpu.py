@@ -1,7 +1,8 @@
 """qk_gemm (tcgen05 tensor-core dequant-GEMM) against the oracle fed the same
 bf16 activations: |Y - Y_ref| <= 5e-3 * sum|w x| per output.  Shapes cover
 one tile, ragged weight rows and token counts, a K whose last 64-block is
-half empty (32-weight blocks), every quant type, and M from 1 to 300."""
+half empty (32-weight blocks), every quant type, M from 1 to 1100, token
+tiles whose second 256-token accumulator is empty, partial or full."""
 import numpy as np
 import pytest
 import torch
@@ -21,6 +22,9 @@ CASES = [
     ("Q5_0", 256, 160, 1),
     ("Q5_0", 64, 1024, 257),
     ("Q8_0", 384, 2048, 512),
+    ("Q4_K", 256, 512, 600),     # two 512-token tiles, the second with one live accumulator
+    ("Q6_K", 130, 512, 1100),    # three token tiles, ragged rows
+    ("Q5_0", 128, 320, 513),     # second tile holds a single token
 ]
 
 
