@@ -38,6 +38,8 @@ SIGNATURES = {
     "qk_gemv_workspace": (_sz, [_int, _i64, _i64, _i64]),
     "qk_gemv": (_int, [_int, _p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
     "qk_gemv_noalloc": (_int, [_int, _p, _i64, _i64, _p, _i64, _p, _p]),
+    "qk_gemv_batch": (_int, [_int, _int, ctypes.POINTER(_p), ctypes.POINTER(_i64), _i64, _p,
+                             ctypes.POINTER(_p), _p]),
     "qk_gemm_workspace": (_sz, [_int, _i64, _i64, _i64]),
     "qk_gemm": (_int, [_int, _p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
     "qk_unpack": (_int, [_int, _p, _i64, _p, _p, _p, _p, _p, _p]),
@@ -136,6 +138,20 @@ def gemv_noalloc(t: int, W, rows: int, cols: int, x, y=None, stream=None):
     _check(load().qk_gemv_noalloc(t, _ptr(W), rows, cols, _ptr(x), M, _ptr(y), _stream(stream)),
            "qk_gemv_noalloc")
     return y
+
+
+def gemv_batch(t: int, Ws, rows, cols: int, x, ys=None, stream=None):
+    """qk_gemv_batch: y_i = W_i x for matrices sharing one fp32 activation row
+    x [cols] (or [1, cols]); returns the list of fp32 outputs [rows_i]."""
+    import torch
+    n = len(Ws)
+    if ys is None:
+        ys = [torch.empty(r, dtype=torch.float32, device=x.device) for r in rows]
+    Wp = (_p * n)(*[_ptr(w) for w in Ws])
+    rp = (_i64 * n)(*rows)
+    yp = (_p * n)(*[_ptr(y) for y in ys])
+    _check(load().qk_gemv_batch(t, n, Wp, rp, cols, _ptr(x), yp, _stream(stream)), "qk_gemv_batch")
+    return ys
 
 
 def gemm_workspace(t: int, rows: int, cols: int, M: int) -> int:

@@ -178,6 +178,46 @@ qk_status qk_gemv(int type, const void* W, int64_t rows, int64_t cols, const flo
     return QK_OK;
 }
 
+qk_status qk_gemv_batch(int type, int n_mat, const void* const* W, const int64_t* rows, int64_t cols,
+                        const float* x, float* const* y, void* stream) {
+    if (!known_type(type)) return fail(QK_ERR_TYPE, "unknown quant type %d", type);
+    if (n_mat < 1 || n_mat > QK_GEMV_BATCH_MAX)
+        return fail(QK_ERR_ARG, "n_mat=%d outside 1..%d", n_mat, QK_GEMV_BATCH_MAX);
+    if (!W || !rows || !y) return fail(QK_ERR_NULL, "W, rows or y array is NULL");
+    int64_t total = 0;
+    for (int i = 0; i < n_mat; ++i) {
+        qk_status st = check_matrix(type, W[i], rows[i], cols);
+        if (st != QK_OK) return st;
+        if (rows[i] > 0) {
+            if (!y[i]) return fail(QK_ERR_NULL, "y[%d] is NULL", i);
+            if (!aligned(y[i], 4)) return fail(QK_ERR_ALIGN, "y[%d] is not 4-byte aligned", i);
+        }
+        total += rows[i];
+    }
+    if (total == 0) return QK_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cols == 0) {
+        for (int i = 0; i < n_mat; ++i) {
+            if (rows[i] == 0) continue;
+            cudaError_t e = cudaMemsetAsync(y[i], 0, (size_t)rows[i] * sizeof(float), s);
+            if (e != cudaSuccess) return cuda_fail(e, "qk_gemv_batch zero fill");
+        }
+        return QK_OK;
+    }
+    if (!x) return fail(QK_ERR_NULL, "x is NULL");
+    if (!aligned(x, 16)) return fail(QK_ERR_ALIGN, "x is not 16-byte aligned");
+    int sms = 0;
+    qk_status st = device_state(nullptr, &sms);
+    if (st != QK_OK) return st;
+    if (qk::gemv5_ring_pairs(type, n_mat, rows, cols, sms) == 0)
+        return fail(QK_ERR_SHAPE, "cols=%lld is too large for the batched decode kernel", (long long)cols);
+    cudaError_t e = qk::launch_gemv5(type, n_mat, reinterpret_cast<const uint8_t* const*>(W), rows, cols, x, y, sms,
+                                     s);
+    if (e != cudaSuccess) return cuda_fail(e, "qk_gemv_batch launch");
+    g_last_error.clear();
+    return QK_OK;
+}
+
 size_t qk_gemm_workspace(int type, int64_t rows, int64_t cols, int64_t M) {
     (void)type; (void)rows; (void)cols; (void)M;
     return 0;

@@ -20,11 +20,19 @@ cudaError_t launch_unpack(int type, const uint8_t* W, int64_t nblocks, int16_t* 
 
 // GEMV launch plan: how the [rows, cols] x [M] problem is cut into CTAs.
 struct GemvPlan {
+    bool decode = false; // M == 1 decode kernel (activation prep inside; no workspace)
+    int sms = 0;         // SM count the plan was made for
     int mt = 1;          // activation rows per CTA pass (template width)
     int splits = 1;      // K splits (partials reduced by a second kernel)
     int64_t ws_bytes = 0;
 };
 GemvPlan plan_gemv(int type, int64_t rows, int64_t cols, int64_t M, int sm_count);
+// Decode GEMV (M == 1) over n <= QK_GEMV_BATCH_MAX matrices sharing x:
+// ring depth (row pairs per warp) that fits the kernel's shared memory for
+// this shape (0: K too large, use the prep + tiled kernel).
+int gemv5_ring_pairs(int type, int n, const int64_t* rows, int64_t cols, int sms);
+cudaError_t launch_gemv5(int type, int n, const uint8_t* const* W, const int64_t* rows, int64_t cols, const float* x,
+                         float* const* y, int sms, cudaStream_t s);
 cudaError_t launch_gemv(int type, const GemvPlan& plan, const uint8_t* W, int64_t rows, int64_t cols,
                         const float* x, int64_t M, float* y, float* ws, unsigned* status, cudaStream_t s);
 

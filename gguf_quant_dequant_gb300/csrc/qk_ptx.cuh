@@ -114,6 +114,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
+// 16-byte cp.async to a shared address given as a 32-bit offset, with an L2
+// cache policy (e.g. evict-first for bytes read once); issued only when
+// off < lim (unsigned).
+__device__ __forceinline__ void cp_async16_if_lt(uint32_t sdst, const void* src, uint64_t policy, uint32_t off,
+                                                 uint32_t lim) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.lt.u32 q, %3, %4;\n\t"
+        "@q cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;\n\t}" ::"r"(sdst),
+        "l"(src), "l"(policy), "r"(off), "r"(lim)
+        : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }

@@ -117,6 +117,33 @@ qk_status qk_gemv(int type, const void* W, int64_t rows, int64_t cols,
                   const float* x, int64_t M, float* y,
                   void* ws, size_t ws_bytes, void* stream);
 
+/* Most matrices one qk_gemv_batch call takes. */
+#define QK_GEMV_BATCH_MAX 8
+
+/* Decode GEMV over several matrices that read the same activation vector, in
+ * one launch: y_i[n] = sum_k W_i[n, k] * x[k] for i < n_mat, n < rows[i].
+ * In a decoder layer the query, key and value projections are applied to the
+ * same hidden state ("How LLM Inference Engines Work", Grouped-Query
+ * Attention (GQA) and KV Cache), and so are the gate and up projections of
+ * the feed-forward block (same page, SwiGLU Feed-Forward Network).  One call
+ * per such group prepares x once and spreads the rows of all its matrices
+ * over the GPU, instead of paying a launch and a ramp per matrix.
+ *   type, cols  common to all matrices.
+ *   W     host array of n_mat device pointers, W[i] = packed blocks
+ *         [rows[i], cols], 16-byte aligned.
+ *   rows  host array of n_mat row counts (0 allowed: that matrix is skipped).
+ *   x     fp32 [cols] (one activation row), 16-byte aligned, device.
+ *   y     host array of n_mat device pointers, y[i] = fp32 [rows[i]], 4-byte
+ *         aligned; fully overwritten.
+ * The host arrays are read during the call only.  No workspace.  K is
+ * limited by the kernel's shared memory (the limbs of x take 112 bytes per
+ * 32 elements, beside at least four row slots per warp): about 12K columns
+ * for Q8_0 up to about 21K for Q4_K; a larger cols is QK_ERR_SHAPE.
+ * n_mat outside 1..QK_GEMV_BATCH_MAX is QK_ERR_ARG.  Accuracy and
+ * determinism as qk_gemv. */
+qk_status qk_gemv_batch(int type, int n_mat, const void* const* W, const int64_t* rows, int64_t cols,
+                        const float* x, float* const* y, void* stream);
+
 /* Size of the fixed scratch array qk_gemv_noalloc uses: 8 MiB per device. */
 #define QK_GEMV_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 

@@ -80,6 +80,31 @@ def test_argument_errors_are_caught_on_host(lib):
     assert lib.qk_unpack(qk.Q4_K, fake, -1, None, None, None, None, None, None) == 2
 
 
+def test_batch_argument_errors_are_caught_on_host(lib):
+    fake, odd = 0x10000, 0x10008
+    P = ctypes.c_void_p
+
+    def call(t, n, Ws, rows, cols, x, ys):
+        Wa = (P * max(len(Ws), 1))(*Ws)
+        ra = (ctypes.c_int64 * max(len(rows), 1))(*rows)
+        ya = (P * max(len(ys), 1))(*ys)
+        return lib.qk_gemv_batch(t, n, Wa, ra, cols, x, ya, None)
+
+    assert call(9, 1, [fake], [4], 256, fake, [fake]) == 1
+    assert call(qk.Q4_K, 0, [fake], [4], 256, fake, [fake]) == 8
+    assert call(qk.Q4_K, 9, [fake] * 9, [4] * 9, 256, fake, [fake] * 9) == 8
+    assert b"n_mat" in lib.qk_last_error()
+    assert call(qk.Q4_K, 2, [fake, odd], [4, 4], 256, fake, [fake, fake]) == 3
+    assert call(qk.Q4_K, 2, [fake, fake], [4, 4], 256, fake, [fake, None]) == 4
+    assert call(qk.Q4_K, 2, [fake, fake], [4, 4], 100, fake, [fake, fake]) == 2
+    assert call(qk.Q4_K, 2, [fake, fake], [4, -1], 256, fake, [fake, fake]) == 2
+    assert call(qk.Q4_K, 1, [fake], [4], 256, None, [fake]) == 4
+    assert call(qk.Q4_K, 1, [fake], [4], 256, odd, [fake]) == 3
+    assert lib.qk_gemv_batch(qk.Q4_K, 1, None, None, 256, fake, None, None) == 4
+    # all-empty batches queue nothing
+    assert call(qk.Q4_K, 2, [None, None], [0, 0], 256, None, [None, None]) == 0
+
+
 def test_empty_problems_queue_nothing(lib):
     fake = ctypes.c_void_p(0x10000)
     # rows == 0 or M == 0: success without touching the device.

@@ -130,12 +130,78 @@ def test_output_canaries_and_empty(gpu):
 
 
 def test_workspace_too_small_is_rejected(gpu):
+    # M = 2 runs the activation-prep kernel, whose output lives in the workspace.
     t, rows, cols = qk.Q4_K, 16, 4096
-    need = qk.gemv_workspace(t, rows, cols, 1)
+    need = qk.gemv_workspace(t, rows, cols, 2)
     assert need > 0
     W = dev_u8(synth.random_blocks("Q4_K", rows, cols, 97), gpu)
-    x = dev_f32(synth.activations(1, cols, 98), gpu)
+    x = dev_f32(synth.activations(2, cols, 98), gpu)
     small = torch.empty(need - 16, dtype=torch.uint8, device=gpu)
     with pytest.raises(qk.QKError) as e:
         qk.gemv(t, W, rows, cols, x, ws=small)
     assert e.value.status == 5
+
+
+def test_decode_needs_no_workspace_and_large_k_falls_back(gpu):
+    # M = 1 preps x inside the decode kernel: no workspace.  When x's limbs
+    # would not fit that kernel's shared memory (Q6_K, K = 20480), the call
+    # takes the prep + tiled path, whose workspace holds the limbs.
+    assert qk.gemv_workspace(qk.Q4_K, 4096, 4096, 1) == 0
+    assert qk.gemv_workspace(qk.Q6_K, 4096, 11008, 1) == 0
+    rows, cols = 24, 20480
+    assert qk.gemv_workspace(qk.Q6_K, rows, cols, 1) > 0
+    W = synth.random_blocks("Q6_K", rows, cols, 4321)
+    x = synth.activations(1, cols, 4322)
+    y = qk.gemv(qk.Q6_K, dev_u8(W, gpu), rows, cols, dev_f32(x, gpu)).cpu().numpy()
+    y_ref, S = oracle.gemv(qk.Q6_K, W, rows, cols, x)
+    assert_gemv_close(y, y_ref, S, what="Q6_K K=20480 fallback")
+
+
+@pytest.mark.parametrize("name,rows,cols", [("Q6_K", 9, 11008), ("Q4_K", 151, 4096), ("Q4_K", 153, 2304),
+                                            ("Q8_0", 1000, 4128), ("Q5_0", 3, 96)])
+def test_decode_row_splits(gpu, name, rows, cols):
+    # Fewer rows than SMs, one row more than the SMs on some CTAs, a K whose
+    # last 2048-slice is short, and a K that is a single 32-block short of
+    # full slices.
+    t = type_id(name)
+    W = synth.random_blocks(name, rows, cols, 4400 + rows)
+    x = synth.activations(1, cols, 4500 + rows)
+    y = qk.gemv(t, dev_u8(W, gpu), rows, cols, dev_f32(x, gpu)).cpu().numpy()
+    y_ref, S = oracle.gemv(t, W, rows, cols, x)
+    assert_gemv_close(y, y_ref, S, what=f"{name} {rows}x{cols}")
+
+
+@pytest.mark.parametrize("name,rows_list,cols", [
+    ("Q4_K", [512, 128, 128], 4096),                       # q / k / v (grouped-query shapes)
+    ("Q4_K", [700, 700], 2048),                            # gate / up
+    ("Q6_K", [300, 0, 45], 11008),                         # an empty member
+    ("Q8_0", [1, 2, 3, 5, 8, 13, 21, 34], 1024),           # the most members, tiny ones
+    ("Q5_0", [333, 77], 1056),
+])
+def test_gemv_batch_matches_oracle(gpu, name, rows_list, cols):
+    # One launch over matrices that share x gives each matrix's GEMV.
+    t = type_id(name)
+    x = synth.activations(1, cols, 4600 + cols)
+    xd = dev_f32(x, gpu)
+    Ws = [synth.random_blocks(name, r, cols, 4700 + 31 * i + r) if r else np.zeros(0, np.uint8)
+          for i, r in enumerate(rows_list)]
+    Wd = [dev_u8(W, gpu) if W.size else torch.zeros(16, dtype=torch.uint8, device=gpu) for W in Ws]
+    ys = qk.gemv_batch(t, Wd, rows_list, cols, xd[0])
+    qk.device_status()
+    for i, (W, r) in enumerate(zip(Ws, rows_list)):
+        if r == 0:
+            continue
+        y_ref, S = oracle.gemv(t, W, r, cols, x)
+        assert_gemv_close(ys[i].cpu().numpy()[None, :], y_ref, S, what=f"{name} member {i}")
+        # and the same as the single-matrix entry point, to the tolerance
+        y1 = qk.gemv(t, Wd[i], r, cols, xd).cpu().numpy()
+        assert_gemv_close(ys[i].cpu().numpy()[None, :], y1.astype(np.float64), S, what=f"{name} member {i} vs qk_gemv")
+
+
+def test_gemv_batch_rejects_large_k(gpu):
+    t, cols = qk.Q6_K, 20480
+    W = torch.zeros(8 * qk.row_bytes(t, cols), dtype=torch.uint8, device=gpu)
+    x = torch.zeros(cols, device=gpu)
+    with pytest.raises(qk.QKError) as e:
+        qk.gemv_batch(t, [W], [8], cols, x)
+    assert e.value.status == 2

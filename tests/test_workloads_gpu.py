@@ -75,3 +75,23 @@ def test_llama3_ffn_batches(gpu, name, M):
         xd = torch.randn((M, cols), device=gpu, generator=g)
         y = qk.gemv(t, Wd, rows, cols, xd).cpu().numpy()
         _sampled_check(gpu, t, Wd, rows, cols, xd, y, 48, 6200 + i, f"{nm} M={M}")
+
+
+def test_decode_large_rows_several_reduction_chunks(gpu):
+    # 40000 x 16384 Q4_K at M = 1: eight K slices, so a CTA's 264 rows are
+    # reduced in two chunks of partial sums; sampled outputs, with rows at
+    # both ends of the matrix.
+    name, rows, cols = "Q4_K", 40000, 16384
+    t = type_id(name)
+    Wd = synth.random_blocks_torch(name, rows, cols, 7100, gpu)
+    g = torch.Generator(device=gpu)
+    g.manual_seed(7101)
+    xd = torch.randn((1, cols), device=gpu, generator=g)
+    y = qk.gemv(t, Wd, rows, cols, xd).cpu().numpy()
+    _sampled_check(gpu, t, Wd, rows, cols, xd, y, 48, 7102, "Q4_K 40000x16384")
+    rb = qk.row_bytes(t, cols)
+    ends = np.array([0, 255, 256, 263, 264, rows - 1])
+    Wrows = torch.cat([Wd[n * rb:(n + 1) * rb] for n in ends]).cpu().numpy()
+    y_ref, S = oracle.entries(t, Wrows, ends.size, cols, np.zeros(ends.size, dtype=np.int64),
+                              np.arange(ends.size), x=xd.cpu().numpy())
+    assert_gemv_close(y[0, ends], y_ref, S, what="chunk edges")
