@@ -2,11 +2,13 @@
 layer at decode batch 1 (q/k/v/o 4096x4096 Q4_K, gate/up 11008x4096 Q4_K,
 down 4096x11008 Q6_K; x fp32 ~ N(0, 1)).
 
-One step = the seven GEMVs of one layer through the C ABI (qk_gemv), i.e.
-one pass of the whole hot path: load packed blocks, unpack scales and codes,
-dequantize inside the dot product, accumulate, reduce.  The step cycles
-through distinct copies of the layer whose total exceeds the L2 cache, so
-every step streams its weights from HBM.
+One step = the seven GEMVs of one layer through the C ABI, i.e. one pass of
+the whole hot path: load packed blocks, unpack scales and codes, dequantize
+inside the dot product, accumulate, reduce.  Matrices that read the same
+activation vector go in one launch, as in a decoder layer: q/k/v
+(qk_gemv_batch), o (qk_gemv), gate/up (qk_gemv_batch), down (qk_gemv).  The
+step cycles through distinct copies of the layer whose total exceeds the L2
+cache, so every step streams its weights from HBM.
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on
 the host cores instead (a bounded sample of the same workload).
@@ -40,14 +42,46 @@ def peaks():
         return 6800.0, "fallback"
 
 
-def layer_bytes(layer):
-    """Algorithmic bytes of one decode step of the layer: packed weights +
-    fp32 activations read + fp32 outputs written."""
+def group_bytes(layer, group):
+    """Algorithmic bytes of one launch: the group's packed weights, its one
+    fp32 activation vector and its fp32 outputs."""
     import synth
-    tot = 0
-    for (_, name, rows, cols) in layer:
-        tot += rows * synth.row_bytes(name, cols) + 4 * cols + 4 * rows
+    tot = 4 * layer[group[0]][3]
+    for i in group:
+        (_, name, rows, cols) = layer[i]
+        tot += rows * synth.row_bytes(name, cols) + 4 * rows
     return tot
+
+
+def layer_bytes(layer, groups):
+    return sum(group_bytes(layer, g) for g in groups)
+
+
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemv_decode_q4k_traffic.json")
+KERNEL_SOURCES = ["qk_gemv5.cu", "qk_lanes.cuh", "qk_ptx.cuh", "qk_formats.cuh"]
+
+
+def kernel_sources_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "gguf_quant_dequant_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic():
+    """DRAM bytes per Q4_K decode launch of the step (mean over q/k/v, o and
+    gate/up) from the committed ncu summary, or None when the kernel sources
+    changed since it was captured."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        if rec.get("kernel_sources_sha256") != kernel_sources_digest():
+            return None
+        return float(rec["mean_dram_bytes_per_launch"])
+    except Exception:
+        return None
 
 
 class Clocks:
@@ -126,29 +160,29 @@ def _max_over_ranks(v: float, world: int) -> float:
 
 def build_layer_copies(dev, ncopies):
     """ncopies distinct layers of packed weights on the device, plus one
-    activation vector, output and workspace per matrix."""
+    activation vector per launch group and one output per matrix."""
     import torch
-    import gguf_quant_dequant_gb300 as qk
     import synth
-    layer = synth.LLAMA7B_LAYER
+    layer, groups = synth.LLAMA7B_LAYER, synth.LLAMA7B_LAYER_GROUPS
     Ws = [[synth.random_blocks_torch(name, rows, cols, 100 * c + i, dev)
            for i, (_, name, rows, cols) in enumerate(layer)] for c in range(ncopies)]
     g = torch.Generator(device=dev)
     g.manual_seed(4242)
-    xs = [torch.randn((1, cols), device=dev, generator=g) for (_, _, _, cols) in layer]
-    ys = [torch.empty((1, rows), device=dev) for (_, _, rows, _) in layer]
-    ws_need = max(qk.gemv_workspace(synth.TYPE_IDS[name], rows, cols, 1) for (_, name, rows, cols) in layer)
-    ws = torch.empty(max(ws_need, 16), dtype=torch.uint8, device=dev)
-    return layer, Ws, xs, ys, ws
+    xs = [torch.randn(layer[grp[0]][3], device=dev, generator=g) for grp in groups]
+    ys = [torch.empty(rows, device=dev) for (_, _, rows, _) in layer]
+    return layer, groups, Ws, xs, ys
 
 
-def launches_per_step(layer):
+def run_group(layer, grp, W, x, ys):
+    """One launch: qk_gemv for a single matrix, qk_gemv_batch for a group."""
     import gguf_quant_dequant_gb300 as qk
     import synth
-    n = 0
-    for (_, name, rows, cols) in layer:
-        n += 1 + (qk.gemv_workspace(synth.TYPE_IDS[name], rows, cols, 1) > 0)
-    return n
+    (_, name, rows, cols) = layer[grp[0]]
+    t = synth.TYPE_IDS[name]
+    if len(grp) == 1:
+        qk.gemv(t, W[grp[0]], rows, cols, x.view(1, cols), y=ys[grp[0]].view(1, rows))
+    else:
+        qk.gemv_batch(t, [W[i] for i in grp], [layer[i][2] for i in grp], cols, x, ys=[ys[i] for i in grp])
 
 
 def run_gpu(args):
@@ -169,17 +203,19 @@ def run_gpu(args):
 
     wbytes = sum(rows * synth.row_bytes(name, cols) for (_, name, rows, cols) in synth.LLAMA7B_LAYER)
     ncopies = max(2, -(-4 * L2_BYTES // wbytes))
-    layer, Ws, xs, ys, ws = build_layer_copies(dev, ncopies)
-    lb = layer_bytes(layer)
+    layer, groups, Ws, xs, ys = build_layer_copies(dev, ncopies)
+    lb = layer_bytes(layer, groups)
+    for grp in groups:   # every launch runs the decode kernel (no workspace, no prep kernel)
+        (_, name, rows, cols) = layer[grp[0]]
+        assert qk.gemv_workspace(synth.TYPE_IDS[name], rows, cols, 1) == 0
 
     def step(c):
-        for i, (_, name, rows, cols) in enumerate(layer):
-            qk.gemv(synth.TYPE_IDS[name], Ws[c][i], rows, cols, xs[i], y=ys[i], ws=ws)
+        for gi, grp in enumerate(groups):
+            run_group(layer, grp, Ws[c], xs[gi], ys)
 
-    def sub_step(c, idx):
-        for i in idx:
-            (_, name, rows, cols) = layer[i]
-            qk.gemv(synth.TYPE_IDS[name], Ws[c][i], rows, cols, xs[i], y=ys[i], ws=ws)
+    def sub_step(c, gidx):
+        for gi in gidx:
+            run_group(layer, groups[gi], Ws[c], xs[gi], ys)
 
     # Warm the kernels up eagerly once (module load, attributes), then capture
     # one CUDA graph per layer copy.
@@ -192,19 +228,19 @@ def run_gpu(args):
         with torch.cuda.graph(g):
             step(c)
         graphs.append(g)
-    q4_idx = [i for i, l in enumerate(layer) if l[1] == "Q4_K"]
+    q4_groups = [gi for gi, grp in enumerate(groups) if layer[grp[0]][1] == "Q4_K"]
     q4_graphs = []
     for c in range(ncopies):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            sub_step(c, q4_idx)
+            sub_step(c, q4_groups)
         q4_graphs.append(g)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
     K, W = args.steps, args.warmup
     with Clocks(local) as clk:
-        t_end = time.time() + 1.0
+        t_end = time.time() + args.min_warmup_s
         i = 0
         while i < W or time.time() < t_end:
             graphs[i % ncopies].replay()
@@ -224,7 +260,8 @@ def run_gpu(args):
         ms = e0.elapsed_time(e1)
         _barrier(world)
         torch.cuda.synchronize()
-        # Dominant kernel alone: the six Q4_K GEMVs of a layer, same rotation.
+        # Dominant kernel alone: the three Q4_K launches of a layer (q/k/v,
+        # o, gate/up), same rotation.
         reps = max(K, 200)
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
@@ -239,12 +276,11 @@ def run_gpu(args):
     ms_step = ms_max / K
     value = world * lb / (ms_step * 1e-3) / 1e9
 
-    q4_launch_bytes = sum(layer[i][2] * synth.row_bytes("Q4_K", layer[i][3]) + 4 * layer[i][3] + 4 * layer[i][2]
-                          for i in q4_idx) / len(q4_idx)
-    q4_launch_ms = q4_ms / (reps * len(q4_idx))
+    q4_launch_bytes = sum(group_bytes(layer, groups[gi]) for gi in q4_groups) / len(q4_groups)
+    q4_launch_ms = q4_ms / (reps * len(q4_groups))
     achieved = q4_launch_bytes / (q4_launch_ms * 1e-3) / 1e9
 
-    e2e = run_e2e(args, dev, layer, Ws[0], xs, lb) if rank == 0 else None
+    e2e = run_e2e(args, dev, layer, groups, Ws[0], xs, lb) if rank == 0 else None
     del Ws, graphs, q4_graphs
     torch.cuda.empty_cache()
     gemm = None
@@ -258,6 +294,7 @@ def run_gpu(args):
         except Exception:
             pass
     cpu = cpu_baseline(layer) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    traffic = recorded_traffic()
     if rank == 0:
         out = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -266,17 +303,19 @@ def run_gpu(args):
             "data": "synthetic (seeded random blocks, x ~ N(0,1))",
             "config": {"workload": "Llama-7B-shaped decoder layer, decode batch 1: q/k/v/o 4096x4096 Q4_K, "
                                    "gate/up 11008x4096 Q4_K, down 4096x11008 Q6_K",
+                       "launches": "q/k/v one qk_gemv_batch (shared x), o qk_gemv, gate/up one qk_gemv_batch "
+                                   "(shared x), down qk_gemv",
                        "bytes_per_step": lb, "layer_copies_rotated": ncopies,
                        "l2": f"inputs larger than L2: {ncopies} distinct layer copies "
                              f"({ncopies * wbytes / 2**20:.0f} MiB) rotated per step",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "timing": "CUDA graph per layer copy, CUDA events on the launch stream"},
             "frac_of_peak": round(value / world / hbm_peak, 4),
-            "roofline": {"bound": "hbm", "kernel": "gemv4_kernel<Q4_K> (M=1 decode)", "achieved": round(achieved, 2),
-                         "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s",
-                         "frac": round(achieved / hbm_peak, 4), "traffic": None,
+            "roofline": {"bound": "hbm", "kernel": "gemv5_kernel<Q4_K> (decode; q/k/v, o and gate/up launches)",
+                         "achieved": round(achieved, 2), "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s",
+                         "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                          "launch_bytes": int(q4_launch_bytes), "launch_us": round(q4_launch_ms * 1e3, 3)},
-            "gpu_launches": K * launches_per_step(layer),
+            "gpu_launches": K * len(groups),
             "clocks": clocks,
             "e2e": e2e,
             "cpu_baseline": cpu,
@@ -350,29 +389,27 @@ def run_gemm_bench(dev, reps: int = 5):
             "comparator_note": "qk_dequant to bf16 then torch.matmul, same 9 matrices (vocab excluded)"}
 
 
-def run_e2e(args, dev, layer, Wd, xs, lb):
+def run_e2e(args, dev, layer, groups, Wd, xs, lb):
     """Same step through the C ABI from pinned HOST buffers: every step copies
-    the layer's packed weights and activations host->device, runs the seven
-    GEMVs and copies the outputs back; all inside the timed region."""
+    the layer's packed weights and activations host->device, runs the four
+    launches and copies the outputs back; all inside the timed region."""
     import torch
-    import gguf_quant_dequant_gb300 as qk
-    import synth
     Wh = [w.cpu().pin_memory() for w in Wd]
     xh = [x.cpu().pin_memory() for x in xs]
-    yd = [torch.empty((1, rows), device=dev) for (_, _, rows, _) in layer]
-    yh = [torch.empty((1, rows)).pin_memory() for (_, _, rows, _) in layer]
+    yd = [torch.empty(rows, device=dev) for (_, _, rows, _) in layer]
+    yh = [torch.empty(rows).pin_memory() for (_, _, rows, _) in layer]
     xd = [torch.empty_like(x, device=dev) for x in xs]
     Wdd = [torch.empty_like(w, device=dev) for w in Wd]
-    ws_need = max(qk.gemv_workspace(synth.TYPE_IDS[name], rows, cols, 1) for (_, name, rows, cols) in layer)
-    ws = torch.empty(max(ws_need, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def step():
-        for i, (_, name, rows, cols) in enumerate(layer):
-            Wdd[i].copy_(Wh[i], non_blocking=True)
-            xd[i].copy_(xh[i], non_blocking=True)
-            qk.gemv(synth.TYPE_IDS[name], Wdd[i], rows, cols, xd[i], y=yd[i], ws=ws)
-            yh[i].copy_(yd[i], non_blocking=True)
+        for gi, grp in enumerate(groups):
+            for i in grp:
+                Wdd[i].copy_(Wh[i], non_blocking=True)
+            xd[gi].copy_(xh[gi], non_blocking=True)
+            run_group(layer, grp, Wdd, xd[gi], yd)
+            for i in grp:
+                yh[i].copy_(yd[i], non_blocking=True)
 
     for _ in range(3):
         step()
@@ -397,11 +434,15 @@ def _oracle_layer_sample(row_div: int):
     rows of each matrix (a bounded sample of the same workload)."""
     import synth
     mats = []
-    for i, (nm, name, rows, cols) in enumerate(synth.LLAMA7B_LAYER):
-        r = max(1, rows // row_div)
-        W = synth.random_blocks(name, r, cols, 300 + i)
-        x = synth.activations(1, cols, 400 + i)
-        mats.append((synth.TYPE_IDS[name], W, r, cols, x, r * synth.row_bytes(name, cols) + 4 * cols + 4 * r))
+    for gi, grp in enumerate(synth.LLAMA7B_LAYER_GROUPS):
+        cols = synth.LLAMA7B_LAYER[grp[0]][3]
+        x = synth.activations(1, cols, 400 + gi)          # one activation vector per launch group
+        for k, i in enumerate(grp):
+            (nm, name, rows, _) = synth.LLAMA7B_LAYER[i]
+            r = max(1, rows // row_div)
+            W = synth.random_blocks(name, r, cols, 300 + i)
+            mats.append((synth.TYPE_IDS[name], W, r, cols, x,
+                         r * synth.row_bytes(name, cols) + 4 * r + (4 * cols if k == 0 else 0)))
     return mats
 
 
@@ -468,11 +509,22 @@ def main():
     ap.add_argument("--impl", default="qk", choices=["qk", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-gemm", action="store_true", help="skip the prefill GEMM leg")
+    ap.add_argument("--gemm-only", action="store_true",
+                    help="run only the prefill GEMM leg and print its JSON (for profiling)")
+    ap.add_argument("--min-warmup-s", type=float, default=1.0,
+                    help="keep replaying warm-up steps for at least this long (clocks settle)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.gemm_only:
+        import torch
+        from gguf_quant_dequant_gb300 import build as qkbuild
+        qkbuild.build()
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps(run_gemm_bench(dev, reps=args.steps)))
     else:
         run_gpu(args)
 

@@ -242,6 +242,8 @@ qk_status qk_gemm(int type, const void* W, int64_t rows, int64_t cols, const voi
     if (!aligned(X_bf16, 16)) return fail(QK_ERR_ALIGN, "X is not 16-byte aligned");
     if (rows > (int64_t)1 << 31 || M > (int64_t)1 << 31 || cols > (int64_t)1 << 31)
         return fail(QK_ERR_SHAPE, "qk_gemm: dimensions must be below 2^31");
+    if ((rows + 127) / 128 > 65535)
+        return fail(QK_ERR_SHAPE, "qk_gemm: rows=%lld above 65535 tiles of 128", (long long)rows);
     unsigned* status = nullptr;
     st = device_state(&status, nullptr);
     if (st != QK_OK) return st;

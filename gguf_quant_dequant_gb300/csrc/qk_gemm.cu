@@ -347,8 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t row0 = (int64_t)blockIdx.x * kBM;
-    const int64_t tok0 = (int64_t)blockIdx.y * kBN;
+    // Token tiles vary fastest: the CTAs that share a weight tile run
+    // together, so each packed weight byte comes from DRAM once.
+    const int64_t row0 = (int64_t)blockIdx.y * kBM;
+    const int64_t tok0 = (int64_t)blockIdx.x * kBN;
     const int nacc = p.M - tok0 > kBNM ? 2 : 1;   // accumulators holding real tokens
 
     if (threadIdx.x == 0) {
@@ -531,7 +533,7 @@ static cudaError_t gemm_t(const gm::Args& a, const CUtensorMap& map, cudaStream_
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, gm::Pk<T>::SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((a.rows + gm::kBM - 1) / gm::kBM), (unsigned)((a.M + gm::kBN - 1) / gm::kBN));
+    cfg.gridDim = dim3((unsigned)((a.M + gm::kBN - 1) / gm::kBN), (unsigned)((a.rows + gm::kBM - 1) / gm::kBM));
     cfg.blockDim = dim3(gm::kThreads);
     cfg.dynamicSmemBytes = gm::Pk<T>::SMEM;
     cfg.stream = s;

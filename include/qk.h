@@ -186,7 +186,8 @@ size_t qk_gemm_workspace(int type, int64_t rows, int64_t cols, int64_t M);
  * Accuracy: |Y - Y_exact(bf16 X)| <= 5e-3 * sum_k |w x|; the weights are
  * rounded to bf16 before the product (Q8_0, Q5_0 and Q6_K codes and most
  * Q4_K weights are exact in bf16 up to the block scale).
- * M == 0 or rows == 0 queues nothing; cols == 0 zero-fills Y. */
+ * M == 0 or rows == 0 queues nothing; cols == 0 zero-fills Y.  rows above
+ * 65535 * 128 = 8,388,480 is QK_ERR_SHAPE. */
 qk_status qk_gemm(int type, const void* W, int64_t rows, int64_t cols,
                   const void* X_bf16, int64_t M, float* Y,
                   void* ws, size_t ws_bytes, void* stream);

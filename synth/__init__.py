@@ -116,6 +116,11 @@ LLAMA7B_LAYER = [
 ]
 
 
+# The layer's matrices grouped by the activation vector they read: q/k/v
+# project the same hidden state, gate/up the same one (one launch each).
+LLAMA7B_LAYER_GROUPS = [(0, 1, 2), (3,), (4, 5), (6,)]
+
+
 def llama7b_stack(n_layers: int = 32):
     """32 decoder layers + lm_head 32000 x 4096 Q6_K + two 4096^2 Q8_0 tensors."""
     out = []

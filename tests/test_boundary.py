@@ -105,6 +105,12 @@ def test_batch_argument_errors_are_caught_on_host(lib):
     assert call(qk.Q4_K, 2, [None, None], [0, 0], 256, None, [None, None]) == 0
 
 
+def test_gemm_row_tile_limit_is_checked_on_host(lib):
+    fake = ctypes.c_void_p(0x10000)
+    assert lib.qk_gemm(qk.Q4_K, fake, 65535 * 128 + 1, 256, fake, 4, fake, None, 0, None) == 2
+    assert b"65535" in lib.qk_last_error()
+
+
 def test_empty_problems_queue_nothing(lib):
     fake = ctypes.c_void_p(0x10000)
     # rows == 0 or M == 0: success without touching the device.

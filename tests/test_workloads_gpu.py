@@ -95,3 +95,23 @@ def test_decode_large_rows_several_reduction_chunks(gpu):
     y_ref, S = oracle.entries(t, Wrows, ends.size, cols, np.zeros(ends.size, dtype=np.int64),
                               np.arange(ends.size), x=xd.cpu().numpy())
     assert_gemv_close(y[0, ends], y_ref, S, what="chunk edges")
+
+
+def test_llama7b_layer_in_bench_launch_configuration(gpu):
+    # The bench's step: q/k/v in one batched launch, o alone, gate/up batched,
+    # down alone; one activation vector per launch; every output checked.
+    import bench
+    layer, groups = synth.LLAMA7B_LAYER, synth.LLAMA7B_LAYER_GROUPS
+    Wh = [synth.random_blocks(name, rows, cols, 7300 + i) for i, (_, name, rows, cols) in enumerate(layer)]
+    xh = [synth.activations(1, layer[g[0]][3], 7400 + gi) for gi, g in enumerate(groups)]
+    Wd = [dev_u8(W, gpu) for W in Wh]
+    xd = [dev_f32(x, gpu)[0] for x in xh]
+    ys = [torch.empty(rows, device=gpu) for (_, _, rows, _) in layer]
+    for gi, grp in enumerate(groups):
+        bench.run_group(layer, grp, Wd, xd[gi], ys)
+    qk.device_status()
+    for gi, grp in enumerate(groups):
+        for i in grp:
+            (nm, name, rows, cols) = layer[i]
+            y_ref, S = oracle.gemv(type_id(name), Wh[i], rows, cols, xh[gi])
+            assert_gemv_close(ys[i].cpu().numpy()[None, :], y_ref, S, what=f"bench layer {nm}")
