@@ -44,6 +44,7 @@ SIGNATURES = {
     "qk_gemm": (_int, [_int, _p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
     "qk_unpack": (_int, [_int, _p, _i64, _p, _p, _p, _p, _p, _p]),
     "qk_device_status": (_int, [_p]),
+    "qk_test_stalled_wait": (_int, [ctypes.c_uint32, _p]),
     "qk_last_error": (ctypes.c_char_p, []),
 }
 
@@ -186,6 +187,11 @@ def unpack(t: int, W, nblocks: int, stream=None):
     _check(load().qk_unpack(t, _ptr(W), nblocks, _ptr(codes), _ptr(sc), _ptr(mins), _ptr(d), _ptr(dmin),
                             _stream(stream)), "qk_unpack")
     return codes, sc, mins, d, dmin
+
+
+def test_stalled_wait(limit_us: int, stream=None) -> None:
+    """qk_test_stalled_wait: a bounded wait on a barrier nothing arrives on."""
+    _check(load().qk_test_stalled_wait(limit_us, _stream(stream)), "qk_test_stalled_wait")
 
 
 def device_status(stream=None) -> None:

@@ -266,6 +266,17 @@ qk_status qk_unpack(int type, const void* W, int64_t nblocks, int16_t* codes, in
     return QK_OK;
 }
 
+qk_status qk_test_stalled_wait(uint32_t limit_us, void* stream) {
+    if (limit_us < 1 || limit_us > 10000000u) return fail(QK_ERR_ARG, "limit_us=%u outside 1..10000000", limit_us);
+    unsigned* status = nullptr;
+    qk_status st = device_state(&status, nullptr);
+    if (st != QK_OK) return st;
+    cudaError_t e = qk::launch_stalled_wait(status, (uint64_t)limit_us * 1000u, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "qk_test_stalled_wait launch");
+    g_last_error.clear();
+    return QK_OK;
+}
+
 qk_status qk_device_status(void* stream) {
     unsigned* status = nullptr;
     qk_status st = device_state(&status, nullptr);

@@ -36,6 +36,9 @@ cudaError_t launch_gemv5(int type, int n, const uint8_t* const* W, const int64_t
 cudaError_t launch_gemv(int type, const GemvPlan& plan, const uint8_t* W, int64_t rows, int64_t cols,
                         const float* x, int64_t M, float* y, float* ws, unsigned* status, cudaStream_t s);
 
+// One thread waiting on an mbarrier nothing arrives on (bounded by limit_ns).
+cudaError_t launch_stalled_wait(unsigned* status, uint64_t limit_ns, cudaStream_t s);
+
 // Tensor-core dequant-GEMM (bf16 activations, fp32 output); no workspace.
 cudaError_t launch_gemm(int type, const uint8_t* W, int64_t rows, int64_t cols, const void* X, int64_t M, float* Y,
                         unsigned* status, cudaStream_t s);

@@ -12,7 +12,7 @@ enum : unsigned { STATUS_TIMEOUT = 1u };
 // Spin budget of one bounded mbarrier wait.  try_wait already suspends the
 // thread for a hardware-chosen interval per attempt, so this bound is far
 // beyond any legitimate wait (a bulk copy completes in microseconds).
-constexpr uint32_t kWaitSpins = 1u << 24;
+constexpr uint32_t kWaitSpins = 1u << 30;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -52,11 +52,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Nanoseconds of the GPU's global timer.
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// A wait gives up after this long (time, checked every 256 polls) or after
+// kWaitSpins polls, whichever comes first.
+constexpr uint64_t kWaitNs = 2000000000ull;
+
 // Bounded wait for phase `parity` of `bar` to complete.  Returns false when
 // the budget runs out, after setting STATUS_TIMEOUT in *status.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned* status) {
-    for (uint32_t i = 0; i < kWaitSpins; ++i)
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned* status,
+                                                  uint64_t limit_ns = kWaitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1; i < kWaitSpins; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) break;
+    }
     atomicOr(status, STATUS_TIMEOUT);
     return false;
 }
@@ -76,10 +92,14 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
     return ok != 0;
 }
 
-// Bounded wait with suspension between checks (total bound about 2 s).
+// Bounded wait with suspension between checks (same time bound).
 __device__ __forceinline__ bool mbar_wait_sleep_bounded(uint64_t* bar, uint32_t parity, unsigned* status) {
-    for (uint32_t i = 0; i < (1u << 21); ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0; i < (1u << 24); ++i) {
         if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
+        if (globaltimer_ns() - t0 > kWaitNs) break;
+    }
     atomicOr(status, STATUS_TIMEOUT);
     return false;
 }

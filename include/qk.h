@@ -203,6 +203,16 @@ qk_status qk_gemm(int type, const void* W, int64_t rows, int64_t cols,
 qk_status qk_unpack(int type, const void* W, int64_t nblocks, int16_t* codes,
                     int16_t* sc, uint8_t* mins, float* d, float* dmin, void* stream);
 
+/* Diagnostic of the failure-detection path; the pages have no counterpart.
+ * Every mbarrier wait inside the library's kernels is bounded (2 s): when it
+ * runs out the kernel records a timeout in the device status word, drains
+ * its copies in flight, releases its tensor memory and returns, so the
+ * context stays usable.  This call queues one thread that waits, through
+ * the same bounded wait, on a barrier nothing arrives on, with the limit
+ * shortened to limit_us microseconds (1 .. 10,000,000; else QK_ERR_ARG).
+ * Afterwards qk_device_status() reports QK_ERR_TIMEOUT (and clears it). */
+qk_status qk_test_stalled_wait(uint32_t limit_us, void* stream);
+
 /* Synchronize `stream`, then read and clear this device's kernel status
  * word: QK_OK, or QK_ERR_TIMEOUT when a bounded wait ran out since the last
  * call (the affected outputs are then invalid). */
