@@ -218,34 +218,40 @@ def run_gpu(args):
             run_group(layer, groups[gi], Ws[c], xs[gi], ys)
 
     # Warm the kernels up eagerly once (module load, attributes), then capture
-    # one CUDA graph per layer copy.
+    # the steps of all layer copies back to back in one CUDA graph (as a
+    # model's forward pass over consecutive layers is captured), plus one
+    # graph per copy for a remainder of steps.
     for c in range(ncopies):
         step(c)
     torch.cuda.synchronize()
-    graphs = []
-    for c in range(ncopies):
+
+    def capture(fn):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            step(c)
-        graphs.append(g)
+            fn()
+        return g
+
     q4_groups = [gi for gi, grp in enumerate(groups) if layer[grp[0]][1] == "Q4_K"]
-    q4_graphs = []
-    for c in range(ncopies):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            sub_step(c, q4_groups)
-        q4_graphs.append(g)
+    g_all = capture(lambda: [step(c) for c in range(ncopies)])
+    graphs = [capture(lambda c=c: step(c)) for c in range(ncopies)]
+    q4_all = capture(lambda: [sub_step(c, q4_groups) for c in range(ncopies)])
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
+
+    def run_steps(n, whole, single):
+        for _ in range(n // ncopies):
+            whole.replay()
+        for k in range(n % ncopies):
+            single[k].replay()
 
     K, W = args.steps, args.warmup
     with Clocks(local) as clk:
         t_end = time.time() + args.min_warmup_s
         i = 0
         while i < W or time.time() < t_end:
-            graphs[i % ncopies].replay()
-            i += 1
-            if i % 64 == 0:
+            g_all.replay()
+            i += ncopies
+            if i % (16 * ncopies) == 0:
                 torch.cuda.synchronize()
         torch.cuda.synchronize()
         _barrier(world)
@@ -253,8 +259,7 @@ def run_gpu(args):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for k in range(K):
-            graphs[k % ncopies].replay()
+        run_steps(K, g_all, graphs)
         e1.record(stream)
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1)
@@ -262,12 +267,12 @@ def run_gpu(args):
         torch.cuda.synchronize()
         # Dominant kernel alone: the three Q4_K launches of a layer (q/k/v,
         # o, gate/up), same rotation.
-        reps = max(K, 200)
+        reps = max(K // ncopies, 40)
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
         f0.record(stream)
-        for k in range(reps):
-            q4_graphs[k % ncopies].replay()
+        for _ in range(reps):
+            q4_all.replay()
         f1.record(stream)
         torch.cuda.synchronize()
         q4_ms = f0.elapsed_time(f1)
@@ -277,11 +282,11 @@ def run_gpu(args):
     value = world * lb / (ms_step * 1e-3) / 1e9
 
     q4_launch_bytes = sum(group_bytes(layer, groups[gi]) for gi in q4_groups) / len(q4_groups)
-    q4_launch_ms = q4_ms / (reps * len(q4_groups))
+    q4_launch_ms = q4_ms / (reps * ncopies * len(q4_groups))
     achieved = q4_launch_bytes / (q4_launch_ms * 1e-3) / 1e9
 
     e2e = run_e2e(args, dev, layer, groups, Ws[0], xs, lb) if rank == 0 else None
-    del Ws, graphs, q4_graphs
+    del Ws, graphs, g_all, q4_all
     torch.cuda.empty_cache()
     gemm = None
     if rank == 0 and not args.no_gemm:
@@ -309,7 +314,8 @@ def run_gpu(args):
                        "l2": f"inputs larger than L2: {ncopies} distinct layer copies "
                              f"({ncopies * wbytes / 2**20:.0f} MiB) rotated per step",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "timing": "CUDA graph per layer copy, CUDA events on the launch stream"},
+                       "timing": f"one CUDA graph of {ncopies} consecutive layer steps (one per copy), "
+                                 "replayed; CUDA events on the launch stream"},
             "frac_of_peak": round(value / world / hbm_peak, 4),
             "roofline": {"bound": "hbm", "kernel": "gemv5_kernel<Q4_K> (decode; q/k/v, o and gate/up launches)",
                          "achieved": round(achieved, 2), "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s",
