@@ -288,6 +288,8 @@ def run_gpu(args):
     e2e = run_e2e(args, dev, layer, groups, Ws[0], xs, lb) if rank == 0 else None
     del Ws, graphs, g_all, q4_all
     torch.cuda.empty_cache()
+    stack = run_stack(dev) if (rank == 0 and not args.no_stack) else None
+    sweep = run_ffn_sweep(dev) if (rank == 0 and not args.no_sweep) else None
     gemm = None
     if rank == 0 and not args.no_gemm:
         gemm = run_gemm_bench(dev)
@@ -326,6 +328,8 @@ def run_gpu(args):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gemm": gemm,
+            "stack": stack,
+            "ffn_sweep": sweep,
         }
         print(json.dumps(out))
     if world > 1:
@@ -393,6 +397,128 @@ def run_gemm_bench(dev, reps: int = 5):
             "tflops": round(tot_flop / (tot_ms * 1e-3) / 1e12, 1), "per_matrix_tflops": per,
             "comparator_dequant_then_cublas_tflops": round(cmp_flop / (cmp_ms * 1e-3) / 1e12, 1),
             "comparator_note": "qk_dequant to bf16 then torch.matmul, same 9 matrices (vocab excluded)"}
+
+
+def _graph_time_us(fn, reps: int = 20, warm: int = 3) -> float:
+    """Median over reps of one replay of a CUDA graph of fn, in microseconds."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    for _ in range(warm):
+        g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    del g
+    return statistics.median(ts)
+
+
+def run_stack(dev):
+    """The full Llama-7B-shaped stack at decode batch 1 (32 layers in the
+    bench's four launches each, lm_head 32000x4096 Q6_K, two 4096^2 Q8_0):
+    one token = one pass over 3.87 GiB of packed weights, captured in one
+    CUDA graph.  Reports tokens/s-equivalent and GB/s."""
+    import torch
+    import gguf_quant_dequant_gb300 as qk
+    import synth
+    layer, groups = synth.LLAMA7B_LAYER, synth.LLAMA7B_LAYER_GROUPS
+    g = torch.Generator(device=dev)
+    g.manual_seed(5151)
+    L = 32
+    Ws = [[synth.random_blocks_torch(name, rows, cols, 6000 + 10 * l + i, dev)
+           for i, (_, name, rows, cols) in enumerate(layer)] for l in range(L)]
+    tail = [("Q6_K", 32000, 4096), ("Q8_0", 4096, 4096), ("Q8_0", 4096, 4096)]
+    Wt = [synth.random_blocks_torch(n, r, c, 6900 + i, dev) for i, (n, r, c) in enumerate(tail)]
+    xs = [torch.randn(layer[grp[0]][3], device=dev, generator=g) for grp in groups]
+    x4 = torch.randn(4096, device=dev, generator=g)
+    ys = [torch.empty(rows, device=dev) for (_, _, rows, _) in layer]
+    yt = [torch.empty(r, device=dev) for (_, r, _) in tail]
+    nbytes = sum(w.numel() for ws_ in Ws for w in ws_) + sum(w.numel() for w in Wt)
+
+    def token():
+        for l in range(L):
+            for gi, grp in enumerate(groups):
+                run_group(layer, grp, Ws[l], xs[gi], ys)
+        for i, (n, r, c) in enumerate(tail):
+            qk.gemv(synth.TYPE_IDS[n], Wt[i], r, c, x4.view(1, c), y=yt[i].view(1, r))
+
+    us = _graph_time_us(token, reps=20)
+    launches = L * len(groups) + len(tail)
+    del Ws, Wt
+    torch.cuda.empty_cache()
+    return {"workload": "Llama-7B-shaped stack, decode batch 1: 32 layers + lm_head 32000x4096 Q6_K + 2 x 4096^2 Q8_0",
+            "weight_bytes": int(nbytes), "us_per_token": round(us, 1),
+            "tokens_per_s_equiv": round(1e6 / us, 1), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+            "launches_per_token": launches, "timing": "one CUDA graph per token, median of 20 replays"}
+
+
+def run_ffn_sweep(dev):
+    """Llama-3-8B FFN (gate/up 14336x4096, down 4096x14336) in Q4_K and Q5_0,
+    activation batches M in {1, 4, 16, 64}: the fused GEMV (qk_gemv; M = 1
+    with gate/up as one qk_gemv_batch) against the tensor-core GEMM (qk_gemm,
+    bf16 activations), per M.  Three copies of the weights rotate (beyond
+    L2).  GB/s counts packed weights + x + y; TFLOP/s = 2*M*N*K / time."""
+    import torch
+    import gguf_quant_dequant_gb300 as qk
+    import synth
+    out = {}
+    g = torch.Generator(device=dev)
+    g.manual_seed(5252)
+    for name in ("Q4_K", "Q5_0"):
+        t = synth.TYPE_IDS[name]
+        mats = synth.llama3_ffn(name)
+        ncop = 3
+        Ws = [[synth.random_blocks_torch(name, r, c, 7000 + 10 * k + i, dev) for i, (_, _, r, c) in enumerate(mats)]
+              for k in range(ncop)]
+        wbytes = sum(w.numel() for w in Ws[0])
+        flop1 = sum(2.0 * r * c for (_, _, r, c) in mats)
+        res = {}
+        for M in synth.FFN_BATCHES:
+            X = {c: torch.randn((M, c), device=dev, generator=g) for c in (4096, 14336)}
+            Xb = {c: v.to(torch.bfloat16) for c, v in X.items()}
+            Y = [torch.empty((M, r), device=dev) for (_, _, r, _) in mats]
+            ws = torch.empty(max(16, max(qk.gemv_workspace(t, r, c, M) for (_, _, r, c) in mats)),
+                             dtype=torch.uint8, device=dev)
+
+            def gemv_pass():
+                for k in range(ncop):
+                    if M == 1:
+                        qk.gemv_batch(t, Ws[k][0:2], [14336, 14336], 4096, X[4096][0], ys=[Y[0][0], Y[1][0]])
+                    else:
+                        for i in range(2):
+                            qk.gemv(t, Ws[k][i], 14336, 4096, X[4096], y=Y[i], ws=ws)
+                    qk.gemv(t, Ws[k][2], 4096, 14336, X[14336], y=Y[2], ws=ws)
+
+            def gemm_pass():
+                for k in range(ncop):
+                    for i, (_, _, r, c) in enumerate(mats):
+                        qk.gemm(t, Ws[k][i], r, c, Xb[c], Y=Y[i])
+
+            us_v = _graph_time_us(gemv_pass) / ncop
+            us_m = _graph_time_us(gemm_pass) / ncop
+            io = 4 * M * (4096 + 14336) + 4 * M * (2 * 14336 + 4096)
+            res[str(M)] = {"gemv_us": round(us_v, 2), "gemm_us": round(us_m, 2),
+                           "gemv_gbs": round((wbytes + io) / (us_v * 1e-6) / 1e9, 1),
+                           "gemm_gbs": round((wbytes + io) / (us_m * 1e-6) / 1e9, 1),
+                           "gemv_tflops": round(M * flop1 / (us_v * 1e-6) / 1e12, 2),
+                           "gemm_tflops": round(M * flop1 / (us_m * 1e-6) / 1e12, 2),
+                           "faster": "gemv" if us_v <= us_m else "gemm"}
+            del X, Xb, Y, ws
+        cross = next((int(M) for M, v in res.items() if v["faster"] == "gemm"), None)
+        out[name] = {"per_M": res, "weight_bytes": int(wbytes), "gemm_faster_from_M": cross}
+        del Ws
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, dev, layer, groups, Wd, xs, lb):
@@ -515,6 +641,8 @@ def main():
     ap.add_argument("--impl", default="qk", choices=["qk", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-gemm", action="store_true", help="skip the prefill GEMM leg")
+    ap.add_argument("--no-stack", action="store_true", help="skip the 32-layer stack leg")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the Llama-3 FFN batch sweep")
     ap.add_argument("--gemm-only", action="store_true",
                     help="run only the prefill GEMM leg and print its JSON (for profiling)")
     ap.add_argument("--min-warmup-s", type=float, default=1.0,
