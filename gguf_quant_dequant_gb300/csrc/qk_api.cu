@@ -219,13 +219,12 @@ qk_status qk_gemv_batch(int type, int n_mat, const void* const* W, const int64_t
 }
 
 size_t qk_gemm_workspace(int type, int64_t rows, int64_t cols, int64_t M) {
-    (void)type; (void)rows; (void)cols; (void)M;
-    return 0;
+    if (!known_type(type) || rows <= 0 || cols <= 0 || M <= 0 || cols % block_elems(type) != 0) return 0;
+    return (size_t)qk::plan_gemm(type, rows, cols, M, sm_count_or_default()).ws_bytes;
 }
 
 qk_status qk_gemm(int type, const void* W, int64_t rows, int64_t cols, const void* X_bf16, int64_t M, float* Y,
                   void* ws, size_t ws_bytes, void* stream) {
-    (void)ws; (void)ws_bytes;
     qk_status st = check_matrix(type, W, rows, cols);
     if (st != QK_OK) return st;
     if (M < 0) return fail(QK_ERR_SHAPE, "negative M=%lld", (long long)M);
@@ -245,9 +244,18 @@ qk_status qk_gemm(int type, const void* W, int64_t rows, int64_t cols, const voi
     if ((rows + 127) / 128 > 65535)
         return fail(QK_ERR_SHAPE, "qk_gemm: rows=%lld above 65535 tiles of 128", (long long)rows);
     unsigned* status = nullptr;
-    st = device_state(&status, nullptr);
+    int sms = 0;
+    st = device_state(&status, &sms);
     if (st != QK_OK) return st;
-    cudaError_t e = qk::launch_gemm(type, static_cast<const uint8_t*>(W), rows, cols, X_bf16, M, Y, status, s);
+    const qk::GemmPlan pl = qk::plan_gemm(type, rows, cols, M, sms);
+    if (pl.ws_bytes > 0) {
+        if (ws_bytes < (size_t)pl.ws_bytes)
+            return fail(QK_ERR_WORKSPACE, "workspace %zu bytes < %lld needed", ws_bytes, (long long)pl.ws_bytes);
+        if (!ws) return fail(QK_ERR_NULL, "workspace is NULL");
+        if (!aligned(ws, 16)) return fail(QK_ERR_ALIGN, "workspace is not 16-byte aligned");
+    }
+    cudaError_t e = qk::launch_gemm(type, pl, static_cast<const uint8_t*>(W), rows, cols, X_bf16, M, Y,
+                                    static_cast<float*>(ws), status, s);
     if (e != cudaSuccess) return cuda_fail(e, "qk_gemm launch");
     g_last_error.clear();
     return QK_OK;

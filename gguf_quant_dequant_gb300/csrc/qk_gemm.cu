@@ -86,8 +86,11 @@ struct Args {
     const uint8_t* W;
     int64_t rows, cols, row_bytes, M, total16;
     float* Y;
+    float* part;          // split-K partials [splits][M][rows] (nullptr: write Y)
     unsigned* status;
-    int nkb;
+    int nkb;              // 64-wide k-blocks of K
+    int kb_per_split;     // k-blocks per split (a multiple of the macro-block's)
+    int nmma;             // MMA N (tokens per accumulator): 256, or M rounded up to 16 when M <= 256
 };
 
 // (unit, half) of the 16 weights that start `o` weights into a block.
@@ -352,6 +355,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int64_t row0 = (int64_t)blockIdx.y * kBM;
     const int64_t tok0 = (int64_t)blockIdx.x * kBN;
     const int nacc = p.M - tok0 > kBNM ? 2 : 1;   // accumulators holding real tokens
+    // This CTA's share of K: k-blocks [kb0, kb1) (blockIdx.z = split).
+    const int kb0 = (int)blockIdx.z * p.kb_per_split;
+    const int kb1 = min(p.nkb, kb0 + p.kb_per_split);
+    const int nk = kb1 - kb0;
+    const uint32_t bsub = (uint32_t)p.nmma * (kBK * 2);   // bytes of one accumulator's activation tile
+    float* out = p.part ? p.part + (size_t)blockIdx.z * (size_t)p.M * (size_t)p.rows : p.Y;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNS; ++s) {
@@ -378,26 +387,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         if (lane == 0) {
             pdl_wait_prior();
             int issued = 0;
-            for (int kb = 0; kb < p.nkb; ++kb) {
-                const int s = kb % kNS;
-                if (kb >= kNS && !mbar_wait_sleep_bounded(&empty[s], (uint32_t)((kb / kNS - 1) & 1), p.status)) break;
-                mbar_arrive_expect_tx(&full_x[s], (uint32_t)(kBsub * nacc));
+            for (int i = 0; i < nk; ++i) {   // local k-block i = k-block kb0 + i
+                const int s = i % kNS;
+                if (i >= kNS && !mbar_wait_sleep_bounded(&empty[s], (uint32_t)((i / kNS - 1) & 1), p.status)) break;
+                mbar_arrive_expect_tx(&full_x[s], bsub * (uint32_t)nacc);
                 for (int j = 0; j < nacc; ++j)
-                    tc::tma_load_2d(smem + s * kStage + kA + j * kBsub, &xmap, kb * kBK, (int)tok0 + kBNM * j,
+                    tc::tma_load_2d(smem + s * kStage + kA + j * kBsub, &xmap, (kb0 + i) * kBK, (int)tok0 + kBNM * j,
                                     &full_x[s]);
-                issued = kb + 1;
+                issued = i + 1;
             }
             // Every load issued must land before the CTA may exit.
-            for (int kb = issued > kNS ? issued - kNS : 0; kb < issued; ++kb)
-                mbar_wait_bounded(&full_x[kb % kNS], (uint32_t)((kb / kNS) & 1), p.status);
+            for (int i = issued > kNS ? issued - kNS : 0; i < issued; ++i)
+                mbar_wait_bounded(&full_x[i % kNS], (uint32_t)((i / kNS) & 1), p.status);
         }
     } else if (warp == 1) {
         // MMA issuer.
         if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBNM);
-            for (int kb = 0; kb < p.nkb; ++kb) {
-                const int s = kb % kNS;
-                const uint32_t par = (uint32_t)((kb / kNS) & 1);
+            const uint32_t idesc = tc::idesc_bf16_f32(kBM, p.nmma);
+            for (int i = 0; i < nk; ++i) {
+                const int s = i % kNS;
+                const uint32_t par = (uint32_t)((i / kNS) & 1);
                 if (!mbar_wait_sleep_bounded(&full_x[s], par, p.status) ||
                     !mbar_wait_sleep_bounded(&full_w[s], par, p.status))
                     break;
@@ -407,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         tc::mma_bf16(tmem + kBNM * j, tc::sdesc_k128(a + 32 * kk),
-                                     tc::sdesc_k128(b + kBsub * j + 32 * kk), idesc, (kb | kk) != 0 ? 1u : 0u);
+                                     tc::sdesc_k128(b + kBsub * j + 32 * kk), idesc, (i | kk) != 0 ? 1u : 0u);
                 }
                 tc::commit(&empty[s]);
             }
@@ -423,31 +432,36 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const int dw = warp - 2;
         const int r = 8 * dw + (lane >> 2), qq = lane & 3;
         const int64_t row = row0 + r;
-        const int64_t nmb = (p.cols + K::MB - 1) / K::MB;
+        // Macro-blocks m0 .. m0 + nmb - 1 cover this CTA's k-blocks (kb0 is a
+        // multiple of the macro-block's k-blocks).
+        const int64_t m0 = kb0 / K::KPM;
+        const int64_t nmb = (kb1 + K::KPM - 1) / K::KPM - m0;
         bool ok = true;
 #pragma unroll 1
-        for (int m = 0; m < kNSP - 1; ++m) {
-            if (m < nmb) issue_packed<T>(p, packed + m * K::STAGE, row0, m, r, qq);
+        for (int mi = 0; mi < kNSP - 1; ++mi) {
+            if (mi < nmb) issue_packed<T>(p, packed + mi * K::STAGE, row0, m0 + mi, r, qq);
             cp_async_commit();
         }
 #pragma unroll 1
-        for (int64_t m = 0; m < nmb; ++m) {
-            if (m + kNSP - 1 < nmb)
-                issue_packed<T>(p, packed + ((m + kNSP - 1) % kNSP) * K::STAGE, row0, m + kNSP - 1, r, qq);
+        for (int64_t mi = 0; mi < nmb; ++mi) {
+            const int64_t m = m0 + mi;
+            if (mi + kNSP - 1 < nmb)
+                issue_packed<T>(p, packed + ((mi + kNSP - 1) % kNSP) * K::STAGE, row0, m + kNSP - 1, r, qq);
             cp_async_commit();
             cp_async_wait<kNSP - 1>();
-            uint8_t* pk = packed + (m % kNSP) * K::STAGE;
+            uint8_t* pk = packed + (mi % kNSP) * K::STAGE;
             if (qq == 0 && row < p.rows) tail_fix<T>(p, pk + r * K::SLOT, row, m);
             __syncwarp();   // this warp's rows of macro-block m are visible
             const int64_t st = row * p.row_bytes + m * K::BYTES;
             const uint8_t* mbp = pk + r * K::SLOT + (int)(st & 15);
             for (int kk = 0; kk < K::KPM; ++kk) {
                 const int64_t kb = m * K::KPM + kk;
-                if (kb >= p.nkb) break;
-                const int s = (int)(kb % kNS);
-                if (ok && kb >= kNS) {   // one lane polls, the warp follows
+                if (kb >= kb1) break;
+                const int li = (int)(kb - kb0);   // local k-block
+                const int s = li % kNS;
+                if (ok && li >= kNS) {   // one lane polls, the warp follows
                     int good = 1;
-                    if (lane == 0) good = mbar_wait_bounded(&empty[s], (uint32_t)((kb / kNS - 1) & 1), p.status);
+                    if (lane == 0) good = mbar_wait_bounded(&empty[s], (uint32_t)((li / kNS - 1) & 1), p.status);
                     ok = __shfl_sync(0xffffffffu, good, 0) != 0;
                 }
                 if (ok) {
@@ -491,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int64_t tok = tok0 + col + i;
-                        if (tok < p.M) p.Y[tok * p.rows + orow] = __uint_as_float(v[i]);
+                        if (tok < p.M) out[tok * p.rows + orow] = __uint_as_float(v[i]);
                     }
                 }
             }
@@ -502,6 +516,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (warp == 1) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Y = sum over splits of the partials, in split order (deterministic).
+__global__ void __launch_bounds__(256) reduce_splits_kernel(const float* __restrict__ part, int splits, int64_t n,
+                                                           float* __restrict__ Y) {
+    pdl_wait_prior();
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        float a = part[i];
+        for (int s = 1; s < splits; ++s) a += part[(int64_t)s * n + i];
+        Y[i] = a;
     }
 }
 
@@ -527,13 +552,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 template <int T>
-static cudaError_t gemm_t(const gm::Args& a, const CUtensorMap& map, cudaStream_t s) {
+static cudaError_t gemm_t(const gm::Args& a, const GemmPlan& pl, const CUtensorMap& map, cudaStream_t s) {
     static_assert(gm::Pk<T>::SMEM <= 227 * 1024, "shared memory per CTA");
     auto kern = gm::gemm_kernel<T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, gm::Pk<T>::SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((a.M + gm::kBN - 1) / gm::kBN), (unsigned)((a.rows + gm::kBM - 1) / gm::kBM));
+    cfg.gridDim = dim3((unsigned)((a.M + gm::kBN - 1) / gm::kBN), (unsigned)((a.rows + gm::kBM - 1) / gm::kBM),
+                       (unsigned)pl.splits);
     cfg.blockDim = dim3(gm::kThreads);
     cfg.dynamicSmemBytes = gm::Pk<T>::SMEM;
     cfg.stream = s;
@@ -545,28 +571,66 @@ static cudaError_t gemm_t(const gm::Args& a, const CUtensorMap& map, cudaStream_
     return cudaLaunchKernelEx(&cfg, kern, map, a);
 }
 
-cudaError_t launch_gemm(int type, const uint8_t* W, int64_t rows, int64_t cols, const void* X, int64_t M, float* Y,
-                        unsigned* status, cudaStream_t s) {
+namespace {
+int k_blocks_per_macro(int type) { return type == T_Q8_0 ? 2 : 4; }   // Pk<T>::KPM
+}  // namespace
+
+// Split K when the (token, row) tiles leave SMs idle: among 1..16 splits
+// (on macro-block boundaries) take the fewest waves x k-blocks per CTA, with
+// a fixed cost of ~6 k-blocks per CTA for its prologue and epilogue.  Only a
+// single token tile is split (the partials, splits x M x rows floats, are
+// small there), and only for a gain of at least 15 %.
+GemmPlan plan_gemm(int type, int64_t rows, int64_t cols, int64_t M, int sms) {
+    GemmPlan pl;
+    if (rows <= 0 || cols <= 0 || M <= 0) return pl;
+    const int64_t nkb = (cols + gm::kBK - 1) / gm::kBK;
+    const int64_t kpm = k_blocks_per_macro(type);
+    pl.nmma = M > gm::kBNM ? gm::kBNM : (int)std::max<int64_t>(16, (M + 15) / 16 * 16);
+    const int64_t tiles = ((M + gm::kBN - 1) / gm::kBN) * ((rows + gm::kBM - 1) / gm::kBM);
+    const int64_t S = std::max(sms, 1);
+    int64_t best_cost = -1;
+    const int64_t max_split = M <= gm::kBN ? 16 : 1;
+    for (int64_t sp = 1; sp <= max_split; ++sp) {
+        const int64_t kps = ((nkb + sp - 1) / sp + kpm - 1) / kpm * kpm;
+        const int64_t se = (nkb + kps - 1) / kps;
+        if (se != sp && sp > 1) continue;
+        const int64_t waves = (tiles * se + S - 1) / S;
+        const int64_t cost = waves * (kps + 6) * (se > 1 ? 20 : 17);   // splitting must win by 15 %
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            pl.splits = (int)se;
+            pl.kb_per_split = (int)kps;
+        }
+    }
+    pl.ws_bytes = pl.splits > 1 ? (int64_t)pl.splits * M * rows * (int64_t)sizeof(float) : 0;
+    return pl;
+}
+
+cudaError_t launch_gemm(int type, const GemmPlan& pl, const uint8_t* W, int64_t rows, int64_t cols, const void* X,
+                        int64_t M, float* Y, float* ws, unsigned* status, cudaStream_t s) {
     auto encode = encode_fn();
     if (!encode) return cudaErrorNotSupported;
-    // X: bf16 [M, cols] row-major; tiles of 64 (k) x 256 (tokens), 128-byte swizzle.
+    // X: bf16 [M, cols] row-major; tiles of 64 (k) x nmma (tokens), 128-byte swizzle.
     CUtensorMap map;
     cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)M};
     cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {(cuuint32_t)gm::kBK, (cuuint32_t)gm::kBNM};
+    cuuint32_t box[2] = {(cuuint32_t)gm::kBK, (cuuint32_t)pl.nmma};
     cuuint32_t estride[2] = {1, 1};
     CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), gdim, gstride, box, estride,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    gm::Args a;
+    gm::Args a = {};
     a.W = W;
     a.rows = rows;
     a.cols = cols;
     a.M = M;
     a.Y = Y;
+    a.part = pl.splits > 1 ? ws : nullptr;
     a.status = status;
     a.nkb = (int)((cols + gm::kBK - 1) / gm::kBK);
+    a.kb_per_split = pl.kb_per_split > 0 ? pl.kb_per_split : a.nkb;
+    a.nmma = pl.nmma;
     switch (type) {
     case T_Q4_K: a.row_bytes = cols / 256 * 144; break;
     case T_Q6_K: a.row_bytes = cols / 256 * 210; break;
@@ -575,13 +639,26 @@ cudaError_t launch_gemm(int type, const uint8_t* W, int64_t rows, int64_t cols, 
     default: return cudaErrorInvalidValue;
     }
     a.total16 = (rows * a.row_bytes) & ~(int64_t)15;
+    cudaError_t e = cudaErrorInvalidValue;
     switch (type) {
-    case T_Q4_K: return gemm_t<T_Q4_K>(a, map, s);
-    case T_Q6_K: return gemm_t<T_Q6_K>(a, map, s);
-    case T_Q8_0: return gemm_t<T_Q8_0>(a, map, s);
-    case T_Q5_0: return gemm_t<T_Q5_0>(a, map, s);
+    case T_Q4_K: e = gemm_t<T_Q4_K>(a, pl, map, s); break;
+    case T_Q6_K: e = gemm_t<T_Q6_K>(a, pl, map, s); break;
+    case T_Q8_0: e = gemm_t<T_Q8_0>(a, pl, map, s); break;
+    case T_Q5_0: e = gemm_t<T_Q5_0>(a, pl, map, s); break;
     }
-    return cudaErrorInvalidValue;
+    if (e != cudaSuccess || pl.splits <= 1) return e;
+    // Add the partials in split order.
+    const int64_t n = M * rows;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)std::min<int64_t>((n + 255) / 256, 4096));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gm::reduce_splits_kernel, (const float*)ws, pl.splits, n, Y);
 }
 
 }  // namespace qk

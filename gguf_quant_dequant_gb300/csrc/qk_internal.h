@@ -39,8 +39,16 @@ cudaError_t launch_gemv(int type, const GemvPlan& plan, const uint8_t* W, int64_
 // One thread waiting on an mbarrier nothing arrives on (bounded by limit_ns).
 cudaError_t launch_stalled_wait(unsigned* status, uint64_t limit_ns, cudaStream_t s);
 
-// Tensor-core dequant-GEMM (bf16 activations, fp32 output); no workspace.
-cudaError_t launch_gemm(int type, const uint8_t* W, int64_t rows, int64_t cols, const void* X, int64_t M, float* Y,
-                        unsigned* status, cudaStream_t s);
+// Tensor-core dequant-GEMM (bf16 activations, fp32 output).  Small problems
+// split K over CTAs; the partials [splits, M, rows] live in the workspace.
+struct GemmPlan {
+    int splits = 1;
+    int kb_per_split = 0;   // 64-wide k-blocks per split
+    int nmma = 256;         // MMA N
+    int64_t ws_bytes = 0;
+};
+GemmPlan plan_gemm(int type, int64_t rows, int64_t cols, int64_t M, int sm_count);
+cudaError_t launch_gemm(int type, const GemmPlan& plan, const uint8_t* W, int64_t rows, int64_t cols, const void* X,
+                        int64_t M, float* Y, float* ws, unsigned* status, cudaStream_t s);
 
 }  // namespace qk

@@ -71,3 +71,39 @@ def test_gemm_empty_and_zero_k(gpu):
     qk.gemm(t, torch.zeros(144, dtype=torch.uint8, device=gpu), 0, 256,
             torch.zeros((4, 256), dtype=torch.bfloat16, device=gpu), Y=torch.empty((4, 0), device=gpu))
     qk.device_status()
+
+
+# Small token batches against long K: the plan splits K over CTAs (partials
+# in the workspace, added in split order) and narrows the MMA to M rounded up
+# to 16.
+SPLIT_CASES = [
+    ("Q4_K", 256, 8192, 4),
+    ("Q6_K", 100, 14336, 16),
+    ("Q8_0", 384, 4096, 64),
+    ("Q5_0", 96, 5120, 9),
+    ("Q4_K", 130, 2048, 1),
+]
+
+
+@pytest.mark.parametrize("name,rows,cols,M", SPLIT_CASES)
+def test_gemm_split_k_parity(gpu, name, rows, cols, M):
+    t = type_id(name)
+    assert qk.gemm_workspace(t, rows, cols, M) > 0          # the split path is taken
+    Y, Y_ref, S = run_gemm(gpu, name, rows, cols, M, 3500 + rows + M)
+    assert_gemv_close(Y, Y_ref, S, rtol=GEMM_RTOL, atol=0.0, what=f"split gemm {name} {rows}x{cols} M={M}")
+
+
+def test_gemm_split_k_is_deterministic_and_checks_workspace(gpu):
+    name, rows, cols, M = "Q4_K", 256, 8192, 8
+    t = type_id(name)
+    W = dev_u8(synth.random_blocks(name, rows, cols, 3600), gpu)
+    Xb = synth.activations_bf16_bits(M, cols, 3601)
+    Xd = torch.from_numpy(Xb.view(np.int16)).to(gpu).view(torch.bfloat16)
+    a = qk.gemm(t, W, rows, cols, Xd).cpu().numpy()
+    b = qk.gemm(t, W, rows, cols, Xd).cpu().numpy()
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    need = qk.gemm_workspace(t, rows, cols, M)
+    small = torch.empty(need - 16, dtype=torch.uint8, device=gpu)
+    with pytest.raises(qk.QKError) as e:
+        qk.gemm(t, W, rows, cols, Xd, ws=small)
+    assert e.value.status == 5
