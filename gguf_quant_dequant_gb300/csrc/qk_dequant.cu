@@ -98,6 +98,7 @@ cudaError_t launch_dequant(int type, const uint8_t* W, int64_t rows, int64_t col
     case T_Q6_K: return dequant_t<T_Q6_K>(W, rows, cols, out, out_bf16, s);
     case T_Q8_0: return dequant_t<T_Q8_0>(W, rows, cols, out, out_bf16, s);
     case T_Q5_0: return dequant_t<T_Q5_0>(W, rows, cols, out, out_bf16, s);
+    case T_Q4_0: return dequant_t<T_Q4_0>(W, rows, cols, out, out_bf16, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -111,6 +112,7 @@ cudaError_t launch_unpack(int type, const uint8_t* W, int64_t nblocks, int16_t* 
     case T_Q6_K: unpack_kernel<T_Q6_K><<<grid, 256, 0, s>>>(W, nblocks, codes, sc, mins, d, dmin); break;
     case T_Q8_0: unpack_kernel<T_Q8_0><<<grid, 256, 0, s>>>(W, nblocks, codes, sc, mins, d, dmin); break;
     case T_Q5_0: unpack_kernel<T_Q5_0><<<grid, 256, 0, s>>>(W, nblocks, codes, sc, mins, d, dmin); break;
+    case T_Q4_0: unpack_kernel<T_Q4_0><<<grid, 256, 0, s>>>(W, nblocks, codes, sc, mins, d, dmin); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -11,6 +11,7 @@
 //   Q6_K  w = (d*sc)*(q - 32)
 //   Q8_0  w = d*q                      ("Hitchhiker's Guide", 11.1)
 //   Q5_0  w = d*(q - 16)
+//   Q4_0  w = d*(q - 8)                ("Hitchhiker's Guide", 11.1 figure)
 // Each product before the last rounding is exact in fp32 (an fp16 d has 11
 // significant bits, a scale at most 8, a code at most 8), so the weights are
 // bit-identical to the formula evaluated in fp32 whatever the contraction.
@@ -21,7 +22,7 @@
 
 namespace qk {
 
-enum : int { T_Q4_K = 1, T_Q6_K = 2, T_Q8_0 = 3, T_Q5_0 = 4 };
+enum : int { T_Q4_K = 1, T_Q6_K = 2, T_Q8_0 = 3, T_Q5_0 = 4, T_Q4_0 = 5 };
 
 // 16-bit and 32-bit little-endian loads from a 2-byte-aligned address that
 // never touch a byte outside [p, p + size).
@@ -153,6 +154,24 @@ template <> struct Fmt<T_Q5_0> {
 #pragma unroll
         for (int i = 0; i < 16; ++i)
             c[i] = (int)(((byte_of(q, i) >> (4 * h)) & 15u) | (((qh >> i) & 1u) << 4));
+    }
+    __device__ static __forceinline__ void params(const uint8_t* blk, int, int, float& A, float& B) {
+        A = h2f(ld_u16(blk));
+        B = 0.0f;
+    }
+};
+
+// ---------------------------------------------------------------- Q4_0 --
+// Bytes 0-1 d, 2-17 qs.  Element j < 16: low nibble of qs[j]; element j + 16:
+// high nibble of qs[j].  w = d*(q - 8).
+template <> struct Fmt<T_Q4_0> {
+    static constexpr int BB = 18, BE = 32, UPB = 1, OFF = 8;
+    __device__ static __forceinline__ int koff(int, int h) { return 16 * h; }
+    __device__ static __forceinline__ void codes16(const uint8_t* blk, int, int h, int (&c)[16]) {
+        const uint8_t* p = blk + 2;
+        const uint32_t q[4] = {ld_u32_a2(p), ld_u32_a2(p + 4), ld_u32_a2(p + 8), ld_u32_a2(p + 12)};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) c[i] = (int)((byte_of(q, i) >> (4 * h)) & 15u);
     }
     __device__ static __forceinline__ void params(const uint8_t* blk, int, int, float& A, float& B) {
         A = h2f(ld_u16(blk));

@@ -293,7 +293,7 @@ __device__ __forceinline__ void store_row_chunks2(uint8_t* A, int r, int cbase, 
     }
 }
 
-// Generic (Q5_0) 16 weights via the shared decoders: k in [k0, k0 + 16).
+// Generic (Q5_0, Q4_0) 16 weights via the shared decoders: k in [k0, k0 + 16).
 template <int T>
 __device__ __forceinline__ void generic16(const uint8_t* mb, int o, uint32_t (&pk)[8]) {
     using F = Fmt<T>;
@@ -636,6 +636,7 @@ cudaError_t launch_gemm(int type, const GemmPlan& pl, const uint8_t* W, int64_t 
     case T_Q6_K: a.row_bytes = cols / 256 * 210; break;
     case T_Q8_0: a.row_bytes = cols / 32 * 34; break;
     case T_Q5_0: a.row_bytes = cols / 32 * 22; break;
+    case T_Q4_0: a.row_bytes = cols / 32 * 18; break;
     default: return cudaErrorInvalidValue;
     }
     a.total16 = (rows * a.row_bytes) & ~(int64_t)15;
@@ -645,6 +646,7 @@ cudaError_t launch_gemm(int type, const GemmPlan& pl, const uint8_t* W, int64_t 
     case T_Q6_K: e = gemm_t<T_Q6_K>(a, pl, map, s); break;
     case T_Q8_0: e = gemm_t<T_Q8_0>(a, pl, map, s); break;
     case T_Q5_0: e = gemm_t<T_Q5_0>(a, pl, map, s); break;
+    case T_Q4_0: e = gemm_t<T_Q4_0>(a, pl, map, s); break;
     }
     if (e != cudaSuccess || pl.splits <= 1) return e;
     // Add the partials in split order.

@@ -346,6 +346,7 @@ int slot_of(int type) {
     case T_Q6_K: return slot_bytes<T_Q6_K>();
     case T_Q8_0: return slot_bytes<T_Q8_0>();
     case T_Q5_0: return slot_bytes<T_Q5_0>();
+    case T_Q4_0: return slot_bytes<T_Q4_0>();
     }
     return 0;
 }
@@ -433,6 +434,7 @@ int64_t row_bytes_of(int type, int64_t cols) {
     case T_Q6_K: return cols / 256 * 210;
     case T_Q8_0: return cols / 32 * 34;
     case T_Q5_0: return cols / 32 * 22;
+    case T_Q4_0: return cols / 32 * 18;
     }
     return 0;
 }
@@ -469,6 +471,7 @@ cudaError_t launch_gemv5(int type, int n, const uint8_t* const* W, const int64_t
     case T_Q6_K: return launch5_t<T_Q6_K>(a, pl, s);
     case T_Q8_0: return launch5_t<T_Q8_0>(a, pl, s);
     case T_Q5_0: return launch5_t<T_Q5_0>(a, pl, s);
+    case T_Q4_0: return launch5_t<T_Q4_0>(a, pl, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -84,7 +84,7 @@ __device__ __forceinline__ void load_x(const uint8_t* xs, int j0, int j1, XL& x)
 
 // Exact integer dot of 4 code words (16 codes) with 16 limb triples, limb
 // words w0..w0+3 of x-block j; accumulates into A, B, C.  Every code byte
-// fed here is a valid signed byte (Q4_K 0..15, Q6_K 0..63, Q5_0 0..31, Q8_0
+// fed here is a valid signed byte (Q4_K 0..15, Q6_K 0..63, Q5_0 0..31, Q4_0 0..15, Q8_0
 // signed), so the signed x signed form is used throughout.
 __device__ __forceinline__ void dot16(const uint32_t (&q)[4], const XL& x, int j, int w0, int& A, int& B, int& C) {
 #pragma unroll
@@ -280,6 +280,37 @@ template <> struct Lane<T_Q8_0> {
             dot16(qa, x, j, 0, A, B, C);
             dot16(qb, x, j, 4, A, B, C);
             r = fmaf(h2f(ld_u16(blk)) * x.meta[j].x, limbs_to_f(A, B, C), r);
+        }
+        return r;
+    }
+};
+
+// Q4_0: lane l -> blocks 2l and 2l+1 (x-blocks 2l, 2l+1).  Element e < 16 is
+// the low nibble of qs[e], element e + 16 the high nibble.  w = d * (q - 8).
+template <> struct Lane<T_Q4_0> {
+    int l;
+    __device__ __forceinline__ explicit Lane(int lane) : l(lane) {}
+    __device__ __forceinline__ bool valid(int nblk) const { return 2 * l < nblk; }
+    __device__ __forceinline__ void xblocks(int lane, int& j0, int& j1) const { j0 = 2 * lane; j1 = 2 * lane + 1; }
+    __device__ __forceinline__ float dot(const uint8_t* seg, const XL& x, int nblk) const {
+        float r = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            if (2 * l + j >= nblk) break;
+            const uint8_t* blk = seg + 36 * l + 18 * j;
+            uint32_t q[4];
+            lds_words_a2<4>(blk + 2, q);
+            uint32_t lo[4], hi[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                lo[i] = q[i] & 0x0F0F0F0Fu;
+                hi[i] = (q[i] >> 4) & 0x0F0F0F0Fu;
+            }
+            int A = 0, B = 0, C = 0;
+            dot16(lo, x, j, 0, A, B, C);
+            dot16(hi, x, j, 4, A, B, C);
+            const float4 mt = x.meta[j];
+            r = fmaf(h2f(ld_u16(blk)), fmaf(mt.x, limbs_to_f(A, B, C), -8.0f * mt.w), r);
         }
         return r;
     }

@@ -19,6 +19,11 @@
  *   Q5_0  32 weights in 22 bytes: fp16 d, a 32-bit word of fifth bits, 16
  *         bytes of nibbles; weight = d*(q - 16).  ("Local LLM inference",
  *         "The mmap backend": one of the block types of a Q4_K_M file.)
+ *   Q4_0  32 weights in 18 bytes: fp16 d, 16 bytes of nibbles (low nibbles
+ *         elements 0-15, high nibbles 16-31); weight = d*(q - 8).
+ *         ("Hitchhiker's Guide", section 11.1, Q4_0 block figure; "How LLM
+ *         Inference Engines Work", "Loading GGUF Models", the Q4_0
+ *         dequantizer.)
  * The bit placement inside the Q4_K scale bytes, the Q6_K code bytes and the
  * Q5_0 block is the k-quant / GGUF packing: low nibbles of a group of bytes
  * are the first weights, high nibbles the next ("How LLM Inference Engines
@@ -55,7 +60,7 @@ extern "C" {
 #endif
 
 /* Quant types.  The numbers are this library's own. */
-typedef enum { QK_Q4_K = 1, QK_Q6_K = 2, QK_Q8_0 = 3, QK_Q5_0 = 4 } qk_type;
+typedef enum { QK_Q4_K = 1, QK_Q6_K = 2, QK_Q8_0 = 3, QK_Q5_0 = 4, QK_Q4_0 = 5 } qk_type;
 
 typedef enum {
     QK_OK = 0,

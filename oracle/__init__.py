@@ -8,7 +8,7 @@ The arithmetic lives in ``qk_oracle.c`` (scalar C, fp32 weights in the order
 the formulas state, fp64 accumulation).  This module compiles it with gcc on
 first use and wraps it with numpy in / numpy out functions.
 
-Type ids: Q4_K=1, Q6_K=2, Q8_0=3, Q5_0=4 (and Q4_0=5, oracle only).
+Type ids: Q4_K=1, Q6_K=2, Q8_0=3, Q5_0=4, Q4_0=5.
 """
 from __future__ import annotations
 

@@ -38,8 +38,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_sizes(lib):
-    assert [qk.block_bytes(t) for t in (1, 2, 3, 4)] == [144, 210, 34, 22]
-    assert [qk.block_elems(t) for t in (1, 2, 3, 4)] == [256, 256, 32, 32]
+    assert [qk.block_bytes(t) for t in (1, 2, 3, 4, 5)] == [144, 210, 34, 22, 18]
+    assert [qk.block_elems(t) for t in (1, 2, 3, 4, 5)] == [256, 256, 32, 32, 32]
     assert qk.block_bytes(9) == 0 and qk.block_elems(0) == 0
     assert qk.row_bytes(qk.Q6_K, 11008) == 9030
     assert qk.row_bytes(qk.Q4_K, 4096) == 2304

@@ -13,7 +13,7 @@ from golden_io import all_fixtures, load
 from gpu_helpers import dev_u8, gpu, type_id  # noqa: F401
 
 pytestmark = pytest.mark.gpu
-NAMES = ["Q4_K", "Q6_K", "Q8_0", "Q5_0"]
+NAMES = ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0"]
 
 
 @pytest.mark.parametrize("name", NAMES)
@@ -53,7 +53,7 @@ def test_dequant_bf16_rounding(gpu, name):
     assert np.array_equal(got, ref)
 
 
-@pytest.mark.parametrize("path", [p for p in all_fixtures() if "q4_0" not in p], ids=lambda p: p.rsplit("/", 1)[-1])
+@pytest.mark.parametrize("path", all_fixtures(), ids=lambda p: p.rsplit("/", 1)[-1])
 def test_golden_blocks_on_device(gpu, path):
     name, blk, expect = load(path)
     t = type_id(name)

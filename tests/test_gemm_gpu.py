@@ -25,6 +25,7 @@ CASES = [
     ("Q4_K", 256, 512, 600),     # two 512-token tiles, the second with one live accumulator
     ("Q6_K", 130, 512, 1100),    # three token tiles, ragged rows
     ("Q5_0", 128, 320, 513),     # second tile holds a single token
+    ("Q4_0", 200, 1056, 77),
 ]
 
 
@@ -82,6 +83,7 @@ SPLIT_CASES = [
     ("Q8_0", 384, 4096, 64),
     ("Q5_0", 96, 5120, 9),
     ("Q4_K", 130, 2048, 1),
+    ("Q4_0", 64, 8192, 5),
 ]
 
 

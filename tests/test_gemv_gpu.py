@@ -11,7 +11,7 @@ import synth
 from gpu_helpers import assert_gemv_close, dev_f32, dev_u8, gpu, type_id  # noqa: F401
 
 pytestmark = pytest.mark.gpu
-NAMES = ["Q4_K", "Q6_K", "Q8_0", "Q5_0"]
+NAMES = ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0"]
 
 
 def run(gpu, name, rows, cols, M, seed, W=None, x=None):
@@ -34,6 +34,7 @@ SHAPES = {
     "Q6_K": [(1, 256), (5, 1280), (37, 3328), (9, 11008)],
     "Q8_0": [(1, 32), (5, 1056), (37, 3104), (300, 1024)],
     "Q5_0": [(1, 32), (5, 1056), (37, 3104), (300, 1024)],
+    "Q4_0": [(1, 32), (5, 1056), (37, 3104), (300, 1024)],
 }
 
 

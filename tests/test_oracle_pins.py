@@ -211,7 +211,7 @@ def test_zero_scale_block_is_zero(oracle_mod):
 
 # ------------------------------------------------------ dot products --
 
-@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q5_0"])
+@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0"])
 @pytest.mark.parametrize("rows,cols,M", [(1, 256, 1), (3, 512, 2), (4, 1024, 3)])
 def test_gemv_matches_numpy_float64_matmul(oracle_mod, name, rows, cols, M):
     t = T[name]
