@@ -399,6 +399,41 @@ def run_gemm_bench(dev, reps: int = 5):
             "comparator_note": "qk_dequant to bf16 then torch.matmul, same 9 matrices (vocab excluded)"}
 
 
+def run_ffn_gemm(dev, M: int, reps: int = 20):
+    """Small-batch dequant-GEMM alone: the Llama-3-8B FFN matrices (gate/up
+    14336x4096, down 4096x14336) in Q4_K through qk_gemm at activation batch
+    M, four rotating weight copies (beyond L2).  Per matrix: 2 warm-up launches,
+    then `reps` launches back to back between two CUDA events; GB/s counts
+    packed weights + X (bf16) + Y (fp32)."""
+    import torch
+    import gguf_quant_dequant_gb300 as qk
+    import synth
+    t = qk.Q4_K
+    stream = torch.cuda.current_stream()
+    g = torch.Generator(device=dev)
+    g.manual_seed(4242)
+    out = {}
+    for i, (nm, name, rows, cols) in enumerate(synth.llama3_ffn("Q4_K")):
+        Ws = [synth.random_blocks_torch(name, rows, cols, 8000 + 10 * i + k, dev) for k in range(4)]
+        X = torch.randn((M, cols), device=dev, generator=g).to(torch.bfloat16)
+        Y = torch.empty((M, rows), device=dev)
+        ws = torch.empty(max(16, qk.gemm_workspace(t, rows, cols, M)), dtype=torch.uint8, device=dev)
+        for k in range(2):
+            qk.gemm(t, Ws[k], rows, cols, X, Y=Y, ws=ws)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(reps):
+            qk.gemm(t, Ws[k % 4], rows, cols, X, Y=Y, ws=ws)
+        e1.record(stream)
+        e1.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        nbytes = Ws[0].numel() + 2 * M * cols + 4 * M * rows
+        out[nm] = {"us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                   "tflops": round(2.0 * M * rows * cols / (us * 1e-6) / 1e12, 2)}
+        del Ws, X, Y, ws
+    return {"workload": f"Llama-3-8B FFN Q4_K, qk_gemm at M={M}", "per_matrix": out}
+
+
 def _graph_time_us(fn, reps: int = 20, warm: int = 3) -> float:
     """Median over reps of one replay of a CUDA graph of fn, in microseconds."""
     import torch
@@ -645,6 +680,8 @@ def main():
     ap.add_argument("--no-sweep", action="store_true", help="skip the Llama-3 FFN batch sweep")
     ap.add_argument("--gemm-only", action="store_true",
                     help="run only the prefill GEMM leg and print its JSON (for profiling)")
+    ap.add_argument("--ffn-gemm", type=int, default=0, metavar="M",
+                    help="run only the small-batch GEMM over the Llama-3 FFN at batch M (for profiling)")
     ap.add_argument("--min-warmup-s", type=float, default=1.0,
                     help="keep replaying warm-up steps for at least this long (clocks settle)")
     args = ap.parse_args()
@@ -652,13 +689,16 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
-    elif args.gemm_only:
+    elif args.gemm_only or args.ffn_gemm > 0:
         import torch
         from gguf_quant_dequant_gb300 import build as qkbuild
         qkbuild.build()
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
-        print(json.dumps(run_gemm_bench(dev, reps=args.steps)))
+        if args.ffn_gemm > 0:
+            print(json.dumps(run_ffn_gemm(dev, args.ffn_gemm, reps=args.steps)))
+        else:
+            print(json.dumps(run_gemm_bench(dev, reps=args.steps)))
     else:
         run_gpu(args)
 

@@ -48,38 +48,75 @@ namespace gm {
 __device__ __forceinline__ uint4 lds128_g(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
 
 constexpr int kBM = 128;          // weight rows per CTA (MMA M)
-constexpr int kBNM = 256;         // tokens per MMA / accumulator (MMA N)
-constexpr int kNAcc = 2;          // accumulators per CTA
-constexpr int kBN = kBNM * kNAcc; // tokens per CTA
 constexpr int kBK = 64;           // K per stage (one 128-byte swizzle row)
-constexpr int kNS = 2;            // bf16 operand stages
-constexpr int kA = kBM * kBK * 2; // 16 KB
-constexpr int kBsub = kBNM * kBK * 2;   // 32 KB per accumulator's activation tile
-constexpr int kB = kBsub * kNAcc; // 64 KB
-constexpr int kStage = kA + kB;
+constexpr int kA = kBM * kBK * 2; // 16 KB of bf16 weights per stage
 constexpr int kDeqWarps = 16;
 constexpr int kDeqThreads = kDeqWarps * 32;
+constexpr int kThreads = (2 + kDeqWarps) * 32;   // TMA warp, MMA warp, dequant warps
 constexpr int kParts = kDeqThreads / kBM;            // threads per tile row (4): 16 weights each
-constexpr int kThreads = (2 + kDeqWarps) * 32;
-constexpr int kTmemCols = kBNM * kNAcc;   // 512: all of tensor memory
-constexpr int kNSP = 2;           // packed macro-block stages
+
+// Pipeline shape.  Three rings: NS weight stages (bf16 operand A, written by
+// the dequant warps), an activation ring of run-time depth (operand B, one
+// 64-wide k-block of every accumulator's tokens per stage, loaded by TMA)
+// and NSP packed macro-block stages; NACC accumulators of BNM tokens each.
+// The activation ring has its own barriers, so its loads run as far ahead of
+// the tensor core as its depth allows instead of waiting for the weight
+// stage they pair with.
+//   Wide (prefill, M > 64): two 256-token accumulators fill tensor memory and
+//   each k-block carries 8 MMAs of 128 x 256 x 16, so two weight stages keep
+//   the tensor core fed.
+//   Skinny (M <= 64): one accumulator of at most 64 tokens; a k-block's MMA
+//   work is tiny, so the dequant warps run up to NS k-blocks ahead of the
+//   tensor core and two packed macro-blocks stream in while a third is
+//   decoded.
+// WARP_ISSUE: the MMA issuer's loop runs on the whole warp (warp-uniform
+// indices, one elected lane issues) rather than on lane 0 alone; measured
+// faster for the skinny pipeline's short MMAs, slower for the wide one.
+template <int NS_, int NACC_, int BNM_, int NSP_, bool WARP_ISSUE_> struct Cfg {
+    static constexpr int NS = NS_, NACC = NACC_, BNM = BNM_, NSP = NSP_;
+    static constexpr bool WARP_ISSUE = WARP_ISSUE_;
+    static constexpr int BN = BNM * NACC;            // tokens per CTA
+    static constexpr int TMEM = BN < 32 ? 32 : BN;   // power of two >= 32
+    static_assert((TMEM & (TMEM - 1)) == 0, "tensor memory columns");
+};
+using Wide = Cfg<2, 2, 256, 2, false>;
+constexpr int kSkinnyBN = 64;     // largest M the skinny pipeline takes
+constexpr int kMaxXStages = 16;   // activation ring depth limit
+constexpr int kSmemMax = 227 * 1024;
 
 // Packed macro-block geometry: weights and bytes per row (one super-block,
 // or four / eight 32-weight blocks), and the per-row slot: the aligned-down
 // window starts up to 14 bytes early and the funnel-shifted word reads run up
 // to 4 bytes past the end.
-template <int T> struct Pk {
+template <int T> struct PkGeo {
     static constexpr int MB = T == T_Q8_0 ? 128 : 256;
     static constexpr int KPM = MB / kBK;                         // k-blocks per macro-block
-    static constexpr int BYTES = MB / Fmt<T>::BE * Fmt<T>::BB;   // 144, 210, 136, 176
+    static constexpr int BYTES = MB / Fmt<T>::BE * Fmt<T>::BB;   // 144, 210, 136, 176, 144
     // Row slots are 16-byte multiples (cp.async) and an odd number of 16-byte
     // units, so the 32 rows a warp reads spread over 8 bank groups.
     static constexpr int SLOT0 = (BYTES + 14 + 4 + 15) / 16 * 16;
     static constexpr int SLOT = (SLOT0 / 16) % 2 == 0 ? SLOT0 + 16 : SLOT0;
     static constexpr int STAGE = kBM * SLOT;
-    static constexpr int OFF_P = 1024 + kNS * kStage;             // packed ring (after the operand stages)
-    static constexpr int OFF_BAR = OFF_P + kNSP * STAGE;
-    static constexpr int SMEM = OFF_BAR + (3 * kNS + 1) * 8 + 16;
+};
+
+// Skinny pipeline: up to 6 weight stages beside three packed stages,
+// keeping 48 KB for the activation ring.
+template <int T> struct SkinnyNS {
+    static constexpr int FREE = kSmemMax - 1024 - 3 * PkGeo<T>::STAGE - 48 * 1024 - 1024;
+    static constexpr int V = FREE / kA > 6 ? 6 : FREE / kA;
+};
+template <int T> using Skinny = Cfg<SkinnyNS<T>::V, 1, kSkinnyBN, 3, true>;
+
+// Shared-memory map (from the 1024-byte aligned base): NS weight stages, the
+// activation ring (nsb stages of xst bytes), the packed ring, the mbarriers
+// and the tensor-memory address slot.  FIX is everything but the activation
+// ring and the barriers; 1 KB of slack covers the base alignment.
+template <int T, class C> struct Pk : PkGeo<T> {
+    static constexpr int OFF_X = C::NS * kA;
+    static constexpr int FIX = 1024 + C::NS * kA + C::NSP * PkGeo<T>::STAGE;
+    __host__ __device__ static constexpr int smem(int nsb, int xst) {
+        return FIX + nsb * xst + (2 * C::NS + 2 * nsb + 1) * 8 + 16;
+    }
 };
 
 struct Args {
@@ -91,6 +128,8 @@ struct Args {
     int nkb;              // 64-wide k-blocks of K
     int kb_per_split;     // k-blocks per split (a multiple of the macro-block's)
     int nmma;             // MMA N (tokens per accumulator): 256, or M rounded up to 16 when M <= 256
+    int nsb;              // activation ring depth
+    int xst;              // bytes per activation stage (accumulators x nmma x 128)
 };
 
 // (unit, half) of the 16 weights that start `o` weights into a block.
@@ -109,47 +148,9 @@ __device__ __forceinline__ void locate(int o, int& u, int& h) {
     }
 }
 
-// 32 bf16 weights, k in [k0, k0 + 32) of row `row`, decoded from the row's
-// packed macro-block in shared memory (`mb` points at its first byte; the
-// macro-block starts at k = kmb), into 4 swizzled 16-byte chunks of the A
-// stage (chunks cbase..cbase+3 of tile row r).  Rows past the matrix and k
-// past cols are zero.
-template <int T>
-__device__ __forceinline__ void dequant32(const Args& p, uint8_t* A, int r, int64_t row, const uint8_t* mb,
-                                          int64_t kmb, int64_t k0, int cbase) {
-    using F = Fmt<T>;
-    uint32_t packed[16];
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-        const int64_t k = k0 + 16 * hf;
-        float w[16];
-        if (row < p.rows && k < p.cols) {
-            const int o = (int)(k - kmb);               // offset inside the macro-block
-            int u, h;
-            locate<T>(o % F::BE, u, h);
-            dequant_half<T>(mb + (o / F::BE) * F::BB, u, h, w);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = 0.0f;
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const __nv_bfloat162 v = __floats2bfloat162_rn(w[2 * i], w[2 * i + 1]);
-            packed[8 * hf + i] = *reinterpret_cast<const uint32_t*>(&v);
-        }
-    }
-    uint8_t* rowp = A + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const int chunk = (cbase + c) ^ (r & 7);
-        *reinterpret_cast<uint4*>(rowp + chunk * 16) =
-            make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-    }
-}
-
 // ---------------------------------------------------------------------------
-// Fast bf16 decoders (32 weights of one tile row for one 64-wide k-block,
-// half hh).  A code byte is placed into an fp32 mantissa by one byte permute
+// Fast bf16 decoders (16 weights of one tile row: quarter qq of a 64-wide
+// k-block).  A code byte is placed into an fp32 mantissa by one byte permute
 // (exact: 128 + q with the code in bits 16-23 of 0x43000000, or 256 + u/128
 // with the byte in bits 8-15 of 0x43800000), then one packed fp32 FMA per two
 // weights applies scale and offset, and one convert packs two bf16.
@@ -172,83 +173,44 @@ __device__ __forceinline__ void four_hi(uint32_t v, float2 a, float2 c, uint32_t
     o1 = pack_bf16(w23.x, w23.y);
 }
 
-__device__ __forceinline__ void store_row_chunks(uint8_t* A, int r, int cbase, const uint32_t (&pk)[16]) {
-    uint8_t* rowp = A + (r >> 3) * 1024 + (r & 7) * 128;
+// Q4_K header of super-block `blk` (16-byte aligned) -> FMA operands for
+// sub-blocks 2c + hh, c = 0..3 (the ones a thread with quarter qq, hh =
+// qq / 2, decodes in the four k-blocks):  w = a*(128 + q) + o with a = d*sc,
+// o = -(128 a + dmin*m).  The twelve scale bytes are unpacked four at a time:
+// sub-blocks 0-3 take the low 6 bits of bytes 0-3 (scales) and 4-7 (mins);
+// sub-blocks 4-7 take the low / high nibble of bytes 8-11 plus the top two
+// bits of bytes 0-3 / 4-7.
+__device__ __forceinline__ void q4k_operands(const uint8_t* blk, int hh, float2 (&a)[4], float2 (&o)[4]) {
+    const uint4 h = lds128_g(blk);
+    const uint32_t sh = 8u * (uint32_t)hh;
+    const uint32_t sc_lo = (h.y & 0x3F3F3F3Fu) >> sh, m_lo = (h.z & 0x3F3F3F3Fu) >> sh;
+    const uint32_t sc_hi = ((h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u)) >> sh;
+    const uint32_t m_hi = (((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u)) >> sh;
+    const float d = h2f(h.x & 0xFFFFu), dmin = h2f(h.x >> 16);
+    const uint32_t sc[4] = {sc_lo, sc_lo >> 16, sc_hi, sc_hi >> 16};
+    const uint32_t mm[4] = {m_lo, m_lo >> 16, m_hi, m_hi >> 16};
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        const int chunk = (cbase + c) ^ (r & 7);
-        *reinterpret_cast<uint4*>(rowp + chunk * 16) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        const float ds = d * (float)(sc[c] & 0xFFu), dm = dmin * (float)(mm[c] & 0xFFu);
+        const float off = -(128.0f * ds + dm);
+        a[c] = make_float2(ds, ds);
+        o[c] = make_float2(off, off);
     }
 }
 
-// Q4_K: k-block c = kb % 4 of super-block `blk` (16-byte aligned in shared
-// memory), sub-block j = 2c + hh: codes are nibble hh of qs[32c .. 32c+31].
-// w = (d*sc)*q - dmin*m = ds*(128 + q) - (128 ds + dm).
-__device__ __forceinline__ void fast_q4k(const uint8_t* blk, int c, int hh, uint32_t (&pk)[16]) {
-    const uint4 h = lds128_g(blk);
-    const uint4 q0 = lds128_g(blk + 16 + 32 * c), q1 = lds128_g(blk + 32 + 32 * c);
-    uint32_t sc, m;
-    Fmt<T_Q4_K>::scale_min(blk, 2 * c + hh, sc, m);
-    const float ds = h2f(h.x & 0xFFFFu) * (float)sc, dm = h2f(h.x >> 16) * (float)m;
-    const float2 a = make_float2(ds, ds), cc = make_float2(-(128.0f * ds + dm), -(128.0f * ds + dm));
-    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) four_hi((w[i] >> (4 * hh)) & 0x0F0F0F0Fu, a, cc, pk[2 * i], pk[2 * i + 1]);
-}
-
-// Q8_0: one 34-byte block (2-byte aligned): w = d*q = 128d*(256 + u/128) - 32896d, u = q + 128.
-__device__ __forceinline__ void fast_q80(const uint8_t* blk, uint32_t (&pk)[16]) {
-    uint32_t q[8];
-    gv::lds_words_a2<8>(blk + 2, q);
-    const float d = h2f(ld_u16(blk));
-    const float2 a = make_float2(128.0f * d, 128.0f * d), cc = make_float2(-32896.0f * d, -32896.0f * d);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t u = q[i] ^ 0x80808080u;
-        const float f0 = __uint_as_float(__byte_perm(u, 0x43800000u, 0x7604));
-        const float f1 = __uint_as_float(__byte_perm(u, 0x43800000u, 0x7614));
-        const float f2 = __uint_as_float(__byte_perm(u, 0x43800000u, 0x7624));
-        const float f3 = __uint_as_float(__byte_perm(u, 0x43800000u, 0x7634));
-        const float2 w01 = __ffma2_rn(a, make_float2(f0, f1), cc);
-        const float2 w23 = __ffma2_rn(a, make_float2(f2, f3), cc);
-        pk[2 * i] = pack_bf16(w01.x, w01.y);
-        pk[2 * i + 1] = pack_bf16(w23.x, w23.y);
-    }
-}
-
-// Q6_K: 32 weights o = 64c + 32hh .. of super-block `blk` (2-byte aligned):
-// half t = o / 128, group g = (o % 128) / 32; w = d*sc*(q - 32) = ds*(128 + q) - 160 ds.
-__device__ __forceinline__ void fast_q6k(const uint8_t* blk, int c, int hh, uint32_t (&pk)[16]) {
-    const int o = 64 * c + 32 * hh, t = o >> 7, g = (o >> 5) & 3;
-    uint32_t ql[8], qh[8];
-    gv::lds_words_a2<8>(blk + 64 * t + 32 * (g & 1), ql);
-    gv::lds_words_a2<8>(blk + 128 + 32 * t, qh);
-    const uint32_t sw = ld_u16(blk + 192 + 8 * t + 2 * g);
-    const float d = h2f(ld_u16(blk + 208));
-    const float ds0 = d * (float)(int)(int8_t)(sw & 0xFFu), ds1 = d * (float)(int)(int8_t)(sw >> 8);
-    const int nsh = 4 * (g >> 1), hsh = 2 * g;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float ds = i < 4 ? ds0 : ds1;
-        const uint32_t v = ((ql[i] >> nsh) & 0x0F0F0F0Fu) | (((qh[i] >> hsh) & 0x03030303u) << 4);
-        four_hi(v, make_float2(ds, ds), make_float2(-160.0f * ds, -160.0f * ds), pk[2 * i], pk[2 * i + 1]);
-    }
-}
-
-// 16-weight variants: quarter qq (0..3) of the 64-wide k-block c.
-__device__ __forceinline__ void fast16_q4k(const uint8_t* blk, int c, int qq, uint32_t (&pk)[8]) {
-    const int hh = qq >> 1;   // sub-block 2c + hh, code bytes 16 (qq & 1) .. +16 of its 32
-    const uint4 h = lds128_g(blk);
+// 16 Q4_K weights of k-block c, quarter qq (codes: nibble qq / 2 of bytes
+// 16 (qq & 1) .. +15 of the k-block's 32 code bytes), operands from
+// q4k_operands.
+__device__ __forceinline__ void q4k16(const uint8_t* blk, int c, int qq, float2 a, float2 o, uint32_t (&pk)[8]) {
     const uint4 q = lds128_g(blk + 16 + 32 * c + 16 * (qq & 1));
-    uint32_t sc, m;
-    Fmt<T_Q4_K>::scale_min(blk, 2 * c + hh, sc, m);
-    const float ds = h2f(h.x & 0xFFFFu) * (float)sc, dm = h2f(h.x >> 16) * (float)m;
-    const float2 a = make_float2(ds, ds), cc = make_float2(-(128.0f * ds + dm), -(128.0f * ds + dm));
+    const uint32_t sh = 4u * (uint32_t)(qq >> 1);
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) four_hi((w[i] >> (4 * hh)) & 0x0F0F0F0Fu, a, cc, pk[2 * i], pk[2 * i + 1]);
+    for (int i = 0; i < 4; ++i) four_hi((w[i] >> sh) & 0x0F0F0F0Fu, a, o, pk[2 * i], pk[2 * i + 1]);
 }
 
+// Q8_0: 16 weights of one 34-byte block (2-byte aligned), half `half`:
+// w = d*q = 128d*(256 + u/128) - 32896d with u = q + 128.
 __device__ __forceinline__ void fast16_q80(const uint8_t* blk, int half, uint32_t (&pk)[8]) {
     uint32_t q[4];
     gv::lds_words_a2<4>(blk + 2 + 16 * half, q);
@@ -268,6 +230,8 @@ __device__ __forceinline__ void fast16_q80(const uint8_t* blk, int half, uint32_
     }
 }
 
+// Q6_K: 16 weights o = 64c + 16qq .. of super-block `blk` (2-byte aligned):
+// half t = o / 128, group g = (o % 128) / 32; w = d*sc*(q - 32) = ds*(128 + q) - 160 ds.
 __device__ __forceinline__ void fast16_q6k(const uint8_t* blk, int c, int qq, uint32_t (&pk)[8]) {
     const int o = 64 * c + 16 * qq, t = o >> 7, g = (o >> 5) & 3, l0 = o & 31;
     uint32_t ql[4], qh[4];
@@ -281,15 +245,6 @@ __device__ __forceinline__ void fast16_q6k(const uint8_t* blk, int c, int qq, ui
     for (int i = 0; i < 4; ++i) {
         const uint32_t v = ((ql[i] >> nsh) & 0x0F0F0F0Fu) | (((qh[i] >> hsh) & 0x03030303u) << 4);
         four_hi(v, a, cc, pk[2 * i], pk[2 * i + 1]);
-    }
-}
-
-__device__ __forceinline__ void store_row_chunks2(uint8_t* A, int r, int cbase, const uint32_t (&pk)[8]) {
-    uint8_t* rowp = A + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-        const int chunk = (cbase + c) ^ (r & 7);
-        *reinterpret_cast<uint4*>(rowp + chunk * 16) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
     }
 }
 
@@ -311,7 +266,7 @@ __device__ __forceinline__ void generic16(const uint8_t* mb, int o, uint32_t (&p
 // consumer of that row (tail_fix).
 template <int T>
 __device__ __forceinline__ void issue_packed(const Args& p, uint8_t* dst, int64_t row0, int64_t m, int r, int part) {
-    using K = Pk<T>;
+    using K = PkGeo<T>;
     const int64_t row = row0 + r;
     if (row >= p.rows) return;
     const int64_t kb0 = m * K::MB;
@@ -326,7 +281,7 @@ __device__ __forceinline__ void issue_packed(const Args& p, uint8_t* dst, int64_
 
 template <int T>
 __device__ __forceinline__ void tail_fix(const Args& p, uint8_t* slot_row, int64_t row, int64_t m) {
-    using K = Pk<T>;
+    using K = PkGeo<T>;
     const int64_t kb0 = m * K::MB;
     const int64_t len = min((int64_t)K::MB, p.cols - kb0) / Fmt<T>::BE * Fmt<T>::BB;
     const int64_t st = row * p.row_bytes + m * K::BYTES;
@@ -335,44 +290,55 @@ __device__ __forceinline__ void tail_fix(const Args& p, uint8_t* slot_row, int64
     for (int64_t b = max(st, p.total16); b < st + len; ++b) base[b] = p.W[b];
 }
 
-template <int T>
+template <int T, class C>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
-    using K = Pk<T>;
+    using K = Pk<T, C>;
+    constexpr int kNS = C::NS, kNSP = C::NSP, kBNM = C::BNM;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base (the 128-byte swizzle atoms must be aligned).
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    uint8_t* packed = smem_raw + K::OFF_P;
-    uint64_t* full_x = reinterpret_cast<uint64_t*>(smem_raw + K::OFF_BAR);
-    uint64_t* full_w = full_x + kNS;
-    uint64_t* empty = full_w + kNS;
-    uint64_t* accum = empty + kNS;
+    uint8_t* xring = smem + K::OFF_X;
+    const int nsb = p.nsb;
+    uint8_t* packed = smem + K::OFF_X + nsb * p.xst;
+    uint64_t* full_w = reinterpret_cast<uint64_t*>(packed + kNSP * K::STAGE);   // weight stage written
+    uint64_t* empty = full_w + kNS;                                             // weight stage consumed
+    uint64_t* full_x = empty + kNS;                                             // activation stage landed
+    uint64_t* empty_x = full_x + nsb;                                           // activation stage consumed
+    uint64_t* accum = empty_x + nsb;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Token tiles vary fastest: the CTAs that share a weight tile run
     // together, so each packed weight byte comes from DRAM once.
     const int64_t row0 = (int64_t)blockIdx.y * kBM;
-    const int64_t tok0 = (int64_t)blockIdx.x * kBN;
-    const int nacc = p.M - tok0 > kBNM ? 2 : 1;   // accumulators holding real tokens
+    const int64_t tok0 = (int64_t)blockIdx.x * C::BN;
+    const int nacc = C::NACC > 1 && p.M - tok0 > kBNM ? 2 : 1;   // accumulators holding real tokens
     // This CTA's share of K: k-blocks [kb0, kb1) (blockIdx.z = split).
     const int kb0 = (int)blockIdx.z * p.kb_per_split;
     const int kb1 = min(p.nkb, kb0 + p.kb_per_split);
     const int nk = kb1 - kb0;
+    // Macro-blocks m0 .. m0 + nmb - 1 cover these k-blocks (kb0 is a multiple
+    // of the macro-block's k-blocks).
+    const int m0 = kb0 / K::KPM;
+    const int nmb = (kb1 + K::KPM - 1) / K::KPM - m0;
     const uint32_t bsub = (uint32_t)p.nmma * (kBK * 2);   // bytes of one accumulator's activation tile
     float* out = p.part ? p.part + (size_t)blockIdx.z * (size_t)p.M * (size_t)p.rows : p.Y;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNS; ++s) {
-            mbar_init(&full_x[s], 1);
             mbar_init(&full_w[s], kDeqWarps);
             mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < nsb; ++s) {
+            mbar_init(&full_x[s], 1);
+            mbar_init(&empty_x[s], 1);
         }
         mbar_init(accum, 1);
         fence_barrier_init();
     }
     if (warp == 1) {
-        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_alloc(tmem_slot, C::TMEM);
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
@@ -386,117 +352,163 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         // previous kernel: wait for it first).
         if (lane == 0) {
             pdl_wait_prior();
-            int issued = 0;
-            for (int i = 0; i < nk; ++i) {   // local k-block i = k-block kb0 + i
-                const int s = i % kNS;
-                if (i >= kNS && !mbar_wait_sleep_bounded(&empty[s], (uint32_t)((i / kNS - 1) & 1), p.status)) break;
+            int issued = 0, s = 0;
+            uint32_t par = 1;   // phase parity of empty_x[s] to wait for (from the second lap)
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (issued >= nsb && !mbar_wait_sleep_bounded(&empty_x[s], par, p.status)) break;
                 mbar_arrive_expect_tx(&full_x[s], bsub * (uint32_t)nacc);
                 for (int j = 0; j < nacc; ++j)
-                    tc::tma_load_2d(smem + s * kStage + kA + j * kBsub, &xmap, (kb0 + i) * kBK, (int)tok0 + kBNM * j,
-                                    &full_x[s]);
-                issued = i + 1;
+                    tc::tma_load_2d(xring + s * p.xst + j * bsub, &xmap, kb * kBK, (int)tok0 + kBNM * j, &full_x[s]);
+                ++issued;
+                if (++s == nsb) {
+                    s = 0;
+                    par ^= 1u;
+                }
             }
             // Every load issued must land before the CTA may exit.
-            for (int i = issued > kNS ? issued - kNS : 0; i < issued; ++i)
-                mbar_wait_bounded(&full_x[i % kNS], (uint32_t)((i / kNS) & 1), p.status);
+            for (int i = issued > nsb ? issued - nsb : 0; i < issued; ++i)
+                mbar_wait_bounded(&full_x[i % nsb], (uint32_t)((i / nsb) & 1), p.status);
         }
     } else if (warp == 1) {
-        // MMA issuer.
-        if (lane == 0) {
-            const uint32_t idesc = tc::idesc_bf16_f32(kBM, p.nmma);
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % kNS;
-                const uint32_t par = (uint32_t)((i / kNS) & 1);
-                if (!mbar_wait_sleep_bounded(&full_x[s], par, p.status) ||
-                    !mbar_wait_sleep_bounded(&full_w[s], par, p.status))
-                    break;
-                tc::fence_after_sync();
-                const uint32_t a = smem_u32(smem + s * kStage), b = a + kA;
+        // MMA issuer.  With WARP_ISSUE the whole warp runs the loop, so the
+        // stage indices and operand descriptors stay warp-uniform; lane 0
+        // polls the barriers and one elected lane issues every MMA and commit
+        // (a commit tracks the MMAs of the thread that issues it).  Otherwise
+        // lane 0 runs the loop alone.  Descriptor start addresses advance in
+        // 16-byte units from the ring bases.
+        const bool leader = C::WARP_ISSUE ? tc::elect_one() : lane == 0;
+        const uint32_t idesc = tc::idesc_bf16_f32(kBM, p.nmma);
+        const uint64_t da0 = tc::sdesc_k128(smem_u32(smem)), db0 = tc::sdesc_k128(smem_u32(xring));
+        const uint64_t dbj = (uint64_t)(bsub >> 4);   // second accumulator's activation tile
+        int s = 0, sx = 0;
+        uint32_t par = 0, parx = 0;   // phase parities of full_w[s] and full_x[sx]
+        for (int i = 0; i < nk && (C::WARP_ISSUE || leader); ++i) {
+            int good = 1;
+            if (lane == 0)
+                good = mbar_wait_sleep_bounded(&full_x[sx], parx, p.status) &&
+                       mbar_wait_sleep_bounded(&full_w[s], par, p.status);
+            if (C::WARP_ISSUE) good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) break;
+            tc::fence_after_sync();
+            const uint64_t da = da0 + (uint64_t)((s * kA) >> 4), db = db0 + (uint64_t)((sx * p.xst) >> 4);
+            if (leader) {
                 for (int j = 0; j < nacc; ++j) {
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
-                        tc::mma_bf16(tmem + kBNM * j, tc::sdesc_k128(a + 32 * kk),
-                                     tc::sdesc_k128(b + kBsub * j + 32 * kk), idesc, (i | kk) != 0 ? 1u : 0u);
+                        tc::mma_bf16(tmem + kBNM * j, da + 2 * kk, db + dbj * j + 2 * kk, idesc,
+                                     (i | kk) != 0 ? 1u : 0u);
                 }
-                tc::commit(&empty[s]);
+                tc::commit(&empty[s]);     // both stages free once these MMAs complete
+                tc::commit(&empty_x[sx]);
             }
-            tc::commit(accum);   // fires once every MMA issued above has completed
-            // Tensor memory may only be released after the MMAs are done.
-            mbar_wait_sleep_bounded(accum, 0, p.status);
+            if (C::WARP_ISSUE) __syncwarp();
+            if (++s == kNS) {
+                s = 0;
+                par ^= 1u;
+            }
+            if (++sx == nsb) {
+                sx = 0;
+                parx ^= 1u;
+            }
         }
+        if (leader) tc::commit(accum);   // fires once every MMA issued above has completed
+        __syncwarp();
+        // Tensor memory may only be released after the MMAs are done.
+        if (lane == 0) mbar_wait_sleep_bounded(accum, 0, p.status);
+        __syncwarp();
     } else {
         // Dequant warps.  Warp dw owns tile rows 8dw .. 8dw+7; lane -> (row
         // 8dw + lane/4, 16-weight quarter lane%4 of each 64-wide k-block).  The
-        // warp streams its rows' packed macro-blocks into a 2-deep ring with
+        // warp streams its rows' packed macro-blocks into an NSP-deep ring with
         // cp.async and decodes them with no CTA barrier.
         const int dw = warp - 2;
         const int r = 8 * dw + (lane >> 2), qq = lane & 3;
         const int64_t row = row0 + r;
-        // Macro-blocks m0 .. m0 + nmb - 1 cover this CTA's k-blocks (kb0 is a
-        // multiple of the macro-block's k-blocks).
-        const int64_t m0 = kb0 / K::KPM;
-        const int64_t nmb = (kb1 + K::KPM - 1) / K::KPM - m0;
+        const bool live = row < p.rows;
+        // This thread's two swizzled 16-byte chunks inside an operand stage.
+        const uint32_t rbase = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
+        const uint32_t dst0 = rbase + ((((uint32_t)(2 * qq)) ^ (uint32_t)(r & 7)) << 4);
+        const uint32_t dst1 = rbase + ((((uint32_t)(2 * qq + 1)) ^ (uint32_t)(r & 7)) << 4);
+        // k-block kb holds this thread's 16 weights iff 64 kb < kq.
+        const int64_t kq = p.cols - 16 * qq;
         bool ok = true;
+        int s = 0;            // operand stage of the next local k-block
+        uint32_t par = 1;     // phase parity of empty[s] to wait for (after the first NS k-blocks)
+        int li = 0;           // local k-block
+        int ps = 0;           // packed slot of the current macro-block
 #pragma unroll 1
         for (int mi = 0; mi < kNSP - 1; ++mi) {
-            if (mi < nmb) issue_packed<T>(p, packed + mi * K::STAGE, row0, m0 + mi, r, qq);
+            if (mi < nmb) issue_packed<T>(p, packed + mi * K::STAGE, row0, (int64_t)(m0 + mi), r, qq);
             cp_async_commit();
         }
 #pragma unroll 1
-        for (int64_t mi = 0; mi < nmb; ++mi) {
-            const int64_t m = m0 + mi;
+        for (int mi = 0; mi < nmb; ++mi) {
+            const int m = m0 + mi;
+            const int pn = ps == 0 ? kNSP - 1 : ps - 1;   // slot of macro-block mi + NSP - 1
             if (mi + kNSP - 1 < nmb)
-                issue_packed<T>(p, packed + ((mi + kNSP - 1) % kNSP) * K::STAGE, row0, m + kNSP - 1, r, qq);
+                issue_packed<T>(p, packed + pn * K::STAGE, row0, (int64_t)(m + kNSP - 1), r, qq);
             cp_async_commit();
             cp_async_wait<kNSP - 1>();
-            uint8_t* pk = packed + (mi % kNSP) * K::STAGE;
-            if (qq == 0 && row < p.rows) tail_fix<T>(p, pk + r * K::SLOT, row, m);
+            uint8_t* pk = packed + ps * K::STAGE;
+            if (qq == 0 && live) tail_fix<T>(p, pk + r * K::SLOT, row, (int64_t)m);
             __syncwarp();   // this warp's rows of macro-block m are visible
-            const int64_t st = row * p.row_bytes + m * K::BYTES;
+            const int64_t st = row * p.row_bytes + (int64_t)m * K::BYTES;
             const uint8_t* mbp = pk + r * K::SLOT + (int)(st & 15);
+            const int kbm = m * K::KPM;
+            float2 qa[4], qo[4];
+            if constexpr (T == T_Q4_K) {
+                if (live) q4k_operands(mbp, qq >> 1, qa, qo);
+            }
+#pragma unroll
             for (int kk = 0; kk < K::KPM; ++kk) {
-                const int64_t kb = m * K::KPM + kk;
+                const int kb = kbm + kk;
                 if (kb >= kb1) break;
-                const int li = (int)(kb - kb0);   // local k-block
-                const int s = li % kNS;
                 if (ok && li >= kNS) {   // one lane polls, the warp follows
                     int good = 1;
-                    if (lane == 0) good = mbar_wait_bounded(&empty[s], (uint32_t)((li / kNS - 1) & 1), p.status);
+                    if (lane == 0) good = mbar_wait_bounded(&empty[s], par, p.status);
                     ok = __shfl_sync(0xffffffffu, good, 0) != 0;
                 }
                 if (ok) {
                     uint32_t pk8[8];
-                    const int c = kk;
-                    if (row < p.rows && kb * kBK + 16 * qq < p.cols) {
-                        if constexpr (T == T_Q4_K) fast16_q4k(mbp, c, qq, pk8);
-                        else if constexpr (T == T_Q6_K) fast16_q6k(mbp, c, qq, pk8);
-                        else if constexpr (T == T_Q8_0) fast16_q80(mbp + (2 * c + (qq >> 1)) * 34, qq & 1, pk8);
+                    if (live && (int64_t)kb * kBK < kq) {
+                        if constexpr (T == T_Q4_K) q4k16(mbp, kk, qq, qa[kk], qo[kk], pk8);
+                        else if constexpr (T == T_Q6_K) fast16_q6k(mbp, kk, qq, pk8);
+                        else if constexpr (T == T_Q8_0) fast16_q80(mbp + (2 * kk + (qq >> 1)) * 34, qq & 1, pk8);
                         else generic16<T>(mbp, kk * kBK + 16 * qq, pk8);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 8; ++i) pk8[i] = 0u;
                     }
-                    store_row_chunks2(smem + s * kStage, r, 2 * qq, pk8);
+                    uint8_t* As = smem + s * kA;
+                    *reinterpret_cast<uint4*>(As + dst0) = make_uint4(pk8[0], pk8[1], pk8[2], pk8[3]);
+                    *reinterpret_cast<uint4*>(As + dst1) = make_uint4(pk8[4], pk8[5], pk8[6], pk8[7]);
                 }
                 fence_proxy_async_smem();   // generic stores -> visible to the tensor core
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full_w[s]);
+                ++li;
+                if (++s == kNS) {
+                    s = 0;
+                    par ^= 1u;
+                }
             }
-            __syncwarp();   // this warp is done reading slot m % kNSP
+            __syncwarp();   // this warp is done reading slot ps
+            if (++ps == kNSP) ps = 0;
         }
         cp_async_wait<0>();
         // Epilogue: warp w may read tensor-memory lanes 32 (w % 4) .. +31 (its
         // quarter of the weight rows); the four warps of a quarter split the
-        // 512 accumulator columns (tokens) into 128-column groups.
+        // accumulator columns (tokens) into four equal groups.
         {
+            constexpr int kGrp = C::BN / 4;
             const int q = warp & 3, grp = dw >> 2;
             if (lane == 0) mbar_wait_sleep_bounded(accum, 0, p.status);
             __syncwarp();
             tc::fence_after_sync();
             const int64_t orow = row0 + 32 * q + lane;
 #pragma unroll 1
-            for (int j = 0; j < 128 / 16; ++j) {
-                const int col = 128 * grp + 16 * j;
+            for (int j = 0; j < kGrp / 16; ++j) {
+                const int col = kGrp * grp + 16 * j;
                 if (tok0 + col >= p.M) break;   // warp-uniform
                 uint32_t v[16];
                 tc::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + col, v);
@@ -515,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     __syncthreads();
     if (warp == 1) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, kTmemCols);
+        tc::tmem_dealloc(tmem, C::TMEM);
     }
 }
 
@@ -551,17 +563,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 }  // namespace
 
-template <int T>
-static cudaError_t gemm_t(const gm::Args& a, const GemmPlan& pl, const CUtensorMap& map, cudaStream_t s) {
-    static_assert(gm::Pk<T>::SMEM <= 227 * 1024, "shared memory per CTA");
-    auto kern = gm::gemm_kernel<T>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, gm::Pk<T>::SMEM);
+template <int T, class C>
+static cudaError_t gemm_tc(gm::Args a, const GemmPlan& pl, const CUtensorMap& map, cudaStream_t s) {
+    using K = gm::Pk<T, C>;
+    // Activation ring: stages of one 64-wide k-block for every accumulator a
+    // token tile can fill; as many as fit (at most 16).
+    a.xst = (C::NACC > 1 && a.M > C::BNM ? C::NACC : 1) * a.nmma * gm::kBK * 2;
+    a.nsb = std::min(gm::kMaxXStages, (gm::kSmemMax - K::smem(0, 0)) / (a.xst + 16));
+    if (a.nsb < 1) return cudaErrorInvalidValue;
+    const int smem = K::smem(a.nsb, a.xst);
+    auto kern = gm::gemm_kernel<T, C>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, gm::kSmemMax);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((a.M + gm::kBN - 1) / gm::kBN), (unsigned)((a.rows + gm::kBM - 1) / gm::kBM),
+    cfg.gridDim = dim3((unsigned)((a.M + C::BN - 1) / C::BN), (unsigned)((a.rows + gm::kBM - 1) / gm::kBM),
                        (unsigned)pl.splits);
     cfg.blockDim = dim3(gm::kThreads);
-    cfg.dynamicSmemBytes = gm::Pk<T>::SMEM;
+    cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -571,8 +589,13 @@ static cudaError_t gemm_t(const gm::Args& a, const GemmPlan& pl, const CUtensorM
     return cudaLaunchKernelEx(&cfg, kern, map, a);
 }
 
+template <int T>
+static cudaError_t gemm_t(const gm::Args& a, const GemmPlan& pl, const CUtensorMap& map, cudaStream_t s) {
+    return pl.skinny ? gemm_tc<T, gm::Skinny<T>>(a, pl, map, s) : gemm_tc<T, gm::Wide>(a, pl, map, s);
+}
+
 namespace {
-int k_blocks_per_macro(int type) { return type == T_Q8_0 ? 2 : 4; }   // Pk<T>::KPM
+int k_blocks_per_macro(int type) { return type == T_Q8_0 ? 2 : 4; }   // PkGeo<T>::KPM
 }  // namespace
 
 // Split K when the (token, row) tiles leave SMs idle: among 1..16 splits
@@ -585,11 +608,13 @@ GemmPlan plan_gemm(int type, int64_t rows, int64_t cols, int64_t M, int sms) {
     if (rows <= 0 || cols <= 0 || M <= 0) return pl;
     const int64_t nkb = (cols + gm::kBK - 1) / gm::kBK;
     const int64_t kpm = k_blocks_per_macro(type);
-    pl.nmma = M > gm::kBNM ? gm::kBNM : (int)std::max<int64_t>(16, (M + 15) / 16 * 16);
-    const int64_t tiles = ((M + gm::kBN - 1) / gm::kBN) * ((rows + gm::kBM - 1) / gm::kBM);
+    pl.skinny = M <= gm::kSkinnyBN;
+    const int64_t bn = pl.skinny ? gm::kSkinnyBN : gm::Wide::BN;
+    pl.nmma = M > gm::Wide::BNM ? gm::Wide::BNM : (int)std::max<int64_t>(16, (M + 15) / 16 * 16);
+    const int64_t tiles = ((M + bn - 1) / bn) * ((rows + gm::kBM - 1) / gm::kBM);
     const int64_t S = std::max(sms, 1);
     int64_t best_cost = -1;
-    const int64_t max_split = M <= gm::kBN ? 16 : 1;
+    const int64_t max_split = M <= bn ? 16 : 1;
     for (int64_t sp = 1; sp <= max_split; ++sp) {
         const int64_t kps = ((nkb + sp - 1) / sp + kpm - 1) / kpm * kpm;
         const int64_t se = (nkb + kps - 1) / kps;

@@ -45,6 +45,7 @@ struct GemmPlan {
     int splits = 1;
     int kb_per_split = 0;   // 64-wide k-blocks per split
     int nmma = 256;         // MMA N
+    bool skinny = false;    // M <= 64: deep pipeline, one small accumulator
     int64_t ws_bytes = 0;
 };
 GemmPlan plan_gemm(int type, int64_t rows, int64_t cols, int64_t M, int sm_count);

@@ -35,6 +35,17 @@ __device__ __forceinline__ uint64_t sdesc_k128(uint32_t smem_addr) {
     return d;
 }
 
+// One lane of the (fully active) warp, chosen by the hardware: true there.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t is = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(is));
+    return is != 0;
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
                  "r"(ncols)

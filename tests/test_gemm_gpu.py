@@ -2,7 +2,8 @@
 bf16 activations: |Y - Y_ref| <= 5e-3 * sum|w x| per output.  Shapes cover
 one tile, ragged weight rows and token counts, a K whose last 64-block is
 half empty (32-weight blocks), every quant type, M from 1 to 1100, token
-tiles whose second 256-token accumulator is empty, partial or full."""
+tiles whose second 256-token accumulator is empty, partial or full, and the
+skinny pipeline (M <= 64) with fewer k-blocks than it has stages."""
 import numpy as np
 import pytest
 import torch
@@ -26,6 +27,13 @@ CASES = [
     ("Q6_K", 130, 512, 1100),    # three token tiles, ragged rows
     ("Q5_0", 128, 320, 513),     # second tile holds a single token
     ("Q4_0", 200, 1056, 77),
+    # Skinny pipeline (M <= 64): fewer k-blocks than operand stages, a half
+    # k-block at the end, ragged rows, one token.
+    ("Q4_K", 130, 256, 40),
+    ("Q8_0", 200, 96, 64),
+    ("Q5_0", 257, 2080, 48),
+    ("Q6_K", 129, 1536, 2),
+    ("Q4_0", 128, 64 * 32, 63),
 ]
 
 
