@@ -529,10 +529,15 @@ int oq_pack(int type, int64_t nblocks, const int16_t* codes, const int16_t* sc,
 /* A plain quantizer (input generation only; off the hot path)              */
 /* ------------------------------------------------------------------------ */
 
-/* Round half away from zero, in fp32. */
-static float rnd(float v) { return roundf(v); }
-
-static int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
+/* clamp(round(v), lo, hi): round half away from zero in fp32, clamp while
+ * still a float (so no out-of-range float reaches the int conversion; a NaN
+ * quotient takes the low end), then convert. */
+static int qclamp(float v, int lo, int hi) {
+    float r = roundf(v);
+    if (!(r >= (float)lo)) r = (float)lo;
+    if (r > (float)hi) r = (float)hi;
+    return (int)r;
+}
 
 /* Deterministic min/max quantizer.  The pages name the k-quant quantizer
  * (llama.cpp's quantize_row_q4_K) but do not give it; this is the plainest
@@ -546,7 +551,9 @@ static int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v
  *   Q8_0: d = max|w|/127, q = round(w/d) in -128..127.
  *   Q5_0: d = max|w|/15,  q = round(w/d) + 16 in 0..31.
  *   Q4_0: d = max|w|/7,   q = round(w/d) + 8 in 0..15.
- * All in fp32; a zero divisor gives the zero code. */
+ * All in fp32, each quotient an IEEE division; round() is half away from
+ * zero and the clamp is applied before the conversion to an integer (a NaN
+ * quotient gives the lowest code).  A zero divisor gives the zero code. */
 int oq_quantize(int type, const float* w, int64_t rows, int64_t cols, uint8_t* out) {
     int rc = check_shape(type, rows, cols);
     if (rc) return rc;
@@ -577,13 +584,13 @@ int oq_quantize(int type, const float* w, int64_t rows, int64_t cols, uint8_t* o
             dmb = oq_float_to_half(maxm / 63.0f);
             float d = oq_half_to_float(db), dmin = oq_half_to_float(dmb);
             for (int j = 0; j < 8; j++) {
-                s[j] = (int16_t)(d > 0.0f ? clampi((int)rnd(scf[j] / d), 0, 63) : 0);
-                m[j] = (uint8_t)(dmin > 0.0f ? clampi((int)rnd(mf[j] / dmin), 0, 63) : 0);
+                s[j] = (int16_t)(d > 0.0f ? qclamp(scf[j] / d, 0, 63) : 0);
+                m[j] = (uint8_t)(dmin > 0.0f ? qclamp(mf[j] / dmin, 0, 63) : 0);
                 float ds = d * (float)s[j];
                 float dm = dmin * (float)m[j];
                 for (int l = 0; l < 32; l++) {
                     float v = x[32 * j + l];
-                    q[32 * j + l] = (int16_t)(ds > 0.0f ? clampi((int)rnd((v + dm) / ds), 0, 15) : 0);
+                    q[32 * j + l] = (int16_t)(ds > 0.0f ? qclamp((v + dm) / ds, 0, 15) : 0);
                 }
             }
         } else if (type == OQ_Q6_K) {
@@ -600,11 +607,11 @@ int oq_quantize(int type, const float* w, int64_t rows, int64_t cols, uint8_t* o
             db = oq_float_to_half(maxs / 127.0f);
             float d = oq_half_to_float(db);
             for (int j = 0; j < 16; j++) {
-                s[j] = (int16_t)(d > 0.0f ? clampi((int)rnd(sf[j] / d), -128, 127) : 0);
+                s[j] = (int16_t)(d > 0.0f ? qclamp(sf[j] / d, -128, 127) : 0);
                 float ds = d * (float)s[j];
                 for (int l = 0; l < 16; l++) {
                     float v = x[16 * j + l];
-                    q[16 * j + l] = (int16_t)(ds != 0.0f ? clampi((int)rnd(v / ds) + 32, 0, 63) : 32);
+                    q[16 * j + l] = (int16_t)(ds != 0.0f ? qclamp(v / ds, -32, 31) + 32 : 32);
                 }
             }
         } else {
@@ -620,7 +627,7 @@ int oq_quantize(int type, const float* w, int64_t rows, int64_t cols, uint8_t* o
             db = oq_float_to_half(a / div);
             float d = oq_half_to_float(db);
             for (int l = 0; l < 32; l++)
-                q[l] = (int16_t)(d > 0.0f ? clampi((int)rnd(x[l] / d) + off, lo, hi) : off);
+                q[l] = (int16_t)(d > 0.0f ? qclamp(x[l] / d, lo - off, hi - off) + off : off);
         }
         rc = oq_pack(type, 1, q, s, m, &db, &dmb, out + i * bb);
         if (rc) return rc;

@@ -282,3 +282,62 @@ def test_quantizer_error_bounds(oracle_mod):
     step = (d[:, None] * sc[:, :8]).repeat(32, axis=1).reshape(-1)
     bound = step + np.repeat(dmin, 256) * 0.5 + 1e-6
     assert np.all(np.abs(dq.reshape(-1) - w.reshape(-1)) <= bound)
+
+
+def _codes(oracle_mod, t, W, nblocks):
+    return oracle_mod.unpack(t, W, nblocks)
+
+
+def test_quantizer_exact_codes_on_dyadic_grids(oracle_mod):
+    # Values on the grid d*(q - off) with the extreme code present give a
+    # scale d = max|w| / (top code) that is exact in fp16, so every code is
+    # recovered exactly: pins the divisor, the offset and the sign.
+    rng = np.random.default_rng(91)
+    for t, top, off, d_true, lo_q, hi_q in ((3, 127, 0, 2.0 ** -7, -127, 127),   # Q8_0
+                                            (4, 15, 16, 2.0 ** -4, 1, 31),       # Q5_0
+                                            (5, 7, 8, 2.0 ** -3, 1, 15)):        # Q4_0
+        q = rng.integers(lo_q, hi_q + 1, size=(4, 32))
+        q[:, 0] = hi_q
+        q[:, 1] = lo_q
+        w = ((q - off) * d_true).astype(np.float32)
+        W = oracle_mod.quantize(t, w.reshape(1, -1))
+        codes, _, _, d, _ = _codes(oracle_mod, t, W, 4)
+        assert np.all(d == d_true)
+        assert np.array_equal(codes[:, :32], q)
+
+
+def test_quantizer_exact_codes_k_quants(oracle_mod):
+    # Q4_K: every sub-block spans [lo, hi] with lo < 0 in 15 equal steps, so
+    # sc = m = 63 and the code is the step count (the fp16 rounding of d and
+    # dmin moves (w + dmin*m) / (d*sc) by < 0.01).  Pins the sign of the min
+    # term, the 6-bit scale packing and the nibble order.
+    rng = np.random.default_rng(92)
+    lo, hi = -0.37, 0.81
+    k = rng.integers(0, 16, size=256)
+    k[::32] = 0
+    k[1::32] = 15
+    w = (lo + k * (hi - lo) / 15.0).astype(np.float32)
+    W = oracle_mod.quantize(1, w.reshape(1, -1))
+    codes, sc, mins, d, dmin = _codes(oracle_mod, 1, W, 1)
+    assert np.array_equal(codes[0], k)
+    assert np.all(sc[0, :8] == 63) and np.all(mins[0] == 63)
+    # Q6_K: each 16-group has max |w| = A, values A*k/32 for k in -32..31:
+    # sc = 127 and the code is k + 32.
+    A = 0.23
+    k6 = rng.integers(-32, 32, size=256)
+    k6[::16] = -32
+    w6 = (A * k6 / 32.0).astype(np.float32)
+    W6 = oracle_mod.quantize(2, w6.reshape(1, -1))
+    c6, s6, _, _, _ = _codes(oracle_mod, 2, W6, 1)
+    assert np.array_equal(c6[0], k6 + 32)
+    assert np.all(s6[0, :16] == 127)
+
+
+def test_quantizer_zero_blocks(oracle_mod):
+    # An all-zero block takes the zero-divisor path: d = 0 and the offset code.
+    for t, n, code in ((1, 256, 0), (2, 256, 32), (3, 32, 0), (4, 32, 16), (5, 32, 8)):
+        W = oracle_mod.quantize(t, np.zeros((1, n), np.float32))
+        codes, sc, mins, d, dmin = _codes(oracle_mod, t, W, 1)
+        assert np.all(codes[0, :n] == code) and d[0] == 0.0
+        if t == 1:
+            assert dmin[0] == 0.0 and not sc.any() and not mins.any()
