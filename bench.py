@@ -300,6 +300,7 @@ def run_gpu(args):
             gemm["frac_of_bf16_sustained"] = round(gemm["tflops"] / float(pk["bf16_tflops_sustained"]), 4)
         except Exception:
             pass
+    quant = run_quantize(dev, hbm_peak) if (rank == 0 and not args.no_quant) else None
     cpu = cpu_baseline(layer) if (rank == 0 and world == 1 and not args.no_cpu) else None
     traffic = recorded_traffic()
     if rank == 0:
@@ -330,6 +331,7 @@ def run_gpu(args):
             "gemm": gemm,
             "stack": stack,
             "ffn_sweep": sweep,
+            "quantize": quant,
         }
         print(json.dumps(out))
     if world > 1:
@@ -432,6 +434,41 @@ def run_ffn_gemm(dev, M: int, reps: int = 20):
                    "tflops": round(2.0 * M * rows * cols / (us * 1e-6) / 1e12, 2)}
         del Ws, X, Y, ws
     return {"workload": f"Llama-3-8B FFN Q4_K, qk_gemm at M={M}", "per_matrix": out}
+
+
+def run_quantize(dev, hbm_peak=None, reps: int = 20):
+    """The write side: qk_quantize of one 14336x4096 fp32 matrix (N(0, 0.02),
+    235 MB, beyond L2) into each block type.  Per type: 2 warm-up launches,
+    then `reps` launches back to back between two CUDA events.  GB/s counts
+    the 4 bytes read and the packed bytes written per weight."""
+    import torch
+    import gguf_quant_dequant_gb300 as qk
+    import synth
+    rows, cols = 14336, 4096
+    stream = torch.cuda.current_stream()
+    g = torch.Generator(device=dev)
+    g.manual_seed(2024)
+    w = torch.randn((rows, cols), device=dev, generator=g) * 0.02
+    per = {}
+    for name in ("Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0"):
+        t = synth.TYPE_IDS[name]
+        o = torch.empty(rows * qk.row_bytes(t, cols), dtype=torch.uint8, device=dev)
+        for _ in range(2):
+            qk.quantize(t, w, out=o)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            qk.quantize(t, w, out=o)
+        e1.record(stream)
+        e1.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        gbs = (4 * rows * cols + o.numel()) / (us * 1e-6) / 1e9
+        per[name] = {"us": round(us, 2), "gbs": round(gbs, 1)}
+        if hbm_peak:
+            per[name]["frac_of_hbm"] = round(gbs / hbm_peak, 4)
+        del o
+    del w
+    return {"workload": "qk_quantize, 14336x4096 fp32 N(0, 0.02) -> each block type", "per_type": per}
 
 
 def _graph_time_us(fn, reps: int = 20, warm: int = 3) -> float:
@@ -680,6 +717,9 @@ def main():
     ap.add_argument("--no-sweep", action="store_true", help="skip the Llama-3 FFN batch sweep")
     ap.add_argument("--gemm-only", action="store_true",
                     help="run only the prefill GEMM leg and print its JSON (for profiling)")
+    ap.add_argument("--no-quant", action="store_true", help="skip the quantizer leg")
+    ap.add_argument("--quantize-only", action="store_true",
+                    help="run only the quantizer leg and print its JSON (for profiling)")
     ap.add_argument("--ffn-gemm", type=int, default=0, metavar="M",
                     help="run only the small-batch GEMM over the Llama-3 FFN at batch M (for profiling)")
     ap.add_argument("--min-warmup-s", type=float, default=1.0,
@@ -689,13 +729,15 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
-    elif args.gemm_only or args.ffn_gemm > 0:
+    elif args.gemm_only or args.ffn_gemm > 0 or args.quantize_only:
         import torch
         from gguf_quant_dequant_gb300 import build as qkbuild
         qkbuild.build()
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
-        if args.ffn_gemm > 0:
+        if args.quantize_only:
+            print(json.dumps(run_quantize(dev, reps=args.steps)))
+        elif args.ffn_gemm > 0:
             print(json.dumps(run_ffn_gemm(dev, args.ffn_gemm, reps=args.steps)))
         else:
             print(json.dumps(run_gemm_bench(dev, reps=args.steps)))

@@ -35,6 +35,7 @@ SIGNATURES = {
     "qk_block_elems": (_int, [_int]),
     "qk_row_bytes": (_sz, [_int, _i64]),
     "qk_dequant": (_int, [_int, _p, _i64, _i64, _p, _int, _p]),
+    "qk_quantize": (_int, [_int, _p, _i64, _i64, _p, _p]),
     "qk_gemv_workspace": (_sz, [_int, _i64, _i64, _i64]),
     "qk_gemv": (_int, [_int, _p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
     "qk_gemv_noalloc": (_int, [_int, _p, _i64, _i64, _p, _i64, _p, _p]),
@@ -107,6 +108,17 @@ def dequant(t: int, W, rows: int, cols: int, out=None, bf16: bool = False, strea
         out = torch.empty((rows, cols), dtype=torch.bfloat16 if bf16 else torch.float32, device=W.device)
     _check(load().qk_dequant(t, _ptr(W), rows, cols, _ptr(out), OUT_BF16 if bf16 else OUT_F32,
                              _stream(stream)), "qk_dequant")
+    return out
+
+
+def quantize(t: int, w, out=None, stream=None):
+    """w: fp32 CUDA tensor [rows, cols] -> out: uint8 packed blocks, rows *
+    row_bytes(t, cols) bytes (allocated when not given)."""
+    import torch
+    rows, cols = w.shape
+    if out is None:
+        out = torch.empty(rows * row_bytes(t, cols), dtype=torch.uint8, device=w.device)
+    _check(load().qk_quantize(t, _ptr(w), rows, cols, _ptr(out), _stream(stream)), "qk_quantize")
     return out
 
 

@@ -99,6 +99,31 @@ size_t qk_row_bytes(int type, int64_t cols);
 qk_status qk_dequant(int type, const void* W, int64_t rows, int64_t cols,
                      void* out, int out_dtype, void* stream);
 
+/* Quantize fp32 weights into packed blocks: the write side of the format.
+ * The pages name the k-quant quantizer ("12 -- llama.cpp / GGUF / Local
+ * Inference Mastery", reading list: quantize_row_q4_K) without giving it,
+ * and describe plain quantization as minimising the weight-space error
+ * ("Hitchhiker's Guide -- Lab 01", 11.3); this is the plain min/max scheme,
+ * each quotient an IEEE fp32 division and each code clamp(round half away
+ * from zero(quotient)):
+ *   Q4_K per 32-weight sub-block: lo = min(0, min w), hi = max w,
+ *        sc_f = (hi - lo)/15, m_f = -lo; d = fp16(max sc_f / 63),
+ *        dmin = fp16(max m_f / 63); sc = cr(sc_f/d, 0..63),
+ *        m = cr(m_f/dmin, 0..63); q = cr((w + dmin*m) / (d*sc), 0..15).
+ *   Q6_K per 16 weights: s = max|w| / 32, d = fp16(max s / 127),
+ *        sc = cr(s/d, -128..127), q = cr(w / (d*sc), -32..31) + 32.
+ *   Q8_0 / Q5_0 / Q4_0 per 32: d = fp16(max|w| / 127 | 15 | 7),
+ *        q = cr(w/d) + 0 | 16 | 8, clamped to the code range.
+ * A zero divisor gives the offset code; NaN inputs are not rejected (they are
+ * skipped by the maxima and a NaN quotient takes the lowest code).
+ *   w   fp32 [rows, cols] row-major, 16-byte aligned.
+ *   out rows * qk_row_bytes(type, cols) bytes, 4-byte aligned; fully
+ *       overwritten.
+ * Deterministic; the bytes do not depend on the launch.  rows == 0 or
+ * cols == 0 queues nothing.  Errors: QK_ERR_TYPE, QK_ERR_SHAPE (cols not a
+ * multiple of the block size, negative sizes), QK_ERR_NULL, QK_ERR_ALIGN. */
+qk_status qk_quantize(int type, const float* w, int64_t rows, int64_t cols, void* out, void* stream);
+
 /* Workspace bytes qk_gemv needs for this problem on the current device (0
  * when it needs none).  The value depends on the device's SM count. */
 size_t qk_gemv_workspace(int type, int64_t rows, int64_t cols, int64_t M);

@@ -105,6 +105,23 @@ def test_batch_argument_errors_are_caught_on_host(lib):
     assert call(qk.Q4_K, 2, [None, None], [0, 0], 256, None, [None, None]) == 0
 
 
+def test_quantize_argument_errors_are_caught_on_host(lib):
+    fake = ctypes.c_void_p(0x10000)          # 16-byte aligned, never dereferenced
+    odd4 = ctypes.c_void_p(0x10004)          # 4-byte aligned only
+    odd2 = ctypes.c_void_p(0x10002)          # 2-byte aligned only
+    assert lib.qk_quantize(0, fake, 4, 256, fake, None) == 1
+    assert lib.qk_quantize(qk.Q4_K, fake, 4, 100, fake, None) == 2
+    assert lib.qk_quantize(qk.Q8_0, fake, -1, 32, fake, None) == 2
+    assert lib.qk_quantize(qk.Q8_0, fake, 1 << 40, 1 << 10, fake, None) == 2   # 2^50 weights
+    assert b"too large" in lib.qk_last_error()
+    assert lib.qk_quantize(qk.Q4_K, None, 4, 256, fake, None) == 4
+    assert lib.qk_quantize(qk.Q4_K, fake, 4, 256, None, None) == 4
+    assert lib.qk_quantize(qk.Q4_K, odd4, 4, 256, fake, None) == 3     # w needs 16 bytes
+    assert lib.qk_quantize(qk.Q4_K, fake, 4, 256, odd2, None) == 3     # out needs 4 bytes
+    assert lib.qk_quantize(qk.Q5_0, fake, 0, 64, fake, None) == 0       # nothing to do
+    assert lib.qk_quantize(qk.Q5_0, fake, 3, 0, fake, None) == 0
+
+
 def test_gemm_row_tile_limit_is_checked_on_host(lib):
     fake = ctypes.c_void_p(0x10000)
     assert lib.qk_gemm(qk.Q4_K, fake, 65535 * 128 + 1, 256, fake, 4, fake, None, 0, None) == 2
