@@ -172,6 +172,27 @@ def gemv(t: int, W: np.ndarray, rows: int, cols: int, x: np.ndarray):
     return y, S
 
 
+def silu(z) -> np.ndarray:
+    """SiLU(z) = z / (1 + e^-z) in fp64: the gate nonlinearity of the SwiGLU
+    feed-forward ("How LLM Inference Engines Work", "SwiGLU Feed-Forward
+    Network"; the page names SiLU without writing it out, this is its standard
+    definition z * sigmoid(z)).  e^-z overflowing to inf gives -0."""
+    z = np.asarray(z, np.float64)
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def swiglu(t: int, Wg: np.ndarray, Wu: np.ndarray, rows: int, cols: int, x: np.ndarray):
+    """Decode SwiGLU gate (same page and section): h = SiLU(Wg x) * (Wu x)
+    over the exactly dequantized weights, fp64.  x fp32 [cols].  Returns
+    (h, g, u, Sg, Su), each fp64 [rows]; Sg, Su = sum_k |w x| of the two
+    products (for the tolerance)."""
+    g, Sg = gemv(t, Wg, rows, cols, x)
+    u, Su = gemv(t, Wu, rows, cols, x)
+    g, u, Sg, Su = g[0], u[0], Sg[0], Su[0]
+    return silu(g) * u, g, u, Sg, Su
+
+
 def gemm_bf16(t: int, W: np.ndarray, rows: int, cols: int, X_bits: np.ndarray):
     """X_bits uint16 bf16 bit patterns [M, cols] -> (Y fp64 [M, rows], S)."""
     W = np.ascontiguousarray(W, dtype=np.uint8)

@@ -341,3 +341,40 @@ def test_quantizer_zero_blocks(oracle_mod):
         assert np.all(codes[0, :n] == code) and d[0] == 0.0
         if t == 1:
             assert dmin[0] == 0.0 and not sc.any() and not mins.any()
+
+
+# ------------------------------------------------------------ SwiGLU --
+
+def test_silu_against_the_logistic_function(oracle_mod):
+    # SiLU(z) = z * sigmoid(z); sigmoid from scipy's expit (a library routine).
+    special = pytest.importorskip("scipy.special")
+    z = np.concatenate([np.linspace(-40.0, 40.0, 4001), [-1e3, -745.5, 0.0, 1e-300, 745.5, 1e3]])
+    s = oracle_mod.silu(z)
+    ref = z * special.expit(z)
+    assert np.allclose(s, ref, rtol=4e-16, atol=1e-300)
+    assert s[z == 0.0][0] == 0.0 and s[-1] == 1e3 and s[z == -1e3][0] == 0.0   # e^1000 overflows: -0
+
+
+def test_silu_reflection_identity(oracle_mod):
+    # SiLU(-z) = -z (1 - sigmoid(z)) = SiLU(z) - z.
+    z = np.linspace(-30.0, 30.0, 601)
+    assert np.allclose(oracle_mod.silu(-z), oracle_mod.silu(z) - z, rtol=1e-14, atol=1e-13)
+
+
+def test_swiglu_on_an_exact_block(oracle_mod):
+    # Q8_0 with d = 1 (fp16 0x3C00): w = q exactly, so g and u are exact
+    # integer dot products; h = SiLU(g) * u from the closed form.
+    rng = np.random.default_rng(93)
+    rows, cols = 3, 64
+    def mat(seed):
+        q = np.random.default_rng(seed).integers(-5, 6, size=(rows, cols))
+        blk = np.zeros((rows, cols // 32, 34), np.uint8)
+        blk[:, :, 0], blk[:, :, 1] = 0x00, 0x3C
+        blk[:, :, 2:] = q.reshape(rows, cols // 32, 32).astype(np.int8).view(np.uint8)
+        return blk.reshape(-1), q
+    (Wg, qg), (Wu, qu) = mat(1), mat(2)
+    x = rng.integers(-3, 4, size=cols).astype(np.float32)
+    h, g, u, _, _ = oracle_mod.swiglu(3, Wg, Wu, rows, cols, x)
+    ge, ue = qg @ x.astype(np.float64), qu @ x.astype(np.float64)
+    assert np.array_equal(g, ge) and np.array_equal(u, ue)
+    assert np.allclose(h, ge / (1.0 + np.exp(-ge)) * ue, rtol=0, atol=0)
