@@ -301,6 +301,7 @@ def run_gpu(args):
         except Exception:
             pass
     quant = run_quantize(dev, hbm_peak) if (rank == 0 and not args.no_quant) else None
+    swi = run_swiglu(dev, hbm_peak) if (rank == 0 and not args.no_swiglu) else None
     cpu = cpu_baseline(layer) if (rank == 0 and world == 1 and not args.no_cpu) else None
     traffic = recorded_traffic()
     if rank == 0:
@@ -332,6 +333,7 @@ def run_gpu(args):
             "stack": stack,
             "ffn_sweep": sweep,
             "quantize": quant,
+            "swiglu": swi,
         }
         print(json.dumps(out))
     if world > 1:
@@ -434,6 +436,47 @@ def run_ffn_gemm(dev, M: int, reps: int = 20):
                    "tflops": round(2.0 * M * rows * cols / (us * 1e-6) / 1e12, 2)}
         del Ws, X, Y, ws
     return {"workload": f"Llama-3-8B FFN Q4_K, qk_gemm at M={M}", "per_matrix": out}
+
+
+def run_swiglu(dev, hbm_peak=None):
+    """Decode SwiGLU gate h = SiLU(Wg x) * (Wu x) in Q4_K for the Llama-7B
+    (11008x4096) and Llama-3-8B (14336x4096) FFN: the fused qk_gemv_swiglu
+    (one launch, h only) against qk_gemv_batch(gate, up) followed by
+    torch's silu(g) * u.  Four weight copies rotate (beyond L2), each timed
+    as a CUDA graph.  GB/s counts both matrices' packed bytes + x + h."""
+    import torch
+    import gguf_quant_dequant_gb300 as qk
+    import synth
+    t = qk.Q4_K
+    out = {}
+    for label, rows, cols in (("llama7b_gate_up", 11008, 4096), ("llama3_8b_gate_up", 14336, 4096)):
+        nc = 4
+        Wg = [synth.random_blocks_torch("Q4_K", rows, cols, 9100 + k, dev) for k in range(nc)]
+        Wu = [synth.random_blocks_torch("Q4_K", rows, cols, 9200 + k, dev) for k in range(nc)]
+        x = torch.randn(cols, device=dev)
+        h = torch.empty(rows, device=dev)
+        g = torch.empty(rows, device=dev)
+        u = torch.empty(rows, device=dev)
+
+        def fused():
+            for k in range(nc):
+                qk.gemv_swiglu(t, Wg[k], Wu[k], rows, cols, x, h=h)
+
+        def unfused():
+            for k in range(nc):
+                qk.gemv_batch(t, [Wg[k], Wu[k]], [rows, rows], cols, x, ys=[g, u])
+                torch.mul(torch.nn.functional.silu(g), u, out=h)
+
+        us_f = _graph_time_us(fused) / nc
+        us_u = _graph_time_us(unfused) / nc
+        nbytes = 2 * Wg[0].numel() + 4 * cols + 4 * rows
+        out[label] = {"fused_us": round(us_f, 2), "unfused_us": round(us_u, 2),
+                      "fused_gbs": round(nbytes / (us_f * 1e-6) / 1e9, 1),
+                      "unfused_gbs": round(nbytes / (us_u * 1e-6) / 1e9, 1)}
+        if hbm_peak:
+            out[label]["fused_frac_of_hbm"] = round(nbytes / (us_f * 1e-6) / 1e9 / hbm_peak, 4)
+        del Wg, Wu
+    return {"workload": "decode SwiGLU gate, Q4_K, batch 1", "per_shape": out}
 
 
 def run_quantize(dev, hbm_peak=None, reps: int = 20):
@@ -718,6 +761,9 @@ def main():
     ap.add_argument("--gemm-only", action="store_true",
                     help="run only the prefill GEMM leg and print its JSON (for profiling)")
     ap.add_argument("--no-quant", action="store_true", help="skip the quantizer leg")
+    ap.add_argument("--no-swiglu", action="store_true", help="skip the fused SwiGLU leg")
+    ap.add_argument("--swiglu-only", action="store_true",
+                    help="run only the fused SwiGLU leg and print its JSON (for profiling)")
     ap.add_argument("--quantize-only", action="store_true",
                     help="run only the quantizer leg and print its JSON (for profiling)")
     ap.add_argument("--ffn-gemm", type=int, default=0, metavar="M",
@@ -729,13 +775,15 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
-    elif args.gemm_only or args.ffn_gemm > 0 or args.quantize_only:
+    elif args.gemm_only or args.ffn_gemm > 0 or args.quantize_only or args.swiglu_only:
         import torch
         from gguf_quant_dequant_gb300 import build as qkbuild
         qkbuild.build()
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
-        if args.quantize_only:
+        if args.swiglu_only:
+            print(json.dumps(run_swiglu(dev)))
+        elif args.quantize_only:
             print(json.dumps(run_quantize(dev, reps=args.steps)))
         elif args.ffn_gemm > 0:
             print(json.dumps(run_ffn_gemm(dev, args.ffn_gemm, reps=args.steps)))

@@ -41,6 +41,7 @@ SIGNATURES = {
     "qk_gemv_noalloc": (_int, [_int, _p, _i64, _i64, _p, _i64, _p, _p]),
     "qk_gemv_batch": (_int, [_int, _int, ctypes.POINTER(_p), ctypes.POINTER(_i64), _i64, _p,
                              ctypes.POINTER(_p), _p]),
+    "qk_gemv_swiglu": (_int, [_int, _p, _p, _i64, _i64, _p, _p, _p]),
     "qk_gemm_workspace": (_sz, [_int, _i64, _i64, _i64]),
     "qk_gemm": (_int, [_int, _p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
     "qk_unpack": (_int, [_int, _p, _i64, _p, _p, _p, _p, _p, _p]),
@@ -120,6 +121,16 @@ def quantize(t: int, w, out=None, stream=None):
         out = torch.empty(rows * row_bytes(t, cols), dtype=torch.uint8, device=w.device)
     _check(load().qk_quantize(t, _ptr(w), rows, cols, _ptr(out), _stream(stream)), "qk_quantize")
     return out
+
+
+def gemv_swiglu(t: int, Wg, Wu, rows: int, cols: int, x, h=None, stream=None):
+    """Decode SwiGLU: x fp32 CUDA [cols] -> h = SiLU(Wg x) * (Wu x), fp32 [rows]."""
+    import torch
+    if h is None:
+        h = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _check(load().qk_gemv_swiglu(t, _ptr(Wg), _ptr(Wu), rows, cols, _ptr(x), _ptr(h), _stream(stream)),
+           "qk_gemv_swiglu")
+    return h
 
 
 def gemv_workspace(t: int, rows: int, cols: int, M: int) -> int:

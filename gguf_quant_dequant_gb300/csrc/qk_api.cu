@@ -236,6 +236,35 @@ qk_status qk_gemv_batch(int type, int n_mat, const void* const* W, const int64_t
     return QK_OK;
 }
 
+qk_status qk_gemv_swiglu(int type, const void* Wg, const void* Wu, int64_t rows, int64_t cols, const float* x,
+                         float* h, void* stream) {
+    qk_status st = check_matrix(type, Wg, rows, cols);
+    if (st != QK_OK) return st;
+    st = check_matrix(type, Wu, rows, cols);
+    if (st != QK_OK) return st;
+    if (rows == 0) return QK_OK;
+    if (!h) return fail(QK_ERR_NULL, "h is NULL");
+    if (!aligned(h, 4)) return fail(QK_ERR_ALIGN, "h is not 4-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cols == 0) {   // g = u = 0, SiLU(0) * 0 = 0
+        cudaError_t e = cudaMemsetAsync(h, 0, (size_t)rows * sizeof(float), s);
+        if (e != cudaSuccess) return cuda_fail(e, "qk_gemv_swiglu zero fill");
+        return QK_OK;
+    }
+    if (!x) return fail(QK_ERR_NULL, "x is NULL");
+    if (!aligned(x, 16)) return fail(QK_ERR_ALIGN, "x is not 16-byte aligned");
+    int sms = 0;
+    st = device_state(nullptr, &sms);
+    if (st != QK_OK) return st;
+    if (qk::gemv5_ring_pairs(type, 1, &rows, cols, sms) == 0)
+        return fail(QK_ERR_SHAPE, "cols=%lld is too large for the decode kernel", (long long)cols);
+    cudaError_t e = qk::launch_gemv5_swiglu(type, static_cast<const uint8_t*>(Wg), static_cast<const uint8_t*>(Wu),
+                                            rows, cols, x, h, sms, s);
+    if (e != cudaSuccess) return cuda_fail(e, "qk_gemv_swiglu launch");
+    g_last_error.clear();
+    return QK_OK;
+}
+
 size_t qk_gemm_workspace(int type, int64_t rows, int64_t cols, int64_t M) {
     if (!known_type(type) || rows <= 0 || cols <= 0 || M <= 0 || cols % block_elems(type) != 0) return 0;
     return (size_t)qk::plan_gemm(type, rows, cols, M, sm_count_or_default()).ws_bytes;

@@ -177,7 +177,9 @@ __device__ __forceinline__ void tail_fill(uint8_t* slot, const uint8_t* base, ui
 }
 
 // NP = ring depth in row pairs (one cp.async group per pair).
-template <int T, int NP>
+// SWI: one matrix pair, W[0] = gate and W[1] = up of the same shape, y[0] = h
+// = SiLU(gate x) * (up x).
+template <int T, int NP, bool SWI>
 __global__ void __launch_bounds__(kThreads, 2) gemv5_kernel(const Args p) {
     using C = Cfg<T>;
     constexpr int NIT = ((C::SEG + 30) / 16 + 31) / 32;   // 16-byte copies per lane per row segment, at most
@@ -219,7 +221,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv5_kernel(const Args p) {
     };
 
     bool prepped = false;
-    for (int64_t cb = r_begin; cb < r_end; cb += p.chunk) {
+    // SwiGLU: each chunk of rows is walked twice, through the gate matrix and
+    // then the up matrix; the gate results wait in h (written and read back
+    // by the same thread) until the up pass finishes the row.
+    constexpr int npass = SWI ? 2 : 1;
+    for (int64_t cb = r_begin; cb < r_end; cb += p.chunk)
+    for (int pass = 0; pass < npass; ++pass) {
         const int nrc = (int)min((int64_t)p.chunk, r_end - cb);
         const int npr = (nrc + 1) >> 1;                 // row pairs per slice (the last may be single)
         const int U = npr * p.nsl;
@@ -227,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv5_kernel(const Args p) {
         const int nu = (int)((int64_t)(warp + 1) * U / kWarps) - u0;
         // 32-bit byte offsets relative to an aligned base at the chunk's first row.
         const int64_t cboff = cb * (int64_t)rb;
-        const uint8_t* base = Wm + (cboff & ~(int64_t)15);
+        const uint8_t* base = (SWI && pass ? p.W[1] : Wm) + (cboff & ~(int64_t)15);
         const uint8_t* gl = base + 16 * lane;
         const uint32_t mis = (uint32_t)(cboff & 15);
         const int64_t lim64 = total16 - (cboff & ~(int64_t)15);
@@ -328,7 +335,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv5_kernel(const Args p) {
         for (int t = threadIdx.x; t < nrc; t += kThreads) {
             float acc = 0.0f;
             for (int s = 0; s < p.nsl; ++s) acc += red[s * nrc + t];
-            ym[cb + t] = acc;
+            if (!SWI || pass == 0) {
+                ym[cb + t] = acc;
+            } else {   // h = SiLU(g) * u, SiLU(g) = g / (1 + e^-g)
+                const float g = ym[cb + t];
+                ym[cb + t] = g / (1.0f + expf(-g)) * acc;
+            }
         }
         __syncthreads();   // partials consumed before the next chunk writes them
     }
@@ -401,9 +413,9 @@ Plan5 plan5(int type, int n, const int64_t* rows, int64_t cols, int sms) {
     return p;
 }
 
-template <int T, int NP>
+template <int T, int NP, bool SWI>
 cudaError_t launch5_np(const gv5::Args& a, const Plan5& pl, cudaStream_t s) {
-    auto kern = gv5::gemv5_kernel<T, NP>;
+    auto kern = gv5::gemv5_kernel<T, NP, SWI>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, gv5::kSmemBudget);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -419,13 +431,25 @@ cudaError_t launch5_np(const gv5::Args& a, const Plan5& pl, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int T>
+template <int T, bool SWI>
 cudaError_t launch5_t(const gv5::Args& a, const Plan5& pl, cudaStream_t s) {
     switch (pl.np) {
-    case 2: return launch5_np<T, 2>(a, pl, s);
-    case 3: return launch5_np<T, 3>(a, pl, s);
-    default: return launch5_np<T, 4>(a, pl, s);
+    case 2: return launch5_np<T, 2, SWI>(a, pl, s);
+    case 3: return launch5_np<T, 3, SWI>(a, pl, s);
+    default: return launch5_np<T, 4, SWI>(a, pl, s);
     }
+}
+
+template <bool SWI>
+cudaError_t launch5_type(int type, const gv5::Args& a, const Plan5& pl, cudaStream_t s) {
+    switch (type) {
+    case T_Q4_K: return launch5_t<T_Q4_K, SWI>(a, pl, s);
+    case T_Q6_K: return launch5_t<T_Q6_K, SWI>(a, pl, s);
+    case T_Q8_0: return launch5_t<T_Q8_0, SWI>(a, pl, s);
+    case T_Q5_0: return launch5_t<T_Q5_0, SWI>(a, pl, s);
+    case T_Q4_0: return launch5_t<T_Q4_0, SWI>(a, pl, s);
+    }
+    return cudaErrorInvalidValue;
 }
 
 int64_t row_bytes_of(int type, int64_t cols) {
@@ -466,14 +490,32 @@ cudaError_t launch_gemv5(int type, int n, const uint8_t* const* W, const int64_t
         a.rows_r[i] = (int)pl.rows_r[i];
     }
     for (int i = 0; i <= gv5::kMaxGroup; ++i) a.cta0[i] = pl.cta0[i];
-    switch (type) {
-    case T_Q4_K: return launch5_t<T_Q4_K>(a, pl, s);
-    case T_Q6_K: return launch5_t<T_Q6_K>(a, pl, s);
-    case T_Q8_0: return launch5_t<T_Q8_0>(a, pl, s);
-    case T_Q5_0: return launch5_t<T_Q5_0>(a, pl, s);
-    case T_Q4_0: return launch5_t<T_Q4_0>(a, pl, s);
-    }
-    return cudaErrorInvalidValue;
+    return launch5_type<false>(type, a, pl, s);
 }
+
+cudaError_t launch_gemv5_swiglu(int type, const uint8_t* Wg, const uint8_t* Wu, int64_t rows, int64_t cols,
+                                const float* x, float* h, int sms, cudaStream_t s) {
+    const Plan5 pl = plan5(type, 1, &rows, cols, sms);
+    if (pl.np == 0) return cudaErrorInvalidValue;
+    if (pl.grid == 0) return cudaSuccess;
+    gv5::Args a = {};
+    a.x = x;
+    a.cols = cols;
+    a.row_bytes = (uint32_t)row_bytes_of(type, cols);
+    a.n = 1;
+    a.nsl = pl.nsl;
+    a.chunk = pl.chunk;
+    a.off_ring = pl.off_ring;
+    a.off_red = pl.off_red;
+    a.W[0] = Wg;
+    a.W[1] = Wu;
+    a.y[0] = h;
+    a.rows[0] = rows;
+    a.rows_q[0] = pl.rows_q[0];
+    a.rows_r[0] = (int)pl.rows_r[0];
+    for (int i = 0; i <= gv5::kMaxGroup; ++i) a.cta0[i] = pl.cta0[i];
+    return launch5_type<true>(type, a, pl, s);
+}
+
 
 }  // namespace qk

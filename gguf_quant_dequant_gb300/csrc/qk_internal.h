@@ -35,6 +35,9 @@ GemvPlan plan_gemv(int type, int64_t rows, int64_t cols, int64_t M, int sm_count
 int gemv5_ring_pairs(int type, int n, const int64_t* rows, int64_t cols, int sms);
 cudaError_t launch_gemv5(int type, int n, const uint8_t* const* W, const int64_t* rows, int64_t cols, const float* x,
                          float* const* y, int sms, cudaStream_t s);
+// Decode SwiGLU: h = SiLU(Wg x) * (Wu x), both matrices walked by the same CTAs.
+cudaError_t launch_gemv5_swiglu(int type, const uint8_t* Wg, const uint8_t* Wu, int64_t rows, int64_t cols,
+                                const float* x, float* h, int sms, cudaStream_t s);
 cudaError_t launch_gemv(int type, const GemvPlan& plan, const uint8_t* W, int64_t rows, int64_t cols,
                         const float* x, int64_t M, float* y, float* ws, unsigned* status, cudaStream_t s);
 

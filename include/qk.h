@@ -124,6 +124,23 @@ qk_status qk_dequant(int type, const void* W, int64_t rows, int64_t cols,
  * multiple of the block size, negative sizes), QK_ERR_NULL, QK_ERR_ALIGN. */
 qk_status qk_quantize(int type, const float* w, int64_t rows, int64_t cols, void* out, void* stream);
 
+/* Fused decode FFN gate: h[n] = SiLU(g[n]) * u[n] with g = Wg x, u = Wu x
+ * (batch 1) and SiLU(z) = z / (1 + e^-z) ("How LLM Inference Engines
+ * Work", "SwiGLU Feed-Forward Network": the gate projection passes through
+ * SiLU and multiplies the up projection element-wise; SiLU is not written
+ * out on the page, the standard z * sigmoid(z) is used).  One launch: the
+ * same CTAs walk their rows of Wg and then of Wu (x prepared once), and
+ * write h only; g and u never reach memory.
+ *   Wg, Wu [rows, cols] packed blocks of the same type, 16-byte aligned.
+ *   x      fp32 [cols], 16-byte aligned.
+ *   h      fp32 [rows], 4-byte aligned; fully overwritten.
+ * Accuracy: g and u each as qk_gemv (1e-4 * sum|w x| + 1e-6), then the fp32
+ * epilogue (expf, one division, one product).  QK_ERR_SHAPE when cols is too
+ * large for the decode kernel's shared memory (the same limit as qk_gemv_batch).
+ * rows == 0 queues nothing; cols == 0 zero-fills h. */
+qk_status qk_gemv_swiglu(int type, const void* Wg, const void* Wu, int64_t rows, int64_t cols,
+                         const float* x, float* h, void* stream);
+
 /* Workspace bytes qk_gemv needs for this problem on the current device (0
  * when it needs none).  The value depends on the device's SM count. */
 size_t qk_gemv_workspace(int type, int64_t rows, int64_t cols, int64_t M);

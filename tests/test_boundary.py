@@ -122,6 +122,22 @@ def test_quantize_argument_errors_are_caught_on_host(lib):
     assert lib.qk_quantize(qk.Q5_0, fake, 3, 0, fake, None) == 0
 
 
+def test_swiglu_argument_errors_are_caught_on_host(lib):
+    fake = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10008)
+    odd2 = ctypes.c_void_p(0x10002)
+    assert lib.qk_gemv_swiglu(9, fake, fake, 4, 256, fake, fake, None) == 1
+    assert lib.qk_gemv_swiglu(qk.Q4_K, fake, fake, 4, 100, fake, fake, None) == 2
+    assert lib.qk_gemv_swiglu(qk.Q4_K, None, fake, 4, 256, fake, fake, None) == 4
+    assert lib.qk_gemv_swiglu(qk.Q4_K, fake, None, 4, 256, fake, fake, None) == 4
+    assert lib.qk_gemv_swiglu(qk.Q4_K, fake, odd, 4, 256, fake, fake, None) == 3
+    assert lib.qk_gemv_swiglu(qk.Q4_K, fake, fake, 4, 256, fake, None, None) == 4
+    assert lib.qk_gemv_swiglu(qk.Q4_K, fake, fake, 4, 256, fake, odd2, None) == 3
+    assert lib.qk_gemv_swiglu(qk.Q4_K, fake, fake, 4, 256, None, fake, None) == 4
+    assert lib.qk_gemv_swiglu(qk.Q4_K, fake, fake, 4, 256, odd, fake, None) == 3
+    assert lib.qk_gemv_swiglu(qk.Q4_K, fake, fake, 0, 256, fake, fake, None) == 0
+
+
 def test_gemm_row_tile_limit_is_checked_on_host(lib):
     fake = ctypes.c_void_p(0x10000)
     assert lib.qk_gemm(qk.Q4_K, fake, 65535 * 128 + 1, 256, fake, 4, fake, None, 0, None) == 2
