@@ -17,7 +17,8 @@ Q4_K, Q6_K, Q8_0, Q5_0, Q4_0 = 1, 2, 3, 4, 5
 TYPES = {"Q4_K": Q4_K, "Q6_K": Q6_K, "Q8_0": Q8_0, "Q5_0": Q5_0, "Q4_0": Q4_0}
 OUT_F32, OUT_BF16 = 0, 1
 STATUS = {0: "QK_OK", 1: "QK_ERR_TYPE", 2: "QK_ERR_SHAPE", 3: "QK_ERR_ALIGN", 4: "QK_ERR_NULL",
-          5: "QK_ERR_WORKSPACE", 6: "QK_ERR_CUDA", 7: "QK_ERR_TIMEOUT", 8: "QK_ERR_ARG"}
+          5: "QK_ERR_WORKSPACE", 6: "QK_ERR_CUDA", 7: "QK_ERR_TIMEOUT", 8: "QK_ERR_ARG",
+          9: "QK_ERR_FORMAT", 10: "QK_ERR_IO"}
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqk.so")
 _lib = None
@@ -27,6 +28,19 @@ _p = ctypes.c_void_p
 _i64 = ctypes.c_int64
 _sz = ctypes.c_size_t
 _int = ctypes.c_int
+_u32 = ctypes.c_uint32
+_u64 = ctypes.c_uint64
+_f64p = ctypes.POINTER(ctypes.c_double)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_u64p = ctypes.POINTER(ctypes.c_uint64)
+
+
+class GGUFTensorInfo(ctypes.Structure):
+    """qk_gguf_tensor_info."""
+    _fields_ = [("name", ctypes.c_char_p), ("n_dims", ctypes.c_uint32), ("dims", ctypes.c_int64 * 4),
+                ("ggml_type", ctypes.c_uint32), ("qk_type", ctypes.c_int), ("offset", ctypes.c_uint64),
+                ("nbytes", ctypes.c_uint64), ("data", ctypes.c_void_p)]
+
 
 # name: (restype, argtypes), exactly as declared in include/qk.h
 SIGNATURES = {
@@ -48,6 +62,27 @@ SIGNATURES = {
     "qk_device_status": (_int, [_p]),
     "qk_test_stalled_wait": (_int, [ctypes.c_uint32, _p]),
     "qk_last_error": (ctypes.c_char_p, []),
+    "qk_gguf_open": (_int, [ctypes.c_char_p, ctypes.POINTER(_p)]),
+    "qk_gguf_parse": (_int, [_p, _u64, ctypes.POINTER(_p)]),
+    "qk_gguf_close": (None, [_p]),
+    "qk_gguf_version": (_u32, [_p]),
+    "qk_gguf_n_kv": (_i64, [_p]),
+    "qk_gguf_n_tensors": (_i64, [_p]),
+    "qk_gguf_alignment": (_u64, [_p]),
+    "qk_gguf_data_offset": (_u64, [_p]),
+    "qk_gguf_image": (_p, [_p]),
+    "qk_gguf_find_kv": (_i64, [_p, ctypes.c_char_p]),
+    "qk_gguf_kv_key": (ctypes.c_char_p, [_p, _i64]),
+    "qk_gguf_kv_type": (_int, [_p, _i64]),
+    "qk_gguf_kv_int": (_int, [_p, _i64, _i64p]),
+    "qk_gguf_kv_float": (_int, [_p, _i64, _f64p]),
+    "qk_gguf_kv_str": (_p, [_p, _i64, _u64p]),
+    "qk_gguf_kv_array": (_int, [_p, _i64, ctypes.POINTER(_int), _u64p]),
+    "qk_gguf_kv_array_int": (_int, [_p, _i64, _u64, _i64p]),
+    "qk_gguf_kv_array_float": (_int, [_p, _i64, _u64, _f64p]),
+    "qk_gguf_kv_array_str": (_p, [_p, _i64, _u64, _u64p]),
+    "qk_gguf_find_tensor": (_i64, [_p, ctypes.c_char_p]),
+    "qk_gguf_tensor": (_int, [_p, _i64, ctypes.POINTER(GGUFTensorInfo)]),
 }
 
 
@@ -219,3 +254,123 @@ def test_stalled_wait(limit_us: int, stream=None) -> None:
 
 def device_status(stream=None) -> None:
     _check(load().qk_device_status(_stream(stream)), "qk_device_status")
+
+
+# ------------------------------------------------------------ GGUF reader --
+
+_V_STR, _V_ARR, _V_F32, _V_F64 = 8, 9, 6, 12
+
+
+class GGUF:
+    """A parsed GGUF image (qk_gguf_*): header, metadata and tensor infos.
+    Open a file (memory-mapped) with GGUF(path=...) or parse bytes the object
+    keeps alive with GGUF(data=...).  Tensor data stays in the image."""
+
+    def __init__(self, path: str | None = None, data: bytes | None = None):
+        L = load()
+        h = _p()
+        self._buf = None
+        if path is not None:
+            _check(L.qk_gguf_open(os.fsencode(path), ctypes.byref(h)), "qk_gguf_open")
+        else:
+            self._buf = ctypes.create_string_buffer(bytes(data), len(data))
+            _check(L.qk_gguf_parse(ctypes.cast(self._buf, _p), len(data), ctypes.byref(h)), "qk_gguf_parse")
+        self._h = h
+
+    def close(self) -> None:
+        if self._h:
+            load().qk_gguf_close(self._h)
+            self._h = _p()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def version(self) -> int:
+        return load().qk_gguf_version(self._h)
+
+    @property
+    def alignment(self) -> int:
+        return load().qk_gguf_alignment(self._h)
+
+    @property
+    def data_offset(self) -> int:
+        return load().qk_gguf_data_offset(self._h)
+
+    def keys(self) -> list:
+        L = load()
+        return [L.qk_gguf_kv_key(self._h, i).decode() for i in range(L.qk_gguf_n_kv(self._h))]
+
+    def kv_type(self, key: str) -> int:
+        L = load()
+        return L.qk_gguf_kv_type(self._h, L.qk_gguf_find_kv(self._h, key.encode()))
+
+    def _str(self, ptr, n) -> str:
+        return ctypes.string_at(ptr, n.value).decode("utf-8", "surrogateescape") if n.value else ""
+
+    def kv(self, key: str):
+        """The value of `key` as int / float / str / list (KeyError if absent)."""
+        L = load()
+        i = L.qk_gguf_find_kv(self._h, key.encode())
+        if i < 0:
+            raise KeyError(key)
+        t = L.qk_gguf_kv_type(self._h, i)
+        n = ctypes.c_uint64()
+        if t == _V_STR:
+            return self._str(L.qk_gguf_kv_str(self._h, i, ctypes.byref(n)), n)
+        if t in (_V_F32, _V_F64):
+            v = ctypes.c_double()
+            _check(L.qk_gguf_kv_float(self._h, i, ctypes.byref(v)), "qk_gguf_kv_float")
+            return v.value
+        if t == _V_ARR:
+            et = _int()
+            _check(L.qk_gguf_kv_array(self._h, i, ctypes.byref(et), ctypes.byref(n)), "qk_gguf_kv_array")
+            out = []
+            for j in range(n.value):
+                if et.value == _V_STR:
+                    m = ctypes.c_uint64()
+                    out.append(self._str(L.qk_gguf_kv_array_str(self._h, i, j, ctypes.byref(m)), m))
+                elif et.value in (_V_F32, _V_F64):
+                    v = ctypes.c_double()
+                    _check(L.qk_gguf_kv_array_float(self._h, i, j, ctypes.byref(v)), "qk_gguf_kv_array_float")
+                    out.append(v.value)
+                elif et.value == _V_ARR:
+                    raise QKError(1, "GGUF.kv", "nested arrays are not exposed")
+                else:
+                    v = ctypes.c_int64()
+                    _check(L.qk_gguf_kv_array_int(self._h, i, j, ctypes.byref(v)), "qk_gguf_kv_array_int")
+                    out.append(v.value)
+            return out
+        v = ctypes.c_int64()
+        _check(L.qk_gguf_kv_int(self._h, i, ctypes.byref(v)), "qk_gguf_kv_int")
+        return v.value
+
+    def tensors(self) -> list:
+        L = load()
+        return [self._info(i) for i in range(L.qk_gguf_n_tensors(self._h))]
+
+    def _info(self, i: int) -> dict:
+        info = GGUFTensorInfo()
+        _check(load().qk_gguf_tensor(self._h, i, ctypes.byref(info)), "qk_gguf_tensor")
+        return {"name": info.name.decode(), "dims": list(info.dims[:info.n_dims]), "ggml_type": info.ggml_type,
+                "qk_type": info.qk_type, "offset": info.offset, "nbytes": info.nbytes, "data": info.data}
+
+    def tensor(self, name: str) -> dict:
+        i = load().qk_gguf_find_tensor(self._h, name.encode())
+        if i < 0:
+            raise KeyError(name)
+        return self._info(i)
+
+    def tensor_bytes(self, name: str) -> bytes:
+        """A copy of the tensor's data bytes."""
+        t = self.tensor(name)
+        return ctypes.string_at(t["data"], t["nbytes"])

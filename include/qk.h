@@ -71,7 +71,9 @@ typedef enum {
     QK_ERR_WORKSPACE = 5, /* workspace smaller than the matching *_workspace()  */
     QK_ERR_CUDA = 6,      /* the CUDA runtime reported an error                 */
     QK_ERR_TIMEOUT = 7,   /* a bounded wait inside a kernel ran out             */
-    QK_ERR_ARG = 8        /* any other invalid argument                         */
+    QK_ERR_ARG = 8,       /* any other invalid argument                         */
+    QK_ERR_FORMAT = 9,    /* a GGUF image is malformed or truncated             */
+    QK_ERR_IO = 10        /* a file could not be opened or mapped               */
 } qk_status;
 
 /* Output element types of qk_dequant. */
@@ -264,6 +266,72 @@ qk_status qk_test_stalled_wait(uint32_t limit_us, void* stream);
  * word: QK_OK, or QK_ERR_TIMEOUT when a bounded wait ran out since the last
  * call (the affected outputs are then invalid). */
 qk_status qk_device_status(void* stream);
+
+/* ------------------------------------------------------------------------
+ * GGUF container reader (host code; no GPU involved).  The file the blocks
+ * come in ("12 -- llama.cpp / GGUF / Local Inference Mastery", "Part 1 --
+ * The GGUF format (bit-level)"): header (magic "GGUF", version uint32,
+ * tensor_count uint64, metadata_kv_count uint64), metadata entries
+ * (length-prefixed key, value type, value), tensor infos (name, n_dims,
+ * shape, ggml type, offset), padding to the alignment, tensor data.
+ * Versions 2 and 3, little-endian.  The value-type codes (0 u8, 1 i8, 2 u16,
+ * 3 i16, 4 u32, 5 i32, 6 f32, 7 bool, 8 string, 9 array, 10 u64, 11 i64,
+ * 12 f64), the ggml tensor types (0 F32, 1 F16, 2 Q4_0, 6 Q5_0, 8 Q8_0,
+ * 12 Q4_K, 14 Q6_K, 30 BF16 are sized here; others are listed with nbytes 0)
+ * and the "general.alignment" key (uint32 power of two, default 32) follow
+ * the GGUF specification the page cites.
+ * Every length, count and offset is checked against the image before use;
+ * a malformed or truncated image gives QK_ERR_FORMAT and no handle.  Tensor
+ * data is never copied: qk_gguf_tensor gives a pointer into the image.  A
+ * handle is read-only and may be used from several threads. */
+typedef struct qk_gguf qk_gguf;
+
+typedef struct {
+    const char* name;      /* NUL-terminated, valid while the handle is open      */
+    uint32_t n_dims;       /* 1..4                                                */
+    int64_t dims[4];       /* dims[0] innermost (a weight matrix: cols, rows); 1 past n_dims */
+    uint32_t ggml_type;
+    int qk_type;           /* this library's type id (QK_Q4_K ...), -1 for others */
+    uint64_t offset;       /* absolute byte offset in the image                   */
+    uint64_t nbytes;       /* data bytes; 0 when the type's size is not known here */
+    const void* data;      /* image + offset                                      */
+} qk_gguf_tensor_info;
+
+/* Open `path` read-only (memory-mapped) and parse it.  *out is NULL on error
+ * (QK_ERR_IO, QK_ERR_FORMAT, QK_ERR_NULL). */
+qk_status qk_gguf_open(const char* path, qk_gguf** out);
+/* Parse an image the caller owns; it must outlive the handle. */
+qk_status qk_gguf_parse(const void* data, uint64_t size, qk_gguf** out);
+/* Release the handle (and its mapping).  NULL is ignored. */
+void qk_gguf_close(qk_gguf* g);
+
+uint32_t qk_gguf_version(const qk_gguf* g);
+int64_t qk_gguf_n_kv(const qk_gguf* g);
+int64_t qk_gguf_n_tensors(const qk_gguf* g);
+uint64_t qk_gguf_alignment(const qk_gguf* g);
+uint64_t qk_gguf_data_offset(const qk_gguf* g);   /* start of the tensor data section */
+const void* qk_gguf_image(const qk_gguf* g);
+
+/* Metadata entry i (0 .. n_kv-1); the index of `key`, or -1. */
+int64_t qk_gguf_find_kv(const qk_gguf* g, const char* key);
+const char* qk_gguf_kv_key(const qk_gguf* g, int64_t i);   /* NULL when out of range */
+int qk_gguf_kv_type(const qk_gguf* g, int64_t i);          /* -1 when out of range */
+/* Scalar values: integers of any width and bools as int64 (a uint64 above
+ * INT64_MAX gives QK_ERR_TYPE), floats as double; QK_ERR_TYPE for another
+ * type, QK_ERR_ARG for a bad index. */
+qk_status qk_gguf_kv_int(const qk_gguf* g, int64_t i, int64_t* v);
+qk_status qk_gguf_kv_float(const qk_gguf* g, int64_t i, double* v);
+/* A string value (not NUL-terminated: *len bytes), NULL when not a string. */
+const char* qk_gguf_kv_str(const qk_gguf* g, int64_t i, uint64_t* len);
+/* Arrays: element type and count; element j as int64 / double / string. */
+qk_status qk_gguf_kv_array(const qk_gguf* g, int64_t i, int* elem_type, uint64_t* n);
+qk_status qk_gguf_kv_array_int(const qk_gguf* g, int64_t i, uint64_t j, int64_t* v);
+qk_status qk_gguf_kv_array_float(const qk_gguf* g, int64_t i, uint64_t j, double* v);
+const char* qk_gguf_kv_array_str(const qk_gguf* g, int64_t i, uint64_t j, uint64_t* len);
+
+/* Tensor i (0 .. n_tensors-1); the index of `name`, or -1. */
+int64_t qk_gguf_find_tensor(const qk_gguf* g, const char* name);
+qk_status qk_gguf_tensor(const qk_gguf* g, int64_t i, qk_gguf_tensor_info* info);
 
 /* Text of the last error on the calling thread ("" if none). */
 const char* qk_last_error(void);
