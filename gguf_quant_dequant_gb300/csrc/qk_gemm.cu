@@ -18,6 +18,7 @@
 // tile halves it per FLOP compared with one 256-column accumulator.
 // Every mbarrier wait is bounded; tensor memory is always released.
 #include <algorithm>
+#include <cstring>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
@@ -65,21 +66,14 @@ constexpr int kParts = kDeqThreads / kBM;            // threads per tile row (4)
 //   Wide (prefill, M > 64): two 256-token accumulators fill tensor memory and
 //   each k-block carries 8 MMAs of 128 x 256 x 16, so two weight stages keep
 //   the tensor core fed.
-//   Skinny (M <= 64): one accumulator of at most 64 tokens; a k-block's MMA
-//   work is tiny, so the dequant warps run up to NS k-blocks ahead of the
-//   tensor core and two packed macro-blocks stream in while a third is
-//   decoded.
-// WARP_ISSUE: the MMA issuer's loop runs on the whole warp (warp-uniform
-// indices, one elected lane issues) rather than on lane 0 alone; measured
-// faster for the skinny pipeline's short MMAs, slower for the wide one.
-template <int NS_, int NACC_, int BNM_, int NSP_, bool WARP_ISSUE_> struct Cfg {
+//   Small batches (M <= 64) use gemm_skinny_kernel below instead.
+template <int NS_, int NACC_, int BNM_, int NSP_> struct Cfg {
     static constexpr int NS = NS_, NACC = NACC_, BNM = BNM_, NSP = NSP_;
-    static constexpr bool WARP_ISSUE = WARP_ISSUE_;
     static constexpr int BN = BNM * NACC;            // tokens per CTA
     static constexpr int TMEM = BN < 32 ? 32 : BN;   // power of two >= 32
     static_assert((TMEM & (TMEM - 1)) == 0, "tensor memory columns");
 };
-using Wide = Cfg<2, 2, 256, 2, false>;
+using Wide = Cfg<2, 2, 256, 2>;
 constexpr int kSkinnyBN = 64;     // largest M the skinny pipeline takes
 constexpr int kMaxXStages = 16;   // activation ring depth limit
 constexpr int kSmemMax = 227 * 1024;
@@ -99,13 +93,33 @@ template <int T> struct PkGeo {
     static constexpr int STAGE = kBM * SLOT;
 };
 
-// Skinny pipeline: up to 6 weight stages beside three packed stages,
-// keeping 48 KB for the activation ring.
-template <int T> struct SkinnyNS {
-    static constexpr int FREE = kSmemMax - 1024 - 3 * PkGeo<T>::STAGE - 48 * 1024 - 1024;
-    static constexpr int V = FREE / kA > 6 ? 6 : FREE / kA;
+// Small-batch kernel (M <= 64): 256-weight macro-blocks for every type (four
+// 64-wide k-blocks), a CTA-wide packed ring of NSP stages filled by bulk
+// copies, NS bf16 weight stages.  20 warps: activation producer, two MMA
+// issuers, packed producer, 16 dequant warps (4 row quarters x 4 k-block
+// phases).
+template <int T> struct SkGeo {
+    static constexpr int BYTES = 256 / Fmt<T>::BE * Fmt<T>::BB;          // 144, 210, 272, 176, 144
+    // 2D TMA box width, also the row stride of a packed stage: the
+    // macro-block itself, or for Q6_K (whose starts are 2-byte aligned) 240
+    // bytes from the 16-byte boundary below its start.  An odd number of
+    // 16-byte units, so the 32 rows a warp reads spread over 8 bank groups.
+    // The word reads of the 32-weight types run up to 4 bytes past a row's
+    // box (into the next row, or past the ring into the barriers): read, never
+    // used.
+    static constexpr int BOXW = T == T_Q6_K ? 240 : BYTES;
+    static_assert(BOXW % 16 == 0 && (BOXW / 16) % 2 == 1, "packed TMA box");
+    static constexpr int STAGE = kBM * BOXW;
+    static constexpr int NSP = 3;
+    static constexpr int NS = T == T_Q8_0 ? 4 : 6;
+    static constexpr int FIX = 1024 + NS * kA + NSP * STAGE;
+    __host__ __device__ static constexpr int smem(int nsb, int xst) {
+        return FIX + nsb * xst + (2 * NS + 2 * nsb + 2 * NSP + 1) * 8 + 16;
+    }
 };
-template <int T> using Skinny = Cfg<SkinnyNS<T>::V, 1, kSkinnyBN, 3, true>;
+constexpr int kSkMma = 2;                      // MMA warps, one accumulator each
+constexpr int kSkThreads = (2 + kSkMma + 16) * 32;   // activation producer, MMA warps, packed producer, 16 dequant
+constexpr int kSkTmem = 64 * kSkMma;
 
 // Shared-memory map (from the 1024-byte aligned base): NS weight stages, the
 // activation ring (nsb stages of xst bytes), the packed ring, the mbarriers
@@ -248,6 +262,103 @@ __device__ __forceinline__ void fast16_q6k(const uint8_t* blk, int c, int qq, ui
     }
 }
 
+// ---------------------------------------------------------------------------
+// 64-weight decoders (small-batch kernel): one thread decodes one tile row's
+// 64-wide k-block kk (0..3) of a 256-weight macro-block at `blk` in shared
+// memory into 32 bf16x2 words in k order.  Same arithmetic as above: a byte
+// permute puts 128 + q (or 256 + u/128) in an fp32 mantissa, one packed FMA
+// applies scale and offset, one convert packs two bf16.
+
+// Q4_K (blk 16-byte aligned): k-block kk is sub-blocks 2kk (low nibbles of
+// code bytes 32kk .. 32kk+31) and 2kk+1 (their high nibbles).
+__device__ __forceinline__ void q4k64(const uint8_t* blk, int kk, uint32_t (&pk)[32]) {
+    const uint4 h = lds128_g(blk);
+    // Scale / min bytes of sub-blocks 0-3 (kk < 2) or 4-7; this pair is bytes
+    // 2(kk & 1) and 2(kk & 1) + 1 of the word.
+    const uint32_t scw = kk < 2 ? (h.y & 0x3F3F3F3Fu) : ((h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u));
+    const uint32_t mw = kk < 2 ? (h.z & 0x3F3F3F3Fu) : (((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u));
+    const uint32_t sh = 16u * (uint32_t)(kk & 1);
+    const float d = h2f(h.x & 0xFFFFu), dmin = h2f(h.x >> 16);
+    const float ds0 = d * (float)((scw >> sh) & 0xFFu), ds1 = d * (float)((scw >> (sh + 8u)) & 0xFFu);
+    const float dm0 = dmin * (float)((mw >> sh) & 0xFFu), dm1 = dmin * (float)((mw >> (sh + 8u)) & 0xFFu);
+    const float o0 = -(128.0f * ds0 + dm0), o1 = -(128.0f * ds1 + dm1);
+    const uint4 c0 = lds128_g(blk + 16 + 32 * kk), c1 = lds128_g(blk + 32 + 32 * kk);
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        four_hi(w[i] & 0x0F0F0F0Fu, make_float2(ds0, ds0), make_float2(o0, o0), pk[2 * i], pk[2 * i + 1]);
+        four_hi((w[i] >> 4) & 0x0F0F0F0Fu, make_float2(ds1, ds1), make_float2(o1, o1), pk[16 + 2 * i],
+                pk[17 + 2 * i]);
+    }
+}
+
+// Q6_K (blk 2-byte aligned): k-block kk is half t = kk / 2, groups g = 2(kk & 1)
+// and g + 1: low 4 bits from ql[64t .. 64t + 63] (nibble kk & 1), high 2 bits
+// from qh[32t + l] bits 2g (+ 2), sixteen-weight scales 8t + 2g .. + 3.
+__device__ __forceinline__ void q6k64(const uint8_t* blk, int kk, uint32_t (&pk)[32]) {
+    const int t = kk >> 1, hi = kk & 1;
+    uint32_t ql[16], qh[8];
+    gv::lds_words_a2<16>(blk + 64 * t, ql);
+    gv::lds_words_a2<8>(blk + 128 + 32 * t, qh);
+    const uint32_t sw = ld_u32_a2(blk + 192 + 8 * t + 4 * hi);
+    const float d = h2f(ld_u16(blk + 208));
+    float ds[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) ds[e] = d * (float)(int)(int8_t)((sw >> (8 * e)) & 0xFFu);
+    const int nsh = 4 * hi, hsh = 4 * hi;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float a = ds[i >> 2], b = ds[2 + (i >> 2)];
+        const uint32_t v0 = ((ql[i] >> nsh) & 0x0F0F0F0Fu) | (((qh[i] >> hsh) & 0x03030303u) << 4);
+        const uint32_t v1 = ((ql[8 + i] >> nsh) & 0x0F0F0F0Fu) | (((qh[i] >> (hsh + 2)) & 0x03030303u) << 4);
+        four_hi(v0, make_float2(a, a), make_float2(-160.0f * a, -160.0f * a), pk[2 * i], pk[2 * i + 1]);
+        four_hi(v1, make_float2(b, b), make_float2(-160.0f * b, -160.0f * b), pk[16 + 2 * i], pk[17 + 2 * i]);
+    }
+}
+
+// Bits 0-3 of x to bit 0 of bytes 0-3.
+__device__ __forceinline__ uint32_t spread4(uint32_t x) { return (x * 0x00204081u) & 0x01010101u; }
+
+// One 32-weight block (2-byte aligned) -> 16 words.  Q8_0: d, 32 signed codes,
+// w = d*q.  Q5_0: d, a word of fifth bits, 16 nibble bytes, w = d*(q - 16).
+// Q4_0: d, 16 nibble bytes, w = d*(q - 8).  Nibble bytes: element j low,
+// element j + 16 high.
+template <int T>
+__device__ __forceinline__ void block32(const uint8_t* b, uint32_t* pk) {
+    const float d = h2f(ld_u16(b));
+    if constexpr (T == T_Q8_0) {
+        uint32_t q[8];
+        gv::lds_words_a2<8>(b + 2, q);
+        const float2 a = make_float2(128.0f * d, 128.0f * d), c = make_float2(-32896.0f * d, -32896.0f * d);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t u = q[i] ^ 0x80808080u;
+            const float f0 = __uint_as_float(__byte_perm(u, 0x43800000u, 0x7604));
+            const float f1 = __uint_as_float(__byte_perm(u, 0x43800000u, 0x7614));
+            const float f2 = __uint_as_float(__byte_perm(u, 0x43800000u, 0x7624));
+            const float f3 = __uint_as_float(__byte_perm(u, 0x43800000u, 0x7634));
+            const float2 w01 = __ffma2_rn(a, make_float2(f0, f1), c);
+            const float2 w23 = __ffma2_rn(a, make_float2(f2, f3), c);
+            pk[2 * i] = pack_bf16(w01.x, w01.y);
+            pk[2 * i + 1] = pack_bf16(w23.x, w23.y);
+        }
+    } else {
+        constexpr bool k5 = T == T_Q5_0;
+        uint32_t qs[4];
+        gv::lds_words_a2<4>(b + (k5 ? 6 : 2), qs);
+        const uint32_t qh = k5 ? ld_u32_a2(b + 2) : 0u;
+        const float off = k5 ? -144.0f * d : -136.0f * d;
+        const float2 a = make_float2(d, d), c = make_float2(off, off);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = (qs[i] & 0x0F0F0F0Fu) | (k5 ? spread4((qh >> (4 * i)) & 15u) << 4 : 0u);
+            const uint32_t hi = ((qs[i] >> 4) & 0x0F0F0F0Fu) | (k5 ? spread4((qh >> (16 + 4 * i)) & 15u) << 4 : 0u);
+            four_hi(lo, a, c, pk[2 * i], pk[2 * i + 1]);
+            four_hi(hi, a, c, pk[8 + 2 * i], pk[9 + 2 * i]);
+        }
+    }
+}
+
 // Generic (Q5_0, Q4_0) 16 weights via the shared decoders: k in [k0, k0 + 16).
 template <int T>
 __device__ __forceinline__ void generic16(const uint8_t* mb, int o, uint32_t (&pk)[8]) {
@@ -370,25 +481,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 mbar_wait_bounded(&full_x[i % nsb], (uint32_t)((i / nsb) & 1), p.status);
         }
     } else if (warp == 1) {
-        // MMA issuer.  With WARP_ISSUE the whole warp runs the loop, so the
-        // stage indices and operand descriptors stay warp-uniform; lane 0
-        // polls the barriers and one elected lane issues every MMA and commit
-        // (a commit tracks the MMAs of the thread that issues it).  Otherwise
-        // lane 0 runs the loop alone.  Descriptor start addresses advance in
-        // 16-byte units from the ring bases.
-        const bool leader = C::WARP_ISSUE ? tc::elect_one() : lane == 0;
+        // MMA issuer: lane 0 runs the loop.  Descriptor start addresses
+        // advance in 16-byte units from the ring bases.
+        const bool leader = lane == 0;
         const uint32_t idesc = tc::idesc_bf16_f32(kBM, p.nmma);
         const uint64_t da0 = tc::sdesc_k128(smem_u32(smem)), db0 = tc::sdesc_k128(smem_u32(xring));
         const uint64_t dbj = (uint64_t)(bsub >> 4);   // second accumulator's activation tile
         int s = 0, sx = 0;
         uint32_t par = 0, parx = 0;   // phase parities of full_w[s] and full_x[sx]
-        for (int i = 0; i < nk && (C::WARP_ISSUE || leader); ++i) {
-            int good = 1;
-            if (lane == 0)
-                good = mbar_wait_sleep_bounded(&full_x[sx], parx, p.status) &&
-                       mbar_wait_sleep_bounded(&full_w[s], par, p.status);
-            if (C::WARP_ISSUE) good = __shfl_sync(0xffffffffu, good, 0);
-            if (!good) break;
+        for (int i = 0; i < nk && leader; ++i) {
+            if (!mbar_wait_sleep_bounded(&full_x[sx], parx, p.status) ||
+                !mbar_wait_sleep_bounded(&full_w[s], par, p.status))
+                break;
             tc::fence_after_sync();
             const uint64_t da = da0 + (uint64_t)((s * kA) >> 4), db = db0 + (uint64_t)((sx * p.xst) >> 4);
             if (leader) {
@@ -401,7 +505,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 tc::commit(&empty[s]);     // both stages free once these MMAs complete
                 tc::commit(&empty_x[sx]);
             }
-            if (C::WARP_ISSUE) __syncwarp();
             if (++s == kNS) {
                 s = 0;
                 par ^= 1u;
@@ -531,6 +634,262 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
 }
 
+// ---------------------------------------------------------------------------
+// Small-batch dequant-GEMM (M <= 64, one token tile): each dequant thread owns
+// one weight row and decodes a whole 64-wide k-block of it, so scale decoding,
+// synchronisation and stores are paid once per 64 weights.
+//   warp 0  TMA producer of the activation tiles (its own ring);
+//   warps 1-2  MMA issuers: warp 1 + w takes local k-blocks w, w + 2, ...
+//           into accumulator w (issuing a k-block's MMAs and commits costs a
+//           few hundred ns whatever N is, so two issuers halve that per
+//           k-block); the epilogue adds the two accumulators in order.  Each
+//           runs its loop on the whole warp, one elected lane issuing;
+//   warp 3  packed producer: each 256-weight macro-block of the 128 rows into
+//           a CTA-wide ring (full_p / empty_p barriers) as one 2D TMA box of
+//           W seen as [rows, row_bytes] (row_bytes must be a multiple of 16:
+//           the planner sends other shapes to gemm_kernel);
+//   warps 4..19  dequant: row quarter q = warp % 4 (the TMEM lanes it may
+//           read back), phase ph = (warp - 4) / 4: k-block ph of every
+//           macro-block; the four warps of a phase fill one weight stage.
+template <int T>
+__global__ void __launch_bounds__(kSkThreads, 1) gemm_skinny_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                   const __grid_constant__ CUtensorMap wmap,
+                                                                   const Args p) {
+    using G = SkGeo<T>;
+    using F = Fmt<T>;
+    constexpr int kNS = G::NS, kNSP = G::NSP;
+    static_assert(kNS % kSkMma == 0, "each MMA warp owns whole weight stages");
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);   // 1024-aligned (swizzle atoms)
+    const int nsb = p.nsb;
+    uint8_t* xring = smem + kNS * kA;
+    uint8_t* packed = xring + nsb * p.xst;
+    uint64_t* full_w = reinterpret_cast<uint64_t*>(packed + kNSP * G::STAGE);
+    uint64_t* empty = full_w + kNS;
+    uint64_t* full_x = empty + kNS;
+    uint64_t* empty_x = full_x + nsb;
+    uint64_t* full_p = empty_x + nsb;
+    uint64_t* empty_p = full_p + kNSP;
+    uint64_t* accum = empty_p + kNSP;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row0 = (int64_t)blockIdx.y * kBM;
+    const int kb0 = (int)blockIdx.z * p.kb_per_split;   // a multiple of 4
+    const int kb1 = min(p.nkb, kb0 + p.kb_per_split);
+    const int nk = kb1 - kb0;
+    const int m0 = kb0 / 4, nmb = (kb1 + 3) / 4 - m0;
+    const uint32_t bsub = (uint32_t)p.nmma * (kBK * 2);
+    float* out = p.part ? p.part + (size_t)blockIdx.z * (size_t)p.M * (size_t)p.rows : p.Y;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(&full_w[s], 4);
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < nsb; ++s) {
+            mbar_init(&full_x[s], 1);
+            mbar_init(&empty_x[s], 1);
+        }
+        for (int s = 0; s < kNSP; ++s) {
+            mbar_init(&full_p[s], 1);
+            mbar_init(&empty_p[s], kDeqWarps);
+        }
+        mbar_init(accum, kSkMma);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, kSkTmem);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    pdl_launch_dependents();
+
+    if (warp == 0) {
+        // Activation tiles (they may come from the previous kernel: wait for it).
+        if (lane == 0) {
+            pdl_wait_prior();
+            int issued = 0, s = 0;
+            uint32_t par = 1;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (issued >= nsb && !mbar_wait_sleep_bounded(&empty_x[s], par, p.status)) break;
+                mbar_arrive_expect_tx(&full_x[s], bsub);
+                tc::tma_load_2d(xring + s * p.xst, &xmap, kb * kBK, 0, &full_x[s]);
+                ++issued;
+                if (++s == nsb) {
+                    s = 0;
+                    par ^= 1u;
+                }
+            }
+            for (int i = issued > nsb ? issued - nsb : 0; i < issued; ++i)
+                mbar_wait_bounded(&full_x[i % nsb], (uint32_t)((i / nsb) & 1), p.status);
+        }
+    } else if (warp <= kSkMma) {
+        // MMA issuer w: local k-blocks w, w + kSkMma, ... into accumulator w
+        // (weight stage and activation stage both advance by kSkMma; NS and
+        // the activation ring depth are multiples of kSkMma).
+        const int mw = warp - 1;
+        const bool leader = tc::elect_one();
+        const uint32_t idesc = tc::idesc_bf16_f32(kBM, p.nmma);
+        const uint64_t da0 = tc::sdesc_k128(smem_u32(smem)), db0 = tc::sdesc_k128(smem_u32(xring));
+        const uint32_t acc = tmem + (uint32_t)(64 * mw);
+        int s = mw, sx = mw;
+        uint32_t par = 0, parx = 0;
+        for (int i = mw; i < nk; i += kSkMma) {
+            int good = 1;
+            if (lane == 0)
+                good = mbar_wait_sleep_bounded(&full_x[sx], parx, p.status) &&
+                       mbar_wait_sleep_bounded(&full_w[s], par, p.status);
+            if (__shfl_sync(0xffffffffu, good, 0) == 0) break;
+            tc::fence_after_sync();
+            const uint64_t da = da0 + (uint64_t)((s * kA) >> 4), db = db0 + (uint64_t)((sx * p.xst) >> 4);
+            if (leader) {
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    tc::mma_bf16(acc, da + 2 * kk, db + 2 * kk, idesc, (i != mw || kk != 0) ? 1u : 0u);
+                tc::commit(&empty[s]);
+                tc::commit(&empty_x[sx]);
+            }
+            __syncwarp();
+            if ((s += kSkMma) >= kNS) {
+                s -= kNS;
+                par ^= 1u;
+            }
+            if ((sx += kSkMma) >= nsb) {
+                sx -= nsb;
+                parx ^= 1u;
+            }
+        }
+        if (leader) tc::commit(accum);
+        __syncwarp();
+        if (lane == 0) mbar_wait_sleep_bounded(accum, 0, p.status);
+        __syncwarp();
+    } else if (warp == kSkMma + 1) {
+        // Packed producer: each macro-block of the tile's 128 rows as one 2D
+        // TMA box of W seen as [rows, row_bytes] (4-byte elements): rows past
+        // the matrix and bytes past a row's end arrive as zeros.
+        int ps = 0, issued = 0;
+        uint32_t par = 1;
+        if (lane == 0) {
+            for (int mi = 0; mi < nmb; ++mi) {
+                const int64_t m = m0 + mi;
+                if (mi >= kNSP && !mbar_wait_sleep_bounded(&empty_p[ps], par, p.status)) break;
+                mbar_arrive_expect_tx(&full_p[ps], (uint32_t)(kBM * G::BOXW));
+                tc::tma_load_2d(packed + ps * G::STAGE, &wmap, (int)(((m * G::BYTES) & ~(int64_t)15) / 4), (int)row0,
+                                &full_p[ps]);
+                ++issued;
+                if (++ps == kNSP) {
+                    ps = 0;
+                    par ^= 1u;
+                }
+            }
+            // Every copy issued must land before the CTA may exit.
+            for (int i = issued > kNSP ? issued - kNSP : 0; i < issued; ++i)
+                mbar_wait_bounded(&full_p[i % kNSP], (uint32_t)((i / kNSP) & 1), p.status);
+        }
+    } else {
+        const int q = warp & 3, ph = (warp - kSkMma - 2) >> 2;
+        const int r = 32 * q + lane;
+        const int64_t row = row0 + r;
+        const bool live = row < p.rows;
+        const uint32_t line = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);   // row r's line in a weight stage
+        bool ok = true;
+        int ps = 0;
+        uint32_t ppar = 0;
+#pragma unroll 1
+        for (int mi = 0; mi < nmb; ++mi) {
+            const int m = m0 + mi;
+            if (ok) {
+                int good = 1;
+                if (lane == 0) good = mbar_wait_bounded(&full_p[ps], ppar, p.status);
+                ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+            }
+            const int kb = 4 * m + ph;
+            if (kb < kb1) {
+                const int li = kb - kb0;
+                const int s = li % kNS;
+                if (ok && li >= kNS) {
+                    int good = 1;
+                    if (lane == 0) good = mbar_wait_bounded(&empty[s], (uint32_t)((li / kNS - 1) & 1), p.status);
+                    ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+                }
+                if (ok) {
+                    uint32_t pk[32];
+                    if (live) {
+                        const int64_t st = row * p.row_bytes + (int64_t)m * G::BYTES;
+                        const uint8_t* blk = packed + ps * G::STAGE + r * G::BOXW + (int)(st & 15);
+                        if constexpr (T == T_Q4_K) {
+                            q4k64(blk, ph, pk);
+                        } else if constexpr (T == T_Q6_K) {
+                            q6k64(blk, ph, pk);
+                        } else {
+                            // Two 32-weight blocks; the second may lie past cols.
+                            block32<T>(blk + (2 * ph) * F::BB, pk);
+                            if ((int64_t)kb * kBK + 32 < p.cols) {
+                                block32<T>(blk + (2 * ph + 1) * F::BB, pk + 16);
+                            } else {
+#pragma unroll
+                                for (int i = 16; i < 32; ++i) pk[i] = 0u;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) pk[i] = 0u;
+                    }
+                    uint8_t* As = smem + s * kA + line;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(As + ((c ^ (r & 7)) << 4)) =
+                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                }
+                fence_proxy_async_smem();   // generic stores -> visible to the tensor core
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full_w[s]);
+            }
+            __syncwarp();   // every lane is done reading packed slot ps
+            if (lane == 0) mbar_arrive(&empty_p[ps]);
+            if (++ps == kNSP) {
+                ps = 0;
+                ppar ^= 1u;
+            }
+        }
+        // Epilogue: warp reads TMEM lanes 32q .. 32q+31; the four phases of a
+        // quarter split the 64 columns into groups of 16.
+        if (lane == 0) mbar_wait_sleep_bounded(accum, 0, p.status);
+        __syncwarp();
+        tc::fence_after_sync();
+        const int col = 16 * ph;
+        if (col < p.M) {
+            uint32_t v[16];
+            tc::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + col, v);
+            tc::tmem_wait_ld();
+#pragma unroll 1
+            for (int w = 1; w < kSkMma && w < nk; ++w) {   // the other accumulators, in order
+                uint32_t u[16];
+                tc::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * w) + col, u);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(u[e]));
+            }
+            if (live) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (col + i < p.M) out[(int64_t)(col + i) * p.rows + row] = __uint_as_float(v[i]);
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kSkTmem);
+    }
+}
+
 // Y = sum over splits of the partials, in split order (deterministic).
 __global__ void __launch_bounds__(256) reduce_splits_kernel(const float* __restrict__ part, int splits, int64_t n,
                                                            float* __restrict__ Y) {
@@ -590,8 +949,46 @@ static cudaError_t gemm_tc(gm::Args a, const GemmPlan& pl, const CUtensorMap& ma
 }
 
 template <int T>
+static cudaError_t gemm_sk(gm::Args a, const GemmPlan& pl, const CUtensorMap& map, cudaStream_t s) {
+    using G = gm::SkGeo<T>;
+    // Packed weights by 2D TMA: W (16-byte aligned, rows a multiple of 16
+    // bytes: the planner checks) as 4-byte elements, box (BOXW / 4) x 128 rows.
+    if (a.row_bytes % 16 != 0) return cudaErrorInvalidValue;
+    auto encode = encode_fn();
+    if (!encode) return cudaErrorNotSupported;
+    CUtensorMap wmap;
+    cuuint64_t gdim[2] = {(cuuint64_t)(a.row_bytes / 4), (cuuint64_t)a.rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)a.row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)(G::BOXW / 4), (cuuint32_t)gm::kBM};
+    cuuint32_t estride[2] = {1, 1};
+    if (encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(a.W), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    // Activation ring: one nmma x 64 tile per stage, as many as fit (at most 16).
+    a.xst = a.nmma * gm::kBK * 2;
+    a.nsb = std::min(gm::kMaxXStages, (gm::kSmemMax - G::smem(0, 0)) / (a.xst + 16)) / gm::kSkMma * gm::kSkMma;
+    if (a.nsb < gm::kSkMma) return cudaErrorInvalidValue;
+    const int smem = G::smem(a.nsb, a.xst);
+    auto kern = gm::gemm_skinny_kernel<T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, gm::kSmemMax);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1u, (unsigned)((a.rows + gm::kBM - 1) / gm::kBM), (unsigned)pl.splits);
+    cfg.blockDim = dim3(gm::kSkThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, map, wmap, a);
+}
+
+template <int T>
 static cudaError_t gemm_t(const gm::Args& a, const GemmPlan& pl, const CUtensorMap& map, cudaStream_t s) {
-    return pl.skinny ? gemm_tc<T, gm::Skinny<T>>(a, pl, map, s) : gemm_tc<T, gm::Wide>(a, pl, map, s);
+    return pl.skinny ? gemm_sk<T>(a, pl, map, s) : gemm_tc<T, gm::Wide>(a, pl, map, s);
 }
 
 namespace {
@@ -607,9 +1004,19 @@ GemmPlan plan_gemm(int type, int64_t rows, int64_t cols, int64_t M, int sms) {
     GemmPlan pl;
     if (rows <= 0 || cols <= 0 || M <= 0) return pl;
     const int64_t nkb = (cols + gm::kBK - 1) / gm::kBK;
-    const int64_t kpm = k_blocks_per_macro(type);
-    pl.skinny = M <= gm::kSkinnyBN;
-    const int64_t bn = pl.skinny ? gm::kSkinnyBN : gm::Wide::BN;
+    // Small batches take gemm_skinny_kernel when W's rows can be loaded as TMA
+    // boxes (row bytes a multiple of 16), else gemm_kernel.
+    int64_t rb = 0;
+    switch (type) {
+    case T_Q4_K: rb = cols / 256 * 144; break;
+    case T_Q6_K: rb = cols / 256 * 210; break;
+    case T_Q8_0: rb = cols / 32 * 34; break;
+    case T_Q5_0: rb = cols / 32 * 22; break;
+    case T_Q4_0: rb = cols / 32 * 18; break;
+    }
+    pl.skinny = M <= gm::kSkinnyBN && rb % 16 == 0;
+    const int64_t kpm = pl.skinny ? 4 : k_blocks_per_macro(type);   // the small-batch kernel's macro-blocks are 256 wide
+    const int64_t bn = M <= gm::kSkinnyBN ? gm::kSkinnyBN : gm::Wide::BN;
     pl.nmma = M > gm::Wide::BNM ? gm::Wide::BNM : (int)std::max<int64_t>(16, (M + 15) / 16 * 16);
     const int64_t tiles = ((M + bn - 1) / bn) * ((rows + gm::kBM - 1) / gm::kBM);
     const int64_t S = std::max(sms, 1);
