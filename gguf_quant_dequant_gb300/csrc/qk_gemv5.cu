@@ -403,13 +403,14 @@ Plan5 plan5(int type, int n, const int64_t* rows, int64_t cols, int sms) {
     p.chunk = (int)std::min<int64_t>(per_cta, gv5::kRedFloats / p.nsl);
     const int64_t xbytes = (cols / 32) * gv::kXBytes;          // 16-byte multiple
     const int64_t red = ((int64_t)p.chunk * p.nsl * 4 + 15) & ~(int64_t)15;
-    const int64_t room = gv5::kSmemBudget - xbytes - red;
+    const int64_t ring0 = (xbytes + red + 127) & ~(int64_t)127;   // the ring starts on a 128-byte line
+    const int64_t room = gv5::kSmemBudget - ring0;
     const int64_t np = room / ((int64_t)gv5::kWarps * 2 * slot);
     if (np < gv5::kMinPairs) return Plan5{};
     p.np = (int)std::min<int64_t>(np, gv5::kMaxPairs);
     p.off_red = (uint32_t)xbytes;
-    p.off_ring = (uint32_t)(xbytes + red);
-    p.smem = (uint32_t)(xbytes + red + (int64_t)gv5::kWarps * p.np * 2 * slot);
+    p.off_ring = (uint32_t)ring0;
+    p.smem = (uint32_t)(ring0 + (int64_t)gv5::kWarps * p.np * 2 * slot);
     return p;
 }
 
