@@ -271,14 +271,18 @@ __global__ void __launch_bounds__(kThreads, 2) gemv5_kernel(const Args p) {
             ioff += PAIR;
             if (ioff == RING) ioff = 0;
         };
-#pragma unroll
-        for (int i = 0; i < NP - 1; ++i) issue_next();
+        // One pair's copies overlap the previous kernel; the rest wait until
+        // x (which may be that kernel's output) is in shared memory, so that
+        // x's loads do not queue behind them.
+        issue_next();
         if (!prepped) {
-            pdl_wait_prior();   // x may be the previous kernel's output
+            pdl_wait_prior();
             prep_x(p.x, nxb, smem);
             prepped = true;
         }
         __syncthreads();   // limbs visible to every warp
+#pragma unroll
+        for (int i = 1; i < NP - 1; ++i) issue_next();
 
         // Consume cursor: my pair j is (slice cs, pair cp) at offset rel_c, slot coff.
         int cs = u0 / npr, cp = u0 - cs * npr, xsl = -1, nblk = 0;
