@@ -117,3 +117,25 @@ def test_gemm_split_k_is_deterministic_and_checks_workspace(gpu):
     with pytest.raises(qk.QKError) as e:
         qk.gemm(t, W, rows, cols, Xd, ws=small)
     assert e.value.status == 5
+
+
+
+# Small batches at full size and with many row tiles: the Llama-3-8B FFN
+# shapes (K split or not by the plan), sampled rows including both ends of
+# row tiles, every token, against the oracle on those rows.
+@pytest.mark.parametrize("rows,cols,M", [(14336, 4096, 16), (4096, 14336, 64), (14336, 4096, 1), (38400, 1024, 5)])
+def test_gemm_small_batch_llama3_ffn_sampled(gpu, rows, cols, M):
+    t = qk.Q4_K
+    Wd = synth.random_blocks_torch("Q4_K", rows, cols, 3800 + M, gpu)
+    g = torch.Generator(device=gpu)
+    g.manual_seed(3801 + M)
+    Xd = torch.randn((M, cols), device=gpu, generator=g).to(torch.bfloat16)
+    Y = qk.gemm(t, Wd, rows, cols, Xd).cpu().numpy()
+    qk.device_status()
+    rng = synth.rng(3802 + M)
+    ni = np.unique(np.concatenate([rng.choice(rows, 40, replace=False), [0, 127, 128, 255, rows - 1]]))
+    rb = qk.row_bytes(t, cols)
+    Wrows = torch.cat([Wd[n * rb:(n + 1) * rb] for n in ni]).cpu().numpy()
+    Xb = Xd.view(torch.int16).cpu().numpy().view(np.uint16)
+    Y_ref, S = oracle.gemm_bf16(t, Wrows, ni.size, cols, Xb)
+    assert_gemv_close(Y[:, ni], Y_ref, S, rtol=GEMM_RTOL, atol=0.0, what=f"FFN gemm {rows}x{cols} M={M}")
