@@ -8,7 +8,7 @@ The arithmetic lives in ``qk_oracle.c`` (scalar C, fp32 weights in the order
 the formulas state, fp64 accumulation).  This module compiles it with gcc on
 first use and wraps it with numpy in / numpy out functions.
 
-Type ids: Q4_K=1, Q6_K=2, Q8_0=3, Q5_0=4, Q4_0=5.
+Type ids: Q4_K=1, Q6_K=2, Q8_0=3, Q5_0=4, Q4_0=5, Q5_K=6.
 """
 from __future__ import annotations
 
@@ -19,8 +19,8 @@ import threading
 
 import numpy as np
 
-Q4_K, Q6_K, Q8_0, Q5_0, Q4_0 = 1, 2, 3, 4, 5
-TYPES = {"Q4_K": Q4_K, "Q6_K": Q6_K, "Q8_0": Q8_0, "Q5_0": Q5_0, "Q4_0": Q4_0}
+Q4_K, Q6_K, Q8_0, Q5_0, Q4_0, Q5_K = 1, 2, 3, 4, 5, 6
+TYPES = {"Q4_K": Q4_K, "Q6_K": Q6_K, "Q8_0": Q8_0, "Q5_0": Q5_0, "Q4_0": Q4_0, "Q5_K": Q5_K}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "qk_oracle.c")

@@ -27,7 +27,10 @@
  * Field sizes for Q6_K (ql 128 B, qh 64 B, 16 int8 scales, fp16 d) and Q5_0
  * (fp16 d, 4 B high bits, 16 B nibbles) are not on the pages; they come from
  * the workload definition, and the bit placement inside them is a reading
- * (see the per-type comments).
+ * (see the per-type comments).  Q5_K appears on the pages only as 5.5-5.7
+ * bits/weight on 256-weight super-blocks ([LC] "Other k-quants at a
+ * glance"); its whole layout is a reading (the GGUF k-quant one, see
+ * unpack_q5_K).
  *
  * All arithmetic that produces a weight is fp32 in the order the formulas
  * state; dot products accumulate in fp64.  Compile with -ffp-contract=off so
@@ -40,7 +43,7 @@
 
 /* Type ids of the oracle (same numbers as the library's public enum; both
  * sides define them independently). */
-enum { OQ_Q4_K = 1, OQ_Q6_K = 2, OQ_Q8_0 = 3, OQ_Q5_0 = 4, OQ_Q4_0 = 5 };
+enum { OQ_Q4_K = 1, OQ_Q6_K = 2, OQ_Q8_0 = 3, OQ_Q5_0 = 4, OQ_Q4_0 = 5, OQ_Q5_K = 6 };
 
 /* ------------------------------------------------------------------------ */
 /* Sizes                                                                    */
@@ -57,6 +60,7 @@ int oq_block_bytes(int type) {
     case OQ_Q8_0: return 2 + 32;
     case OQ_Q5_0: return 2 + 4 + 16;
     case OQ_Q4_0: return 2 + 16;
+    case OQ_Q5_K: return 2 + 2 + 12 + 32 + 128;
     default: return -1;
     }
 }
@@ -65,7 +69,7 @@ int oq_block_bytes(int type) {
  * classic blocks [HG 11.1]. */
 int oq_block_elems(int type) {
     switch (type) {
-    case OQ_Q4_K: case OQ_Q6_K: return 256;
+    case OQ_Q4_K: case OQ_Q6_K: case OQ_Q5_K: return 256;
     case OQ_Q8_0: case OQ_Q5_0: case OQ_Q4_0: return 32;
     default: return -1;
     }
@@ -188,6 +192,37 @@ static void unpack_q4_K(const uint8_t* b, int16_t* q, int16_t* sc, uint8_t* mn, 
     }
 }
 
+/* Q5_K super-block (176 bytes = 5.5 bits/weight, the low end of [LC]'s
+ * 5.5-5.7): a Q4_K super-block with a fifth code bit per weight.  Reading
+ * (the GGUF k-quant layout): bytes 0-1 d, 2-3 dmin, 4-15 the eight
+ * (6-bit scale, 6-bit min) pairs packed exactly as in Q4_K, 16-47 qh (one
+ * high bit per weight), 48-175 qs (the low 4 bits, placed as Q4_K's codes).
+ * Weight n, with c = n/64, h = (n/32)%2, l = n%32:
+ *   lo4 = (qs[32c + l] >> 4h) & 15,   hb = (qh[l] >> (2c + h)) & 1,
+ *   q = lo4 | hb << 4   (0..31),       w = (d*sc)*q - dmin*m of sub-block n/32. */
+static void unpack_q5_K(const uint8_t* b, int16_t* q, int16_t* sc, uint8_t* mn, float* d, float* dmin) {
+    const uint8_t* s = b + 4;
+    const uint8_t* qh = b + 16;
+    const uint8_t* qs = b + 48;
+    *d = oq_half_to_float(rd16(b));
+    *dmin = oq_half_to_float(rd16(b + 2));
+    for (int j = 0; j < 8; j++) {
+        if (j < 4) {
+            sc[j] = (int16_t)(s[j] & 63);
+            mn[j] = (uint8_t)(s[j + 4] & 63);
+        } else {
+            sc[j] = (int16_t)((s[j + 4] & 15) | ((s[j - 4] >> 6) << 4));
+            mn[j] = (uint8_t)((s[j + 4] >> 4) | ((s[j] >> 6) << 4));
+        }
+    }
+    for (int n = 0; n < 256; n++) {
+        int c = n / 64, h = (n / 32) % 2, l = n % 32;
+        int lo4 = (qs[32 * c + l] >> (4 * h)) & 15;
+        int hb = (qh[l] >> (2 * c + h)) & 1;
+        q[n] = (int16_t)(lo4 | (hb << 4));
+    }
+}
+
 /* Q6_K super-block (210 bytes): bytes 0-127 ql (low 4 bits of each code),
  * 128-191 qh (high 2 bits), 192-207 sixteen int8 sub-block scales (one per
  * 16 weights), 208-209 d.  Reading of the bit placement: within half
@@ -263,6 +298,7 @@ int oq_unpack(int type, const uint8_t* blocks, int64_t nblocks,
         case OQ_Q8_0: unpack_q8_0(b, q, &dd); break;
         case OQ_Q5_0: unpack_q5_0(b, q, &dd); break;
         case OQ_Q4_0: unpack_q4_0(b, q, &dd); break;
+        case OQ_Q5_K: unpack_q5_K(b, q, s, m, &dd, &dm); break;
         }
         if (codes) memcpy(codes + i * be, q, (size_t)be * sizeof(int16_t));
         if (sc) memcpy(sc + i * 16, s, sizeof s);
@@ -279,6 +315,7 @@ int oq_unpack(int type, const uint8_t* blocks, int64_t nblocks,
 
 /* One block -> block_elems fp32 weights.
  *   Q4_K: ds = d*sc, dm = dmin*m, w = ds*q - dm   [HG 11.2, LC pseudo-code]
+ *   Q5_K: the same with 5-bit codes
  *   Q6_K: w = (d*sc) * (q - 32)
  *   Q8_0: w = d * q                                [HG 11.1]
  *   Q5_0: w = d * (q - 16)
@@ -290,6 +327,15 @@ static void dequant_block(int type, const uint8_t* b, float* w) {
     switch (type) {
     case OQ_Q4_K:
         unpack_q4_K(b, q, s, m, &d, &dmin);
+        for (int n = 0; n < 256; n++) {
+            float ds = d * (float)s[n / 32];
+            float dm = dmin * (float)m[n / 32];
+            float t = ds * (float)q[n];
+            w[n] = t - dm;
+        }
+        break;
+    case OQ_Q5_K:
+        unpack_q5_K(b, q, s, m, &d, &dmin);
         for (int n = 0; n < 256; n++) {
             float ds = d * (float)s[n / 32];
             float dm = dmin * (float)m[n / 32];
@@ -437,9 +483,10 @@ int oq_entries(int type, const uint8_t* W, int64_t rows, int64_t cols,
 /* Pack: the exact inverse of unpack (codes, scales, mins, fp16 bits)       */
 /* ------------------------------------------------------------------------ */
 
-/* codes [nblocks * block_elems]: Q4_K 0..15, Q6_K 0..63, Q8_0 -128..127,
- * Q5_0 0..31, Q4_0 0..15.  sc [nblocks*16]: Q4_K 0..63 (8 used), Q6_K
- * -128..127.  mins [nblocks*8]: Q4_K 0..63.  d_bits / dmin_bits: binary16.
+/* codes [nblocks * block_elems]: Q4_K 0..15, Q5_K 0..31, Q6_K 0..63, Q8_0
+ * -128..127, Q5_0 0..31, Q4_0 0..15.  sc [nblocks*16]: Q4_K / Q5_K 0..63
+ * (8 used), Q6_K -128..127.  mins [nblocks*8]: Q4_K / Q5_K 0..63.
+ * d_bits / dmin_bits: binary16.
  * Returns -5 when a field is out of range. */
 int oq_pack(int type, int64_t nblocks, const int16_t* codes, const int16_t* sc,
             const uint8_t* mins, const uint16_t* d_bits, const uint16_t* dmin_bits,
@@ -451,11 +498,14 @@ int oq_pack(int type, int64_t nblocks, const int16_t* codes, const int16_t* sc,
         const int16_t* q = codes + i * be;
         memset(b, 0, (size_t)bb);
         switch (type) {
-        case OQ_Q4_K: {
+        case OQ_Q4_K:
+        case OQ_Q5_K: {
+            const int five = type == OQ_Q5_K;
             const int16_t* s = sc + i * 16;
             const uint8_t* m = mins + i * 8;
             uint8_t* S = b + 4;
-            uint8_t* qs = b + 16;
+            uint8_t* qh = b + 16;                  /* Q5_K only */
+            uint8_t* qs = b + (five ? 48 : 16);
             wr16(b, d_bits[i]);
             wr16(b + 2, dmin_bits[i]);
             for (int j = 0; j < 8; j++)
@@ -466,9 +516,10 @@ int oq_pack(int type, int64_t nblocks, const int16_t* codes, const int16_t* sc,
                 S[j + 8] = (uint8_t)((s[j + 4] & 15) | ((m[j + 4] & 15) << 4));
             }
             for (int n = 0; n < 256; n++) {
-                if (q[n] < 0 || q[n] > 15) return -5;
+                if (q[n] < 0 || q[n] > (five ? 31 : 15)) return -5;
                 int c = n / 64, h = (n / 32) % 2, l = n % 32;
-                qs[32 * c + l] |= (uint8_t)(q[n] << (4 * h));
+                qs[32 * c + l] |= (uint8_t)((q[n] & 15) << (4 * h));
+                if (five) qh[l] |= (uint8_t)((q[n] >> 4) << (2 * c + h));
             }
             break;
         }
@@ -546,6 +597,7 @@ static int qclamp(float v, int lo, int hi) {
  *        m_f = -mn; d = max sc_f / 63, dmin = max m_f / 63 (stored fp16);
  *        sc = round(sc_f/d), m = round(m_f/dmin) in 0..63;
  *        q = round((w + dmin*m) / (d*sc)) in 0..15.
+ *   Q5_K: the same with 31 in place of 15 (codes 0..31).
  *   Q6_K per 16 weights: s = max|w|/32; d = max s / 127; sc = round(s/d);
  *        q = round(w / (d*sc)) + 32 in 0..63.
  *   Q8_0: d = max|w|/127, q = round(w/d) in -128..127.
@@ -566,7 +618,8 @@ int oq_quantize(int type, const float* w, int64_t rows, int64_t cols, uint8_t* o
         uint16_t db = 0, dmb = 0;
         memset(s, 0, sizeof s);
         memset(m, 0, sizeof m);
-        if (type == OQ_Q4_K) {
+        if (type == OQ_Q4_K || type == OQ_Q5_K) {
+            const int top = type == OQ_Q5_K ? 31 : 15;
             float scf[8], mf[8], maxsc = 0.0f, maxm = 0.0f;
             for (int j = 0; j < 8; j++) {
                 float lo = 0.0f, hi = x[32 * j];
@@ -575,7 +628,7 @@ int oq_quantize(int type, const float* w, int64_t rows, int64_t cols, uint8_t* o
                     if (v < lo) lo = v;
                     if (v > hi) hi = v;
                 }
-                scf[j] = (hi - lo) / 15.0f;
+                scf[j] = (hi - lo) / (float)top;
                 mf[j] = -lo;
                 if (scf[j] > maxsc) maxsc = scf[j];
                 if (mf[j] > maxm) maxm = mf[j];
@@ -590,7 +643,7 @@ int oq_quantize(int type, const float* w, int64_t rows, int64_t cols, uint8_t* o
                 float dm = dmin * (float)m[j];
                 for (int l = 0; l < 32; l++) {
                     float v = x[32 * j + l];
-                    q[32 * j + l] = (int16_t)(ds > 0.0f ? qclamp((v + dm) / ds, 0, 15) : 0);
+                    q[32 * j + l] = (int16_t)(ds > 0.0f ? qclamp((v + dm) / ds, 0, top) : 0);
                 }
             }
         } else if (type == OQ_Q6_K) {

@@ -14,7 +14,7 @@ from golden_io import all_fixtures, load
 
 pytestmark = pytest.mark.filterwarnings("ignore")
 
-T = {"Q4_K": 1, "Q6_K": 2, "Q8_0": 3, "Q5_0": 4, "Q4_0": 5}
+T = {"Q4_K": 1, "Q6_K": 2, "Q8_0": 3, "Q5_0": 4, "Q4_0": 5, "Q5_K": 6}
 
 
 # ---------------------------------------------------------------- sizes --
@@ -33,6 +33,10 @@ def test_block_sizes_and_bits_per_weight(oracle_mod):
     # Q8_0: fp16 d + 32 int8 = 34 B; Q5_0: fp16 d + 4 B + 16 B = 22 B.
     assert o.block_bytes(T["Q8_0"]) == 34 and o.block_elems(T["Q8_0"]) == 32
     assert o.block_bytes(T["Q5_0"]) == 22 and o.block_elems(T["Q5_0"]) == 32
+    # "12 -- llama.cpp / GGUF", k-quants table: Q5_K at 5.5-5.7 bits/weight on
+    # 256-weight super-blocks; the reading's 176 bytes is the low end.
+    assert o.block_bytes(T["Q5_K"]) == 176 and o.block_elems(T["Q5_K"]) == 256
+    assert o.block_bytes(T["Q5_K"]) * 8 / 256 == 5.5
     # Row bytes: cols / elems * block bytes (the workload's 9,030-byte rows).
     assert o.row_bytes(T["Q6_K"], 11008) == 9030
     assert o.row_bytes(T["Q4_K"], 1024) * 256 == 147456
@@ -124,7 +128,7 @@ def test_q5_0_low_nibbles_follow_q4_0_convention(oracle_mod):
 
 # ------------------------------------------------------ round trips --
 
-@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0"])
+@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K"])
 def test_bytes_unpack_pack_bijection(oracle_mod, name):
     # Every byte of these blocks is used, so unpack followed by pack must give
     # back the same bytes (and unpack of that, the same fields).
@@ -135,10 +139,10 @@ def test_bytes_unpack_pack_bijection(oracle_mod, name):
     dbits = np.array([oracle_mod.float_to_half(float(v)) for v in d], np.uint16)
     dminbits = np.array([oracle_mod.float_to_half(float(v)) for v in dmin], np.uint16)
     # fp16 NaN payloads do not survive a float round trip; restore raw bits.
-    off = {"Q4_K": 0, "Q6_K": 208, "Q8_0": 0, "Q5_0": 0, "Q4_0": 0}[name]
+    off = {"Q4_K": 0, "Q6_K": 208, "Q8_0": 0, "Q5_0": 0, "Q4_0": 0, "Q5_K": 0}[name]
     raw_d = W.reshape(nb, bb)[:, off:off + 2].copy().view(np.uint16).reshape(nb)
     dbits = raw_d
-    if name == "Q4_K":
+    if name in ("Q4_K", "Q5_K"):
         dminbits = W.reshape(nb, bb)[:, 2:4].copy().view(np.uint16).reshape(nb)
     again = oracle_mod.pack(t, codes, sc, mins, dbits, dminbits)
     assert np.array_equal(again, W)
@@ -181,6 +185,56 @@ def test_q6k_q8_q5_code_ranges_round_trip(oracle_mod):
         assert np.all(d == 0.5)
 
 
+def test_q5k_is_q4k_plus_a_fifth_bit(oracle_mod):
+    # Q5_K (a reading of the GGUF layout; the pages give only its size) is
+    # Q4_K's super-block with a 32-byte high-bit plane inserted after the
+    # scales.  With every high bit clear it must decode exactly as the Q4_K
+    # block holding the same d, dmin, scale bytes and code bytes (a path
+    # pinned by the pages' Q4_K figures), and with every high bit set each
+    # code grows by exactly 16.  A wrong offset of qs, of the scales or of the
+    # plane, or a high bit added at the wrong weight, breaks one of the two.
+    nb = 64
+    W4 = synth.random_blocks("Q4_K", 1, 256 * nb, 31).reshape(nb, 144)
+    for fill, shift in ((0x00, 0), (0xFF, 16)):
+        W5 = np.zeros((nb, 176), np.uint8)
+        W5[:, :16] = W4[:, :16]
+        W5[:, 16:48] = fill
+        W5[:, 48:] = W4[:, 16:]
+        c4, sc4, m4, d4, dm4 = oracle_mod.unpack(1, W4.reshape(-1), nb)
+        c5, sc5, m5, d5, dm5 = oracle_mod.unpack(6, W5.reshape(-1), nb)
+        assert np.array_equal(c5, c4 + shift)
+        assert np.array_equal(sc5, sc4) and np.array_equal(m5, m4)
+        assert np.array_equal(d5, d4) and np.array_equal(dm5, dm4)
+        if shift == 0:
+            assert np.array_equal(oracle_mod.dequant(6, W5.reshape(-1), 1, 256 * nb),
+                                  oracle_mod.dequant(1, W4.reshape(-1), 1, 256 * nb))
+
+
+def test_q5k_high_bit_planes_select_their_weights(oracle_mod):
+    # One high bit at a time: bit b of qh[l] must raise exactly one code by
+    # 16 (and no other), and over all 256 (byte, bit) pairs each code is
+    # raised exactly once -- the plane is a bijection onto the weights, in
+    # the same low-half / high-half order as the nibbles of each 64-weight
+    # group (bit 2c + h of qh[l] belongs to the weight whose low nibble is
+    # half h of qs[32c + l]).
+    base = np.zeros((256, 176), np.uint8)
+    base[:, 0:2] = np.frombuffer(np.float16(1.0).tobytes(), np.uint8)
+    hit = np.zeros(256, int)
+    for k in range(256):
+        l, b = k // 8, k % 8
+        base[k, 16 + l] = 1 << b
+    codes, _, _, _, _ = oracle_mod.unpack(6, base.reshape(-1), 256)
+    for k in range(256):
+        l, b = k // 8, k % 8
+        (raised,) = np.nonzero(codes[k])
+        assert raised.size == 1 and codes[k, raised[0]] == 16
+        n = raised[0]
+        hit[n] += 1
+        # its low nibble lives in qs[32 (n // 64) + n % 32], half (n // 32) % 2
+        assert n % 32 == l and 2 * (n // 64) + (n // 32) % 2 == b
+    assert np.all(hit == 1)
+
+
 # --------------------------------------------- dequant formula checks --
 
 def test_q4k_formula_exact_in_fp32(oracle_mod):
@@ -197,8 +251,22 @@ def test_q4k_formula_exact_in_fp32(oracle_mod):
     assert np.array_equal(got, exact.astype(np.float32))
 
 
+def test_q5k_formula_exact_in_fp32(oracle_mod):
+    # As for Q4_K: d*sc (11 + 6 bits) times a 5-bit code stays within 24 bits,
+    # so only the final subtraction rounds.
+    W = synth.random_blocks("Q5_K", 8, 2048, 22)
+    codes, sc, mins, d, dmin = oracle_mod.unpack(6, W, 64)
+    ds = d[:, None].astype(np.float64) * sc[:, :8].astype(np.float64)
+    dm = dmin[:, None].astype(np.float64) * mins.astype(np.float64)
+    sub = np.repeat(np.arange(8), 32)
+    exact = ds[:, sub] * codes.astype(np.float64) - dm[:, sub]
+    got = oracle_mod.dequant(6, W, 8, 2048).reshape(64, 256)
+    assert np.array_equal(got, exact.astype(np.float32))
+    assert codes.min() == 0 and codes.max() == 31
+
+
 def test_zero_scale_block_is_zero(oracle_mod):
-    for name in ("Q4_K", "Q6_K", "Q8_0", "Q5_0"):
+    for name in ("Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q5_K"):
         W = synth.random_blocks(name, 2, 512, 22)
         bb, be, doff, dmoff = synth.GEOMETRY[name]
         B = W.reshape(-1, bb)
@@ -211,7 +279,7 @@ def test_zero_scale_block_is_zero(oracle_mod):
 
 # ------------------------------------------------------ dot products --
 
-@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0"])
+@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K"])
 @pytest.mark.parametrize("rows,cols,M", [(1, 256, 1), (3, 512, 2), (4, 1024, 3)])
 def test_gemv_matches_numpy_float64_matmul(oracle_mod, name, rows, cols, M):
     t = T[name]
@@ -331,11 +399,20 @@ def test_quantizer_exact_codes_k_quants(oracle_mod):
     c6, s6, _, _, _ = _codes(oracle_mod, 2, W6, 1)
     assert np.array_equal(c6[0], k6 + 32)
     assert np.all(s6[0, :16] == 127)
+    # Q5_K: the Q4_K construction with 31 steps; codes 0..31 come back.
+    k5 = rng.integers(0, 32, size=256)
+    k5[::32] = 0
+    k5[1::32] = 31
+    w5 = (lo + k5 * (hi - lo) / 31.0).astype(np.float32)
+    W5 = oracle_mod.quantize(6, w5.reshape(1, -1))
+    c5, s5, m5, _, _ = _codes(oracle_mod, 6, W5, 1)
+    assert np.array_equal(c5[0], k5)
+    assert np.all(s5[0, :8] == 63) and np.all(m5[0] == 63)
 
 
 def test_quantizer_zero_blocks(oracle_mod):
     # An all-zero block takes the zero-divisor path: d = 0 and the offset code.
-    for t, n, code in ((1, 256, 0), (2, 256, 32), (3, 32, 0), (4, 32, 16), (5, 32, 8)):
+    for t, n, code in ((1, 256, 0), (2, 256, 32), (3, 32, 0), (4, 32, 16), (5, 32, 8), (6, 256, 0)):
         W = oracle_mod.quantize(t, np.zeros((1, n), np.float32))
         codes, sc, mins, d, dmin = _codes(oracle_mod, t, W, 1)
         assert np.all(codes[0, :n] == code) and d[0] == 0.0
