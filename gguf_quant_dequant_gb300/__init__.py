@@ -5,7 +5,7 @@ device pointers, sizes and the current CUDA stream of PyTorch tensors, and
 raises QKError on a non-zero status.  There is no CPU fallback: if libqk.so
 has not been built, load() raises.
 
-Type ids: Q4_K = 1, Q6_K = 2, Q8_0 = 3, Q5_0 = 4, Q4_0 = 5.
+Type ids: Q4_K = 1, Q6_K = 2, Q8_0 = 3, Q5_0 = 4, Q4_0 = 5, Q5_K = 6.
 """
 from __future__ import annotations
 
@@ -13,8 +13,8 @@ import ctypes
 import os
 import threading
 
-Q4_K, Q6_K, Q8_0, Q5_0, Q4_0 = 1, 2, 3, 4, 5
-TYPES = {"Q4_K": Q4_K, "Q6_K": Q6_K, "Q8_0": Q8_0, "Q5_0": Q5_0, "Q4_0": Q4_0}
+Q4_K, Q6_K, Q8_0, Q5_0, Q4_0, Q5_K = 1, 2, 3, 4, 5, 6
+TYPES = {"Q4_K": Q4_K, "Q6_K": Q6_K, "Q8_0": Q8_0, "Q5_0": Q5_0, "Q4_0": Q4_0, "Q5_K": Q5_K}
 OUT_F32, OUT_BF16 = 0, 1
 STATUS = {0: "QK_OK", 1: "QK_ERR_TYPE", 2: "QK_ERR_SHAPE", 3: "QK_ERR_ALIGN", 4: "QK_ERR_NULL",
           5: "QK_ERR_WORKSPACE", 6: "QK_ERR_CUDA", 7: "QK_ERR_TIMEOUT", 8: "QK_ERR_ARG",

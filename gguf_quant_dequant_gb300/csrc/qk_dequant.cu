@@ -57,9 +57,9 @@ __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t* __restrict__
     if (sc)
         for (int j = 0; j < 16; ++j) {
             int v = 0;
-            if constexpr (T == T_Q4_K) {
+            if constexpr (T == T_Q4_K || T == T_Q5_K) {
                 uint32_t s, m;
-                if (j < 8) { F::scale_min(blk, j, s, m); v = (int)s; }
+                if (j < 8) { Fmt<T_Q4_K>::scale_min(blk, j, s, m); v = (int)s; }
             } else if constexpr (T == T_Q6_K) {
                 v = (int)(int8_t)blk[192 + j];
             }
@@ -68,14 +68,14 @@ __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t* __restrict__
     if (mins)
         for (int j = 0; j < 8; ++j) {
             uint32_t s = 0, m = 0;
-            if constexpr (T == T_Q4_K) F::scale_min(blk, j, s, m);
+            if constexpr (T == T_Q4_K || T == T_Q5_K) Fmt<T_Q4_K>::scale_min(blk, j, s, m);
             mins[b * 8 + j] = (uint8_t)m;
         }
     if (d) {
         if constexpr (T == T_Q6_K) d[b] = h2f(ld_u16(blk + 208));
         else d[b] = h2f(ld_u16(blk));
     }
-    if (dmin) dmin[b] = (T == T_Q4_K) ? h2f(ld_u16(blk + 2)) : 0.0f;
+    if (dmin) dmin[b] = (T == T_Q4_K || T == T_Q5_K) ? h2f(ld_u16(blk + 2)) : 0.0f;
 }
 
 template <int T>
@@ -99,6 +99,7 @@ cudaError_t launch_dequant(int type, const uint8_t* W, int64_t rows, int64_t col
     case T_Q8_0: return dequant_t<T_Q8_0>(W, rows, cols, out, out_bf16, s);
     case T_Q5_0: return dequant_t<T_Q5_0>(W, rows, cols, out, out_bf16, s);
     case T_Q4_0: return dequant_t<T_Q4_0>(W, rows, cols, out, out_bf16, s);
+    case T_Q5_K: return dequant_t<T_Q5_K>(W, rows, cols, out, out_bf16, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -113,6 +114,7 @@ cudaError_t launch_unpack(int type, const uint8_t* W, int64_t nblocks, int16_t* 
     case T_Q8_0: unpack_kernel<T_Q8_0><<<grid, 256, 0, s>>>(W, nblocks, codes, sc, mins, d, dmin); break;
     case T_Q5_0: unpack_kernel<T_Q5_0><<<grid, 256, 0, s>>>(W, nblocks, codes, sc, mins, d, dmin); break;
     case T_Q4_0: unpack_kernel<T_Q4_0><<<grid, 256, 0, s>>>(W, nblocks, codes, sc, mins, d, dmin); break;
+    case T_Q5_K: unpack_kernel<T_Q5_K><<<grid, 256, 0, s>>>(W, nblocks, codes, sc, mins, d, dmin); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -12,6 +12,8 @@
 //   Q8_0  w = d*q                      ("Hitchhiker's Guide", 11.1)
 //   Q5_0  w = d*(q - 16)
 //   Q4_0  w = d*(q - 8)                ("Hitchhiker's Guide", 11.1 figure)
+//   Q5_K  w = (d*sc)*q - dmin*m, 5-bit q (the GGUF k-quant layout: only the
+//         size, 5.5 bits/weight, is on the pages)
 // Each product before the last rounding is exact in fp32 (an fp16 d has 11
 // significant bits, a scale at most 8, a code at most 8), so the weights are
 // bit-identical to the formula evaluated in fp32 whatever the contraction.
@@ -22,7 +24,7 @@
 
 namespace qk {
 
-enum : int { T_Q4_K = 1, T_Q6_K = 2, T_Q8_0 = 3, T_Q5_0 = 4, T_Q4_0 = 5 };
+enum : int { T_Q4_K = 1, T_Q6_K = 2, T_Q8_0 = 3, T_Q5_0 = 4, T_Q4_0 = 5, T_Q5_K = 6 };
 
 // 16-bit and 32-bit little-endian loads from a 2-byte-aligned address that
 // never touch a byte outside [p, p + size).
@@ -85,6 +87,32 @@ template <> struct Fmt<T_Q4_K> {
     __device__ static __forceinline__ void params(const uint8_t* blk, int u, int h, float& A, float& B) {
         uint32_t sc, m;
         scale_min(blk, 2 * (u >> 1) + h, sc, m);
+        A = h2f(ld_u16(blk)) * (float)sc;
+        B = h2f(ld_u16(blk + 2)) * (float)m;
+    }
+};
+
+// ---------------------------------------------------------------- Q5_K --
+// Bytes 0-1 d, 2-3 dmin, 4-15 scales (packed as Q4_K's), 16-47 qh, 48-175 qs.
+// Weight 64c + 32h + l: low 4 bits are nibble h of qs[32c + l] (as Q4_K),
+// the fifth bit is bit 2c + h of qh[l].  Units and halves as Q4_K's.
+template <> struct Fmt<T_Q5_K> {
+    static constexpr int BB = 176, BE = 256, UPB = 8, OFF = 0;
+    __device__ static __forceinline__ int koff(int u, int h) { return 64 * (u >> 1) + 32 * h + 16 * (u & 1); }
+    __device__ static __forceinline__ void codes16(const uint8_t* blk, int u, int h, int (&c)[16]) {
+        const int cg = u >> 1, hp = u & 1;
+        const uint4 q4 = *reinterpret_cast<const uint4*>(blk + 48 + 32 * cg + 16 * hp);
+        const uint4 h4 = *reinterpret_cast<const uint4*>(blk + 16 + 16 * hp);
+        const uint32_t q[4] = {q4.x, q4.y, q4.z, q4.w};
+        const uint32_t hb[4] = {h4.x, h4.y, h4.z, h4.w};
+        const int sh = 2 * cg + h;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            c[i] = (int)(((byte_of(q, i) >> (4 * h)) & 15u) | (((byte_of(hb, i) >> sh) & 1u) << 4));
+    }
+    __device__ static __forceinline__ void params(const uint8_t* blk, int u, int h, float& A, float& B) {
+        uint32_t sc, m;
+        Fmt<T_Q4_K>::scale_min(blk, 2 * (u >> 1) + h, sc, m);
         A = h2f(ld_u16(blk)) * (float)sc;
         B = h2f(ld_u16(blk + 2)) * (float)m;
     }

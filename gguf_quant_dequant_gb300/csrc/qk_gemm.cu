@@ -149,7 +149,7 @@ struct Args {
 // (unit, half) of the 16 weights that start `o` weights into a block.
 template <int T>
 __device__ __forceinline__ void locate(int o, int& u, int& h) {
-    if constexpr (T == T_Q4_K) {          // koff = 64(u>>1) + 32h + 16(u&1)
+    if constexpr (T == T_Q4_K || T == T_Q5_K) {   // koff = 64(u>>1) + 32h + 16(u&1)
         u = 2 * (o >> 6) + ((o >> 4) & 1);
         h = (o >> 5) & 1;
     } else if constexpr (T == T_Q6_K) {   // koff = 128(u>>2) + 32((u>>1&1) + 2h) + 16(u&1)
@@ -223,6 +223,19 @@ __device__ __forceinline__ void q4k16(const uint8_t* blk, int c, int qq, float2 
     for (int i = 0; i < 4; ++i) four_hi((w[i] >> sh) & 0x0F0F0F0Fu, a, o, pk[2 * i], pk[2 * i + 1]);
 }
 
+// 16 Q5_K weights of k-block c, quarter qq: the Q4_K codes (at byte 48 of
+// the super-block) with bit 2c + qq/2 of qh[16 (qq & 1) + i] as the fifth bit
+// of code i; operands from q4k_operands (the header is Q4_K's).
+__device__ __forceinline__ void q5k16(const uint8_t* blk, int c, int qq, float2 a, float2 o, uint32_t (&pk)[8]) {
+    const uint4 q = lds128_g(blk + 48 + 32 * c + 16 * (qq & 1));
+    const uint4 e = lds128_g(blk + 16 + 16 * (qq & 1));
+    const uint32_t sh = 4u * (uint32_t)(qq >> 1), hs = 2u * (uint32_t)c + (uint32_t)(qq >> 1);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w}, hb[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        four_hi(((w[i] >> sh) & 0x0F0F0F0Fu) | (((hb[i] >> hs) & 0x01010101u) << 4), a, o, pk[2 * i], pk[2 * i + 1]);
+}
+
 // Q8_0: 16 weights of one 34-byte block (2-byte aligned), half `half`:
 // w = d*q = 128d*(256 + u/128) - 32896d with u = q + 128.
 __device__ __forceinline__ void fast16_q80(const uint8_t* blk, int half, uint32_t (&pk)[8]) {
@@ -289,6 +302,32 @@ __device__ __forceinline__ void q4k64(const uint8_t* blk, int kk, uint32_t (&pk)
         four_hi(w[i] & 0x0F0F0F0Fu, make_float2(ds0, ds0), make_float2(o0, o0), pk[2 * i], pk[2 * i + 1]);
         four_hi((w[i] >> 4) & 0x0F0F0F0Fu, make_float2(ds1, ds1), make_float2(o1, o1), pk[16 + 2 * i],
                 pk[17 + 2 * i]);
+    }
+}
+
+// Q5_K (blk 16-byte aligned): q4k64's header and codes (at byte 48) with the
+// fifth bits of k-block kk: bit 2kk of qh[l] for the low-nibble code of byte
+// 32kk + l, bit 2kk + 1 for its high-nibble code.
+__device__ __forceinline__ void q5k64(const uint8_t* blk, int kk, uint32_t (&pk)[32]) {
+    const uint4 h = lds128_g(blk);
+    const uint32_t scw = kk < 2 ? (h.y & 0x3F3F3F3Fu) : ((h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u));
+    const uint32_t mw = kk < 2 ? (h.z & 0x3F3F3F3Fu) : (((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u));
+    const uint32_t sh = 16u * (uint32_t)(kk & 1);
+    const float d = h2f(h.x & 0xFFFFu), dmin = h2f(h.x >> 16);
+    const float ds0 = d * (float)((scw >> sh) & 0xFFu), ds1 = d * (float)((scw >> (sh + 8u)) & 0xFFu);
+    const float dm0 = dmin * (float)((mw >> sh) & 0xFFu), dm1 = dmin * (float)((mw >> (sh + 8u)) & 0xFFu);
+    const float o0 = -(128.0f * ds0 + dm0), o1 = -(128.0f * ds1 + dm1);
+    const uint4 c0 = lds128_g(blk + 48 + 32 * kk), c1 = lds128_g(blk + 64 + 32 * kk);
+    const uint4 e0 = lds128_g(blk + 16), e1 = lds128_g(blk + 32);
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const uint32_t e[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t b = e[i] >> (2 * kk);   // bit 0: low code's fifth bit, bit 1: high code's
+        four_hi((w[i] & 0x0F0F0F0Fu) | ((b << 4) & 0x10101010u), make_float2(ds0, ds0), make_float2(o0, o0),
+                pk[2 * i], pk[2 * i + 1]);
+        four_hi(((w[i] >> 4) & 0x0F0F0F0Fu) | ((b << 3) & 0x10101010u), make_float2(ds1, ds1),
+                make_float2(o1, o1), pk[16 + 2 * i], pk[17 + 2 * i]);
     }
 }
 
@@ -559,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const uint8_t* mbp = pk + r * K::SLOT + (int)(st & 15);
             const int kbm = m * K::KPM;
             float2 qa[4], qo[4];
-            if constexpr (T == T_Q4_K) {
+            if constexpr (T == T_Q4_K || T == T_Q5_K) {
                 if (live) q4k_operands(mbp, qq >> 1, qa, qo);
             }
 #pragma unroll
@@ -575,6 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     uint32_t pk8[8];
                     if (live && (int64_t)kb * kBK < kq) {
                         if constexpr (T == T_Q4_K) q4k16(mbp, kk, qq, qa[kk], qo[kk], pk8);
+                        else if constexpr (T == T_Q5_K) q5k16(mbp, kk, qq, qa[kk], qo[kk], pk8);
                         else if constexpr (T == T_Q6_K) fast16_q6k(mbp, kk, qq, pk8);
                         else if constexpr (T == T_Q8_0) fast16_q80(mbp + (2 * kk + (qq >> 1)) * 34, qq & 1, pk8);
                         else generic16<T>(mbp, kk * kBK + 16 * qq, pk8);
@@ -824,6 +864,8 @@ __global__ void __launch_bounds__(kSkThreads, 1) gemm_skinny_kernel(const __grid
                         const uint8_t* blk = packed + ps * G::STAGE + r * G::BOXW + (int)(st & 15);
                         if constexpr (T == T_Q4_K) {
                             q4k64(blk, ph, pk);
+                        } else if constexpr (T == T_Q5_K) {
+                            q5k64(blk, ph, pk);
                         } else if constexpr (T == T_Q6_K) {
                             q6k64(blk, ph, pk);
                         } else {
@@ -1013,6 +1055,7 @@ GemmPlan plan_gemm(int type, int64_t rows, int64_t cols, int64_t M, int sms) {
     case T_Q8_0: rb = cols / 32 * 34; break;
     case T_Q5_0: rb = cols / 32 * 22; break;
     case T_Q4_0: rb = cols / 32 * 18; break;
+    case T_Q5_K: rb = cols / 256 * 176; break;
     }
     pl.skinny = M <= gm::kSkinnyBN && rb % 16 == 0;
     const int64_t kpm = pl.skinny ? 4 : k_blocks_per_macro(type);   // the small-batch kernel's macro-blocks are 256 wide
@@ -1069,6 +1112,7 @@ cudaError_t launch_gemm(int type, const GemmPlan& pl, const uint8_t* W, int64_t 
     case T_Q8_0: a.row_bytes = cols / 32 * 34; break;
     case T_Q5_0: a.row_bytes = cols / 32 * 22; break;
     case T_Q4_0: a.row_bytes = cols / 32 * 18; break;
+    case T_Q5_K: a.row_bytes = cols / 256 * 176; break;
     default: return cudaErrorInvalidValue;
     }
     a.total16 = (rows * a.row_bytes) & ~(int64_t)15;
@@ -1079,6 +1123,7 @@ cudaError_t launch_gemm(int type, const GemmPlan& pl, const uint8_t* W, int64_t 
     case T_Q8_0: e = gemm_t<T_Q8_0>(a, pl, map, s); break;
     case T_Q5_0: e = gemm_t<T_Q5_0>(a, pl, map, s); break;
     case T_Q4_0: e = gemm_t<T_Q4_0>(a, pl, map, s); break;
+    case T_Q5_K: e = gemm_t<T_Q5_K>(a, pl, map, s); break;
     }
     if (e != cudaSuccess || pl.splits <= 1) return e;
     // Add the partials in split order.

@@ -154,6 +154,50 @@ template <> struct Lane<T_Q4_K> {
     }
 };
 
+// Q5_K: the Q4_K lane mapping (lane l -> super-block l/4, code group
+// c = l%4, x-blocks 2l and 2l+1) with each code's fifth bit merged in from
+// the 32-byte plane: bit 2c of qh[k] belongs to the low-nibble code of
+// qs[32c + k], bit 2c + 1 to its high-nibble code.  Codes 0..31 are valid
+// signed bytes for the signed x signed dp4a.  w = (d*sc)*q - dmin*m.
+template <> struct Lane<T_Q5_K> {
+    int sb, c, sh;
+    bool hi4;  // c >= 2: sub-blocks 4..7, whose 6-bit fields are split
+    __device__ __forceinline__ explicit Lane(int lane) : sb(lane >> 2), c(lane & 3), sh(16 * (lane & 1)), hi4(c >= 2) {}
+    __device__ __forceinline__ bool valid(int nblk) const { return sb < nblk; }
+    __device__ __forceinline__ void xblocks(int lane, int& j0, int& j1) const { j0 = 2 * lane; j1 = 2 * lane + 1; }
+    __device__ __forceinline__ float dot(const uint8_t* seg, const XL& x, int nblk) const {
+        const uint8_t* blk = seg + sb * 176;
+        const uint4 h = lds128(blk);
+        const uint4 e0 = lds128(blk + 16), e1 = lds128(blk + 32);                    // qh[0..31]
+        const uint4 q0 = lds128(blk + 48 + 32 * c), q1 = lds128(blk + 64 + 32 * c);  // qs[32c..32c+31]
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        const uint32_t e[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+        uint32_t lo[2][4], hi[2][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t b = e[i] >> (2 * c);   // bit 0: low code's fifth bit, bit 1: high code's
+            lo[i >> 2][i & 3] = (w[i] & 0x0F0F0F0Fu) | ((b << 4) & 0x10101010u);
+            hi[i >> 2][i & 3] = ((w[i] >> 4) & 0x0F0F0F0Fu) | ((b << 3) & 0x10101010u);
+        }
+        int A0 = 0, B0 = 0, C0 = 0, A1 = 0, B1 = 0, C1 = 0;
+        dot16(lo[0], x, 0, 0, A0, B0, C0);
+        dot16(lo[1], x, 0, 4, A0, B0, C0);
+        dot16(hi[0], x, 1, 0, A1, B1, C1);
+        dot16(hi[1], x, 1, 4, A1, B1, C1);
+        // Scales and mins of sub-blocks 2c, 2c+1: the Q4_K packing.
+        const uint32_t lsc = hi4 ? h.w : h.y, lm = hi4 ? (h.w >> 4) : h.z;
+        const uint32_t lmask = hi4 ? 15u : 63u, hmask = hi4 ? 3u : 0u;
+        const uint32_t sc0 = ((lsc >> sh) & lmask) | (((h.y >> (sh + 6)) & hmask) << 4);
+        const uint32_t sc1 = ((lsc >> (sh + 8)) & lmask) | (((h.y >> (sh + 14)) & hmask) << 4);
+        const uint32_t m0 = ((lm >> sh) & lmask) | (((h.z >> (sh + 6)) & hmask) << 4);
+        const uint32_t m1 = ((lm >> (sh + 8)) & lmask) | (((h.z >> (sh + 14)) & hmask) << 4);
+        const float d = h2f(h.x & 0xFFFFu), dmin = h2f(h.x >> 16);
+        const float f0 = limbs3_to_f(A0, B0, C0) * x.meta[0].x;
+        const float f1 = limbs3_to_f(A1, B1, C1) * x.meta[1].x;
+        return d * fmaf((float)sc0, f0, (float)sc1 * f1) - dmin * fmaf((float)m0, x.meta[0].w, (float)m1 * x.meta[1].w);
+    }
+};
+
 // Byte k of v as an exact fp32 (0..255), via the 2^23 magic constant.
 __device__ __forceinline__ float byte_to_f(uint32_t v, uint32_t sel) {
     return __uint_as_float(__byte_perm(v, 0x4B000000u, sel)) - 8388608.0f;

@@ -8,6 +8,7 @@
 //        sc_f = (hi - lo) / 15, m_f = -lo; d = fp16(max sc_f / 63),
 //        dmin = fp16(max m_f / 63); sc = cr(sc_f / d, 0, 63),
 //        m = cr(m_f / dmin, 0, 63); q = cr((w + dmin*m) / (d*sc), 0, 15).
+//   Q5_K, the same with 31 in place of 15 (codes 0..31).
 //   Q6_K, per 16 weights: s = max|w| / 32; d = fp16(max s / 127);
 //        sc = cr(s / d, -128, 127); q = cr(w / (d*sc), -32, 31) + 32.
 //   Q8_0 / Q5_0 / Q4_0, per 32 weights: d = fp16(max|w| / 127, 15, 7);
@@ -102,6 +103,60 @@ __device__ __forceinline__ void lane_q4k(const float (&v)[32], int lane, bool li
 #pragma unroll
         for (int k = 0; k < 8; ++k) st_u32(blk + 16 + 16 * j + 4 * k, wd[k]);   // 16 + 32 (j / 2)
     }
+    if (j < 4) {
+        blk[4 + j] = (uint8_t)(s | ((s4 >> 4) << 6));
+        blk[8 + j] = (uint8_t)(m | ((m4 >> 4) << 6));
+        blk[12 + j] = (uint8_t)((s4 & 15) | ((m4 & 15) << 4));
+    }
+    if (j == 0) st_u32(blk, db | (dmb << 16));
+}
+
+// Q5_K: as Q4_K with 31 steps; the low 4 bits of each code go where Q4_K's
+// codes go (from byte 48), the fifth bit of sub-block j's code l is bit j of
+// qh[l] (byte 16 + l).  Lane j writes qh bytes 4j .. 4j+3, gathering bit j'
+// of each from lane j' of its super-block.
+__device__ __forceinline__ uint32_t spread4(uint32_t x) { return (x * 0x00204081u) & 0x01010101u; }
+
+__device__ __forceinline__ void lane_q5k(const float (&v)[32], int lane, bool live, uint8_t* blk) {
+    const int j = lane & 7;
+    float lo = 0.0f, hi = v[0];
+#pragma unroll
+    for (int l = 0; l < 32; ++l) {
+        if (v[l] < lo) lo = v[l];
+        if (v[l] > hi) hi = v[l];
+    }
+    const float scf = __fdiv_rn(__fsub_rn(hi, lo), 31.0f), mf = -lo;
+    const uint32_t db = half_bits(__fdiv_rn(group_max_pos<8>(scf), 63.0f));
+    const uint32_t dmb = half_bits(__fdiv_rn(group_max_pos<8>(mf), 63.0f));
+    const float d = half_val(db), dmin = half_val(dmb);
+    const int s = d > 0.0f ? cr(__fdiv_rn(scf, d), 0, 63) : 0;
+    const int m = dmin > 0.0f ? cr(__fdiv_rn(mf, dmin), 0, 63) : 0;
+    const float ds = __fmul_rn(d, (float)s), dm = __fmul_rn(dmin, (float)m);
+    int q[32];
+#pragma unroll
+    for (int l = 0; l < 32; ++l) q[l] = ds > 0.0f ? cr(__fdiv_rn(__fadd_rn(v[l], dm), ds), 0, 31) : 0;
+    uint32_t wd[8], hb = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t mine = bytes4(&q[4 * k]) & 0x0F0F0F0Fu;
+        const uint32_t odd = __shfl_down_sync(kFull, mine, 1);
+        wd[k] = mine | (odd << 4);
+    }
+#pragma unroll
+    for (int l = 0; l < 32; ++l) hb |= (uint32_t)(q[l] >> 4) << l;
+    uint32_t qhw = 0;
+#pragma unroll
+    for (int jp = 0; jp < 8; ++jp) {
+        const uint32_t t = __shfl_sync(kFull, hb, (lane & ~7) + jp);
+        qhw |= spread4((t >> (4 * j)) & 15u) << jp;
+    }
+    const int s4 = __shfl_down_sync(kFull, s, 4), m4 = __shfl_down_sync(kFull, m, 4);
+    if (!live) return;
+    if ((j & 1) == 0) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) st_u32(blk + 48 + 16 * j + 4 * k, wd[k]);   // 48 + 32 (j / 2)
+    }
+    st_u32(blk + 16 + 4 * j, qhw);
     if (j < 4) {
         blk[4 + j] = (uint8_t)(s | ((s4 >> 4) << 6));
         blk[8 + j] = (uint8_t)(m | ((m4 >> 4) << 6));
@@ -220,7 +275,7 @@ __device__ __forceinline__ void lane_small(const float (&v)[32], bool live, uint
 template <int T>
 __global__ void __launch_bounds__(kWarps * 32) quantize_kernel(const float* __restrict__ w, int64_t ngroups,
                                                                 uint8_t* __restrict__ out) {
-    constexpr bool kK = T == T_Q4_K || T == T_Q6_K;
+    constexpr bool kK = T == T_Q4_K || T == T_Q6_K || T == T_Q5_K;
     constexpr int kBB = Fmt<T>::BB;
     __shared__ uint32_t buf[kWarps][kBufWords];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -246,6 +301,7 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_kernel(const float* __re
     }
     uint8_t* sb = reinterpret_cast<uint8_t*>(buf[warp]);
     if constexpr (T == T_Q4_K) lane_q4k(v, lane, live, sb + (lane >> 3) * kBB);
+    else if constexpr (T == T_Q5_K) lane_q5k(v, lane, live, sb + (lane >> 3) * kBB);
     else if constexpr (T == T_Q6_K) lane_q6k(v, lane, live, sb + (lane >> 3) * kBB);
     else lane_small<T>(v, live, sb + lane * kBB);
     __syncwarp();
@@ -277,6 +333,7 @@ cudaError_t launch_quantize(int type, const float* w, int64_t rows, int64_t cols
     case T_Q8_0: return qz::launch_t<T_Q8_0>(w, ngroups, out, s);
     case T_Q5_0: return qz::launch_t<T_Q5_0>(w, ngroups, out, s);
     case T_Q4_0: return qz::launch_t<T_Q4_0>(w, ngroups, out, s);
+    case T_Q5_K: return qz::launch_t<T_Q5_K>(w, ngroups, out, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -24,6 +24,13 @@
  *         ("Hitchhiker's Guide", section 11.1, Q4_0 block figure; "How LLM
  *         Inference Engines Work", "Loading GGUF Models", the Q4_0
  *         dequantizer.)
+ *   Q5_K  256 weights in 176 bytes: fp16 d, fp16 dmin, the 12 scale bytes
+ *         of Q4_K, 32 bytes of fifth code bits (bit 2c + h of byte l for
+ *         weight 64c + 32h + l), 128 bytes of low nibbles placed as Q4_K's
+ *         codes; weight = (d*sc)*q - dmin*m, q in 0..31.  The pages give only
+ *         its size ("12 -- llama.cpp / GGUF", "Other k-quants at a glance":
+ *         256-weight super-block, 5.5-5.7 bits/weight); the layout is the
+ *         GGUF k-quant one.
  * The bit placement inside the Q4_K scale bytes, the Q6_K code bytes and the
  * Q5_0 block is the k-quant / GGUF packing: low nibbles of a group of bytes
  * are the first weights, high nibbles the next ("How LLM Inference Engines
@@ -60,7 +67,7 @@ extern "C" {
 #endif
 
 /* Quant types.  The numbers are this library's own. */
-typedef enum { QK_Q4_K = 1, QK_Q6_K = 2, QK_Q8_0 = 3, QK_Q5_0 = 4, QK_Q4_0 = 5 } qk_type;
+typedef enum { QK_Q4_K = 1, QK_Q6_K = 2, QK_Q8_0 = 3, QK_Q5_0 = 4, QK_Q4_0 = 5, QK_Q5_K = 6 } qk_type;
 
 typedef enum {
     QK_OK = 0,
@@ -112,6 +119,7 @@ qk_status qk_dequant(int type, const void* W, int64_t rows, int64_t cols,
  *        sc_f = (hi - lo)/15, m_f = -lo; d = fp16(max sc_f / 63),
  *        dmin = fp16(max m_f / 63); sc = cr(sc_f/d, 0..63),
  *        m = cr(m_f/dmin, 0..63); q = cr((w + dmin*m) / (d*sc), 0..15).
+ *   Q5_K the same with 31 in place of 15.
  *   Q6_K per 16 weights: s = max|w| / 32, d = fp16(max s / 127),
  *        sc = cr(s/d, -128..127), q = cr(w / (d*sc), -32..31) + 32.
  *   Q8_0 / Q5_0 / Q4_0 per 32: d = fp16(max|w| / 127 | 15 | 7),
@@ -277,7 +285,8 @@ qk_status qk_device_status(void* stream);
  * Versions 2 and 3, little-endian.  The value-type codes (0 u8, 1 i8, 2 u16,
  * 3 i16, 4 u32, 5 i32, 6 f32, 7 bool, 8 string, 9 array, 10 u64, 11 i64,
  * 12 f64), the ggml tensor types (0 F32, 1 F16, 2 Q4_0, 6 Q5_0, 8 Q8_0,
- * 12 Q4_K, 14 Q6_K, 30 BF16 are sized here; others are listed with nbytes 0)
+ * 12 Q4_K, 13 Q5_K, 14 Q6_K, 30 BF16 are sized here; others are listed with
+ * nbytes 0)
  * and the "general.alignment" key (uint32 power of two, default 32) follow
  * the GGUF specification the page cites.
  * Every length, count and offset is checked against the image before use;

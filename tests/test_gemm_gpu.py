@@ -27,6 +27,7 @@ CASES = [
     ("Q6_K", 130, 512, 1100),    # three token tiles, ragged rows
     ("Q5_0", 128, 320, 513),     # second tile holds a single token
     ("Q4_0", 200, 1056, 77),
+    ("Q5_K", 200, 512, 300),     # the wide kernel: ragged rows, a partial second token tile
     # Skinny pipeline (M <= 64): fewer k-blocks than operand stages, a half
     # k-block at the end, ragged rows, one token.
     ("Q4_K", 130, 256, 40),
@@ -34,6 +35,7 @@ CASES = [
     ("Q5_0", 257, 2080, 48),
     ("Q6_K", 129, 1536, 2),
     ("Q4_0", 128, 64 * 32, 63),
+    ("Q5_K", 130, 768, 40),
 ]
 
 
@@ -92,6 +94,7 @@ SPLIT_CASES = [
     ("Q5_0", 96, 5120, 9),
     ("Q4_K", 130, 2048, 1),
     ("Q4_0", 64, 8192, 5),
+    ("Q5_K", 300, 8192, 16),
 ]
 
 

@@ -22,6 +22,7 @@ CASES = [
     ("Q8_0", 130, 512),
     ("Q5_0", 17, 256),
     ("Q4_0", 40, 4096),
+    ("Q5_K", 96, 2048),
 ]
 
 
