@@ -8,7 +8,7 @@ The arithmetic lives in ``qk_oracle.c`` (scalar C, fp32 weights in the order
 the formulas state, fp64 accumulation).  This module compiles it with gcc on
 first use and wraps it with numpy in / numpy out functions.
 
-Type ids: Q4_K=1, Q6_K=2, Q8_0=3, Q5_0=4, Q4_0=5, Q5_K=6.
+Type ids: Q4_K=1, Q6_K=2, Q8_0=3, Q5_0=4, Q4_0=5, Q5_K=6, Q2_K=7, Q3_K=8.
 """
 from __future__ import annotations
 
@@ -19,8 +19,9 @@ import threading
 
 import numpy as np
 
-Q4_K, Q6_K, Q8_0, Q5_0, Q4_0, Q5_K = 1, 2, 3, 4, 5, 6
-TYPES = {"Q4_K": Q4_K, "Q6_K": Q6_K, "Q8_0": Q8_0, "Q5_0": Q5_0, "Q4_0": Q4_0, "Q5_K": Q5_K}
+Q4_K, Q6_K, Q8_0, Q5_0, Q4_0, Q5_K, Q2_K, Q3_K = 1, 2, 3, 4, 5, 6, 7, 8
+TYPES = {"Q4_K": Q4_K, "Q6_K": Q6_K, "Q8_0": Q8_0, "Q5_0": Q5_0, "Q4_0": Q4_0, "Q5_K": Q5_K, "Q2_K": Q2_K,
+         "Q3_K": Q3_K}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "qk_oracle.c")
@@ -122,13 +123,13 @@ def float_to_bf16_array(a: np.ndarray) -> np.ndarray:
 
 def unpack(t: int, blocks: np.ndarray, nblocks: int):
     """Returns (codes int16 [nblocks, elems], sc int16 [nblocks, 16],
-    mins uint8 [nblocks, 8], d f32 [nblocks], dmin f32 [nblocks])."""
+    mins uint8 [nblocks, 16], d f32 [nblocks], dmin f32 [nblocks])."""
     blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
     assert blocks.size >= nblocks * block_bytes(t)
     be = block_elems(t)
     codes = np.zeros((nblocks, be), np.int16)
     sc = np.zeros((nblocks, 16), np.int16)
-    mins = np.zeros((nblocks, 8), np.uint8)
+    mins = np.zeros((nblocks, 16), np.uint8)
     d = np.zeros(nblocks, np.float32)
     dmin = np.zeros(nblocks, np.float32)
     _check(lib().oq_unpack(t, _ptr(blocks), nblocks, _ptr(codes), _ptr(sc), _ptr(mins),
@@ -142,7 +143,7 @@ def pack(t: int, codes: np.ndarray, sc: np.ndarray | None = None, mins: np.ndarr
     codes = np.ascontiguousarray(codes, dtype=np.int16).reshape(-1, be)
     nb = codes.shape[0]
     sc = np.zeros((nb, 16), np.int16) if sc is None else np.ascontiguousarray(sc, np.int16).reshape(nb, 16)
-    mins = np.zeros((nb, 8), np.uint8) if mins is None else np.ascontiguousarray(mins, np.uint8).reshape(nb, 8)
+    mins = np.zeros((nb, 16), np.uint8) if mins is None else np.ascontiguousarray(mins, np.uint8).reshape(nb, 16)
     d_bits = np.zeros(nb, np.uint16) if d_bits is None else np.ascontiguousarray(d_bits, np.uint16).reshape(nb)
     dmin_bits = (np.zeros(nb, np.uint16) if dmin_bits is None
                  else np.ascontiguousarray(dmin_bits, np.uint16).reshape(nb))

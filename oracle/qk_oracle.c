@@ -30,7 +30,8 @@
  * (see the per-type comments).  Q5_K appears on the pages only as 5.5-5.7
  * bits/weight on 256-weight super-blocks ([LC] "Other k-quants at a
  * glance"); its whole layout is a reading (the GGUF k-quant one, see
- * unpack_q5_K).
+ * unpack_q5_K).  So are Q2_K (2.5-2.6 bits/weight there) and Q3_K (3.4-4.0),
+ * see unpack_q2_K and unpack_q3_K.
  *
  * All arithmetic that produces a weight is fp32 in the order the formulas
  * state; dot products accumulate in fp64.  Compile with -ffp-contract=off so
@@ -43,7 +44,7 @@
 
 /* Type ids of the oracle (same numbers as the library's public enum; both
  * sides define them independently). */
-enum { OQ_Q4_K = 1, OQ_Q6_K = 2, OQ_Q8_0 = 3, OQ_Q5_0 = 4, OQ_Q4_0 = 5, OQ_Q5_K = 6 };
+enum { OQ_Q4_K = 1, OQ_Q6_K = 2, OQ_Q8_0 = 3, OQ_Q5_0 = 4, OQ_Q4_0 = 5, OQ_Q5_K = 6, OQ_Q2_K = 7, OQ_Q3_K = 8 };
 
 /* ------------------------------------------------------------------------ */
 /* Sizes                                                                    */
@@ -61,6 +62,8 @@ int oq_block_bytes(int type) {
     case OQ_Q5_0: return 2 + 4 + 16;
     case OQ_Q4_0: return 2 + 16;
     case OQ_Q5_K: return 2 + 2 + 12 + 32 + 128;
+    case OQ_Q2_K: return 16 + 64 + 2 + 2;
+    case OQ_Q3_K: return 32 + 64 + 12 + 2;
     default: return -1;
     }
 }
@@ -69,7 +72,7 @@ int oq_block_bytes(int type) {
  * classic blocks [HG 11.1]. */
 int oq_block_elems(int type) {
     switch (type) {
-    case OQ_Q4_K: case OQ_Q6_K: case OQ_Q5_K: return 256;
+    case OQ_Q4_K: case OQ_Q6_K: case OQ_Q5_K: case OQ_Q2_K: case OQ_Q3_K: return 256;
     case OQ_Q8_0: case OQ_Q5_0: case OQ_Q4_0: return 32;
     default: return -1;
     }
@@ -223,6 +226,56 @@ static void unpack_q5_K(const uint8_t* b, int16_t* q, int16_t* sc, uint8_t* mn, 
     }
 }
 
+/* Q2_K super-block (84 bytes = 2.625 bits/weight, [LC]'s "2.5-2.6"):
+ * sixteen 16-weight groups, each with a 4-bit scale and a 4-bit min.
+ * Reading (the GGUF k-quant layout): bytes 0-15 one byte per group (scale in
+ * the low nibble, min in the high nibble), 16-79 qs (2-bit codes), 80-81 d,
+ * 82-83 dmin.  Weight n, with t = n/128, j = (n%128)/32, l = n%32:
+ *   q = (qs[32t + l] >> 2j) & 3   (0..3),   group g = n/16,
+ *   w = (d*sc_g)*q - dmin*m_g. */
+static void unpack_q2_K(const uint8_t* b, int16_t* q, int16_t* sc, uint8_t* mn, float* d, float* dmin) {
+    const uint8_t* qs = b + 16;
+    *d = oq_half_to_float(rd16(b + 80));
+    *dmin = oq_half_to_float(rd16(b + 82));
+    for (int g = 0; g < 16; g++) {
+        sc[g] = (int16_t)(b[g] & 15);
+        mn[g] = (uint8_t)(b[g] >> 4);
+    }
+    for (int n = 0; n < 256; n++) {
+        int t = n / 128, j = (n % 128) / 32, l = n % 32;
+        q[n] = (int16_t)((qs[32 * t + l] >> (2 * j)) & 3);
+    }
+}
+
+/* Q3_K super-block (110 bytes = 3.4375 bits/weight, within [LC]'s
+ * "3.4-4.0"): sixteen 16-weight groups with signed 6-bit scales, 3-bit
+ * codes.  Reading (the GGUF k-quant layout): bytes 0-31 hmask, 32-95 qs
+ * (low 2 bits of each code), 96-107 the sixteen 6-bit scales, 108-109 d.
+ * Weight n, with t = n/128, j = (n%128)/32, l = n%32:
+ *   lo2 = (qs[32t + l] >> 2j) & 3,  hb = (hmask[l] >> (4t + j)) & 1,
+ *   q = lo2 - 4 when hb is clear, lo2 when set   (-4..3).
+ * Scale of group g (0..15), from s = bytes 96..107: the low 4 bits are the
+ * low (g < 8) or high (g >= 8) nibble of s[g % 8], the high 2 bits are bits
+ * 2(g/4), 2(g/4)+1 of s[8 + g % 4]; the 6-bit value minus 32 is the scale
+ * (-32..31).  w = (d*sc_g)*q. */
+static void unpack_q3_K(const uint8_t* b, int16_t* q, int16_t* sc, float* d) {
+    const uint8_t* hm = b;
+    const uint8_t* qs = b + 32;
+    const uint8_t* s = b + 96;
+    *d = oq_half_to_float(rd16(b + 108));
+    for (int g = 0; g < 16; g++) {
+        int lo4 = (s[g % 8] >> (4 * (g / 8))) & 15;
+        int hi2 = (s[8 + g % 4] >> (2 * (g / 4))) & 3;
+        sc[g] = (int16_t)((lo4 | (hi2 << 4)) - 32);
+    }
+    for (int n = 0; n < 256; n++) {
+        int t = n / 128, j = (n % 128) / 32, l = n % 32;
+        int lo2 = (qs[32 * t + l] >> (2 * j)) & 3;
+        int hb = (hm[l] >> (4 * t + j)) & 1;
+        q[n] = (int16_t)(hb ? lo2 : lo2 - 4);
+    }
+}
+
 /* Q6_K super-block (210 bytes): bytes 0-127 ql (low 4 bits of each code),
  * 128-191 qh (high 2 bits), 192-207 sixteen int8 sub-block scales (one per
  * 16 weights), 208-209 d.  Reading of the bit placement: within half
@@ -279,8 +332,9 @@ static void unpack_q4_0(const uint8_t* b, int16_t* q, float* d) {
 }
 
 /* Unpack nblocks blocks.  codes: [nblocks * block_elems]; sc: [nblocks * 16]
- * (Q4_K uses 8 slots, Q6_K 16; unused slots are 0); mins: [nblocks * 8]
- * (Q4_K only); d, dmin: [nblocks].  Any output pointer may be NULL. */
+ * (Q4_K / Q5_K use 8 slots, Q6_K / Q2_K / Q3_K 16; unused slots are 0);
+ * mins: [nblocks * 16] (Q4_K / Q5_K 8 slots, Q2_K 16; 0 elsewhere); d, dmin:
+ * [nblocks].  Any output pointer may be NULL. */
 int oq_unpack(int type, const uint8_t* blocks, int64_t nblocks,
               int16_t* codes, int16_t* sc, uint8_t* mins, float* d, float* dmin) {
     int bb = oq_block_bytes(type), be = oq_block_elems(type);
@@ -288,7 +342,7 @@ int oq_unpack(int type, const uint8_t* blocks, int64_t nblocks,
     for (int64_t i = 0; i < nblocks; i++) {
         const uint8_t* b = blocks + i * bb;
         int16_t q[256], s[16];
-        uint8_t m[8];
+        uint8_t m[16];
         float dd = 0.0f, dm = 0.0f;
         memset(s, 0, sizeof s);
         memset(m, 0, sizeof m);
@@ -299,10 +353,12 @@ int oq_unpack(int type, const uint8_t* blocks, int64_t nblocks,
         case OQ_Q5_0: unpack_q5_0(b, q, &dd); break;
         case OQ_Q4_0: unpack_q4_0(b, q, &dd); break;
         case OQ_Q5_K: unpack_q5_K(b, q, s, m, &dd, &dm); break;
+        case OQ_Q2_K: unpack_q2_K(b, q, s, m, &dd, &dm); break;
+        case OQ_Q3_K: unpack_q3_K(b, q, s, &dd); break;
         }
         if (codes) memcpy(codes + i * be, q, (size_t)be * sizeof(int16_t));
         if (sc) memcpy(sc + i * 16, s, sizeof s);
-        if (mins) memcpy(mins + i * 8, m, sizeof m);
+        if (mins) memcpy(mins + i * 16, m, sizeof m);
         if (d) d[i] = dd;
         if (dmin) dmin[i] = dm;
     }
@@ -316,13 +372,15 @@ int oq_unpack(int type, const uint8_t* blocks, int64_t nblocks,
 /* One block -> block_elems fp32 weights.
  *   Q4_K: ds = d*sc, dm = dmin*m, w = ds*q - dm   [HG 11.2, LC pseudo-code]
  *   Q5_K: the same with 5-bit codes
+ *   Q2_K: the same per 16-weight group with 2-bit codes and 4-bit sc, m
+ *   Q3_K: w = (d*sc) * q, signed sc and q
  *   Q6_K: w = (d*sc) * (q - 32)
  *   Q8_0: w = d * q                                [HG 11.1]
  *   Q5_0: w = d * (q - 16)
  *   Q4_0: w = d * (q - 8)                          [HG 11.1, EN]          */
 static void dequant_block(int type, const uint8_t* b, float* w) {
     int16_t q[256], s[16];
-    uint8_t m[8];
+    uint8_t m[16];
     float d = 0.0f, dmin = 0.0f;
     switch (type) {
     case OQ_Q4_K:
@@ -341,6 +399,22 @@ static void dequant_block(int type, const uint8_t* b, float* w) {
             float dm = dmin * (float)m[n / 32];
             float t = ds * (float)q[n];
             w[n] = t - dm;
+        }
+        break;
+    case OQ_Q2_K:
+        unpack_q2_K(b, q, s, m, &d, &dmin);
+        for (int n = 0; n < 256; n++) {
+            float ds = d * (float)s[n / 16];
+            float dm = dmin * (float)m[n / 16];
+            float t = ds * (float)q[n];
+            w[n] = t - dm;
+        }
+        break;
+    case OQ_Q3_K:
+        unpack_q3_K(b, q, s, &d);
+        for (int n = 0; n < 256; n++) {
+            float ds = d * (float)s[n / 16];
+            w[n] = ds * (float)q[n];
         }
         break;
     case OQ_Q6_K:
@@ -484,8 +558,9 @@ int oq_entries(int type, const uint8_t* W, int64_t rows, int64_t cols,
 /* ------------------------------------------------------------------------ */
 
 /* codes [nblocks * block_elems]: Q4_K 0..15, Q5_K 0..31, Q6_K 0..63, Q8_0
- * -128..127, Q5_0 0..31, Q4_0 0..15.  sc [nblocks*16]: Q4_K / Q5_K 0..63
- * (8 used), Q6_K -128..127.  mins [nblocks*8]: Q4_K / Q5_K 0..63.
+ * -128..127, Q5_0 0..31, Q4_0 0..15, Q2_K 0..3, Q3_K -4..3.  sc [nblocks*16]:
+ * Q4_K / Q5_K 0..63 (8 used), Q6_K -128..127, Q2_K 0..15, Q3_K -32..31.
+ * mins [nblocks*16]: Q4_K / Q5_K 0..63 (8 used), Q2_K 0..15.
  * d_bits / dmin_bits: binary16.
  * Returns -5 when a field is out of range. */
 int oq_pack(int type, int64_t nblocks, const int16_t* codes, const int16_t* sc,
@@ -502,7 +577,7 @@ int oq_pack(int type, int64_t nblocks, const int16_t* codes, const int16_t* sc,
         case OQ_Q5_K: {
             const int five = type == OQ_Q5_K;
             const int16_t* s = sc + i * 16;
-            const uint8_t* m = mins + i * 8;
+            const uint8_t* m = mins + i * 16;
             uint8_t* S = b + 4;
             uint8_t* qh = b + 16;                  /* Q5_K only */
             uint8_t* qs = b + (five ? 48 : 16);
@@ -521,6 +596,40 @@ int oq_pack(int type, int64_t nblocks, const int16_t* codes, const int16_t* sc,
                 qs[32 * c + l] |= (uint8_t)((q[n] & 15) << (4 * h));
                 if (five) qh[l] |= (uint8_t)((q[n] >> 4) << (2 * c + h));
             }
+            break;
+        }
+        case OQ_Q2_K: {
+            const int16_t* s = sc + i * 16;
+            const uint8_t* m = mins + i * 16;
+            for (int g = 0; g < 16; g++) {
+                if (s[g] < 0 || s[g] > 15 || m[g] > 15) return -5;
+                b[g] = (uint8_t)(s[g] | (m[g] << 4));
+            }
+            for (int n = 0; n < 256; n++) {
+                if (q[n] < 0 || q[n] > 3) return -5;
+                int t = n / 128, j = (n % 128) / 32, l = n % 32;
+                b[16 + 32 * t + l] |= (uint8_t)(q[n] << (2 * j));
+            }
+            wr16(b + 80, d_bits[i]);
+            wr16(b + 82, dmin_bits[i]);
+            break;
+        }
+        case OQ_Q3_K: {
+            const int16_t* s = sc + i * 16;
+            for (int g = 0; g < 16; g++) {
+                if (s[g] < -32 || s[g] > 31) return -5;
+                int v = s[g] + 32;
+                b[96 + g % 8] |= (uint8_t)((v & 15) << (4 * (g / 8)));
+                b[104 + g % 4] |= (uint8_t)((v >> 4) << (2 * (g / 4)));
+            }
+            for (int n = 0; n < 256; n++) {
+                if (q[n] < -4 || q[n] > 3) return -5;
+                int t = n / 128, j = (n % 128) / 32, l = n % 32;
+                int hb = q[n] >= 0, lo2 = hb ? q[n] : q[n] + 4;
+                b[32 + 32 * t + l] |= (uint8_t)(lo2 << (2 * j));
+                b[l] |= (uint8_t)(hb << (4 * t + j));
+            }
+            wr16(b + 108, d_bits[i]);
             break;
         }
         case OQ_Q6_K: {
@@ -598,6 +707,10 @@ static int qclamp(float v, int lo, int hi) {
  *        sc = round(sc_f/d), m = round(m_f/dmin) in 0..63;
  *        q = round((w + dmin*m) / (d*sc)) in 0..15.
  *   Q5_K: the same with 31 in place of 15 (codes 0..31).
+ *   Q2_K per 16-weight group: the Q4_K scheme with 3 steps and 4-bit scale
+ *        and min (d = max sc_f / 15, dmin = max m_f / 15, codes 0..3).
+ *   Q3_K per 16 weights: s = max|w|/4; d = max s / 31; sc = round(s/d) in
+ *        -32..31; q = round(w / (d*sc)) in -4..3.
  *   Q6_K per 16 weights: s = max|w|/32; d = max s / 127; sc = round(s/d);
  *        q = round(w / (d*sc)) + 32 in 0..63.
  *   Q8_0: d = max|w|/127, q = round(w/d) in -128..127.
@@ -614,7 +727,7 @@ int oq_quantize(int type, const float* w, int64_t rows, int64_t cols, uint8_t* o
     for (int64_t i = 0; i < nblk; i++) {
         const float* x = w + i * be;
         int16_t q[256], s[16];
-        uint8_t m[8];
+        uint8_t m[16];
         uint16_t db = 0, dmb = 0;
         memset(s, 0, sizeof s);
         memset(m, 0, sizeof m);
@@ -644,6 +757,54 @@ int oq_quantize(int type, const float* w, int64_t rows, int64_t cols, uint8_t* o
                 for (int l = 0; l < 32; l++) {
                     float v = x[32 * j + l];
                     q[32 * j + l] = (int16_t)(ds > 0.0f ? qclamp((v + dm) / ds, 0, top) : 0);
+                }
+            }
+        } else if (type == OQ_Q2_K) {
+            float scf[16], mf[16], maxsc = 0.0f, maxm = 0.0f;
+            for (int g = 0; g < 16; g++) {
+                float lo = 0.0f, hi = x[16 * g];
+                for (int l = 0; l < 16; l++) {
+                    float v = x[16 * g + l];
+                    if (v < lo) lo = v;
+                    if (v > hi) hi = v;
+                }
+                scf[g] = (hi - lo) / 3.0f;
+                mf[g] = -lo;
+                if (scf[g] > maxsc) maxsc = scf[g];
+                if (mf[g] > maxm) maxm = mf[g];
+            }
+            db = oq_float_to_half(maxsc / 15.0f);
+            dmb = oq_float_to_half(maxm / 15.0f);
+            float d = oq_half_to_float(db), dmin = oq_half_to_float(dmb);
+            for (int g = 0; g < 16; g++) {
+                s[g] = (int16_t)(d > 0.0f ? qclamp(scf[g] / d, 0, 15) : 0);
+                m[g] = (uint8_t)(dmin > 0.0f ? qclamp(mf[g] / dmin, 0, 15) : 0);
+                float ds = d * (float)s[g];
+                float dm = dmin * (float)m[g];
+                for (int l = 0; l < 16; l++) {
+                    float v = x[16 * g + l];
+                    q[16 * g + l] = (int16_t)(ds > 0.0f ? qclamp((v + dm) / ds, 0, 3) : 0);
+                }
+            }
+        } else if (type == OQ_Q3_K) {
+            float sf[16], maxs = 0.0f;
+            for (int g = 0; g < 16; g++) {
+                float a = 0.0f;
+                for (int l = 0; l < 16; l++) {
+                    float v = fabsf(x[16 * g + l]);
+                    if (v > a) a = v;
+                }
+                sf[g] = a / 4.0f;
+                if (sf[g] > maxs) maxs = sf[g];
+            }
+            db = oq_float_to_half(maxs / 31.0f);
+            float d = oq_half_to_float(db);
+            for (int g = 0; g < 16; g++) {
+                s[g] = (int16_t)(d > 0.0f ? qclamp(sf[g] / d, -32, 31) : 0);
+                float ds = d * (float)s[g];
+                for (int l = 0; l < 16; l++) {
+                    float v = x[16 * g + l];
+                    q[16 * g + l] = (int16_t)(ds != 0.0f ? qclamp(v / ds, -4, 3) : 0);
                 }
             }
         } else if (type == OQ_Q6_K) {

@@ -12,12 +12,13 @@ Block geometry (bytes, weights) and the byte offsets of the binary16 fields:
   Q4_K 144 B / 256 w, d at 0, dmin at 2     Q6_K 210 B / 256 w, d at 208
   Q8_0  34 B /  32 w, d at 0                Q5_0  22 B /  32 w, d at 0
   Q4_0  18 B /  32 w, d at 0                Q5_K 176 B / 256 w, d at 0, dmin at 2
+  Q2_K  84 B / 256 w, d at 80, dmin at 82   Q3_K 110 B / 256 w, d at 108
 """
 from __future__ import annotations
 
 import numpy as np
 
-TYPE_IDS = {"Q4_K": 1, "Q6_K": 2, "Q8_0": 3, "Q5_0": 4, "Q4_0": 5, "Q5_K": 6}
+TYPE_IDS = {"Q4_K": 1, "Q6_K": 2, "Q8_0": 3, "Q5_0": 4, "Q4_0": 5, "Q5_K": 6, "Q2_K": 7, "Q3_K": 8}
 GEOMETRY = {  # name: (block bytes, weights per block, d offset, dmin offset or None)
     "Q4_K": (144, 256, 0, 2),
     "Q6_K": (210, 256, 208, None),
@@ -25,6 +26,8 @@ GEOMETRY = {  # name: (block bytes, weights per block, d offset, dmin offset or 
     "Q5_0": (22, 32, 0, None),
     "Q4_0": (18, 32, 0, None),
     "Q5_K": (176, 256, 0, 2),
+    "Q2_K": (84, 256, 80, 82),
+    "Q3_K": (110, 256, 108, None),
 }
 
 

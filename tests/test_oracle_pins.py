@@ -14,7 +14,7 @@ from golden_io import all_fixtures, load
 
 pytestmark = pytest.mark.filterwarnings("ignore")
 
-T = {"Q4_K": 1, "Q6_K": 2, "Q8_0": 3, "Q5_0": 4, "Q4_0": 5, "Q5_K": 6}
+T = {"Q4_K": 1, "Q6_K": 2, "Q8_0": 3, "Q5_0": 4, "Q4_0": 5, "Q5_K": 6, "Q2_K": 7, "Q3_K": 8}
 
 
 # ---------------------------------------------------------------- sizes --
@@ -37,6 +37,13 @@ def test_block_sizes_and_bits_per_weight(oracle_mod):
     # 256-weight super-blocks; the reading's 176 bytes is the low end.
     assert o.block_bytes(T["Q5_K"]) == 176 and o.block_elems(T["Q5_K"]) == 256
     assert o.block_bytes(T["Q5_K"]) * 8 / 256 == 5.5
+    # The same table: Q2_K at 2.5-2.6 and Q3_K at 3.4-4.0 bits/weight, both on
+    # 256-weight super-blocks; the readings' 84 and 110 bytes.
+    bpw2 = o.block_bytes(T["Q2_K"]) * 8 / o.block_elems(T["Q2_K"])
+    bpw3 = o.block_bytes(T["Q3_K"]) * 8 / o.block_elems(T["Q3_K"])
+    assert o.block_elems(T["Q2_K"]) == o.block_elems(T["Q3_K"]) == 256
+    assert bpw2 == 2.625 and 2.5 <= round(bpw2, 1) <= 2.6
+    assert bpw3 == 3.4375 and 3.4 <= bpw3 <= 4.0
     # Row bytes: cols / elems * block bytes (the workload's 9,030-byte rows).
     assert o.row_bytes(T["Q6_K"], 11008) == 9030
     assert o.row_bytes(T["Q4_K"], 1024) * 256 == 147456
@@ -128,7 +135,7 @@ def test_q5_0_low_nibbles_follow_q4_0_convention(oracle_mod):
 
 # ------------------------------------------------------ round trips --
 
-@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K"])
+@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K", "Q2_K", "Q3_K"])
 def test_bytes_unpack_pack_bijection(oracle_mod, name):
     # Every byte of these blocks is used, so unpack followed by pack must give
     # back the same bytes (and unpack of that, the same fields).
@@ -139,11 +146,13 @@ def test_bytes_unpack_pack_bijection(oracle_mod, name):
     dbits = np.array([oracle_mod.float_to_half(float(v)) for v in d], np.uint16)
     dminbits = np.array([oracle_mod.float_to_half(float(v)) for v in dmin], np.uint16)
     # fp16 NaN payloads do not survive a float round trip; restore raw bits.
-    off = {"Q4_K": 0, "Q6_K": 208, "Q8_0": 0, "Q5_0": 0, "Q4_0": 0, "Q5_K": 0}[name]
+    off = {"Q4_K": 0, "Q6_K": 208, "Q8_0": 0, "Q5_0": 0, "Q4_0": 0, "Q5_K": 0, "Q2_K": 80, "Q3_K": 108}[name]
     raw_d = W.reshape(nb, bb)[:, off:off + 2].copy().view(np.uint16).reshape(nb)
     dbits = raw_d
     if name in ("Q4_K", "Q5_K"):
         dminbits = W.reshape(nb, bb)[:, 2:4].copy().view(np.uint16).reshape(nb)
+    if name == "Q2_K":
+        dminbits = W.reshape(nb, bb)[:, 82:84].copy().view(np.uint16).reshape(nb)
     again = oracle_mod.pack(t, codes, sc, mins, dbits, dminbits)
     assert np.array_equal(again, W)
 
@@ -153,9 +162,9 @@ def test_q4k_every_6bit_value_in_every_slot(oracle_mod):
     g = synth.rng(12)
     nb = 64 * 8
     sc = np.zeros((nb, 16), np.int16)
-    mn = np.zeros((nb, 8), np.uint8)
+    mn = np.zeros((nb, 16), np.uint8)   # 8 used
     sc[:, :8] = g.integers(0, 64, (nb, 8))
-    mn[:, :] = g.integers(0, 64, (nb, 8))
+    mn[:, :8] = g.integers(0, 64, (nb, 8))
     for i in range(nb):
         v, slot = i % 64, i // 64
         sc[i, slot] = v
@@ -235,6 +244,79 @@ def test_q5k_high_bit_planes_select_their_weights(oracle_mod):
     assert np.all(hit == 1)
 
 
+def _one_bit_blocks(nbytes_total, plane_off, plane_len, bits):
+    """Blocks with a single set bit each: one per (byte of the plane, bit)."""
+    blocks = np.zeros((plane_len * len(bits), nbytes_total), np.uint8)
+    for k in range(plane_len):
+        for i, b in enumerate(bits):
+            blocks[k * len(bits) + i, plane_off + k] = 1 << b
+    return blocks
+
+
+def test_q2k_code_pairs_are_a_bijection_onto_the_weights(oracle_mod):
+    # Q2_K (a reading; the pages give only its size): every 2-bit field of the
+    # 64 code bytes must be the code of exactly one weight, all 256 covered.
+    # A field set to 1 in an otherwise zero block raises exactly one code to 1.
+    B = np.zeros((256, 84), np.uint8)
+    for k in range(64):
+        for j in range(4):
+            B[4 * k + j, 16 + k] = 1 << (2 * j)
+    codes, _, _, _, _ = oracle_mod.unpack(7, B.reshape(-1), 256)
+    hit = np.zeros(256, int)
+    for e in range(256):
+        (n,) = np.nonzero(codes[e])
+        assert n.size == 1 and codes[e, n[0]] == 1
+        hit[n[0]] += 1
+        k, j = e // 4, e % 4
+        # byte 32t + l, field j: weight 128t + 32j + l
+        assert n[0] == 128 * (k // 32) + 32 * j + k % 32
+    assert np.all(hit == 1)
+
+
+def test_q3k_mask_and_code_planes(oracle_mod):
+    # Q3_K (a reading): with every mask bit clear a code is its 2-bit field
+    # minus 4 (all codes -4 on a zero block); each of the 256 mask bits lifts
+    # exactly one weight by 4, and each 2-bit field set to 1 raises exactly
+    # one code by 1 -- both bijections onto the weights, matching each other.
+    zero = np.zeros(110, np.uint8)
+    c0, _, _, _, _ = oracle_mod.unpack(8, zero, 1)
+    assert np.all(c0 == -4)
+    M = _one_bit_blocks(110, 0, 32, range(8))
+    cm, _, _, _, _ = oracle_mod.unpack(8, M.reshape(-1), 256)
+    Q = np.zeros((256, 110), np.uint8)
+    for k in range(64):
+        for j in range(4):
+            Q[4 * k + j, 32 + k] = 1 << (2 * j)
+    cq, _, _, _, _ = oracle_mod.unpack(8, Q.reshape(-1), 256)
+    hm = np.zeros(256, int)
+    hq = np.zeros(256, int)
+    for e in range(256):
+        (nm,) = np.nonzero(cm[e] + 4)
+        (nq,) = np.nonzero(cq[e] + 4)
+        assert nm.size == 1 and cm[e, nm[0]] == 0
+        assert nq.size == 1 and cq[e, nq[0]] == -3
+        hm[nm[0]] += 1
+        hq[nq[0]] += 1
+        # mask byte l, bit 4t + j and code byte 32t + l, field j: weight 128t + 32j + l
+        l, bit = e // 8, e % 8
+        assert nm[0] == 128 * (bit // 4) + 32 * (bit % 4) + l
+    assert np.all(hm == 1) and np.all(hq == 1)
+
+
+@pytest.mark.parametrize("name", ["Q2_K", "Q3_K"])
+def test_group_scales_follow_weight_order(oracle_mod, name):
+    # Sixteen distinct scales and all codes equal: the weights step through
+    # the scales in group order, 16 weights each (pairs each scale field with
+    # its 16 weights: a wrong group index or a wrong scale unpacking moves a
+    # weight to another scale).
+    t = T[name]
+    sc = np.arange(16, dtype=np.int16)[None, :] + (0 if name == "Q2_K" else -8)
+    codes = np.full((1, 256), 1, np.int16)
+    W = oracle_mod.pack(t, codes, sc, None, np.array([0x3C00], np.uint16), np.array([0], np.uint16))
+    w = oracle_mod.dequant(t, W, 1, 256)[0]
+    assert np.array_equal(w, np.repeat(sc[0].astype(np.float32), 16))
+
+
 # --------------------------------------------- dequant formula checks --
 
 def test_q4k_formula_exact_in_fp32(oracle_mod):
@@ -265,8 +347,23 @@ def test_q5k_formula_exact_in_fp32(oracle_mod):
     assert codes.min() == 0 and codes.max() == 31
 
 
+@pytest.mark.parametrize("name", ["Q2_K", "Q3_K"])
+def test_q2k_q3k_formula_exact_in_fp32(oracle_mod, name):
+    # d*sc (11 + 6 bits) times a code of at most 3 bits and dmin*m stay
+    # within 24 bits: only Q2_K's final subtraction rounds.
+    t = T[name]
+    W = synth.random_blocks(name, 8, 2048, 23)
+    codes, sc, mins, d, dmin = oracle_mod.unpack(t, W, 64)
+    grp = np.repeat(np.arange(16), 16)
+    ds = d[:, None].astype(np.float64) * sc.astype(np.float64)
+    dm = dmin[:, None].astype(np.float64) * mins.astype(np.float64)
+    exact = ds[:, grp] * codes.astype(np.float64) - dm[:, grp]
+    got = oracle_mod.dequant(t, W, 8, 2048).reshape(64, 256)
+    assert np.array_equal(got, exact.astype(np.float32))
+
+
 def test_zero_scale_block_is_zero(oracle_mod):
-    for name in ("Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q5_K"):
+    for name in ("Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q5_K", "Q2_K", "Q3_K"):
         W = synth.random_blocks(name, 2, 512, 22)
         bb, be, doff, dmoff = synth.GEOMETRY[name]
         B = W.reshape(-1, bb)
@@ -279,7 +376,7 @@ def test_zero_scale_block_is_zero(oracle_mod):
 
 # ------------------------------------------------------ dot products --
 
-@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K"])
+@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K", "Q2_K", "Q3_K"])
 @pytest.mark.parametrize("rows,cols,M", [(1, 256, 1), (3, 512, 2), (4, 1024, 3)])
 def test_gemv_matches_numpy_float64_matmul(oracle_mod, name, rows, cols, M):
     t = T[name]
@@ -388,7 +485,7 @@ def test_quantizer_exact_codes_k_quants(oracle_mod):
     W = oracle_mod.quantize(1, w.reshape(1, -1))
     codes, sc, mins, d, dmin = _codes(oracle_mod, 1, W, 1)
     assert np.array_equal(codes[0], k)
-    assert np.all(sc[0, :8] == 63) and np.all(mins[0] == 63)
+    assert np.all(sc[0, :8] == 63) and np.all(mins[0, :8] == 63)
     # Q6_K: each 16-group has max |w| = A, values A*k/32 for k in -32..31:
     # sc = 127 and the code is k + 32.
     A = 0.23
@@ -407,12 +504,29 @@ def test_quantizer_exact_codes_k_quants(oracle_mod):
     W5 = oracle_mod.quantize(6, w5.reshape(1, -1))
     c5, s5, m5, _, _ = _codes(oracle_mod, 6, W5, 1)
     assert np.array_equal(c5[0], k5)
-    assert np.all(s5[0, :8] == 63) and np.all(m5[0] == 63)
+    assert np.all(s5[0, :8] == 63) and np.all(m5[0, :8] == 63)
+    # Q2_K: each 16-group spans [lo, hi] in 3 steps: sc = m = 15, code = step.
+    k2 = rng.integers(0, 4, size=256)
+    k2[::16] = 0
+    k2[1::16] = 3
+    w2 = (lo + k2 * (hi - lo) / 3.0).astype(np.float32)
+    c2, s2, m2, _, _ = _codes(oracle_mod, 7, oracle_mod.quantize(7, w2.reshape(1, -1)), 1)
+    assert np.array_equal(c2[0], k2)
+    assert np.all(s2[0] == 15) and np.all(m2[0] == 15)
+    # Q3_K: each 16-group has max |w| = A at code -4, values A*k/4 for k in
+    # -4..3: sc = 31 and the code is k.
+    k3 = rng.integers(-4, 4, size=256)
+    k3[::16] = -4
+    w3 = (A * k3 / 4.0).astype(np.float32)
+    c3, s3, _, _, _ = _codes(oracle_mod, 8, oracle_mod.quantize(8, w3.reshape(1, -1)), 1)
+    assert np.array_equal(c3[0], k3)
+    assert np.all(s3[0] == 31)
 
 
 def test_quantizer_zero_blocks(oracle_mod):
     # An all-zero block takes the zero-divisor path: d = 0 and the offset code.
-    for t, n, code in ((1, 256, 0), (2, 256, 32), (3, 32, 0), (4, 32, 16), (5, 32, 8), (6, 256, 0)):
+    for t, n, code in ((1, 256, 0), (2, 256, 32), (3, 32, 0), (4, 32, 16), (5, 32, 8), (6, 256, 0), (7, 256, 0),
+                       (8, 256, 0)):
         W = oracle_mod.quantize(t, np.zeros((1, n), np.float32))
         codes, sc, mins, d, dmin = _codes(oracle_mod, t, W, 1)
         assert np.all(codes[0, :n] == code) and d[0] == 0.0
