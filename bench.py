@@ -528,7 +528,7 @@ def run_quantize(dev, hbm_peak=None, reps: int = 20):
     g.manual_seed(2024)
     w = torch.randn((rows, cols), device=dev, generator=g) * 0.02
     per = {}
-    for name in ("Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K"):
+    for name in ("Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K", "Q2_K", "Q3_K"):
         t = synth.TYPE_IDS[name]
         o = torch.empty(rows * qk.row_bytes(t, cols), dtype=torch.uint8, device=dev)
         for _ in range(2):

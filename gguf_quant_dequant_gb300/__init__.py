@@ -5,7 +5,7 @@ device pointers, sizes and the current CUDA stream of PyTorch tensors, and
 raises QKError on a non-zero status.  There is no CPU fallback: if libqk.so
 has not been built, load() raises.
 
-Type ids: Q4_K = 1, Q6_K = 2, Q8_0 = 3, Q5_0 = 4, Q4_0 = 5, Q5_K = 6.
+Type ids: Q4_K = 1, Q6_K = 2, Q8_0 = 3, Q5_0 = 4, Q4_0 = 5, Q5_K = 6, Q2_K = 7, Q3_K = 8.
 """
 from __future__ import annotations
 
@@ -13,8 +13,9 @@ import ctypes
 import os
 import threading
 
-Q4_K, Q6_K, Q8_0, Q5_0, Q4_0, Q5_K = 1, 2, 3, 4, 5, 6
-TYPES = {"Q4_K": Q4_K, "Q6_K": Q6_K, "Q8_0": Q8_0, "Q5_0": Q5_0, "Q4_0": Q4_0, "Q5_K": Q5_K}
+Q4_K, Q6_K, Q8_0, Q5_0, Q4_0, Q5_K, Q2_K, Q3_K = 1, 2, 3, 4, 5, 6, 7, 8
+TYPES = {"Q4_K": Q4_K, "Q6_K": Q6_K, "Q8_0": Q8_0, "Q5_0": Q5_0, "Q4_0": Q4_0, "Q5_K": Q5_K, "Q2_K": Q2_K,
+         "Q3_K": Q3_K}
 OUT_F32, OUT_BF16 = 0, 1
 STATUS = {0: "QK_OK", 1: "QK_ERR_TYPE", 2: "QK_ERR_SHAPE", 3: "QK_ERR_ALIGN", 4: "QK_ERR_NULL",
           5: "QK_ERR_WORKSPACE", 6: "QK_ERR_CUDA", 7: "QK_ERR_TIMEOUT", 8: "QK_ERR_ARG",
@@ -234,12 +235,12 @@ def gemm(t: int, W, rows: int, cols: int, X, Y=None, ws=None, stream=None):
 
 def unpack(t: int, W, nblocks: int, stream=None):
     """-> (codes int16 [nblocks, elems], sc int16 [nblocks, 16], mins uint8
-    [nblocks, 8], d f32 [nblocks], dmin f32 [nblocks]) as CUDA tensors."""
+    [nblocks, 16], d f32 [nblocks], dmin f32 [nblocks]) as CUDA tensors."""
     import torch
     dev = W.device
     codes = torch.empty((nblocks, block_elems(t)), dtype=torch.int16, device=dev)
     sc = torch.empty((nblocks, 16), dtype=torch.int16, device=dev)
-    mins = torch.empty((nblocks, 8), dtype=torch.uint8, device=dev)
+    mins = torch.empty((nblocks, 16), dtype=torch.uint8, device=dev)
     d = torch.empty(nblocks, dtype=torch.float32, device=dev)
     dmin = torch.empty(nblocks, dtype=torch.float32, device=dev)
     _check(load().qk_unpack(t, _ptr(W), nblocks, _ptr(codes), _ptr(sc), _ptr(mins), _ptr(d), _ptr(dmin),

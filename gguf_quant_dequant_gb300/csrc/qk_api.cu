@@ -38,7 +38,7 @@ qk_status cuda_fail(cudaError_t e, const char* where) {
     return fail(QK_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
 }
 
-bool known_type(int t) { return t >= QK_Q4_K && t <= QK_Q5_K; }
+bool known_type(int t) { return t >= QK_Q4_K && t <= QK_Q3_K; }
 
 size_t block_bytes(int t) {
     switch (t) {
@@ -48,13 +48,15 @@ size_t block_bytes(int t) {
     case QK_Q5_0: return 22;
     case QK_Q4_0: return 18;
     case QK_Q5_K: return 176;
+    case QK_Q2_K: return 84;
+    case QK_Q3_K: return 110;
     }
     return 0;
 }
 
 int block_elems(int t) {
     switch (t) {
-    case QK_Q4_K: case QK_Q6_K: case QK_Q5_K: return 256;
+    case QK_Q4_K: case QK_Q6_K: case QK_Q5_K: case QK_Q2_K: case QK_Q3_K: return 256;
     case QK_Q8_0: case QK_Q5_0: case QK_Q4_0: return 32;
     }
     return 0;

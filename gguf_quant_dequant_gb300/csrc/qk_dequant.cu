@@ -62,20 +62,34 @@ __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t* __restrict__
                 if (j < 8) { Fmt<T_Q4_K>::scale_min(blk, j, s, m); v = (int)s; }
             } else if constexpr (T == T_Q6_K) {
                 v = (int)(int8_t)blk[192 + j];
+            } else if constexpr (T == T_Q2_K) {
+                v = (int)(blk[j] & 15u);
+            } else if constexpr (T == T_Q3_K) {
+                v = Fmt<T_Q3_K>::scale(blk, j);
             }
             sc[b * 16 + j] = (int16_t)v;
         }
     if (mins)
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 16; ++j) {
             uint32_t s = 0, m = 0;
-            if constexpr (T == T_Q4_K || T == T_Q5_K) Fmt<T_Q4_K>::scale_min(blk, j, s, m);
-            mins[b * 8 + j] = (uint8_t)m;
+            if constexpr (T == T_Q4_K || T == T_Q5_K) {
+                if (j < 8) Fmt<T_Q4_K>::scale_min(blk, j, s, m);
+            } else if constexpr (T == T_Q2_K) {
+                m = blk[j] >> 4;
+            }
+            mins[b * 16 + j] = (uint8_t)m;
         }
     if (d) {
         if constexpr (T == T_Q6_K) d[b] = h2f(ld_u16(blk + 208));
+        else if constexpr (T == T_Q2_K) d[b] = h2f(ld_u16(blk + 80));
+        else if constexpr (T == T_Q3_K) d[b] = h2f(ld_u16(blk + 108));
         else d[b] = h2f(ld_u16(blk));
     }
-    if (dmin) dmin[b] = (T == T_Q4_K || T == T_Q5_K) ? h2f(ld_u16(blk + 2)) : 0.0f;
+    if (dmin) {
+        if constexpr (T == T_Q4_K || T == T_Q5_K) dmin[b] = h2f(ld_u16(blk + 2));
+        else if constexpr (T == T_Q2_K) dmin[b] = h2f(ld_u16(blk + 82));
+        else dmin[b] = 0.0f;
+    }
 }
 
 template <int T>
@@ -100,6 +114,8 @@ cudaError_t launch_dequant(int type, const uint8_t* W, int64_t rows, int64_t col
     case T_Q5_0: return dequant_t<T_Q5_0>(W, rows, cols, out, out_bf16, s);
     case T_Q4_0: return dequant_t<T_Q4_0>(W, rows, cols, out, out_bf16, s);
     case T_Q5_K: return dequant_t<T_Q5_K>(W, rows, cols, out, out_bf16, s);
+    case T_Q2_K: return dequant_t<T_Q2_K>(W, rows, cols, out, out_bf16, s);
+    case T_Q3_K: return dequant_t<T_Q3_K>(W, rows, cols, out, out_bf16, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -115,6 +131,8 @@ cudaError_t launch_unpack(int type, const uint8_t* W, int64_t nblocks, int16_t* 
     case T_Q5_0: unpack_kernel<T_Q5_0><<<grid, 256, 0, s>>>(W, nblocks, codes, sc, mins, d, dmin); break;
     case T_Q4_0: unpack_kernel<T_Q4_0><<<grid, 256, 0, s>>>(W, nblocks, codes, sc, mins, d, dmin); break;
     case T_Q5_K: unpack_kernel<T_Q5_K><<<grid, 256, 0, s>>>(W, nblocks, codes, sc, mins, d, dmin); break;
+    case T_Q2_K: unpack_kernel<T_Q2_K><<<grid, 256, 0, s>>>(W, nblocks, codes, sc, mins, d, dmin); break;
+    case T_Q3_K: unpack_kernel<T_Q3_K><<<grid, 256, 0, s>>>(W, nblocks, codes, sc, mins, d, dmin); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

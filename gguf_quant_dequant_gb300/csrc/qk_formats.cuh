@@ -14,6 +14,10 @@
 //   Q4_0  w = d*(q - 8)                ("Hitchhiker's Guide", 11.1 figure)
 //   Q5_K  w = (d*sc)*q - dmin*m, 5-bit q (the GGUF k-quant layout: only the
 //         size, 5.5 bits/weight, is on the pages)
+//   Q2_K  w = (d*sc)*q - dmin*m per 16 weights, 2-bit q (GGUF layout; the
+//         pages give 2.5-2.6 bits/weight)
+//   Q3_K  w = (d*sc)*q per 16 weights, q in -4..3, signed 6-bit sc (GGUF
+//         layout; the pages give 3.4-4.0 bits/weight)
 // Each product before the last rounding is exact in fp32 (an fp16 d has 11
 // significant bits, a scale at most 8, a code at most 8), so the weights are
 // bit-identical to the formula evaluated in fp32 whatever the contraction.
@@ -24,7 +28,7 @@
 
 namespace qk {
 
-enum : int { T_Q4_K = 1, T_Q6_K = 2, T_Q8_0 = 3, T_Q5_0 = 4, T_Q4_0 = 5, T_Q5_K = 6 };
+enum : int { T_Q4_K = 1, T_Q6_K = 2, T_Q8_0 = 3, T_Q5_0 = 4, T_Q4_0 = 5, T_Q5_K = 6, T_Q2_K = 7, T_Q3_K = 8 };
 
 // 16-bit and 32-bit little-endian loads from a 2-byte-aligned address that
 // never touch a byte outside [p, p + size).
@@ -115,6 +119,64 @@ template <> struct Fmt<T_Q5_K> {
         Fmt<T_Q4_K>::scale_min(blk, 2 * (u >> 1) + h, sc, m);
         A = h2f(ld_u16(blk)) * (float)sc;
         B = h2f(ld_u16(blk + 2)) * (float)m;
+    }
+};
+
+// ---------------------------------------------------------- Q2_K, Q3_K --
+// Sixteen 16-weight groups; half i of the super-block (unit i/2, h = i%2) is
+// group i, weights 16i..16i+15: t = i/8, j = (i%8)/2, k = i%2, and code l is
+// bits 2j..2j+1 of byte 32t + 16k + l of the 2-bit plane.
+// Q2_K: bytes 0-15 scale (low nibble) / min (high nibble) per group, 16-79
+//       the plane, 80-81 d, 82-83 dmin.  w = (d*sc)*q - dmin*m.
+// Q3_K: bytes 0-31 hmask, 32-95 the plane, 96-107 the scales, 108-109 d.  The
+//       code's third bit is bit 4t + j of hmask[16k + l]; q = lo2 - 4 when it
+//       is clear.  Scale of group g: low 4 bits = nibble g/8 of byte 96 + g%8,
+//       high 2 bits = bits 2(g/4).. of byte 104 + g%4; value minus 32.
+//       w = (d*sc)*q.
+__device__ __forceinline__ int plane_base(int i) { return 32 * (i >> 3) + 16 * (i & 1); }
+__device__ __forceinline__ int plane_shift(int i) { return 2 * ((i & 7) >> 1); }
+
+template <> struct Fmt<T_Q2_K> {
+    static constexpr int BB = 84, BE = 256, UPB = 8, OFF = 0;
+    __device__ static __forceinline__ int koff(int u, int h) { return 32 * u + 16 * h; }
+    __device__ static __forceinline__ void codes16(const uint8_t* blk, int u, int h, int (&c)[16]) {
+        const int i = 2 * u + h;
+        const uint8_t* p = blk + 16 + plane_base(i);
+        const uint32_t q[4] = {ld_u32_a2(p), ld_u32_a2(p + 4), ld_u32_a2(p + 8), ld_u32_a2(p + 12)};
+#pragma unroll
+        for (int l = 0; l < 16; ++l) c[l] = (int)((byte_of(q, l) >> plane_shift(i)) & 3u);
+    }
+    __device__ static __forceinline__ void params(const uint8_t* blk, int u, int h, float& A, float& B) {
+        const uint32_t sm = blk[2 * u + h];
+        A = h2f(ld_u16(blk + 80)) * (float)(sm & 15u);
+        B = h2f(ld_u16(blk + 82)) * (float)(sm >> 4);
+    }
+};
+
+template <> struct Fmt<T_Q3_K> {
+    static constexpr int BB = 110, BE = 256, UPB = 8, OFF = 0;
+    __device__ static __forceinline__ int koff(int u, int h) { return 32 * u + 16 * h; }
+    __device__ static __forceinline__ int scale(const uint8_t* blk, int g) {
+        const uint32_t lo4 = (blk[96 + (g & 7)] >> (4 * (g >> 3))) & 15u;
+        const uint32_t hi2 = (blk[104 + (g & 3)] >> (2 * (g >> 2))) & 3u;
+        return (int)(lo4 | (hi2 << 4)) - 32;
+    }
+    __device__ static __forceinline__ void codes16(const uint8_t* blk, int u, int h, int (&c)[16]) {
+        const int i = 2 * u + h;
+        const uint8_t* p = blk + 32 + plane_base(i);
+        const uint8_t* m = blk + 16 * (i & 1);
+        const uint32_t q[4] = {ld_u32_a2(p), ld_u32_a2(p + 4), ld_u32_a2(p + 8), ld_u32_a2(p + 12)};
+        const uint32_t hm[4] = {ld_u32_a2(m), ld_u32_a2(m + 4), ld_u32_a2(m + 8), ld_u32_a2(m + 12)};
+        const int hb = 4 * (i >> 3) + ((i & 7) >> 1);
+#pragma unroll
+        for (int l = 0; l < 16; ++l) {
+            const int lo2 = (int)((byte_of(q, l) >> plane_shift(i)) & 3u);
+            c[l] = ((byte_of(hm, l) >> hb) & 1u) ? lo2 : lo2 - 4;
+        }
+    }
+    __device__ static __forceinline__ void params(const uint8_t* blk, int u, int h, float& A, float& B) {
+        A = h2f(ld_u16(blk + 108)) * (float)scale(blk, 2 * u + h);
+        B = 0.0f;
     }
 };
 

@@ -107,7 +107,9 @@ template <int T> struct SkGeo {
     // The word reads of the 32-weight types run up to 4 bytes past a row's
     // box (into the next row, or past the ring into the barriers): read, never
     // used.
-    static constexpr int BOXW = T == T_Q6_K ? 240 : BYTES;
+    // Q2_K (84 bytes, starts 4-byte aligned) needs 12 + 84 -> 112; Q3_K
+    // (110 bytes, 2-byte aligned) 14 + 110 -> 144.
+    static constexpr int BOXW = T == T_Q6_K ? 240 : (T == T_Q2_K ? 112 : (T == T_Q3_K ? 144 : BYTES));
     static_assert(BOXW % 16 == 0 && (BOXW / 16) % 2 == 1, "packed TMA box");
     static constexpr int STAGE = kBM * BOXW;
     static constexpr int NSP = 3;
@@ -152,6 +154,9 @@ __device__ __forceinline__ void locate(int o, int& u, int& h) {
     if constexpr (T == T_Q4_K || T == T_Q5_K) {   // koff = 64(u>>1) + 32h + 16(u&1)
         u = 2 * (o >> 6) + ((o >> 4) & 1);
         h = (o >> 5) & 1;
+    } else if constexpr (T == T_Q2_K || T == T_Q3_K) {   // koff = 32u + 16h
+        u = o >> 5;
+        h = (o >> 4) & 1;
     } else if constexpr (T == T_Q6_K) {   // koff = 128(u>>2) + 32((u>>1&1) + 2h) + 16(u&1)
         const int t = o >> 7, g = (o >> 5) & 3;
         u = 4 * t + 2 * (g & 1) + ((o >> 4) & 1);
@@ -328,6 +333,19 @@ __device__ __forceinline__ void q5k64(const uint8_t* blk, int kk, uint32_t (&pk)
                 pk[2 * i], pk[2 * i + 1]);
         four_hi(((w[i] >> 4) & 0x0F0F0F0Fu) | ((b << 3) & 0x10101010u), make_float2(ds1, ds1),
                 make_float2(o1, o1), pk[16 + 2 * i], pk[17 + 2 * i]);
+    }
+}
+
+// Any type with 16-weight halves in k order (Q2_K, Q3_K): k-block kk of a
+// 256-weight macro-block is halves 4kk .. 4kk+3 through the shared decoders.
+template <int T>
+__device__ __forceinline__ void halves64(const uint8_t* blk, int kk, uint32_t (&pk)[32]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float w[16];
+        dequant_half<T>(blk, 2 * kk + (i >> 1), i & 1, w);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) pk[8 * i + k] = pack_bf16(w[2 * k], w[2 * k + 1]);
     }
 }
 
@@ -866,6 +884,8 @@ __global__ void __launch_bounds__(kSkThreads, 1) gemm_skinny_kernel(const __grid
                             q4k64(blk, ph, pk);
                         } else if constexpr (T == T_Q5_K) {
                             q5k64(blk, ph, pk);
+                        } else if constexpr (T == T_Q2_K || T == T_Q3_K) {
+                            halves64<T>(blk, ph, pk);
                         } else if constexpr (T == T_Q6_K) {
                             q6k64(blk, ph, pk);
                         } else {
@@ -1056,6 +1076,8 @@ GemmPlan plan_gemm(int type, int64_t rows, int64_t cols, int64_t M, int sms) {
     case T_Q5_0: rb = cols / 32 * 22; break;
     case T_Q4_0: rb = cols / 32 * 18; break;
     case T_Q5_K: rb = cols / 256 * 176; break;
+    case T_Q2_K: rb = cols / 256 * 84; break;
+    case T_Q3_K: rb = cols / 256 * 110; break;
     }
     pl.skinny = M <= gm::kSkinnyBN && rb % 16 == 0;
     const int64_t kpm = pl.skinny ? 4 : k_blocks_per_macro(type);   // the small-batch kernel's macro-blocks are 256 wide
@@ -1113,6 +1135,8 @@ cudaError_t launch_gemm(int type, const GemmPlan& pl, const uint8_t* W, int64_t 
     case T_Q5_0: a.row_bytes = cols / 32 * 22; break;
     case T_Q4_0: a.row_bytes = cols / 32 * 18; break;
     case T_Q5_K: a.row_bytes = cols / 256 * 176; break;
+    case T_Q2_K: a.row_bytes = cols / 256 * 84; break;
+    case T_Q3_K: a.row_bytes = cols / 256 * 110; break;
     default: return cudaErrorInvalidValue;
     }
     a.total16 = (rows * a.row_bytes) & ~(int64_t)15;
@@ -1124,6 +1148,8 @@ cudaError_t launch_gemm(int type, const GemmPlan& pl, const uint8_t* W, int64_t 
     case T_Q5_0: e = gemm_t<T_Q5_0>(a, pl, map, s); break;
     case T_Q4_0: e = gemm_t<T_Q4_0>(a, pl, map, s); break;
     case T_Q5_K: e = gemm_t<T_Q5_K>(a, pl, map, s); break;
+    case T_Q2_K: e = gemm_t<T_Q2_K>(a, pl, map, s); break;
+    case T_Q3_K: e = gemm_t<T_Q3_K>(a, pl, map, s); break;
     }
     if (e != cudaSuccess || pl.splits <= 1) return e;
     // Add the partials in split order.

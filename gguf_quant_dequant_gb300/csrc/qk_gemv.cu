@@ -335,7 +335,7 @@ int mt_for(int64_t M) { return M >= 4 ? 4 : (M >= 2 ? 2 : 1); }
 
 int64_t nst_for(int type, int64_t cols) {
     switch (type) {
-    case T_Q4_K: case T_Q6_K: case T_Q5_K: return (cols / 256 + 7) / 8;
+    case T_Q4_K: case T_Q6_K: case T_Q5_K: case T_Q2_K: case T_Q3_K: return (cols / 256 + 7) / 8;
     case T_Q8_0: case T_Q5_0: case T_Q4_0: return (cols / 32 + 63) / 64;
     }
     return 0;
@@ -413,6 +413,8 @@ cudaError_t launch_gemv(int type, const GemvPlan& pl, const uint8_t* W, int64_t 
     case T_Q5_0: a.row_bytes = cols / 32 * 22; break;
     case T_Q4_0: a.row_bytes = cols / 32 * 18; break;
     case T_Q5_K: a.row_bytes = cols / 256 * 176; break;
+    case T_Q2_K: a.row_bytes = cols / 256 * 84; break;
+    case T_Q3_K: a.row_bytes = cols / 256 * 110; break;
     default: return cudaErrorInvalidValue;
     }
     a.total16 = (rows * a.row_bytes) & ~(int64_t)15;
@@ -455,6 +457,8 @@ cudaError_t launch_gemv(int type, const GemvPlan& pl, const uint8_t* W, int64_t 
     case T_Q5_0: return launch_mt<T_Q5_0>(pl, a, s);
     case T_Q4_0: return launch_mt<T_Q4_0>(pl, a, s);
     case T_Q5_K: return launch_mt<T_Q5_K>(pl, a, s);
+    case T_Q2_K: return launch_mt<T_Q2_K>(pl, a, s);
+    case T_Q3_K: return launch_mt<T_Q3_K>(pl, a, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -364,12 +364,14 @@ int slot_of(int type) {
     case T_Q5_0: return slot_bytes<T_Q5_0>();
     case T_Q4_0: return slot_bytes<T_Q4_0>();
     case T_Q5_K: return slot_bytes<T_Q5_K>();
+    case T_Q2_K: return slot_bytes<T_Q2_K>();
+    case T_Q3_K: return slot_bytes<T_Q3_K>();
     }
     return 0;
 }
 
 int64_t nsl_of(int type, int64_t cols) {
-    const int be = (type == T_Q4_K || type == T_Q6_K || type == T_Q5_K) ? 256 : 32;
+    const int be = (type == T_Q8_0 || type == T_Q5_0 || type == T_Q4_0) ? 32 : 256;
     const int64_t nb = cols / be, kb = gv::kKR / be;
     return (nb + kb - 1) / kb;
 }
@@ -455,6 +457,8 @@ cudaError_t launch5_type(int type, const gv5::Args& a, const Plan5& pl, cudaStre
     case T_Q5_0: return launch5_t<T_Q5_0, SWI>(a, pl, s);
     case T_Q4_0: return launch5_t<T_Q4_0, SWI>(a, pl, s);
     case T_Q5_K: return launch5_t<T_Q5_K, SWI>(a, pl, s);
+    case T_Q2_K: return launch5_t<T_Q2_K, SWI>(a, pl, s);
+    case T_Q3_K: return launch5_t<T_Q3_K, SWI>(a, pl, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -467,6 +471,8 @@ int64_t row_bytes_of(int type, int64_t cols) {
     case T_Q5_0: return cols / 32 * 22;
     case T_Q4_0: return cols / 32 * 18;
     case T_Q5_K: return cols / 256 * 176;
+    case T_Q2_K: return cols / 256 * 84;
+    case T_Q3_K: return cols / 256 * 110;
     }
     return 0;
 }

@@ -35,7 +35,7 @@ enum : uint32_t {   // metadata value types
 };
 
 enum : uint32_t {   // ggml tensor types this library sizes
-    G_F32 = 0, G_F16 = 1, G_Q4_0 = 2, G_Q5_0 = 6, G_Q8_0 = 8, G_Q4_K = 12, G_Q5_K = 13, G_Q6_K = 14, G_BF16 = 30
+    G_F32 = 0, G_F16 = 1, G_Q4_0 = 2, G_Q5_0 = 6, G_Q8_0 = 8, G_Q2_K = 10, G_Q3_K = 11, G_Q4_K = 12, G_Q5_K = 13, G_Q6_K = 14, G_BF16 = 30
 };
 
 constexpr int kMaxDims = 4;
@@ -64,6 +64,8 @@ void ggml_block(uint32_t g, uint64_t& bb, uint64_t& be, int& qt) {
     case G_Q8_0: bb = 34; be = 32; qt = QK_Q8_0; return;
     case G_Q4_K: bb = 144; be = 256; qt = QK_Q4_K; return;
     case G_Q5_K: bb = 176; be = 256; qt = QK_Q5_K; return;
+    case G_Q2_K: bb = 84; be = 256; qt = QK_Q2_K; return;
+    case G_Q3_K: bb = 110; be = 256; qt = QK_Q3_K; return;
     case G_Q6_K: bb = 210; be = 256; qt = QK_Q6_K; return;
     }
     bb = 0;

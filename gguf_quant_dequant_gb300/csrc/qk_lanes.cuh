@@ -198,6 +198,95 @@ template <> struct Lane<T_Q5_K> {
     }
 };
 
+// Q2_K and Q3_K: lane l -> super-block l/4, c = l%4, x-blocks 2l and 2l+1:
+// weights 64c .. 64c+63 = 16-weight groups 4c .. 4c+3.  All of them take
+// their 2-bit codes from bytes 32t .. 32t+31 of the code plane (t = c/2):
+// x-block e uses bits 2j.. with j = 2(c%2) + e, bytes 0-15 for its first
+// group and 16-31 for its second.  Per group the dp4a sums stay separate and
+// are weighted by the group's integer scale before the conversion to fp32.
+template <> struct Lane<T_Q2_K> {
+    int sb, c;
+    __device__ __forceinline__ explicit Lane(int lane) : sb(lane >> 2), c(lane & 3) {}
+    __device__ __forceinline__ bool valid(int nblk) const { return sb < nblk; }
+    __device__ __forceinline__ void xblocks(int lane, int& j0, int& j1) const { j0 = 2 * lane; j1 = 2 * lane + 1; }
+    // Blocks are 84 bytes: 4-byte aligned wherever a row starts on 4 bytes.
+    __device__ __forceinline__ float dot(const uint8_t* seg, const XL& x, int nblk) const {
+        const uint8_t* blk = seg + sb * 84;
+        uint32_t q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = lds32(blk + 16 + 32 * (c >> 1) + 4 * i);
+        const uint32_t sm = lds32(blk + 4 * c);   // (scale, min) bytes of groups 4c .. 4c+3
+        const uint32_t dd = lds32(blk + 80);      // d, dmin
+        float r = 0.0f, rm = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int sh = 2 * (2 * (c & 1) + e);
+            uint32_t lo[4], hi[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                lo[i] = (q[i] >> sh) & 0x03030303u;
+                hi[i] = (q[4 + i] >> sh) & 0x03030303u;
+            }
+            int A0 = 0, B0 = 0, C0 = 0, A1 = 0, B1 = 0, C1 = 0;
+            dot16(lo, x, e, 0, A0, B0, C0);
+            dot16(hi, x, e, 4, A1, B1, C1);
+            const int s0 = (int)((sm >> (16 * e)) & 15u), s1 = (int)((sm >> (16 * e + 8)) & 15u);
+            const float m0 = (float)((sm >> (16 * e + 4)) & 15u), m1 = (float)((sm >> (16 * e + 12)) & 15u);
+            const float4 mt = x.meta[e];
+            r = fmaf(mt.x, limbs3_to_f(s0 * A0 + s1 * A1, s0 * B0 + s1 * B1, s0 * C0 + s1 * C1), r);
+            rm = fmaf(m0, mt.y, fmaf(m1, mt.z, rm));
+        }
+        return h2f(dd & 0xFFFFu) * r - h2f(dd >> 16) * rm;
+    }
+};
+
+template <> struct Lane<T_Q3_K> {
+    int sb, c;
+    __device__ __forceinline__ explicit Lane(int lane) : sb(lane >> 2), c(lane & 3) {}
+    __device__ __forceinline__ bool valid(int nblk) const { return sb < nblk; }
+    __device__ __forceinline__ void xblocks(int lane, int& j0, int& j1) const { j0 = 2 * lane; j1 = 2 * lane + 1; }
+    // Blocks are 110 bytes (2-byte aligned): words through funnel shifts.
+    // A code u = lo2 | mask bit << 2 (0..7) is q + 4: sum q x = sum u x - 4 sum x.
+    __device__ __forceinline__ float dot(const uint8_t* seg, const XL& x, int nblk) const {
+        const uint8_t* blk = seg + sb * 110;
+        uint32_t q[8], hm[8], sw[1];
+        lds_words_a2<8>(blk + 32 + 32 * (c >> 1), q);
+        lds_words_a2<8>(blk, hm);
+        lds_words_a2<1>(blk + 96 + 4 * (c & 1), sw);      // low nibbles of groups 4c.. (byte g % 8)
+        uint32_t sh2[1];
+        lds_words_a2<1>(blk + 104, sh2);                   // high bit pairs (byte 8 + g % 4)
+        const uint32_t lo4w = sw[0] >> (4 * (c >> 1));     // nibble g / 8 of bytes 4(c%2) ..
+        const float d = h2f(ld_u16(blk + 108));
+        float r = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int j = 2 * (c & 1) + e, sh = 2 * j, hb = 4 * (c >> 1) + j;
+            uint32_t lo[4], hi[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                lo[i] = ((q[i] >> sh) & 0x03030303u) | (((hm[i] >> hb) & 0x01010101u) << 2);
+                hi[i] = ((q[4 + i] >> sh) & 0x03030303u) | (((hm[4 + i] >> hb) & 0x01010101u) << 2);
+            }
+            int A0 = 0, B0 = 0, C0 = 0, A1 = 0, B1 = 0, C1 = 0;
+            dot16(lo, x, e, 0, A0, B0, C0);
+            dot16(hi, x, e, 4, A1, B1, C1);
+            // Groups 4c + 2e and 4c + 2e + 1: byte k = 2e (+1) of the words.
+            int sc[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int g = 4 * c + 2 * e + k;
+                const uint32_t l4 = (lo4w >> (8 * (2 * e + k))) & 15u;
+                const uint32_t h2 = (sh2[0] >> (8 * (g & 3) + 2 * (g >> 2))) & 3u;
+                sc[k] = (int)(l4 | (h2 << 4)) - 32;
+            }
+            const float4 mt = x.meta[e];
+            const float T = limbs3_to_f(sc[0] * A0 + sc[1] * A1, sc[0] * B0 + sc[1] * B1, sc[0] * C0 + sc[1] * C1);
+            r += fmaf(mt.x, T, -4.0f * fmaf((float)sc[0], mt.y, (float)sc[1] * mt.z));
+        }
+        return d * r;
+    }
+};
+
 // Byte k of v as an exact fp32 (0..255), via the 2^23 magic constant.
 __device__ __forceinline__ float byte_to_f(uint32_t v, uint32_t sel) {
     return __uint_as_float(__byte_perm(v, 0x4B000000u, sel)) - 8388608.0f;

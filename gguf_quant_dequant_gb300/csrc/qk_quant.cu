@@ -9,6 +9,10 @@
 //        dmin = fp16(max m_f / 63); sc = cr(sc_f / d, 0, 63),
 //        m = cr(m_f / dmin, 0, 63); q = cr((w + dmin*m) / (d*sc), 0, 15).
 //   Q5_K, the same with 31 in place of 15 (codes 0..31).
+//   Q2_K, per 16 weights: the Q4_K scheme with 3 steps, d = fp16(max sc_f /
+//        15), dmin = fp16(max m_f / 15), 4-bit sc and m, codes 0..3.
+//   Q3_K, per 16 weights: s = max|w| / 4; d = fp16(max s / 31);
+//        sc = cr(s / d, -32, 31); q = cr(w / (d*sc), -4, 3).
 //   Q6_K, per 16 weights: s = max|w| / 32; d = fp16(max s / 127);
 //        sc = cr(s / d, -128, 127); q = cr(w / (d*sc), -32, 31) + 32.
 //   Q8_0 / Q5_0 / Q4_0, per 32 weights: d = fp16(max|w| / 127, 15, 7);
@@ -165,6 +169,134 @@ __device__ __forceinline__ void lane_q5k(const float (&v)[32], int lane, bool li
     if (j == 0) st_u32(blk, db | (dmb << 16));
 }
 
+// Q2_K / Q3_K: lane j = lane % 8 holds weights 32j .. 32j+31 of its
+// super-block (groups 2j, 2j+1), whose 2-bit fields are bits 2(j%4).. of code
+// bytes 32(j/4) .. +31: the four lanes that share those bytes OR their
+// fields together.  Q3_K's mask bit of weight 32j + l is bit j of hmask[l]
+// (gathered as Q5_K's fifth bits).  `blk` is 4-byte (Q2_K) or 2-byte (Q3_K)
+// aligned.
+__device__ __forceinline__ void plane_words(const int (&q)[32], int j, uint32_t (&wd)[8]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        uint32_t w = bytes4(&q[4 * k]) << (2 * (j & 3));
+        w |= __shfl_xor_sync(kFull, w, 1);
+        w |= __shfl_xor_sync(kFull, w, 2);
+        wd[k] = w;
+    }
+}
+
+__device__ __forceinline__ void lane_q2k(const float (&v)[32], int lane, bool live, uint8_t* blk) {
+    const int j = lane & 7;
+    float scf[2], mf[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        float lo = 0.0f, hi = v[16 * e];
+#pragma unroll
+        for (int l = 0; l < 16; ++l) {
+            if (v[16 * e + l] < lo) lo = v[16 * e + l];
+            if (v[16 * e + l] > hi) hi = v[16 * e + l];
+        }
+        scf[e] = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
+        mf[e] = -lo;
+    }
+    const float c0 = scf[0] > 0.0f ? scf[0] : 0.0f, c1 = scf[1] > 0.0f ? scf[1] : 0.0f;
+    const float n0 = mf[0] > 0.0f ? mf[0] : 0.0f, n1 = mf[1] > 0.0f ? mf[1] : 0.0f;
+    const uint32_t db = half_bits(__fdiv_rn(group_max_pos<8>(c1 > c0 ? c1 : c0), 15.0f));
+    const uint32_t dmb = half_bits(__fdiv_rn(group_max_pos<8>(n1 > n0 ? n1 : n0), 15.0f));
+    const float d = half_val(db), dmin = half_val(dmb);
+    int q[32];
+    uint32_t sm = 0;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int s = d > 0.0f ? cr(__fdiv_rn(scf[e], d), 0, 15) : 0;
+        const int m = dmin > 0.0f ? cr(__fdiv_rn(mf[e], dmin), 0, 15) : 0;
+        const float ds = __fmul_rn(d, (float)s), dm = __fmul_rn(dmin, (float)m);
+#pragma unroll
+        for (int l = 0; l < 16; ++l)
+            q[16 * e + l] = ds > 0.0f ? cr(__fdiv_rn(__fadd_rn(v[16 * e + l], dm), ds), 0, 3) : 0;
+        sm |= (uint32_t)(s | (m << 4)) << (8 * e);
+    }
+    uint32_t wd[8];
+    plane_words(q, j, wd);
+    if (!live) return;
+    if ((j & 3) == 0) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) st_u32(blk + 16 + 32 * (j >> 2) + 4 * k, wd[k]);
+    }
+    st_u16(blk + 2 * j, sm);
+    if (j == 0) st_u32(blk + 80, db | (dmb << 16));
+}
+
+__device__ __forceinline__ void lane_q3k(const float (&v)[32], int lane, bool live, uint8_t* blk) {
+    const int j = lane & 7;
+    float sf[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        float a = 0.0f;
+#pragma unroll
+        for (int l = 0; l < 16; ++l) {
+            const float x = fabsf(v[16 * e + l]);
+            if (x > a) a = x;
+        }
+        sf[e] = __fdiv_rn(a, 4.0f);
+    }
+    const float c0 = sf[0] > 0.0f ? sf[0] : 0.0f, c1 = sf[1] > 0.0f ? sf[1] : 0.0f;
+    const uint32_t db = half_bits(__fdiv_rn(group_max_pos<8>(c1 > c0 ? c1 : c0), 31.0f));
+    const float d = half_val(db);
+    int q[32], lo2[32], sv[2];
+    uint32_t hb = 0;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int s = d > 0.0f ? cr(__fdiv_rn(sf[e], d), -32, 31) : 0;
+        const float ds = __fmul_rn(d, (float)s);
+#pragma unroll
+        for (int l = 0; l < 16; ++l) q[16 * e + l] = ds != 0.0f ? cr(__fdiv_rn(v[16 * e + l], ds), -4, 3) : 0;
+        sv[e] = s + 32;
+    }
+#pragma unroll
+    for (int l = 0; l < 32; ++l) {
+        lo2[l] = q[l] >= 0 ? q[l] : q[l] + 4;
+        hb |= (uint32_t)(q[l] >= 0) << l;
+    }
+    uint32_t wd[8];
+    plane_words(lo2, j, wd);
+    // hmask bytes 4j .. 4j+3: bit j' of byte l from lane j'.
+    uint32_t hmw = 0;
+#pragma unroll
+    for (int jp = 0; jp < 8; ++jp) {
+        const uint32_t t = __shfl_sync(kFull, hb, (lane & ~7) + jp);
+        hmw |= spread4((t >> (4 * j)) & 15u) << jp;
+    }
+    // Scales of groups g = 2j + e (value + 32): low nibble g/8 of byte g%8
+    // (lanes j and j + 4 share bytes 2j, 2j+1), high bits at 2(g/4) of byte
+    // 8 + g%4 (all eight lanes share bytes 8..11).
+    const int up0 = __shfl_down_sync(kFull, sv[0], 4), up1 = __shfl_down_sync(kFull, sv[1], 4);
+    uint32_t hi2 = 0;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) hi2 |= (uint32_t)(sv[e] >> 4) << (8 * (2 * (j & 1) + e) + 2 * (j >> 1));
+    hi2 |= __shfl_xor_sync(kFull, hi2, 1);
+    hi2 |= __shfl_xor_sync(kFull, hi2, 2);
+    hi2 |= __shfl_xor_sync(kFull, hi2, 4);
+    if (!live) return;
+    if ((j & 3) == 0) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            st_u16(blk + 32 + 32 * (j >> 2) + 4 * k, wd[k]);
+            st_u16(blk + 34 + 32 * (j >> 2) + 4 * k, wd[k] >> 16);
+        }
+    }
+    st_u16(blk + 4 * j, hmw);
+    st_u16(blk + 4 * j + 2, hmw >> 16);
+    if (j < 4)
+        st_u16(blk + 96 + 2 * j, (uint32_t)((sv[0] & 15) | ((up0 & 15) << 4)) |
+                                     ((uint32_t)((sv[1] & 15) | ((up1 & 15) << 4)) << 8));
+    if (j == 0) {
+        st_u16(blk + 104, hi2);
+        st_u16(blk + 106, hi2 >> 16);
+        st_u16(blk + 108, db);
+    }
+}
+
 // Q6_K: lane t = lane % 8 holds weights 32t .. 32t+31 of super-block `sb`,
 // i.e. half h = t / 4, group g = t % 4, and scale groups 2t, 2t+1.  Bytes at
 // `blk` (2-byte aligned).
@@ -275,7 +407,7 @@ __device__ __forceinline__ void lane_small(const float (&v)[32], bool live, uint
 template <int T>
 __global__ void __launch_bounds__(kWarps * 32) quantize_kernel(const float* __restrict__ w, int64_t ngroups,
                                                                 uint8_t* __restrict__ out) {
-    constexpr bool kK = T == T_Q4_K || T == T_Q6_K || T == T_Q5_K;
+    constexpr bool kK = T == T_Q4_K || T == T_Q6_K || T == T_Q5_K || T == T_Q2_K || T == T_Q3_K;
     constexpr int kBB = Fmt<T>::BB;
     __shared__ uint32_t buf[kWarps][kBufWords];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -302,6 +434,8 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_kernel(const float* __re
     uint8_t* sb = reinterpret_cast<uint8_t*>(buf[warp]);
     if constexpr (T == T_Q4_K) lane_q4k(v, lane, live, sb + (lane >> 3) * kBB);
     else if constexpr (T == T_Q5_K) lane_q5k(v, lane, live, sb + (lane >> 3) * kBB);
+    else if constexpr (T == T_Q2_K) lane_q2k(v, lane, live, sb + (lane >> 3) * kBB);
+    else if constexpr (T == T_Q3_K) lane_q3k(v, lane, live, sb + (lane >> 3) * kBB);
     else if constexpr (T == T_Q6_K) lane_q6k(v, lane, live, sb + (lane >> 3) * kBB);
     else lane_small<T>(v, live, sb + lane * kBB);
     __syncwarp();
@@ -334,6 +468,8 @@ cudaError_t launch_quantize(int type, const float* w, int64_t rows, int64_t cols
     case T_Q5_0: return qz::launch_t<T_Q5_0>(w, ngroups, out, s);
     case T_Q4_0: return qz::launch_t<T_Q4_0>(w, ngroups, out, s);
     case T_Q5_K: return qz::launch_t<T_Q5_K>(w, ngroups, out, s);
+    case T_Q2_K: return qz::launch_t<T_Q2_K>(w, ngroups, out, s);
+    case T_Q3_K: return qz::launch_t<T_Q3_K>(w, ngroups, out, s);
     default: return cudaErrorInvalidValue;
     }
 }

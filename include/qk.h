@@ -31,6 +31,16 @@
  *         its size ("12 -- llama.cpp / GGUF", "Other k-quants at a glance":
  *         256-weight super-block, 5.5-5.7 bits/weight); the layout is the
  *         GGUF k-quant one.
+ *   Q2_K  256 weights in 84 bytes, sixteen 16-weight groups: 16 bytes of
+ *         (4-bit scale, 4-bit min) per group, 64 bytes of 2-bit codes (code
+ *         l of group 8t + 2j + k is bits 2j.. of byte 32t + 16k + l), fp16 d,
+ *         fp16 dmin; weight = (d*sc)*q - dmin*m.  (Pages: 2.5-2.6 bits/weight
+ *         on 256-weight super-blocks, same table; layout: GGUF.)
+ *   Q3_K  256 weights in 110 bytes: 32 bytes of high-bit mask, 64 bytes of
+ *         2-bit codes placed as Q2_K's, 12 bytes of sixteen 6-bit scales
+ *         (stored + 32), fp16 d; a code is its 2 bits minus 4 unless its
+ *         mask bit (bit 4t + j of byte 16k + l) is set; weight = (d*sc)*q.
+ *         (Pages: 3.4-4.0 bits/weight, same table; layout: GGUF.)
  * The bit placement inside the Q4_K scale bytes, the Q6_K code bytes and the
  * Q5_0 block is the k-quant / GGUF packing: low nibbles of a group of bytes
  * are the first weights, high nibbles the next ("How LLM Inference Engines
@@ -67,7 +77,9 @@ extern "C" {
 #endif
 
 /* Quant types.  The numbers are this library's own. */
-typedef enum { QK_Q4_K = 1, QK_Q6_K = 2, QK_Q8_0 = 3, QK_Q5_0 = 4, QK_Q4_0 = 5, QK_Q5_K = 6 } qk_type;
+typedef enum {
+    QK_Q4_K = 1, QK_Q6_K = 2, QK_Q8_0 = 3, QK_Q5_0 = 4, QK_Q4_0 = 5, QK_Q5_K = 6, QK_Q2_K = 7, QK_Q3_K = 8
+} qk_type;
 
 typedef enum {
     QK_OK = 0,
@@ -120,6 +132,10 @@ qk_status qk_dequant(int type, const void* W, int64_t rows, int64_t cols,
  *        dmin = fp16(max m_f / 63); sc = cr(sc_f/d, 0..63),
  *        m = cr(m_f/dmin, 0..63); q = cr((w + dmin*m) / (d*sc), 0..15).
  *   Q5_K the same with 31 in place of 15.
+ *   Q2_K per 16 weights: the Q4_K scheme with 3 in place of 15 and 4-bit
+ *        sc, m (d = fp16(max sc_f / 15), dmin = fp16(max m_f / 15)).
+ *   Q3_K per 16 weights: s = max|w| / 4, d = fp16(max s / 31),
+ *        sc = cr(s/d, -32..31), q = cr(w / (d*sc), -4..3).
  *   Q6_K per 16 weights: s = max|w| / 32, d = fp16(max s / 127),
  *        sc = cr(s/d, -128..127), q = cr(w / (d*sc), -32..31) + 32.
  *   Q8_0 / Q5_0 / Q4_0 per 32: d = fp16(max|w| / 127 | 15 | 7),
@@ -250,12 +266,15 @@ qk_status qk_gemm(int type, const void* W, int64_t rows, int64_t cols,
                   void* ws, size_t ws_bytes, void* stream);
 
 /* Test hook: unpack nblocks consecutive blocks into their integer fields.
- *   codes int16 [nblocks * block_elems]: Q4_K 0..15, Q6_K 0..63,
- *         Q8_0 -128..127, Q5_0 0..31.
- *   sc    int16 [nblocks * 16]: Q4_K 6-bit scales in slots 0..7, Q6_K the
- *         sixteen int8 scales; other slots and types 0.
- *   mins  uint8 [nblocks * 8]: Q4_K 6-bit mins; 0 for other types.
- *   d, dmin fp32 [nblocks]: the decoded binary16 fields (dmin 0 unless Q4_K).
+ *   codes int16 [nblocks * block_elems]: Q4_K 0..15, Q5_K 0..31, Q6_K 0..63,
+ *         Q8_0 -128..127, Q5_0 0..31, Q4_0 0..15, Q2_K 0..3, Q3_K -4..3.
+ *   sc    int16 [nblocks * 16]: Q4_K / Q5_K 6-bit scales in slots 0..7, Q6_K
+ *         the sixteen int8 scales, Q2_K the 4-bit scales, Q3_K the scales
+ *         (-32..31); other slots and types 0.
+ *   mins  uint8 [nblocks * 16]: Q4_K / Q5_K 6-bit mins (8 used), Q2_K 4-bit
+ *         mins; 0 elsewhere.
+ *   d, dmin fp32 [nblocks]: the decoded binary16 fields (dmin 0 unless the
+ *         type has one: Q4_K, Q5_K, Q2_K).
  * All outputs device memory, any may be NULL.  W 16-byte aligned. */
 qk_status qk_unpack(int type, const void* W, int64_t nblocks, int16_t* codes,
                     int16_t* sc, uint8_t* mins, float* d, float* dmin, void* stream);
@@ -285,8 +304,8 @@ qk_status qk_device_status(void* stream);
  * Versions 2 and 3, little-endian.  The value-type codes (0 u8, 1 i8, 2 u16,
  * 3 i16, 4 u32, 5 i32, 6 f32, 7 bool, 8 string, 9 array, 10 u64, 11 i64,
  * 12 f64), the ggml tensor types (0 F32, 1 F16, 2 Q4_0, 6 Q5_0, 8 Q8_0,
- * 12 Q4_K, 13 Q5_K, 14 Q6_K, 30 BF16 are sized here; others are listed with
- * nbytes 0)
+ * 10 Q2_K, 11 Q3_K, 12 Q4_K, 13 Q5_K, 14 Q6_K, 30 BF16 are sized here;
+ * others are listed with nbytes 0)
  * and the "general.alignment" key (uint32 power of two, default 32) follow
  * the GGUF specification the page cites.
  * Every length, count and offset is checked against the image before use;

@@ -16,7 +16,7 @@ VT = {"u8": 0, "i8": 1, "u16": 2, "i16": 3, "u32": 4, "i32": 5, "f32": 6, "bool"
       "u64": 10, "i64": 11, "f64": 12}
 FMT = {"u8": "<B", "i8": "<b", "u16": "<H", "i16": "<h", "u32": "<I", "i32": "<i", "f32": "<f", "bool": "<?",
        "u64": "<Q", "i64": "<q", "f64": "<d"}
-GGML = {"F32": 0, "F16": 1, "Q4_0": 2, "Q5_0": 6, "Q8_0": 8, "Q2_K": 10, "Q4_K": 12, "Q5_K": 13, "Q6_K": 14, "BF16": 30}
+GGML = {"F32": 0, "F16": 1, "Q4_0": 2, "Q4_1": 3, "Q5_0": 6, "Q8_0": 8, "Q2_K": 10, "Q3_K": 11, "Q4_K": 12, "Q5_K": 13, "Q6_K": 14, "BF16": 30}
 
 
 def _s(text: str | bytes) -> bytes:

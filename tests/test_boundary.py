@@ -55,7 +55,7 @@ def test_argument_errors_are_caught_on_host(lib):
     fake = ctypes.c_void_p(0x10000)          # 16-byte aligned, never dereferenced
     odd = ctypes.c_void_p(0x10008)           # 8-byte aligned only
     # bad type
-    assert lib.qk_gemv(7, fake, 4, 256, fake, 1, fake, None, 0, None) == 1
+    assert lib.qk_gemv(99, fake, 4, 256, fake, 1, fake, None, 0, None) == 1
     assert b"type" in lib.qk_last_error()
     # cols not a multiple of the block
     assert lib.qk_gemv(qk.Q4_K, fake, 4, 100, fake, 1, fake, None, 0, None) == 2

@@ -13,7 +13,7 @@ from golden_io import all_fixtures, load
 from gpu_helpers import dev_u8, gpu, type_id  # noqa: F401
 
 pytestmark = pytest.mark.gpu
-NAMES = ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K"]
+NAMES = ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K", "Q2_K", "Q3_K"]
 
 
 @pytest.mark.parametrize("name", NAMES)

@@ -28,6 +28,9 @@ CASES = [
     ("Q5_0", 128, 320, 513),     # second tile holds a single token
     ("Q4_0", 200, 1056, 77),
     ("Q5_K", 200, 512, 300),     # the wide kernel: ragged rows, a partial second token tile
+    ("Q2_K", 200, 512, 300),
+    ("Q3_K", 130, 768, 600),
+    ("Q3_K", 130, 768, 40),      # rows of 330 bytes: the wide kernel at a small batch
     # Skinny pipeline (M <= 64): fewer k-blocks than operand stages, a half
     # k-block at the end, ragged rows, one token.
     ("Q4_K", 130, 256, 40),
@@ -36,6 +39,8 @@ CASES = [
     ("Q6_K", 129, 1536, 2),
     ("Q4_0", 128, 64 * 32, 63),
     ("Q5_K", 130, 768, 40),
+    ("Q2_K", 130, 1024, 40),
+    ("Q3_K", 200, 2048, 16),
 ]
 
 
@@ -95,6 +100,8 @@ SPLIT_CASES = [
     ("Q4_K", 130, 2048, 1),
     ("Q4_0", 64, 8192, 5),
     ("Q5_K", 300, 8192, 16),
+    ("Q3_K", 96, 8192, 4),
+    ("Q2_K", 64, 8192, 9),
 ]
 
 

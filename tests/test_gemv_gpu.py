@@ -11,7 +11,7 @@ import synth
 from gpu_helpers import assert_gemv_close, dev_f32, dev_u8, gpu, type_id  # noqa: F401
 
 pytestmark = pytest.mark.gpu
-NAMES = ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K"]
+NAMES = ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K", "Q2_K", "Q3_K"]
 
 
 def run(gpu, name, rows, cols, M, seed, W=None, x=None):
@@ -36,6 +36,8 @@ SHAPES = {
     "Q5_0": [(1, 32), (5, 1056), (37, 3104), (300, 1024)],
     "Q4_0": [(1, 32), (5, 1056), (37, 3104), (300, 1024)],
     "Q5_K": [(1, 256), (5, 1280), (37, 3328), (300, 1024)],
+    "Q2_K": [(1, 256), (5, 1280), (37, 3328), (300, 1024)],
+    "Q3_K": [(1, 256), (5, 1280), (37, 3328), (300, 1024)],
 }
 
 
@@ -161,6 +163,7 @@ def test_decode_needs_no_workspace_and_large_k_falls_back(gpu):
 
 @pytest.mark.parametrize("name,rows,cols", [("Q6_K", 9, 11008), ("Q4_K", 151, 4096), ("Q4_K", 153, 2304),
                                             ("Q5_K", 151, 4096), ("Q5_K", 1000, 11008),
+                                            ("Q2_K", 151, 4096), ("Q3_K", 1000, 11008),
                                             ("Q8_0", 1000, 4128), ("Q5_0", 3, 96)])
 def test_decode_row_splits(gpu, name, rows, cols):
     # Fewer rows than SMs, one row more than the SMs on some CTAs, a K whose

@@ -94,10 +94,11 @@ KVS = [
 
 def rich_tensors():
     rng = np.random.default_rng(42)
-    ts = [("unsized.q2k", [256, 1], "Q2_K", rng.integers(0, 256, 84, dtype=np.uint8).tobytes())]
+    ts = [("unsized.q41", [32, 1], "Q4_1", rng.integers(0, 256, 20, dtype=np.uint8).tobytes())]
     for name, gt, rows, cols in (("blk.0.ffn_up.weight", "Q4_K", 8, 1024), ("blk.0.attn_v.weight", "Q6_K", 3, 256),
                                  ("blk.0.attn_q.weight", "Q8_0", 5, 64), ("blk.0.ffn_gate.weight", "Q5_0", 2, 32),
-                                 ("blk.0.attn_k.weight", "Q4_0", 1, 96)):
+                                 ("blk.0.attn_k.weight", "Q4_0", 1, 96), ("blk.1.attn_q.weight", "Q5_K", 2, 512),
+                                 ("blk.1.ffn_up.weight", "Q2_K", 3, 256), ("blk.1.ffn_down.weight", "Q3_K", 2, 768)):
         ts.append((name, [cols, rows], gt, synth.random_blocks(gt, rows, cols, 300 + rows).tobytes()))
     ts.append(("norm.weight", [7], "F32", rng.standard_normal(7).astype(np.float32).tobytes()))
     ts.append(("emb.f16", [4, 2], "F16", rng.standard_normal(8).astype(np.float16).tobytes()))
@@ -133,7 +134,7 @@ def test_rich_file_matches_the_oracle_reader(tmp_path):
             assert [(t["name"], t["dims"], t["ggml_type"], t["offset"] - o["data_offset"]) for t in tens] == \
                 [(n, d, gt, off) for (n, d, gt, off) in o["tensors"]]
             for (name, dims, gt, blob), t in zip(ts, tens):
-                if gt == "Q2_K":
+                if gt == "Q4_1":
                     assert t["nbytes"] == 0 and t["qk_type"] == -1   # not sized by this library
                     continue
                 assert t["nbytes"] == len(blob) and g.tensor_bytes(name) == blob
@@ -158,7 +159,7 @@ def test_every_truncation_is_rejected():
     data = write(KVS, ts, alignment=32)
     o = og.read(data)
     # The last sized tensor's data ends here; the unsized one comes first.
-    last = max(off + len(blob) for (_, _, _, off), (_, _, gt, blob) in zip(o["tensors"], ts) if gt != "Q2_K")
+    last = max(off + len(blob) for (_, _, _, off), (_, _, gt, blob) in zip(o["tensors"], ts) if gt != "Q4_1")
     end = o["data_offset"] + last
     for n in range(len(data) + 1):
         st = _status(data[:n])

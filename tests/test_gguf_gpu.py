@@ -17,7 +17,8 @@ pytestmark = pytest.mark.gpu
 
 SHAPES = [("blk.0.attn_q.weight", "Q4_K", 96, 1024), ("blk.0.attn_v.weight", "Q6_K", 40, 512),
           ("blk.0.ffn_down.weight", "Q8_0", 33, 1024), ("blk.0.ffn_gate.weight", "Q5_0", 17, 256),
-          ("blk.0.ffn_up.weight", "Q4_0", 64, 2048), ("blk.0.attn_k.weight", "Q5_K", 40, 1024)]
+          ("blk.0.ffn_up.weight", "Q4_0", 64, 2048), ("blk.0.attn_k.weight", "Q5_K", 40, 1024),
+          ("blk.1.ffn_up.weight", "Q2_K", 24, 1024), ("blk.1.ffn_down.weight", "Q3_K", 16, 768)]
 
 
 def test_gemv_from_a_gguf_file(gpu, tmp_path):

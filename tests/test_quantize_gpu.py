@@ -29,6 +29,10 @@ CASES = [
     ("Q4_0", 3, 352),
     ("Q5_K", 3, 768),
     ("Q5_K", 37, 2048),
+    ("Q2_K", 3, 768),
+    ("Q2_K", 37, 2048),
+    ("Q3_K", 3, 768),
+    ("Q3_K", 37, 2048),
 ]
 
 
@@ -73,10 +77,10 @@ def special_blocks(n):
     return np.stack([np.asarray(r, np.float32) for r in rows])
 
 
-@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K"])
+@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K", "Q2_K", "Q3_K"])
 def test_quantize_special_values(gpu, name):
     t = type_id(name)
-    n = 256 if name in ("Q4_K", "Q6_K", "Q5_K") else 32
+    n = 256 if name in ("Q4_K", "Q6_K", "Q5_K", "Q2_K", "Q3_K") else 32
     w = special_blocks(n)
     # Repeat the patterns along each row so every lane position of a warp sees them.
     w = np.tile(w, (1, 8))

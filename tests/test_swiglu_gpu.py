@@ -23,6 +23,8 @@ CASES = [
     ("Q5_0", 17, 256),
     ("Q4_0", 40, 4096),
     ("Q5_K", 96, 2048),
+    ("Q2_K", 64, 1024),
+    ("Q3_K", 50, 2048),
 ]
 
 
