@@ -51,6 +51,7 @@ SIGNATURES = {
     "qk_row_bytes": (_sz, [_int, _i64]),
     "qk_dequant": (_int, [_int, _p, _i64, _i64, _p, _int, _p]),
     "qk_quantize": (_int, [_int, _p, _i64, _i64, _p, _p]),
+    "qk_quantize_imatrix": (_int, [_int, _p, _i64, _i64, _p, _p, _p]),
     "qk_gemv_workspace": (_sz, [_int, _i64, _i64, _i64]),
     "qk_gemv": (_int, [_int, _p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
     "qk_gemv_noalloc": (_int, [_int, _p, _i64, _i64, _p, _i64, _p, _p]),
@@ -156,6 +157,19 @@ def quantize(t: int, w, out=None, stream=None):
     if out is None:
         out = torch.empty(rows * row_bytes(t, cols), dtype=torch.uint8, device=w.device)
     _check(load().qk_quantize(t, _ptr(w), rows, cols, _ptr(out), _stream(stream)), "qk_quantize")
+    return out
+
+
+def quantize_imatrix(t: int, w, imp, out=None, stream=None):
+    """w: fp32 CUDA [rows, cols], imp: fp32 CUDA [cols] column importances
+    (mean squared activations) -> packed blocks minimising the
+    importance-weighted error (qk_quantize_imatrix)."""
+    import torch
+    rows, cols = w.shape
+    if out is None:
+        out = torch.empty(rows * row_bytes(t, cols), dtype=torch.uint8, device=w.device)
+    _check(load().qk_quantize_imatrix(t, _ptr(w), rows, cols, _ptr(imp), _ptr(out), _stream(stream)),
+           "qk_quantize_imatrix")
     return out
 
 

@@ -160,6 +160,25 @@ qk_status qk_quantize(int type, const float* w, int64_t rows, int64_t cols, void
     return QK_OK;
 }
 
+qk_status qk_quantize_imatrix(int type, const float* w, int64_t rows, int64_t cols, const float* imp, void* out,
+                              void* stream) {
+    if (!known_type(type)) return fail(QK_ERR_TYPE, "unknown type %d", type);
+    if (rows < 0 || cols < 0 || cols % block_elems(type) != 0)
+        return fail(QK_ERR_SHAPE, "bad shape rows=%lld cols=%lld", (long long)rows, (long long)cols);
+    if (rows == 0 || cols == 0) return QK_OK;
+    if (rows > (int64_t(1) << 46) / cols)
+        return fail(QK_ERR_SHAPE, "rows * cols too large (rows=%lld cols=%lld)", (long long)rows, (long long)cols);
+    if (!w) return fail(QK_ERR_NULL, "w is NULL");
+    if (!imp) return fail(QK_ERR_NULL, "imp is NULL");
+    if (!out) return fail(QK_ERR_NULL, "out is NULL");
+    if (!aligned(w, 4) || !aligned(imp, 4)) return fail(QK_ERR_ALIGN, "w or imp is not 4-byte aligned");
+    cudaError_t e = qk::launch_quantize_imatrix(type, w, imp, rows, cols, static_cast<uint8_t*>(out),
+                                               static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "qk_quantize_imatrix launch");
+    g_last_error.clear();
+    return QK_OK;
+}
+
 size_t qk_gemv_workspace(int type, int64_t rows, int64_t cols, int64_t M) {
     if (!known_type(type) || rows <= 0 || cols <= 0 || M <= 0 || cols % block_elems(type) != 0) return 0;
     return (size_t)qk::plan_gemv(type, rows, cols, M, sm_count_or_default()).ws_bytes;

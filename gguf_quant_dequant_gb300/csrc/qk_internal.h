@@ -16,6 +16,8 @@ cudaError_t launch_dequant(int type, const uint8_t* W, int64_t rows, int64_t col
                            int out_bf16, cudaStream_t s);
 
 cudaError_t launch_quantize(int type, const float* w, int64_t rows, int64_t cols, uint8_t* out, cudaStream_t s);
+cudaError_t launch_quantize_imatrix(int type, const float* w, const float* imp, int64_t rows, int64_t cols,
+                                   uint8_t* out, cudaStream_t s);
 
 cudaError_t launch_unpack(int type, const uint8_t* W, int64_t nblocks, int16_t* codes, int16_t* sc,
                           uint8_t* mins, float* d, float* dmin, cudaStream_t s);

@@ -150,6 +150,30 @@ qk_status qk_dequant(int type, const void* W, int64_t rows, int64_t cols,
  * multiple of the block size, negative sizes), QK_ERR_NULL, QK_ERR_ALIGN. */
 qk_status qk_quantize(int type, const float* w, int64_t rows, int64_t cols, void* out, void* stream);
 
+/* Importance-weighted quantization ("Hitchhiker's Guide -- Lab 01", 11.3,
+ * the importance matrix: minimise sum_i E[x_i^2] (w_i - w^_i)^2 rather than
+ * the plain weight-space error).  imp[c] is the mean squared activation met
+ * by weight column c (fp32 [cols], finite and >= 0; the same for every row).
+ * The page gives the objective, not the search; per group (the 32-weight
+ * block of Q8_0 / Q5_0 / Q4_0, the 32-weight sub-block of Q4_K / Q5_K, the
+ * 16-weight group of Q6_K / Q3_K / Q2_K):
+ *   s0 (and m0) = the plain quantizer's group scale (and min); for k = 0..20
+ *   the candidate scale s0 * (90 + k) / 100 rounds the codes, a weighted
+ *   least-squares refit gives the scale (scale and min jointly where the type
+ *   has a min; kept only with a positive determinant, a positive scale and a
+ *   non-negative min), and the candidate of least weighted error wins (the
+ *   first on ties).  The block is then assembled as by qk_quantize with
+ *   those group values, and kept only if its weighted error (summed per
+ *   group, then over groups) is no more than the plain block's; otherwise
+ *   the plain block is written.  fp32 throughout, sums in index order, so
+ *   the bytes are deterministic.  All-zero importances give qk_quantize's
+ *   bytes.
+ *   w, imp  device, 4-byte aligned.   out  rows * qk_row_bytes bytes.
+ * One thread per block: an offline step, not a bandwidth-bound kernel.
+ * Errors as qk_quantize. */
+qk_status qk_quantize_imatrix(int type, const float* w, int64_t rows, int64_t cols, const float* imp, void* out,
+                              void* stream);
+
 /* Fused decode FFN gate: h[n] = SiLU(g[n]) * u[n] with g = Wg x, u = Wu x
  * (batch 1) and SiLU(z) = z / (1 + e^-z) ("How LLM Inference Engines
  * Work", "SwiGLU Feed-Forward Network": the gate projection passes through

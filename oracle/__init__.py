@@ -71,6 +71,7 @@ def lib() -> ctypes.CDLL:
                                      _p, _p, _i64, _p, _p]
             L.oq_pack.argtypes = [ctypes.c_int, _i64, _p, _p, _p, _p, _p, _p]
             L.oq_quantize.argtypes = [ctypes.c_int, _p, _i64, _i64, _p]
+            L.oq_quantize_imatrix.argtypes = [ctypes.c_int, _p, _i64, _i64, _p, _p]
             _lib = L
     return _lib
 
@@ -232,4 +233,16 @@ def quantize(t: int, w: np.ndarray) -> np.ndarray:
     rows, cols = w.shape
     out = np.zeros(rows * row_bytes(t, cols), np.uint8)
     _check(lib().oq_quantize(t, _ptr(w), rows, cols, _ptr(out)), "quantize")
+    return out
+
+
+def quantize_imatrix(t: int, w: np.ndarray, imp: np.ndarray) -> np.ndarray:
+    """fp32 [rows, cols] and column importances fp32 [cols] (finite, >= 0)
+    -> packed blocks minimising the importance-weighted error (see
+    oq_quantize_imatrix)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    rows, cols = w.shape
+    imp = np.ascontiguousarray(imp, dtype=np.float32).reshape(cols)
+    out = np.zeros(rows * row_bytes(t, cols), np.uint8)
+    _check(lib().oq_quantize_imatrix(t, _ptr(w), rows, cols, _ptr(imp), _ptr(out)), "quantize_imatrix")
     return out

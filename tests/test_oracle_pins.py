@@ -569,3 +569,64 @@ def test_swiglu_on_an_exact_block(oracle_mod):
     ge, ue = qg @ x.astype(np.float64), qu @ x.astype(np.float64)
     assert np.array_equal(g, ge) and np.array_equal(u, ue)
     assert np.allclose(h, ge / (1.0 + np.exp(-ge)) * ue, rtol=0, atol=0)
+
+
+# ------------------------------------------- importance-weighted quantizer --
+# "Hitchhiker's Guide -- Lab 01", 11.3: minimise sum_i E[x_i^2] (w_i - w^_i)^2.
+
+def _heavy_importances(cols, seed):
+    g = np.random.default_rng(seed)
+    return (g.standard_normal(cols) ** 2 * np.exp(2.0 * g.standard_normal(cols))).astype(np.float32)
+
+
+def _block_errors(oracle_mod, t, W, w, imp):
+    rows, cols = w.shape
+    be = oracle_mod.block_elems(t)
+    dq = oracle_mod.dequant(t, W, rows, cols).astype(np.float64)
+    e = (dq - w.astype(np.float64)) ** 2 * imp.astype(np.float64)[None, :]
+    return e.reshape(rows, cols // be, be).sum(axis=2)
+
+
+@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K", "Q2_K", "Q3_K"])
+def test_imatrix_never_worse_and_clearly_better(oracle_mod, name):
+    # Per block, the weighted error never exceeds the plain quantizer's (the
+    # plain block is the fall-back); over the matrix, with heavy-tailed
+    # importances, it is clearly lower (a no-op search would fail this).
+    t = T[name]
+    w = synth.normal_weights(12, 1024, 501)
+    imp = _heavy_importances(1024, 502)
+    Wp = oracle_mod.quantize(t, w)
+    Wi = oracle_mod.quantize_imatrix(t, w, imp)
+    ep = _block_errors(oracle_mod, t, Wp, w, imp)
+    ei = _block_errors(oracle_mod, t, Wi, w, imp)
+    assert np.all(ei <= ep * (1 + 1e-5) + 1e-30)
+    assert ei.sum() < 0.8 * ep.sum()
+
+
+def test_imatrix_degenerate_importances(oracle_mod):
+    w = synth.normal_weights(4, 512, 503)
+    for name, t in T.items():
+        # All-zero importance: no refit is possible, the plain bytes come back.
+        assert np.array_equal(oracle_mod.quantize_imatrix(t, w, np.zeros(512, np.float32)), oracle_mod.quantize(t, w))
+        # Only relative importances matter: a power-of-two factor scales every
+        # sum exactly, so the bytes cannot change.
+        imp = _heavy_importances(512, 504)
+        a = oracle_mod.quantize_imatrix(t, w, imp)
+        b = oracle_mod.quantize_imatrix(t, w, imp * np.float32(8.0))
+        assert np.array_equal(a, b), name
+
+
+def test_imatrix_protects_the_important_column(oracle_mod):
+    # One dominant column per 32-block: the symmetric 32-weight types refit
+    # their scale on it, so its reconstruction error falls well below the
+    # plain quantizer's on every block.
+    rows, cols = 16, 1024
+    w = synth.normal_weights(rows, cols, 505)
+    imp = np.full(cols, 1e-6, np.float32)
+    imp[5::32] = 1.0
+    for t in (T["Q8_0"], T["Q5_0"], T["Q4_0"]):
+        dp = oracle_mod.dequant(t, oracle_mod.quantize(t, w), rows, cols)
+        di = oracle_mod.dequant(t, oracle_mod.quantize_imatrix(t, w, imp), rows, cols)
+        ep = np.abs(dp - w)[:, 5::32]
+        ei = np.abs(di - w)[:, 5::32]
+        assert ei.mean() < 0.25 * ep.mean()

@@ -119,3 +119,24 @@ def test_quantize_is_deterministic_and_takes_4_byte_aligned_output(gpu):
     assert np.array_equal(a, b[4:4 + nb])
     assert np.all(b[:4] == 0xAB) and np.all(b[4 + nb:] == 0xAB)   # nothing written outside
     assert np.array_equal(a, oracle.quantize(t, w))
+
+
+@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K", "Q2_K", "Q3_K"])
+@pytest.mark.parametrize("rows,cols", [(3, 512), (33, 2048)])
+def test_quantize_imatrix_matches_oracle(gpu, name, rows, cols):
+    # Bytes identical to the oracle's importance-weighted quantizer, with
+    # heavy-tailed importances, a run of zero-importance columns and one
+    # dominant column.
+    t = type_id(name)
+    w = synth.normal_weights(rows, cols, 610 + t)
+    g = np.random.default_rng(611 + t)
+    imp = (g.standard_normal(cols) ** 2 * np.exp(2.0 * g.standard_normal(cols))).astype(np.float32)
+    imp[40:72] = 0.0
+    imp[100] = 1e4
+    ref = oracle.quantize_imatrix(t, w, imp)
+    got = qk.quantize_imatrix(t, torch.from_numpy(w).to(gpu), torch.from_numpy(imp).to(gpu)).cpu().numpy()
+    qk.device_status()
+    assert np.array_equal(got, ref), f"{name}: {int((got != ref).sum())} bytes differ"
+    # All-zero importances: the plain quantizer's bytes.
+    z = qk.quantize_imatrix(t, torch.from_numpy(w).to(gpu), torch.zeros(cols, device=gpu)).cpu().numpy()
+    assert np.array_equal(z, oracle.quantize(t, w))
