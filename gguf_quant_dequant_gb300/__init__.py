@@ -52,6 +52,8 @@ SIGNATURES = {
     "qk_dequant": (_int, [_int, _p, _i64, _i64, _p, _int, _p]),
     "qk_quantize": (_int, [_int, _p, _i64, _i64, _p, _p]),
     "qk_quantize_imatrix": (_int, [_int, _p, _i64, _i64, _p, _p, _p]),
+    "qk_attn_decode_workspace": (ctypes.c_size_t, [_int, _i64, _int, _int, _int]),
+    "qk_attn_decode": (_int, [_int, _p, _p, _p, _i64, _int, _int, _int, ctypes.c_float, _p, _p, ctypes.c_size_t, _p]),
     "qk_gemv_workspace": (_sz, [_int, _i64, _i64, _i64]),
     "qk_gemv": (_int, [_int, _p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
     "qk_gemv_noalloc": (_int, [_int, _p, _i64, _i64, _p, _i64, _p, _p]),
@@ -170,6 +172,26 @@ def quantize_imatrix(t: int, w, imp, out=None, stream=None):
         out = torch.empty(rows * row_bytes(t, cols), dtype=torch.uint8, device=w.device)
     _check(load().qk_quantize_imatrix(t, _ptr(w), rows, cols, _ptr(imp), _ptr(out), _stream(stream)),
            "qk_quantize_imatrix")
+    return out
+
+
+def attn_decode_workspace(t: int, T: int, n_heads: int, n_kv: int, d: int) -> int:
+    return load().qk_attn_decode_workspace(t, T, n_heads, n_kv, d)
+
+
+def attn_decode(t: int, q, K, V, T: int, n_heads: int, n_kv: int, d: int, scale: float, out=None, ws=None,
+                stream=None):
+    """Decode attention over a block-quantized KV cache (qk_attn_decode):
+    q fp32 CUDA [n_heads, d]; K, V packed caches [T, n_kv, d] -> out fp32
+    [n_heads, d]."""
+    import torch
+    if out is None:
+        out = torch.empty((n_heads, d), dtype=torch.float32, device=q.device)
+    need = attn_decode_workspace(t, T, n_heads, n_kv, d)
+    if ws is None:
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(load().qk_attn_decode(t, _ptr(q), _ptr(K), _ptr(V), T, n_heads, n_kv, d, scale, _ptr(out), _ptr(ws),
+                                 ws.numel() * ws.element_size(), _stream(stream)), "qk_attn_decode")
     return out
 
 

@@ -179,6 +179,31 @@ qk_status qk_quantize_imatrix(int type, const float* w, int64_t rows, int64_t co
     return QK_OK;
 }
 
+size_t qk_attn_decode_workspace(int type, int64_t T, int n_heads, int n_kv, int d) {
+    if ((type != QK_Q8_0 && type != QK_Q5_0 && type != QK_Q4_0) || T < 1 || !qk::attn_decode_shape_ok(n_heads, n_kv, d))
+        return 0;
+    return (size_t)qk::attn_decode_ws_bytes(T, n_heads, d);
+}
+
+qk_status qk_attn_decode(int type, const float* q, const void* K, const void* V, int64_t T, int n_heads, int n_kv, int d,
+                         float scale, float* out, void* ws, size_t ws_bytes, void* stream) {
+    if (type != QK_Q8_0 && type != QK_Q5_0 && type != QK_Q4_0)
+        return fail(QK_ERR_TYPE, "KV cache type %d: Q8_0, Q5_0 or Q4_0 expected", type);
+    if (T < 1 || T > (int64_t)65535 * 256 || !qk::attn_decode_shape_ok(n_heads, n_kv, d))
+        return fail(QK_ERR_SHAPE, "bad attention shape T=%lld n_heads=%d n_kv=%d d=%d", (long long)T, n_heads, n_kv, d);
+    if (!q || !K || !V || !out || !ws) return fail(QK_ERR_NULL, "NULL pointer argument");
+    if (!aligned(q, 4) || !aligned(out, 4) || !aligned(ws, 4) || !aligned(K, 16) || !aligned(V, 16))
+        return fail(QK_ERR_ALIGN, "q, out and ws must be 4-byte aligned, K and V 16-byte aligned");
+    const int64_t need = qk::attn_decode_ws_bytes(T, n_heads, d);
+    if (ws_bytes < (size_t)need) return fail(QK_ERR_WORKSPACE, "workspace %zu bytes < %lld needed", ws_bytes, (long long)need);
+    cudaError_t e = qk::launch_attn_decode(type, q, static_cast<const uint8_t*>(K), static_cast<const uint8_t*>(V), T,
+                                           n_heads, n_kv, d, scale, out, static_cast<float*>(ws),
+                                           static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "qk_attn_decode launch");
+    g_last_error.clear();
+    return QK_OK;
+}
+
 size_t qk_gemv_workspace(int type, int64_t rows, int64_t cols, int64_t M) {
     if (!known_type(type) || rows <= 0 || cols <= 0 || M <= 0 || cols % block_elems(type) != 0) return 0;
     return (size_t)qk::plan_gemv(type, rows, cols, M, sm_count_or_default()).ws_bytes;

@@ -1,0 +1,428 @@
+// qk_attn.cu -- decode attention over a block-quantized KV cache.
+//
+// "Hitchhiker's Guide -- Lab 01", 13.2: the KV-cache is quantized at serve
+// time (q8_0 the safe default, q4_0 at a quality cost) and read inside
+// attention; the heads share K/V in groups (grouped-query attention).  One
+// query token: for query head h and its kv head g = h / (n_heads / n_kv),
+//   s_t = scale * q_h . K[t, g],  p = softmax(s),  out_h = sum_t p_t V[t, g].
+// K and V are [T, n_kv, d]; each (t, g) row is d/32 blocks of a 32-weight
+// type (Q8_0, Q5_0, Q4_0), decoded in the dot products.
+//
+// Split over positions (the cache is streamed once per token, so the work is
+// HBM-bound): CTA (g, c) takes kv head g and positions [256c, 256c + 256).
+// All its K rows and then all its V rows are requested at once with 16-byte
+// cp.async copies into shared memory (each row's aligned-down window; the
+// copy that reaches the end of the cache takes only the bytes that exist),
+// so every byte of the chunk is in flight together; the scores start as
+// soon as the K rows have landed, while V is still arriving.
+// Pass 1: each warp takes every 8th position.  With the group size G known
+// at compile time (and 4 <= G d/32 <= 32), lane l works for head l / (32/G)
+// on G d/32 consecutive elements (inside one block): the group's queries are
+// first turned into three-limb fixed point (as the decode GEMV's activations:
+// x = s (65536 a + 256 b + c) per 32-block, signed 8-bit limbs), so each
+// score is an exact integer dp4a sum over the cache's codes, added over the
+// head's lanes by shuffles.  Otherwise lane l owns d/32 elements and forms its
+// share of q_h . K[t, g] for every head in fp32.  The
+// chunk's softmax statistics (max, sum of exp) follow in shared memory.
+// Pass 2: the same row mapping over V accumulates sum_t e^(s_t - m) V[t, g]
+// per head; warps are added in order.  A second kernel combines the chunks
+// (log-sum-exp), in chunk order: deterministic.
+#include "qk_formats.cuh"
+#include "qk_internal.h"
+#include "qk_lanes.cuh"
+#include "qk_ptx.cuh"
+
+namespace qk {
+namespace at {
+
+constexpr int kChunk = 256;    // positions per CTA
+constexpr int kWarps = 8;
+constexpr int kMaxG = 8;       // query heads per kv head, at most
+constexpr int kMaxD = 256;     // head dimension, at most (32, 64, 128 or 256)
+
+// Integer code (offset removed) of element e (0..31) of a 32-weight block
+// (in shared memory).
+template <int T>
+__device__ __forceinline__ int code_at(const uint8_t* blk, int e) {
+    if constexpr (T == T_Q8_0) {
+        return (int)(int8_t)blk[2 + e];
+    } else if constexpr (T == T_Q4_0) {
+        return (int)((blk[2 + (e & 15)] >> (4 * (e >> 4))) & 15) - 8;
+    } else {   // Q5_0: nibble plus bit e of the fifth-bit word
+        const uint32_t lo = (blk[6 + (e & 15)] >> (4 * (e >> 4))) & 15;
+        const uint32_t hb = (blk[2 + (e >> 3)] >> (e & 7)) & 1;
+        return (int)(lo | (hb << 4)) - 16;
+    }
+}
+
+// Bytes of one (t, g) row and its shared-memory slot: the aligned-down
+// 16-byte window (start up to 14 bytes early, rows being 2-byte aligned).
+template <int T, int NB> struct Rows {
+    static constexpr int ROWB = NB * Fmt<T>::BB;
+    static constexpr int SLOT = (ROWB + 14 + 15) / 16 * 16;
+    static constexpr int NCH = SLOT / 16;   // 16-byte copies per row
+    static constexpr int SMEM = 2 * kChunk * SLOT;
+};
+
+// 16-byte cp.async that reads only the first n (1..16) bytes of src and
+// zero-fills the rest of the destination.
+__device__ __forceinline__ void cp_async_upto16(uint32_t sdst, const void* src, uint32_t n) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sdst), "l"(src), "r"(n) : "memory");
+}
+
+// Requests the chunk's rows of one cache (K or V) into `slots`.
+template <int T, int NB>
+__device__ __forceinline__ void stage_rows(uint8_t* slots, const uint8_t* C, int64_t t0, int nt, int n_kv, int g,
+                                           int64_t total) {
+    using R = Rows<T, NB>;
+    const uint32_t s0 = smem_u32(slots);
+    for (int idx = threadIdx.x; idx < nt * R::NCH; idx += blockDim.x) {
+        const int j = idx / R::NCH, k = idx - j * R::NCH;
+        const int64_t a = (((t0 + j) * n_kv + g) * (int64_t)R::ROWB & ~(int64_t)15) + 16 * k;
+        if (a < total) cp_async_upto16(s0 + (uint32_t)(j * R::SLOT + 16 * k), C + a, (uint32_t)min((int64_t)16, total - a));
+    }
+}
+
+// Codes of elements e0 .. e0 + 4W - 1 of a 32-weight block (2-byte aligned, in
+// shared memory) as W words of signed bytes with the offset still in (Q4_0 and
+// Q5_0 codes are 0..15 / 0..31); the range never straddles element 16 unless
+// it is the whole block.
+template <int T, int W>
+__device__ __forceinline__ void code_words(const uint8_t* blk, int e0, uint32_t (&cw)[W]) {
+    if constexpr (T == T_Q8_0) {
+        gv::lds_words_a2<W>(blk + 2 + e0, cw);
+    } else {
+        constexpr int QS = T == T_Q5_0 ? 6 : 2;
+        if constexpr (W == 8) {   // the whole block: low nibbles 0..15, high nibbles 16..31
+            uint32_t w[4];
+            gv::lds_words_a2<4>(blk + QS, w);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                cw[i] = w[i] & 0x0F0F0F0Fu;
+                cw[4 + i] = (w[i] >> 4) & 0x0F0F0F0Fu;
+            }
+        } else {
+            const int sh = e0 >= 16 ? 4 : 0;
+            uint32_t w[W];
+            gv::lds_words_a2<W>(blk + QS + (e0 & 15), w);
+#pragma unroll
+            for (int i = 0; i < W; ++i) cw[i] = (w[i] >> sh) & 0x0F0F0F0Fu;
+        }
+        if constexpr (T == T_Q5_0) {
+            const uint32_t qh = ld_u32_a2(blk + 2);
+#pragma unroll
+            for (int i = 0; i < W; ++i) {
+                const uint32_t t = (qh >> (e0 + 4 * i)) & 15u;
+                cw[i] |= ((t * 0x00204081u) & 0x01010101u) << 4;
+            }
+        }
+    }
+}
+
+template <int T, int NB, int GT>   // NB = d / 32; GT = heads per kv head when fixed, 0 when not
+__global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __restrict__ q, const uint8_t* __restrict__ K,
+                                                                const uint8_t* __restrict__ V, int64_t T_len, int n_heads,
+                                                                int n_kv, float scale, float* __restrict__ ws) {
+    using R = Rows<T, NB>;
+    constexpr int D = 32 * NB, BB = Fmt<T>::BB;
+    constexpr int64_t ROWB = R::ROWB;            // bytes of one (t, g) row: d / 32 blocks
+    extern __shared__ __align__(16) uint8_t dyn[];
+    uint8_t* sK = dyn;                           // [kChunk][SLOT] row windows
+    uint8_t* sV = dyn + kChunk * R::SLOT;
+    __shared__ float sq[kMaxG][kMaxD];           // the group's queries
+    __shared__ float ss[kMaxG][kChunk];          // scores, then e^(s - m)
+    __shared__ float sred[kWarps][kMaxG];
+    __shared__ float so[kMaxG][kMaxD];           // partial outputs, warps added in order
+    const int g = blockIdx.x, c = blockIdx.y, G = n_heads / n_kv;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t0 = (int64_t)c * kChunk;
+    const int nt = (int)min((int64_t)kChunk, T_len - t0);
+    const int64_t total = T_len * n_kv * ROWB;   // bytes of each cache
+    pdl_wait_prior();
+    stage_rows<T, NB>(sK, K, t0, nt, n_kv, g, total);
+    cp_async_commit();
+    stage_rows<T, NB>(sV, V, t0, nt, n_kv, g, total);
+    cp_async_commit();
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) sq[i / D][i % D] = q[(int64_t)(g * G + i / D) * D + i % D];
+    __syncthreads();
+    // Lane l: elements e0 .. e0 + NB - 1 of block eb (pass 2, and pass 1 without a fixed group).
+    const int e0 = (lane * NB) & 31, eb = (lane * NB) >> 5;
+    constexpr int GG = GT > 0 ? GT : kMaxG;
+    if constexpr (GT > 0) {
+        constexpr int LPH = 32 / GT, EPL = D / LPH, W = EPL / 4;   // lanes per head, elements per lane
+        static_assert(EPL % 4 == 0 && EPL <= 32, "one lane's elements lie in one block");
+        const int h = lane / LPH, ea = (lane % LPH) * EPL;          // head, first element
+        const int kb = ea >> 5, k0 = ea & 31;
+        // The lane's limbs: block maximum over the 32 / EPL lanes that share the block.
+        float qv[EPL], amax = 0.0f;
+#pragma unroll
+        for (int k = 0; k < EPL; ++k) {
+            qv[k] = sq[h][ea + k];
+            amax = fmaxf(amax, fabsf(qv[k]));
+        }
+#pragma unroll
+        for (int o = 1; o < 32 / EPL; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float sx = amax * (1.0f / gv::kXMax);
+        const float inv = amax > 0.0f ? __fdividef(gv::kXMax, amax) : 0.0f;
+        uint32_t la[W], lb[W], lc[W];
+        int xsum = 0;
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+            uint32_t Y[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int X = __float2int_rn(qv[4 * i + k] * inv);
+                xsum += X;
+                Y[k] = (uint32_t)(X + 0x808080);
+            }
+            la[i] = (((Y[0] >> 16) & 255u) | (((Y[1] >> 16) & 255u) << 8) | (((Y[2] >> 16) & 255u) << 16) |
+                     (((Y[3] >> 16) & 255u) << 24)) ^ 0x80808080u;
+            lb[i] = (((Y[0] >> 8) & 255u) | (((Y[1] >> 8) & 255u) << 8) | (((Y[2] >> 8) & 255u) << 16) |
+                     (((Y[3] >> 8) & 255u) << 24)) ^ 0x80808080u;
+            lc[i] = ((Y[0] & 255u) | ((Y[1] & 255u) << 8) | ((Y[2] & 255u) << 16) | ((Y[3] & 255u) << 24)) ^
+                    0x80808080u;
+        }
+        constexpr float kOff = T == T_Q8_0 ? 0.0f : (T == T_Q5_0 ? 16.0f : 8.0f);
+        const float offx = kOff * (float)xsum;
+        cp_async_wait<1>();   // this thread's K copies
+        __syncthreads();      // ... and everyone's
+        for (int j = warp; j < nt; j += kWarps) {
+            const uint8_t* blk = sK + j * R::SLOT + (int)((((t0 + j) * n_kv + g) * ROWB) & 15) + kb * BB;
+            uint32_t cw[W];
+            code_words<T, W>(blk, k0, cw);
+            int A = 0, B = 0, C = 0;
+#pragma unroll
+            for (int i = 0; i < W; ++i) {
+                A = gv::dp4a_ss(cw[i], la[i], A);
+                B = gv::dp4a_ss(cw[i], lb[i], B);
+                C = gv::dp4a_ss(cw[i], lc[i], C);
+            }
+            float v = h2f(ld_u16(blk)) * (sx * (gv::limbs3_to_f(A, B, C) - offx));
+#pragma unroll
+            for (int o = LPH / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane % LPH == 0) ss[h][j] = scale * v;
+        }
+    } else {
+    float qr[kMaxG][NB];
+#pragma unroll
+    for (int h = 0; h < kMaxG; ++h)
+#pragma unroll
+        for (int k = 0; k < NB; ++k) qr[h][k] = h < G ? sq[h][lane * NB + k] : 0.0f;
+
+    cp_async_wait<1>();   // this thread's K copies
+    __syncthreads();      // ... and everyone's
+    // Pass 1: scores.
+    for (int j = warp; j < nt; j += kWarps) {
+        const uint8_t* blk = sK + j * R::SLOT + (int)((((t0 + j) * n_kv + g) * ROWB) & 15) + eb * BB;
+        const float dk = h2f(blk[0] | ((uint32_t)blk[1] << 8));
+        int cv[NB];
+#pragma unroll
+        for (int k = 0; k < NB; ++k) cv[k] = code_at<T>(blk, e0 + k);
+#pragma unroll
+        for (int h = 0; h < kMaxG; ++h) {
+            if (h >= G) break;
+            float a = 0.0f;
+#pragma unroll
+            for (int k = 0; k < NB; ++k) a = fmaf(qr[h][k], (float)cv[k], a);
+            a *= dk;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+            if (lane == 0) ss[h][j] = scale * a;
+        }
+    }
+    }
+    __syncthreads();
+    // Chunk statistics per head: m = max s, then e^(s - m) and their sum.
+    for (int h = warp; h < G; h += kWarps) {
+        float m = -__int_as_float(0x7f800000);
+        for (int j = lane; j < nt; j += 32) m = fmaxf(m, ss[h][j]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float l = 0.0f;
+        for (int j = lane; j < nt; j += 32) {
+            const float e = expf(ss[h][j] - m);
+            ss[h][j] = e;
+            l += e;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) {
+            sred[0][h] = m;
+            sred[1][h] = l;
+        }
+    }
+    __syncthreads();
+    cp_async_wait<0>();
+    __syncthreads();
+    // Pass 2: sum_t e^(s_t - m) V[t, g], this warp's positions.
+    float acc[GG][NB];
+#pragma unroll
+    for (int h = 0; h < GG; ++h)
+#pragma unroll
+        for (int k = 0; k < NB; ++k) acc[h][k] = 0.0f;
+    for (int j = warp; j < nt; j += kWarps) {
+        const uint8_t* blk = sV + j * R::SLOT + (int)((((t0 + j) * n_kv + g) * ROWB) & 15) + eb * BB;
+        const float dv = h2f(blk[0] | ((uint32_t)blk[1] << 8));
+        float vv[NB];
+#pragma unroll
+        for (int k = 0; k < NB; ++k) vv[k] = dv * (float)code_at<T>(blk, e0 + k);
+#pragma unroll
+        for (int h = 0; h < GG; ++h) {
+            if (GT == 0 && h >= G) break;
+            const float p = ss[h][j];
+#pragma unroll
+            for (int k = 0; k < NB; ++k) acc[h][k] = fmaf(p, vv[k], acc[h][k]);
+        }
+    }
+    for (int w = 0; w < kWarps; ++w) {   // warp 0 writes, the others add, in warp order
+        if (warp == w) {
+#pragma unroll
+            for (int h = 0; h < GG; ++h)
+#pragma unroll
+                for (int k = 0; k < NB; ++k)
+                    if (h < G) so[h][lane * NB + k] = w == 0 ? acc[h][k] : so[h][lane * NB + k] + acc[h][k];
+        }
+        __syncthreads();
+    }
+    // Chunk partial (m, l, o[d]) per head.
+    const int nchunks = gridDim.y;
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+        const int h = i / D, e = i % D;
+        float* dst = ws + ((int64_t)(g * G + h) * nchunks + c) * (D + 2);
+        dst[2 + e] = so[h][e];
+        if (e == 0) {
+            dst[0] = sred[0][h];
+            dst[1] = sred[1][h];
+        }
+    }
+}
+
+// out[h, e] = sum_c e^(m_c - M) o_c[e] / sum_c e^(m_c - M) l_c.  CTA (h, e0)
+// takes head h and elements e0 .. e0 + 31: M by a fixed tree over the chunks,
+// the l-sum by a fixed tree, and each element's o-sum split over 8 chunk
+// groups (chunks c = k mod 8) that are added in group order: deterministic.
+__global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ ws, int nchunks, int D,
+                                                          float* __restrict__ out) {
+    __shared__ float red[256];
+    __shared__ float part[8][32];
+    pdl_wait_prior();
+    const int h = blockIdx.x, tid = threadIdx.x;
+    const int64_t stride = D + 2;
+    const float* base = ws + (int64_t)h * nchunks * stride;
+    float m = -__int_as_float(0x7f800000);
+    for (int c = tid; c < nchunks; c += 256) m = fmaxf(m, base[(int64_t)c * stride]);
+    red[tid] = m;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (tid < o) red[tid] = fmaxf(red[tid], red[tid + o]);
+        __syncthreads();
+    }
+    const float M = red[0];
+    __syncthreads();
+    float l = 0.0f;
+    for (int c = tid; c < nchunks; c += 256) l += expf(base[(int64_t)c * stride] - M) * base[(int64_t)c * stride + 1];
+    red[tid] = l;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (tid < o) red[tid] += red[tid + o];
+        __syncthreads();
+    }
+    const float L = red[0];
+    const int el = tid & 31, cg = tid >> 5, e = blockIdx.y * 32 + el;
+    float acc = 0.0f;
+    if (e < D) {
+#pragma unroll 4
+        for (int c = cg; c < nchunks; c += 8) {
+            const float* p = base + (int64_t)c * stride;
+            acc = fmaf(expf(p[0] - M), p[2 + e], acc);
+        }
+    }
+    part[cg][el] = acc;
+    __syncthreads();
+    if (cg == 0 && e < D) {
+        float o = part[0][el];
+        for (int k = 1; k < 8; ++k) o += part[k][el];
+        out[(int64_t)h * D + e] = o / L;
+    }
+}
+
+template <int T, int NB, int GT>
+cudaError_t launch_tn(const float* q, const uint8_t* K, const uint8_t* V, int64_t T_len, int n_heads, int n_kv,
+                      float scale, float* out, float* ws, cudaStream_t s) {
+    const int64_t nch = (T_len + kChunk - 1) / kChunk;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.stream = s;
+    cfg.gridDim = dim3((unsigned)n_kv, (unsigned)nch);
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = Rows<T, NB>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(attn_chunk_kernel<T, NB, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Rows<T, NB>::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, attn_chunk_kernel<T, NB, GT>, q, K, V, T_len, n_heads, n_kv, scale, ws);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3((unsigned)n_heads, (unsigned)((32 * NB + 31) / 32));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, attn_combine_kernel, (const float*)ws, (int)nch, 32 * NB, out);
+}
+
+// The fixed-group kernel where a lane's G d/32 elements make whole words
+// inside one block, the runtime-group one otherwise.
+template <int T, int NB>
+cudaError_t launch_g(const float* q, const uint8_t* K, const uint8_t* V, int64_t T_len, int n_heads, int n_kv,
+                     float scale, float* out, float* ws, cudaStream_t s) {
+    const int G = n_heads / n_kv;
+    if constexpr (NB <= 4) {
+        if (G == 8 && 8 * NB <= 32) return launch_tn<T, NB, 8>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, s);
+    }
+    if constexpr (NB >= 1 && NB <= 8) {
+        if (G == 4 && 4 * NB >= 4 && 4 * NB <= 32) return launch_tn<T, NB, 4>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, s);
+    }
+    if constexpr (NB >= 2) {
+        if (G == 2 && 2 * NB <= 32) return launch_tn<T, NB, 2>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, s);
+    }
+    if constexpr (NB >= 4) {
+        if (G == 1) return launch_tn<T, NB, 1>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, s);
+    }
+    return launch_tn<T, NB, 0>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, s);
+}
+
+template <int T>
+cudaError_t launch_t(const float* q, const uint8_t* K, const uint8_t* V, int64_t T_len, int n_heads, int n_kv, int d,
+                     float scale, float* out, float* ws, cudaStream_t s) {
+    switch (d) {
+    case 32: return launch_g<T, 1>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, s);
+    case 64: return launch_g<T, 2>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, s);
+    case 128: return launch_g<T, 4>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, s);
+    case 256: return launch_g<T, 8>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace at
+
+int64_t attn_decode_ws_bytes(int64_t T_len, int n_heads, int d) {
+    const int64_t nch = (T_len + at::kChunk - 1) / at::kChunk;
+    return nch * n_heads * (int64_t)(d + 2) * (int64_t)sizeof(float);
+}
+
+bool attn_decode_shape_ok(int n_heads, int n_kv, int d) {
+    return n_kv > 0 && n_heads % n_kv == 0 && n_heads / n_kv <= at::kMaxG && (d == 32 || d == 64 || d == 128 || d == 256);
+}
+
+cudaError_t launch_attn_decode(int type, const float* q, const uint8_t* K, const uint8_t* V, int64_t T_len, int n_heads,
+                               int n_kv, int d, float scale, float* out, float* ws, cudaStream_t s) {
+    switch (type) {
+    case T_Q8_0: return at::launch_t<T_Q8_0>(q, K, V, T_len, n_heads, n_kv, d, scale, out, ws, s);
+    case T_Q5_0: return at::launch_t<T_Q5_0>(q, K, V, T_len, n_heads, n_kv, d, scale, out, ws, s);
+    case T_Q4_0: return at::launch_t<T_Q4_0>(q, K, V, T_len, n_heads, n_kv, d, scale, out, ws, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace qk

@@ -150,6 +150,30 @@ qk_status qk_dequant(int type, const void* W, int64_t rows, int64_t cols,
  * multiple of the block size, negative sizes), QK_ERR_NULL, QK_ERR_ALIGN. */
 qk_status qk_quantize(int type, const float* w, int64_t rows, int64_t cols, void* out, void* stream);
 
+/* Decode attention over a block-quantized KV cache ("Hitchhiker's Guide --
+ * Lab 01", 13.2: K and V cached as q8_0, or q4_0 at a quality cost, and read
+ * inside attention; grouped-query attention shares each kv head among
+ * n_heads / n_kv query heads).  One query token:
+ *   s_t = scale * sum_i q[h, i] K[t, g, i],  g = h / (n_heads / n_kv),
+ *   p = softmax(s) over t = 0 .. T-1,  out[h, i] = sum_t p_t V[t, g, i].
+ *   type   QK_Q8_0, QK_Q5_0 or QK_Q4_0 (the cache's block type).
+ *   q      fp32 [n_heads, d], device, 4-byte aligned.
+ *   K, V   [T, n_kv, d]: each (t, g) row is d / 32 blocks (so a cache row
+ *          of all kv heads is qk_row_bytes(type, n_kv * d) bytes, written by
+ *          qk_quantize from fp32 [T, n_kv * d]); device, 16-byte aligned.
+ *   d      32, 64, 128 or 256; n_heads a multiple of n_kv, at most 8 query
+ *          heads per kv head; 1 <= T <= 65535 * 256.
+ *   out    fp32 [n_heads, d]; ws at least qk_attn_decode_workspace bytes.
+ * Positions are split in chunks of 256 (one CTA per kv head and chunk, the
+ * cache streamed once); each chunk keeps its max score, sum of exponentials
+ * and weighted value sum, and a second launch combines the chunks
+ * (log-sum-exp) in chunk order: deterministic.  fp32 arithmetic.
+ * Errors: QK_ERR_TYPE, QK_ERR_SHAPE, QK_ERR_NULL, QK_ERR_ALIGN,
+ * QK_ERR_WORKSPACE. */
+size_t qk_attn_decode_workspace(int type, int64_t T, int n_heads, int n_kv, int d);
+qk_status qk_attn_decode(int type, const float* q, const void* K, const void* V, int64_t T, int n_heads, int n_kv, int d,
+                         float scale, float* out, void* ws, size_t ws_bytes, void* stream);
+
 /* Importance-weighted quantization ("Hitchhiker's Guide -- Lab 01", 11.3,
  * the importance matrix: minimise sum_i E[x_i^2] (w_i - w^_i)^2 rather than
  * the plain weight-space error).  imp[c] is the mean squared activation met

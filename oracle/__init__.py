@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
             L.oq_pack.argtypes = [ctypes.c_int, _i64, _p, _p, _p, _p, _p, _p]
             L.oq_quantize.argtypes = [ctypes.c_int, _p, _i64, _i64, _p]
             L.oq_quantize_imatrix.argtypes = [ctypes.c_int, _p, _i64, _i64, _p, _p]
+            L.oq_attn_decode.argtypes = [ctypes.c_int, _p, _p, _p, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_float, _p, _p]
             _lib = L
     return _lib
 
@@ -246,3 +248,19 @@ def quantize_imatrix(t: int, w: np.ndarray, imp: np.ndarray) -> np.ndarray:
     out = np.zeros(rows * row_bytes(t, cols), np.uint8)
     _check(lib().oq_quantize_imatrix(t, _ptr(w), rows, cols, _ptr(imp), _ptr(out)), "quantize_imatrix")
     return out
+
+
+def attn_decode(t: int, q: np.ndarray, K: np.ndarray, V: np.ndarray, T: int, n_heads: int, n_kv: int, d: int,
+                scale: float):
+    """Decode attention over a block-quantized KV cache (oq_attn_decode):
+    q fp32 [n_heads, d]; K, V packed [T, n_kv, d] rows of 32-weight blocks.
+    Returns (out fp64 [n_heads, d], Sv fp64 [n_heads, d])."""
+    q = np.ascontiguousarray(q, dtype=np.float32).reshape(n_heads, d)
+    K = np.ascontiguousarray(K, dtype=np.uint8)
+    V = np.ascontiguousarray(V, dtype=np.uint8)
+    assert K.size >= T * n_kv * row_bytes(t, d) and V.size >= T * n_kv * row_bytes(t, d)
+    out = np.zeros((n_heads, d), np.float64)
+    Sv = np.zeros((n_heads, d), np.float64)
+    _check(lib().oq_attn_decode(t, _ptr(q), _ptr(K), _ptr(V), T, n_heads, n_kv, d, scale, _ptr(out), _ptr(Sv)),
+           "attn_decode")
+    return out, Sv

@@ -1060,3 +1060,62 @@ int oq_quantize_imatrix(int type, const float* w, int64_t rows, int64_t cols, co
         }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention over a block-quantized KV cache                          */
+/* ------------------------------------------------------------------------ */
+
+/* [HG] 13.2 (KV-cache quantization at serve time): keys and values are
+ * stored as q8_0 (or q4_0) blocks and read inside attention.  One query
+ * token: for query head h (kv head g = h / (n_heads / n_kv), grouped-query
+ * attention as the page describes), s_t = scale * sum_i q[h,i] K[t,g,i],
+ * p = softmax(s) over t = 0..T-1, out[h,i] = sum_t p_t V[t,g,i].  K and V are
+ * [T, n_kv, d] with each (t, g) row d/32 blocks of a 32-weight type; the
+ * oracle dequantizes them exactly and does the rest in fp64 (softmax with the
+ * maximum subtracted).  Sv[h,i] = sum_t p_t |V[t,g,i]| is returned for the
+ * tolerance. */
+int oq_attn_decode(int type, const float* q, const uint8_t* K, const uint8_t* V, int64_t T, int n_heads,
+                   int n_kv, int d, float scale, double* out, double* Sv) {
+    if (oq_block_elems(type) != 32 || d % 32 != 0 || n_kv <= 0 || n_heads % n_kv != 0 || T < 1) return -2;
+    int bb = oq_block_bytes(type);
+    int64_t rowb = (int64_t)(d / 32) * bb;
+    int grp = n_heads / n_kv;
+    float* k = (float*)malloc(sizeof(float) * (size_t)d);
+    float* v = (float*)malloc(sizeof(float) * (size_t)d);
+    double* s = (double*)malloc(sizeof(double) * (size_t)T);
+    if (!k || !v || !s) { free(k); free(v); free(s); return -3; }
+    for (int h = 0; h < n_heads; h++) {
+        int g = h / grp;
+        double mx = -INFINITY;
+        for (int64_t t = 0; t < T; t++) {
+            const uint8_t* row = K + (t * n_kv + g) * rowb;
+            for (int b = 0; b < d / 32; b++) dequant_block(type, row + b * bb, k + 32 * b);
+            double acc = 0.0;
+            for (int i = 0; i < d; i++) acc += (double)q[(int64_t)h * d + i] * (double)k[i];
+            s[t] = (double)scale * acc;
+            if (s[t] > mx) mx = s[t];
+        }
+        double l = 0.0;
+        for (int64_t t = 0; t < T; t++) {
+            s[t] = exp(s[t] - mx);
+            l += s[t];
+        }
+        for (int i = 0; i < d; i++) {
+            out[(int64_t)h * d + i] = 0.0;
+            Sv[(int64_t)h * d + i] = 0.0;
+        }
+        for (int64_t t = 0; t < T; t++) {
+            const uint8_t* row = V + (t * n_kv + g) * rowb;
+            for (int b = 0; b < d / 32; b++) dequant_block(type, row + b * bb, v + 32 * b);
+            double p = s[t] / l;
+            for (int i = 0; i < d; i++) {
+                out[(int64_t)h * d + i] += p * (double)v[i];
+                Sv[(int64_t)h * d + i] += p * fabs((double)v[i]);
+            }
+        }
+    }
+    free(k);
+    free(v);
+    free(s);
+    return 0;
+}

@@ -1,0 +1,94 @@
+"""qk_attn_decode (decode attention over a Q8_0 / Q5_0 / Q4_0 KV cache)
+against the oracle on the same blocks: |out - ref| <= 2e-4 * sum_t p_t |V| +
+1e-6 per output.  Shapes cover one position, a ragged last chunk, several
+chunks, grouped-query heads (1, 4 and 8 query heads per kv head) and head
+dimensions 32 to 256; a long cache is checked on sampled heads."""
+import numpy as np
+import pytest
+import torch
+
+import gguf_quant_dequant_gb300 as qk
+import oracle
+import synth
+from gpu_helpers import dev_u8, gpu, type_id  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+
+RTOL = 2e-4
+
+
+def run(gpu, name, Tn, nh, nkv, d, seed, scale=None):
+    t = type_id(name)
+    K = synth.random_blocks(name, Tn * nkv, d, seed)
+    V = synth.random_blocks(name, Tn * nkv, d, seed + 1)
+    q = synth.activations(nh, d, seed + 2)
+    scale = scale if scale is not None else 1.0 / np.sqrt(d)
+    out = qk.attn_decode(t, torch.from_numpy(q).to(gpu), dev_u8(K, gpu), dev_u8(V, gpu), Tn, nh, nkv, d, scale)
+    qk.device_status()
+    ref, Sv = oracle.attn_decode(t, q, K, V, Tn, nh, nkv, d, scale)
+    return out.cpu().numpy(), ref, Sv
+
+
+CASES = [
+    ("Q8_0", 1, 4, 4, 128),
+    ("Q8_0", 300, 32, 8, 128),     # a ragged second chunk, 4 heads per kv head
+    ("Q8_0", 1000, 8, 1, 64),      # 8 heads per kv head
+    ("Q4_0", 777, 16, 4, 128),
+    ("Q5_0", 513, 8, 8, 32),
+    ("Q8_0", 260, 4, 2, 256),
+]
+
+
+@pytest.mark.parametrize("name,Tn,nh,nkv,d", CASES)
+def test_attn_decode_parity(gpu, name, Tn, nh, nkv, d):
+    out, ref, Sv = run(gpu, name, Tn, nh, nkv, d, 800 + Tn + d)
+    err = np.abs(out - ref) - (RTOL * Sv + 1e-6)
+    assert (err <= 0).all(), f"{name} T={Tn}: worst excess {err.max():.3e}"
+
+
+def test_attn_decode_peaked_scores(gpu):
+    # A large scale makes the softmax nearly one-hot: the chunk maxima and
+    # the log-sum-exp combination carry the result.
+    out, ref, Sv = run(gpu, "Q8_0", 1500, 8, 2, 128, 900, scale=3.0)
+    assert (np.abs(out - ref) <= RTOL * Sv + 1e-6).all()
+
+
+def test_attn_decode_long_cache_sampled_heads(gpu):
+    # 32k positions, Llama-3-8B-like heads (32 query, 8 kv, d = 128): every
+    # output of two sampled kv heads against the oracle on those heads' rows.
+    t, Tn, nh, nkv, d = qk.Q8_0, 32768, 32, 8, 128
+    K = synth.random_blocks_torch("Q8_0", Tn * nkv, d, 950, gpu)
+    V = synth.random_blocks_torch("Q8_0", Tn * nkv, d, 951, gpu)
+    g = torch.Generator(device=gpu)
+    g.manual_seed(952)
+    q = torch.randn((nh, d), device=gpu, generator=g)
+    out = qk.attn_decode(t, q, K, V, Tn, nh, nkv, d, 1.0 / np.sqrt(d)).cpu().numpy()
+    qk.device_status()
+    rb = qk.row_bytes(t, d)
+    grp = nh // nkv
+    for kv in (0, 5):
+        rows = torch.arange(Tn, device=gpu) * nkv + kv
+        idx = (rows[:, None] * rb + torch.arange(rb, device=gpu)[None, :]).reshape(-1)
+        Kh, Vh = K[idx].cpu().numpy(), V[idx].cpu().numpy()
+        qh = q[kv * grp:(kv + 1) * grp].cpu().numpy()
+        ref, Sv = oracle.attn_decode(t, qh, Kh, Vh, Tn, grp, 1, d, 1.0 / np.sqrt(d))
+        got = out[kv * grp:(kv + 1) * grp]
+        assert (np.abs(got - ref) <= RTOL * Sv + 1e-6).all(), f"kv head {kv}"
+
+
+def test_attn_decode_deterministic(gpu):
+    a, _, _ = run(gpu, "Q4_0", 2000, 16, 4, 128, 990)
+    b, _, _ = run(gpu, "Q4_0", 2000, 16, 4, 128, 990)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("name,Tn,nh,nkv,d", [
+    ("Q4_0", 400, 8, 8, 128),    # one head per kv head
+    ("Q5_0", 350, 16, 8, 64),    # two heads per kv head
+    ("Q8_0", 290, 8, 1, 32),     # eight heads, d = 32 (whole blocks per lane)
+    ("Q5_0", 700, 32, 4, 256),   # eight heads, d = 256: the runtime-group path
+    ("Q4_0", 100, 2, 1, 32),     # two heads, d = 32: the runtime-group path
+])
+def test_attn_decode_every_group_path(gpu, name, Tn, nh, nkv, d):
+    out, ref, Sv = run(gpu, name, Tn, nh, nkv, d, 1100 + Tn + d)
+    assert (np.abs(out - ref) <= RTOL * Sv + 1e-6).all()

@@ -161,3 +161,35 @@ def test_binding_refuses_to_run_without_library(monkeypatch, tmp_path):
     with pytest.raises(RuntimeError):
         mod.load()
     importlib.reload(qk)
+
+
+def test_new_block_type_sizes(lib):
+    assert [qk.block_bytes(t) for t in (6, 7, 8)] == [176, 84, 110]
+    assert [qk.block_elems(t) for t in (6, 7, 8)] == [256, 256, 256]
+    assert qk.row_bytes(qk.Q5_K, 4096) == 2816 and qk.row_bytes(qk.Q2_K, 4096) == 1344
+    assert qk.row_bytes(qk.Q3_K, 4096) == 1760
+
+
+def test_imatrix_and_attention_argument_errors_are_caught_on_host(lib):
+    fake = ctypes.c_void_p(0x10000)
+    odd1 = ctypes.c_void_p(0x10001)
+    odd2 = ctypes.c_void_p(0x10002)
+    f = ctypes.c_float
+    assert lib.qk_quantize_imatrix(0, fake, 4, 256, fake, fake, None) == 1
+    assert lib.qk_quantize_imatrix(qk.Q4_K, fake, 4, 100, fake, fake, None) == 2
+    assert lib.qk_quantize_imatrix(qk.Q4_K, fake, 4, 256, None, fake, None) == 4
+    assert lib.qk_quantize_imatrix(qk.Q4_K, odd2, 4, 256, fake, fake, None) == 3
+    assert lib.qk_quantize_imatrix(qk.Q4_K, fake, 0, 256, None, None, None) == 0
+    ws = qk.attn_decode_workspace(qk.Q8_0, 300, 32, 8, 128)
+    assert ws == 2 * 32 * 130 * 4   # two chunks x heads x (d + 2) floats
+    assert qk.attn_decode_workspace(qk.Q4_K, 300, 32, 8, 128) == 0
+    call = lib.qk_attn_decode
+    assert call(qk.Q4_K, fake, fake, fake, 300, 32, 8, 128, f(0.1), fake, fake, ws, None) == 1
+    assert call(qk.Q8_0, fake, fake, fake, 300, 32, 8, 96, f(0.1), fake, fake, ws, None) == 2     # d
+    assert call(qk.Q8_0, fake, fake, fake, 300, 30, 8, 128, f(0.1), fake, fake, ws, None) == 2    # groups
+    assert call(qk.Q8_0, fake, fake, fake, 300, 32, 2, 128, f(0.1), fake, fake, ws, None) == 2    # 16 per kv
+    assert call(qk.Q8_0, fake, fake, fake, 0, 32, 8, 128, f(0.1), fake, fake, ws, None) == 2      # T
+    assert call(qk.Q8_0, None, fake, fake, 300, 32, 8, 128, f(0.1), fake, fake, ws, None) == 4
+    assert call(qk.Q8_0, fake, odd1, fake, 300, 32, 8, 128, f(0.1), fake, fake, ws, None) == 3
+    assert call(qk.Q8_0, fake, fake, odd2, 300, 32, 8, 128, f(0.1), fake, fake, ws, None) == 3
+    assert call(qk.Q8_0, fake, fake, fake, 300, 32, 8, 128, f(0.1), fake, fake, ws - 4, None) == 5

@@ -630,3 +630,55 @@ def test_imatrix_protects_the_important_column(oracle_mod):
         ep = np.abs(dp - w)[:, 5::32]
         ei = np.abs(di - w)[:, 5::32]
         assert ei.mean() < 0.25 * ep.mean()
+
+
+# ------------------------------------------- attention over a quantized KV cache --
+# "Hitchhiker's Guide -- Lab 01", 13.2: q8_0 / q4_0 K and V read inside attention.
+
+def _kv(name, T, nkv, d, seed):
+    return (synth.random_blocks(name, T * nkv, d, seed), synth.random_blocks(name, T * nkv, d, seed + 1))
+
+
+@pytest.mark.parametrize("name", ["Q8_0", "Q4_0", "Q5_0"])
+def test_attn_matches_torch_sdpa(oracle_mod, name):
+    # torch's scaled_dot_product_attention in fp64 on the dequantized caches
+    # (an independent library routine), grouped-query heads expanded by hand.
+    t = T[name]
+    Tn, nh, nkv, d = 37, 8, 2, 64
+    K, V = _kv(name, Tn, nkv, d, 700)
+    q = synth.activations(nh, d, 702)
+    out, _ = oracle_mod.attn_decode(t, q, K, V, Tn, nh, nkv, d, 0.125)
+    Kd = torch.from_numpy(oracle_mod.dequant(t, K, Tn * nkv, d).reshape(Tn, nkv, d)).double()
+    Vd = torch.from_numpy(oracle_mod.dequant(t, V, Tn * nkv, d).reshape(Tn, nkv, d)).double()
+    grp = nh // nkv
+    k = Kd.permute(1, 0, 2).repeat_interleave(grp, dim=0)     # [nh, T, d]
+    v = Vd.permute(1, 0, 2).repeat_interleave(grp, dim=0)
+    qq = torch.from_numpy(q).double().unsqueeze(1)             # [nh, 1, d]
+    ref = torch.nn.functional.scaled_dot_product_attention(qq, k, v, scale=0.125).squeeze(1).numpy()
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_attn_special_cases(oracle_mod):
+    t, d, nkv = T["Q8_0"], 32, 1
+    # One position: the output is that position's value row, exactly.
+    K, V = _kv("Q8_0", 1, nkv, d, 710)
+    q = synth.activations(2, d, 711)
+    out, Sv = oracle_mod.attn_decode(t, q, K, V, 1, 2, nkv, d, 1.0)
+    v0 = oracle_mod.dequant(t, V, 1, d)[0].astype(np.float64)
+    assert np.array_equal(out[0], v0) and np.array_equal(out[1], v0)
+    assert np.array_equal(Sv[0], np.abs(v0))
+    # Identical keys: uniform attention, the output is the mean value row.
+    Tn = 9
+    K1, V9 = _kv("Q8_0", Tn, nkv, d, 712)
+    K9 = np.tile(K1.reshape(Tn, -1)[:1], (Tn, 1)).reshape(-1)
+    out, _ = oracle_mod.attn_decode(t, q, K9, V9, Tn, 2, nkv, d, 0.5)
+    mean = oracle_mod.dequant(t, V9, Tn, d).astype(np.float64).mean(axis=0)
+    assert np.allclose(out, mean[None, :], rtol=1e-13, atol=1e-13)
+    # Grouped heads: equal queries in one group give equal outputs; the
+    # other group reads other rows.
+    Tn, nh, nkv = 11, 4, 2
+    K, V = _kv("Q8_0", Tn, nkv, d, 713)
+    q = np.tile(synth.activations(1, d, 714), (nh, 1))
+    out, _ = oracle_mod.attn_decode(t, q, K, V, Tn, nh, nkv, d, 0.3)
+    assert np.array_equal(out[0], out[1]) and np.array_equal(out[2], out[3])
+    assert not np.array_equal(out[0], out[2])
