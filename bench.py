@@ -87,7 +87,7 @@ def recorded_traffic():
 TRAFFIC_COMMAND = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
                    "--clock-control none -k regex:gemv5 -s 32 -c 12 --csv --log-file traffic.csv "
                    "python bench.py --steps 20 --warmup 3 --min-warmup-s 0 --no-cpu --no-gemm --no-stack "
-                   "--no-sweep --no-quant --no-swiglu")
+                   "--no-sweep --no-quant --no-swiglu --no-attn")
 
 
 def record_traffic(csv_path: str) -> dict:
@@ -337,6 +337,7 @@ def run_gpu(args):
             pass
     quant = run_quantize(dev, hbm_peak) if (rank == 0 and not args.no_quant) else None
     swi = run_swiglu(dev, hbm_peak) if (rank == 0 and not args.no_swiglu) else None
+    attn = run_attn(dev, hbm_peak) if (rank == 0 and not args.no_attn) else None
     cpu = cpu_baseline(layer) if (rank == 0 and world == 1 and not args.no_cpu) else None
     traffic = recorded_traffic()
     if rank == 0:
@@ -369,6 +370,7 @@ def run_gpu(args):
             "ffn_sweep": sweep,
             "quantize": quant,
             "swiglu": swi,
+            "kv_attention": attn,
         }
         print(json.dumps(out))
     if world > 1:
@@ -512,6 +514,40 @@ def run_swiglu(dev, hbm_peak=None):
             out[label]["fused_frac_of_hbm"] = round(nbytes / (us_f * 1e-6) / 1e9 / hbm_peak, 4)
         del Wg, Wu
     return {"workload": "decode SwiGLU gate, Q4_K, batch 1", "per_shape": out}
+
+
+def run_attn(dev, hbm_peak=None):
+    """Decode attention over a quantized KV cache (qk_attn_decode): Llama-3-8B
+    heads (32 query, 8 kv, d = 128) at 32k positions, one query token, the
+    cache in Q8_0 and in Q4_0.  Three cache copies rotate (beyond L2), timed
+    as a CUDA graph.  GB/s counts the K and V bytes (the queries and output
+    are a few KB)."""
+    import torch
+    import gguf_quant_dequant_gb300 as qk
+    import synth
+    Tn, nh, nkv, d = 32768, 32, 8, 128
+    out = {}
+    for name in ("Q8_0", "Q4_0"):
+        t = synth.TYPE_IDS[name]
+        nc = 3
+        Ks = [synth.random_blocks_torch(name, Tn * nkv, d, 9300 + k, dev) for k in range(nc)]
+        Vs = [synth.random_blocks_torch(name, Tn * nkv, d, 9400 + k, dev) for k in range(nc)]
+        q = torch.randn((nh, d), device=dev)
+        o = torch.empty((nh, d), device=dev)
+        ws = torch.empty(qk.attn_decode_workspace(t, Tn, nh, nkv, d), dtype=torch.uint8, device=dev)
+
+        def step():
+            for k in range(nc):
+                qk.attn_decode(t, q, Ks[k], Vs[k], Tn, nh, nkv, d, 1.0 / d ** 0.5, out=o, ws=ws)
+
+        us = _graph_time_us(step) / nc
+        nbytes = 2 * Ks[0].numel()
+        out[name] = {"us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "kv_bytes": nbytes}
+        if hbm_peak:
+            out[name]["frac_of_hbm"] = round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 4)
+        del Ks, Vs
+    return {"workload": "decode attention, 32 query / 8 kv heads, d = 128, 32768 cached positions",
+            "per_cache_type": out}
 
 
 def run_quantize(dev, hbm_peak=None, reps: int = 20):
@@ -879,6 +915,7 @@ def main():
     ap.add_argument("--record-traffic", metavar="CSV",
                     help="write the decode kernel's DRAM-traffic record from the launch list of its ncu command")
     ap.add_argument("--no-swiglu", action="store_true", help="skip the fused SwiGLU leg")
+    ap.add_argument("--no-attn", action="store_true", help="skip the quantized-KV attention leg")
     ap.add_argument("--swiglu-only", action="store_true",
                     help="run only the fused SwiGLU leg and print its JSON (for profiling)")
     ap.add_argument("--quantize-only", action="store_true",
