@@ -916,6 +916,7 @@ def main():
                     help="write the decode kernel's DRAM-traffic record from the launch list of its ncu command")
     ap.add_argument("--no-swiglu", action="store_true", help="skip the fused SwiGLU leg")
     ap.add_argument("--no-attn", action="store_true", help="skip the quantized-KV attention leg")
+    ap.add_argument("--attn-only", action="store_true", help="run the quantized-KV attention leg alone")
     ap.add_argument("--swiglu-only", action="store_true",
                     help="run only the fused SwiGLU leg and print its JSON (for profiling)")
     ap.add_argument("--quantize-only", action="store_true",
@@ -932,7 +933,7 @@ def main():
         return
     if args.impl == "reference":
         run_reference(args)
-    elif args.gemm_only or args.ffn_gemm > 0 or args.quantize_only or args.swiglu_only:
+    elif args.gemm_only or args.ffn_gemm > 0 or args.quantize_only or args.swiglu_only or args.attn_only:
         import torch
         from gguf_quant_dequant_gb300 import build as qkbuild
         qkbuild.build()
@@ -940,6 +941,8 @@ def main():
         torch.cuda.set_device(dev)
         if args.swiglu_only:
             print(json.dumps(run_swiglu(dev)))
+        elif args.attn_only:
+            print(json.dumps(run_attn(dev)))
         elif args.quantize_only:
             print(json.dumps(run_quantize(dev, reps=args.steps)))
         elif args.ffn_gemm > 0:
