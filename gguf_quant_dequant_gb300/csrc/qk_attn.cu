@@ -9,7 +9,10 @@
 // type (Q8_0, Q5_0, Q4_0), decoded in the dot products.
 //
 // Split over positions (the cache is streamed once per token, so the work is
-// HBM-bound): CTA (g, c) takes kv head g and positions [256c, 256c + 256).
+// HBM-bound): CTA c n_kv + g takes kv head g and positions [CH c, CH c + CH).
+// The chunk CH is set per cache type: a smaller chunk lowers the shared
+// memory per CTA, so more CTAs share an SM and hide each other's latency,
+// but repeats the per-CTA work (query limbs, softmax, warp sums) more often.
 // All its K rows and then all its V rows are requested at once with 16-byte
 // cp.async copies into shared memory (each row's aligned-down window; the
 // copy that reaches the end of the cache takes only the bytes that exist),
@@ -35,10 +38,13 @@
 namespace qk {
 namespace at {
 
-constexpr int kChunk = 256;    // positions per CTA
+constexpr int kMinChunk = 128;   // positions per CTA, at least (the workspace is sized for it)
+// Measured on 32k positions, 32 / 8 heads, d = 128: Q8_0 58.8 / 56.1 / 60.9 us
+// at 128 / 192 / 256 positions, Q5_0 59.5 / 60.9 us at 192 / 256, Q4_0
+// 52.0 / 50.6 us at 192 / 256.
+template <int T> constexpr int chunk_of() { return T == T_Q4_0 ? 256 : 192; }
 constexpr int kWarps = 8;
 constexpr int kMaxG = 8;       // query heads per kv head, at most
-constexpr int kMaxD = 256;     // head dimension, at most (32, 64, 128 or 256)
 
 // Integer code (offset removed) of element e (0..31) of a 32-weight block
 // (in shared memory).
@@ -56,12 +62,16 @@ __device__ __forceinline__ int code_at(const uint8_t* blk, int e) {
 }
 
 // Bytes of one (t, g) row and its shared-memory slot: the aligned-down
-// 16-byte window (start up to 14 bytes early, rows being 2-byte aligned).
-template <int T, int NB> struct Rows {
+// 16-byte window.  Rows start at multiples of ROWB from a 16-byte aligned
+// cache, so a window starts at most 16 - gcd(ROWB, 16) bytes before its row.
+// The 16 bytes past the last slot keep the word loads that read one word
+// ahead inside the allocation.
+template <int T, int NB, int CH> struct Rows {
     static constexpr int ROWB = NB * Fmt<T>::BB;
-    static constexpr int SLOT = (ROWB + 14 + 15) / 16 * 16;
+    static constexpr int ALIGN = (ROWB & 15) == 0 ? 16 : ((ROWB & 7) == 0 ? 8 : ((ROWB & 3) == 0 ? 4 : 2));
+    static constexpr int SLOT = (ROWB + 16 - ALIGN + 15) / 16 * 16;
     static constexpr int NCH = SLOT / 16;   // 16-byte copies per row
-    static constexpr int SMEM = 2 * kChunk * SLOT;
+    static constexpr int SMEM = 2 * CH * SLOT + 16;
 };
 
 // 16-byte cp.async that reads only the first n (1..16) bytes of src and
@@ -71,10 +81,10 @@ __device__ __forceinline__ void cp_async_upto16(uint32_t sdst, const void* src, 
 }
 
 // Requests the chunk's rows of one cache (K or V) into `slots`.
-template <int T, int NB>
+template <int T, int NB, int CH>
 __device__ __forceinline__ void stage_rows(uint8_t* slots, const uint8_t* C, int64_t t0, int nt, int n_kv, int g,
                                            int64_t total) {
-    using R = Rows<T, NB>;
+    using R = Rows<T, NB, CH>;
     const uint32_t s0 = smem_u32(slots);
     for (int idx = threadIdx.x; idx < nt * R::NCH; idx += blockDim.x) {
         const int j = idx / R::NCH, k = idx - j * R::NCH;
@@ -83,71 +93,119 @@ __device__ __forceinline__ void stage_rows(uint8_t* slots, const uint8_t* C, int
     }
 }
 
-// Codes of elements e0 .. e0 + 4W - 1 of a 32-weight block (2-byte aligned, in
-// shared memory) as W words of signed bytes with the offset still in (Q4_0 and
-// Q5_0 codes are 0..15 / 0..31); the range never straddles element 16 unless
-// it is the whole block.
-template <int T, int W>
-__device__ __forceinline__ void code_words(const uint8_t* blk, int e0, uint32_t (&cw)[W]) {
-    if constexpr (T == T_Q8_0) {
-        gv::lds_words_a2<W>(blk + 2 + e0, cw);
-    } else {
-        constexpr int QS = T == T_Q5_0 ? 6 : 2;
-        if constexpr (W == 8) {   // the whole block: low nibbles 0..15, high nibbles 16..31
-            uint32_t w[4];
-            gv::lds_words_a2<4>(blk + QS, w);
+// N words from a 2-byte aligned address in shared memory, for a lane whose
+// address moves by multiples of 16 bytes from position to position: the
+// aligned word address and the funnel shift are fixed once.  (The word
+// address is reached by pointer arithmetic, so the loads stay shared-space
+// loads.)
+template <int N> struct Run {
+    const uint8_t* a;
+    uint32_t sh;
+    __device__ __forceinline__ explicit Run(const uint8_t* p) {
+        const uint32_t m = (uint32_t)reinterpret_cast<uintptr_t>(p) & 3u;
+        a = p - m;
+        sh = 8u * m;
+    }
+    __device__ __forceinline__ void load(uint32_t off, uint32_t (&w)[N]) const {
+        const uint32_t* q = reinterpret_cast<const uint32_t*>(a + off);
+        uint32_t prev = q[0];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                cw[i] = w[i] & 0x0F0F0F0Fu;
-                cw[4 + i] = (w[i] >> 4) & 0x0F0F0F0Fu;
-            }
-        } else {
-            const int sh = e0 >= 16 ? 4 : 0;
-            uint32_t w[W];
-            gv::lds_words_a2<W>(blk + QS + (e0 & 15), w);
-#pragma unroll
-            for (int i = 0; i < W; ++i) cw[i] = (w[i] >> sh) & 0x0F0F0F0Fu;
+        for (int i = 0; i < N; ++i) {
+            const uint32_t next = q[i + 1];
+            w[i] = __funnelshift_r(prev, next, sh);
+            prev = next;
         }
-        if constexpr (T == T_Q5_0) {
-            const uint32_t qh = ld_u32_a2(blk + 2);
+    }
+};
+__device__ __forceinline__ uint32_t lds16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
+
+// The codes of elements e0 .. e0 + 4W - 1 of a 32-weight block in shared
+// memory at blk (+ the position's offset) as W words of bytes, the offset
+// still in (Q4_0 and Q5_0 codes are 0..15 / 0..31).  The range never
+// straddles element 16 unless it is the whole block.
+template <int T, int W> struct Codes {
+    static constexpr bool kWhole = T != T_Q8_0 && W == 8;   // the whole block of a nibble type
+    static constexpr int QS = T == T_Q8_0 ? 2 : (T == T_Q5_0 ? 6 : 2);
+    Run<kWhole ? 4 : W> run;
+    Run<1> qh;
+    uint32_t nsh;
+    int e0;
+    __device__ __forceinline__ Codes(const uint8_t* blk, int e0_)
+        : run(kWhole || T == T_Q8_0 ? blk + QS + (kWhole ? 0 : e0_) : blk + QS + (e0_ & 15)),
+          qh(blk + 2), nsh(e0_ >= 16 ? 4u : 0u), e0(e0_) {}
+    __device__ __forceinline__ void load(uint32_t off, uint32_t (&cw)[W]) const {
+        if constexpr (T == T_Q8_0) {
+            run.load(off, cw);
+        } else {
+            if constexpr (kWhole) {
+                uint32_t w[4];
+                run.load(off, w);
 #pragma unroll
-            for (int i = 0; i < W; ++i) {
-                const uint32_t t = (qh >> (e0 + 4 * i)) & 15u;
-                cw[i] |= ((t * 0x00204081u) & 0x01010101u) << 4;
+                for (int i = 0; i < 4; ++i) {
+                    cw[i] = w[i] & 0x0F0F0F0Fu;
+                    cw[4 + i] = (w[i] >> 4) & 0x0F0F0F0Fu;
+                }
+            } else {
+                uint32_t w[W];
+                run.load(off, w);
+#pragma unroll
+                for (int i = 0; i < W; ++i) cw[i] = (w[i] >> nsh) & 0x0F0F0F0Fu;
+            }
+            if constexpr (T == T_Q5_0) {
+                uint32_t h[1];
+                qh.load(off, h);
+#pragma unroll
+                for (int i = 0; i < W; ++i) {
+                    const uint32_t t = (h[0] >> (e0 + 4 * i)) & 15u;
+                    cw[i] |= ((t * 0x00204081u) & 0x01010101u) << 4;
+                }
             }
         }
     }
+};
+
+// The integer code held in the low byte of b, as Codes leaves it (offset
+// still in for Q4_0 / Q5_0).
+template <int T>
+__device__ __forceinline__ int code_of_byte(uint32_t b) {
+    if constexpr (T == T_Q8_0) return (int)(int8_t)(b & 255u);
+    else return (int)(b & 255u) - (T == T_Q5_0 ? 16 : 8);
 }
 
-template <int T, int NB, int GT>   // NB = d / 32; GT = heads per kv head when fixed, 0 when not
+template <int T, int NB, int GT, int CH>   // NB = d / 32; GT = heads per kv head when fixed, 0 when not; CH = chunk
 __global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __restrict__ q, const uint8_t* __restrict__ K,
                                                                 const uint8_t* __restrict__ V, int64_t T_len, int n_heads,
                                                                 int n_kv, float scale, float* __restrict__ ws) {
-    using R = Rows<T, NB>;
+    using R = Rows<T, NB, CH>;
     constexpr int D = 32 * NB, BB = Fmt<T>::BB;
+    constexpr int GG = GT > 0 ? GT : kMaxG;      // heads per kv head, at most
     constexpr int64_t ROWB = R::ROWB;            // bytes of one (t, g) row: d / 32 blocks
     extern __shared__ __align__(16) uint8_t dyn[];
-    uint8_t* sK = dyn;                           // [kChunk][SLOT] row windows
-    uint8_t* sV = dyn + kChunk * R::SLOT;
-    __shared__ float sq[kMaxG][kMaxD];           // the group's queries
-    __shared__ float ss[kMaxG][kChunk];          // scores, then e^(s - m)
-    __shared__ float sred[kWarps][kMaxG];
-    __shared__ float so[kMaxG][kMaxD];           // partial outputs, warps added in order
-    const int g = blockIdx.x, c = blockIdx.y, G = n_heads / n_kv;
+    uint8_t* sK = dyn;                           // [CH][SLOT] row windows
+    uint8_t* sV = dyn + CH * R::SLOT;
+    __shared__ float sq[GG][D];                  // the group's queries
+    __shared__ __align__(16) float ss[CH][GG];   // scores, then e^(s - m), per position
+    __shared__ float sred[2][GG];
+    __shared__ float so[GG][D];                  // partial outputs, warps added in order
+    const int g = (int)(blockIdx.x % (unsigned)n_kv), c = (int)(blockIdx.x / (unsigned)n_kv), G = n_heads / n_kv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t t0 = (int64_t)c * kChunk;
-    const int nt = (int)min((int64_t)kChunk, T_len - t0);
+    const int64_t t0 = (int64_t)c * CH;
+    const int nt = (int)min((int64_t)CH, T_len - t0);
     const int64_t total = T_len * n_kv * ROWB;   // bytes of each cache
+    // Where a row starts in its slot: the same for all of a warp's positions
+    // (they are 8 apart and rows are an even number of bytes, so 8 rows span
+    // a multiple of 16 bytes).
+    const int mis = (int)((((t0 + warp) * n_kv + g) * ROWB) & 15);
+    constexpr int STEP = kWarps * R::SLOT;       // slot bytes between a warp's positions
     pdl_wait_prior();
-    stage_rows<T, NB>(sK, K, t0, nt, n_kv, g, total);
+    stage_rows<T, NB, CH>(sK, K, t0, nt, n_kv, g, total);
     cp_async_commit();
-    stage_rows<T, NB>(sV, V, t0, nt, n_kv, g, total);
+    stage_rows<T, NB, CH>(sV, V, t0, nt, n_kv, g, total);
     cp_async_commit();
     for (int i = threadIdx.x; i < G * D; i += blockDim.x) sq[i / D][i % D] = q[(int64_t)(g * G + i / D) * D + i % D];
     __syncthreads();
     // Lane l: elements e0 .. e0 + NB - 1 of block eb (pass 2, and pass 1 without a fixed group).
     const int e0 = (lane * NB) & 31, eb = (lane * NB) >> 5;
-    constexpr int GG = GT > 0 ? GT : kMaxG;
     if constexpr (GT > 0) {
         constexpr int LPH = 32 / GT, EPL = D / LPH, W = EPL / 4;   // lanes per head, elements per lane
         static_assert(EPL % 4 == 0 && EPL <= 32, "one lane's elements lie in one block");
@@ -186,10 +244,12 @@ __global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __
         const float offx = kOff * (float)xsum;
         cp_async_wait<1>();   // this thread's K copies
         __syncthreads();      // ... and everyone's
-        for (int j = warp; j < nt; j += kWarps) {
-            const uint8_t* blk = sK + j * R::SLOT + (int)((((t0 + j) * n_kv + g) * ROWB) & 15) + kb * BB;
+        const uint8_t* kblk = sK + warp * R::SLOT + mis + kb * BB;
+        const Codes<T, W> kc(kblk, k0);
+        uint32_t off = 0;
+        for (int j = warp; j < nt; j += kWarps, off += STEP) {
             uint32_t cw[W];
-            code_words<T, W>(blk, k0, cw);
+            kc.load(off, cw);
             int A = 0, B = 0, C = 0;
 #pragma unroll
             for (int i = 0; i < W; ++i) {
@@ -197,10 +257,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __
                 B = gv::dp4a_ss(cw[i], lb[i], B);
                 C = gv::dp4a_ss(cw[i], lc[i], C);
             }
-            float v = h2f(ld_u16(blk)) * (sx * (gv::limbs3_to_f(A, B, C) - offx));
+            float v = h2f(lds16(kblk + off)) * (sx * (gv::limbs3_to_f(A, B, C) - offx));
 #pragma unroll
             for (int o = LPH / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane % LPH == 0) ss[h][j] = scale * v;
+            if (lane % LPH == 0) ss[j][h] = scale * v;
         }
     } else {
     float qr[kMaxG][NB];
@@ -212,9 +272,9 @@ __global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __
     cp_async_wait<1>();   // this thread's K copies
     __syncthreads();      // ... and everyone's
     // Pass 1: scores.
-    for (int j = warp; j < nt; j += kWarps) {
-        const uint8_t* blk = sK + j * R::SLOT + (int)((((t0 + j) * n_kv + g) * ROWB) & 15) + eb * BB;
-        const float dk = h2f(blk[0] | ((uint32_t)blk[1] << 8));
+    const uint8_t* blk = sK + warp * R::SLOT + mis + eb * BB;
+    for (int j = warp; j < nt; j += kWarps, blk += STEP) {
+        const float dk = h2f(ld_u16(blk));
         int cv[NB];
 #pragma unroll
         for (int k = 0; k < NB; ++k) cv[k] = code_at<T>(blk, e0 + k);
@@ -227,7 +287,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __
             a *= dk;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-            if (lane == 0) ss[h][j] = scale * a;
+            if (lane == 0) ss[j][h] = scale * a;
         }
     }
     }
@@ -235,13 +295,13 @@ __global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __
     // Chunk statistics per head: m = max s, then e^(s - m) and their sum.
     for (int h = warp; h < G; h += kWarps) {
         float m = -__int_as_float(0x7f800000);
-        for (int j = lane; j < nt; j += 32) m = fmaxf(m, ss[h][j]);
+        for (int j = lane; j < nt; j += 32) m = fmaxf(m, ss[j][h]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         float l = 0.0f;
         for (int j = lane; j < nt; j += 32) {
-            const float e = expf(ss[h][j] - m);
-            ss[h][j] = e;
+            const float e = expf(ss[j][h] - m);
+            ss[j][h] = e;
             l += e;
         }
 #pragma unroll
@@ -260,18 +320,37 @@ __global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __
     for (int h = 0; h < GG; ++h)
 #pragma unroll
         for (int k = 0; k < NB; ++k) acc[h][k] = 0.0f;
-    for (int j = warp; j < nt; j += kWarps) {
-        const uint8_t* blk = sV + j * R::SLOT + (int)((((t0 + j) * n_kv + g) * ROWB) & 15) + eb * BB;
-        const float dv = h2f(blk[0] | ((uint32_t)blk[1] << 8));
+    const uint8_t* vblk = sV + warp * R::SLOT + mis + eb * BB;
+    const Codes<T, (NB >= 4 ? NB / 4 : 1)> vc(vblk, e0);
+    uint32_t voff = 0;
+    for (int j = warp; j < nt; j += kWarps, vblk += STEP, voff += STEP) {
+        const float dv = h2f(lds16(vblk));
         float vv[NB];
+        if constexpr (NB >= 4) {   // the lane's codes as words (they lie in one half of the block)
+            uint32_t cw[NB / 4];
+            vc.load(voff, cw);
 #pragma unroll
-        for (int k = 0; k < NB; ++k) vv[k] = dv * (float)code_at<T>(blk, e0 + k);
+            for (int k = 0; k < NB; ++k) vv[k] = dv * (float)code_of_byte<T>(cw[k >> 2] >> (8 * (k & 3)));
+        } else {
+#pragma unroll
+            for (int k = 0; k < NB; ++k) vv[k] = dv * (float)code_at<T>(vblk, e0 + k);
+        }
+        float p[GG];
+        if constexpr (GT > 0 && GT % 4 == 0) {
+#pragma unroll
+            for (int h = 0; h < GG; h += 4) {
+                const float4 q4 = *reinterpret_cast<const float4*>(&ss[j][h]);
+                p[h] = q4.x; p[h + 1] = q4.y; p[h + 2] = q4.z; p[h + 3] = q4.w;
+            }
+        } else {
+#pragma unroll
+            for (int h = 0; h < GG; ++h) p[h] = (GT > 0 || h < G) ? ss[j][h] : 0.0f;
+        }
 #pragma unroll
         for (int h = 0; h < GG; ++h) {
             if (GT == 0 && h >= G) break;
-            const float p = ss[h][j];
 #pragma unroll
-            for (int k = 0; k < NB; ++k) acc[h][k] = fmaf(p, vv[k], acc[h][k]);
+            for (int k = 0; k < NB; ++k) acc[h][k] = fmaf(p[h], vv[k], acc[h][k]);
         }
     }
     for (int w = 0; w < kWarps; ++w) {   // warp 0 writes, the others add, in warp order
@@ -285,7 +364,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __
         __syncthreads();
     }
     // Chunk partial (m, l, o[d]) per head.
-    const int nchunks = gridDim.y;
+    const int nchunks = (int)(gridDim.x / (unsigned)n_kv);
     for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
         const int h = i / D, e = i % D;
         float* dst = ws + ((int64_t)(g * G + h) * nchunks + c) * (D + 2);
@@ -349,7 +428,9 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
 template <int T, int NB, int GT>
 cudaError_t launch_tn(const float* q, const uint8_t* K, const uint8_t* V, int64_t T_len, int n_heads, int n_kv,
                       float scale, float* out, float* ws, cudaStream_t s) {
-    const int64_t nch = (T_len + kChunk - 1) / kChunk;
+    constexpr int CH = chunk_of<T>();
+    using R = Rows<T, NB, CH>;
+    const int64_t nch = (T_len + CH - 1) / CH;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -357,13 +438,13 @@ cudaError_t launch_tn(const float* q, const uint8_t* K, const uint8_t* V, int64_
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.stream = s;
-    cfg.gridDim = dim3((unsigned)n_kv, (unsigned)nch);
+    cfg.gridDim = dim3((unsigned)(n_kv * nch));
     cfg.blockDim = dim3(kWarps * 32);
-    cfg.dynamicSmemBytes = Rows<T, NB>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(attn_chunk_kernel<T, NB, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Rows<T, NB>::SMEM);
+    cfg.dynamicSmemBytes = R::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(attn_chunk_kernel<T, NB, GT, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         R::SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, attn_chunk_kernel<T, NB, GT>, q, K, V, T_len, n_heads, n_kv, scale, ws);
+    e = cudaLaunchKernelEx(&cfg, attn_chunk_kernel<T, NB, GT, CH>, q, K, V, T_len, n_heads, n_kv, scale, ws);
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3((unsigned)n_heads, (unsigned)((32 * NB + 31) / 32));
     cfg.blockDim = dim3(256);
@@ -407,7 +488,7 @@ cudaError_t launch_t(const float* q, const uint8_t* K, const uint8_t* V, int64_t
 }  // namespace at
 
 int64_t attn_decode_ws_bytes(int64_t T_len, int n_heads, int d) {
-    const int64_t nch = (T_len + at::kChunk - 1) / at::kChunk;
+    const int64_t nch = (T_len + at::kMinChunk - 1) / at::kMinChunk;
     return nch * n_heads * (int64_t)(d + 2) * (int64_t)sizeof(float);
 }
 

@@ -31,7 +31,7 @@ def run(gpu, name, Tn, nh, nkv, d, seed, scale=None):
 
 CASES = [
     ("Q8_0", 1, 4, 4, 128),
-    ("Q8_0", 300, 32, 8, 128),     # a ragged second chunk, 4 heads per kv head
+    ("Q8_0", 300, 32, 8, 128),     # a ragged last chunk, 4 heads per kv head
     ("Q8_0", 1000, 8, 1, 64),      # 8 heads per kv head
     ("Q4_0", 777, 16, 4, 128),
     ("Q5_0", 513, 8, 8, 32),
@@ -42,6 +42,16 @@ CASES = [
 @pytest.mark.parametrize("name,Tn,nh,nkv,d", CASES)
 def test_attn_decode_parity(gpu, name, Tn, nh, nkv, d):
     out, ref, Sv = run(gpu, name, Tn, nh, nkv, d, 800 + Tn + d)
+    err = np.abs(out - ref) - (RTOL * Sv + 1e-6)
+    assert (err <= 0).all(), f"{name} T={Tn}: worst excess {err.max():.3e}"
+
+
+@pytest.mark.parametrize("name", ["Q8_0", "Q5_0", "Q4_0"])
+@pytest.mark.parametrize("Tn", [191, 192, 193, 255, 256, 257, 385, 513])
+def test_attn_decode_chunk_edges(gpu, name, Tn):
+    # Position counts on both sides of one and two chunks of 192 and of 256
+    # positions, and a single position left over in the last chunk.
+    out, ref, Sv = run(gpu, name, Tn, 8, 2, 128, 1200 + Tn)
     err = np.abs(out - ref) - (RTOL * Sv + 1e-6)
     assert (err <= 0).all(), f"{name} T={Tn}: worst excess {err.max():.3e}"
 

@@ -181,7 +181,7 @@ def test_imatrix_and_attention_argument_errors_are_caught_on_host(lib):
     assert lib.qk_quantize_imatrix(qk.Q4_K, odd2, 4, 256, fake, fake, None) == 3
     assert lib.qk_quantize_imatrix(qk.Q4_K, fake, 0, 256, None, None, None) == 0
     ws = qk.attn_decode_workspace(qk.Q8_0, 300, 32, 8, 128)
-    assert ws == 2 * 32 * 130 * 4   # two chunks x heads x (d + 2) floats
+    assert ws == 3 * 32 * 130 * 4   # chunks of 128 (the smallest chunk) x heads x (d + 2) floats
     assert qk.attn_decode_workspace(qk.Q4_K, 300, 32, 8, 128) == 0
     call = lib.qk_attn_decode
     assert call(qk.Q4_K, fake, fake, fake, 300, 32, 8, 128, f(0.1), fake, fake, ws, None) == 1
