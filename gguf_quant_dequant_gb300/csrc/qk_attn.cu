@@ -28,7 +28,7 @@
 // share of q_h . K[t, g] for every head in fp32.  The
 // chunk's softmax statistics (max, sum of exp) follow in shared memory.
 // Pass 2: the same row mapping over V accumulates sum_t e^(s_t - m) V[t, g]
-// per head; warps are added in order.  A second kernel combines the chunks
+// per head; the warps' sums are added in warp order.  A second kernel combines the chunks
 // (log-sum-exp), in chunk order: deterministic.
 #include "qk_formats.cuh"
 #include "qk_internal.h"
@@ -39,10 +39,10 @@ namespace qk {
 namespace at {
 
 constexpr int kMinChunk = 128;   // positions per CTA, at least (the workspace is sized for it)
-// Measured on 32k positions, 32 / 8 heads, d = 128: Q8_0 58.8 / 56.1 / 60.9 us
-// at 128 / 192 / 256 positions, Q5_0 59.5 / 60.9 us at 192 / 256, Q4_0
-// 52.0 / 50.6 us at 192 / 256.
-template <int T> constexpr int chunk_of() { return T == T_Q4_0 ? 256 : 192; }
+// Measured on 32k positions, 32 / 8 heads, d = 128: Q8_0 52.3 / 49.2 / 53.4 us
+// at 128 / 192 / 256 positions, Q5_0 56.1 / 55.3 us and Q4_0 47.2 / 47.2 us at
+// 192 / 256.
+template <int T> constexpr int chunk_of() { return T == T_Q8_0 ? 192 : 256; }
 constexpr int kWarps = 8;
 constexpr int kMaxG = 8;       // query heads per kv head, at most
 
@@ -186,7 +186,6 @@ __global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __
     __shared__ float sq[GG][D];                  // the group's queries
     __shared__ __align__(16) float ss[CH][GG];   // scores, then e^(s - m), per position
     __shared__ float sred[2][GG];
-    __shared__ float so[GG][D];                  // partial outputs, warps added in order
     const int g = (int)(blockIdx.x % (unsigned)n_kv), c = (int)(blockIdx.x / (unsigned)n_kv), G = n_heads / n_kv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t0 = (int64_t)c * CH;
@@ -353,22 +352,26 @@ __global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __
             for (int k = 0; k < NB; ++k) acc[h][k] = fmaf(p[h], vv[k], acc[h][k]);
         }
     }
-    for (int w = 0; w < kWarps; ++w) {   // warp 0 writes, the others add, in warp order
-        if (warp == w) {
+    // The warps' partial sums go to the row slots (no longer needed), then
+    // every output element adds them in warp order.
+    static_assert(kWarps * GG * D * 4 <= 2 * CH * R::SLOT, "the partial sums fit in the row slots");
+    float* part = reinterpret_cast<float*>(dyn);   // [kWarps][GG][D]
+    __syncthreads();   // every warp is done with the slots
 #pragma unroll
-            for (int h = 0; h < GG; ++h)
+    for (int h = 0; h < GG; ++h)
 #pragma unroll
-                for (int k = 0; k < NB; ++k)
-                    if (h < G) so[h][lane * NB + k] = w == 0 ? acc[h][k] : so[h][lane * NB + k] + acc[h][k];
-        }
-        __syncthreads();
-    }
+        for (int k = 0; k < NB; ++k)
+            if (h < G) part[(warp * GG + h) * D + lane * NB + k] = acc[h][k];
+    __syncthreads();
     // Chunk partial (m, l, o[d]) per head.
     const int nchunks = (int)(gridDim.x / (unsigned)n_kv);
     for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
         const int h = i / D, e = i % D;
+        float o = part[h * D + e];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) o += part[(w * GG + h) * D + e];
         float* dst = ws + ((int64_t)(g * G + h) * nchunks + c) * (D + 2);
-        dst[2 + e] = so[h][e];
+        dst[2 + e] = o;
         if (e == 0) {
             dst[0] = sred[0][h];
             dst[1] = sred[1][h];

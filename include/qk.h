@@ -164,7 +164,7 @@ qk_status qk_quantize(int type, const float* w, int64_t rows, int64_t cols, void
  *   d      32, 64, 128 or 256; n_heads a multiple of n_kv, at most 8 query
  *          heads per kv head; 1 <= T <= 65535 * 256.
  *   out    fp32 [n_heads, d]; ws at least qk_attn_decode_workspace bytes.
- * Positions are split in chunks of 192 (Q8_0, Q5_0) or 256 (Q4_0) (one CTA
+ * Positions are split in chunks of 192 (Q8_0) or 256 (Q5_0, Q4_0) (one CTA
  * per kv head and chunk, the cache streamed once); each chunk keeps its max
  * score, sum of exponentials and weighted value sum, and a second launch
  * combines the chunks (log-sum-exp) in chunk order: deterministic.  fp32
