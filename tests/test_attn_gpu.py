@@ -102,3 +102,21 @@ def test_attn_decode_deterministic(gpu):
 def test_attn_decode_every_group_path(gpu, name, Tn, nh, nkv, d):
     out, ref, Sv = run(gpu, name, Tn, nh, nkv, d, 1100 + Tn + d)
     assert (np.abs(out - ref) <= RTOL * Sv + 1e-6).all()
+
+
+def test_attn_decode_maximum_positions(gpu):
+    # The largest cache the call accepts, T = 65535 * 256 positions (one kv
+    # head, two query heads, d = 32, Q4_0: 2 x 302 MB), every output against
+    # the oracle.
+    t, Tn, nh, nkv, d = qk.Q4_0, 65535 * 256, 2, 1, 32
+    K = synth.random_blocks_torch("Q4_0", Tn * nkv, d, 1300, gpu)
+    V = synth.random_blocks_torch("Q4_0", Tn * nkv, d, 1301, gpu)
+    g = torch.Generator(device=gpu)
+    g.manual_seed(1302)
+    q = torch.randn((nh, d), device=gpu, generator=g)
+    out = qk.attn_decode(t, q, K, V, Tn, nh, nkv, d, 1.0 / np.sqrt(d)).cpu().numpy()
+    qk.device_status()
+    ref, Sv = oracle.attn_decode(t, q.cpu().numpy(), K.cpu().numpy(), V.cpu().numpy(), Tn, nh, nkv, d, 1.0 / np.sqrt(d))
+    assert (np.abs(out - ref) <= RTOL * Sv + 1e-6).all()
+    del K, V
+    torch.cuda.empty_cache()

@@ -189,6 +189,8 @@ def test_imatrix_and_attention_argument_errors_are_caught_on_host(lib):
     assert call(qk.Q8_0, fake, fake, fake, 300, 30, 8, 128, f(0.1), fake, fake, ws, None) == 2    # groups
     assert call(qk.Q8_0, fake, fake, fake, 300, 32, 2, 128, f(0.1), fake, fake, ws, None) == 2    # 16 per kv
     assert call(qk.Q8_0, fake, fake, fake, 0, 32, 8, 128, f(0.1), fake, fake, ws, None) == 2      # T
+    big = qk.attn_decode_workspace(qk.Q8_0, 65535 * 256 + 1, 32, 8, 128)
+    assert call(qk.Q8_0, fake, fake, fake, 65535 * 256 + 1, 32, 8, 128, f(0.1), fake, fake, big, None) == 2
     assert call(qk.Q8_0, None, fake, fake, 300, 32, 8, 128, f(0.1), fake, fake, ws, None) == 4
     assert call(qk.Q8_0, fake, odd1, fake, 300, 32, 8, 128, f(0.1), fake, fake, ws, None) == 3
     assert call(qk.Q8_0, fake, fake, odd2, 300, 32, 8, 128, f(0.1), fake, fake, ws, None) == 3

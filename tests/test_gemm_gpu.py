@@ -149,3 +149,30 @@ def test_gemm_small_batch_llama3_ffn_sampled(gpu, rows, cols, M):
     Xb = Xd.view(torch.int16).cpu().numpy().view(np.uint16)
     Y_ref, S = oracle.gemm_bf16(t, Wrows, ni.size, cols, Xb)
     assert_gemv_close(Y[:, ni], Y_ref, S, rtol=GEMM_RTOL, atol=0.0, what=f"FFN gemm {rows}x{cols} M={M}")
+
+
+# The prefill workload at full size in the bench's launch configuration:
+# every matrix of the M = 2048 recipe (Q4_K / Q6_K / Q8_0 at 4096x4096,
+# 14336x4096 and 4096x14336, and the 128256x4096 Q6_K vocabulary), all 2048
+# tokens of sampled rows (both ends of row tiles among them) against the
+# oracle on those rows.
+@pytest.mark.parametrize("i", range(len(synth.PREFILL)), ids=[p[0] for p in synth.PREFILL])
+def test_gemm_prefill_recipe_full_size_sampled(gpu, i):
+    nm, name, rows, cols = synth.PREFILL[i]
+    t = synth.TYPE_IDS[name]
+    M = synth.PREFILL_M
+    Wd = synth.random_blocks_torch(name, rows, cols, 4100 + i, gpu)
+    g = torch.Generator(device=gpu)
+    g.manual_seed(4200 + i)
+    Xd = torch.randn((M, cols), device=gpu, generator=g).to(torch.bfloat16)
+    Y = qk.gemm(t, Wd, rows, cols, Xd).cpu().numpy()   # as the bench calls it
+    qk.device_status()
+    rng = synth.rng(4300 + i)
+    ni = np.unique(np.concatenate([rng.choice(rows, 12, replace=False), [0, 127, 128, rows - 129, rows - 1]]))
+    rb = qk.row_bytes(t, cols)
+    Wrows = torch.cat([Wd[n * rb:(n + 1) * rb] for n in ni]).cpu().numpy()
+    Xb = Xd.view(torch.int16).cpu().numpy().view(np.uint16)
+    Y_ref, S = oracle.gemm_bf16(t, Wrows, ni.size, cols, Xb)
+    assert_gemv_close(Y[:, ni], Y_ref, S, rtol=GEMM_RTOL, atol=0.0, what=f"prefill {nm} {rows}x{cols} M={M}")
+    del Wd, Xd
+    torch.cuda.empty_cache()
