@@ -90,6 +90,30 @@ def test_quantize_special_values(gpu, name):
     assert np.array_equal(got, ref), f"{name}: {int((got != ref).sum())} bytes differ"
 
 
+@pytest.mark.parametrize("name,qmax", [("Q8_0", 100), ("Q5_0", 14), ("Q4_0", 6)])
+def test_quantize_near_ties(gpu, name, qmax):
+    # Weights whose quotient by the block scale lies just beside a half-integer
+    # (offsets from 0 to +-1e-3 of a code step): the code decisions near the
+    # rounding boundary.  The block's largest weight is kept from a first
+    # quantization, so the fp16 scale d is known and stays the same.
+    t = type_id(name)
+    rng = np.random.default_rng(7070)
+    nb = 512
+    base = rng.standard_normal((nb, 32)).astype(np.float32)
+    d = oracle.quantize(t, base).reshape(nb, -1)[:, :2].copy().view(np.float16).astype(np.float64)[:, 0]
+    deltas = np.array([0.0, 1e-7, -1e-7, 1e-6, -1e-6, 1e-5, -1e-5, 5e-5, -5e-5,
+                       1.2e-4, -1.2e-4, 2.4e-4, -2.4e-4, 2.6e-4, -2.6e-4, 1e-3, -1e-3])
+    m = rng.integers(-qmax - 1, qmax + 1, size=(nb, 32))
+    dl = deltas[rng.integers(0, deltas.size, size=(nb, 32))]
+    w = ((m + 0.5 + dl) * d[:, None]).astype(np.float32)
+    keep = np.argmax(np.abs(base), axis=1)
+    w[np.arange(nb), keep] = base[np.arange(nb), keep]
+    ref = oracle.quantize(t, w.reshape(16, -1))
+    assert np.array_equal(ref.reshape(nb, -1)[:, :2], oracle.quantize(t, base).reshape(nb, -1)[:, :2])   # same scales
+    got = run(gpu, t, w.reshape(16, -1))
+    assert np.array_equal(got, ref), f"{name}: {int((got != ref).sum())} bytes differ"
+
+
 def test_quantize_bench_size_sampled_rows(gpu):
     # The bench's launch: a 14336 x 4096 fp32 matrix (235 MB, beyond L2); the
     # oracle quantizes sampled rows (blocks never straddle rows).
