@@ -379,37 +379,56 @@ __global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __
     }
 }
 
+// (m, l) of two sets of scores merged: m = max, l = sum of l_i e^(m_i - m).
+__device__ __forceinline__ void ml_merge(float& m, float& l, float m2, float l2) {
+    const float mm = fmaxf(m, m2);
+    if (mm == -__int_as_float(0x7f800000)) return;   // both empty
+    l = l * expf(m - mm) + l2 * expf(m2 - mm);
+    m = mm;
+}
+
 // out[h, e] = sum_c e^(m_c - M) o_c[e] / sum_c e^(m_c - M) l_c.  CTA (h, e0)
-// takes head h and elements e0 .. e0 + 31: M by a fixed tree over the chunks,
-// the l-sum by a fixed tree, and each element's o-sum split over 8 chunk
-// groups (chunks c = k mod 8) that are added in group order: deterministic.
+// takes head h and elements e0 .. e0 + 31: (M, L) by merging the chunks'
+// (m_c, l_c) in a fixed order (each thread its chunks c = tid mod 256 in
+// turn, then a shuffle tree per warp, then the warps in order), and each
+// element's o-sum split over 8 chunk groups (chunks c = k mod 8) that are
+// added in group order: deterministic.
 __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ ws, int nchunks, int D,
                                                           float* __restrict__ out) {
-    __shared__ float red[256];
+    __shared__ float wm[8], wl[8], ML[2];
     __shared__ float part[8][32];
     pdl_wait_prior();
-    const int h = blockIdx.x, tid = threadIdx.x;
+    const int h = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t stride = D + 2;
     const float* base = ws + (int64_t)h * nchunks * stride;
-    float m = -__int_as_float(0x7f800000);
-    for (int c = tid; c < nchunks; c += 256) m = fmaxf(m, base[(int64_t)c * stride]);
-    red[tid] = m;
-    __syncthreads();
-    for (int o = 128; o > 0; o >>= 1) {
-        if (tid < o) red[tid] = fmaxf(red[tid], red[tid + o]);
-        __syncthreads();
+    float m = -__int_as_float(0x7f800000), l = 0.0f;
+    for (int c = tid; c < nchunks; c += 256) ml_merge(m, l, base[(int64_t)c * stride], base[(int64_t)c * stride + 1]);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o), l2 = __shfl_xor_sync(0xffffffffu, l, o);
+        // Lanes that meet merge in lane order, so both ends of a pair hold the same bits.
+        if (lane & o) {
+            float mb = m2, lb = l2;
+            ml_merge(mb, lb, m, l);
+            m = mb;
+            l = lb;
+        } else {
+            ml_merge(m, l, m2, l2);
+        }
     }
-    const float M = red[0];
-    __syncthreads();
-    float l = 0.0f;
-    for (int c = tid; c < nchunks; c += 256) l += expf(base[(int64_t)c * stride] - M) * base[(int64_t)c * stride + 1];
-    red[tid] = l;
-    __syncthreads();
-    for (int o = 128; o > 0; o >>= 1) {
-        if (tid < o) red[tid] += red[tid + o];
-        __syncthreads();
+    if (lane == 0) {
+        wm[warp] = m;
+        wl[warp] = l;
     }
-    const float L = red[0];
+    __syncthreads();
+    if (tid == 0) {
+        float M = wm[0], L = wl[0];
+        for (int w = 1; w < 8; ++w) ml_merge(M, L, wm[w], wl[w]);
+        ML[0] = M;
+        ML[1] = L;
+    }
+    __syncthreads();
+    const float M = ML[0], L = ML[1];
     const int el = tid & 31, cg = tid >> 5, e = blockIdx.y * 32 + el;
     float acc = 0.0f;
     if (e < D) {
