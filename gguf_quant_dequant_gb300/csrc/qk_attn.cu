@@ -25,11 +25,11 @@
 // x = s (65536 a + 256 b + c) per 32-block, signed 8-bit limbs), so each
 // score is an exact integer dp4a sum over the cache's codes, added over the
 // head's lanes by shuffles.  Otherwise lane l owns d/32 elements and forms its
-// share of q_h . K[t, g] for every head in fp32.  The
-// chunk's softmax statistics (max, sum of exp) follow in shared memory.
+// share of q_h . K[t, g] for every head in fp32.  The chunk's softmax
+// statistics (max, sum of exp) follow in shared memory.
 // Pass 2: the same row mapping over V accumulates sum_t e^(s_t - m) V[t, g]
-// per head; the warps' sums are added in warp order.  A second kernel combines the chunks
-// (log-sum-exp), in chunk order: deterministic.
+// per head; the warps' sums are added in warp order.  A second kernel
+// combines the chunks (log-sum-exp) in a fixed order: deterministic.
 #include "qk_formats.cuh"
 #include "qk_internal.h"
 #include "qk_lanes.cuh"

@@ -167,7 +167,7 @@ qk_status qk_quantize(int type, const float* w, int64_t rows, int64_t cols, void
  * Positions are split in chunks of 192 (Q8_0) or 256 (Q5_0, Q4_0) (one CTA
  * per kv head and chunk, the cache streamed once); each chunk keeps its max
  * score, sum of exponentials and weighted value sum, and a second launch
- * combines the chunks (log-sum-exp) in chunk order: deterministic.  fp32
+ * combines the chunks (log-sum-exp) in a fixed order: deterministic.  fp32
  * arithmetic.
  * Errors: QK_ERR_TYPE, QK_ERR_SHAPE, QK_ERR_NULL, QK_ERR_ALIGN,
  * QK_ERR_WORKSPACE. */
