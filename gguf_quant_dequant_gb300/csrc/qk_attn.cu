@@ -93,12 +93,21 @@ __device__ __forceinline__ void stage_rows(uint8_t* slots, const uint8_t* C, int
     }
 }
 
+// A shared-memory word load at a 32-bit shared address (volatile: it stays
+// after the copy waits and barriers that precede it).
+__device__ __forceinline__ uint32_t sld32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
 // N words from a 2-byte aligned address in shared memory, for a lane whose
 // address moves by multiples of 16 bytes from position to position: the
-// aligned word address and the funnel shift are fixed once.  (The word
-// address is reached by pointer arithmetic, so the loads stay shared-space
-// loads.)
-template <int N> struct Run {
+// aligned word address and the funnel shift are fixed once.  The word address
+// is reached by pointer arithmetic, so plain loads stay shared-space loads;
+// ASM issues them as explicit shared loads instead (measured faster for the
+// nibble types, slower for Q8_0).
+template <int N, bool ASM = false> struct Run {
     const uint8_t* a;
     uint32_t sh;
     __device__ __forceinline__ explicit Run(const uint8_t* p) {
@@ -107,13 +116,24 @@ template <int N> struct Run {
         sh = 8u * m;
     }
     __device__ __forceinline__ void load(uint32_t off, uint32_t (&w)[N]) const {
-        const uint32_t* q = reinterpret_cast<const uint32_t*>(a + off);
-        uint32_t prev = q[0];
+        if constexpr (ASM) {
+            const uint32_t b = smem_u32(a) + off;
+            uint32_t prev = sld32(b);
 #pragma unroll
-        for (int i = 0; i < N; ++i) {
-            const uint32_t next = q[i + 1];
-            w[i] = __funnelshift_r(prev, next, sh);
-            prev = next;
+            for (int i = 0; i < N; ++i) {
+                const uint32_t next = sld32(b + 4u * (i + 1));
+                w[i] = __funnelshift_r(prev, next, sh);
+                prev = next;
+            }
+        } else {
+            const uint32_t* q = reinterpret_cast<const uint32_t*>(a + off);
+            uint32_t prev = q[0];
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                const uint32_t next = q[i + 1];
+                w[i] = __funnelshift_r(prev, next, sh);
+                prev = next;
+            }
         }
     }
 };
@@ -126,8 +146,8 @@ __device__ __forceinline__ uint32_t lds16(const uint8_t* p) { return *reinterpre
 template <int T, int W> struct Codes {
     static constexpr bool kWhole = T != T_Q8_0 && W == 8;   // the whole block of a nibble type
     static constexpr int QS = T == T_Q8_0 ? 2 : (T == T_Q5_0 ? 6 : 2);
-    Run<kWhole ? 4 : W> run;
-    Run<1> qh;
+    Run<kWhole ? 4 : W, T != T_Q8_0> run;
+    Run<1, T != T_Q8_0> qh;
     uint32_t nsh;
     int e0;
     __device__ __forceinline__ Codes(const uint8_t* blk, int e0_)
