@@ -112,6 +112,21 @@ namespace qk {
 // Record `msg` as the calling thread's last error and return `st` (for entry
 // points defined in other translation units).
 qk_status set_error(qk_status st, const char* msg) { return fail(st, "%s", msg); }
+
+// The argument checks of qk_gemv, in its order (no launch, no device call).
+qk_status gemv_check_args(int type, const void* W, int64_t rows, int64_t cols, const float* x, int64_t M,
+                          const float* y) {
+    qk_status st = check_matrix(type, W, rows, cols);
+    if (st != QK_OK) return st;
+    if (M < 0) return fail(QK_ERR_SHAPE, "negative M=%lld", (long long)M);
+    if (rows == 0 || M == 0) return QK_OK;
+    if (!y) return fail(QK_ERR_NULL, "y is NULL");
+    if (!aligned(y, 4)) return fail(QK_ERR_ALIGN, "y is not 4-byte aligned");
+    if (cols == 0) return QK_OK;
+    if (!x) return fail(QK_ERR_NULL, "x is NULL");
+    if (!aligned(x, 16)) return fail(QK_ERR_ALIGN, "x is not 16-byte aligned");
+    return QK_OK;
+}
 }  // namespace qk
 
 extern "C" {
@@ -211,20 +226,15 @@ size_t qk_gemv_workspace(int type, int64_t rows, int64_t cols, int64_t M) {
 
 qk_status qk_gemv(int type, const void* W, int64_t rows, int64_t cols, const float* x, int64_t M, float* y,
                   void* ws, size_t ws_bytes, void* stream) {
-    qk_status st = check_matrix(type, W, rows, cols);
+    qk_status st = qk::gemv_check_args(type, W, rows, cols, x, M, y);
     if (st != QK_OK) return st;
-    if (M < 0) return fail(QK_ERR_SHAPE, "negative M=%lld", (long long)M);
     if (rows == 0 || M == 0) return QK_OK;
-    if (!y) return fail(QK_ERR_NULL, "y is NULL");
-    if (!aligned(y, 4)) return fail(QK_ERR_ALIGN, "y is not 4-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cols == 0) {
         cudaError_t e = cudaMemsetAsync(y, 0, (size_t)(M * rows) * sizeof(float), s);
         if (e != cudaSuccess) return cuda_fail(e, "qk_gemv zero fill");
         return QK_OK;
     }
-    if (!x) return fail(QK_ERR_NULL, "x is NULL");
-    if (!aligned(x, 16)) return fail(QK_ERR_ALIGN, "x is not 16-byte aligned");
     unsigned* status = nullptr;
     int sms = 0;
     st = device_state(&status, &sms);

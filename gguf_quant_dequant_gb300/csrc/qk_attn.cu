@@ -36,7 +36,7 @@
 #include "qk_ptx.cuh"
 
 namespace qk {
-namespace at {
+namespace attn {
 
 constexpr int kMinChunk = 128;   // positions per CTA, at least (the workspace is sized for it)
 // Measured on 32k positions, 32 / 8 heads, d = 128: Q8_0 52.3 / 49.2 / 53.4 us
@@ -527,23 +527,23 @@ cudaError_t launch_t(const float* q, const uint8_t* K, const uint8_t* V, int64_t
     return cudaErrorInvalidValue;
 }
 
-}  // namespace at
+}  // namespace attn
 
 int64_t attn_decode_ws_bytes(int64_t T_len, int n_heads, int d) {
-    const int64_t nch = (T_len + at::kMinChunk - 1) / at::kMinChunk;
+    const int64_t nch = (T_len + attn::kMinChunk - 1) / attn::kMinChunk;
     return nch * n_heads * (int64_t)(d + 2) * (int64_t)sizeof(float);
 }
 
 bool attn_decode_shape_ok(int n_heads, int n_kv, int d) {
-    return n_kv > 0 && n_heads % n_kv == 0 && n_heads / n_kv <= at::kMaxG && (d == 32 || d == 64 || d == 128 || d == 256);
+    return n_kv > 0 && n_heads % n_kv == 0 && n_heads / n_kv <= attn::kMaxG && (d == 32 || d == 64 || d == 128 || d == 256);
 }
 
 cudaError_t launch_attn_decode(int type, const float* q, const uint8_t* K, const uint8_t* V, int64_t T_len, int n_heads,
                                int n_kv, int d, float scale, float* out, float* ws, cudaStream_t s) {
     switch (type) {
-    case T_Q8_0: return at::launch_t<T_Q8_0>(q, K, V, T_len, n_heads, n_kv, d, scale, out, ws, s);
-    case T_Q5_0: return at::launch_t<T_Q5_0>(q, K, V, T_len, n_heads, n_kv, d, scale, out, ws, s);
-    case T_Q4_0: return at::launch_t<T_Q4_0>(q, K, V, T_len, n_heads, n_kv, d, scale, out, ws, s);
+    case T_Q8_0: return attn::launch_t<T_Q8_0>(q, K, V, T_len, n_heads, n_kv, d, scale, out, ws, s);
+    case T_Q5_0: return attn::launch_t<T_Q5_0>(q, K, V, T_len, n_heads, n_kv, d, scale, out, ws, s);
+    case T_Q4_0: return attn::launch_t<T_Q4_0>(q, K, V, T_len, n_heads, n_kv, d, scale, out, ws, s);
     }
     return cudaErrorInvalidValue;
 }

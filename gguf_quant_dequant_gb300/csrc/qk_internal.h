@@ -11,6 +11,10 @@ namespace qk {
 
 // Sets the calling thread's qk_last_error() text; returns st.
 qk_status set_error(qk_status st, const char* msg);
+// qk_gemv's argument checks (type, shape, NULL and alignment), in its order;
+// sets the error text on failure.
+qk_status gemv_check_args(int type, const void* W, int64_t rows, int64_t cols, const float* x, int64_t M,
+                          const float* y);
 
 cudaError_t launch_dequant(int type, const uint8_t* W, int64_t rows, int64_t cols, void* out,
                            int out_bf16, cudaStream_t s);

@@ -22,6 +22,10 @@ void* g_scratch_ptr[kMaxDevices] = {};
 
 extern "C" qk_status qk_gemv_noalloc(int type, const void* W, int64_t rows, int64_t cols, const float* x,
                                      int64_t M, float* y, void* stream) {
+    // Argument errors first, in qk_gemv's order, so that a bad pointer is
+    // reported as such whatever the problem's size.
+    const qk_status st = qk::gemv_check_args(type, W, rows, cols, x, M, y);
+    if (st != QK_OK) return st;
     const size_t need = qk_gemv_workspace(type, rows, cols, M);
     if (need > QK_GEMV_NOALLOC_SCRATCH_BYTES) {
         char msg[256];

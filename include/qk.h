@@ -284,7 +284,10 @@ qk_status qk_gemv_batch(int type, int n_mat, const void* const* W, const int64_t
  *     is queued.  This call itself allocates nothing.
  *   Set-up: the first call on each device, with that device current, looks
  *     up the array's device address; make that first call before starting
- *     any stream capture.
+ *     any stream capture.  The library keeps that address (and the address
+ *     of its device status word) per device for the life of the process; a
+ *     cudaDeviceReset() unloads the module and leaves them stale, so make no
+ *     qk_* call on a device after resetting it.
  *   Sharing: every call on a device uses the same array and leaves its
  *     contents behind; each call clears what must start at zero itself.
  *     Calls whose kernels overlap on the GPU (different streams without an

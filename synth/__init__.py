@@ -148,3 +148,18 @@ PREFILL_M = 2048
 PREFILL = ([(f"{s}_{t}", t, r, c) for t in ("Q4_K", "Q6_K", "Q8_0")
             for (s, r, c) in (("sq", 4096, 4096), ("up", 14336, 4096), ("down", 4096, 14336))]
            + [("vocab", "Q6_K", 128256, 4096)])
+
+
+def activations_outliers(M: int, K: int, seed: int, ratio: float, block: int = 32):
+    """fp32 [M, K] ~ N(0, 1) with one coordinate per `block` consecutive
+    elements replaced by +-ratio (a massive activation, `ratio` times the
+    typical magnitude).  Returns (x, pos) with pos int64 [M, K // block] the
+    position of the outlier inside each block."""
+    g = rng(seed)
+    x = g.standard_normal((M, K)).astype(np.float32)
+    nb = K // block
+    pos = g.integers(0, block, size=(M, nb))
+    sign = np.where(g.integers(0, 2, size=(M, nb)) == 0, -1.0, 1.0)
+    cols = np.arange(nb)[None, :] * block + pos
+    x[np.arange(M)[:, None], cols] = (sign * ratio).astype(np.float32)
+    return x, pos
