@@ -282,12 +282,17 @@ qk_status qk_gemv_batch(int type, int n_mat, const void* const* W, const int64_t
     if (!x) return fail(QK_ERR_NULL, "x is NULL");
     if (!aligned(x, 16)) return fail(QK_ERR_ALIGN, "x is not 16-byte aligned");
     int sms = 0;
-    qk_status st = device_state(nullptr, &sms);
+    unsigned* status = nullptr;
+    qk_status st = device_state(&status, &sms);
     if (st != QK_OK) return st;
-    if (qk::gemv5_ring_pairs(type, n_mat, rows, cols, sms) == 0)
-        return fail(QK_ERR_SHAPE, "cols=%lld is too large for the batched decode kernel", (long long)cols);
-    cudaError_t e = qk::launch_gemv5(type, n_mat, reinterpret_cast<const uint8_t* const*>(W), rows, cols, x, y, sms,
-                                     s);
+    cudaError_t e;
+    if (qk::hgemv_ok(type, n_mat, rows, cols, sms)) {
+        e = qk::launch_hgemv(type, n_mat, reinterpret_cast<const uint8_t* const*>(W), rows, cols, x, y, sms, status, s);
+    } else {
+        if (qk::gemv5_ring_pairs(type, n_mat, rows, cols, sms) == 0)
+            return fail(QK_ERR_SHAPE, "cols=%lld is too large for the batched decode kernel", (long long)cols);
+        e = qk::launch_gemv5(type, n_mat, reinterpret_cast<const uint8_t* const*>(W), rows, cols, x, y, sms, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "qk_gemv_batch launch");
     g_last_error.clear();
     return QK_OK;
@@ -311,12 +316,19 @@ qk_status qk_gemv_swiglu(int type, const void* Wg, const void* Wu, int64_t rows,
     if (!x) return fail(QK_ERR_NULL, "x is NULL");
     if (!aligned(x, 16)) return fail(QK_ERR_ALIGN, "x is not 16-byte aligned");
     int sms = 0;
-    st = device_state(nullptr, &sms);
+    unsigned* status = nullptr;
+    st = device_state(&status, &sms);
     if (st != QK_OK) return st;
-    if (qk::gemv5_ring_pairs(type, 1, &rows, cols, sms) == 0)
-        return fail(QK_ERR_SHAPE, "cols=%lld is too large for the decode kernel", (long long)cols);
-    cudaError_t e = qk::launch_gemv5_swiglu(type, static_cast<const uint8_t*>(Wg), static_cast<const uint8_t*>(Wu),
-                                            rows, cols, x, h, sms, s);
+    cudaError_t e;
+    if (qk::hgemv_ok(type, 1, &rows, cols, sms)) {
+        e = qk::launch_hgemv_swiglu(type, static_cast<const uint8_t*>(Wg), static_cast<const uint8_t*>(Wu), rows, cols,
+                                    x, h, sms, status, s);
+    } else {
+        if (qk::gemv5_ring_pairs(type, 1, &rows, cols, sms) == 0)
+            return fail(QK_ERR_SHAPE, "cols=%lld is too large for the decode kernel", (long long)cols);
+        e = qk::launch_gemv5_swiglu(type, static_cast<const uint8_t*>(Wg), static_cast<const uint8_t*>(Wu), rows, cols,
+                                    x, h, sms, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "qk_gemv_swiglu launch");
     g_last_error.clear();
     return QK_OK;

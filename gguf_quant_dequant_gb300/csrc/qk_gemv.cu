@@ -347,6 +347,10 @@ int64_t align16(int64_t v) { return (v + 15) & ~(int64_t)15; }
 GemvPlan plan_gemv(int type, int64_t rows, int64_t cols, int64_t M, int sm_count) {
     GemvPlan pl;
     pl.sms = sm_count;
+    if (M == 1 && hgemv_ok(type, 1, &rows, cols, sm_count)) {   // tensor-core decode kernel, prep inside
+        pl.decode = pl.tc = true;
+        return pl;
+    }
     if (M == 1 && gemv5_ring_pairs(type, 1, &rows, cols, sm_count) > 0) {   // decode kernel, prep inside
         pl.decode = true;
         return pl;
@@ -400,6 +404,7 @@ static cudaError_t launch_mt(const GemvPlan& pl, const gv::Args& a, cudaStream_t
 
 cudaError_t launch_gemv(int type, const GemvPlan& pl, const uint8_t* W, int64_t rows, int64_t cols, const float* x,
                         int64_t M, float* y, float* ws, unsigned* status, cudaStream_t s) {
+    if (pl.decode && pl.tc) return launch_hgemv(type, 1, &W, &rows, cols, x, &y, pl.sms, status, s);
     if (pl.decode) return launch_gemv5(type, 1, &W, &rows, cols, x, &y, pl.sms, s);
     gv::Args a = {};
     a.W = W;

@@ -1,0 +1,504 @@
+// qk_hgemv.cu -- the decode GEMV on the tensor cores: y[n] = sum_k w[n, k] x[k]
+// for one activation row, the batched form over matrices that share x
+// (q/k/v, gate/up) and the fused SwiGLU gate.
+//
+// Token generation streams every packed weight once per token and is bound
+// by memory bandwidth ("12 -- llama.cpp / GGUF", performance model; "Local
+// LLM inference": dequantize inside the dot product).  The work per weight
+// is kept small enough for the SMs to keep pace with HBM:
+//   * the dot products run on the fp16 warp MMA (qk_hunits.cuh): 16 rows x
+//     16 weights per instruction, codes converted to fp16 with one mask and
+//     one exact add per two weights, x held as two fp16 terms (hi + lo);
+//   * two CTAs per SM, each of eight consumer warps and one producer warp
+//     (more warps would not help: the decode is bound by the SM's integer,
+//     tensor and shared-memory pipes, not by latency);  A CTA owns
+//     a contiguous range of rows (of one matrix) and all of K.  The producer
+//     streams "stages" of 16 rows x 2048 weights into a shared-memory ring:
+//     one bulk async copy per row segment (its aligned-down 16-byte window;
+//     Q6_K rows of 11008 weights are 9030 bytes apart), completion counted on
+//     the stage's full mbarrier, release on its empty mbarrier.  Every wait
+//     is bounded in time.
+//   * consumer warp w decodes unit w (256 weights) of each stage for the 16
+//     rows, so the stage's K range is spread over the warps; stages go K
+//     chunk by K chunk over the CTA's row tiles, so that a warp keeps its
+//     unit of x in registers for all its tiles; partial sums of each row
+//     collect in shared memory and are added in a fixed order
+//     (deterministic);
+//   * x is converted in each CTA's shared memory after the grid-dependency
+//     wait (the previous kernel may produce it), while the producer already
+//     streams weights: no separate prep kernel runs between two GEMVs.
+#include <algorithm>
+
+#include "qk_formats.cuh"
+#include "qk_hunits.cuh"
+#include "qk_internal.h"
+#include "qk_ptx.cuh"
+
+namespace qk {
+namespace hg {
+using namespace hm;
+
+constexpr int kCW = 8;                      // consumer warps
+constexpr int kThreads = (kCW + 1) * 32;    // + one producer warp
+constexpr int kTileRows = 16;               // rows per MMA tile
+constexpr int kUnitW = 256;                 // weights per unit (16 rows x 256 weights: one warp's work item)
+constexpr int kXBB = 128;                   // prepared bytes per x-block: 2 planes x 8 words x 8 bytes
+constexpr int kMaxGroup = QK_GEMV_BATCH_MAX;
+constexpr int kMinStages = 2, kMaxStages = 8;
+
+struct Args {
+    const float* x;
+    int64_t cols;
+    uint32_t row_bytes;
+    int n;               // matrices (SwiGLU: 1, with W[1] the up matrix)
+    int nxb;             // x-blocks of x (cols / 32)
+    int nxb_pad;         // rounded up to whole units
+    int nunits;          // units per row
+    int nchunks;         // stages per row (per tile)
+    int stages;          // ring depth
+    uint32_t slot;       // bytes per row slot of a stage
+    uint32_t off_xb, off_xm, off_ring, off_bar, off_red;
+    unsigned* status;
+    const uint8_t* W[kMaxGroup];
+    float* y[kMaxGroup];
+    int64_t rows[kMaxGroup];
+    int64_t rows_q[kMaxGroup];   // rows / CTAs of the matrix
+    int rows_r[kMaxGroup];       // its first rows_r CTAs take one row more
+    int cta0[kMaxGroup + 1];
+};
+
+// x -> B fragments in shared memory.  x-block j (32 elements), plane h:
+//   xb[(2j + h) * 64 + 8i] = half2(x_h[4i], x_h[4i+2]), half2(x_h[4i+1], x_h[4i+3])
+// with x' = x * 2^-e, x_0 = fp16(x'), x_1 = fp16(x' - x_0); xm[j] = (sum of x
+// over the block, 2^e).  e = 0 unless max|x| of the block reaches 2^15, then
+// the block is scaled into [2^14, 2^15).  Four threads per block (eight
+// elements each); blocks past x are zero.
+__device__ __forceinline__ void prep_x(const float* __restrict__ x, int nxb, int nxb_pad, uint8_t* xb, float2* xm,
+                                       int ctid) {
+    const int q = ctid & 3;
+    for (int base = ctid & ~3; base < nxb_pad * 4; base += kCW * 32) {
+        const int j = (base >> 2);
+        float v[8];
+        if (j < nxb) {
+            const float4 u0 = __ldg(reinterpret_cast<const float4*>(x) + 8 * j + 2 * q);
+            const float4 u1 = __ldg(reinterpret_cast<const float4*>(x) + 8 * j + 2 * q + 1);
+            v[0] = u0.x; v[1] = u0.y; v[2] = u0.z; v[3] = u0.w;
+            v[4] = u1.x; v[5] = u1.y; v[6] = u1.z; v[7] = u1.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+        }
+        float amax = 0.0f, sum = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            amax = fmaxf(amax, fabsf(v[i]));
+            sum += v[i];
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        // Scale exponent: floor(log2 max|x|) - 14 when that is positive.
+        const int ex = (int)((__float_as_uint(amax) >> 23) & 255u) - 127;
+        const int e = max(0, ex - 14);
+        const float down = __uint_as_float((uint32_t)(127 - e) << 23), up = __uint_as_float((uint32_t)(127 + e) << 23);
+        uint32_t hi[8], lo[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float sv = v[i] * down;
+            const __half h = __float2half_rn(sv);
+            hi[i] = __half_as_ushort(h);
+            lo[i] = __half_as_ushort(__float2half_rn(sv - __half2float(h)));
+        }
+        // Words 2q and 2q+1: elements 8q + {0,2}, {1,3}, {4,6}, {5,7}.
+        *reinterpret_cast<uint4*>(xb + j * kXBB + 16 * q) =
+            make_uint4(hi[0] | hi[2] << 16, hi[1] | hi[3] << 16, hi[4] | hi[6] << 16, hi[5] | hi[7] << 16);
+        *reinterpret_cast<uint4*>(xb + j * kXBB + 64 + 16 * q) =
+            make_uint4(lo[0] | lo[2] << 16, lo[1] | lo[3] << 16, lo[4] | lo[6] << 16, lo[5] | lo[7] << 16);
+        if (q == 0) xm[j] = make_float2(sum, up);
+    }
+}
+
+__device__ __forceinline__ void named_sync_consumers() { asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory"); }
+
+// Bounded wait that also gives up when another warp of the CTA has already
+// given up (*abort set); on its own timeout it sets *abort and the status.
+// Between checks the warp is suspended by the hardware until the phase
+// completes (or a microsecond passes), so waiting warps take no issue slots
+// from the working ones.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, unsigned* status, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1; i < (1u << 24); ++i) {
+        if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > kWaitNs) break;
+    }
+    *abort = 1;
+    atomicOr(status, STATUS_TIMEOUT);
+    return false;
+}
+
+// SWI: one matrix pair (W[0] gate, W[1] up, same shape), y[0] = h =
+// SiLU(gate x) * (up x); each 16-row tile is walked through the gate matrix
+// and then the up matrix.
+//
+// Order of the work: K chunks outermost, row tiles inside, so that a warp's
+// B fragments (its unit of x) stay in registers for all the CTA's tiles of a
+// chunk.  Each warp adds its partial sums of a (tile, row) into shared memory
+// in chunk order; at the end the warps' partials of a row are added in warp
+// order.  The result does not depend on timing.
+template <int T, bool SWI>
+__global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
+    using U = HU<T>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+    uint64_t* empty = full + p.stages;
+    volatile int* abort = reinterpret_cast<volatile int*>(empty + p.stages);
+    float* part = reinterpret_cast<float*>(smem + p.off_red);   // [tile pass][kCW][16]
+    uint8_t* xb = smem + p.off_xb;
+    float2* xm = reinterpret_cast<float2*>(smem + p.off_xm);
+    uint8_t* ring = smem + p.off_ring;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // My matrix and rows.
+    const uint8_t* Wm = p.W[0];
+    float* ym = p.y[0];
+    int64_t rows = p.rows[0], rq = p.rows_q[0];
+    int rr = p.rows_r[0], bx = (int)blockIdx.x;
+#pragma unroll
+    for (int i = 1; i < kMaxGroup; ++i)
+        if (!SWI && i < p.n && (int)blockIdx.x >= p.cta0[i]) {
+            Wm = p.W[i];
+            ym = p.y[i];
+            rows = p.rows[i];
+            rq = p.rows_q[i];
+            rr = p.rows_r[i];
+            bx = (int)blockIdx.x - p.cta0[i];
+        }
+    const int64_t r_begin = bx * rq + min(bx, rr);
+    const int nrows = (int)(rq + (bx < rr ? 1 : 0));
+    const int ntiles = (nrows + kTileRows - 1) / kTileRows;
+    constexpr int npass = SWI ? 2 : 1;
+    const uint32_t rb = p.row_bytes;
+    const uint32_t CB = (uint32_t)kCW * U::UB;   // bytes of a full chunk (a multiple of 16)
+    const uint32_t stage_bytes = kTileRows * p.slot;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCW);
+        }
+        *abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == kCW) {
+        // ---------------- producer ----------------
+        const uint64_t pol = policy_evict_first();
+        const int64_t total16 = (rows * (int64_t)rb) & ~(int64_t)15;
+        int it = 0, s = 0;
+        uint32_t ph = 0;   // phase parity of stage s's barriers in this round of the ring
+        bool dead = false;
+        for (int c = 0; c < p.nchunks && !dead; ++c) {
+            const int64_t coff = (int64_t)c * CB;
+            const int64_t len = min((int64_t)CB, (int64_t)rb - coff);
+            for (int tile = 0; tile < ntiles && !dead; ++tile) {
+                const int nr = min(kTileRows, nrows - tile * kTileRows);
+                const int64_t off = (r_begin + tile * kTileRows + lane) * (int64_t)rb + coff;
+                for (int pass = 0; pass < npass; ++pass, ++it) {
+                    const uint8_t* Wp = (SWI && pass) ? p.W[1] : Wm;
+                    if (it >= p.stages && !wait_phase(&empty[s], ph ^ 1u, p.status, abort)) {
+                        dead = true;
+                        break;
+                    }
+                    uint8_t* st = ring + (uint32_t)s * stage_bytes;
+                    uint32_t bytes = 0;
+                    const int64_t a = off & ~(int64_t)15;
+                    if (lane < nr) {
+                        const int64_t e = min((off + len + 15) & ~(int64_t)15, total16);
+                        bytes = e > a ? (uint32_t)(e - a) : 0u;
+                        // Bytes past the last full 16 bytes of the matrix (its final row).
+                        for (int64_t b = max(off, total16); b < off + len; ++b) st[lane * p.slot + (uint32_t)(b - a)] = Wp[b];
+                    }
+                    uint32_t total = bytes;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_expect_tx(&full[s], total);
+                    __syncwarp();
+                    if (bytes) bulk_g2s(st + lane * p.slot, Wp + a, bytes, &full[s], pol);
+                    if (++s == p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+        }
+        if (dead) {
+            // Let the copies already requested land before the CTA exits.
+            for (int k = max(0, it - p.stages); k < it; ++k)
+                mbar_wait_bounded(&full[k % p.stages], (uint32_t)(k / p.stages) & 1u, p.status);
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    const int ctid = threadIdx.x;
+    const int g = lane >> 2, t = lane & 3;
+    const int npart = ntiles * npass * kCW * kTileRows;
+    for (int i = ctid; i < npart; i += kCW * 32) part[i] = 0.0f;
+    pdl_wait_prior();
+    prep_x(p.x, p.nxb, p.nxb_pad, xb, xm, ctid);
+    named_sync_consumers();
+    // B fragments: the thread whose column g belongs to its group t (g / 2 ==
+    // t) reads plane g % 2 of the group's x-blocks; every other thread
+    // supplies zeros.
+    const bool owner = (g >> 1) == t;
+    const int units_last = p.nunits - (p.nchunks - 1) * kCW;
+    int s = 0;
+    uint32_t ph = 0;
+    bool dead = false;
+    for (int c = 0; c < p.nchunks; ++c) {
+        const int u = c * kCW + warp;   // my unit of every row of the chunk
+        const bool act = warp < (c == p.nchunks - 1 ? units_last : kCW);
+        XB xb0 = {}, xb1 = {};
+        float2 xm0 = make_float2(0.0f, 0.0f), xm1 = xm0;
+        if (act) {
+            if (owner) {
+                load_xb(xb + ((u * 8 + U::X0(t)) * 2 + (g & 1)) * 64, xb0);
+                load_xb(xb + ((u * 8 + U::X1(t)) * 2 + (g & 1)) * 64, xb1);
+            }
+            xm0 = xm[u * 8 + U::X0(t)];
+            xm1 = xm[u * 8 + U::X1(t)];
+        }
+        const int nvb = min(8, p.nxb - 8 * u);
+        for (int tile = 0; tile < ntiles; ++tile) {
+            // Rows g and g + 8 start (row * row_bytes) mod 16 bytes into their
+            // slots (a chunk is a multiple of 16 bytes).
+            const int64_t rt0 = r_begin + tile * kTileRows;
+            const uint32_t o0 = g * p.slot + (uint32_t)(((rt0 + g) * (int64_t)rb) & 15) + warp * U::UB;
+            const uint32_t o1 = (g + 8) * p.slot + (uint32_t)(((rt0 + g + 8) * (int64_t)rb) & 15) + warp * U::UB;
+            for (int pass = 0; pass < npass; ++pass) {
+                if (!dead && !wait_phase(&full[s], ph, p.status, abort)) dead = true;
+                float y0 = 0.0f, y1 = 0.0f;
+                if (act && !dead) {
+                    const uint8_t* st = ring + (uint32_t)s * stage_bytes;
+                    U::unit(st + o0, st + o1, xb0, xb1, xm0, xm1, t, nvb, y0, y1);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                if (++s == p.stages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+                // Row sums of this unit: the four threads of a row.
+                y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
+                y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
+                y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
+                y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
+                if (t == 0 && act) {
+                    float* pp = part + ((tile * npass + pass) * kCW + warp) * kTileRows;
+                    pp[g] += y0;
+                    pp[g + 8] += y1;
+                }
+            }
+        }
+    }
+    named_sync_consumers();
+    if (dead) return;
+    for (int i = ctid; i < nrows; i += kCW * 32) {
+        const int tile = i / kTileRows, r = i % kTileRows;
+        const float* pp = part + tile * npass * kCW * kTileRows + r;
+        float v = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kCW; ++w) v += pp[w * kTileRows];
+        if (SWI) {   // h = SiLU(g) * u, SiLU(g) = g / (1 + e^-g)
+            float uu = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kCW; ++w) uu += pp[(kCW + w) * kTileRows];
+            v = v / (1.0f + expf(-v)) * uu;
+        }
+        ym[r_begin + i] = v;
+    }
+}
+
+}  // namespace hg
+
+namespace {
+
+bool hg_supported(int type) { return type == T_Q4_K || type == T_Q6_K || type == T_Q8_0; }
+
+int hg_block_bytes(int type) {
+    switch (type) {
+    case T_Q4_K: return 144;
+    case T_Q6_K: return 210;
+    case T_Q8_0: return 34;
+    case T_Q5_0: return 22;
+    case T_Q4_0: return 18;
+    case T_Q5_K: return 176;
+    case T_Q2_K: return 84;
+    case T_Q3_K: return 110;
+    }
+    return 0;
+}
+int hg_block_elems(int type) { return (type == T_Q8_0 || type == T_Q5_0 || type == T_Q4_0) ? 32 : 256; }
+
+// Two CTAs per SM: the rings of both (about 150 KB) keep enough copies in
+// flight to cover the loaded HBM latency (about 3 us), and when one CTA of
+// an SM finishes, the next launch's CTA (programmatic dependent launch)
+// takes its place and starts streaming while the other still runs.
+constexpr int64_t kSmemBudget = 113 * 1024;
+
+struct PlanH {
+    int grid = 0, stages = 0, nunits = 0, nchunks = 0, nxb = 0, nxb_pad = 0;
+    uint32_t slot = 0, off_xb = 0, off_xm = 0, off_ring = 0, off_bar = 0, off_red = 0, smem = 0;
+    int64_t rows_q[hg::kMaxGroup] = {}, rows_r[hg::kMaxGroup] = {};
+    int cta0[hg::kMaxGroup + 1] = {};
+};
+
+PlanH planh(int type, int n, const int64_t* rows, int64_t cols, int sms, bool swiglu) {
+    PlanH p;
+    if (!hg_supported(type) || n < 1 || n > hg::kMaxGroup || cols <= 0) return p;
+    int64_t total = 0;
+    for (int i = 0; i < n; ++i) total += std::max<int64_t>(rows[i], 0);
+    if (total == 0) return p;
+    const int BB = hg_block_bytes(type), BE = hg_block_elems(type);
+    p.nxb = (int)(cols / 32);
+    p.nunits = (int)((cols + hg::kUnitW - 1) / hg::kUnitW);
+    p.nxb_pad = p.nunits * 8;
+    const int64_t UB = (int64_t)(hg::kUnitW / BE) * BB;
+    // CTAs in proportion to each matrix's rows (at least one per non-empty
+    // matrix, at most one per row).
+    const int64_t G = 2 * (int64_t)std::max(sms, 1);
+    int64_t g0 = 0, per_cta = 0;
+    for (int i = 0; i < n; ++i) {
+        p.cta0[i] = (int)g0;
+        if (rows[i] <= 0) continue;
+        const int64_t g = std::max<int64_t>(1, std::min<int64_t>(rows[i], (G * rows[i] + total / 2) / total));
+        p.rows_q[i] = rows[i] / g;
+        p.rows_r[i] = rows[i] % g;
+        per_cta = std::max<int64_t>(per_cta, p.rows_q[i] + (p.rows_r[i] ? 1 : 0));
+        g0 += g;
+    }
+    for (int i = n; i <= hg::kMaxGroup; ++i) p.cta0[i] = (int)g0;
+    p.grid = (int)g0;
+    // Layout: B fragments and block sums of all of x, partial sums
+    // [tile pass][8 warps][16],
+    // mbarriers + abort word, ring.
+    const int64_t ntp = (per_cta + hg::kTileRows - 1) / hg::kTileRows * (swiglu ? 2 : 1);
+    const int64_t xbb = (int64_t)p.nxb_pad * hg::kXBB;
+    const int64_t xmb = (int64_t)p.nxb_pad * 8;
+    const int64_t redb = ntp * hg::kCW * hg::kTileRows * 4;
+    const int64_t barb = 2 * hg::kMaxStages * 8 + 16;
+    p.off_xb = 0;
+    p.off_xm = (uint32_t)xbb;
+    p.off_red = (uint32_t)(xbb + xmb);
+    p.off_bar = (uint32_t)((p.off_red + redb + 15) & ~(int64_t)15);
+    p.off_ring = (uint32_t)((p.off_bar + barb + 127) & ~(int64_t)127);
+    const int64_t CB = hg::kCW * UB;
+    // Room for the alignment remainder and word reads past the end, and a
+    // stride of 16 mod 32 bytes: the 16-byte code loads of rows g and g + 1
+    // then fall in different shared-memory banks.
+    uint32_t slot = (uint32_t)(((CB + 15 + 15) & ~(int64_t)15) + 16);
+    if (slot % 32 == 0) slot += 16;
+    const int64_t stage = (int64_t)hg::kTileRows * slot;
+    const int64_t ns = (kSmemBudget - p.off_ring) / stage;
+    if (ns < hg::kMinStages) return PlanH{};
+    p.slot = slot;
+    p.nchunks = (p.nunits + hg::kCW - 1) / hg::kCW;
+    p.stages = (int)std::min<int64_t>(ns, hg::kMaxStages);
+    p.smem = (uint32_t)(p.off_ring + p.stages * stage);
+    return p;
+}
+
+template <int T, bool SWI>
+cudaError_t launch_h_t(const hg::Args& a, const PlanH& pl, cudaStream_t s) {
+    auto kern = hg::hgemv_kernel<T, SWI>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid);
+    cfg.blockDim = dim3(hg::kThreads);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <bool SWI>
+cudaError_t launch_h_type(int type, const hg::Args& a, const PlanH& pl, cudaStream_t s) {
+    switch (type) {
+    case T_Q4_K: return launch_h_t<T_Q4_K, SWI>(a, pl, s);
+    case T_Q6_K: return launch_h_t<T_Q6_K, SWI>(a, pl, s);
+    case T_Q8_0: return launch_h_t<T_Q8_0, SWI>(a, pl, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+hg::Args make_args(int type, const PlanH& pl, int64_t cols, const float* x, unsigned* status) {
+    hg::Args a = {};
+    a.x = x;
+    a.cols = cols;
+    a.row_bytes = (uint32_t)(cols / hg_block_elems(type) * hg_block_bytes(type));
+    a.nxb = pl.nxb;
+    a.nxb_pad = pl.nxb_pad;
+    a.nunits = pl.nunits;
+    a.nchunks = pl.nchunks;
+    a.stages = pl.stages;
+    a.slot = pl.slot;
+    a.off_xb = pl.off_xb;
+    a.off_xm = pl.off_xm;
+    a.off_ring = pl.off_ring;
+    a.off_bar = pl.off_bar;
+    a.off_red = pl.off_red;
+    a.status = status;
+    for (int i = 0; i <= hg::kMaxGroup; ++i) a.cta0[i] = pl.cta0[i];
+    return a;
+}
+}  // namespace
+
+bool hgemv_ok(int type, int n, const int64_t* rows, int64_t cols, int sms) {
+    return planh(type, n, rows, cols, sms, false).stages > 0;
+}
+
+cudaError_t launch_hgemv(int type, int n, const uint8_t* const* W, const int64_t* rows, int64_t cols, const float* x,
+                         float* const* y, int sms, unsigned* status, cudaStream_t s) {
+    const PlanH pl = planh(type, n, rows, cols, sms, false);
+    if (pl.stages == 0) return cudaErrorInvalidValue;
+    if (pl.grid == 0) return cudaSuccess;
+    hg::Args a = make_args(type, pl, cols, x, status);
+    a.n = n;
+    for (int i = 0; i < n; ++i) {
+        a.W[i] = W[i];
+        a.y[i] = y[i];
+        a.rows[i] = rows[i];
+        a.rows_q[i] = pl.rows_q[i];
+        a.rows_r[i] = (int)pl.rows_r[i];
+    }
+    return launch_h_type<false>(type, a, pl, s);
+}
+
+cudaError_t launch_hgemv_swiglu(int type, const uint8_t* Wg, const uint8_t* Wu, int64_t rows, int64_t cols,
+                                const float* x, float* h, int sms, unsigned* status, cudaStream_t s) {
+    const PlanH pl = planh(type, 1, &rows, cols, sms, true);
+    if (pl.stages == 0) return cudaErrorInvalidValue;
+    if (pl.grid == 0) return cudaSuccess;
+    hg::Args a = make_args(type, pl, cols, x, status);
+    a.n = 1;
+    a.W[0] = Wg;
+    a.W[1] = Wu;
+    a.y[0] = h;
+    a.rows[0] = rows;
+    a.rows_q[0] = pl.rows_q[0];
+    a.rows_r[0] = (int)pl.rows_r[0];
+    return launch_h_type<true>(type, a, pl, s);
+}
+
+}  // namespace qk

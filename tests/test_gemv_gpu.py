@@ -93,9 +93,13 @@ def test_linearity_and_batch_rows(gpu):
     W = dev_u8(synth.random_blocks(name, rows, cols, 91), gpu)
     x = synth.activations(4, cols, 92)
     Y = qk.gemv(t, W, rows, cols, dev_f32(x, gpu)).cpu().numpy()
+    _, S4 = oracle.gemv(t, W.cpu().numpy(), rows, cols, x)
     for m in range(4):
+        # A single row may run on another kernel than the batch (decode
+        # kernel vs tiled kernel): each result is within its own bound of the
+        # exact product, so the two differ by at most the sum of the bounds.
         y1 = qk.gemv(t, W, rows, cols, dev_f32(x[m:m + 1], gpu)).cpu().numpy()[0]
-        assert np.allclose(Y[m], y1, rtol=1e-5, atol=1e-5)
+        assert np.all(np.abs(Y[m] - y1) <= 2e-4 * S4[m] + 2e-6)
     # Linearity, within the sum of the three results' error bounds.
     a, b = 0.5, -2.0
     yc = qk.gemv(t, W, rows, cols, dev_f32(a * x[0:1] + b * x[1:2], gpu)).cpu().numpy()[0]
