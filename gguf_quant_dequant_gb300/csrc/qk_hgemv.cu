@@ -70,10 +70,10 @@ struct Args {
 // x -> B fragments in shared memory.  x-block j (32 elements), plane h:
 //   xb[(2j + h) * 64 + 8i] = half2(x_h[4i], x_h[4i+2]), half2(x_h[4i+1], x_h[4i+3])
 // with x' = x * 2^-e, x_0 = fp16(x'), x_1 = fp16(x' - x_0); xm[j] = (sum of x
-// over the block, 2^e).  e = 0 unless max|x| of the block reaches 2^15, then
+// over the block, 2^e, sum over its first 16 elements, over its last 16).  e = 0 unless max|x| of the block reaches 2^15, then
 // the block is scaled into [2^14, 2^15).  Four threads per block (eight
 // elements each); blocks past x are zero.
-__device__ __forceinline__ void prep_x(const float* __restrict__ x, int nxb, int nxb_pad, uint8_t* xb, float2* xm,
+__device__ __forceinline__ void prep_x(const float* __restrict__ x, int nxb, int nxb_pad, uint8_t* xb, float4* xm,
                                        int ctid) {
     const int q = ctid & 3;
     for (int base = ctid & ~3; base < nxb_pad * 4; base += kCW * 32) {
@@ -96,8 +96,8 @@ __device__ __forceinline__ void prep_x(const float* __restrict__ x, int nxb, int
         }
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);           // sum of 16 elements (one half)
+        const float other = __shfl_xor_sync(0xffffffffu, sum, 2);
         // Scale exponent: floor(log2 max|x|) - 14 when that is positive.
         const int ex = (int)((__float_as_uint(amax) >> 23) & 255u) - 127;
         const int e = max(0, ex - 14);
@@ -115,7 +115,7 @@ __device__ __forceinline__ void prep_x(const float* __restrict__ x, int nxb, int
             make_uint4(hi[0] | hi[2] << 16, hi[1] | hi[3] << 16, hi[4] | hi[6] << 16, hi[5] | hi[7] << 16);
         *reinterpret_cast<uint4*>(xb + j * kXBB + 64 + 16 * q) =
             make_uint4(lo[0] | lo[2] << 16, lo[1] | lo[3] << 16, lo[4] | lo[6] << 16, lo[5] | lo[7] << 16);
-        if (q == 0) xm[j] = make_float2(sum, up);
+        if (q == 0) xm[j] = make_float4(sum + other, up, sum, other);
     }
 }
 
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
     volatile int* abort = reinterpret_cast<volatile int*>(empty + p.stages);
     float* part = reinterpret_cast<float*>(smem + p.off_red);   // [tile pass][kCW][16]
     uint8_t* xb = smem + p.off_xb;
-    float2* xm = reinterpret_cast<float2*>(smem + p.off_xm);
+    float4* xm = reinterpret_cast<float4*>(smem + p.off_xm);
     uint8_t* ring = smem + p.off_ring;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
         const int u = c * kCW + warp;   // my unit of every row of the chunk
         const bool act = warp < (c == p.nchunks - 1 ? units_last : kCW);
         XB xb0 = {}, xb1 = {};
-        float2 xm0 = make_float2(0.0f, 0.0f), xm1 = xm0;
+        float4 xm0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), xm1 = xm0;
         if (act) {
             if (owner) {
                 load_xb(xb + ((u * 8 + U::X0(t)) * 2 + (g & 1)) * 64, xb0);
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
 
 namespace {
 
-bool hg_supported(int type) { return type == T_Q4_K || type == T_Q6_K || type == T_Q8_0; }
+bool hg_supported(int type) { return type >= T_Q4_K && type <= T_Q3_K; }
 
 int hg_block_bytes(int type) {
     switch (type) {
@@ -390,7 +390,7 @@ PlanH planh(int type, int n, const int64_t* rows, int64_t cols, int sms, bool sw
     // mbarriers + abort word, ring.
     const int64_t ntp = (per_cta + hg::kTileRows - 1) / hg::kTileRows * (swiglu ? 2 : 1);
     const int64_t xbb = (int64_t)p.nxb_pad * hg::kXBB;
-    const int64_t xmb = (int64_t)p.nxb_pad * 8;
+    const int64_t xmb = (int64_t)p.nxb_pad * 16;
     const int64_t redb = ntp * hg::kCW * hg::kTileRows * 4;
     const int64_t barb = 2 * hg::kMaxStages * 8 + 16;
     p.off_xb = 0;
@@ -438,6 +438,11 @@ cudaError_t launch_h_type(int type, const hg::Args& a, const PlanH& pl, cudaStre
     case T_Q4_K: return launch_h_t<T_Q4_K, SWI>(a, pl, s);
     case T_Q6_K: return launch_h_t<T_Q6_K, SWI>(a, pl, s);
     case T_Q8_0: return launch_h_t<T_Q8_0, SWI>(a, pl, s);
+    case T_Q5_0: return launch_h_t<T_Q5_0, SWI>(a, pl, s);
+    case T_Q4_0: return launch_h_t<T_Q4_0, SWI>(a, pl, s);
+    case T_Q5_K: return launch_h_t<T_Q5_K, SWI>(a, pl, s);
+    case T_Q2_K: return launch_h_t<T_Q2_K, SWI>(a, pl, s);
+    case T_Q3_K: return launch_h_t<T_Q3_K, SWI>(a, pl, s);
     }
     return cudaErrorInvalidValue;
 }
