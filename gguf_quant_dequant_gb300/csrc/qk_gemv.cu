@@ -344,11 +344,18 @@ int64_t nst_for(int type, int64_t cols) {
 int64_t align16(int64_t v) { return (v + 15) & ~(int64_t)15; }
 }  // namespace
 
+// Activation rows up to which qk_gemv runs the tensor-core kernel (two rows
+// per launch, weights streamed once per launch); beyond, the tiled kernel
+// (weights decoded once per tile of up to four rows, prepped x in the
+// workspace).
+constexpr int64_t kTcMaxM = 64;
+
 GemvPlan plan_gemv(int type, int64_t rows, int64_t cols, int64_t M, int sm_count) {
     GemvPlan pl;
     pl.sms = sm_count;
-    if (M == 1 && hgemv_ok(type, 1, &rows, cols, sm_count)) {   // tensor-core decode kernel, prep inside
-        pl.decode = pl.tc = true;
+    if (M <= kTcMaxM && hgemv_ok(type, 1, &rows, cols, sm_count)) {   // tensor-core kernel, prep inside
+        pl.decode = M == 1;
+        pl.tc = true;
         return pl;
     }
     if (M == 1 && gemv5_ring_pairs(type, 1, &rows, cols, sm_count) > 0) {   // decode kernel, prep inside
@@ -404,7 +411,8 @@ static cudaError_t launch_mt(const GemvPlan& pl, const gv::Args& a, cudaStream_t
 
 cudaError_t launch_gemv(int type, const GemvPlan& pl, const uint8_t* W, int64_t rows, int64_t cols, const float* x,
                         int64_t M, float* y, float* ws, unsigned* status, cudaStream_t s) {
-    if (pl.decode && pl.tc) return launch_hgemv(type, 1, &W, &rows, cols, x, &y, pl.sms, status, s);
+    if (pl.tc && M == 1) return launch_hgemv(type, 1, &W, &rows, cols, x, &y, pl.sms, status, s);
+    if (pl.tc) return launch_hgemv_tokens(type, W, rows, cols, x, M, y, pl.sms, status, s);
     if (pl.decode) return launch_gemv5(type, 1, &W, &rows, cols, x, &y, pl.sms, s);
     gv::Args a = {};
     a.W = W;

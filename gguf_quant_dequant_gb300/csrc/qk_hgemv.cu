@@ -28,6 +28,7 @@
 //     wait (the previous kernel may produce it), while the producer already
 //     streams weights: no separate prep kernel runs between two GEMVs.
 #include <algorithm>
+#include <type_traits>
 
 #include "qk_formats.cuh"
 #include "qk_hunits.cuh"
@@ -51,6 +52,7 @@ struct Args {
     int64_t cols;
     uint32_t row_bytes;
     int n;               // matrices (SwiGLU: 1, with W[1] the up matrix)
+    int64_t ystride;     // elements between the outputs of consecutive tokens (MT > 1)
     int nxb;             // x-blocks of x (cols / 32)
     int nxb_pad;         // rounded up to whole units
     int nunits;          // units per row
@@ -58,6 +60,7 @@ struct Args {
     int stages;          // ring depth
     uint32_t slot;       // bytes per row slot of a stage
     uint32_t off_xb, off_xm, off_ring, off_bar, off_red;
+    uint32_t xtok;       // bytes of one token's B fragments (then its block sums follow the same stride / 8)
     unsigned* status;
     const uint8_t* W[kMaxGroup];
     float* y[kMaxGroup];
@@ -148,14 +151,15 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, unsig
 // chunk.  Each warp adds its partial sums of a (tile, row) into shared memory
 // in chunk order; at the end the warps' partials of a row are added in warp
 // order.  The result does not depend on timing.
-template <int T, bool SWI>
+template <int T, int MT, bool SWI>
 __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
+    static_assert(!SWI || MT == 1, "the SwiGLU form takes one activation row");
     using U = HU<T>;
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     uint64_t* empty = full + p.stages;
     volatile int* abort = reinterpret_cast<volatile int*>(empty + p.stages);
-    float* part = reinterpret_cast<float*>(smem + p.off_red);   // [tile pass][kCW][16]
+    float* part = reinterpret_cast<float*>(smem + p.off_red);   // [tile pass][token][kCW][16]
     uint8_t* xb = smem + p.off_xb;
     float4* xm = reinterpret_cast<float4*>(smem + p.off_xm);
     uint8_t* ring = smem + p.off_ring;
@@ -248,10 +252,12 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
     // ---------------- consumers ----------------
     const int ctid = threadIdx.x;
     const int g = lane >> 2, t = lane & 3;
-    const int npart = ntiles * npass * kCW * kTileRows;
+    const int npart = ntiles * npass * MT * kCW * kTileRows;
     for (int i = ctid; i < npart; i += kCW * 32) part[i] = 0.0f;
     pdl_wait_prior();
-    prep_x(p.x, p.nxb, p.nxb_pad, xb, xm, ctid);
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+        prep_x(p.x + (int64_t)m * p.cols, p.nxb, p.nxb_pad, xb + m * p.xtok, xm + m * p.nxb_pad, ctid);
     named_sync_consumers();
     // B fragments: the thread whose column g belongs to its group t (g / 2 ==
     // t) reads plane g % 2 of the group's x-blocks; every other thread
@@ -264,15 +270,33 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
     for (int c = 0; c < p.nchunks; ++c) {
         const int u = c * kCW + warp;   // my unit of every row of the chunk
         const bool act = warp < (c == p.nchunks - 1 ? units_last : kCW);
-        XB xb0 = {}, xb1 = {};
-        float4 xm0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), xm1 = xm0;
+        // One token: its B fragments for the chunk in registers; more: read
+        // from shared memory step by step.
+        using BP = typename std::conditional<MT == 1, BRegs, BSmem<MT>>::type;
+        BP bp = {};
+        float4 xm0[MT], xm1[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) xm0[m] = xm1[m] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         if (act) {
-            if (owner) {
-                load_xb(xb + ((u * 8 + U::X0(t)) * 2 + (g & 1)) * 64, xb0);
-                load_xb(xb + ((u * 8 + U::X1(t)) * 2 + (g & 1)) * 64, xb1);
+            const uint32_t o0 = ((u * 8 + U::X0(t)) * 2 + (g & 1)) * 64, o1 = ((u * 8 + U::X1(t)) * 2 + (g & 1)) * 64;
+            if constexpr (MT == 1) {
+                if (owner) {
+                    load_xb(xb + o0, bp.x0);
+                    load_xb(xb + o1, bp.x1);
+                }
+            } else {
+                bp.own = owner;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    bp.p[m][0] = xb + m * p.xtok + o0;
+                    bp.p[m][1] = xb + m * p.xtok + o1;
+                }
             }
-            xm0 = xm[u * 8 + U::X0(t)];
-            xm1 = xm[u * 8 + U::X1(t)];
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                xm0[m] = xm[m * p.nxb_pad + u * 8 + U::X0(t)];
+                xm1[m] = xm[m * p.nxb_pad + u * 8 + U::X1(t)];
+            }
         }
         const int nvb = min(8, p.nxb - 8 * u);
         for (int tile = 0; tile < ntiles; ++tile) {
@@ -283,10 +307,12 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
             const uint32_t o1 = (g + 8) * p.slot + (uint32_t)(((rt0 + g + 8) * (int64_t)rb) & 15) + warp * U::UB;
             for (int pass = 0; pass < npass; ++pass) {
                 if (!dead && !wait_phase(&full[s], ph, p.status, abort)) dead = true;
-                float y0 = 0.0f, y1 = 0.0f;
+                float y0[MT], y1[MT];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) y0[m] = y1[m] = 0.0f;
                 if (act && !dead) {
                     const uint8_t* st = ring + (uint32_t)s * stage_bytes;
-                    U::unit(st + o0, st + o1, xb0, xb1, xm0, xm1, t, nvb, y0, y1);
+                    run_unit<T, MT>(st + o0, st + o1, bp, xm0, xm1, t, nvb, y0, y1);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
@@ -295,23 +321,28 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
                     ph ^= 1u;
                 }
                 // Row sums of this unit: the four threads of a row.
-                y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
-                y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
-                y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
-                y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
-                if (t == 0 && act) {
-                    float* pp = part + ((tile * npass + pass) * kCW + warp) * kTileRows;
-                    pp[g] += y0;
-                    pp[g + 8] += y1;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    float a = y0[m], b = y1[m];
+                    a += __shfl_xor_sync(0xffffffffu, a, 1);
+                    a += __shfl_xor_sync(0xffffffffu, a, 2);
+                    b += __shfl_xor_sync(0xffffffffu, b, 1);
+                    b += __shfl_xor_sync(0xffffffffu, b, 2);
+                    if (t == 0 && act) {
+                        float* pp = part + (((tile * npass + pass) * MT + m) * kCW + warp) * kTileRows;
+                        pp[g] += a;
+                        pp[g + 8] += b;
+                    }
                 }
             }
         }
     }
     named_sync_consumers();
     if (dead) return;
-    for (int i = ctid; i < nrows; i += kCW * 32) {
-        const int tile = i / kTileRows, r = i % kTileRows;
-        const float* pp = part + tile * npass * kCW * kTileRows + r;
+    for (int i = ctid; i < nrows * MT; i += kCW * 32) {
+        const int m = i / nrows, ri = i - m * nrows;
+        const int tile = ri / kTileRows, r = ri % kTileRows;
+        const float* pp = part + ((tile * npass) * MT + m) * kCW * kTileRows + r;
         float v = 0.0f;
 #pragma unroll
         for (int w = 0; w < kCW; ++w) v += pp[w * kTileRows];
@@ -321,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
             for (int w = 0; w < kCW; ++w) uu += pp[(kCW + w) * kTileRows];
             v = v / (1.0f + expf(-v)) * uu;
         }
-        ym[r_begin + i] = v;
+        ym[(int64_t)m * p.ystride + r_begin + ri] = v;
     }
 }
 
@@ -354,14 +385,15 @@ constexpr int64_t kSmemBudget = 113 * 1024;
 
 struct PlanH {
     int grid = 0, stages = 0, nunits = 0, nchunks = 0, nxb = 0, nxb_pad = 0;
-    uint32_t slot = 0, off_xb = 0, off_xm = 0, off_ring = 0, off_bar = 0, off_red = 0, smem = 0;
+    uint32_t slot = 0, off_xb = 0, off_xm = 0, off_ring = 0, off_bar = 0, off_red = 0, smem = 0, xtok = 0;
     int64_t rows_q[hg::kMaxGroup] = {}, rows_r[hg::kMaxGroup] = {};
     int cta0[hg::kMaxGroup + 1] = {};
 };
 
-PlanH planh(int type, int n, const int64_t* rows, int64_t cols, int sms, bool swiglu) {
+// mt = activation rows (tokens) per launch; swiglu = the two-pass form.
+PlanH planh(int type, int n, const int64_t* rows, int64_t cols, int sms, int mt, bool swiglu) {
     PlanH p;
-    if (!hg_supported(type) || n < 1 || n > hg::kMaxGroup || cols <= 0) return p;
+    if (!hg_supported(type) || n < 1 || n > hg::kMaxGroup || cols <= 0 || mt < 1) return p;
     int64_t total = 0;
     for (int i = 0; i < n; ++i) total += std::max<int64_t>(rows[i], 0);
     if (total == 0) return p;
@@ -369,7 +401,6 @@ PlanH planh(int type, int n, const int64_t* rows, int64_t cols, int sms, bool sw
     p.nxb = (int)(cols / 32);
     p.nunits = (int)((cols + hg::kUnitW - 1) / hg::kUnitW);
     p.nxb_pad = p.nunits * 8;
-    const int64_t UB = (int64_t)(hg::kUnitW / BE) * BB;
     // CTAs in proportion to each matrix's rows (at least one per non-empty
     // matrix, at most one per row).
     const int64_t G = 2 * (int64_t)std::max(sms, 1);
@@ -385,19 +416,20 @@ PlanH planh(int type, int n, const int64_t* rows, int64_t cols, int sms, bool sw
     }
     for (int i = n; i <= hg::kMaxGroup; ++i) p.cta0[i] = (int)g0;
     p.grid = (int)g0;
-    // Layout: B fragments and block sums of all of x, partial sums
-    // [tile pass][8 warps][16],
-    // mbarriers + abort word, ring.
+    // Layout: B fragments of each token, block sums of each token, partial
+    // sums [tile pass][token][8 warps][16], mbarriers + abort word, ring.
     const int64_t ntp = (per_cta + hg::kTileRows - 1) / hg::kTileRows * (swiglu ? 2 : 1);
-    const int64_t xbb = (int64_t)p.nxb_pad * hg::kXBB;
-    const int64_t xmb = (int64_t)p.nxb_pad * 16;
-    const int64_t redb = ntp * hg::kCW * hg::kTileRows * 4;
+    p.xtok = (uint32_t)((int64_t)p.nxb_pad * hg::kXBB);
+    const int64_t xbb = (int64_t)mt * p.xtok;
+    const int64_t xmb = (int64_t)mt * p.nxb_pad * 16;
+    const int64_t redb = ntp * mt * hg::kCW * hg::kTileRows * 4;
     const int64_t barb = 2 * hg::kMaxStages * 8 + 16;
     p.off_xb = 0;
     p.off_xm = (uint32_t)xbb;
     p.off_red = (uint32_t)(xbb + xmb);
     p.off_bar = (uint32_t)((p.off_red + redb + 15) & ~(int64_t)15);
     p.off_ring = (uint32_t)((p.off_bar + barb + 127) & ~(int64_t)127);
+    const int64_t UB = (int64_t)(hg::kUnitW / BE) * BB;
     const int64_t CB = hg::kCW * UB;
     // Room for the alignment remainder and word reads past the end, and a
     // stride of 16 mod 32 bytes: the 16-byte code loads of rows g and g + 1
@@ -414,9 +446,9 @@ PlanH planh(int type, int n, const int64_t* rows, int64_t cols, int sms, bool sw
     return p;
 }
 
-template <int T, bool SWI>
+template <int T, int MT, bool SWI>
 cudaError_t launch_h_t(const hg::Args& a, const PlanH& pl, cudaStream_t s) {
-    auto kern = hg::hgemv_kernel<T, SWI>;
+    auto kern = hg::hgemv_kernel<T, MT, SWI>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -432,17 +464,17 @@ cudaError_t launch_h_t(const hg::Args& a, const PlanH& pl, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <bool SWI>
+template <int MT, bool SWI>
 cudaError_t launch_h_type(int type, const hg::Args& a, const PlanH& pl, cudaStream_t s) {
     switch (type) {
-    case T_Q4_K: return launch_h_t<T_Q4_K, SWI>(a, pl, s);
-    case T_Q6_K: return launch_h_t<T_Q6_K, SWI>(a, pl, s);
-    case T_Q8_0: return launch_h_t<T_Q8_0, SWI>(a, pl, s);
-    case T_Q5_0: return launch_h_t<T_Q5_0, SWI>(a, pl, s);
-    case T_Q4_0: return launch_h_t<T_Q4_0, SWI>(a, pl, s);
-    case T_Q5_K: return launch_h_t<T_Q5_K, SWI>(a, pl, s);
-    case T_Q2_K: return launch_h_t<T_Q2_K, SWI>(a, pl, s);
-    case T_Q3_K: return launch_h_t<T_Q3_K, SWI>(a, pl, s);
+    case T_Q4_K: return launch_h_t<T_Q4_K, MT, SWI>(a, pl, s);
+    case T_Q6_K: return launch_h_t<T_Q6_K, MT, SWI>(a, pl, s);
+    case T_Q8_0: return launch_h_t<T_Q8_0, MT, SWI>(a, pl, s);
+    case T_Q5_0: return launch_h_t<T_Q5_0, MT, SWI>(a, pl, s);
+    case T_Q4_0: return launch_h_t<T_Q4_0, MT, SWI>(a, pl, s);
+    case T_Q5_K: return launch_h_t<T_Q5_K, MT, SWI>(a, pl, s);
+    case T_Q2_K: return launch_h_t<T_Q2_K, MT, SWI>(a, pl, s);
+    case T_Q3_K: return launch_h_t<T_Q3_K, MT, SWI>(a, pl, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -463,6 +495,7 @@ hg::Args make_args(int type, const PlanH& pl, int64_t cols, const float* x, unsi
     a.off_ring = pl.off_ring;
     a.off_bar = pl.off_bar;
     a.off_red = pl.off_red;
+    a.xtok = pl.xtok;
     a.status = status;
     for (int i = 0; i <= hg::kMaxGroup; ++i) a.cta0[i] = pl.cta0[i];
     return a;
@@ -470,12 +503,12 @@ hg::Args make_args(int type, const PlanH& pl, int64_t cols, const float* x, unsi
 }  // namespace
 
 bool hgemv_ok(int type, int n, const int64_t* rows, int64_t cols, int sms) {
-    return planh(type, n, rows, cols, sms, false).stages > 0;
+    return planh(type, n, rows, cols, sms, 1, false).stages > 0;
 }
 
 cudaError_t launch_hgemv(int type, int n, const uint8_t* const* W, const int64_t* rows, int64_t cols, const float* x,
                          float* const* y, int sms, unsigned* status, cudaStream_t s) {
-    const PlanH pl = planh(type, n, rows, cols, sms, false);
+    const PlanH pl = planh(type, n, rows, cols, sms, 1, false);
     if (pl.stages == 0) return cudaErrorInvalidValue;
     if (pl.grid == 0) return cudaSuccess;
     hg::Args a = make_args(type, pl, cols, x, status);
@@ -487,12 +520,35 @@ cudaError_t launch_hgemv(int type, int n, const uint8_t* const* W, const int64_t
         a.rows_q[i] = pl.rows_q[i];
         a.rows_r[i] = (int)pl.rows_r[i];
     }
-    return launch_h_type<false>(type, a, pl, s);
+    return launch_h_type<1, false>(type, a, pl, s);
+}
+
+cudaError_t launch_hgemv_tokens(int type, const uint8_t* W, int64_t rows, int64_t cols, const float* x, int64_t M,
+                                float* y, int sms, unsigned* status, cudaStream_t s) {
+    // Two activation rows per launch (the fp16 code conversion of a weight
+    // is shared by both), one for an odd last row.
+    for (int64_t m0 = 0; m0 < M;) {
+        const int mt = (M - m0 >= 2 && planh(type, 1, &rows, cols, sms, 2, false).stages > 0) ? 2 : 1;
+        const PlanH pl = planh(type, 1, &rows, cols, sms, mt, false);
+        if (pl.stages == 0) return cudaErrorInvalidValue;
+        hg::Args a = make_args(type, pl, cols, x + m0 * cols, status);
+        a.n = 1;
+        a.ystride = rows;
+        a.W[0] = W;
+        a.y[0] = y + m0 * rows;
+        a.rows[0] = rows;
+        a.rows_q[0] = pl.rows_q[0];
+        a.rows_r[0] = (int)pl.rows_r[0];
+        const cudaError_t e = mt == 2 ? launch_h_type<2, false>(type, a, pl, s) : launch_h_type<1, false>(type, a, pl, s);
+        if (e != cudaSuccess) return e;
+        m0 += mt;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_hgemv_swiglu(int type, const uint8_t* Wg, const uint8_t* Wu, int64_t rows, int64_t cols,
                                 const float* x, float* h, int sms, unsigned* status, cudaStream_t s) {
-    const PlanH pl = planh(type, 1, &rows, cols, sms, true);
+    const PlanH pl = planh(type, 1, &rows, cols, sms, 1, true);
     if (pl.stages == 0) return cudaErrorInvalidValue;
     if (pl.grid == 0) return cudaSuccess;
     hg::Args a = make_args(type, pl, cols, x, status);
@@ -503,7 +559,7 @@ cudaError_t launch_hgemv_swiglu(int type, const uint8_t* Wg, const uint8_t* Wu, 
     a.rows[0] = rows;
     a.rows_q[0] = pl.rows_q[0];
     a.rows_r[0] = (int)pl.rows_r[0];
-    return launch_h_type<true>(type, a, pl, s);
+    return launch_h_type<1, true>(type, a, pl, s);
 }
 
 }  // namespace qk

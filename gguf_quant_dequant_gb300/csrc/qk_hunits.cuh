@@ -116,11 +116,18 @@ __device__ __forceinline__ void load_xb(const uint8_t* p, XB& x) {
     }
 }
 
-// Every unit decoder takes the unit's bytes of rows g (r0) and g + 8 (r1),
-// the B fragments of the thread's x-blocks (zero unless the thread owns the
-// B column), the sums and scales of its group's x-blocks, its group t, and
-// nvb = the blocks of 32 weights present in the unit (8 except in a short
-// last unit of the 32-weight types), and adds its rows' sums to y0, y1.
+// Every unit decoder HU<T> provides:
+//   Ctx                        the unit's code words and scales of rows g, g + 8
+//   load(ctx, r0, r1, t)       read them from the unit's bytes of the two rows
+//   conv(ctx, i, t, A)         A fragments of step i: A[0..3] for x-block X0
+//                              (row g bytes 0/2, row g+8 bytes 0/2, row g
+//                              bytes 1/3, row g+8 bytes 1/3), A[4..7] for X1
+//   epi(ctx, c, xm0, xm1, t, nvb, y0, y1)   scale the accumulators of one
+//                              token (c[0..1] X0, c[2..3] X1: the two halves
+//                              of each x-block for the 16-weight-group types,
+//                              even / odd steps otherwise) and add the rows'
+//                              sums; nvb = blocks of 32 weights present in
+//                              the unit (8 except in a short last unit).
 
 // Row sums of one unit for rows g and g + 8: C columns (hi, lo) of group t.
 __device__ __forceinline__ float csum_g(const float (&c)[4]) { return c[0] + c[1]; }
@@ -155,6 +162,7 @@ template <int T> struct HU;
 // (x-block X0 = 2t), high nibbles sub-block 2t+1 (X1 = 2t+1).
 template <> struct HU<T_Q4_K> {
     static constexpr int UB = 144;   // bytes per unit per row
+    static constexpr bool kGroup16 = false;
     __device__ static __forceinline__ int X0(int t) { return 2 * t; }
     __device__ static __forceinline__ int X1(int t) { return 2 * t + 1; }
     // [sc(2t), sc(2t+1), m(2t), m(2t+1)] as bytes, from the 12 scale bytes
@@ -169,50 +177,59 @@ template <> struct HU<T_Q4_K> {
         return t >= 2 ? split : (p & 0x3F3F3F3Fu);
     }
     struct Row {
-        uint32_t clo, chi;   // half2 offsets -(1024 + o_lo), -(64 + o_hi)
+        uint32_t clo, chi;   // half2 offsets -(magic + o) of the low and high nibble codes
         float ds_lo, ds_hi, r_lo, r_hi;
     };
-    __device__ static __forceinline__ Row row_params(const uint4& h, int t) {
+    // The per-sub-block factors d*sc and dmin*m, the nearest code o of their
+    // ratio and the residual r = dmin*m - d*sc*o; the high codes use magic
+    // 64 (hi_magic64) or 1024 (codes moved down first, as Q5_K's).
+    template <bool hi_magic64>
+    __device__ static __forceinline__ Row row_params(const uint4& h, int t, float qmax) {
         const uint32_t f = fields(h, t);
         const float d = h2f(h.x & 0xFFFFu), dmin = h2f(h.x >> 16);
         Row r;
         r.ds_lo = d * ubyte_f(f, 0);
         r.ds_hi = d * ubyte_f(f, 1);
         const float dm_lo = dmin * ubyte_f(f, 2), dm_hi = dmin * ubyte_f(f, 3);
-        const float m_lo = nearest_code_m(dm_lo, r.ds_lo, 15.0f), m_hi = nearest_code_m(dm_hi, r.ds_hi, 15.0f);
+        const float m_lo = nearest_code_m(dm_lo, r.ds_lo, qmax), m_hi = nearest_code_m(dm_hi, r.ds_hi, qmax);
         r.r_lo = fmaf(-r.ds_lo, m_lo - 12582912.0f, dm_lo);
         r.r_hi = fmaf(-r.ds_hi, m_hi - 12582912.0f, dm_hi);
         r.clo = neg_magic1024(m_lo);
-        r.chi = neg_magic64(m_hi);
+        r.chi = hi_magic64 ? neg_magic64(m_hi) : neg_magic1024(m_hi);
         return r;
     }
-    __device__ static __forceinline__ void unit(const uint8_t* r0, const uint8_t* r1, const XB& xb0, const XB& xb1,
-                                                float4 xm0, float4 xm1, int t, int nvb, float& y0, float& y1) {
+    struct Ctx {
+        uint32_t w0[8], w1[8];
+        Row p0, p1;
+    };
+    __device__ static __forceinline__ void load(Ctx& x, const uint8_t* r0, const uint8_t* r1, int t) {
         const uint4 h0 = lds128(r0), h1 = lds128(r1);
         const uint4 a0 = lds128(r0 + 16 + 32 * t), a1 = lds128(r0 + 32 + 32 * t);
         const uint4 b0 = lds128(r1 + 16 + 32 * t), b1 = lds128(r1 + 32 + 32 * t);
-        const uint32_t w0[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const uint32_t w1[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-        const Row p0 = row_params(h0, t), p1 = row_params(h1, t);
-        // Two accumulator chains per sub-block (even and odd steps) for more
-        // independent MMAs in flight.
-        float c[4][4] = {};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t u0 = w0[i] >> 8, u1 = w1[i] >> 8;
-            mma16816(c[i & 1], hadd2(and_or(w0[i], 0x000F000Fu, 0x64006400u), p0.clo),
-                     hadd2(and_or(w1[i], 0x000F000Fu, 0x64006400u), p1.clo),
-                     hadd2(and_or(u0, 0x000F000Fu, 0x64006400u), p0.clo), hadd2(and_or(u1, 0x000F000Fu, 0x64006400u), p1.clo),
-                     xb0.b[2 * i], xb0.b[2 * i + 1]);
-            mma16816(c[2 + (i & 1)], hadd2(and_or(w0[i], 0x00F000F0u, 0x54005400u), p0.chi),
-                     hadd2(and_or(w1[i], 0x00F000F0u, 0x54005400u), p1.chi),
-                     hadd2(and_or(u0, 0x00F000F0u, 0x54005400u), p0.chi), hadd2(and_or(u1, 0x00F000F0u, 0x54005400u), p1.chi),
-                     xb1.b[2 * i], xb1.b[2 * i + 1]);
-        }
+        x.w0[0] = a0.x; x.w0[1] = a0.y; x.w0[2] = a0.z; x.w0[3] = a0.w;
+        x.w0[4] = a1.x; x.w0[5] = a1.y; x.w0[6] = a1.z; x.w0[7] = a1.w;
+        x.w1[0] = b0.x; x.w1[1] = b0.y; x.w1[2] = b0.z; x.w1[3] = b0.w;
+        x.w1[4] = b1.x; x.w1[5] = b1.y; x.w1[6] = b1.z; x.w1[7] = b1.w;
+        x.p0 = row_params<true>(h0, t, 15.0f);
+        x.p1 = row_params<true>(h1, t, 15.0f);
+    }
+    __device__ static __forceinline__ void conv(const Ctx& x, int i, int, uint32_t (&A)[8]) {
+        const uint32_t u0 = x.w0[i] >> 8, u1 = x.w1[i] >> 8;
+        A[0] = hadd2(and_or(x.w0[i], 0x000F000Fu, 0x64006400u), x.p0.clo);
+        A[1] = hadd2(and_or(x.w1[i], 0x000F000Fu, 0x64006400u), x.p1.clo);
+        A[2] = hadd2(and_or(u0, 0x000F000Fu, 0x64006400u), x.p0.clo);
+        A[3] = hadd2(and_or(u1, 0x000F000Fu, 0x64006400u), x.p1.clo);
+        A[4] = hadd2(and_or(x.w0[i], 0x00F000F0u, 0x54005400u), x.p0.chi);
+        A[5] = hadd2(and_or(x.w1[i], 0x00F000F0u, 0x54005400u), x.p1.chi);
+        A[6] = hadd2(and_or(u0, 0x00F000F0u, 0x54005400u), x.p0.chi);
+        A[7] = hadd2(and_or(u1, 0x00F000F0u, 0x54005400u), x.p1.chi);
+    }
+    __device__ static __forceinline__ void epi(const Ctx& x, const float (&c)[4][4], float4 xm0, float4 xm1, int, int,
+                                               float& y0, float& y1) {
         const float tl0 = csum_g(c[0]) + csum_g(c[1]), th0 = csum_g(c[2]) + csum_g(c[3]);
         const float tl1 = csum_g8(c[0]) + csum_g8(c[1]), th1 = csum_g8(c[2]) + csum_g8(c[3]);
-        y0 += fmaf(p0.ds_lo * xm0.y, tl0, -p0.r_lo * xm0.x) + fmaf(p0.ds_hi * xm1.y, th0, -p0.r_hi * xm1.x);
-        y1 += fmaf(p1.ds_lo * xm0.y, tl1, -p1.r_lo * xm0.x) + fmaf(p1.ds_hi * xm1.y, th1, -p1.r_hi * xm1.x);
+        y0 += fmaf(x.p0.ds_lo * xm0.y, tl0, -x.p0.r_lo * xm0.x) + fmaf(x.p0.ds_hi * xm1.y, th0, -x.p0.r_hi * xm1.x);
+        y1 += fmaf(x.p1.ds_lo * xm0.y, tl1, -x.p1.r_lo * xm0.x) + fmaf(x.p1.ds_hi * xm1.y, th1, -x.p1.r_hi * xm1.x);
     }
 };
 
@@ -224,49 +241,52 @@ template <> struct HU<T_Q4_K> {
 // its first 16-weight group, words 4-7 the second; w = d * sc * (q - 32).
 template <> struct HU<T_Q6_K> {
     static constexpr int UB = 210;
+    static constexpr bool kGroup16 = true;
     __device__ static __forceinline__ int X0(int t) { return 4 * (t >> 1) + (t & 1); }
     __device__ static __forceinline__ int X1(int t) { return 4 * (t >> 1) + (t & 1) + 2; }
-    __device__ static __forceinline__ void unit(const uint8_t* r0, const uint8_t* r1, const XB& xb0, const XB& xb1,
-                                                float4 xm0, float4 xm1, int t, int nvb, float& y0, float& y1) {
-        const int th = t >> 1, gl = t & 1;
+    struct Ctx {
         uint32_t ql0[8], qh0[8], ql1[8], qh1[8];
-        words_a2<8>(r0 + 64 * th + 32 * gl, ql0);
-        words_a2<8>(r0 + 128 + 32 * th, qh0);
-        words_a2<8>(r1 + 64 * th + 32 * gl, ql1);
-        words_a2<8>(r1 + 128 + 32 * th, qh1);
-        // int8 scales of the four 16-weight groups: sc[8th + 2gl + {0, 1}]
-        // (block X0) and sc[8th + 2gl + 4 + {0, 1}] (block X1).
-        const uint32_t s0 = ld_u16(r0 + 192 + 8 * th + 2 * gl) | (ld_u16(r0 + 196 + 8 * th + 2 * gl) << 16);
-        const uint32_t s1 = ld_u16(r1 + 192 + 8 * th + 2 * gl) | (ld_u16(r1 + 196 + 8 * th + 2 * gl) << 16);
-        const float d0 = h2f(ld_u16(r0 + 208)), d1 = h2f(ld_u16(r1 + 208));
-        const int sh = 4 - 2 * gl;   // qh bits 2gl -> bits 4-5 of a byte, bits 2gl+4 -> bits 8-9 of a half
-        float c[4][4] = {};
+        uint32_t s0, s1;   // int8 scales of the four 16-weight groups, rows g and g + 8
+        float d0, d1;
+    };
+    __device__ static __forceinline__ void load(Ctx& x, const uint8_t* r0, const uint8_t* r1, int t) {
+        const int th = t >> 1, gl = t & 1;
+        words_a2<8>(r0 + 64 * th + 32 * gl, x.ql0);
+        words_a2<8>(r0 + 128 + 32 * th, x.qh0);
+        words_a2<8>(r1 + 64 * th + 32 * gl, x.ql1);
+        words_a2<8>(r1 + 128 + 32 * th, x.qh1);
+        // sc[8th + 2gl + {0, 1}] (block X0) and sc[8th + 2gl + 4 + {0, 1}] (block X1).
+        x.s0 = ld_u16(r0 + 192 + 8 * th + 2 * gl) | (ld_u16(r0 + 196 + 8 * th + 2 * gl) << 16);
+        x.s1 = ld_u16(r1 + 192 + 8 * th + 2 * gl) | (ld_u16(r1 + 196 + 8 * th + 2 * gl) << 16);
+        x.d0 = h2f(ld_u16(r0 + 208));
+        x.d1 = h2f(ld_u16(r1 + 208));
+    }
+    __device__ static __forceinline__ void conv(const Ctx& x, int i, int t, uint32_t (&A)[8]) {
+        const int sh = 4 - 2 * (t & 1);   // qh bits 2gl -> bits 4-5 of a byte, bits 2gl+4 -> bits 8-9 of a half
+        const uint32_t v0 = x.qh0[i] << sh, v1 = x.qh1[i] << sh;
+        // Bytes 1 and 3: shift down first, so that byte 3's bits stay in the word.
+        const uint32_t u0 = x.ql0[i] >> 8, u1 = x.ql1[i] >> 8, e0 = (x.qh0[i] >> 8) << sh, e1 = (x.qh1[i] >> 8) << sh;
         const uint32_t CLO = dup16(0xE420u), CHI = dup16(0xD600u);   // -(1024 + 32), -(64 + 32)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t v0 = qh0[i] << sh, v1 = qh1[i] << sh;
-            // Bytes 1 and 3: shift down first, so that byte 3's bits stay in the word.
-            const uint32_t u0 = ql0[i] >> 8, u1 = ql1[i] >> 8, e0 = (qh0[i] >> 8) << sh, e1 = (qh1[i] >> 8) << sh;
-            const int a = i >> 2;   // first or second 16-weight group of the block
-            // (low code bits & m1) | (high code bits & m2) | magic: two logic ops.
-            auto cv = [](uint32_t lo, uint32_t m1, uint32_t hi, uint32_t m2, uint32_t mg) {
-                return and_or(lo, m1, and_or(hi, m2, mg));
-            };
-            mma16816(c[a], hadd2(cv(ql0[i], 0x000F000Fu, v0, 0x00300030u, 0x64006400u), CLO),
-                     hadd2(cv(ql1[i], 0x000F000Fu, v1, 0x00300030u, 0x64006400u), CLO),
-                     hadd2(cv(u0, 0x000F000Fu, e0, 0x00300030u, 0x64006400u), CLO),
-                     hadd2(cv(u1, 0x000F000Fu, e1, 0x00300030u, 0x64006400u), CLO), xb0.b[2 * i], xb0.b[2 * i + 1]);
-            mma16816(c[2 + a], hadd2(cv(ql0[i], 0x00F000F0u, v0, 0x03000300u, 0x54005400u), CHI),
-                     hadd2(cv(ql1[i], 0x00F000F0u, v1, 0x03000300u, 0x54005400u), CHI),
-                     hadd2(cv(u0, 0x00F000F0u, e0, 0x03000300u, 0x54005400u), CHI),
-                     hadd2(cv(u1, 0x00F000F0u, e1, 0x03000300u, 0x54005400u), CHI), xb1.b[2 * i], xb1.b[2 * i + 1]);
-        }
-        const float f00 = d0 * xm0.y, f01 = d0 * xm1.y, f10 = d1 * xm0.y, f11 = d1 * xm1.y;
+        // (low code bits & m1) | (high code bits & m2) | magic: two logic ops.
+        auto cv = [](uint32_t lo, uint32_t m1, uint32_t hi, uint32_t m2, uint32_t mg) {
+            return and_or(lo, m1, and_or(hi, m2, mg));
+        };
+        A[0] = hadd2(cv(x.ql0[i], 0x000F000Fu, v0, 0x00300030u, 0x64006400u), CLO);
+        A[1] = hadd2(cv(x.ql1[i], 0x000F000Fu, v1, 0x00300030u, 0x64006400u), CLO);
+        A[2] = hadd2(cv(u0, 0x000F000Fu, e0, 0x00300030u, 0x64006400u), CLO);
+        A[3] = hadd2(cv(u1, 0x000F000Fu, e1, 0x00300030u, 0x64006400u), CLO);
+        A[4] = hadd2(cv(x.ql0[i], 0x00F000F0u, v0, 0x03000300u, 0x54005400u), CHI);
+        A[5] = hadd2(cv(x.ql1[i], 0x00F000F0u, v1, 0x03000300u, 0x54005400u), CHI);
+        A[6] = hadd2(cv(u0, 0x00F000F0u, e0, 0x03000300u, 0x54005400u), CHI);
+        A[7] = hadd2(cv(u1, 0x00F000F0u, e1, 0x03000300u, 0x54005400u), CHI);
+    }
+    __device__ static __forceinline__ void epi(const Ctx& x, const float (&c)[4][4], float4 xm0, float4 xm1, int, int,
+                                               float& y0, float& y1) {
         auto sc = [](uint32_t s, int k) { return (float)(int8_t)((s >> (8 * k)) & 0xFFu); };
-        y0 += f00 * fmaf(sc(s0, 0), csum_g(c[0]), sc(s0, 1) * csum_g(c[1])) +
-              f01 * fmaf(sc(s0, 2), csum_g(c[2]), sc(s0, 3) * csum_g(c[3]));
-        y1 += f10 * fmaf(sc(s1, 0), csum_g8(c[0]), sc(s1, 1) * csum_g8(c[1])) +
-              f11 * fmaf(sc(s1, 2), csum_g8(c[2]), sc(s1, 3) * csum_g8(c[3]));
+        y0 += x.d0 * (xm0.y * fmaf(sc(x.s0, 0), csum_g(c[0]), sc(x.s0, 1) * csum_g(c[1])) +
+                      xm1.y * fmaf(sc(x.s0, 2), csum_g(c[2]), sc(x.s0, 3) * csum_g(c[3])));
+        y1 += x.d1 * (xm0.y * fmaf(sc(x.s1, 0), csum_g8(c[0]), sc(x.s1, 1) * csum_g8(c[1])) +
+                      xm1.y * fmaf(sc(x.s1, 2), csum_g8(c[2]), sc(x.s1, 3) * csum_g8(c[3])));
     }
 };
 
@@ -275,30 +295,51 @@ template <> struct HU<T_Q6_K> {
 // consecutive bytes.  w = d * q, q signed: the magic holds q + 128.
 template <> struct HU<T_Q8_0> {
     static constexpr int UB = 8 * 34;
+    static constexpr bool kGroup16 = false;
     __device__ static __forceinline__ int X0(int t) { return 2 * t; }
     __device__ static __forceinline__ int X1(int t) { return 2 * t + 1; }
-    __device__ static __forceinline__ void unit(const uint8_t* r0, const uint8_t* r1, const XB& xb0, const XB& xb1,
-                                                float4 xm0, float4 xm1, int t, int nvb, float& y0, float& y1) {
+    struct Ctx {
+        uint32_t q00[8], q01[8], q10[8], q11[8];
+        float d00, d01, d10, d11;
+    };
+    __device__ static __forceinline__ void load(Ctx& x, const uint8_t* r0, const uint8_t* r1, int t) {
         const uint8_t* p0 = r0 + 68 * t;
         const uint8_t* p1 = r1 + 68 * t;
-        uint32_t q00[8], q01[8], q10[8], q11[8];
-        words_a2<8>(p0 + 2, q00);
-        words_a2<8>(p0 + 36, q01);
-        words_a2<8>(p1 + 2, q10);
-        words_a2<8>(p1 + 36, q11);
-        const float d00 = h2f(ld_u16(p0)), d01 = h2f(ld_u16(p0 + 34)), d10 = h2f(ld_u16(p1)), d11 = h2f(ld_u16(p1 + 34));
+        words_a2<8>(p0 + 2, x.q00);
+        words_a2<8>(p0 + 36, x.q01);
+        words_a2<8>(p1 + 2, x.q10);
+        words_a2<8>(p1 + 36, x.q11);
+        x.d00 = h2f(ld_u16(p0));
+        x.d01 = h2f(ld_u16(p0 + 34));
+        x.d10 = h2f(ld_u16(p1));
+        x.d11 = h2f(ld_u16(p1 + 34));
+    }
+    __device__ static __forceinline__ void conv(const Ctx& x, int i, int, uint32_t (&A)[8]) {
         const uint32_t C = dup16(0xE480u);   // -(1024 + 128)
-        float c[4][4] = {};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            mma16816(c[i & 1], hadd2(and_xor(q00[i], 0x00FF00FFu, 0x64806480u), C), hadd2(and_xor(q10[i], 0x00FF00FFu, 0x64806480u), C),
-                     hadd2(and_xor(q00[i] >> 8, 0x00FF00FFu, 0x64806480u), C),
-                     hadd2(and_xor(q10[i] >> 8, 0x00FF00FFu, 0x64806480u), C), xb0.b[2 * i], xb0.b[2 * i + 1]);
-            mma16816(c[2 + (i & 1)], hadd2(and_xor(q01[i], 0x00FF00FFu, 0x64806480u), C), hadd2(and_xor(q11[i], 0x00FF00FFu, 0x64806480u), C),
-                     hadd2(and_xor(q01[i] >> 8, 0x00FF00FFu, 0x64806480u), C),
-                     hadd2(and_xor(q11[i] >> 8, 0x00FF00FFu, 0x64806480u), C), xb1.b[2 * i], xb1.b[2 * i + 1]);
-        }
+        A[0] = hadd2(and_xor(x.q00[i], 0x00FF00FFu, 0x64806480u), C);
+        A[1] = hadd2(and_xor(x.q10[i], 0x00FF00FFu, 0x64806480u), C);
+        A[2] = hadd2(and_xor(x.q00[i] >> 8, 0x00FF00FFu, 0x64806480u), C);
+        A[3] = hadd2(and_xor(x.q10[i] >> 8, 0x00FF00FFu, 0x64806480u), C);
+        A[4] = hadd2(and_xor(x.q01[i], 0x00FF00FFu, 0x64806480u), C);
+        A[5] = hadd2(and_xor(x.q11[i], 0x00FF00FFu, 0x64806480u), C);
+        A[6] = hadd2(and_xor(x.q01[i] >> 8, 0x00FF00FFu, 0x64806480u), C);
+        A[7] = hadd2(and_xor(x.q11[i] >> 8, 0x00FF00FFu, 0x64806480u), C);
+    }
+    __device__ static __forceinline__ void epi(const Ctx& x, const float (&c)[4][4], float4 xm0, float4 xm1, int t,
+                                               int nvb, float& y0, float& y1) {
         // Blocks past the end of a short last unit hold stale bytes: skipped.
+        const bool v0 = 2 * t < nvb, v1 = 2 * t + 1 < nvb;
+        const float t00 = csum_g(c[0]) + csum_g(c[1]), t01 = csum_g(c[2]) + csum_g(c[3]);
+        const float t10 = csum_g8(c[0]) + csum_g8(c[1]), t11 = csum_g8(c[2]) + csum_g8(c[3]);
+        y0 += (v0 ? x.d00 * xm0.y * t00 : 0.0f) + (v1 ? x.d01 * xm1.y * t01 : 0.0f);
+        y1 += (v0 ? x.d10 * xm0.y * t10 : 0.0f) + (v1 ? x.d11 * xm1.y * t11 : 0.0f);
+    }
+};
+
+// Epilogue of the two-block types (Q8_0, Q4_0, Q5_0): y += d * 2^e * T per block.
+struct Epi2 {
+    __device__ static __forceinline__ void run(float d00, float d01, float d10, float d11, const float (&c)[4][4],
+                                               float4 xm0, float4 xm1, int t, int nvb, float& y0, float& y1) {
         const bool v0 = 2 * t < nvb, v1 = 2 * t + 1 < nvb;
         const float t00 = csum_g(c[0]) + csum_g(c[1]), t01 = csum_g(c[2]) + csum_g(c[3]);
         const float t10 = csum_g8(c[0]) + csum_g8(c[1]), t11 = csum_g8(c[2]) + csum_g8(c[3]);
@@ -310,45 +351,46 @@ template <> struct HU<T_Q8_0> {
 // ---------------------------------------------------------------- Q4_0 --
 // A unit is 8 blocks of 32 (18 bytes: fp16 d, 16 bytes of nibbles); group t
 // = blocks 2t (X0) and 2t+1 (X1).  Element e < 16 is the low nibble of qs[e],
-// element 16 + e its high nibble: words 0-3 of a block are the low nibbles
-// of its four code words, words 4-7 the high nibbles.  w = d * (q - 8).
+// element 16 + e its high nibble: steps 0-3 of a block are the low nibbles
+// of its four code words, steps 4-7 the high nibbles.  w = d * (q - 8).
 template <> struct HU<T_Q4_0> {
     static constexpr int UB = 8 * 18;
+    static constexpr bool kGroup16 = false;
     __device__ static __forceinline__ int X0(int t) { return 2 * t; }
     __device__ static __forceinline__ int X1(int t) { return 2 * t + 1; }
-    __device__ static __forceinline__ void unit(const uint8_t* r0, const uint8_t* r1, const XB& xb0, const XB& xb1,
-                                                float4 xm0, float4 xm1, int t, int nvb, float& y0, float& y1) {
+    struct Ctx {
+        uint32_t q00[4], q01[4], q10[4], q11[4];
+        float d00, d01, d10, d11;
+    };
+    __device__ static __forceinline__ void load(Ctx& x, const uint8_t* r0, const uint8_t* r1, int t) {
         const uint8_t* p0 = r0 + 36 * t;
         const uint8_t* p1 = r1 + 36 * t;
-        uint32_t q00[4], q01[4], q10[4], q11[4];
-        words_a2<4>(p0 + 2, q00);
-        words_a2<4>(p0 + 20, q01);
-        words_a2<4>(p1 + 2, q10);
-        words_a2<4>(p1 + 20, q11);
-        const float d00 = h2f(ld_u16(p0)), d01 = h2f(ld_u16(p0 + 18)), d10 = h2f(ld_u16(p1)), d11 = h2f(ld_u16(p1 + 18));
-        const uint32_t CL = dup16(0xE408u), CH = dup16(0xD480u);   // -(1024 + 8), -(64 + 8)
-        float c[4][4] = {};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t a0 = q00[i] >> 8, a1 = q10[i] >> 8, b0 = q01[i] >> 8, b1 = q11[i] >> 8;
-            mma16816(c[0], hadd2(and_or(q00[i], 0x000F000Fu, 0x64006400u), CL), hadd2(and_or(q10[i], 0x000F000Fu, 0x64006400u), CL),
-                     hadd2(and_or(a0, 0x000F000Fu, 0x64006400u), CL), hadd2(and_or(a1, 0x000F000Fu, 0x64006400u), CL),
-                     xb0.b[2 * i], xb0.b[2 * i + 1]);
-            mma16816(c[1], hadd2(and_or(q00[i], 0x00F000F0u, 0x54005400u), CH), hadd2(and_or(q10[i], 0x00F000F0u, 0x54005400u), CH),
-                     hadd2(and_or(a0, 0x00F000F0u, 0x54005400u), CH), hadd2(and_or(a1, 0x00F000F0u, 0x54005400u), CH),
-                     xb0.b[8 + 2 * i], xb0.b[8 + 2 * i + 1]);
-            mma16816(c[2], hadd2(and_or(q01[i], 0x000F000Fu, 0x64006400u), CL), hadd2(and_or(q11[i], 0x000F000Fu, 0x64006400u), CL),
-                     hadd2(and_or(b0, 0x000F000Fu, 0x64006400u), CL), hadd2(and_or(b1, 0x000F000Fu, 0x64006400u), CL),
-                     xb1.b[2 * i], xb1.b[2 * i + 1]);
-            mma16816(c[3], hadd2(and_or(q01[i], 0x00F000F0u, 0x54005400u), CH), hadd2(and_or(q11[i], 0x00F000F0u, 0x54005400u), CH),
-                     hadd2(and_or(b0, 0x00F000F0u, 0x54005400u), CH), hadd2(and_or(b1, 0x00F000F0u, 0x54005400u), CH),
-                     xb1.b[8 + 2 * i], xb1.b[8 + 2 * i + 1]);
-        }
-        const bool v0 = 2 * t < nvb, v1 = 2 * t + 1 < nvb;
-        const float t00 = csum_g(c[0]) + csum_g(c[1]), t01 = csum_g(c[2]) + csum_g(c[3]);
-        const float t10 = csum_g8(c[0]) + csum_g8(c[1]), t11 = csum_g8(c[2]) + csum_g8(c[3]);
-        y0 += (v0 ? d00 * xm0.y * t00 : 0.0f) + (v1 ? d01 * xm1.y * t01 : 0.0f);
-        y1 += (v0 ? d10 * xm0.y * t10 : 0.0f) + (v1 ? d11 * xm1.y * t11 : 0.0f);
+        words_a2<4>(p0 + 2, x.q00);
+        words_a2<4>(p0 + 20, x.q01);
+        words_a2<4>(p1 + 2, x.q10);
+        words_a2<4>(p1 + 20, x.q11);
+        x.d00 = h2f(ld_u16(p0));
+        x.d01 = h2f(ld_u16(p0 + 18));
+        x.d10 = h2f(ld_u16(p1));
+        x.d11 = h2f(ld_u16(p1 + 18));
+    }
+    __device__ static __forceinline__ void conv(const Ctx& x, int i, int, uint32_t (&A)[8]) {
+        const int w = i & 3;
+        // Low nibbles: magic 1024, -(1024 + 8); high nibbles: magic 64, -(64 + 8).
+        const uint32_t M = i < 4 ? 0x000F000Fu : 0x00F000F0u, G = i < 4 ? 0x64006400u : 0x54005400u;
+        const uint32_t C = i < 4 ? dup16(0xE408u) : dup16(0xD480u);
+        A[0] = hadd2(and_or(x.q00[w], M, G), C);
+        A[1] = hadd2(and_or(x.q10[w], M, G), C);
+        A[2] = hadd2(and_or(x.q00[w] >> 8, M, G), C);
+        A[3] = hadd2(and_or(x.q10[w] >> 8, M, G), C);
+        A[4] = hadd2(and_or(x.q01[w], M, G), C);
+        A[5] = hadd2(and_or(x.q11[w], M, G), C);
+        A[6] = hadd2(and_or(x.q01[w] >> 8, M, G), C);
+        A[7] = hadd2(and_or(x.q11[w] >> 8, M, G), C);
+    }
+    __device__ static __forceinline__ void epi(const Ctx& x, const float (&c)[4][4], float4 xm0, float4 xm1, int t,
+                                               int nvb, float& y0, float& y1) {
+        Epi2::run(x.d00, x.d01, x.d10, x.d11, c, xm0, xm1, t, nvb, y0, y1);
     }
 };
 
@@ -359,43 +401,47 @@ template <> struct HU<T_Q4_0> {
 // w = d * (q - 16).
 template <> struct HU<T_Q5_0> {
     static constexpr int UB = 8 * 22;
+    static constexpr bool kGroup16 = false;
     __device__ static __forceinline__ int X0(int t) { return 2 * t; }
     __device__ static __forceinline__ int X1(int t) { return 2 * t + 1; }
     // Four bits z (bit k = fifth bit of byte k) -> 0x10 in each byte whose bit is set.
     __device__ static __forceinline__ uint32_t spread(uint32_t z) { return ((z & 15u) * 0x02040810u) & 0x10101010u; }
-    // One block's 8 steps for rows g (word arrays a) and g + 8 (b): code bytes
-    // = nibble | fifth bit << 4, then the two byte pairs of a word.
-    __device__ static __forceinline__ void block(const uint32_t (&a)[5], const uint32_t (&b)[5], const XB& xb, float (&c)[4],
-                                                 float (&c2)[4]) {
-        const uint32_t C = dup16(0xE410u);   // -(1024 + 16)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int w = i & 3, h = i >> 2;   // code word, nibble
-            const uint32_t ca = and_or(h ? a[1 + w] >> 4 : a[1 + w], 0x0F0F0F0Fu, spread(a[0] >> (4 * i)));
-            const uint32_t cb = and_or(h ? b[1 + w] >> 4 : b[1 + w], 0x0F0F0F0Fu, spread(b[0] >> (4 * i)));
-            mma16816(h ? c2 : c, hadd2(and_or(ca, 0x001F001Fu, 0x64006400u), C), hadd2(and_or(cb, 0x001F001Fu, 0x64006400u), C),
-                     hadd2(and_or(ca >> 8, 0x001F001Fu, 0x64006400u), C), hadd2(and_or(cb >> 8, 0x001F001Fu, 0x64006400u), C),
-                     xb.b[2 * i], xb.b[2 * i + 1]);
-        }
-    }
-    __device__ static __forceinline__ void unit(const uint8_t* r0, const uint8_t* r1, const XB& xb0, const XB& xb1,
-                                                float4 xm0, float4 xm1, int t, int nvb, float& y0, float& y1) {
+    struct Ctx {
+        uint32_t a0[5], a1[5], b0[5], b1[5];   // fifth-bit word, then the four code words
+        float d00, d01, d10, d11;
+    };
+    __device__ static __forceinline__ void load(Ctx& x, const uint8_t* r0, const uint8_t* r1, int t) {
         const uint8_t* p0 = r0 + 44 * t;
         const uint8_t* p1 = r1 + 44 * t;
-        uint32_t a0[5], a1[5], b0[5], b1[5];   // fifth-bit word, then the four code words
-        words_a2<5>(p0 + 2, a0);
-        words_a2<5>(p0 + 24, a1);
-        words_a2<5>(p1 + 2, b0);
-        words_a2<5>(p1 + 24, b1);
-        const float d00 = h2f(ld_u16(p0)), d01 = h2f(ld_u16(p0 + 22)), d10 = h2f(ld_u16(p1)), d11 = h2f(ld_u16(p1 + 22));
-        float c[4][4] = {};
-        block(a0, b0, xb0, c[0], c[1]);
-        block(a1, b1, xb1, c[2], c[3]);
-        const bool v0 = 2 * t < nvb, v1 = 2 * t + 1 < nvb;
-        const float t00 = csum_g(c[0]) + csum_g(c[1]), t01 = csum_g(c[2]) + csum_g(c[3]);
-        const float t10 = csum_g8(c[0]) + csum_g8(c[1]), t11 = csum_g8(c[2]) + csum_g8(c[3]);
-        y0 += (v0 ? d00 * xm0.y * t00 : 0.0f) + (v1 ? d01 * xm1.y * t01 : 0.0f);
-        y1 += (v0 ? d10 * xm0.y * t10 : 0.0f) + (v1 ? d11 * xm1.y * t11 : 0.0f);
+        words_a2<5>(p0 + 2, x.a0);
+        words_a2<5>(p0 + 24, x.a1);
+        words_a2<5>(p1 + 2, x.b0);
+        words_a2<5>(p1 + 24, x.b1);
+        x.d00 = h2f(ld_u16(p0));
+        x.d01 = h2f(ld_u16(p0 + 22));
+        x.d10 = h2f(ld_u16(p1));
+        x.d11 = h2f(ld_u16(p1 + 22));
+    }
+    // Code bytes (0..31) of step i: nibble | fifth bit << 4.
+    __device__ static __forceinline__ uint32_t codes(const uint32_t (&q)[5], int i) {
+        const int w = i & 3;
+        return and_or(i < 4 ? q[1 + w] : q[1 + w] >> 4, 0x0F0F0F0Fu, spread(q[0] >> (4 * i)));
+    }
+    __device__ static __forceinline__ void conv(const Ctx& x, int i, int, uint32_t (&A)[8]) {
+        const uint32_t C = dup16(0xE410u);   // -(1024 + 16)
+        const uint32_t ca = codes(x.a0, i), cb = codes(x.b0, i), cc = codes(x.a1, i), cd = codes(x.b1, i);
+        A[0] = hadd2(and_or(ca, 0x001F001Fu, 0x64006400u), C);
+        A[1] = hadd2(and_or(cb, 0x001F001Fu, 0x64006400u), C);
+        A[2] = hadd2(and_or(ca >> 8, 0x001F001Fu, 0x64006400u), C);
+        A[3] = hadd2(and_or(cb >> 8, 0x001F001Fu, 0x64006400u), C);
+        A[4] = hadd2(and_or(cc, 0x001F001Fu, 0x64006400u), C);
+        A[5] = hadd2(and_or(cd, 0x001F001Fu, 0x64006400u), C);
+        A[6] = hadd2(and_or(cc >> 8, 0x001F001Fu, 0x64006400u), C);
+        A[7] = hadd2(and_or(cd >> 8, 0x001F001Fu, 0x64006400u), C);
+    }
+    __device__ static __forceinline__ void epi(const Ctx& x, const float (&c)[4][4], float4 xm0, float4 xm1, int t,
+                                               int nvb, float& y0, float& y1) {
+        Epi2::run(x.d00, x.d01, x.d10, x.d11, c, xm0, xm1, t, nvb, y0, y1);
     }
 };
 
@@ -403,27 +449,18 @@ template <> struct HU<T_Q5_0> {
 // Q4_K's header and code placement (group t = qs[32t .. 32t+31] at byte 48:
 // low nibbles sub-block 2t, high nibbles 2t+1) with the fifth code bits in
 // qh[l] (byte 16 + l): bit 2t for the low nibble's code, bit 2t+1 for the
-// high nibble's.  w = (d*sc)*q - dmin*m, q in 0..31.
+// high nibble's.  Both codes are moved to bits 0-4 (magic 1024).
+// w = (d*sc)*q - dmin*m, q in 0..31.
 template <> struct HU<T_Q5_K> {
     static constexpr int UB = 176;
+    static constexpr bool kGroup16 = false;
     __device__ static __forceinline__ int X0(int t) { return 2 * t; }
     __device__ static __forceinline__ int X1(int t) { return 2 * t + 1; }
-    __device__ static __forceinline__ HU<T_Q4_K>::Row row_params(const uint4& h, int t) {
-        const uint32_t f = HU<T_Q4_K>::fields(h, t);
-        const float d = h2f(h.x & 0xFFFFu), dmin = h2f(h.x >> 16);
-        HU<T_Q4_K>::Row r;
-        r.ds_lo = d * ubyte_f(f, 0);
-        r.ds_hi = d * ubyte_f(f, 1);
-        const float dm_lo = dmin * ubyte_f(f, 2), dm_hi = dmin * ubyte_f(f, 3);
-        const float m_lo = nearest_code_m(dm_lo, r.ds_lo, 31.0f), m_hi = nearest_code_m(dm_hi, r.ds_hi, 31.0f);
-        r.r_lo = fmaf(-r.ds_lo, m_lo - 12582912.0f, dm_lo);
-        r.r_hi = fmaf(-r.ds_hi, m_hi - 12582912.0f, dm_hi);
-        r.clo = neg_magic1024(m_lo);
-        r.chi = neg_magic1024(m_hi);
-        return r;
-    }
-    __device__ static __forceinline__ void unit(const uint8_t* r0, const uint8_t* r1, const XB& xb0, const XB& xb1,
-                                                float4 xm0, float4 xm1, int t, int nvb, float& y0, float& y1) {
+    struct Ctx {
+        uint32_t w0[8], w1[8], v0[8], v1[8];
+        HU<T_Q4_K>::Row p0, p1;
+    };
+    __device__ static __forceinline__ void load(Ctx& x, const uint8_t* r0, const uint8_t* r1, int t) {
         const uint4 h0 = lds128(r0), h1 = lds128(r1);
         const uint4 a0 = lds128(r0 + 48 + 32 * t), a1 = lds128(r0 + 64 + 32 * t);
         const uint4 b0 = lds128(r1 + 48 + 32 * t), b1 = lds128(r1 + 64 + 32 * t);
@@ -432,29 +469,36 @@ template <> struct HU<T_Q5_K> {
         const uint32_t w1[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
         const uint32_t v0[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
         const uint32_t v1[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-        const HU<T_Q4_K>::Row p0 = row_params(h0, t), p1 = row_params(h1, t);
-        float c[4][4] = {};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            // Code bytes (0..31) of the low and the high nibbles, then the pairs.
-            const uint32_t u0 = v0[i] >> (2 * t), u1 = v1[i] >> (2 * t);
-            const uint32_t l0 = and_or(w0[i], 0x0F0F0F0Fu, (u0 << 4) & 0x10101010u);
-            const uint32_t l1 = and_or(w1[i], 0x0F0F0F0Fu, (u1 << 4) & 0x10101010u);
-            const uint32_t k0 = and_or(w0[i] >> 4, 0x0F0F0F0Fu, (u0 << 3) & 0x10101010u);
-            const uint32_t k1 = and_or(w1[i] >> 4, 0x0F0F0F0Fu, (u1 << 3) & 0x10101010u);
-            mma16816(c[i & 1], hadd2(and_or(l0, 0x001F001Fu, 0x64006400u), p0.clo),
-                     hadd2(and_or(l1, 0x001F001Fu, 0x64006400u), p1.clo),
-                     hadd2(and_or(l0 >> 8, 0x001F001Fu, 0x64006400u), p0.clo),
-                     hadd2(and_or(l1 >> 8, 0x001F001Fu, 0x64006400u), p1.clo), xb0.b[2 * i], xb0.b[2 * i + 1]);
-            mma16816(c[2 + (i & 1)], hadd2(and_or(k0, 0x001F001Fu, 0x64006400u), p0.chi),
-                     hadd2(and_or(k1, 0x001F001Fu, 0x64006400u), p1.chi),
-                     hadd2(and_or(k0 >> 8, 0x001F001Fu, 0x64006400u), p0.chi),
-                     hadd2(and_or(k1 >> 8, 0x001F001Fu, 0x64006400u), p1.chi), xb1.b[2 * i], xb1.b[2 * i + 1]);
+            x.w0[i] = w0[i];
+            x.w1[i] = w1[i];
+            x.v0[i] = v0[i] >> (2 * t);   // bit 0 of each byte: low code's fifth bit, bit 1: high code's
+            x.v1[i] = v1[i] >> (2 * t);
         }
+        x.p0 = HU<T_Q4_K>::row_params<false>(h0, t, 31.0f);
+        x.p1 = HU<T_Q4_K>::row_params<false>(h1, t, 31.0f);
+    }
+    __device__ static __forceinline__ void conv(const Ctx& x, int i, int, uint32_t (&A)[8]) {
+        const uint32_t l0 = and_or(x.w0[i], 0x0F0F0F0Fu, (x.v0[i] << 4) & 0x10101010u);
+        const uint32_t l1 = and_or(x.w1[i], 0x0F0F0F0Fu, (x.v1[i] << 4) & 0x10101010u);
+        const uint32_t k0 = and_or(x.w0[i] >> 4, 0x0F0F0F0Fu, (x.v0[i] << 3) & 0x10101010u);
+        const uint32_t k1 = and_or(x.w1[i] >> 4, 0x0F0F0F0Fu, (x.v1[i] << 3) & 0x10101010u);
+        A[0] = hadd2(and_or(l0, 0x001F001Fu, 0x64006400u), x.p0.clo);
+        A[1] = hadd2(and_or(l1, 0x001F001Fu, 0x64006400u), x.p1.clo);
+        A[2] = hadd2(and_or(l0 >> 8, 0x001F001Fu, 0x64006400u), x.p0.clo);
+        A[3] = hadd2(and_or(l1 >> 8, 0x001F001Fu, 0x64006400u), x.p1.clo);
+        A[4] = hadd2(and_or(k0, 0x001F001Fu, 0x64006400u), x.p0.chi);
+        A[5] = hadd2(and_or(k1, 0x001F001Fu, 0x64006400u), x.p1.chi);
+        A[6] = hadd2(and_or(k0 >> 8, 0x001F001Fu, 0x64006400u), x.p0.chi);
+        A[7] = hadd2(and_or(k1 >> 8, 0x001F001Fu, 0x64006400u), x.p1.chi);
+    }
+    __device__ static __forceinline__ void epi(const Ctx& x, const float (&c)[4][4], float4 xm0, float4 xm1, int, int,
+                                               float& y0, float& y1) {
         const float tl0 = csum_g(c[0]) + csum_g(c[1]), th0 = csum_g(c[2]) + csum_g(c[3]);
         const float tl1 = csum_g8(c[0]) + csum_g8(c[1]), th1 = csum_g8(c[2]) + csum_g8(c[3]);
-        y0 += fmaf(p0.ds_lo * xm0.y, tl0, -p0.r_lo * xm0.x) + fmaf(p0.ds_hi * xm1.y, th0, -p0.r_hi * xm1.x);
-        y1 += fmaf(p1.ds_lo * xm0.y, tl1, -p1.r_lo * xm0.x) + fmaf(p1.ds_hi * xm1.y, th1, -p1.r_hi * xm1.x);
+        y0 += fmaf(x.p0.ds_lo * xm0.y, tl0, -x.p0.r_lo * xm0.x) + fmaf(x.p0.ds_hi * xm1.y, th0, -x.p0.r_hi * xm1.x);
+        y1 += fmaf(x.p1.ds_lo * xm0.y, tl1, -x.p1.r_lo * xm0.x) + fmaf(x.p1.ds_hi * xm1.y, th1, -x.p1.r_hi * xm1.x);
     }
 };
 
@@ -463,12 +507,13 @@ template <> struct HU<T_Q5_K> {
 // bytes of 2-bit codes, fp16 d, fp16 dmin.  Weight 128t' + 32j + l has code
 // (qs[32t' + l] >> 2j) & 3; group t = weights 64t .. 64t+63 = code bytes
 // qs[32(t/2) ..] with j = 2(t%2) (x-block X0 = 2t) and j + 1 (X1 = 2t+1), and
-// the 16-weight groups 4t .. 4t+3 (words 0-3 / 4-7 of each x-block).  A code
+// the 16-weight groups 4t .. 4t+3 (steps 0-3 / 4-7 of each x-block).  A code
 // at bits 2j of a byte sits in the mantissa of the magic 2^(10 - 2j) with
 // unit weight.  w = (d*sc)*q - dmin*m per 16-weight group, with the code
 // offset o = the code nearest dmin*m / (d*sc) as for Q4_K.
 template <> struct HU<T_Q2_K> {
     static constexpr int UB = 84;
+    static constexpr bool kGroup16 = true;
     __device__ static __forceinline__ int X0(int t) { return 2 * t; }
     __device__ static __forceinline__ int X1(int t) { return 2 * t + 1; }
     struct Row {
@@ -485,46 +530,55 @@ template <> struct HU<T_Q2_K> {
         for (int k = 0; k < 4; ++k) {
             w.ds[k] = d * ubyte_f(scb, k);
             const float dm = dmin * ubyte_f(mb, k);
-            const float m = nearest_code_m(dm, w.ds[k], 3.0f);
-            const float o = m - 12582912.0f;
+            const float o = nearest_code_m(dm, w.ds[k], 3.0f) - 12582912.0f;
             w.r[k] = fmaf(-w.ds[k], o, dm);
             w.cst[k] = h2dup(-((k < 2 ? magic0 : magic1) + o));
         }
         return w;
     }
-    __device__ static __forceinline__ void unit(const uint8_t* r0, const uint8_t* r1, const XB& xb0, const XB& xb1,
-                                                float4 xm0, float4 xm1, int t, int nvb, float& y0, float& y1) {
+    struct Ctx {
+        uint32_t w0[8], w1[8];
+        Row p0, p1;
+    };
+    __device__ static __forceinline__ void load(Ctx& x, const uint8_t* r0, const uint8_t* r1, int t) {
         const int j0 = 2 * (t & 1);
+        // 84-byte blocks are 4-byte aligned (not 16): word loads.
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            x.w0[i] = lds32(r0 + 16 + 32 * (t >> 1) + 4 * i);
+            x.w1[i] = lds32(r1 + 16 + 32 * (t >> 1) + 4 * i);
+        }
+        const float mg0 = j0 ? 64.0f : 1024.0f, mg1 = j0 ? 16.0f : 256.0f;
+        x.p0 = row_params(r0, t, mg0, mg1);
+        x.p1 = row_params(r1, t, mg0, mg1);
+    }
+    __device__ static __forceinline__ void conv(const Ctx& x, int i, int t, uint32_t (&A)[8]) {
+        const int j0 = 2 * (t & 1), k = i >> 2;
         // Masks and magics of the two code positions: j0 = 0 -> bits 0-1 (1024),
         // j0 = 2 -> bits 4-5 (64); j0 + 1 -> bits 2-3 (256) or 6-7 (16).
         const uint32_t M0 = j0 ? 0x00300030u : 0x00030003u, G0 = j0 ? 0x54005400u : 0x64006400u;
         const uint32_t M1 = j0 ? 0x00C000C0u : 0x000C000Cu, G1 = j0 ? 0x4C004C00u : 0x5C005C00u;
-        const float mg0 = j0 ? 64.0f : 1024.0f, mg1 = j0 ? 16.0f : 256.0f;
-        // 84-byte blocks are 4-byte aligned (not 16): word loads.
-        uint32_t w0[8], w1[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            w0[i] = lds32(r0 + 16 + 32 * (t >> 1) + 4 * i);
-            w1[i] = lds32(r1 + 16 + 32 * (t >> 1) + 4 * i);
-        }
-        const Row p0 = row_params(r0, t, mg0, mg1), p1 = row_params(r1, t, mg0, mg1);
-        float c[4][4] = {};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int k = i >> 2;   // 16-weight group within the x-block
-            const uint32_t u0 = w0[i] >> 8, u1 = w1[i] >> 8;
-            mma16816(c[k], hadd2(and_or(w0[i], M0, G0), p0.cst[k]), hadd2(and_or(w1[i], M0, G0), p1.cst[k]),
-                     hadd2(and_or(u0, M0, G0), p0.cst[k]), hadd2(and_or(u1, M0, G0), p1.cst[k]), xb0.b[2 * i],
-                     xb0.b[2 * i + 1]);
-            mma16816(c[2 + k], hadd2(and_or(w0[i], M1, G1), p0.cst[2 + k]), hadd2(and_or(w1[i], M1, G1), p1.cst[2 + k]),
-                     hadd2(and_or(u0, M1, G1), p0.cst[2 + k]), hadd2(and_or(u1, M1, G1), p1.cst[2 + k]), xb1.b[2 * i],
-                     xb1.b[2 * i + 1]);
-        }
+        const uint32_t u0 = x.w0[i] >> 8, u1 = x.w1[i] >> 8;
+        A[0] = hadd2(and_or(x.w0[i], M0, G0), x.p0.cst[k]);
+        A[1] = hadd2(and_or(x.w1[i], M0, G0), x.p1.cst[k]);
+        A[2] = hadd2(and_or(u0, M0, G0), x.p0.cst[k]);
+        A[3] = hadd2(and_or(u1, M0, G0), x.p1.cst[k]);
+        A[4] = hadd2(and_or(x.w0[i], M1, G1), x.p0.cst[2 + k]);
+        A[5] = hadd2(and_or(x.w1[i], M1, G1), x.p1.cst[2 + k]);
+        A[6] = hadd2(and_or(u0, M1, G1), x.p0.cst[2 + k]);
+        A[7] = hadd2(and_or(u1, M1, G1), x.p1.cst[2 + k]);
+    }
+    __device__ static __forceinline__ void epi(const Ctx& x, const float (&c)[4][4], float4 xm0, float4 xm1, int, int,
+                                               float& y0, float& y1) {
         // Groups 4t, 4t+1 (x-block X0 halves) and 4t+2, 4t+3 (X1 halves).
-        y0 += fmaf(p0.ds[0] * xm0.y, csum_g(c[0]), -p0.r[0] * xm0.z) + fmaf(p0.ds[1] * xm0.y, csum_g(c[1]), -p0.r[1] * xm0.w) +
-              fmaf(p0.ds[2] * xm1.y, csum_g(c[2]), -p0.r[2] * xm1.z) + fmaf(p0.ds[3] * xm1.y, csum_g(c[3]), -p0.r[3] * xm1.w);
-        y1 += fmaf(p1.ds[0] * xm0.y, csum_g8(c[0]), -p1.r[0] * xm0.z) + fmaf(p1.ds[1] * xm0.y, csum_g8(c[1]), -p1.r[1] * xm0.w) +
-              fmaf(p1.ds[2] * xm1.y, csum_g8(c[2]), -p1.r[2] * xm1.z) + fmaf(p1.ds[3] * xm1.y, csum_g8(c[3]), -p1.r[3] * xm1.w);
+        y0 += fmaf(x.p0.ds[0] * xm0.y, csum_g(c[0]), -x.p0.r[0] * xm0.z) +
+              fmaf(x.p0.ds[1] * xm0.y, csum_g(c[1]), -x.p0.r[1] * xm0.w) +
+              fmaf(x.p0.ds[2] * xm1.y, csum_g(c[2]), -x.p0.r[2] * xm1.z) +
+              fmaf(x.p0.ds[3] * xm1.y, csum_g(c[3]), -x.p0.r[3] * xm1.w);
+        y1 += fmaf(x.p1.ds[0] * xm0.y, csum_g8(c[0]), -x.p1.r[0] * xm0.z) +
+              fmaf(x.p1.ds[1] * xm0.y, csum_g8(c[1]), -x.p1.r[1] * xm0.w) +
+              fmaf(x.p1.ds[2] * xm1.y, csum_g8(c[2]), -x.p1.r[2] * xm1.z) +
+              fmaf(x.p1.ds[3] * xm1.y, csum_g8(c[3]), -x.p1.r[3] * xm1.w);
     }
 };
 
@@ -540,10 +594,32 @@ template <> struct HU<T_Q2_K> {
 // 104 + k.
 template <> struct HU<T_Q3_K> {
     static constexpr int UB = 110;
+    static constexpr bool kGroup16 = true;
     __device__ static __forceinline__ int X0(int t) { return 2 * t; }
     __device__ static __forceinline__ int X1(int t) { return 2 * t + 1; }
-    __device__ static __forceinline__ void unit(const uint8_t* r0, const uint8_t* r1, const XB& xb0, const XB& xb1,
-                                                float4 xm0, float4 xm1, int t, int nvb, float& y0, float& y1) {
+    struct Ctx {
+        uint32_t q0[8], q1[8], m0[8], m1[8];
+        uint32_t S0, S1;   // the four scales (+ 32) of rows g and g + 8, as bytes
+        float d0, d1;
+    };
+    __device__ static __forceinline__ void load(Ctx& x, const uint8_t* r0, const uint8_t* r1, int t) {
+        const int tp = t >> 1;
+        words_a2<8>(r0 + 32 + 32 * tp, x.q0);
+        words_a2<8>(r1 + 32 + 32 * tp, x.q1);
+        words_a2<8>(r0, x.m0);
+        words_a2<8>(r1, x.m1);
+        uint32_t l0[1], l1[1], u0[1], u1[1];
+        words_a2<1>(r0 + 96 + 4 * (t & 1), l0);
+        words_a2<1>(r1 + 96 + 4 * (t & 1), l1);
+        words_a2<1>(r0 + 104, u0);
+        words_a2<1>(r1 + 104, u1);
+        x.S0 = ((l0[0] >> (4 * tp)) & 0x0F0F0F0Fu) | (((u0[0] >> (2 * t)) & 0x03030303u) << 4);
+        x.S1 = ((l1[0] >> (4 * tp)) & 0x0F0F0F0Fu) | (((u1[0] >> (2 * t)) & 0x03030303u) << 4);
+        x.d0 = h2f(ld_u16(r0 + 108));
+        x.d1 = h2f(ld_u16(r1 + 108));
+    }
+    __device__ static __forceinline__ uint32_t shl(uint32_t v, int s) { return s >= 0 ? v << s : v >> (-s); }
+    __device__ static __forceinline__ void conv(const Ctx& x, int i, int t, uint32_t (&A)[8]) {
         const int tp = t >> 1, j0 = 2 * (t & 1), j1 = j0 + 1;
         // Code bits 2j, 2j+1 and the mask bit moved from bit 4t' + j to 2j + 2,
         // per 16-bit half; magic 2^(10 - 2j).
@@ -552,46 +628,71 @@ template <> struct HU<T_Q3_K> {
         const uint32_t G0 = j0 ? 0x54005400u : 0x64006400u, G1 = j0 ? 0x4C004C00u : 0x5C005C00u;
         // -(magic + 4): 1028 = 0x6404 -> 0xE404 (j = 0); 260 = 0x5C10 -> 0xDC10 (j = 1);
         // 68 = 0x5440 -> 0xD440 (j = 2); 20 = 0x4D00 -> 0xCD00 (j = 3).
-        const uint32_t CC0 = j0 ? dup16(0xD440u) : dup16(0xE404u), CC1 = j0 ? dup16(0xCD00u) : dup16(0xDC10u);
-        const int hs0 = 4 * tp + j0, hs1 = 4 * tp + j1;   // mask bit positions
-        const int sh0 = 2 * j0 + 2 - hs0, sh1 = 2 * j1 + 2 - hs1;   // shift to place it (may be negative)
-        uint32_t q0[8], q1[8], m0[8], m1[8];
-        words_a2<8>(r0 + 32 + 32 * tp, q0);
-        words_a2<8>(r1 + 32 + 32 * tp, q1);
-        words_a2<8>(r0, m0);
-        words_a2<8>(r1, m1);
-        auto shl = [](uint32_t v, int s) { return s >= 0 ? v << s : v >> (-s); };
-        float c[4][4] = {};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int k = i >> 2;
-            const uint32_t qa = q0[i], qb = q1[i], qa8 = q0[i] >> 8, qb8 = q1[i] >> 8;
-            const uint32_t ma = m0[i], mb = m1[i], ma8 = m0[i] >> 8, mb8 = m1[i] >> 8;
-            mma16816(c[k], hadd2(and_or(qa, M0, and_or(shl(ma, sh0), B0, G0)), CC0),
-                     hadd2(and_or(qb, M0, and_or(shl(mb, sh0), B0, G0)), CC0),
-                     hadd2(and_or(qa8, M0, and_or(shl(ma8, sh0), B0, G0)), CC0),
-                     hadd2(and_or(qb8, M0, and_or(shl(mb8, sh0), B0, G0)), CC0), xb0.b[2 * i], xb0.b[2 * i + 1]);
-            mma16816(c[2 + k], hadd2(and_or(qa, M1, and_or(shl(ma, sh1), B1, G1)), CC1),
-                     hadd2(and_or(qb, M1, and_or(shl(mb, sh1), B1, G1)), CC1),
-                     hadd2(and_or(qa8, M1, and_or(shl(ma8, sh1), B1, G1)), CC1),
-                     hadd2(and_or(qb8, M1, and_or(shl(mb8, sh1), B1, G1)), CC1), xb1.b[2 * i], xb1.b[2 * i + 1]);
-        }
-        // Scales of groups 4t .. 4t+3 (signed, stored + 32).
-        uint32_t l0[1], l1[1], u0[1], u1[1];
-        words_a2<1>(r0 + 96 + 4 * (t & 1), l0);
-        words_a2<1>(r1 + 96 + 4 * (t & 1), l1);
-        words_a2<1>(r0 + 104, u0);
-        words_a2<1>(r1 + 104, u1);
-        const uint32_t S0 = ((l0[0] >> (4 * tp)) & 0x0F0F0F0Fu) | (((u0[0] >> (2 * t)) & 0x03030303u) << 4);
-        const uint32_t S1 = ((l1[0] >> (4 * tp)) & 0x0F0F0F0Fu) | (((u1[0] >> (2 * t)) & 0x03030303u) << 4);
-        const float d0 = h2f(ld_u16(r0 + 108)), d1 = h2f(ld_u16(r1 + 108));
+        const uint32_t C0 = j0 ? dup16(0xD440u) : dup16(0xE404u), C1 = j0 ? dup16(0xCD00u) : dup16(0xDC10u);
+        const int sh0 = 2 * j0 + 2 - (4 * tp + j0), sh1 = 2 * j1 + 2 - (4 * tp + j1);   // may be negative
+        const uint32_t qa = x.q0[i], qb = x.q1[i], qa8 = qa >> 8, qb8 = qb >> 8;
+        const uint32_t ma = x.m0[i], mb = x.m1[i], ma8 = ma >> 8, mb8 = mb >> 8;
+        A[0] = hadd2(and_or(qa, M0, and_or(shl(ma, sh0), B0, G0)), C0);
+        A[1] = hadd2(and_or(qb, M0, and_or(shl(mb, sh0), B0, G0)), C0);
+        A[2] = hadd2(and_or(qa8, M0, and_or(shl(ma8, sh0), B0, G0)), C0);
+        A[3] = hadd2(and_or(qb8, M0, and_or(shl(mb8, sh0), B0, G0)), C0);
+        A[4] = hadd2(and_or(qa, M1, and_or(shl(ma, sh1), B1, G1)), C1);
+        A[5] = hadd2(and_or(qb, M1, and_or(shl(mb, sh1), B1, G1)), C1);
+        A[6] = hadd2(and_or(qa8, M1, and_or(shl(ma8, sh1), B1, G1)), C1);
+        A[7] = hadd2(and_or(qb8, M1, and_or(shl(mb8, sh1), B1, G1)), C1);
+    }
+    __device__ static __forceinline__ void epi(const Ctx& x, const float (&c)[4][4], float4 xm0, float4 xm1, int, int,
+                                               float& y0, float& y1) {
         auto sc = [](uint32_t S, int k) { return ubyte_f(S, k) - 32.0f; };
-        y0 += d0 * (xm0.y * fmaf(sc(S0, 0), csum_g(c[0]), sc(S0, 1) * csum_g(c[1])) +
-                    xm1.y * fmaf(sc(S0, 2), csum_g(c[2]), sc(S0, 3) * csum_g(c[3])));
-        y1 += d1 * (xm0.y * fmaf(sc(S1, 0), csum_g8(c[0]), sc(S1, 1) * csum_g8(c[1])) +
-                    xm1.y * fmaf(sc(S1, 2), csum_g8(c[2]), sc(S1, 3) * csum_g8(c[3])));
+        y0 += x.d0 * (xm0.y * fmaf(sc(x.S0, 0), csum_g(c[0]), sc(x.S0, 1) * csum_g(c[1])) +
+                      xm1.y * fmaf(sc(x.S0, 2), csum_g(c[2]), sc(x.S0, 3) * csum_g(c[3])));
+        y1 += x.d1 * (xm0.y * fmaf(sc(x.S1, 0), csum_g8(c[0]), sc(x.S1, 1) * csum_g8(c[1])) +
+                      xm1.y * fmaf(sc(x.S1, 2), csum_g8(c[2]), sc(x.S1, 3) * csum_g8(c[3])));
     }
 };
+
+// B fragments of the MT tokens: in registers for one token (the whole
+// chunk's steps), from shared memory step by step for more.
+struct BRegs {
+    XB x0, x1;
+    __device__ __forceinline__ uint2 b(int, int X, int i) const {
+        return X ? make_uint2(x1.b[2 * i], x1.b[2 * i + 1]) : make_uint2(x0.b[2 * i], x0.b[2 * i + 1]);
+    }
+};
+template <int MT>
+struct BSmem {
+    const uint8_t* p[MT][2];   // plane of the thread's column in x-blocks X0, X1 of each token
+    bool own;
+    __device__ __forceinline__ uint2 b(int m, int X, int i) const {
+        return own ? lds64(p[m][X] + 8 * i) : make_uint2(0u, 0u);
+    }
+};
+
+// One unit for MT tokens: each step's A fragments are converted once and
+// multiplied with every token's B; the four accumulators of a token are the
+// two x-blocks' halves (16-weight-group types) or even / odd steps.
+template <int T, int MT, class BP>
+__device__ __forceinline__ void run_unit(const uint8_t* r0, const uint8_t* r1, const BP& bp, const float4 (&xm0)[MT],
+                                         const float4 (&xm1)[MT], int t, int nvb, float (&y0)[MT], float (&y1)[MT]) {
+    using U = HU<T>;
+    typename U::Ctx cx;
+    U::load(cx, r0, r1, t);
+    float c[MT][4][4] = {};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t A[8];
+        U::conv(cx, i, t, A);
+        const int ch = U::kGroup16 ? (i >> 2) : (i & 1);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const uint2 b0 = bp.b(m, 0, i), b1 = bp.b(m, 1, i);
+            mma16816(c[m][ch], A[0], A[1], A[2], A[3], b0.x, b0.y);
+            mma16816(c[m][2 + ch], A[4], A[5], A[6], A[7], b1.x, b1.y);
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) U::epi(cx, c[m], xm0[m], xm1[m], t, nvb, y0[m], y1[m]);
+}
 
 }  // namespace hm
 }  // namespace qk

@@ -33,7 +33,7 @@ cudaError_t launch_unpack(int type, const uint8_t* W, int64_t nblocks, int16_t* 
 // GEMV launch plan: how the [rows, cols] x [M] problem is cut into CTAs.
 struct GemvPlan {
     bool decode = false; // M == 1 decode kernel (activation prep inside; no workspace)
-    bool tc = false;     // ... the tensor-core decode kernel (qk_hgemv.cu)
+    bool tc = false;     // the tensor-core GEMV kernel (qk_hgemv.cu; any M up to 64, no workspace)
     int sms = 0;         // SM count the plan was made for
     int mt = 1;          // activation rows per CTA pass (template width)
     int splits = 1;      // K splits (partials reduced by a second kernel)
@@ -57,6 +57,9 @@ cudaError_t launch_hgemv(int type, int n, const uint8_t* const* W, const int64_t
                          float* const* y, int sms, unsigned* status, cudaStream_t s);
 cudaError_t launch_hgemv_swiglu(int type, const uint8_t* Wg, const uint8_t* Wu, int64_t rows, int64_t cols,
                                 const float* x, float* h, int sms, unsigned* status, cudaStream_t s);
+// M activation rows through the same kernel (two per launch), y [M, rows].
+cudaError_t launch_hgemv_tokens(int type, const uint8_t* W, int64_t rows, int64_t cols, const float* x, int64_t M,
+                                float* y, int sms, unsigned* status, cudaStream_t s);
 cudaError_t launch_gemv(int type, const GemvPlan& plan, const uint8_t* W, int64_t rows, int64_t cols,
                         const float* x, int64_t M, float* y, float* ws, unsigned* status, cudaStream_t s);
 

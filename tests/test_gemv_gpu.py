@@ -43,7 +43,7 @@ SHAPES = {
 
 @pytest.mark.parametrize("name", NAMES)
 @pytest.mark.parametrize("shape_i", range(4))
-@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 9])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 9, 67])
 def test_gemv_parity(gpu, name, shape_i, M):
     rows, cols = SHAPES[name][shape_i]
     y, y_ref, S = run(gpu, name, rows, cols, M, 1000 + 10 * shape_i + M)
@@ -61,13 +61,15 @@ def test_gemv_quantized_codes(gpu, name):
 
 
 def test_split_and_unsplit_paths(gpu):
-    # Batched (M = 2) kernel: 16 rows (one row tile) split K over many CTAs,
-    # 8192 rows do not; the split plan needs room for partials beyond the
-    # prepped activations.  M = 1 uses the K-sliced decode kernel.
-    xp_only = qk.gemv_workspace(qk.Q4_K, 8192, 8192, 2)
-    assert qk.gemv_workspace(qk.Q4_K, 16, 8192, 2) > xp_only
-    for rows in (16, 8192):
-        for M in (1, 2):
+    # Up to 64 activation rows run the tensor-core kernel (no workspace).
+    # Beyond, the tiled kernel: 16 rows (one row tile) split K over many
+    # CTAs, 8192 rows do not; the split plan needs room for partials beyond
+    # the prepped activations.
+    assert qk.gemv_workspace(qk.Q4_K, 16, 8192, 64) == 0
+    xp_only = qk.gemv_workspace(qk.Q4_K, 8192, 8192, 72)
+    assert qk.gemv_workspace(qk.Q4_K, 16, 8192, 72) > xp_only > 0
+    for rows in (16, 1024):
+        for M in (1, 2, 72):
             y, y_ref, S = run(gpu, "Q4_K", rows, 8192, M, 2000 + rows)
             assert_gemv_close(y, y_ref, S, what=f"rows={rows} M={M}")
 
@@ -138,12 +140,12 @@ def test_output_canaries_and_empty(gpu):
 
 
 def test_workspace_too_small_is_rejected(gpu):
-    # M = 2 runs the activation-prep kernel, whose output lives in the workspace.
+    # M = 72 runs the activation-prep kernel, whose output lives in the workspace.
     t, rows, cols = qk.Q4_K, 16, 4096
-    need = qk.gemv_workspace(t, rows, cols, 2)
+    need = qk.gemv_workspace(t, rows, cols, 72)
     assert need > 0
     W = dev_u8(synth.random_blocks("Q4_K", rows, cols, 97), gpu)
-    x = dev_f32(synth.activations(2, cols, 98), gpu)
+    x = dev_f32(synth.activations(72, cols, 98), gpu)
     small = torch.empty(need - 16, dtype=torch.uint8, device=gpu)
     with pytest.raises(qk.QKError) as e:
         qk.gemv(t, W, rows, cols, x, ws=small)
