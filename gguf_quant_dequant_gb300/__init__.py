@@ -225,8 +225,8 @@ def gemv(t: int, W, rows: int, cols: int, x, y=None, ws=None, stream=None):
 
 
 def gemv_noalloc(t: int, W, rows: int, cols: int, x, y=None, stream=None):
-    """qk_gemv_noalloc: the GEMV with the library's fixed device scratch
-    instead of a workspace (for callers that cannot allocate)."""
+    """qk_gemv_noalloc: qk_gemv for callers that cannot allocate device
+    memory (no workspace; the GEMV needs none)."""
     import torch
     M = x.shape[0] if x.dim() == 2 else 1
     if y is None:

@@ -239,15 +239,11 @@ qk_status qk_gemv(int type, const void* W, int64_t rows, int64_t cols, const flo
     int sms = 0;
     st = device_state(&status, &sms);
     if (st != QK_OK) return st;
+    (void)ws;   // no shape needs one
+    (void)ws_bytes;
     const qk::GemvPlan pl = qk::plan_gemv(type, rows, cols, M, sms);
-    if (pl.ws_bytes > 0) {
-        if (ws_bytes < (size_t)pl.ws_bytes)
-            return fail(QK_ERR_WORKSPACE, "workspace %zu bytes < %lld needed", ws_bytes, (long long)pl.ws_bytes);
-        if (!ws) return fail(QK_ERR_NULL, "workspace is NULL");
-        if (!aligned(ws, 16)) return fail(QK_ERR_ALIGN, "workspace is not 16-byte aligned");
-    }
-    cudaError_t e = qk::launch_gemv(type, pl, static_cast<const uint8_t*>(W), rows, cols, x, M, y,
-                                    static_cast<float*>(ws), status, s);
+    if (!pl.ok) return fail(QK_ERR_SHAPE, "rows=%lld cols=%lld: no GEMV launch fits", (long long)rows, (long long)cols);
+    cudaError_t e = qk::launch_gemv(type, pl, static_cast<const uint8_t*>(W), rows, cols, x, M, y, status, s);
     if (e != cudaSuccess) return cuda_fail(e, "qk_gemv launch");
     g_last_error.clear();
     return QK_OK;
@@ -286,13 +282,9 @@ qk_status qk_gemv_batch(int type, int n_mat, const void* const* W, const int64_t
     qk_status st = device_state(&status, &sms);
     if (st != QK_OK) return st;
     cudaError_t e;
-    if (qk::hgemv_ok(type, n_mat, rows, cols, sms)) {
-        e = qk::launch_hgemv(type, n_mat, reinterpret_cast<const uint8_t* const*>(W), rows, cols, x, y, sms, status, s);
-    } else {
-        if (qk::gemv5_ring_pairs(type, n_mat, rows, cols, sms) == 0)
-            return fail(QK_ERR_SHAPE, "cols=%lld is too large for the batched decode kernel", (long long)cols);
-        e = qk::launch_gemv5(type, n_mat, reinterpret_cast<const uint8_t* const*>(W), rows, cols, x, y, sms, s);
-    }
+    if (!qk::hgemv_ok(type, n_mat, rows, cols, sms))
+        return fail(QK_ERR_SHAPE, "cols=%lld: no batched GEMV launch fits", (long long)cols);
+    e = qk::launch_hgemv(type, n_mat, reinterpret_cast<const uint8_t* const*>(W), rows, cols, x, y, sms, status, s);
     if (e != cudaSuccess) return cuda_fail(e, "qk_gemv_batch launch");
     g_last_error.clear();
     return QK_OK;
@@ -319,16 +311,10 @@ qk_status qk_gemv_swiglu(int type, const void* Wg, const void* Wu, int64_t rows,
     unsigned* status = nullptr;
     st = device_state(&status, &sms);
     if (st != QK_OK) return st;
-    cudaError_t e;
-    if (qk::hgemv_ok(type, 1, &rows, cols, sms)) {
-        e = qk::launch_hgemv_swiglu(type, static_cast<const uint8_t*>(Wg), static_cast<const uint8_t*>(Wu), rows, cols,
-                                    x, h, sms, status, s);
-    } else {
-        if (qk::gemv5_ring_pairs(type, 1, &rows, cols, sms) == 0)
-            return fail(QK_ERR_SHAPE, "cols=%lld is too large for the decode kernel", (long long)cols);
-        e = qk::launch_gemv5_swiglu(type, static_cast<const uint8_t*>(Wg), static_cast<const uint8_t*>(Wu), rows, cols,
-                                    x, h, sms, s);
-    }
+    if (!qk::hgemv_ok(type, 1, &rows, cols, sms))
+        return fail(QK_ERR_SHAPE, "rows=%lld cols=%lld: no SwiGLU launch fits", (long long)rows, (long long)cols);
+    const cudaError_t e = qk::launch_hgemv_swiglu(type, static_cast<const uint8_t*>(Wg), static_cast<const uint8_t*>(Wu),
+                                                  rows, cols, x, h, sms, status, s);
     if (e != cudaSuccess) return cuda_fail(e, "qk_gemv_swiglu launch");
     g_last_error.clear();
     return QK_OK;

@@ -18,21 +18,24 @@
 // copy that reaches the end of the cache takes only the bytes that exist),
 // so every byte of the chunk is in flight together; the scores start as
 // soon as the K rows have landed, while V is still arriving.
-// Pass 1: each warp takes every 8th position.  With the group size G known
-// at compile time (and 4 <= G d/32 <= 32), lane l works for head l / (32/G)
-// on G d/32 consecutive elements (inside one block): the group's queries are
-// first turned into three-limb fixed point (as the decode GEMV's activations:
-// x = s (65536 a + 256 b + c) per 32-block, signed 8-bit limbs), so each
-// score is an exact integer dp4a sum over the cache's codes, added over the
-// head's lanes by shuffles.  Otherwise lane l owns d/32 elements and forms its
-// share of q_h . K[t, g] for every head in fp32.  The chunk's softmax
-// statistics (max, sum of exp) follow in shared memory.
-// Pass 2: the same row mapping over V accumulates sum_t e^(s_t - m) V[t, g]
+// Pass 1 runs on the fp16 warp MMA (m16n8k16, fp32 accumulation), the
+// arithmetic of the decode GEMV: A = 16 positions x 16 elements of K codes
+// minus the type's code offset, exact in fp16; B = the group's queries, two
+// fp16 terms (hi, lo) per element after a power-of-two scale per 32-block,
+// one column per (head, term), 8 columns per n-tile; each block's two k16
+// steps are drained into fp32 scores with the block's d and the query
+// block's scale.  Every query element keeps about 22 significant bits
+// whatever the largest element of its block is (massive activations in the
+// query cost no accuracy elsewhere).  Warp w takes the 16-position tiles
+// w, w + 8, ...  The chunk's softmax statistics (max, sum of exp) follow in
+// shared memory.
+// Pass 2: each warp takes every 8th position; lane l owns d/32 elements of
+// V and accumulates sum_t e^(s_t - m) V[t, g]
 // per head; the warps' sums are added in warp order.  A second kernel
 // combines the chunks (log-sum-exp) in a fixed order: deterministic.
 #include "qk_formats.cuh"
 #include "qk_internal.h"
-#include "qk_lanes.cuh"
+#include "qk_hunits.cuh"
 #include "qk_ptx.cuh"
 
 namespace qk {
@@ -192,6 +195,103 @@ __device__ __forceinline__ int code_of_byte(uint32_t b) {
     else return (int)(b & 255u) - (T == T_Q5_0 ? 16 : 8);
 }
 
+// A little-endian word at a 2-byte aligned shared address (the slot has
+// slack past the row, so the second aligned word is always inside it).
+__device__ __forceinline__ uint32_t ldw_a2(const uint8_t* p) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
+    return __funnelshift_r(w[0], w[1], (uint32_t)(a & 3) * 8u);
+}
+
+// Bits 0..3 of z moved to bit 4 of bytes 0..3 (the four products of the
+// multiply land on distinct bits, so nothing carries).
+__device__ __forceinline__ uint32_t bit4_spread(uint32_t z) { return ((z & 15u) * 0x02040810u) & 0x10101010u; }
+
+// The score MMA's A fragments of one 32-weight block of one row (position):
+// the codes minus the type's offset (Q8_0 none, Q5_0 16, Q4_0 8), exact in
+// fp16.  Half s of the block (elements 16 s .. 16 s + 15) is one k16 step;
+// thread tq takes elements 16 s + 4 tq + {0, 2} in a[2 s] (k slots 2 tq,
+// 2 tq + 1) and 16 s + 4 tq + {1, 3} in a[2 s + 1] (slots 2 tq + 8, 2 tq + 9).
+// A code sits in the mantissa of 1024 (or of 64 when it is a high nibble,
+// one unit being 1/16 there) and one fp16 add removes that and the offset.
+template <int T>
+__device__ __forceinline__ void kcodes(const uint8_t* blk, int tq, uint32_t (&a)[4]) {
+    using hm::and_or;
+    using hm::and_xor;
+    using hm::hadd2;
+    if constexpr (T == T_Q8_0) {   // d, 32 signed bytes
+        const uint32_t w0 = ldw_a2(blk + 2 + 4 * tq), w1 = ldw_a2(blk + 18 + 4 * tq);
+        // 0x6480 ^ b = 1024 + 128 + (signed b); minus 1152.
+        a[0] = hadd2(and_xor(w0, 0x00FF00FFu, 0x64806480u), 0xE480E480u);
+        a[1] = hadd2(and_xor(w0 >> 8, 0x00FF00FFu, 0x64806480u), 0xE480E480u);
+        a[2] = hadd2(and_xor(w1, 0x00FF00FFu, 0x64806480u), 0xE480E480u);
+        a[3] = hadd2(and_xor(w1 >> 8, 0x00FF00FFu, 0x64806480u), 0xE480E480u);
+    } else if constexpr (T == T_Q4_0) {   // d, 16 bytes: low nibbles elements 0..15, high 16..31
+        const uint32_t w = ldw_a2(blk + 2 + 4 * tq);
+        a[0] = hadd2(and_or(w, 0x000F000Fu, 0x64006400u), 0xE408E408u);        // 1024 + q - 1032
+        a[1] = hadd2(and_or(w >> 8, 0x000F000Fu, 0x64006400u), 0xE408E408u);
+        a[2] = hadd2(and_or(w, 0x00F000F0u, 0x54005400u), 0xD480D480u);        // 64 + q - 72
+        a[3] = hadd2(and_or(w >> 8, 0x00F000F0u, 0x54005400u), 0xD480D480u);
+    } else {   // Q5_0: d, 32 fifth bits, 16 bytes of nibbles
+        const uint32_t qh = ldw_a2(blk + 2), w = ldw_a2(blk + 6 + 4 * tq);
+        const uint32_t v0 = (w & 0x0F0F0F0Fu) | bit4_spread(qh >> (4 * tq));
+        const uint32_t v1 = ((w >> 4) & 0x0F0F0F0Fu) | bit4_spread(qh >> (16 + 4 * tq));
+        a[0] = hadd2(and_or(v0, 0x00FF00FFu, 0x64006400u), 0xE410E410u);       // 1024 + q - 1040
+        a[1] = hadd2(and_or(v0 >> 8, 0x00FF00FFu, 0x64006400u), 0xE410E410u);
+        a[2] = hadd2(and_or(v1, 0x00FF00FFu, 0x64006400u), 0xE410E410u);
+        a[3] = hadd2(and_or(v1 >> 8, 0x00FF00FFu, 0x64006400u), 0xE410E410u);
+    }
+}
+
+// B fragments of the group's queries (sq: [heads][D] fp32) and the scale of
+// each (head, 32-block).  Per block, x' = q 2^-e with e = max(0,
+// floor(log2 max|q|) - 14), so |x'| < 2^15 fits fp16; hi = fp16(x'), lo =
+// fp16(x' - hi) keep about 22 significant bits of every element, whatever
+// the block's largest element is.  Column gq of n-tile n is head
+// 4 n + gq / 2, term gq % 2 (hi, lo); zero for heads >= G.  Thread (gq, tq)
+// holds elements 32 b + 16 s + 4 tq + {0, 2} / {1, 3} of half s, the order
+// of kcodes.  The four threads of a quad hold the whole block, so its
+// maximum is two shuffles.  sup[h][b] = 2^e (1 for h >= G).
+template <int NB, int NT>
+__device__ __forceinline__ void prep_query(const float* sq, int D, int G, int gq, int tq,
+                                           uint32_t (&bq)[NB][2][NT][2], float* sup) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        const int h = 4 * n + (gq >> 1);
+        const bool live = h < G;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            float v[2][4];
+            float amax = 0.0f;
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                float4 u = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (live) u = *reinterpret_cast<const float4*>(sq + h * D + 32 * b + 16 * s + 4 * tq);
+                v[s][0] = u.x; v[s][1] = u.y; v[s][2] = u.z; v[s][3] = u.w;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fabsf(v[s][k]));
+            }
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            const int e = max(0, (int)((__float_as_uint(amax) >> 23) & 255u) - 127 - 14);
+            const float down = __uint_as_float((uint32_t)(127 - e) << 23);
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                uint32_t hv[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float x = v[s][k] * down;
+                    const __half hi = __float2half_rn(x);
+                    hv[k] = (gq & 1) ? __half_as_ushort(__float2half_rn(x - __half2float(hi))) : __half_as_ushort(hi);
+                }
+                bq[b][s][n][0] = hv[0] | (hv[2] << 16);
+                bq[b][s][n][1] = hv[1] | (hv[3] << 16);
+            }
+            if (tq == 0 && (gq & 1) == 0) sup[h * NB + b] = live ? __uint_as_float((uint32_t)(127 + e) << 23) : 1.0f;
+        }
+    }
+}
+
 template <int T, int NB, int GT, int CH>   // NB = d / 32; GT = heads per kv head when fixed, 0 when not; CH = chunk
 __global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __restrict__ q, const uint8_t* __restrict__ K,
                                                                 const uint8_t* __restrict__ V, int64_t T_len, int n_heads,
@@ -203,9 +303,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __
     extern __shared__ __align__(16) uint8_t dyn[];
     uint8_t* sK = dyn;                           // [CH][SLOT] row windows
     uint8_t* sV = dyn + CH * R::SLOT;
-    __shared__ float sq[GG][D];                  // the group's queries
+    __shared__ __align__(16) float sq[GG][D];    // the group's queries
     __shared__ __align__(16) float ss[CH][GG];   // scores, then e^(s - m), per position
     __shared__ float sred[2][GG];
+    __shared__ float sup[4 * ((2 * GG + 7) / 8)][NB];   // 2^e of each head's query blocks
     const int g = (int)(blockIdx.x % (unsigned)n_kv), c = (int)(blockIdx.x / (unsigned)n_kv), G = n_heads / n_kv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t0 = (int64_t)c * CH;
@@ -223,92 +324,59 @@ __global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __
     cp_async_commit();
     for (int i = threadIdx.x; i < G * D; i += blockDim.x) sq[i / D][i % D] = q[(int64_t)(g * G + i / D) * D + i % D];
     __syncthreads();
-    // Lane l: elements e0 .. e0 + NB - 1 of block eb (pass 2, and pass 1 without a fixed group).
+    // Lane l: elements e0 .. e0 + NB - 1 of block eb (pass 2).
     const int e0 = (lane * NB) & 31, eb = (lane * NB) >> 5;
-    if constexpr (GT > 0) {
-        constexpr int LPH = 32 / GT, EPL = D / LPH, W = EPL / 4;   // lanes per head, elements per lane
-        static_assert(EPL % 4 == 0 && EPL <= 32, "one lane's elements lie in one block");
-        const int h = lane / LPH, ea = (lane % LPH) * EPL;          // head, first element
-        const int kb = ea >> 5, k0 = ea & 31;
-        // The lane's limbs: block maximum over the 32 / EPL lanes that share the block.
-        float qv[EPL], amax = 0.0f;
-#pragma unroll
-        for (int k = 0; k < EPL; ++k) {
-            qv[k] = sq[h][ea + k];
-            amax = fmaxf(amax, fabsf(qv[k]));
-        }
-#pragma unroll
-        for (int o = 1; o < 32 / EPL; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float sx = amax * (1.0f / gv::kXMax);
-        const float inv = amax > 0.0f ? __fdividef(gv::kXMax, amax) : 0.0f;
-        uint32_t la[W], lb[W], lc[W];
-        int xsum = 0;
-#pragma unroll
-        for (int i = 0; i < W; ++i) {
-            uint32_t Y[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int X = __float2int_rn(qv[4 * i + k] * inv);
-                xsum += X;
-                Y[k] = (uint32_t)(X + 0x808080);
-            }
-            la[i] = (((Y[0] >> 16) & 255u) | (((Y[1] >> 16) & 255u) << 8) | (((Y[2] >> 16) & 255u) << 16) |
-                     (((Y[3] >> 16) & 255u) << 24)) ^ 0x80808080u;
-            lb[i] = (((Y[0] >> 8) & 255u) | (((Y[1] >> 8) & 255u) << 8) | (((Y[2] >> 8) & 255u) << 16) |
-                     (((Y[3] >> 8) & 255u) << 24)) ^ 0x80808080u;
-            lc[i] = ((Y[0] & 255u) | ((Y[1] & 255u) << 8) | ((Y[2] & 255u) << 16) | ((Y[3] & 255u) << 24)) ^
-                    0x80808080u;
-        }
-        constexpr float kOff = T == T_Q8_0 ? 0.0f : (T == T_Q5_0 ? 16.0f : 8.0f);
-        const float offx = kOff * (float)xsum;
-        cp_async_wait<1>();   // this thread's K copies
-        __syncthreads();      // ... and everyone's
-        const uint8_t* kblk = sK + warp * R::SLOT + mis + kb * BB;
-        const Codes<T, W> kc(kblk, k0);
-        uint32_t off = 0;
-        for (int j = warp; j < nt; j += kWarps, off += STEP) {
-            uint32_t cw[W];
-            kc.load(off, cw);
-            int A = 0, B = 0, C = 0;
-#pragma unroll
-            for (int i = 0; i < W; ++i) {
-                A = gv::dp4a_ss(cw[i], la[i], A);
-                B = gv::dp4a_ss(cw[i], lb[i], B);
-                C = gv::dp4a_ss(cw[i], lc[i], C);
-            }
-            float v = h2f(lds16(kblk + off)) * (sx * (gv::limbs3_to_f(A, B, C) - offx));
-#pragma unroll
-            for (int o = LPH / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane % LPH == 0) ss[j][h] = scale * v;
-        }
-    } else {
-    float qr[kMaxG][NB];
-#pragma unroll
-    for (int h = 0; h < kMaxG; ++h)
-#pragma unroll
-        for (int k = 0; k < NB; ++k) qr[h][k] = h < G ? sq[h][lane * NB + k] : 0.0f;
-
+    // Pass 1 on the fp16 warp MMA.  A tile is 16 positions; thread (gq, tq)
+    // of the MMA layout (gq = lane / 4, tq = lane % 4) decodes rows gq and
+    // gq + 8 (positions) and holds the B column gq: head 4 nt + gq / 2, term
+    // gq % 2 of the query (hi, lo) in n-tile nt.
+    constexpr int NT = (2 * GG + 7) / 8;
+    const int gq = lane >> 2, tq = lane & 3;
+    uint32_t bq[NB][2][NT][2];
+    prep_query<NB, NT>(&sq[0][0], D, G, gq, tq, bq, &sup[0][0]);
     cp_async_wait<1>();   // this thread's K copies
-    __syncthreads();      // ... and everyone's
-    // Pass 1: scores.
-    const uint8_t* blk = sK + warp * R::SLOT + mis + eb * BB;
-    for (int j = warp; j < nt; j += kWarps, blk += STEP) {
-        const float dk = h2f(ld_u16(blk));
-        int cv[NB];
+    __syncthreads();      // ... and everyone's (and the query scales)
+    float upr[NT][NB];
 #pragma unroll
-        for (int k = 0; k < NB; ++k) cv[k] = code_at<T>(blk, e0 + k);
+    for (int n = 0; n < NT; ++n)
 #pragma unroll
-        for (int h = 0; h < kMaxG; ++h) {
-            if (h >= G) break;
-            float a = 0.0f;
+        for (int b = 0; b < NB; ++b) upr[n][b] = sup[4 * n + tq][b];
+    {
+        // Where row gq starts in its slot: the same in every tile (16 rows
+        // span 16 n_kv ROWB bytes, a multiple of 16) and for row gq + 8.
+        const int misq = (int)((((t0 + gq) * n_kv + g) * ROWB) & 15);
+        const int ntiles = (nt + 15) >> 4;
+        for (int tile = warp; tile < ntiles; tile += kWarps) {
+            const int j0 = 16 * tile + gq;
+            const uint8_t* r0 = sK + j0 * R::SLOT + misq;
+            const uint8_t* r1 = r0 + 8 * R::SLOT;
+            float s0[NT], s1[NT];
 #pragma unroll
-            for (int k = 0; k < NB; ++k) a = fmaf(qr[h][k], (float)cv[k], a);
-            a *= dk;
+            for (int n = 0; n < NT; ++n) s0[n] = s1[n] = 0.0f;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-            if (lane == 0) ss[j][h] = scale * a;
+            for (int b = 0; b < NB; ++b) {
+                uint32_t a0[4], a1[4];
+                kcodes<T>(r0 + b * BB, tq, a0);
+                kcodes<T>(r1 + b * BB, tq, a1);
+                const float d0 = h2f(lds16(r0 + b * BB)), d1 = h2f(lds16(r1 + b * BB));
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    hm::mma16816(c, a0[0], a1[0], a0[1], a1[1], bq[b][0][n][0], bq[b][0][n][1]);
+                    hm::mma16816(c, a0[2], a1[2], a0[3], a1[3], bq[b][1][n][0], bq[b][1][n][1]);
+                    s0[n] = fmaf(d0 * upr[n][b], c[0] + c[1], s0[n]);
+                    s1[n] = fmaf(d1 * upr[n][b], c[2] + c[3], s1[n]);
+                }
+            }
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const int h = 4 * n + tq;
+                if (h < G) {
+                    if (j0 < nt) ss[j0][h] = scale * s0[n];
+                    if (j0 + 8 < nt) ss[j0 + 8][h] = scale * s1[n];
+                }
+            }
         }
-    }
     }
     __syncthreads();
     // Chunk statistics per head: m = max s, then e^(s - m) and their sum.

@@ -54,13 +54,11 @@ struct Args {
     int n;               // matrices (SwiGLU: 1, with W[1] the up matrix)
     int64_t ystride;     // elements between the outputs of consecutive tokens (MT > 1)
     int nxb;             // x-blocks of x (cols / 32)
-    int nxb_pad;         // rounded up to whole units
     int nunits;          // units per row
     int nchunks;         // stages per row (per tile)
     int stages;          // ring depth
     uint32_t slot;       // bytes per row slot of a stage
-    uint32_t off_xb, off_xm, off_ring, off_bar, off_red;
-    uint32_t xtok;       // bytes of one token's B fragments (then its block sums follow the same stride / 8)
+    uint32_t off_xb, off_xm, off_xs, off_ring, off_bar, off_red;
     unsigned* status;
     const uint8_t* W[kMaxGroup];
     float* y[kMaxGroup];
@@ -70,56 +68,59 @@ struct Args {
     int cta0[kMaxGroup + 1];
 };
 
-// x -> B fragments in shared memory.  x-block j (32 elements), plane h:
+// x -> B fragments in shared memory, one unit (256 elements, 8 x-blocks)
+// at a time by the warp that uses it.  Local x-block j of the unit, plane h:
 //   xb[(2j + h) * 64 + 8i] = half2(x_h[4i], x_h[4i+2]), half2(x_h[4i+1], x_h[4i+3])
 // with x' = x * 2^-e, x_0 = fp16(x'), x_1 = fp16(x' - x_0); xm[j] = (sum of x
-// over the block, 2^e, sum over its first 16 elements, over its last 16).  e = 0 unless max|x| of the block reaches 2^15, then
-// the block is scaled into [2^14, 2^15).  Four threads per block (eight
-// elements each); blocks past x are zero.
-__device__ __forceinline__ void prep_x(const float* __restrict__ x, int nxb, int nxb_pad, uint8_t* xb, float4* xm,
-                                       int ctid) {
-    const int q = ctid & 3;
-    for (int base = ctid & ~3; base < nxb_pad * 4; base += kCW * 32) {
-        const int j = (base >> 2);
-        float v[8];
-        if (j < nxb) {
-            const float4 u0 = __ldg(reinterpret_cast<const float4*>(x) + 8 * j + 2 * q);
-            const float4 u1 = __ldg(reinterpret_cast<const float4*>(x) + 8 * j + 2 * q + 1);
-            v[0] = u0.x; v[1] = u0.y; v[2] = u0.z; v[3] = u0.w;
-            v[4] = u1.x; v[5] = u1.y; v[6] = u1.z; v[7] = u1.w;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-        }
-        float amax = 0.0f, sum = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            amax = fmaxf(amax, fabsf(v[i]));
-            sum += v[i];
-        }
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);           // sum of 16 elements (one half)
-        const float other = __shfl_xor_sync(0xffffffffu, sum, 2);
-        // Scale exponent: floor(log2 max|x|) - 14 when that is positive.
-        const int ex = (int)((__float_as_uint(amax) >> 23) & 255u) - 127;
-        const int e = max(0, ex - 14);
-        const float down = __uint_as_float((uint32_t)(127 - e) << 23), up = __uint_as_float((uint32_t)(127 + e) << 23);
-        uint32_t hi[8], lo[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float sv = v[i] * down;
-            const __half h = __float2half_rn(sv);
-            hi[i] = __half_as_ushort(h);
-            lo[i] = __half_as_ushort(__float2half_rn(sv - __half2float(h)));
-        }
-        // Words 2q and 2q+1: elements 8q + {0,2}, {1,3}, {4,6}, {5,7}.
-        *reinterpret_cast<uint4*>(xb + j * kXBB + 16 * q) =
-            make_uint4(hi[0] | hi[2] << 16, hi[1] | hi[3] << 16, hi[4] | hi[6] << 16, hi[5] | hi[7] << 16);
-        *reinterpret_cast<uint4*>(xb + j * kXBB + 64 + 16 * q) =
-            make_uint4(lo[0] | lo[2] << 16, lo[1] | lo[3] << 16, lo[4] | lo[6] << 16, lo[5] | lo[7] << 16);
-        if (q == 0) xm[j] = make_float4(sum + other, up, sum, other);
+// over the block, 2^e, sum over its first 16 elements, over its last 16).
+// e = 0 unless max|x| of the block reaches 2^15, then the block is scaled
+// into [2^14, 2^15).  Lane l takes elements 8q .. 8q + 7 (q = l % 4) of
+// local block l / 4; blocks past x are zero.
+// The unit's x for lane `lane` (eight floats) copied into its 32-byte slot
+// of `xs` without holding registers (cp.async; zeros past x).
+__device__ __forceinline__ void load_unit_x(const float* __restrict__ x, int nxb, int u, int lane, float* xs) {
+    const int j = 8 * u + (lane >> 2), q = lane & 3;
+    float* d = xs + 8 * lane;
+    if (j < nxb) {
+        cp_async16(d, x + 32 * j + 8 * q);
+        cp_async16(d + 4, x + 32 * j + 8 * q + 4);
+    } else {
+        *reinterpret_cast<float4*>(d) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        *reinterpret_cast<float4*>(d + 4) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
+}
+__device__ __forceinline__ void prep_unit_x(const float* xs, uint8_t* xb, float4* xm, int lane) {
+    const int jl = lane >> 2, q = lane & 3;
+    const float4 a = *reinterpret_cast<const float4*>(xs + 8 * lane), b = *reinterpret_cast<const float4*>(xs + 8 * lane + 4);
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float amax = 0.0f, sum = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        amax = fmaxf(amax, fabsf(v[i]));
+        sum += v[i];
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);           // sum of 16 elements (one half)
+    const float other = __shfl_xor_sync(0xffffffffu, sum, 2);
+    // Scale exponent: floor(log2 max|x|) - 14 when that is positive.
+    const int ex = (int)((__float_as_uint(amax) >> 23) & 255u) - 127;
+    const int e = max(0, ex - 14);
+    const float down = __uint_as_float((uint32_t)(127 - e) << 23), up = __uint_as_float((uint32_t)(127 + e) << 23);
+    uint32_t hi[8], lo[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float sv = v[i] * down;
+        const __half h = __float2half_rn(sv);
+        hi[i] = __half_as_ushort(h);
+        lo[i] = __half_as_ushort(__float2half_rn(sv - __half2float(h)));
+    }
+    // Words 2q and 2q+1: elements 8q + {0,2}, {1,3}, {4,6}, {5,7}.
+    *reinterpret_cast<uint4*>(xb + jl * kXBB + 16 * q) =
+        make_uint4(hi[0] | hi[2] << 16, hi[1] | hi[3] << 16, hi[4] | hi[6] << 16, hi[5] | hi[7] << 16);
+    *reinterpret_cast<uint4*>(xb + jl * kXBB + 64 + 16 * q) =
+        make_uint4(lo[0] | lo[2] << 16, lo[1] | lo[3] << 16, lo[4] | lo[6] << 16, lo[5] | lo[7] << 16);
+    if (q == 0) xm[jl] = make_float4(sum + other, up, sum, other);
 }
 
 __device__ __forceinline__ void named_sync_consumers() { asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory"); }
@@ -162,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
     float* part = reinterpret_cast<float*>(smem + p.off_red);   // [tile pass][token][kCW][16]
     uint8_t* xb = smem + p.off_xb;
     float4* xm = reinterpret_cast<float4*>(smem + p.off_xm);
+    float* xst = reinterpret_cast<float*>(smem + p.off_xs);   // [warp][token][256] staged x
     uint8_t* ring = smem + p.off_ring;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -252,17 +254,27 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
     // ---------------- consumers ----------------
     const int ctid = threadIdx.x;
     const int g = lane >> 2, t = lane & 3;
-    const int npart = ntiles * npass * MT * kCW * kTileRows;
-    for (int i = ctid; i < npart; i += kCW * 32) part[i] = 0.0f;
-    pdl_wait_prior();
+    // This warp's partial sums start at zero (only this warp adds into them
+    // until the final barrier).
+    for (int i = lane; i < ntiles * npass * MT * kTileRows; i += 32)
+        part[((i >> 4) * kCW + warp) * kTileRows + (i & 15)] = 0.0f;
+    // This warp's prepared x: its unit of the current chunk, per token.
+    uint8_t* xbw = xb + warp * MT * (8 * kXBB);
+    float4* xmw = xm + warp * MT * 8;
+    float* xsw = xst + warp * MT * 256;
+    pdl_wait_prior();   // x may come from the previous kernel
 #pragma unroll
-    for (int m = 0; m < MT; ++m)
-        prep_x(p.x + (int64_t)m * p.cols, p.nxb, p.nxb_pad, xb + m * p.xtok, xm + m * p.nxb_pad, ctid);
-    named_sync_consumers();
+    for (int m = 0; m < MT; ++m) load_unit_x(p.x + (int64_t)m * p.cols, p.nxb, warp, lane, xsw + m * 256);
+    cp_async_commit();
     // B fragments: the thread whose column g belongs to its group t (g / 2 ==
     // t) reads plane g % 2 of the group's x-blocks; every other thread
     // supplies zeros.
     const bool owner = (g >> 1) == t;
+    // Rows g and g + 8 of every tile start (row * row_bytes) mod 16 bytes
+    // into their slots (a chunk is a multiple of 16 bytes; 16 rows move the
+    // offset by a multiple of 16).
+    const uint32_t o0 = g * p.slot + (uint32_t)(((r_begin + g) * (int64_t)rb) & 15) + warp * U::UB;
+    const uint32_t o1 = (g + 8) * p.slot + (uint32_t)(((r_begin + g + 8) * (int64_t)rb) & 15) + warp * U::UB;
     const int units_last = p.nunits - (p.nchunks - 1) * kCW;
     int s = 0;
     uint32_t ph = 0;
@@ -277,34 +289,41 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
         float4 xm0[MT], xm1[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) xm0[m] = xm1[m] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        // Prepare this chunk's x (loaded one chunk ahead), then request the
+        // next chunk's.
+        cp_async_wait<0>();   // this lane's staged x of the chunk
+        __syncwarp();         // every lane is done reading the previous unit's x
+#pragma unroll
+        for (int m = 0; m < MT; ++m) prep_unit_x(xsw + m * 256, xbw + m * (8 * kXBB), xmw + m * 8, lane);
+        __syncwarp();
+        if (c + 1 < p.nchunks) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) load_unit_x(p.x + (int64_t)m * p.cols, p.nxb, u + kCW, lane, xsw + m * 256);
+            cp_async_commit();
+        }
         if (act) {
-            const uint32_t o0 = ((u * 8 + U::X0(t)) * 2 + (g & 1)) * 64, o1 = ((u * 8 + U::X1(t)) * 2 + (g & 1)) * 64;
+            const uint32_t xo0 = (U::X0(t) * 2 + (g & 1)) * 64, xo1 = (U::X1(t) * 2 + (g & 1)) * 64;
             if constexpr (MT == 1) {
                 if (owner) {
-                    load_xb(xb + o0, bp.x0);
-                    load_xb(xb + o1, bp.x1);
+                    load_xb(xbw + xo0, bp.x0);
+                    load_xb(xbw + xo1, bp.x1);
                 }
             } else {
                 bp.own = owner;
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
-                    bp.p[m][0] = xb + m * p.xtok + o0;
-                    bp.p[m][1] = xb + m * p.xtok + o1;
+                    bp.p[m][0] = xbw + m * (8 * kXBB) + xo0;
+                    bp.p[m][1] = xbw + m * (8 * kXBB) + xo1;
                 }
             }
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                xm0[m] = xm[m * p.nxb_pad + u * 8 + U::X0(t)];
-                xm1[m] = xm[m * p.nxb_pad + u * 8 + U::X1(t)];
+                xm0[m] = xmw[m * 8 + U::X0(t)];
+                xm1[m] = xmw[m * 8 + U::X1(t)];
             }
         }
         const int nvb = min(8, p.nxb - 8 * u);
         for (int tile = 0; tile < ntiles; ++tile) {
-            // Rows g and g + 8 start (row * row_bytes) mod 16 bytes into their
-            // slots (a chunk is a multiple of 16 bytes).
-            const int64_t rt0 = r_begin + tile * kTileRows;
-            const uint32_t o0 = g * p.slot + (uint32_t)(((rt0 + g) * (int64_t)rb) & 15) + warp * U::UB;
-            const uint32_t o1 = (g + 8) * p.slot + (uint32_t)(((rt0 + g + 8) * (int64_t)rb) & 15) + warp * U::UB;
             for (int pass = 0; pass < npass; ++pass) {
                 if (!dead && !wait_phase(&full[s], ph, p.status, abort)) dead = true;
                 float y0[MT], y1[MT];
@@ -384,8 +403,8 @@ int hg_block_elems(int type) { return (type == T_Q8_0 || type == T_Q5_0 || type 
 constexpr int64_t kSmemBudget = 113 * 1024;
 
 struct PlanH {
-    int grid = 0, stages = 0, nunits = 0, nchunks = 0, nxb = 0, nxb_pad = 0;
-    uint32_t slot = 0, off_xb = 0, off_xm = 0, off_ring = 0, off_bar = 0, off_red = 0, smem = 0, xtok = 0;
+    int grid = 0, stages = 0, nunits = 0, nchunks = 0, nxb = 0;
+    uint32_t slot = 0, off_xb = 0, off_xm = 0, off_xs = 0, off_ring = 0, off_bar = 0, off_red = 0, smem = 0;
     int64_t rows_q[hg::kMaxGroup] = {}, rows_r[hg::kMaxGroup] = {};
     int cta0[hg::kMaxGroup + 1] = {};
 };
@@ -400,7 +419,6 @@ PlanH planh(int type, int n, const int64_t* rows, int64_t cols, int sms, int mt,
     const int BB = hg_block_bytes(type), BE = hg_block_elems(type);
     p.nxb = (int)(cols / 32);
     p.nunits = (int)((cols + hg::kUnitW - 1) / hg::kUnitW);
-    p.nxb_pad = p.nunits * 8;
     // CTAs in proportion to each matrix's rows (at least one per non-empty
     // matrix, at most one per row).
     const int64_t G = 2 * (int64_t)std::max(sms, 1);
@@ -419,14 +437,16 @@ PlanH planh(int type, int n, const int64_t* rows, int64_t cols, int sms, int mt,
     // Layout: B fragments of each token, block sums of each token, partial
     // sums [tile pass][token][8 warps][16], mbarriers + abort word, ring.
     const int64_t ntp = (per_cta + hg::kTileRows - 1) / hg::kTileRows * (swiglu ? 2 : 1);
-    p.xtok = (uint32_t)((int64_t)p.nxb_pad * hg::kXBB);
-    const int64_t xbb = (int64_t)mt * p.xtok;
-    const int64_t xmb = (int64_t)mt * p.nxb_pad * 16;
+    // Each consumer warp prepares its own unit of x, per token.
+    const int64_t xbb = (int64_t)mt * hg::kCW * 8 * hg::kXBB;
+    const int64_t xmb = (int64_t)mt * hg::kCW * 8 * 16;
     const int64_t redb = ntp * mt * hg::kCW * hg::kTileRows * 4;
     const int64_t barb = 2 * hg::kMaxStages * 8 + 16;
+    const int64_t xsb = (int64_t)mt * hg::kCW * 256 * 4;   // staged x, 32 bytes per lane per token
     p.off_xb = 0;
     p.off_xm = (uint32_t)xbb;
-    p.off_red = (uint32_t)(xbb + xmb);
+    p.off_xs = (uint32_t)(xbb + xmb);
+    p.off_red = (uint32_t)(xbb + xmb + xsb);
     p.off_bar = (uint32_t)((p.off_red + redb + 15) & ~(int64_t)15);
     p.off_ring = (uint32_t)((p.off_bar + barb + 127) & ~(int64_t)127);
     const int64_t UB = (int64_t)(hg::kUnitW / BE) * BB;
@@ -485,17 +505,16 @@ hg::Args make_args(int type, const PlanH& pl, int64_t cols, const float* x, unsi
     a.cols = cols;
     a.row_bytes = (uint32_t)(cols / hg_block_elems(type) * hg_block_bytes(type));
     a.nxb = pl.nxb;
-    a.nxb_pad = pl.nxb_pad;
     a.nunits = pl.nunits;
     a.nchunks = pl.nchunks;
     a.stages = pl.stages;
     a.slot = pl.slot;
     a.off_xb = pl.off_xb;
     a.off_xm = pl.off_xm;
+    a.off_xs = pl.off_xs;
     a.off_ring = pl.off_ring;
     a.off_bar = pl.off_bar;
     a.off_red = pl.off_red;
-    a.xtok = pl.xtok;
     a.status = status;
     for (int i = 0; i <= hg::kMaxGroup; ++i) a.cta0[i] = pl.cta0[i];
     return a;

@@ -46,6 +46,16 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D = A * B with zero accumulators: the first step of a sum, without
+// clearing four registers first.
+__device__ __forceinline__ void mma16816_z(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};"
+        : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
 // (a & m) | c and (a & m) ^ c as one three-input logic instruction each (the
 // compiler otherwise emits two).
 __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t m, uint32_t c) {
@@ -124,8 +134,9 @@ __device__ __forceinline__ void load_xb(const uint8_t* p, XB& x) {
 //                              bytes 1/3, row g+8 bytes 1/3), A[4..7] for X1
 //   epi(ctx, c, xm0, xm1, t, nvb, y0, y1)   scale the accumulators of one
 //                              token (c[0..1] X0, c[2..3] X1: the two halves
-//                              of each x-block for the 16-weight-group types,
-//                              even / odd steps otherwise) and add the rows'
+//                              of each x-block for the 16-weight-group types;
+//                              otherwise c[0] X0 and c[2] X1, with c[1] and
+//                              c[3] zero) and add the rows'
 //                              sums; nvb = blocks of 32 weights present in
 //                              the unit (8 except in a short last unit).
 
@@ -669,8 +680,10 @@ struct BSmem {
 };
 
 // One unit for MT tokens: each step's A fragments are converted once and
-// multiplied with every token's B; the four accumulators of a token are the
-// two x-blocks' halves (16-weight-group types) or even / odd steps.
+// multiplied with every token's B.  A token's accumulators: the two halves
+// of each x-block for the 16-weight-group types (c[0], c[1] for X0, c[2],
+// c[3] for X1), else one per x-block (c[0] X0, c[2] X1; c[1] and c[3] stay
+// zero and fold away).  The first step of each starts from zero.
 template <int T, int MT, class BP>
 __device__ __forceinline__ void run_unit(const uint8_t* r0, const uint8_t* r1, const BP& bp, const float4 (&xm0)[MT],
                                          const float4 (&xm1)[MT], int t, int nvb, float (&y0)[MT], float (&y1)[MT]) {
@@ -682,12 +695,18 @@ __device__ __forceinline__ void run_unit(const uint8_t* r0, const uint8_t* r1, c
     for (int i = 0; i < 8; ++i) {
         uint32_t A[8];
         U::conv(cx, i, t, A);
-        const int ch = U::kGroup16 ? (i >> 2) : (i & 1);
+        const int ch = U::kGroup16 ? (i >> 2) : 0;
+        const bool first = U::kGroup16 ? (i & 3) == 0 : i == 0;
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             const uint2 b0 = bp.b(m, 0, i), b1 = bp.b(m, 1, i);
-            mma16816(c[m][ch], A[0], A[1], A[2], A[3], b0.x, b0.y);
-            mma16816(c[m][2 + ch], A[4], A[5], A[6], A[7], b1.x, b1.y);
+            if (first) {
+                mma16816_z(c[m][ch], A[0], A[1], A[2], A[3], b0.x, b0.y);
+                mma16816_z(c[m][2 + ch], A[4], A[5], A[6], A[7], b1.x, b1.y);
+            } else {
+                mma16816(c[m][ch], A[0], A[1], A[2], A[3], b0.x, b0.y);
+                mma16816(c[m][2 + ch], A[4], A[5], A[6], A[7], b1.x, b1.y);
+            }
         }
     }
 #pragma unroll

@@ -30,27 +30,16 @@ cudaError_t launch_quantize_imatrix(int type, const float* w, const float* imp, 
 cudaError_t launch_unpack(int type, const uint8_t* W, int64_t nblocks, int16_t* codes, int16_t* sc,
                           uint8_t* mins, float* d, float* dmin, cudaStream_t s);
 
-// GEMV launch plan: how the [rows, cols] x [M] problem is cut into CTAs.
+// qk_gemv's plan: whether the tensor-core GEMV takes the shape (it needs
+// no workspace for any shape).
 struct GemvPlan {
-    bool decode = false; // M == 1 decode kernel (activation prep inside; no workspace)
-    bool tc = false;     // the tensor-core GEMV kernel (qk_hgemv.cu; any M up to 64, no workspace)
+    bool ok = false;
     int sms = 0;         // SM count the plan was made for
-    int mt = 1;          // activation rows per CTA pass (template width)
-    int splits = 1;      // K splits (partials reduced by a second kernel)
     int64_t ws_bytes = 0;
 };
 GemvPlan plan_gemv(int type, int64_t rows, int64_t cols, int64_t M, int sm_count);
-// Decode GEMV (M == 1) over n <= QK_GEMV_BATCH_MAX matrices sharing x:
-// ring depth (row pairs per warp) that fits the kernel's shared memory for
-// this shape (0: K too large, use the prep + tiled kernel).
-int gemv5_ring_pairs(int type, int n, const int64_t* rows, int64_t cols, int sms);
-cudaError_t launch_gemv5(int type, int n, const uint8_t* const* W, const int64_t* rows, int64_t cols, const float* x,
-                         float* const* y, int sms, cudaStream_t s);
-// Decode SwiGLU: h = SiLU(Wg x) * (Wu x), both matrices walked by the same CTAs.
-cudaError_t launch_gemv5_swiglu(int type, const uint8_t* Wg, const uint8_t* Wu, int64_t rows, int64_t cols,
-                                const float* x, float* h, int sms, cudaStream_t s);
-// Tensor-core decode GEMV (qk_hgemv.cu): whether it takes this shape (type
-// supported, x and two stages fit shared memory), the plain / batched launch
+// Tensor-core GEMV (qk_hgemv.cu): whether it takes this shape (type
+// supported, two ring stages fit shared memory), the plain / batched launch
 // (n <= QK_GEMV_BATCH_MAX matrices sharing x) and the SwiGLU launch.
 bool hgemv_ok(int type, int n, const int64_t* rows, int64_t cols, int sms);
 cudaError_t launch_hgemv(int type, int n, const uint8_t* const* W, const int64_t* rows, int64_t cols, const float* x,
@@ -61,7 +50,7 @@ cudaError_t launch_hgemv_swiglu(int type, const uint8_t* Wg, const uint8_t* Wu, 
 cudaError_t launch_hgemv_tokens(int type, const uint8_t* W, int64_t rows, int64_t cols, const float* x, int64_t M,
                                 float* y, int sms, unsigned* status, cudaStream_t s);
 cudaError_t launch_gemv(int type, const GemvPlan& plan, const uint8_t* W, int64_t rows, int64_t cols,
-                        const float* x, int64_t M, float* y, float* ws, unsigned* status, cudaStream_t s);
+                        const float* x, int64_t M, float* y, unsigned* status, cudaStream_t s);
 
 // One thread waiting on an mbarrier nothing arrives on (bounded by limit_ns).
 cudaError_t launch_stalled_wait(unsigned* status, uint64_t limit_ns, cudaStream_t s);

@@ -210,29 +210,38 @@ qk_status qk_quantize_imatrix(int type, const float* w, int64_t rows, int64_t co
  *   x      fp32 [cols], 16-byte aligned.
  *   h      fp32 [rows], 4-byte aligned; fully overwritten.
  * Accuracy: g and u each as qk_gemv (1e-4 * sum|w x| + 1e-6), then the fp32
- * epilogue (expf, one division, one product).  QK_ERR_SHAPE when cols is too
- * large for the decode kernel's shared memory (the same limit as qk_gemv_batch).
+ * epilogue (expf, one division, one product).  No limit on cols beyond the
+ * format's.
  * rows == 0 queues nothing; cols == 0 zero-fills h. */
 qk_status qk_gemv_swiglu(int type, const void* Wg, const void* Wu, int64_t rows, int64_t cols,
                          const float* x, float* h, void* stream);
 
-/* Workspace bytes qk_gemv needs for this problem on the current device (0
- * when it needs none).  The value depends on the device's SM count. */
+/* Workspace bytes qk_gemv needs for this problem: 0 for every shape (the
+ * kernel prepares its activations in shared memory).  Kept so that callers
+ * written against a workspace-taking GEMV need no change. */
 size_t qk_gemv_workspace(int type, int64_t rows, int64_t cols, int64_t M);
 
-/* Fused dequant-GEMV for decode: y[m, n] = sum_k w[n, k] * x[m, k] for
- * m < M, n < rows, with every weight unpacked in registers inside the dot
- * product and never written out ("Local LLM inference", "The mmap backend":
- * blocks dequantized inside the dot product; each weight decoded once per
- * input batch and reused across its rows).  fp32 activations and
- * accumulation.
+/* Fused dequant-GEMV: y[m, n] = sum_k w[n, k] * x[m, k] for m < M,
+ * n < rows, with every weight unpacked in registers inside the dot product
+ * and never written out ("Local LLM inference", "The mmap backend": blocks
+ * dequantized inside the dot product; each weight decoded once per input
+ * batch and reused across its rows).  fp32 activations, fp32 accumulation.
  *   W  [rows, cols] packed blocks, 16-byte aligned.
  *   x  fp32 [M, cols] row-major, 16-byte aligned.
  *   y  fp32 [M, rows] row-major, 4-byte aligned; fully overwritten.
- *   ws workspace of ws_bytes >= qk_gemv_workspace(...) bytes, 16-byte
- *      aligned (may be NULL when that is 0).  Its contents need no
- *      initialisation and are garbage afterwards.
- * Accuracy: |y - y_exact| <= 1e-4 * sum_k |w x| + 1e-6 per output.
+ *   ws, ws_bytes  ignored (no shape needs a workspace; NULL, 0 is fine).
+ * Kernel: the fp16 warp MMA with exact integer codes (the code minus an
+ * integer offset) and x as two fp16 terms per element after a power-of-two
+ * scale per 32-element block; one launch for M == 1, one per pair of
+ * activation rows otherwise (each launch streams W once).
+ * Accuracy: |y - y_exact| <= 1e-4 * sum_k |w x| + 1e-6 per output.  The
+ * per-element error model behind it: |x - (hi + lo) 2^e| <= 2^-22 |x| +
+ * 2^(e-25), with 2^e <= 2^-14 times the block's largest magnitude when e > 0
+ * (so elements down to 2^-17 of that magnitude keep 22 significant bits);
+ * codes are exact, and a weight that is exactly zero contributes exactly
+ * zero.  So blocks holding massive activations (tested at 1e3, 1e4
+ * and 1e5 times the others, beside zero and tiny weights) stay within the
+ * bound; the remaining terms are fp32 roundings of the block sums and scales.
  * Results are deterministic run to run (fixed reduction order).
  * rows == 0 or M == 0 queues nothing; cols == 0 zero-fills y. */
 qk_status qk_gemv(int type, const void* W, int64_t rows, int64_t cols,
@@ -257,17 +266,11 @@ qk_status qk_gemv(int type, const void* W, int64_t rows, int64_t cols,
  *   x     fp32 [cols] (one activation row), 16-byte aligned, device.
  *   y     host array of n_mat device pointers, y[i] = fp32 [rows[i]], 4-byte
  *         aligned; fully overwritten.
- * The host arrays are read during the call only.  No workspace.  K is
- * limited by the kernel's shared memory (the limbs of x take 112 bytes per
- * 32 elements, beside at least four row slots per warp): about 12K columns
- * for Q8_0 up to about 21K for Q4_K; a larger cols is QK_ERR_SHAPE.
- * n_mat outside 1..QK_GEMV_BATCH_MAX is QK_ERR_ARG.  Accuracy and
- * determinism as qk_gemv. */
+ * The host arrays are read during the call only.  No workspace, no limit on
+ * cols beyond the format's.  n_mat outside 1..QK_GEMV_BATCH_MAX is
+ * QK_ERR_ARG.  Kernel, accuracy and determinism as qk_gemv with M == 1. */
 qk_status qk_gemv_batch(int type, int n_mat, const void* const* W, const int64_t* rows, int64_t cols,
                         const float* x, float* const* y, void* stream);
-
-/* Size of the fixed scratch array qk_gemv_noalloc uses: 8 MiB per device. */
-#define QK_GEMV_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 
 /* qk_gemv for callers that cannot allocate device memory.  The pages have no
  * counterpart; this is a convenience of this library.  Some callers of a
@@ -276,23 +279,15 @@ qk_status qk_gemv_batch(int type, int n_mat, const void* const* W, const int64_t
  * budget that must not grow its footprint while serving, and paths that
  * cannot afford the device-wide synchronization that cudaMalloc / cudaFree
  * can cause.  They call this instead of qk_gemv and pass no workspace.
- *   Arguments, results, accuracy and errors are those of qk_gemv.
- *   Scratch: one array of QK_GEMV_NOALLOC_SCRATCH_BYTES that the library
- *     holds in device memory on every GPU that loads it, until the process
- *     exits.  Problems needing more scratch than that (qk_gemv_workspace()
- *     larger than the array) are rejected with QK_ERR_WORKSPACE and nothing
- *     is queued.  This call itself allocates nothing.
- *   Set-up: the first call on each device, with that device current, looks
- *     up the array's device address; make that first call before starting
- *     any stream capture.  The library keeps that address (and the address
- *     of its device status word) per device for the life of the process; a
- *     cudaDeviceReset() unloads the module and leaves them stale, so make no
- *     qk_* call on a device after resetting it.
- *   Sharing: every call on a device uses the same array and leaves its
- *     contents behind; each call clears what must start at zero itself.
- *     Calls whose kernels overlap on the GPU (different streams without an
- *     ordering between them) race on the array and give wrong results;
- *     order them on one stream or with events. */
+ *   Arguments, results, accuracy and errors are those of qk_gemv; argument
+ *   errors are reported exactly as qk_gemv reports them.
+ *   Scratch: none.  The GEMV kernel prepares its activations in shared
+ *   memory, so no shape needs a workspace; this call allocates nothing and
+ *   holds no device memory of its own.
+ *   Set-up: the first qk_* call on a device looks up the library's device
+ *   status word; make it before starting any stream capture.  A
+ *   cudaDeviceReset() unloads the module and leaves that address stale, so
+ *   make no qk_* call on a device after resetting it. */
 qk_status qk_gemv_noalloc(int type, const void* W, int64_t rows, int64_t cols,
                           const float* x, int64_t M, float* y, void* stream);
 

@@ -107,7 +107,7 @@ def test_gemv_outliers_decode(gpu, name, shape_i, ratio):
 
 
 @pytest.mark.parametrize("name", NAMES)
-@pytest.mark.parametrize("M", [2, 3, 8])
+@pytest.mark.parametrize("M", [2, 3, 8, 72])
 @pytest.mark.parametrize("ratio", [1e4, 1e5])
 def test_gemv_outliers_batched_tokens(gpu, name, M, ratio):
     rows, cols = SHAPES[name][1]
