@@ -58,7 +58,7 @@ def layer_bytes(layer, groups):
 
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemv_decode_q4k_traffic.json")
-KERNEL_SOURCES = ["qk_gemv5.cu", "qk_lanes.cuh", "qk_ptx.cuh", "qk_formats.cuh"]
+KERNEL_SOURCES = ["qk_hgemv.cu", "qk_hunits.cuh", "qk_ptx.cuh", "qk_formats.cuh"]
 
 
 def kernel_sources_digest():
@@ -70,30 +70,32 @@ def kernel_sources_digest():
     return h.hexdigest()
 
 
-def recorded_traffic():
-    """DRAM bytes per Q4_K decode launch of the step (mean over q/k/v, o and
-    gate/up) from the committed ncu summary, or None when the kernel sources
-    changed since it was captured."""
+def recorded_traffic(key="mean_dram_bytes_per_launch"):
+    """DRAM bytes per decode launch from the committed ncu summary: the mean
+    over the Q4_K launches of the step (q/k/v, o, gate/up), or with
+    key="q6k_dram_bytes_per_launch" the Q6_K down launch; None when the
+    kernel sources changed since it was captured."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
         if rec.get("kernel_sources_sha256") != kernel_sources_digest():
             return None
-        return float(rec["mean_dram_bytes_per_launch"])
+        return float(rec[key])
     except Exception:
         return None
 
 
+# 4 launches per step (q/k/v, o, gate/up, down); skip 8 warm-up steps, take 3.
 TRAFFIC_COMMAND = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
-                   "--clock-control none -k regex:gemv5 -s 32 -c 12 --csv --log-file traffic.csv "
+                   "--clock-control none -k regex:hgemv -s 32 -c 12 --csv --log-file traffic.csv "
                    "python bench.py --steps 20 --warmup 3 --min-warmup-s 0 --no-cpu --no-gemm --no-stack "
-                   "--no-sweep --no-quant --no-swiglu --no-attn")
+                   "--no-sweep --no-quant --no-swiglu --no-attn --no-codes-check")
 
 
 def record_traffic(csv_path: str) -> dict:
     """Write TRAFFIC_FILE from the launch list of TRAFFIC_COMMAND: DRAM bytes
-    (read + write) per Q4_K decode launch, labelled q/k/v, o, gate/up in step
-    order, with the digest of the kernel sources it was taken on."""
+    (read + write) per decode launch, labelled q/k/v, o, gate/up, down in
+    step order, with the digest of the kernel sources it was taken on."""
     import csv
     rows = list(csv.reader(open(csv_path)))
     h = next(i for i, r in enumerate(rows) if "Metric Name" in r)
@@ -103,15 +105,17 @@ def record_traffic(csv_path: str) -> dict:
     for r in data:
         if len(r) > vi:
             launches.setdefault(r[ii], {"kernel": r[ki]})[r[mi]] = float(r[vi].replace(",", ""))
-    q4 = [v for v in launches.values() if "gemv5_kernel<1," in v["kernel"].replace(" ", "")]
-    labels = ("qkv", "o", "gate_up")
+    labels = ("qkv", "o", "gate_up", "down")
     per = {lab: [] for lab in labels}
-    for n, v in enumerate(q4):
-        per[labels[n % 3]].append(v["dram__bytes_read.sum"] + v["dram__bytes_write.sum"])
+    for n, v in enumerate(launches.values()):
+        per[labels[n % 4]].append(v["dram__bytes_read.sum"] + v["dram__bytes_write.sum"])
     means = {lab: int(round(sum(x) / len(x))) for lab, x in per.items() if x}
-    rec = {"kernel": "gemv5_kernel<Q4_K, NP> (decode GEMV), the three Q4_K launches of one Llama-7B-shaped layer step",
+    q4 = [means[lab] for lab in ("qkv", "o", "gate_up") if lab in means]
+    rec = {"kernel": "hgemv_kernel<Q4_K> (q/k/v, o, gate/up) and hgemv_kernel<Q6_K> (down): the tensor-core "
+                     "decode GEMV, the four launches of one Llama-7B-shaped layer step",
            "command": TRAFFIC_COMMAND, "dram_bytes_per_launch": means,
-           "mean_dram_bytes_per_launch": int(round(sum(means.values()) / len(means))),
+           "mean_dram_bytes_per_launch": int(round(sum(q4) / len(q4))),
+           "q6k_dram_bytes_per_launch": means.get("down"),
            "note": "read + write; writes are ~0 (the outputs stay in L2 within the launch)",
            "kernel_sources": KERNEL_SOURCES, "kernel_sources_sha256": kernel_sources_digest()}
     with open(TRAFFIC_FILE, "w") as f:
@@ -193,18 +197,34 @@ def _max_over_ranks(v: float, world: int) -> float:
     return float(t.item())
 
 
-def build_layer_copies(dev, ncopies):
+def build_layer_copies(dev, ncopies, quantized=True):
     """ncopies distinct layers of packed weights on the device, plus one
-    activation vector per launch group and one output per matrix."""
+    activation vector per launch group and one output per matrix.  The codes
+    come from the library's quantizer applied to seeded N(0, 0.02) fp32
+    weights, or (quantized=False) are seeded random bytes with random fp16
+    scales."""
     import torch
+    import gguf_quant_dequant_gb300 as qk
     import synth
     layer, groups = synth.LLAMA7B_LAYER, synth.LLAMA7B_LAYER_GROUPS
-    Ws = [[synth.random_blocks_torch(name, rows, cols, 100 * c + i, dev)
-           for i, (_, name, rows, cols) in enumerate(layer)] for c in range(ncopies)]
+    Ws = []
+    for c in range(ncopies):
+        Wc = []
+        for i, (_, name, rows, cols) in enumerate(layer):
+            if quantized:
+                gw = torch.Generator(device=dev)
+                gw.manual_seed(100 * c + i)
+                w = torch.randn((rows, cols), device=dev, generator=gw) * 0.02
+                Wc.append(qk.quantize(synth.TYPE_IDS[name], w))
+                del w
+            else:
+                Wc.append(synth.random_blocks_torch(name, rows, cols, 100 * c + i, dev))
+        Ws.append(Wc)
     g = torch.Generator(device=dev)
     g.manual_seed(4242)
     xs = [torch.randn(layer[grp[0]][3], device=dev, generator=g) for grp in groups]
     ys = [torch.empty(rows, device=dev) for (_, _, rows, _) in layer]
+    torch.cuda.synchronize()
     return layer, groups, Ws, xs, ys
 
 
@@ -267,9 +287,11 @@ def run_gpu(args):
         return g
 
     q4_groups = [gi for gi, grp in enumerate(groups) if layer[grp[0]][1] == "Q4_K"]
+    q6_groups = [gi for gi, grp in enumerate(groups) if layer[grp[0]][1] == "Q6_K"]
     g_all = capture(lambda: [step(c) for c in range(ncopies)])
     graphs = [capture(lambda c=c: step(c)) for c in range(ncopies)]
     q4_all = capture(lambda: [sub_step(c, q4_groups) for c in range(ncopies)])
+    q6_all = capture(lambda: [sub_step(c, q6_groups) for c in range(ncopies)])
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
@@ -311,6 +333,13 @@ def run_gpu(args):
         f1.record(stream)
         torch.cuda.synchronize()
         q4_ms = f0.elapsed_time(f1)
+        # The Q6_K down launch alone, same rotation.
+        f0.record(stream)
+        for _ in range(reps):
+            q6_all.replay()
+        f1.record(stream)
+        torch.cuda.synchronize()
+        q6_ms = f0.elapsed_time(f1)
     clocks = clk.summary()
     ms_max = _max_over_ranks(ms, world)
     ms_step = ms_max / K
@@ -319,9 +348,38 @@ def run_gpu(args):
     q4_launch_bytes = sum(group_bytes(layer, groups[gi]) for gi in q4_groups) / len(q4_groups)
     q4_launch_ms = q4_ms / (reps * ncopies * len(q4_groups))
     achieved = q4_launch_bytes / (q4_launch_ms * 1e-3) / 1e9
+    q6_launch_bytes = sum(group_bytes(layer, groups[gi]) for gi in q6_groups) / len(q6_groups)
+    q6_launch_ms = q6_ms / (reps * ncopies * len(q6_groups))
+    achieved_q6 = q6_launch_bytes / (q6_launch_ms * 1e-3) / 1e9
+
+    # The same step on random-byte codes (random fp16 scales), to show the
+    # timing does not depend on how the codes were made.
+    codes_check = None
+    if not args.no_codes_check:
+        del graphs, g_all, q4_all, q6_all
+        _, _, Wr, _, _ = build_layer_copies(dev, ncopies, quantized=False)
+        gr = capture(lambda: [[run_group(layer, grp, Wr[c], xs[gi], ys) for gi, grp in enumerate(groups)]
+                              for c in range(ncopies)])
+        for _ in range(3):
+            gr.replay()
+        torch.cuda.synchronize()
+        r0 = torch.cuda.Event(enable_timing=True)
+        r1 = torch.cuda.Event(enable_timing=True)
+        nrep = max(K // ncopies, 1)
+        r0.record(stream)
+        for _ in range(nrep):
+            gr.replay()
+        r1.record(stream)
+        torch.cuda.synchronize()
+        rand_step = r0.elapsed_time(r1) / (nrep * ncopies)
+        codes_check = {"quantized_codes_ms_per_step": round(ms / K, 6),
+                       "random_byte_codes_ms_per_step": round(rand_step, 6),
+                       "ratio_random_over_quantized": round(rand_step / (ms / K), 4)}
+        del Wr, gr
+        graphs = g_all = q4_all = q6_all = None
 
     e2e = run_e2e(args, dev, layer, groups, Ws[0], xs, lb) if rank == 0 else None
-    del Ws, graphs, g_all, q4_all
+    del Ws, graphs, g_all, q4_all, q6_all
     torch.cuda.empty_cache()
     stack = run_stack(dev) if (rank == 0 and not args.no_stack) else None
     sweep = run_ffn_sweep(dev) if (rank == 0 and not args.no_sweep) else None
@@ -345,7 +403,7 @@ def run_gpu(args):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "q4_k/q6_k blocks, f32 activations and accumulation",
-            "data": "synthetic (seeded random blocks, x ~ N(0,1))",
+            "data": "synthetic (codes from qk_quantize of seeded N(0, 0.02) fp32 weights, x ~ N(0,1))",
             "config": {"workload": "Llama-7B-shaped decoder layer, decode batch 1: q/k/v/o 4096x4096 Q4_K, "
                                    "gate/up 11008x4096 Q4_K, down 4096x11008 Q6_K",
                        "launches": "q/k/v one qk_gemv_batch (shared x), o qk_gemv, gate/up one qk_gemv_batch "
@@ -357,10 +415,16 @@ def run_gpu(args):
                        "timing": f"one CUDA graph of {ncopies} consecutive layer steps (one per copy), "
                                  "replayed; CUDA events on the launch stream"},
             "frac_of_peak": round(value / world / hbm_peak, 4),
-            "roofline": {"bound": "hbm", "kernel": "gemv5_kernel<Q4_K> (decode; q/k/v, o and gate/up launches)",
+            "roofline": {"bound": "hbm", "kernel": "hgemv_kernel<Q4_K> (decode; q/k/v, o and gate/up launches)",
                          "achieved": round(achieved, 2), "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s",
                          "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                          "launch_bytes": int(q4_launch_bytes), "launch_us": round(q4_launch_ms * 1e3, 3)},
+            "roofline_q6k": {"bound": "hbm", "kernel": "hgemv_kernel<Q6_K> (decode; the down launch)",
+                             "achieved": round(achieved_q6, 2), "peak": hbm_peak, "peak_source": peak_src,
+                             "unit": "GB/s", "frac": round(achieved_q6 / hbm_peak, 4),
+                             "traffic": recorded_traffic("q6k_dram_bytes_per_launch"),
+                             "launch_bytes": int(q6_launch_bytes), "launch_us": round(q6_launch_ms * 1e3, 3)},
+            "codes_check": codes_check,
             "gpu_launches": K * len(groups),
             "clocks": clocks,
             "e2e": e2e,
@@ -916,6 +980,8 @@ def main():
                     help="write the decode kernel's DRAM-traffic record from the launch list of its ncu command")
     ap.add_argument("--no-swiglu", action="store_true", help="skip the fused SwiGLU leg")
     ap.add_argument("--no-attn", action="store_true", help="skip the quantized-KV attention leg")
+    ap.add_argument("--no-codes-check", action="store_true",
+                    help="skip timing the layer a second time on random-byte codes")
     ap.add_argument("--attn-only", action="store_true", help="run the quantized-KV attention leg alone")
     ap.add_argument("--swiglu-only", action="store_true",
                     help="run only the fused SwiGLU leg and print its JSON (for profiling)")

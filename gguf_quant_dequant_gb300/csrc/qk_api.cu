@@ -211,8 +211,12 @@ qk_status qk_attn_decode(int type, const float* q, const void* K, const void* V,
         return fail(QK_ERR_ALIGN, "q, out and ws must be 4-byte aligned, K and V 16-byte aligned");
     const int64_t need = qk::attn_decode_ws_bytes(T, n_heads, d);
     if (ws_bytes < (size_t)need) return fail(QK_ERR_WORKSPACE, "workspace %zu bytes < %lld needed", ws_bytes, (long long)need);
+    unsigned* status = nullptr;
+    int sms = 0;
+    const qk_status st = device_state(&status, &sms);
+    if (st != QK_OK) return st;
     cudaError_t e = qk::launch_attn_decode(type, q, static_cast<const uint8_t*>(K), static_cast<const uint8_t*>(V), T,
-                                           n_heads, n_kv, d, scale, out, static_cast<float*>(ws),
+                                           n_heads, n_kv, d, scale, out, static_cast<float*>(ws), status, sms,
                                            static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "qk_attn_decode launch");
     g_last_error.clear();

@@ -33,10 +33,13 @@
 // V and accumulates sum_t e^(s_t - m) V[t, g]
 // per head; the warps' sums are added in warp order.  A second kernel
 // combines the chunks (log-sum-exp) in a fixed order: deterministic.
+#include <algorithm>
+
 #include "qk_formats.cuh"
 #include "qk_internal.h"
 #include "qk_hunits.cuh"
 #include "qk_ptx.cuh"
+#include "qk_tc.cuh"
 
 namespace qk {
 namespace attn {
@@ -467,6 +470,325 @@ __global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __
     }
 }
 
+// ---------------------------------------------------------------------------
+// Streaming kernel.  CTA (g, c) takes kv head g and positions [c P, c P + P)
+// (P a multiple of the stage), so the query preparation, the final merge
+// and the partial written per CTA are paid once per ~P positions.  A
+// producer thread streams each stage (128 positions) of the K and of the V
+// rows into a ring as one 2D TMA box each: the cache seen as [T, n_kv ROWB]
+// bytes, the box the 16-byte aligned window of head g's rows (the same
+// offset in every position) x 128 positions; positions past T arrive as
+// zeros.  One copy request per stage instead of one per row keeps the copy
+// engine off the critical path (a bulk copy costs a fixed few tens of
+// cycles, more than a 144-byte row takes to stream).  Consumer warp w takes
+// positions 16 w .. 16 w + 15 of every stage and keeps its own running
+// softmax (max and sum per head, flash-attention style): scores of its tile
+// on the MMA as in the chunk kernel, then p = e^(s - m) rescales and feeds
+// its fp32 sums of p V (lane l owns d/32 elements of V for every head).  At
+// the end the eight warps' (m, l, o) are merged in warp order: the result
+// does not depend on timing.
+constexpr int kSW = 8;                      // consumer warps
+constexpr int kSThreads = (kSW + 1) * 32;   // + the producer warp
+constexpr int kSPos = 16 * kSW;             // positions per stage
+constexpr int kSMaxStages = 6;
+constexpr int kSBudget = 112 * 1024;        // shared memory per CTA (two CTAs per SM)
+
+template <int T, int NB> struct SGeo {
+    static constexpr int ROWB = NB * Fmt<T>::BB;
+    // Head g's rows start g ROWB bytes into a position's n_kv ROWB bytes, at
+    // most 16 - gcd(ROWB, 16) bytes past a 16-byte boundary; the box (SLOT
+    // bytes wide, at most 256) covers that window, rounded up to 16 bytes.
+    static constexpr int ALIGN = (ROWB & 15) == 0 ? 16 : ((ROWB & 7) == 0 ? 8 : ((ROWB & 3) == 0 ? 4 : 2));
+    static constexpr int SLOT = (ROWB + 16 - ALIGN + 15) / 16 * 16;
+    static constexpr int HALF = kSPos * SLOT;   // the K (or V) rows of a stage
+    static constexpr int STAGE = 2 * HALF;
+    static_assert(HALF % 128 == 0, "stages and halves start 128-byte aligned");
+};
+
+// Shared-memory map of the streaming kernel: ring (+16 bytes for word reads
+// past the last row), queries [G][D], p [warp][16][G], rescale factors
+// [warp][G], mbarriers and the abort word.
+template <int T, int NB, int G> struct SMap {
+    static constexpr int D = 32 * NB;
+    __host__ __device__ static constexpr int off_q(int nstg) { return nstg * SGeo<T, NB>::STAGE + 16; }
+    __host__ __device__ static constexpr int off_p(int nstg) { return off_q(nstg) + G * D * 4; }
+    __host__ __device__ static constexpr int off_a(int nstg) { return off_p(nstg) + kSW * 16 * G * 4; }
+    __host__ __device__ static constexpr int off_bar(int nstg) { return (off_a(nstg) + kSW * G * 4 + 7) / 8 * 8; }
+    // + 128 bytes to align the ring.
+    __host__ __device__ static constexpr int bytes(int nstg) { return off_bar(nstg) + 2 * kSMaxStages * 8 + 16 + 128; }
+};
+
+__device__ __forceinline__ void named_sync_stream_consumers() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kSW * 32) : "memory");
+}
+
+template <int T, int NB, int G>   // NB = d / 32; G = query heads per kv head
+__global__ void __launch_bounds__(kSThreads, 2) attn_stream_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                  const __grid_constant__ CUtensorMap vmap,
+                                                                  const float* __restrict__ q, int64_t T_len, int n_kv,
+                                                                  float scale, float* __restrict__ ws, int P,
+                                                                  int nsplit, int nstg, unsigned* status) {
+    using Gm = SGeo<T, NB>;
+    using Mp = SMap<T, NB, G>;
+    constexpr int D = 32 * NB, BB = Fmt<T>::BB;
+    constexpr int NT = (2 * G + 7) / 8;
+    constexpr int64_t ROWB = Gm::ROWB;
+    extern __shared__ __align__(16) uint8_t dyn[];
+    // The TMA boxes land at 128-byte aligned addresses (stages and halves
+    // are multiples of 128 bytes; the launch adds 128 bytes of room).
+    uint8_t* base = dyn + ((128u - (smem_u32(dyn) & 127u)) & 127u);
+    uint8_t* ring = base;
+    float* sq = reinterpret_cast<float*>(base + Mp::off_q(nstg));
+    float* sp = reinterpret_cast<float*>(base + Mp::off_p(nstg));
+    float* sa = reinterpret_cast<float*>(base + Mp::off_a(nstg));
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + Mp::off_bar(nstg));
+    uint64_t* empty = full + kSMaxStages;
+    volatile int* abort = reinterpret_cast<volatile int*>(empty + kSMaxStages);
+    __shared__ float sup[4 * NT][NB];   // 2^e of each head's query blocks
+
+    const int g = (int)(blockIdx.x % (unsigned)n_kv), c = (int)(blockIdx.x / (unsigned)n_kv);
+    const int64_t p0 = (int64_t)c * P, p1 = min(T_len, p0 + P);
+    const int nst = (int)((p1 - p0 + kSPos - 1) / kSPos);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int xg = (int)(((int64_t)g * ROWB) & ~(int64_t)15);   // box start in a position's bytes
+    const int misg = (int)(((int64_t)g * ROWB) & 15);             // where head g's row starts in the box
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < nstg; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kSW);
+        }
+        *abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+    pdl_wait_prior();   // the cache and the query may come from the previous kernel
+
+    if (warp == kSW) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            int slot = 0, issued = 0;
+            uint32_t ph = 0;
+            for (int st = 0; st < nst; ++st) {
+                if (st >= nstg && !mbar_wait_abortable(&empty[slot], ph ^ 1u, status, abort)) break;
+                uint8_t* dst = ring + slot * Gm::STAGE;
+                const int y = (int)(p0 + (int64_t)st * kSPos);
+                mbar_arrive_expect_tx(&full[slot], (uint32_t)Gm::STAGE);
+                tc::tma_load_2d(dst, &kmap, xg, y, &full[slot]);
+                tc::tma_load_2d(dst + Gm::HALF, &vmap, xg, y, &full[slot]);
+                ++issued;
+                if (++slot == nstg) {
+                    slot = 0;
+                    ph ^= 1u;
+                }
+            }
+            // Every copy requested lands before the CTA may exit.
+            for (int k = max(0, issued - nstg); k < issued; ++k)
+                mbar_wait_bounded(&full[k % nstg], (uint32_t)(k / nstg) & 1u, status);
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    const int tid = threadIdx.x;
+    for (int i = tid; i < G * D; i += kSW * 32) sq[i] = q[(int64_t)g * G * D + i];
+    named_sync_stream_consumers();
+    const int gq = lane >> 2, tq = lane & 3;
+    uint32_t bq[NB][2][NT][2];
+    prep_query<NB, NT>(sq, D, G, gq, tq, bq, &sup[0][0]);
+    named_sync_stream_consumers();
+    float upr[NT][NB];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int b = 0; b < NB; ++b) upr[n][b] = sup[4 * n + tq][b];
+    const int e0 = (lane * NB) & 31, eb = (lane * NB) >> 5;   // this lane's elements of V
+    const float kNegInf = -__int_as_float(0x7f800000);
+    float m_run[NT], l_part[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        m_run[n] = kNegInf;
+        l_part[n] = 0.0f;
+    }
+    // Sums of p V: heads in pairs (packed fp32 FMAs), this lane's elements.
+    constexpr int GP = (G + 1) / 2;
+    float2 acc[GP][NB];
+#pragma unroll
+    for (int h = 0; h < GP; ++h)
+#pragma unroll
+        for (int k = 0; k < NB; ++k) acc[h][k] = make_float2(0.0f, 0.0f);
+    float* spw = sp + warp * 16 * G;
+    float* saw = sa + warp * G;
+    int slot = 0;
+    uint32_t ph = 0;
+    bool dead = false;
+    for (int st = 0; st < nst; ++st) {
+        if (!dead && !mbar_wait_abortable(&full[slot], ph, status, abort)) dead = true;
+        const int jt = 16 * warp;
+        const int64_t tp0 = p0 + (int64_t)st * kSPos + jt;
+        const int nvalid = (int)max((int64_t)0, min((int64_t)16, p1 - tp0));
+        if (!dead && nvalid > 0) {
+            const uint8_t* kst = ring + slot * Gm::STAGE;
+            const uint8_t* vst = kst + Gm::HALF;
+            // Scores of positions gq and gq + 8 of the tile.
+            const uint8_t* r0 = kst + (jt + gq) * Gm::SLOT + misg;
+            const uint8_t* r1 = r0 + 8 * Gm::SLOT;
+            float s0[NT], s1[NT];
+#pragma unroll
+            for (int n = 0; n < NT; ++n) s0[n] = s1[n] = 0.0f;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                uint32_t a0[4], a1[4];
+                kcodes<T>(r0 + b * BB, tq, a0);
+                kcodes<T>(r1 + b * BB, tq, a1);
+                const float d0 = h2f(lds16(r0 + b * BB)), d1 = h2f(lds16(r1 + b * BB));
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    float cc[4];
+                    hm::mma16816_z(cc, a0[0], a1[0], a0[1], a1[1], bq[b][0][n][0], bq[b][0][n][1]);
+                    hm::mma16816(cc, a0[2], a1[2], a0[3], a1[3], bq[b][1][n][0], bq[b][1][n][1]);
+                    s0[n] = fmaf(d0 * upr[n][b], cc[0] + cc[1], s0[n]);
+                    s1[n] = fmaf(d1 * upr[n][b], cc[2] + cc[3], s1[n]);
+                }
+            }
+            // Running softmax of head 4 n + tq over this warp's positions.
+            const bool v0 = gq < nvalid, v1 = gq + 8 < nvalid;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const float a0 = v0 ? scale * s0[n] : kNegInf, a1 = v1 ? scale * s1[n] : kNegInf;
+                float mt = fmaxf(a0, a1);
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+                const float mnew = fmaxf(m_run[n], mt);   // finite: position 0 of the tile is valid
+                const float alpha = expf(m_run[n] - mnew);
+                const float pa = v0 ? expf(a0 - mnew) : 0.0f, pb = v1 ? expf(a1 - mnew) : 0.0f;
+                l_part[n] = fmaf(l_part[n], alpha, pa + pb);
+                m_run[n] = mnew;
+                const int h = 4 * n + tq;
+                if (h < G) {
+                    spw[gq * G + h] = pa;
+                    spw[(gq + 8) * G + h] = pb;
+                    if (gq == 0) saw[h] = alpha;
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int h = 0; h < GP; ++h) {
+                const float2 al = make_float2(saw[2 * h], 2 * h + 1 < G ? saw[2 * h + 1] : 0.0f);
+#pragma unroll
+                for (int k = 0; k < NB; ++k) acc[h][k] = __fmul2_rn(acc[h][k], al);
+            }
+            // sum_j p_j d_j q_j: this lane's elements, every head (a full tile
+            // unrolled, so the loads of several positions are in flight).  The
+            // rows' alignment is the same in every position (misg; slots are
+            // 16-byte multiples), so the code reader is set up once.
+            const uint8_t* vt = vst + jt * Gm::SLOT + misg + eb * BB;
+            const Codes<T, (NB >= 4 ? NB / 4 : 1)> vc(vt, e0);
+            auto vrow = [&](int j) {
+                const uint8_t* vb = vt + j * Gm::SLOT;
+                const float dv = h2f(lds16(vb));
+                float vv[NB];
+                if constexpr (NB >= 4) {
+                    uint32_t cw[NB / 4];
+                    vc.load((uint32_t)(j * Gm::SLOT), cw);
+                    // Byte b as the fp32 2^23 + b (one byte permute), less
+                    // 2^23 and the code offset (Q8_0: bytes flipped to q + 128).
+                    constexpr float kOff = 8388608.0f + (T == T_Q8_0 ? 128.0f : (T == T_Q5_0 ? 16.0f : 8.0f));
+#pragma unroll
+                    for (int w = 0; w < NB / 4; ++w) {
+                        const uint32_t u = T == T_Q8_0 ? cw[w] ^ 0x80808080u : cw[w];
+                        const float2 f01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)),
+                                                                  __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651))),
+                                                      make_float2(-kOff, -kOff));
+                        const float2 f23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)),
+                                                                  __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653))),
+                                                      make_float2(-kOff, -kOff));
+                        vv[4 * w] = f01.x; vv[4 * w + 1] = f01.y; vv[4 * w + 2] = f23.x; vv[4 * w + 3] = f23.y;
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < NB; ++k) vv[k] = (float)code_at<T>(vb, e0 + k);
+                }
+                float pj[2 * GP];
+                if constexpr (G % 4 == 0) {
+#pragma unroll
+                    for (int h = 0; h < G; h += 4) {
+                        const float4 p4 = *reinterpret_cast<const float4*>(spw + j * G + h);
+                        pj[h] = p4.x; pj[h + 1] = p4.y; pj[h + 2] = p4.z; pj[h + 3] = p4.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int h = 0; h < G; ++h) pj[h] = spw[j * G + h];
+                    if constexpr (G % 2) pj[G] = 0.0f;
+                }
+#pragma unroll
+                for (int h = 0; h < GP; ++h) {
+                    const float2 pd = __fmul2_rn(make_float2(pj[2 * h], pj[2 * h + 1]), make_float2(dv, dv));
+#pragma unroll
+                    for (int k = 0; k < NB; ++k) acc[h][k] = __ffma2_rn(pd, make_float2(vv[k], vv[k]), acc[h][k]);
+                }
+            };
+            if (nvalid == 16) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) vrow(j);
+            } else {
+                for (int j = 0; j < nvalid; ++j) vrow(j);
+            }
+            __syncwarp();   // spw and saw are rewritten by the next tile
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (++slot == nstg) {
+            slot = 0;
+            ph ^= 1u;
+        }
+    }
+    // The softmax sums of the warp's positions: the lanes of a head.
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) l_part[n] += __shfl_xor_sync(0xffffffffu, l_part[n], o);
+    // Merge the warps in order (the ring is free now): per warp and head,
+    // (m, l, o[D]) in shared memory, then per output element.
+    named_sync_stream_consumers();
+    float* mg = reinterpret_cast<float*>(ring);   // [kSW][G][D + 2]
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        const int h = 4 * n + tq;
+        if (h < G && gq == 0) {
+            mg[(warp * G + h) * (D + 2)] = m_run[n];
+            mg[(warp * G + h) * (D + 2) + 1] = l_part[n];
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int k = 0; k < NB; ++k)
+            mg[(warp * G + h) * (D + 2) + 2 + lane * NB + k] = (h & 1) ? acc[h >> 1][k].y : acc[h >> 1][k].x;
+    named_sync_stream_consumers();
+    if (*abort) return;
+    for (int i = tid; i < G * D; i += kSW * 32) {
+        const int h = i / D, e = i - h * D;
+        float M = kNegInf;
+#pragma unroll
+        for (int w = 0; w < kSW; ++w) M = fmaxf(M, mg[(w * G + h) * (D + 2)]);
+        float o = 0.0f, L = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kSW; ++w) {
+            const float* r = mg + (w * G + h) * (D + 2);
+            const float f = expf(r[0] - M);   // 0 for a warp with no position
+            o = fmaf(f, r[2 + e], o);
+            L = fmaf(f, r[1], L);
+        }
+        float* dst = ws + ((int64_t)(g * G + h) * nsplit + c) * (D + 2);
+        dst[2 + e] = o;
+        if (e == 0) {
+            dst[0] = M;
+            dst[1] = L;
+        }
+    }
+}
+
 // (m, l) of two sets of scores merged: m = max, l = sum of l_i e^(m_i - m).
 __device__ __forceinline__ void ml_merge(float& m, float& l, float m2, float l2) {
     const float mm = fmaxf(m, m2);
@@ -562,12 +884,92 @@ cudaError_t launch_tn(const float* q, const uint8_t* K, const uint8_t* V, int64_
     return cudaLaunchKernelEx(&cfg, attn_combine_kernel, (const float*)ws, (int)nch, 32 * NB, out);
 }
 
-// The fixed-group kernel where a lane's G d/32 elements make whole words
+// The streaming kernel with CTAs ~ two per SM: P positions each (a multiple
+// of the stage, at least one stage, so the partials fit the workspace sized
+// for 128-position chunks).  It needs the TMA boxes: a position's n_kv ROWB
+// bytes a multiple of 16 (the tensor map's row pitch) and the box at most
+// 256 bytes wide; and two ring stages in its shared memory.
+template <int T, int NB, int G>
+bool stream_fits(int n_kv) {
+    using Gm = SGeo<T, NB>;
+    using Mp = SMap<T, NB, G>;
+    const int nstg = std::min(kSMaxStages, (kSBudget - Mp::bytes(0)) / Gm::STAGE);
+    return ((int64_t)n_kv * Gm::ROWB) % 16 == 0 && Gm::SLOT <= 256 && nstg >= 2 &&
+           kSW * G * (32 * NB + 2) * 4 <= nstg * Gm::STAGE;
+}
+
+// The cache [T, n_kv ROWB] as 8-bit elements, box SLOT x kSPos.
+template <int T, int NB>
+bool encode_cache_map(CUtensorMap* map, const uint8_t* C, int64_t T_len, int n_kv) {
+    using Gm = SGeo<T, NB>;
+    auto encode = encode_fn();
+    if (!encode) return false;
+    const cuuint64_t pitch = (cuuint64_t)n_kv * Gm::ROWB;
+    cuuint64_t gdim[2] = {pitch, (cuuint64_t)T_len};
+    cuuint64_t gstride[1] = {pitch};
+    cuuint32_t box[2] = {(cuuint32_t)Gm::SLOT, (cuuint32_t)kSPos};
+    cuuint32_t estride[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(C), gdim, gstride, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int T, int NB, int G>
+cudaError_t launch_sn(const float* q, const uint8_t* K, const uint8_t* V, int64_t T_len, int n_kv, float scale,
+                      float* out, float* ws, unsigned* status, int sms, cudaStream_t s) {
+    using Gm = SGeo<T, NB>;
+    using Mp = SMap<T, NB, G>;
+    CUtensorMap kmap, vmap;
+    if (!encode_cache_map<T, NB>(&kmap, K, T_len, n_kv) || !encode_cache_map<T, NB>(&vmap, V, T_len, n_kv))
+        return cudaErrorInvalidValue;
+    const int nstg = std::min(kSMaxStages, (kSBudget - Mp::bytes(0)) / Gm::STAGE);
+    const int smem = Mp::bytes(nstg);
+    const int64_t s0 = std::max<int64_t>(1, 2 * (int64_t)std::max(sms, 1) / n_kv);
+    const int64_t per = (T_len + s0 - 1) / s0;
+    const int P = (int)std::max<int64_t>(kSPos, (per + kSPos - 1) / kSPos * kSPos);
+    const int nsplit = (int)((T_len + P - 1) / P);
+    auto kern = attn_stream_kernel<T, NB, G>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.stream = s;
+    cfg.gridDim = dim3((unsigned)(n_kv * nsplit));
+    cfg.blockDim = dim3(kSThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, q, T_len, n_kv, scale, ws, P, nsplit, nstg, status);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3((unsigned)(n_kv * G), (unsigned)NB);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, attn_combine_kernel, (const float*)ws, nsplit, 32 * NB, out);
+}
+
+// The streaming kernel for the fixed groups whose per-lane state fits the
+// registers (G heads x d/32 sums, the query fragments), else the chunk
+// kernels: fixed-group where a lane's G d/32 elements make whole words
 // inside one block, the runtime-group one otherwise.
+template <int T, int NB, int G>
+constexpr bool stream_regs_ok() {
+    return G * NB + 4 * NB * ((2 * G + 7) / 8) <= 48;
+}
+
 template <int T, int NB>
 cudaError_t launch_g(const float* q, const uint8_t* K, const uint8_t* V, int64_t T_len, int n_heads, int n_kv,
-                     float scale, float* out, float* ws, cudaStream_t s) {
+                     float scale, float* out, float* ws, unsigned* status, int sms, cudaStream_t s) {
     const int G = n_heads / n_kv;
+    if constexpr (stream_regs_ok<T, NB, 1>())
+        if (G == 1 && stream_fits<T, NB, 1>(n_kv)) return launch_sn<T, NB, 1>(q, K, V, T_len, n_kv, scale, out, ws, status, sms, s);
+    if constexpr (stream_regs_ok<T, NB, 2>())
+        if (G == 2 && stream_fits<T, NB, 2>(n_kv)) return launch_sn<T, NB, 2>(q, K, V, T_len, n_kv, scale, out, ws, status, sms, s);
+    if constexpr (stream_regs_ok<T, NB, 4>())
+        if (G == 4 && stream_fits<T, NB, 4>(n_kv)) return launch_sn<T, NB, 4>(q, K, V, T_len, n_kv, scale, out, ws, status, sms, s);
+    if constexpr (stream_regs_ok<T, NB, 8>())
+        if (G == 8 && stream_fits<T, NB, 8>(n_kv)) return launch_sn<T, NB, 8>(q, K, V, T_len, n_kv, scale, out, ws, status, sms, s);
     if constexpr (NB <= 4) {
         if (G == 8 && 8 * NB <= 32) return launch_tn<T, NB, 8>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, s);
     }
@@ -585,12 +987,12 @@ cudaError_t launch_g(const float* q, const uint8_t* K, const uint8_t* V, int64_t
 
 template <int T>
 cudaError_t launch_t(const float* q, const uint8_t* K, const uint8_t* V, int64_t T_len, int n_heads, int n_kv, int d,
-                     float scale, float* out, float* ws, cudaStream_t s) {
+                     float scale, float* out, float* ws, unsigned* status, int sms, cudaStream_t s) {
     switch (d) {
-    case 32: return launch_g<T, 1>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, s);
-    case 64: return launch_g<T, 2>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, s);
-    case 128: return launch_g<T, 4>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, s);
-    case 256: return launch_g<T, 8>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, s);
+    case 32: return launch_g<T, 1>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, status, sms, s);
+    case 64: return launch_g<T, 2>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, status, sms, s);
+    case 128: return launch_g<T, 4>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, status, sms, s);
+    case 256: return launch_g<T, 8>(q, K, V, T_len, n_heads, n_kv, scale, out, ws, status, sms, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -607,11 +1009,12 @@ bool attn_decode_shape_ok(int n_heads, int n_kv, int d) {
 }
 
 cudaError_t launch_attn_decode(int type, const float* q, const uint8_t* K, const uint8_t* V, int64_t T_len, int n_heads,
-                               int n_kv, int d, float scale, float* out, float* ws, cudaStream_t s) {
+                               int n_kv, int d, float scale, float* out, float* ws, unsigned* status, int sms,
+                               cudaStream_t s) {
     switch (type) {
-    case T_Q8_0: return attn::launch_t<T_Q8_0>(q, K, V, T_len, n_heads, n_kv, d, scale, out, ws, s);
-    case T_Q5_0: return attn::launch_t<T_Q5_0>(q, K, V, T_len, n_heads, n_kv, d, scale, out, ws, s);
-    case T_Q4_0: return attn::launch_t<T_Q4_0>(q, K, V, T_len, n_heads, n_kv, d, scale, out, ws, s);
+    case T_Q8_0: return attn::launch_t<T_Q8_0>(q, K, V, T_len, n_heads, n_kv, d, scale, out, ws, status, sms, s);
+    case T_Q5_0: return attn::launch_t<T_Q5_0>(q, K, V, T_len, n_heads, n_kv, d, scale, out, ws, status, sms, s);
+    case T_Q4_0: return attn::launch_t<T_Q4_0>(q, K, V, T_len, n_heads, n_kv, d, scale, out, ws, status, sms, s);
     }
     return cudaErrorInvalidValue;
 }

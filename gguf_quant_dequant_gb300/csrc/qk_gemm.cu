@@ -968,7 +968,6 @@ __global__ void __launch_bounds__(256) reduce_splits_kernel(const float* __restr
 
 namespace qk {
 
-namespace {
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static bool tried = false;
@@ -982,7 +981,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     }
     return fn;
 }
-}  // namespace
 
 template <int T, class C>
 static cudaError_t gemm_tc(gm::Args a, const GemmPlan& pl, const CUtensorMap& map, cudaStream_t s) {

@@ -107,41 +107,25 @@ __device__ __forceinline__ void prep_unit_x(const float* xs, uint8_t* xb, float4
     const int ex = (int)((__float_as_uint(amax) >> 23) & 255u) - 127;
     const int e = max(0, ex - 14);
     const float down = __uint_as_float((uint32_t)(127 - e) << 23), up = __uint_as_float((uint32_t)(127 + e) << 23);
-    uint32_t hi[8], lo[8];
+    // Words 2q and 2q+1: elements 8q + {0,2}, {1,3}, {4,6}, {5,7}; each pair
+    // rounded to fp16 by one packed convert, its residual by another.
+    constexpr int kPair[4][2] = {{0, 2}, {1, 3}, {4, 6}, {5, 7}};
+    uint32_t hi[4], lo[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float sv = v[i] * down;
-        const __half h = __float2half_rn(sv);
-        hi[i] = __half_as_ushort(h);
-        lo[i] = __half_as_ushort(__float2half_rn(sv - __half2float(h)));
+    for (int k = 0; k < 4; ++k) {
+        const float a = v[kPair[k][0]] * down, b = v[kPair[k][1]] * down;
+        const __half2 h = __floats2half2_rn(a, b);
+        const float2 hf = __half22float2(h);
+        const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+        hi[k] = *reinterpret_cast<const uint32_t*>(&h);
+        lo[k] = *reinterpret_cast<const uint32_t*>(&l);
     }
-    // Words 2q and 2q+1: elements 8q + {0,2}, {1,3}, {4,6}, {5,7}.
-    *reinterpret_cast<uint4*>(xb + jl * kXBB + 16 * q) =
-        make_uint4(hi[0] | hi[2] << 16, hi[1] | hi[3] << 16, hi[4] | hi[6] << 16, hi[5] | hi[7] << 16);
-    *reinterpret_cast<uint4*>(xb + jl * kXBB + 64 + 16 * q) =
-        make_uint4(lo[0] | lo[2] << 16, lo[1] | lo[3] << 16, lo[4] | lo[6] << 16, lo[5] | lo[7] << 16);
+    *reinterpret_cast<uint4*>(xb + jl * kXBB + 16 * q) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(xb + jl * kXBB + 64 + 16 * q) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     if (q == 0) xm[jl] = make_float4(sum + other, up, sum, other);
 }
 
 __device__ __forceinline__ void named_sync_consumers() { asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory"); }
-
-// Bounded wait that also gives up when another warp of the CTA has already
-// given up (*abort set); on its own timeout it sets *abort and the status.
-// Between checks the warp is suspended by the hardware until the phase
-// completes (or a microsecond passes), so waiting warps take no issue slots
-// from the working ones.
-__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, unsigned* status, volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1; i < (1u << 24); ++i) {
-        if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
-        if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitNs) break;
-    }
-    *abort = 1;
-    atomicOr(status, STATUS_TIMEOUT);
-    return false;
-}
 
 // SWI: one matrix pair (W[0] gate, W[1] up, same shape), y[0] = h =
 // SiLU(gate x) * (up x); each 16-row tile is walked through the gate matrix
@@ -216,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
                 const int64_t off = (r_begin + tile * kTileRows + lane) * (int64_t)rb + coff;
                 for (int pass = 0; pass < npass; ++pass, ++it) {
                     const uint8_t* Wp = (SWI && pass) ? p.W[1] : Wm;
-                    if (it >= p.stages && !wait_phase(&empty[s], ph ^ 1u, p.status, abort)) {
+                    if (it >= p.stages && !mbar_wait_abortable(&empty[s], ph ^ 1u, p.status, abort)) {
                         dead = true;
                         break;
                     }
@@ -325,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
         const int nvb = min(8, p.nxb - 8 * u);
         for (int tile = 0; tile < ntiles; ++tile) {
             for (int pass = 0; pass < npass; ++pass) {
-                if (!dead && !wait_phase(&full[s], ph, p.status, abort)) dead = true;
+                if (!dead && !mbar_wait_abortable(&full[s], ph, p.status, abort)) dead = true;
                 float y0[MT], y1[MT];
 #pragma unroll
                 for (int m = 0; m < MT; ++m) y0[m] = y1[m] = 0.0f;

@@ -4,10 +4,14 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "../../include/qk.h"
 
 namespace qk {
+
+// The driver's cuTensorMapEncodeTiled (looked up once; nullptr if missing).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
 
 // Sets the calling thread's qk_last_error() text; returns st.
 qk_status set_error(qk_status st, const char* msg);
@@ -23,7 +27,8 @@ cudaError_t launch_quantize(int type, const float* w, int64_t rows, int64_t cols
 int64_t attn_decode_ws_bytes(int64_t T_len, int n_heads, int d);
 bool attn_decode_shape_ok(int n_heads, int n_kv, int d);
 cudaError_t launch_attn_decode(int type, const float* q, const uint8_t* K, const uint8_t* V, int64_t T_len, int n_heads,
-                               int n_kv, int d, float scale, float* out, float* ws, cudaStream_t s);
+                               int n_kv, int d, float scale, float* out, float* ws, unsigned* status, int sms,
+                               cudaStream_t s);
 cudaError_t launch_quantize_imatrix(int type, const float* w, const float* imp, int64_t rows, int64_t cols,
                                    uint8_t* out, cudaStream_t s);
 

@@ -104,6 +104,25 @@ __device__ __forceinline__ bool mbar_wait_sleep_bounded(uint64_t* bar, uint32_t 
     return false;
 }
 
+// Bounded wait that also gives up when another warp of the CTA has already
+// given up (*abort set); on its own timeout it sets *abort and the status.
+// Between checks the warp is suspended by the hardware until the phase
+// completes (or a microsecond passes), so waiting warps take no issue slots
+// from the working ones.
+__device__ __forceinline__ bool mbar_wait_abortable(uint64_t* bar, uint32_t parity, unsigned* status,
+                                                    volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1; i < (1u << 24); ++i) {
+        if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > kWaitNs) break;
+    }
+    *abort = 1;
+    atomicOr(status, STATUS_TIMEOUT);
+    return false;
+}
+
 // Evict-first L2 policy for data streamed exactly once (weights of a GEMV).
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t pol;
