@@ -614,11 +614,15 @@ def run_attn(dev, hbm_peak=None):
             "per_cache_type": out}
 
 
-def run_quantize(dev, hbm_peak=None, reps: int = 20):
+def run_quantize(dev, hbm_peak=None, reps: int = 20, imx_reps: int = 3):
     """The write side: qk_quantize of one 14336x4096 fp32 matrix (N(0, 0.02),
     235 MB, beyond L2) into each block type.  Per type: 2 warm-up launches,
     then `reps` launches back to back between two CUDA events.  GB/s counts
-    the 4 bytes read and the packed bytes written per weight."""
+    the 4 bytes read and the packed bytes written per weight.  The
+    importance-weighted quantizer (qk_quantize_imatrix, log-normal column
+    importances exp(N(0, 1))) is timed the same way with one warm-up and
+    `imx_reps` launches: it is bound by its candidate search, so its figure
+    is microseconds and weights per second."""
     import torch
     import gguf_quant_dequant_gb300 as qk
     import synth
@@ -627,6 +631,7 @@ def run_quantize(dev, hbm_peak=None, reps: int = 20):
     g = torch.Generator(device=dev)
     g.manual_seed(2024)
     w = torch.randn((rows, cols), device=dev, generator=g) * 0.02
+    imp = torch.exp(torch.randn(cols, device=dev, generator=g))
     per = {}
     for name in ("Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K", "Q2_K", "Q3_K"):
         t = synth.TYPE_IDS[name]
@@ -644,9 +649,20 @@ def run_quantize(dev, hbm_peak=None, reps: int = 20):
         per[name] = {"us": round(us, 2), "gbs": round(gbs, 1)}
         if hbm_peak:
             per[name]["frac_of_hbm"] = round(gbs / hbm_peak, 4)
+        if imx_reps > 0:
+            qk.quantize_imatrix(t, w, imp, out=o)
+            e0.record(stream)
+            for _ in range(imx_reps):
+                qk.quantize_imatrix(t, w, imp, out=o)
+            e1.record(stream)
+            e1.synchronize()
+            ius = e0.elapsed_time(e1) * 1e3 / imx_reps
+            per[name]["imatrix_us"] = round(ius, 1)
+            per[name]["imatrix_gweights_per_s"] = round(rows * cols / (ius * 1e-6) / 1e9, 2)
         del o
-    del w
-    return {"workload": "qk_quantize, 14336x4096 fp32 N(0, 0.02) -> each block type", "per_type": per}
+    del w, imp
+    return {"workload": "qk_quantize and qk_quantize_imatrix, 14336x4096 fp32 N(0, 0.02) -> each block type",
+            "per_type": per}
 
 
 def _graph_time_us(fn, reps: int = 20, warm: int = 3) -> float:

@@ -169,7 +169,11 @@ qk_status qk_quantize(int type, const float* w, int64_t rows, int64_t cols, void
     if (!out) return fail(QK_ERR_NULL, "out is NULL");
     if (!aligned(w, 16)) return fail(QK_ERR_ALIGN, "w is not 16-byte aligned");
     if (!aligned(out, 4)) return fail(QK_ERR_ALIGN, "out is not 4-byte aligned");
-    cudaError_t e = qk::launch_quantize(type, w, rows, cols, static_cast<uint8_t*>(out), static_cast<cudaStream_t>(stream));
+    int sms = 0;
+    const qk_status st = device_state(nullptr, &sms);
+    if (st != QK_OK) return st;
+    cudaError_t e = qk::launch_quantize(type, w, rows, cols, static_cast<uint8_t*>(out), sms,
+                                        static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "qk_quantize launch");
     g_last_error.clear();
     return QK_OK;
@@ -186,7 +190,8 @@ qk_status qk_quantize_imatrix(int type, const float* w, int64_t rows, int64_t co
     if (!w) return fail(QK_ERR_NULL, "w is NULL");
     if (!imp) return fail(QK_ERR_NULL, "imp is NULL");
     if (!out) return fail(QK_ERR_NULL, "out is NULL");
-    if (!aligned(w, 4) || !aligned(imp, 4)) return fail(QK_ERR_ALIGN, "w or imp is not 4-byte aligned");
+    if (!aligned(w, 16)) return fail(QK_ERR_ALIGN, "w is not 16-byte aligned");
+    if (!aligned(imp, 4) || !aligned(out, 4)) return fail(QK_ERR_ALIGN, "imp or out is not 4-byte aligned");
     cudaError_t e = qk::launch_quantize_imatrix(type, w, imp, rows, cols, static_cast<uint8_t*>(out),
                                                static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "qk_quantize_imatrix launch");

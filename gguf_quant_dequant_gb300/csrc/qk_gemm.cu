@@ -336,16 +336,61 @@ __device__ __forceinline__ void q5k64(const uint8_t* blk, int kk, uint32_t (&pk)
     }
 }
 
-// Any type with 16-weight halves in k order (Q2_K, Q3_K): k-block kk of a
-// 256-weight macro-block is halves 4kk .. 4kk+3 through the shared decoders.
-template <int T>
-__device__ __forceinline__ void halves64(const uint8_t* blk, int kk, uint32_t (&pk)[32]) {
+// Q2_K (blk 2-byte aligned): k-block kk is weights 64kk .. 64kk+63 = plane
+// half t = kk / 2, fields j0 = 2(kk & 1) (first 32) and j0 + 1 (next 32) of
+// code bytes 32t .. 32t+31, groups 4kk .. 4kk+3 with their (scale, min)
+// bytes 4kk .. 4kk+3 (scale low nibble).  w = ds*q - dm, as a*(128 + q) + o.
+__device__ __forceinline__ void q2k64(const uint8_t* blk, int kk, uint32_t (&pk)[32]) {
+    const int t = kk >> 1, j0 = 2 * (kk & 1);
+    uint32_t qs[8];
+    gv::lds_words_a2<8>(blk + 16 + 32 * t, qs);
+    const uint32_t sm = ld_u32_a2(blk + 4 * kk);
+    const float d = h2f(ld_u16(blk + 80)), dmin = h2f(ld_u16(blk + 82));
+    float2 a[4], o[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float w[16];
-        dequant_half<T>(blk, 2 * kk + (i >> 1), i & 1, w);
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t b = (sm >> (8 * e)) & 0xFFu;
+        const float ds = d * (float)(b & 15u), dm = dmin * (float)(b >> 4);
+        const float off = -(128.0f * ds + dm);
+        a[e] = make_float2(ds, ds);
+        o[e] = make_float2(off, off);
+    }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) pk[8 * i + k] = pack_bf16(w[2 * k], w[2 * k + 1]);
+    for (int i = 0; i < 8; ++i) {   // code bytes 4i .. 4i+3: weights 4i.. of each 32
+        four_hi((qs[i] >> (2 * j0)) & 0x03030303u, a[i >> 2], o[i >> 2], pk[2 * i], pk[2 * i + 1]);
+        four_hi((qs[i] >> (2 * j0 + 2)) & 0x03030303u, a[2 + (i >> 2)], o[2 + (i >> 2)], pk[16 + 2 * i],
+                pk[17 + 2 * i]);
+    }
+}
+
+// Q3_K (blk 2-byte aligned): the Q2_K plane at byte 32 with the third bit of
+// weight (j, l) at bit 4t + j of hmask[l] (bytes 0-31), u = lo2 + 4 * bit in
+// 0..7 and q = u - 4; groups 4kk + e take the signed scale (low four bits:
+// nibble t of byte 96 + 4(kk & 1) + e; high two: bits 2kk.. of byte 104 + e;
+// minus 32).  w = ds*(u - 4) = ds*(128 + u) - 132 ds.
+__device__ __forceinline__ void q3k64(const uint8_t* blk, int kk, uint32_t (&pk)[32]) {
+    const int t = kk >> 1, j0 = 2 * (kk & 1);
+    uint32_t qs[8], hm[8];
+    gv::lds_words_a2<8>(blk + 32 + 32 * t, qs);
+    gv::lds_words_a2<8>(blk, hm);
+    const uint32_t lo4 = (ld_u32_a2(blk + 96 + 4 * (kk & 1)) >> (4 * t)) & 0x0F0F0F0Fu;
+    const uint32_t hi2 = (ld_u32_a2(blk + 104) >> (2 * kk)) & 0x03030303u;
+    const uint32_t sw = lo4 | (hi2 << 4);   // byte e: scale of group 4kk + e, plus 32
+    const float d = h2f(ld_u16(blk + 108));
+    float2 a[4], o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float ds = d * ((float)((sw >> (8 * e)) & 0xFFu) - 32.0f);
+        a[e] = make_float2(ds, ds);
+        o[e] = make_float2(-132.0f * ds, -132.0f * ds);
+    }
+    const int hb = 4 * t + j0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t v0 = ((qs[i] >> (2 * j0)) & 0x03030303u) | (((hm[i] >> hb) & 0x01010101u) << 2);
+        const uint32_t v1 = ((qs[i] >> (2 * j0 + 2)) & 0x03030303u) | (((hm[i] >> (hb + 1)) & 0x01010101u) << 2);
+        four_hi(v0, a[i >> 2], o[i >> 2], pk[2 * i], pk[2 * i + 1]);
+        four_hi(v1, a[2 + (i >> 2)], o[2 + (i >> 2)], pk[16 + 2 * i], pk[17 + 2 * i]);
     }
 }
 
@@ -884,8 +929,10 @@ __global__ void __launch_bounds__(kSkThreads, 1) gemm_skinny_kernel(const __grid
                             q4k64(blk, ph, pk);
                         } else if constexpr (T == T_Q5_K) {
                             q5k64(blk, ph, pk);
-                        } else if constexpr (T == T_Q2_K || T == T_Q3_K) {
-                            halves64<T>(blk, ph, pk);
+                        } else if constexpr (T == T_Q2_K) {
+                            q2k64(blk, ph, pk);
+                        } else if constexpr (T == T_Q3_K) {
+                            q3k64(blk, ph, pk);
                         } else if constexpr (T == T_Q6_K) {
                             q6k64(blk, ph, pk);
                         } else {

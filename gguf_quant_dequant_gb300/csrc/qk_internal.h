@@ -23,7 +23,9 @@ qk_status gemv_check_args(int type, const void* W, int64_t rows, int64_t cols, c
 cudaError_t launch_dequant(int type, const uint8_t* W, int64_t rows, int64_t cols, void* out,
                            int out_bf16, cudaStream_t s);
 
-cudaError_t launch_quantize(int type, const float* w, int64_t rows, int64_t cols, uint8_t* out, cudaStream_t s);
+// Plain quantizer: a persistent grid of at most 4 CTAs per SM (sms SMs).
+cudaError_t launch_quantize(int type, const float* w, int64_t rows, int64_t cols, uint8_t* out, int sms,
+                            cudaStream_t s);
 int64_t attn_decode_ws_bytes(int64_t T_len, int n_heads, int d);
 bool attn_decode_shape_ok(int n_heads, int n_kv, int d);
 cudaError_t launch_attn_decode(int type, const float* q, const uint8_t* K, const uint8_t* V, int64_t T_len, int n_heads,

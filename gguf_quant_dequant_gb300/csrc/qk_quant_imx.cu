@@ -1,8 +1,8 @@
 // qk_quant_imx.cu -- importance-weighted quantization (the imatrix objective
 // of "Hitchhiker's Guide -- Lab 01", 11.3: minimise sum_i E[x_i^2] (w_i -
-// w^_i)^2 instead of the plain weight-space error).  Offline work, so one
-// thread encodes one block, in this order (all fp32, every sum in index
-// order, explicit round-to-nearest operations so that nothing is contracted):
+// w^_i)^2 instead of the plain weight-space error).  Per block, in this
+// order (all fp32, every sum in index order, explicit round-to-nearest
+// operations so that nothing is contracted):
 //   1. per group (32-weight block of Q8_0 / Q5_0 / Q4_0, 32-weight sub-block
 //      of Q4_K / Q5_K, 16-weight group of Q6_K / Q3_K / Q2_K): the plain
 //      scheme's scale s0 (and min m0); 21 candidate scales s0 (90 + k) / 100;
@@ -15,81 +15,94 @@
 //   3. that block and the plain one decoded, their weighted errors summed per
 //      group and then over groups; the plain block is kept unless the
 //      weighted one is no worse.
-#include <cuda_fp16.h>
-
-#include "qk_formats.cuh"
+// Layout of the work: the plain quantizer's (qk_qlanes.cuh): a warp takes 32
+// consecutive 32-weight groups, each lane the 32 weights of one (its one or
+// two groups of step 1), so every lane searches its own groups with its
+// weights and importances in registers; both blocks are assembled by the
+// shared lane code into shared memory, each lane decodes its own weights of
+// both, and the lanes of a block add the group errors in group order.
 #include "qk_internal.h"
+#include "qk_qlanes.cuh"
 
 namespace qk {
 namespace imx {
 
-__device__ __forceinline__ int cr(float v, int lo, int hi) {
-    float r = roundf(v);
-    if (!(r >= (float)lo)) r = (float)lo;
-    if (r > (float)hi) r = (float)hi;
-    return (int)r;
-}
-__device__ __forceinline__ uint32_t h16(float v) { return (uint32_t)__half_as_ushort(__float2half_rn(v)); }
-__device__ __forceinline__ float f16(uint32_t b) { return __half2float(__ushort_as_half((unsigned short)b)); }
+constexpr int kWarps = 8;                    // per CTA
+constexpr int kBufWords = 32 * 34 / 4;      // largest warp output: 32 Q8_0 blocks = 1088 bytes
 
-template <int T> struct Geo;   // group size, symmetric?, plain divisor / steps, code range
-template <> struct Geo<T_Q8_0> { static constexpr int G = 32; static constexpr bool SYM = true; static constexpr int DIV = 127, LO = -128, HI = 127; };
-template <> struct Geo<T_Q5_0> { static constexpr int G = 32; static constexpr bool SYM = true; static constexpr int DIV = 15, LO = -16, HI = 15; };
-template <> struct Geo<T_Q4_0> { static constexpr int G = 32; static constexpr bool SYM = true; static constexpr int DIV = 7, LO = -8, HI = 7; };
-template <> struct Geo<T_Q6_K> { static constexpr int G = 16; static constexpr bool SYM = true; static constexpr int DIV = 32, LO = -32, HI = 31; };
-template <> struct Geo<T_Q3_K> { static constexpr int G = 16; static constexpr bool SYM = true; static constexpr int DIV = 4, LO = -4, HI = 3; };
-template <> struct Geo<T_Q4_K> { static constexpr int G = 32; static constexpr bool SYM = false; static constexpr int DIV = 15, LO = 0, HI = 15; };
-template <> struct Geo<T_Q5_K> { static constexpr int G = 32; static constexpr bool SYM = false; static constexpr int DIV = 31, LO = 0, HI = 31; };
-template <> struct Geo<T_Q2_K> { static constexpr int G = 16; static constexpr bool SYM = false; static constexpr int DIV = 3, LO = 0, HI = 3; };
+template <int T> struct Geo;   // symmetric?, code range of step 1
+template <> struct Geo<T_Q8_0> { static constexpr bool SYM = true; static constexpr int LO = -128, HI = 127; };
+template <> struct Geo<T_Q5_0> { static constexpr bool SYM = true; static constexpr int LO = -16, HI = 15; };
+template <> struct Geo<T_Q4_0> { static constexpr bool SYM = true; static constexpr int LO = -8, HI = 7; };
+template <> struct Geo<T_Q6_K> { static constexpr bool SYM = true; static constexpr int LO = -32, HI = 31; };
+template <> struct Geo<T_Q3_K> { static constexpr bool SYM = true; static constexpr int LO = -4, HI = 3; };
+template <> struct Geo<T_Q4_K> { static constexpr bool SYM = false; static constexpr int LO = 0, HI = 15; };
+template <> struct Geo<T_Q5_K> { static constexpr bool SYM = false; static constexpr int LO = 0, HI = 31; };
+template <> struct Geo<T_Q2_K> { static constexpr bool SYM = false; static constexpr int LO = 0, HI = 3; };
 
-// Step 1 for one group at x (weights) and a (importances); plain == true
-// returns the plain (s0, m0) without searching.
-template <int T>
-__device__ void group_params(const float* x, const float* a, bool plain, float& s_out, float& m_out) {
+// Step 1 for one group of G weights x with importances a, from the plain
+// (s0, m0).  The codes of a candidate come from one reciprocal of its scale
+// (group rounding of qk_codes.cuh: the division's codes exactly).
+template <int T, int G>
+__device__ __forceinline__ void search(const float* x, const float* a, float s0, float m0, float& s_out,
+                                       float& m_out) {
     using P = Geo<T>;
-    float s0, m0 = 0.0f;
-    if constexpr (P::SYM) {
-        float amax = 0.0f;
-        for (int l = 0; l < P::G; ++l) {
-            const float v = fabsf(x[l]);
-            if (v > amax) amax = v;
-        }
-        s0 = __fdiv_rn(amax, (float)P::DIV);
-    } else {
-        float lo = 0.0f, hi = x[0];
-        for (int l = 0; l < P::G; ++l) {
-            if (x[l] < lo) lo = x[l];
-            if (x[l] > hi) hi = x[l];
-        }
-        s0 = __fdiv_rn(__fsub_rn(hi, lo), (float)P::DIV);
-        m0 = -lo;
-    }
     s_out = s0;
     m_out = m0;
-    if (plain || !(s0 > 0.0f)) return;
+    if (!(s0 > 0.0f)) return;
+    // Candidate-independent sums of the refit (index order).
+    float Sa = 0.0f, Sw = 0.0f;
+    if constexpr (!P::SYM) {
+#pragma unroll
+        for (int l = 0; l < G; ++l) {
+            Sa = __fadd_rn(Sa, a[l]);
+            Sw = __fadd_rn(Sw, __fmul_rn(a[l], x[l]));
+        }
+    }
+    const float flo = (float)P::LO, fhi = (float)P::HI, magic = 12582912.0f;
+    // The rounding test of group_codes (qk_codes.cuh): per value for wide
+    // code ranges, the group's largest distance for ranges within +-16.
+    constexpr int kM = (-P::LO > P::HI) ? -P::LO : P::HI;
+    constexpr bool kWide = kM > 16;
+    const float limit = kWide ? 0.5f : 0.5f - (float)kM * 0x1p-20f;
     float best = __int_as_float(0x7f800000);
+#pragma unroll 1
     for (int k = 0; k <= 20; ++k) {
         const float s = __fmul_rn(s0, __fdiv_rn((float)(90 + k), 100.0f));
+        const float rd = approx_rcp(s);
+        float q[G];
+        float worst = 0.0f;
+#pragma unroll
+        for (int l = 0; l < G; ++l) {
+            const float u = P::SYM ? x[l] : __fadd_rn(x[l], m0);
+            const float y = fminf(fmaxf(__fmul_rn(u, rd), flo), fhi);
+            q[l] = __fsub_rn(__fadd_rn(y, magic), magic);
+            const float dist = fabsf(__fsub_rn(y, q[l]));
+            worst = fmaxf(worst, kWide ? __fmaf_rn(fabsf(y), 0x1p-20f, dist) : dist);
+        }
+        if (!(rcp_usable(s) && worst < limit)) {   // rare: a code the approximate quotient cannot decide
+#pragma unroll
+            for (int l = 0; l < G; ++l)
+                q[l] = (float)cr(__fdiv_rn(P::SYM ? x[l] : __fadd_rn(x[l], m0), s), P::LO, P::HI);
+        }
         float ss, mm = 0.0f;
         if constexpr (P::SYM) {
             float num = 0.0f, den = 0.0f;
-            for (int l = 0; l < P::G; ++l) {
-                const float q = (float)cr(__fdiv_rn(x[l], s), P::LO, P::HI);
-                const float aq = __fmul_rn(a[l], q);
+#pragma unroll
+            for (int l = 0; l < G; ++l) {
+                const float aq = __fmul_rn(a[l], q[l]);
                 num = __fadd_rn(num, __fmul_rn(aq, x[l]));
-                den = __fadd_rn(den, __fmul_rn(aq, q));
+                den = __fadd_rn(den, __fmul_rn(aq, q[l]));
             }
             if (!(den > 0.0f)) continue;
             ss = __fdiv_rn(num, den);
         } else {
-            float Sa = 0.0f, Sq = 0.0f, Sqq = 0.0f, Sw = 0.0f, Swq = 0.0f;
-            for (int l = 0; l < P::G; ++l) {
-                const float q = (float)cr(__fdiv_rn(__fadd_rn(x[l], m0), s), P::LO, P::HI);
-                const float aq = __fmul_rn(a[l], q);
-                Sa = __fadd_rn(Sa, a[l]);
+            float Sq = 0.0f, Sqq = 0.0f, Swq = 0.0f;
+#pragma unroll
+            for (int l = 0; l < G; ++l) {
+                const float aq = __fmul_rn(a[l], q[l]);
                 Sq = __fadd_rn(Sq, aq);
-                Sqq = __fadd_rn(Sqq, __fmul_rn(aq, q));
-                Sw = __fadd_rn(Sw, __fmul_rn(a[l], x[l]));
+                Sqq = __fadd_rn(Sqq, __fmul_rn(aq, q[l]));
                 Swq = __fadd_rn(Swq, __fmul_rn(aq, x[l]));
             }
             const float det = __fsub_rn(__fmul_rn(Sqq, Sa), __fmul_rn(Sq, Sq));
@@ -98,12 +111,11 @@ __device__ void group_params(const float* x, const float* a, bool plain, float& 
             mm = __fdiv_rn(__fsub_rn(__fmul_rn(Swq, Sq), __fmul_rn(Sqq, Sw)), det);
             if (!(ss > 0.0f) || !(mm >= 0.0f)) continue;
         }
-        // Weighted error of this candidate (codes rounded again with s, m0).
+        // Weighted error of this candidate (the same codes).
         float e = 0.0f;
-        for (int l = 0; l < P::G; ++l) {
-            const float q = P::SYM ? (float)cr(__fdiv_rn(x[l], s), P::LO, P::HI)
-                                   : (float)cr(__fdiv_rn(__fadd_rn(x[l], m0), s), P::LO, P::HI);
-            const float r = __fsub_rn(x[l], __fsub_rn(__fmul_rn(ss, q), mm));
+#pragma unroll
+        for (int l = 0; l < G; ++l) {
+            const float r = __fsub_rn(x[l], __fsub_rn(__fmul_rn(ss, q[l]), mm));
             e = __fadd_rn(e, __fmul_rn(a[l], __fmul_rn(r, r)));
         }
         if (e < best) {
@@ -114,169 +126,140 @@ __device__ void group_params(const float* x, const float* a, bool plain, float& 
     }
 }
 
-// Step 2: the block bytes from per-group (s, m), the plain assembly.
+// Step 3 for the lane's weights: the weighted error of each of its groups,
+// from the block's bytes (`blk`: the super-block for the K types, the
+// lane's block otherwise) decoded by the shared half decoders.  The lane's
+// 32 weights are two halves of 16: (u0, h0) then (u1, h1).
 template <int T>
-__device__ void assemble(const float* x, const float* sg, const float* mg, uint8_t* b) {
-    using F = Fmt<T>;
-    for (int i = 0; i < F::BB; ++i) b[i] = 0;
-    if constexpr (T == T_Q8_0 || T == T_Q5_0 || T == T_Q4_0) {
-        constexpr int off = T == T_Q8_0 ? 0 : (T == T_Q5_0 ? 16 : 8);
-        constexpr int lo = T == T_Q8_0 ? -128 : 0, hi = T == T_Q8_0 ? 127 : (T == T_Q5_0 ? 31 : 15);
-        const uint32_t db = h16(sg[0]);
-        const float d = f16(db);
-        b[0] = (uint8_t)db;
-        b[1] = (uint8_t)(db >> 8);
-        uint32_t qh = 0;
-        for (int l = 0; l < 32; ++l) {
-            const int q = d > 0.0f ? cr(__fdiv_rn(x[l], d), lo - off, hi - off) + off : off;
-            if constexpr (T == T_Q8_0) {
-                b[2 + l] = (uint8_t)(int8_t)q;
-            } else {
-                const int base = T == T_Q5_0 ? 6 : 2;
-                b[base + (l & 15)] |= (uint8_t)((q & 15) << (4 * (l >> 4)));
-                if (T == T_Q5_0) qh |= (uint32_t)(q >> 4) << l;
-            }
+__device__ __forceinline__ void lane_errors(const uint8_t* blk, const float (&x)[32], const float (&a)[32], int lane,
+                                            float (&e)[2]) {
+    const int j = lane & 7;
+    int u0 = 0, h0 = 0, u1 = 0, h1 = 1;
+    if constexpr (T == T_Q4_K || T == T_Q5_K) {   // sub-block j: halves j % 2 of units 2(j/2), 2(j/2) + 1
+        u0 = 2 * (j >> 1);
+        u1 = u0 + 1;
+        h0 = h1 = j & 1;
+    } else if constexpr (T == T_Q2_K || T == T_Q3_K) {   // unit j
+        u0 = u1 = j;
+    } else if constexpr (T == T_Q6_K) {   // weights 32j..: units 4(j/4) + 2(j%2) + {0, 1}, half (j/2) % 2
+        u0 = 4 * (j >> 2) + 2 * (j & 1);
+        u1 = u0 + 1;
+        h0 = h1 = (j >> 1) & 1;
+    }
+    float w0[16], w1[16];
+    dequant_half<T>(blk, u0, h0, w0);
+    dequant_half<T>(blk, u1, h1, w1);
+    float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+    for (int l = 0; l < 16; ++l) {
+        const float r = __fsub_rn(x[l], w0[l]);
+        s0 = __fadd_rn(s0, __fmul_rn(a[l], __fmul_rn(r, r)));
+    }
+    float& t = ql::LaneGeo<T>::G == 32 ? s0 : s1;   // a 32-weight group continues the same sum
+#pragma unroll
+    for (int l = 0; l < 16; ++l) {
+        const float r = __fsub_rn(x[16 + l], w1[l]);
+        t = __fadd_rn(t, __fmul_rn(a[16 + l], __fmul_rn(r, r)));
+    }
+    e[0] = s0;
+    e[1] = s1;
+}
+
+template <int T>
+__global__ void __launch_bounds__(kWarps * 32) quantize_imatrix_kernel(const float* __restrict__ w,
+                                                                       const float* __restrict__ imp, int64_t ngroups,
+                                                                       int64_t groups_per_row,
+                                                                       uint8_t* __restrict__ out) {
+    using LG = ql::LaneGeo<T>;
+    constexpr int kBB = Fmt<T>::BB;
+    __shared__ __align__(16) uint32_t buf[2][kWarps][kBufWords];   // plain, weighted
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t g0 = ((int64_t)blockIdx.x * kWarps + warp) * 32;
+    if (g0 >= ngroups) return;   // whole warp
+    const int64_t left = ngroups - g0;
+    const int ng = left < 32 ? (int)left : 32;   // a multiple of 8 for the K types
+    const bool live = lane < ng;
+    float v[32], a[32];
+    if (live) {
+        const float4* src = reinterpret_cast<const float4*>(w + (g0 + lane) * 32);
+        const float* isrc = imp + ((g0 + lane) % groups_per_row) * 32;   // 4-byte aligned
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 f = __ldcs(src + i);
+            v[4 * i] = f.x;
+            v[4 * i + 1] = f.y;
+            v[4 * i + 2] = f.z;
+            v[4 * i + 3] = f.w;
         }
-        if constexpr (T == T_Q5_0)
-            for (int k = 0; k < 4; ++k) b[2 + k] = (uint8_t)(qh >> (8 * k));
-    } else if constexpr (T == T_Q6_K || T == T_Q3_K) {
-        constexpr bool six = T == T_Q6_K;
-        float maxs = 0.0f;
-        for (int g = 0; g < 16; ++g)
-            if (sg[g] > maxs) maxs = sg[g];
-        const uint32_t db = h16(__fdiv_rn(maxs, six ? 127.0f : 31.0f));
-        const float d = f16(db);
-        for (int g = 0; g < 16; ++g) {
-            const int sc = d > 0.0f ? cr(__fdiv_rn(sg[g], d), six ? -128 : -32, six ? 127 : 31) : 0;
-            const float ds = __fmul_rn(d, (float)sc);
-            if constexpr (six) {
-                b[192 + g] = (uint8_t)(int8_t)sc;
-            } else {
-                const int v = sc + 32;
-                b[96 + (g & 7)] |= (uint8_t)((v & 15) << (4 * (g >> 3)));
-                b[104 + (g & 3)] |= (uint8_t)((v >> 4) << (2 * (g >> 2)));
+        if ((reinterpret_cast<uintptr_t>(imp) & 15) == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 m = __ldg(reinterpret_cast<const float4*>(isrc) + i);
+                a[4 * i] = m.x;
+                a[4 * i + 1] = m.y;
+                a[4 * i + 2] = m.z;
+                a[4 * i + 3] = m.w;
             }
-            for (int l = 0; l < 16; ++l) {
-                const int n = 16 * g + l, t = n >> 7, r = n & 127, j = r >> 5, li = n & 31;
-                if constexpr (six) {
-                    const int q = ds != 0.0f ? cr(__fdiv_rn(x[n], ds), -32, 31) + 32 : 32;
-                    b[64 * t + li + 32 * (j & 1)] |= (uint8_t)(j < 2 ? (q & 15) : (q & 15) << 4);
-                    b[128 + 32 * t + li] |= (uint8_t)((q >> 4) << (2 * j));
-                } else {
-                    const int q = ds != 0.0f ? cr(__fdiv_rn(x[n], ds), -4, 3) : 0;
-                    const int hb = q >= 0, lo2 = hb ? q : q + 4;
-                    b[32 + 32 * t + li] |= (uint8_t)(lo2 << (2 * j));
-                    b[li] |= (uint8_t)(hb << (4 * t + j));
-                }
-            }
-        }
-        const int dpos = six ? 208 : 108;
-        b[dpos] = (uint8_t)db;
-        b[dpos + 1] = (uint8_t)(db >> 8);
-    } else {   // Q4_K, Q5_K (32-weight sub-blocks), Q2_K (16-weight groups)
-        constexpr bool two = T == T_Q2_K;
-        constexpr int G = two ? 16 : 32, NG = two ? 16 : 8, top = T == T_Q5_K ? 31 : (two ? 3 : 15);
-        constexpr int smax = two ? 15 : 63;
-        float maxsc = 0.0f, maxm = 0.0f;
-        for (int g = 0; g < NG; ++g) {
-            if (sg[g] > maxsc) maxsc = sg[g];
-            if (mg[g] > maxm) maxm = mg[g];
-        }
-        const uint32_t db = h16(__fdiv_rn(maxsc, (float)smax)), dmb = h16(__fdiv_rn(maxm, (float)smax));
-        const float d = f16(db), dmin = f16(dmb);
-        int sc[16], mn[16];
-        for (int g = 0; g < NG; ++g) {
-            sc[g] = d > 0.0f ? cr(__fdiv_rn(sg[g], d), 0, smax) : 0;
-            mn[g] = dmin > 0.0f ? cr(__fdiv_rn(mg[g], dmin), 0, smax) : 0;
-            const float ds = __fmul_rn(d, (float)sc[g]), dm = __fmul_rn(dmin, (float)mn[g]);
-            for (int l = 0; l < G; ++l) {
-                const int n = G * g + l;
-                const int q = ds > 0.0f ? cr(__fdiv_rn(__fadd_rn(x[n], dm), ds), 0, top) : 0;
-                if constexpr (two) {
-                    const int t = n >> 7, j = (n & 127) >> 5;
-                    b[16 + 32 * t + (n & 31)] |= (uint8_t)(q << (2 * j));
-                } else {
-                    const int c = n >> 6, h = (n >> 5) & 1, li = n & 31;
-                    const int qs = T == T_Q5_K ? 48 : 16;
-                    b[qs + 32 * c + li] |= (uint8_t)((q & 15) << (4 * h));
-                    if (T == T_Q5_K) b[16 + li] |= (uint8_t)((q >> 4) << (2 * c + h));
-                }
-            }
-        }
-        if constexpr (two) {
-            for (int g = 0; g < 16; ++g) b[g] = (uint8_t)(sc[g] | (mn[g] << 4));
-            b[80] = (uint8_t)db;
-            b[81] = (uint8_t)(db >> 8);
-            b[82] = (uint8_t)dmb;
-            b[83] = (uint8_t)(dmb >> 8);
         } else {
-            for (int j = 0; j < 4; ++j) {
-                b[4 + j] = (uint8_t)(sc[j] | ((sc[j + 4] >> 4) << 6));
-                b[8 + j] = (uint8_t)(mn[j] | ((mn[j + 4] >> 4) << 6));
-                b[12 + j] = (uint8_t)((sc[j + 4] & 15) | ((mn[j + 4] & 15) << 4));
+#pragma unroll
+            for (int l = 0; l < 32; ++l) a[l] = __ldg(isrc + l);
+        }
+    } else {
+#pragma unroll
+        for (int l = 0; l < 32; ++l) v[l] = a[l] = 0.0f;
+    }
+    const int bo = (LG::K ? (lane >> 3) : lane) * kBB;
+    uint8_t* bp = reinterpret_cast<uint8_t*>(buf[0][warp]);
+    uint8_t* bw = reinterpret_cast<uint8_t*>(buf[1][warp]);
+    float sp[2], mp[2], sw[2], mw[2];
+    ql::plain_params<T>(v, sp, mp);
+    ql::assemble<T>(v, sp, mp, lane, live, bp + bo);
+    sw[1] = mw[1] = 0.0f;
+#pragma unroll
+    for (int e = 0; e < LG::NG; ++e) search<T, LG::G>(v + LG::G * e, a + LG::G * e, sp[e], mp[e], sw[e], mw[e]);
+    ql::assemble<T>(v, sw, mw, lane, live, bw + bo);
+    __syncwarp();
+    float ep[2], ew[2];
+    lane_errors<T>(bp + bo, v, a, lane, ep);
+    lane_errors<T>(bw + bo, v, a, lane, ew);
+    // Block totals over its groups in order (a K type's groups sit in the
+    // eight lanes of its super-block, in lane order).
+    float tp = 0.0f, tw = 0.0f;
+    if constexpr (LG::K) {
+#pragma unroll
+        for (int jp = 0; jp < 8; ++jp) {
+#pragma unroll
+            for (int e = 0; e < LG::NG; ++e) {
+                tp = __fadd_rn(tp, __shfl_sync(ql::kFull, ep[e], (lane & ~7) + jp));
+                tw = __fadd_rn(tw, __shfl_sync(ql::kFull, ew[e], (lane & ~7) + jp));
             }
-            b[0] = (uint8_t)db;
-            b[1] = (uint8_t)(db >> 8);
-            b[2] = (uint8_t)dmb;
-            b[3] = (uint8_t)(dmb >> 8);
         }
+    } else {
+        tp = __fadd_rn(tp, ep[0]);
+        tw = __fadd_rn(tw, ew[0]);
     }
-}
-
-// Step 3: weighted error of an encoded block (its weights through the
-// shared half decoders), per group then over groups.
-template <int T>
-__device__ float weighted_error(const uint8_t* b, const float* x, const float* a) {
-    using F = Fmt<T>;
-    constexpr int G = Geo<T>::G;
-    float w[256];
-    for (int u = 0; u < F::UPB; ++u)
-        for (int h = 0; h < 2; ++h) {
-            float v[16];
-            dequant_half<T>(b, u, h, v);
-            for (int i = 0; i < 16; ++i) w[F::koff(u, h) + i] = v[i];
-        }
-    float total = 0.0f;
-    for (int g = 0; g < F::BE / G; ++g) {
-        float e = 0.0f;
-        for (int l = 0; l < G; ++l) {
-            const float r = __fsub_rn(x[G * g + l], w[G * g + l]);
-            e = __fadd_rn(e, __fmul_rn(a[G * g + l], __fmul_rn(r, r)));
-        }
-        total = __fadd_rn(total, e);
+    // The weighted block replaces the plain one where it is no worse; the
+    // lanes of a block copy its bytes.
+    if (live && tw <= tp) {
+        const int nl = LG::K ? 8 : 1, me = LG::K ? (lane & 7) : 0;
+        for (int i = me; i < kBB; i += nl) bp[bo + i] = bw[bo + i];
     }
-    return total;
-}
-
-template <int T>
-__global__ void __launch_bounds__(128) quantize_imatrix_kernel(const float* __restrict__ w, const float* __restrict__ imp,
-                                                               int64_t nblocks, int64_t nb_row, uint8_t* __restrict__ out) {
-    using F = Fmt<T>;
-    constexpr int G = Geo<T>::G, NG = F::BE / G;
-    const int64_t blk = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-    if (blk >= nblocks) return;
-    const int64_t bi = blk % nb_row;
-    const float* x = w + blk * F::BE;      // rows are consecutive blocks
-    const float* a = imp + bi * F::BE;
-    float sg[16], mg[16];
-    alignas(16) uint8_t plain[F::BB + 16], mine[F::BB + 16];
-    for (int g = 0; g < NG; ++g) group_params<T>(x + G * g, a + G * g, true, sg[g], mg[g]);
-    assemble<T>(x, sg, mg, plain);
-    for (int g = 0; g < NG; ++g) group_params<T>(x + G * g, a + G * g, false, sg[g], mg[g]);
-    assemble<T>(x, sg, mg, mine);
-    const float ep = weighted_error<T>(plain, x, a), em = weighted_error<T>(mine, x, a);
-    const uint8_t* src = em <= ep ? mine : plain;
-    uint8_t* o = out + blk * F::BB;
-    for (int i = 0; i < F::BB; ++i) o[i] = src[i];
+    __syncwarp();
+    const int64_t ob = (LG::K ? g0 / 8 : g0) * kBB;
+    const int nb = (LG::K ? ng / 8 : ng) * kBB;
+    uint8_t* dst = out + ob;
+    for (int i = lane; i < nb / 4; i += 32) reinterpret_cast<uint32_t*>(dst)[i] = buf[0][warp][i];
+    if (lane < (nb & 3)) dst[(nb & ~3) + lane] = bp[(nb & ~3) + lane];
 }
 
 template <int T>
 cudaError_t launch_t(const float* w, const float* imp, int64_t rows, int64_t cols, uint8_t* out, cudaStream_t s) {
-    const int64_t nb_row = cols / Fmt<T>::BE, nblocks = rows * nb_row;
-    if (nblocks == 0) return cudaSuccess;
-    const int64_t grid = (nblocks + 127) / 128;
-    if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    quantize_imatrix_kernel<T><<<(unsigned)grid, 128, 0, s>>>(w, imp, nblocks, nb_row, out);
+    const int64_t gpr = cols / 32, ngroups = rows * gpr;
+    if (ngroups == 0) return cudaSuccess;
+    const int64_t warps = (ngroups + 31) / 32;
+    const int64_t blocks = (warps + kWarps - 1) / kWarps;
+    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    quantize_imatrix_kernel<T><<<(unsigned)blocks, kWarps * 32, 0, s>>>(w, imp, ngroups, gpr, out);
     return cudaGetLastError();
 }
 

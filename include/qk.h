@@ -193,8 +193,12 @@ qk_status qk_attn_decode(int type, const float* q, const void* K, const void* V,
  *   the plain block is written.  fp32 throughout, sums in index order, so
  *   the bytes are deterministic.  All-zero importances give qk_quantize's
  *   bytes.
- *   w, imp  device, 4-byte aligned.   out  rows * qk_row_bytes bytes.
- * One thread per block: an offline step, not a bandwidth-bound kernel.
+ *   w    device fp32 [rows, cols], 16-byte aligned.
+ *   imp  device fp32 [cols], 4-byte aligned.
+ *   out  rows * qk_row_bytes(type, cols) bytes, 4-byte aligned.
+ * One lane per 32 weights (it searches its own groups; the codes of a
+ * candidate take one reciprocal of its scale, with the division's rounding
+ * reproduced exactly), a warp per 32 groups.
  * Errors as qk_quantize. */
 qk_status qk_quantize_imatrix(int type, const float* w, int64_t rows, int64_t cols, const float* imp, void* out,
                               void* stream);

@@ -41,6 +41,8 @@ CASES = [
     ("Q5_K", 130, 768, 40),
     ("Q2_K", 130, 1024, 40),
     ("Q3_K", 200, 2048, 16),
+    ("Q2_K", 257, 2304, 16),     # the small-batch decoders: every k-block position, ragged rows
+    ("Q3_K", 131, 1280, 5),
 ]
 
 

@@ -164,3 +164,52 @@ def test_quantize_imatrix_matches_oracle(gpu, name, rows, cols):
     # All-zero importances: the plain quantizer's bytes.
     z = qk.quantize_imatrix(t, torch.from_numpy(w).to(gpu), torch.zeros(cols, device=gpu)).cpu().numpy()
     assert np.array_equal(z, oracle.quantize(t, w))
+
+
+@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q5_0", "Q4_0", "Q5_K", "Q2_K", "Q3_K"])
+def test_quantize_imatrix_special_values(gpu, name):
+    # The special-value blocks (zero divisors, fp16 subnormal and overflowing
+    # scales, exact ties, NaN, infinities, negative zero) through the
+    # importance-weighted search, with positive importances.
+    t = type_id(name)
+    n = 256 if name in ("Q4_K", "Q6_K", "Q5_K", "Q2_K", "Q3_K") else 32
+    w = np.tile(special_blocks(n), (1, 8))
+    imp = np.random.default_rng(8181).uniform(0.1, 4.0, w.shape[1]).astype(np.float32)
+    with np.errstate(invalid="ignore", over="ignore"):
+        ref = oracle.quantize_imatrix(t, w, imp)
+    got = qk.quantize_imatrix(t, torch.from_numpy(w).to(gpu), torch.from_numpy(imp).to(gpu)).cpu().numpy()
+    qk.device_status()
+    assert np.array_equal(got, ref), f"{name}: {int((got != ref).sum())} bytes differ"
+
+
+@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0"])
+def test_quantize_imatrix_bench_size_sampled_rows(gpu, name):
+    # The bench's importance-weighted launch (14336 x 4096, N(0, 0.02) weights,
+    # log-normal importances); the oracle quantizes 24 sampled rows.
+    t, rows, cols = type_id(name), 14336, 4096
+    g = torch.Generator(device=gpu)
+    g.manual_seed(4242)
+    w = torch.randn((rows, cols), device=gpu, generator=g) * 0.02
+    imp = torch.exp(torch.randn(cols, device=gpu, generator=g))
+    got = qk.quantize_imatrix(t, w, imp)
+    qk.device_status()
+    rb = qk.row_bytes(t, cols)
+    pick = np.random.default_rng(8).choice(rows, 24, replace=False)
+    pick[:2] = (0, rows - 1)
+    sel = torch.from_numpy(pick).to(gpu)
+    ref = oracle.quantize_imatrix(t, w[sel].cpu().numpy(), imp.cpu().numpy()).reshape(len(pick), rb)
+    assert np.array_equal(got.view(rows, rb)[sel].cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("name", ["Q4_K", "Q8_0"])
+def test_quantize_imatrix_takes_4_byte_aligned_importances(gpu, name):
+    # imp one float past a 16-byte boundary (the contract asks 4 bytes): the
+    # same bytes as the oracle.
+    t, rows, cols = type_id(name), 5, 512
+    w = synth.normal_weights(rows, cols, 9191)
+    imp = np.random.default_rng(9192).uniform(0.05, 3.0, cols).astype(np.float32)
+    buf = torch.zeros(cols + 4, device=gpu)
+    buf[1:1 + cols] = torch.from_numpy(imp).to(gpu)
+    got = qk.quantize_imatrix(t, torch.from_numpy(w).to(gpu), buf[1:1 + cols]).cpu().numpy()
+    qk.device_status()
+    assert np.array_equal(got, oracle.quantize_imatrix(t, w, imp))
