@@ -246,6 +246,67 @@ __device__ __forceinline__ void kcodes(const uint8_t* blk, int tq, uint32_t (&a)
     }
 }
 
+// kcodes for the streaming kernel, with the row's word addressing set up
+// once.  The three block sizes (34, 18, 22 bytes) are 2 mod 4, so the words a
+// thread reads (element 4 tq of block b, and its second half at + 16 for
+// Q8_0) sit at one misalignment m in the even blocks and m ^ 2 in the odd
+// ones, the same in every row of the CTA (slots are 16-byte multiples).
+// KAddr holds, per parity, the aligned address of block 0's word and the
+// funnel shift; block b adds b * BB (an immediate once b is unrolled).
+struct KAddr {
+    const uint8_t* base[2];   // aligned word address of the element-4tq word of block 0 (even) / block 1 less BB (odd)
+    uint32_t sh[2];           // funnel shifts, bits
+    int qh;                   // Q5_0: offset of the fifth-bit word from the same aligned base
+};
+template <int T>
+__device__ __forceinline__ KAddr kaddr(const uint8_t* row, int tq) {
+    constexpr int BB = Fmt<T>::BB;
+    const int hdr = T == T_Q5_0 ? 6 : 2;   // first code byte
+    const uint8_t* p = row + hdr + 4 * tq;
+    const int m = (int)(reinterpret_cast<uintptr_t>(p) & 3);   // 0 or 2
+    KAddr k;
+    k.base[0] = p - m;
+    k.base[1] = p + BB - (m ^ 2) - BB;   // block 1's word, less BB
+    k.sh[0] = 8u * (uint32_t)m;
+    k.sh[1] = 8u * (uint32_t)(m ^ 2);
+    k.qh = -4 - 4 * tq;                   // Q5_0: the word at byte 2 has the same misalignment
+    return k;
+}
+__device__ __forceinline__ uint32_t kword(const KAddr& k, int par, int off) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(k.base[par] + off);
+    return __funnelshift_r(w[0], w[1], k.sh[par]);
+}
+template <int T>
+__device__ __forceinline__ void kcodes_at(const KAddr& k, int b, uint32_t (&a)[4]) {
+    using hm::and_or;
+    using hm::and_xor;
+    using hm::hadd2;
+    constexpr int BB = Fmt<T>::BB;
+    const int par = b & 1, o = BB * b;
+    if constexpr (T == T_Q8_0) {
+        const uint32_t w0 = kword(k, par, o), w1 = kword(k, par, o + 16);
+        a[0] = hadd2(and_xor(w0, 0x00FF00FFu, 0x64806480u), 0xE480E480u);
+        a[1] = hadd2(and_xor(w0 >> 8, 0x00FF00FFu, 0x64806480u), 0xE480E480u);
+        a[2] = hadd2(and_xor(w1, 0x00FF00FFu, 0x64806480u), 0xE480E480u);
+        a[3] = hadd2(and_xor(w1 >> 8, 0x00FF00FFu, 0x64806480u), 0xE480E480u);
+    } else if constexpr (T == T_Q4_0) {
+        const uint32_t w = kword(k, par, o);
+        a[0] = hadd2(and_or(w, 0x000F000Fu, 0x64006400u), 0xE408E408u);
+        a[1] = hadd2(and_or(w >> 8, 0x000F000Fu, 0x64006400u), 0xE408E408u);
+        a[2] = hadd2(and_or(w, 0x00F000F0u, 0x54005400u), 0xD480D480u);
+        a[3] = hadd2(and_or(w >> 8, 0x00F000F0u, 0x54005400u), 0xD480D480u);
+    } else {
+        const uint32_t qh = kword(k, par, o + k.qh), w = kword(k, par, o);
+        const int tq = (-4 - k.qh) >> 2;
+        const uint32_t v0 = (w & 0x0F0F0F0Fu) | bit4_spread(qh >> (4 * tq));
+        const uint32_t v1 = ((w >> 4) & 0x0F0F0F0Fu) | bit4_spread(qh >> (16 + 4 * tq));
+        a[0] = hadd2(and_or(v0, 0x00FF00FFu, 0x64006400u), 0xE410E410u);
+        a[1] = hadd2(and_or(v0 >> 8, 0x00FF00FFu, 0x64006400u), 0xE410E410u);
+        a[2] = hadd2(and_or(v1, 0x00FF00FFu, 0x64006400u), 0xE410E410u);
+        a[3] = hadd2(and_or(v1 >> 8, 0x00FF00FFu, 0x64006400u), 0xE410E410u);
+    }
+}
+
 // B fragments of the group's queries (sq: [heads][D] fp32) and the scale of
 // each (head, 32-block).  Per block, x' = q 2^-e with e = max(0,
 // floor(log2 max|q|) - 14), so |x'| < 2^15 fits fp16; hi = fp16(x'), lo =
@@ -633,14 +694,15 @@ __global__ void __launch_bounds__(kSThreads, 2) attn_stream_kernel(const __grid_
             // Scores of positions gq and gq + 8 of the tile.
             const uint8_t* r0 = kst + (jt + gq) * Gm::SLOT + misg;
             const uint8_t* r1 = r0 + 8 * Gm::SLOT;
+            const KAddr k0 = kaddr<T>(r0, tq), k1 = kaddr<T>(r1, tq);
             float s0[NT], s1[NT];
 #pragma unroll
             for (int n = 0; n < NT; ++n) s0[n] = s1[n] = 0.0f;
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
                 uint32_t a0[4], a1[4];
-                kcodes<T>(r0 + b * BB, tq, a0);
-                kcodes<T>(r1 + b * BB, tq, a1);
+                kcodes_at<T>(k0, b, a0);
+                kcodes_at<T>(k1, b, a1);
                 const float d0 = h2f(lds16(r0 + b * BB)), d1 = h2f(lds16(r1 + b * BB));
 #pragma unroll
                 for (int n = 0; n < NT; ++n) {
