@@ -54,7 +54,6 @@ constexpr int kA = kBM * kBK * 2; // 16 KB of bf16 weights per stage
 constexpr int kDeqWarps = 16;
 constexpr int kDeqThreads = kDeqWarps * 32;
 constexpr int kThreads = (2 + kDeqWarps) * 32;   // TMA warp, MMA warp, dequant warps
-constexpr int kParts = kDeqThreads / kBM;            // threads per tile row (4): 16 weights each
 
 // Pipeline shape.  Three rings: NS weight stages (bf16 operand A, written by
 // the dequant warps), an activation ring of run-time depth (operand B, one
@@ -473,23 +472,32 @@ __device__ __forceinline__ void generic16(const uint8_t* mb, int o, uint32_t (&p
     for (int i = 0; i < 8; ++i) pk[i] = pack_bf16(w[2 * i], w[2 * i + 1]);
 }
 
-// Copy macro-block `m` of the tile's 128 rows into packed slot `dst` with
-// 16-byte cp.async (aligned-down windows; thread t takes row t/2, every
-// other chunk).  Bytes past the last full 16 bytes of W are loaded by the
-// consumer of that row (tail_fix).
+// Copy macro-block `m` of one warp's 8 tile rows (8 dw .. 8 dw + 7) into
+// packed slot `dst` with 16-byte cp.async (each row's aligned-down window).
+// The (row, chunk) pairs are numbered row-major over SLOT / 16 chunk places
+// per row and taken by consecutive lanes, so that one instruction's lanes
+// read a few rows' contiguous windows (few cache lines) and write
+// consecutive 16-byte units of shared memory (a slot is an odd number of
+// them: no bank conflicts).  Bytes past the last full 16 bytes of W are
+// loaded by the consumer of that row (tail_fix).
 template <int T>
-__device__ __forceinline__ void issue_packed(const Args& p, uint8_t* dst, int64_t row0, int64_t m, int r, int part) {
+__device__ __forceinline__ void issue_packed(const Args& p, uint8_t* dst, int64_t row0, int64_t m, int dw, int lane) {
     using K = PkGeo<T>;
-    const int64_t row = row0 + r;
-    if (row >= p.rows) return;
+    constexpr int NCH = K::SLOT / 16;   // chunk places per row (at least the longest window)
     const int64_t kb0 = m * K::MB;
     const int64_t len = min((int64_t)K::MB, p.cols - kb0) / Fmt<T>::BE * Fmt<T>::BB;
-    const int64_t st = row * p.row_bytes + m * K::BYTES;
-    const int64_t a = st & ~(int64_t)15;
-    const int64_t e = min((st + len + 15) & ~(int64_t)15, p.total16);
-    const int nch = e > a ? (int)((e - a) >> 4) : 0;
-    uint8_t* d = dst + r * K::SLOT;
-    for (int ch = part; ch < nch; ch += kParts) cp_async16(d + 16 * ch, p.W + a + 16 * ch);
+#pragma unroll
+    for (int k = 0; k < (8 * NCH + 31) / 32; ++k) {
+        const int pr = lane + 32 * k, rl = pr / NCH, ch = pr - rl * NCH;
+        const int r = 8 * dw + rl;
+        const int64_t row = row0 + r;
+        if (rl < 8 && row < p.rows) {
+            const int64_t st = row * p.row_bytes + m * K::BYTES;
+            const int64_t a = st & ~(int64_t)15;
+            const int64_t e = min((st + len + 15) & ~(int64_t)15, p.total16);
+            if (a + 16 * ch < e) cp_async16(dst + r * K::SLOT + 16 * ch, p.W + a + 16 * ch);
+        }
+    }
 }
 
 template <int T>
@@ -643,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         int ps = 0;           // packed slot of the current macro-block
 #pragma unroll 1
         for (int mi = 0; mi < kNSP - 1; ++mi) {
-            if (mi < nmb) issue_packed<T>(p, packed + mi * K::STAGE, row0, (int64_t)(m0 + mi), r, qq);
+            if (mi < nmb) issue_packed<T>(p, packed + mi * K::STAGE, row0, (int64_t)(m0 + mi), dw, lane);
             cp_async_commit();
         }
 #pragma unroll 1
@@ -651,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const int m = m0 + mi;
             const int pn = ps == 0 ? kNSP - 1 : ps - 1;   // slot of macro-block mi + NSP - 1
             if (mi + kNSP - 1 < nmb)
-                issue_packed<T>(p, packed + pn * K::STAGE, row0, (int64_t)(m + kNSP - 1), r, qq);
+                issue_packed<T>(p, packed + pn * K::STAGE, row0, (int64_t)(m + kNSP - 1), dw, lane);
             cp_async_commit();
             cp_async_wait<kNSP - 1>();
             uint8_t* pk = packed + ps * K::STAGE;
