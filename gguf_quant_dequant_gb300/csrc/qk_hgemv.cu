@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
         const uint64_t pol = policy_evict_first();
         const int64_t total16 = (rows * (int64_t)rb) & ~(int64_t)15;
         int it = 0, s = 0;
-        uint32_t ph = 0;   // phase parity of stage s's barriers in this round of the ring
+        uint32_t ph = 0;   // phase parity of stage s's barriers in this pass over the ring
         bool dead = false;
         for (int c = 0; c < p.nchunks && !dead; ++c) {
             const int64_t coff = (int64_t)c * CB;
