@@ -102,6 +102,11 @@ __device__ __forceinline__ void sym_codes(const float* v, float ds, uint32_t* q)
 //   Q4_K / Q5_K / Q2_K: lo = min(0, min w), hi = max w, s = (hi - lo) / (15,
 //   31, 3), m = -lo;  Q6_K / Q3_K: s = max|w| / (32, 4);  Q8_0 / Q5_0 / Q4_0:
 //   s = max|w| / (127, 15, 7).
+// The scans are the sequential "if (x < lo) lo = x" from 0 and "if (x > hi)
+// hi = x" from the first weight: fminf / fmaxf chains give the same values
+// (both skip NaN), except that hi stays NaN when the first weight is NaN.
+// Signed zeros may come out the other way round, which no code or scale
+// depends on.
 template <int T>
 __device__ __forceinline__ void plain_params(const float (&v)[32], float (&s)[2], float (&m)[2]) {
     constexpr int G = LaneGeo<T>::G;
@@ -113,9 +118,10 @@ __device__ __forceinline__ void plain_params(const float (&v)[32], float (&s)[2]
             float lo = 0.0f, hi = v[G * e];
 #pragma unroll
             for (int l = 0; l < G; ++l) {
-                if (v[G * e + l] < lo) lo = v[G * e + l];
-                if (v[G * e + l] > hi) hi = v[G * e + l];
+                lo = fminf(lo, v[G * e + l]);
+                hi = fmaxf(hi, v[G * e + l]);
             }
+            if (v[G * e] != v[G * e]) hi = v[G * e];   // a NaN first weight: the scan keeps it
             s[e] = __fdiv_rn(__fsub_rn(hi, lo), kDiv);
             m[e] = -lo;
         } else {
@@ -123,10 +129,7 @@ __device__ __forceinline__ void plain_params(const float (&v)[32], float (&s)[2]
                                  : T == T_Q8_0 ? 127.0f : (T == T_Q5_0 ? 15.0f : 7.0f);
             float a = 0.0f;
 #pragma unroll
-            for (int l = 0; l < G; ++l) {
-                const float x = fabsf(v[G * e + l]);
-                if (x > a) a = x;
-            }
+            for (int l = 0; l < G; ++l) a = fmaxf(a, fabsf(v[G * e + l]));
             s[e] = __fdiv_rn(a, kDiv);
         }
     }

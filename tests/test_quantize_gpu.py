@@ -69,6 +69,8 @@ def special_blocks(n):
         np.where(np.arange(n) % 32 == 0, 127.0 / 128.0,
                  (np.arange(n) % 32 - 16 + 0.5) / 128.0),       # max 127/128: Q8_0 d = 1/128, exact .5 ties
         np.where(np.arange(n) == 7, np.nan, base),               # NaN inside a block
+        np.where(np.arange(n) % 32 == 0, np.nan, base),          # NaN first in every 32-weight group
+        np.where(np.arange(n) % 16 == 0, np.nan, -np.abs(base)),  # ... and every 16-weight group
         np.where(np.arange(n) == 9, np.inf, base),
         np.where(np.arange(n) == 9, -np.inf, base),
         np.where(np.arange(n) % 3 == 0, -0.0, base),
