@@ -52,7 +52,6 @@ constexpr int kBM = 128;          // weight rows per CTA (MMA M)
 constexpr int kBK = 64;           // K per stage (one 128-byte swizzle row)
 constexpr int kA = kBM * kBK * 2; // 16 KB of bf16 weights per stage
 constexpr int kDeqWarps = 16;
-constexpr int kDeqThreads = kDeqWarps * 32;
 constexpr int kThreads = (2 + kDeqWarps) * 32;   // TMA warp, MMA warp, dequant warps
 
 // Pipeline shape.  Three rings: NS weight stages (bf16 operand A, written by
