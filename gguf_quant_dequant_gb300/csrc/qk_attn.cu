@@ -257,6 +257,7 @@ struct KAddr {
     const uint8_t* base[2];   // aligned word address of the element-4tq word of block 0 (even) / block 1 less BB (odd)
     uint32_t sh[2];           // funnel shifts, bits
     int qh;                   // Q5_0: offset of the fifth-bit word from the same aligned base
+    int tq;                   // the thread's group of the MMA layout
 };
 template <int T>
 __device__ __forceinline__ KAddr kaddr(const uint8_t* row, int tq) {
@@ -270,6 +271,7 @@ __device__ __forceinline__ KAddr kaddr(const uint8_t* row, int tq) {
     k.sh[0] = 8u * (uint32_t)m;
     k.sh[1] = 8u * (uint32_t)(m ^ 2);
     k.qh = -4 - 4 * tq;                   // Q5_0: the word at byte 2 has the same misalignment
+    k.tq = tq;
     return k;
 }
 __device__ __forceinline__ uint32_t kword(const KAddr& k, int par, int off) {
@@ -297,9 +299,8 @@ __device__ __forceinline__ void kcodes_at(const KAddr& k, int b, uint32_t (&a)[4
         a[3] = hadd2(and_or(w >> 8, 0x00F000F0u, 0x54005400u), 0xD480D480u);
     } else {
         const uint32_t qh = kword(k, par, o + k.qh), w = kword(k, par, o);
-        const int tq = (-4 - k.qh) >> 2;
-        const uint32_t v0 = (w & 0x0F0F0F0Fu) | bit4_spread(qh >> (4 * tq));
-        const uint32_t v1 = ((w >> 4) & 0x0F0F0F0Fu) | bit4_spread(qh >> (16 + 4 * tq));
+        const uint32_t v0 = (w & 0x0F0F0F0Fu) | bit4_spread(qh >> (4 * k.tq));
+        const uint32_t v1 = ((w >> 4) & 0x0F0F0F0Fu) | bit4_spread(qh >> (16 + 4 * k.tq));
         a[0] = hadd2(and_or(v0, 0x00FF00FFu, 0x64006400u), 0xE410E410u);
         a[1] = hadd2(and_or(v0 >> 8, 0x00FF00FFu, 0x64006400u), 0xE410E410u);
         a[2] = hadd2(and_or(v1, 0x00FF00FFu, 0x64006400u), 0xE410E410u);

@@ -215,3 +215,14 @@ def test_quantize_imatrix_takes_4_byte_aligned_importances(gpu, name):
     got = qk.quantize_imatrix(t, torch.from_numpy(w).to(gpu), buf[1:1 + cols]).cpu().numpy()
     qk.device_status()
     assert np.array_equal(got, oracle.quantize_imatrix(t, w, imp))
+
+
+@pytest.mark.parametrize("name", ["Q4_K", "Q6_K", "Q8_0", "Q3_K"])
+def test_quantize_persistent_grid_ragged_tail(gpu, name):
+    # 1201 x 2304: 86,472 groups = 2,702 tiles of 32 groups and a last tile of 8,
+    # more tiles than the persistent grid's warps, so warps take several tiles
+    # and one of them the ragged tail.
+    t = type_id(name)
+    w = synth.normal_weights(1201, 2304, 9393)
+    got = run(gpu, t, w)
+    assert np.array_equal(got, oracle.quantize(t, w))
