@@ -93,12 +93,12 @@ __device__ __forceinline__ void prep_unit_x(const float* xs, uint8_t* xb, float4
     const int jl = lane >> 2, q = lane & 3;
     const float4 a = *reinterpret_cast<const float4*>(xs + 8 * lane), b = *reinterpret_cast<const float4*>(xs + 8 * lane + 4);
     const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    float amax = 0.0f, sum = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        amax = fmaxf(amax, fabsf(v[i]));
-        sum += v[i];
-    }
+    const float amax_a = fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w)));
+    float amax = fmaxf(amax_a, fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+    // The eight elements' sum by packed pair adds (any order: an fp32 block sum).
+    const float2 s2 = __fadd2_rn(__fadd2_rn(make_float2(a.x, a.y), make_float2(a.z, a.w)),
+                                 __fadd2_rn(make_float2(b.x, b.y), make_float2(b.z, b.w)));
+    float sum = s2.x + s2.y;
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     sum += __shfl_xor_sync(0xffffffffu, sum, 1);           // sum of 16 elements (one half)
@@ -113,10 +113,11 @@ __device__ __forceinline__ void prep_unit_x(const float* xs, uint8_t* xb, float4
     uint32_t hi[4], lo[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const float a = v[kPair[k][0]] * down, b = v[kPair[k][1]] * down;
-        const __half2 h = __floats2half2_rn(a, b);
+        const float2 ab = __fmul2_rn(make_float2(v[kPair[k][0]], v[kPair[k][1]]), make_float2(down, down));
+        const __half2 h = __floats2half2_rn(ab.x, ab.y);
         const float2 hf = __half22float2(h);
-        const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+        const float2 r = __ffma2_rn(hf, make_float2(-1.0f, -1.0f), ab);   // x' - hi, exact
+        const __half2 l = __floats2half2_rn(r.x, r.y);
         hi[k] = *reinterpret_cast<const uint32_t*>(&h);
         lo[k] = *reinterpret_cast<const uint32_t*>(&l);
     }

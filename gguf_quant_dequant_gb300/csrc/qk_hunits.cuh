@@ -275,8 +275,9 @@ template <> struct HU<T_Q6_K> {
     __device__ static __forceinline__ void conv(const Ctx& x, int i, int t, uint32_t (&A)[8]) {
         const int sh = 4 - 2 * (t & 1);   // qh bits 2gl -> bits 4-5 of a byte, bits 2gl+4 -> bits 8-9 of a half
         const uint32_t v0 = x.qh0[i] << sh, v1 = x.qh1[i] << sh;
-        // Bytes 1 and 3: shift down first, so that byte 3's bits stay in the word.
-        const uint32_t u0 = x.ql0[i] >> 8, u1 = x.ql1[i] >> 8, e0 = (x.qh0[i] >> 8) << sh, e1 = (x.qh1[i] >> 8) << sh;
+        // Bytes 1 and 3: one right shift puts their qh bits where v has those
+        // of bytes 0 and 2 (the other bits it moves are masked off).
+        const uint32_t u0 = x.ql0[i] >> 8, u1 = x.ql1[i] >> 8, e0 = x.qh0[i] >> (8 - sh), e1 = x.qh1[i] >> (8 - sh);
         const uint32_t CLO = dup16(0xE420u), CHI = dup16(0xD600u);   // -(1024 + 32), -(64 + 32)
         // (low code bits & m1) | (high code bits & m2) | magic: two logic ops.
         auto cv = [](uint32_t lo, uint32_t m1, uint32_t hi, uint32_t m2, uint32_t mg) {
