@@ -189,25 +189,54 @@ template <> struct HU<T_Q4_K> {
     }
     struct Row {
         uint32_t clo, chi;   // half2 offsets -(magic + o) of the low and high nibble codes
-        float ds_lo, ds_hi, r_lo, r_hi;
+        float2 ds;           // d*sc of the low and high sub-block
+        float2 nr;           // -r = d*sc*o - dmin*m of each
     };
     // The per-sub-block factors d*sc and dmin*m, the nearest code o of their
     // ratio and the residual r = dmin*m - d*sc*o; the high codes use magic
-    // 64 (hi_magic64) or 1024 (codes moved down first, as Q5_K's).
+    // 64 (hi_magic64) or 1024 (codes moved down first, as Q5_K's).  The two
+    // sub-blocks go through packed fp32 pair operations (each lane rounds as
+    // the scalar operation would).
     template <bool hi_magic64>
     __device__ static __forceinline__ Row row_params(const uint4& h, int t, float qmax) {
         const uint32_t f = fields(h, t);
         const float d = h2f(h.x & 0xFFFFu), dmin = h2f(h.x >> 16);
+        constexpr float kM = 8388608.0f, kR = 12582912.0f;   // 2^23, 1.5 * 2^23
+        const float2 sc = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(f, 0x4B000000u, 0x7650)),
+                                                 __uint_as_float(__byte_perm(f, 0x4B000000u, 0x7651))),
+                                     make_float2(-kM, -kM));
+        const float2 mm = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(f, 0x4B000000u, 0x7652)),
+                                                 __uint_as_float(__byte_perm(f, 0x4B000000u, 0x7653))),
+                                     make_float2(-kM, -kM));
         Row r;
-        r.ds_lo = d * ubyte_f(f, 0);
-        r.ds_hi = d * ubyte_f(f, 1);
-        const float dm_lo = dmin * ubyte_f(f, 2), dm_hi = dmin * ubyte_f(f, 3);
-        const float m_lo = nearest_code_m(dm_lo, r.ds_lo, qmax), m_hi = nearest_code_m(dm_hi, r.ds_hi, qmax);
-        r.r_lo = fmaf(-r.ds_lo, m_lo - 12582912.0f, dm_lo);
-        r.r_hi = fmaf(-r.ds_hi, m_hi - 12582912.0f, dm_hi);
-        r.clo = neg_magic1024(m_lo);
-        r.chi = hi_magic64 ? neg_magic64(m_hi) : neg_magic1024(m_hi);
+        r.ds = __fmul2_rn(make_float2(d, d), sc);
+        const float2 ndm = __fmul2_rn(make_float2(-dmin, -dmin), mm);   // -dmin*m, exact
+        // The nearest code of dm / ds (nearest_code_m, per lane): the ratio's
+        // sign is carried by the saturating multiply's factor.
+        float rc0, rc1, u0, u1;
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc0) : "f"(r.ds.x));
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc1) : "f"(r.ds.y));
+        const float2 q = __fmul2_rn(ndm, make_float2(rc0, rc1));
+        asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(u0) : "f"(q.x), "f"(-1.0f / qmax));
+        asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(u1) : "f"(q.y), "f"(-1.0f / qmax));
+        const float2 m = __ffma2_rn(make_float2(u0, u1), make_float2(qmax, qmax), make_float2(kR, kR));
+        const float2 o = __fadd2_rn(m, make_float2(-kR, -kR));
+        r.nr = __ffma2_rn(r.ds, o, ndm);
+        r.clo = neg_magic1024(m.x);
+        r.chi = hi_magic64 ? neg_magic64(m.y) : neg_magic1024(m.y);
         return r;
+    }
+    // y0, y1 += the unit's sums of rows g, g + 8 (low / high sub-block sums
+    // of group t in c[0] / c[2]): ds*2^e*t - r*X per sub-block, packed.
+    __device__ static __forceinline__ void epi_min(const Row& p0, const Row& p1, const float (&c)[4][4], float4 xm0,
+                                                   float4 xm1, float& y0, float& y1) {
+        const float2 t0 = __fadd2_rn(make_float2(c[0][0], c[2][0]), make_float2(c[0][1], c[2][1]));   // row g
+        const float2 t1 = __fadd2_rn(make_float2(c[0][2], c[2][2]), make_float2(c[0][3], c[2][3]));   // row g + 8
+        const float2 e = make_float2(xm0.y, xm1.y), X = make_float2(xm0.x, xm1.x);
+        const float2 z0 = __ffma2_rn(__fmul2_rn(p0.ds, e), t0, __fmul2_rn(p0.nr, X));
+        const float2 z1 = __ffma2_rn(__fmul2_rn(p1.ds, e), t1, __fmul2_rn(p1.nr, X));
+        y0 += z0.x + z0.y;
+        y1 += z1.x + z1.y;
     }
     struct Ctx {
         uint32_t w0[8], w1[8];
@@ -237,10 +266,7 @@ template <> struct HU<T_Q4_K> {
     }
     __device__ static __forceinline__ void epi(const Ctx& x, const float (&c)[4][4], float4 xm0, float4 xm1, int, int,
                                                float& y0, float& y1) {
-        const float tl0 = csum_g(c[0]) + csum_g(c[1]), th0 = csum_g(c[2]) + csum_g(c[3]);
-        const float tl1 = csum_g8(c[0]) + csum_g8(c[1]), th1 = csum_g8(c[2]) + csum_g8(c[3]);
-        y0 += fmaf(x.p0.ds_lo * xm0.y, tl0, -x.p0.r_lo * xm0.x) + fmaf(x.p0.ds_hi * xm1.y, th0, -x.p0.r_hi * xm1.x);
-        y1 += fmaf(x.p1.ds_lo * xm0.y, tl1, -x.p1.r_lo * xm0.x) + fmaf(x.p1.ds_hi * xm1.y, th1, -x.p1.r_hi * xm1.x);
+        epi_min(x.p0, x.p1, c, xm0, xm1, y0, y1);
     }
 };
 
@@ -507,10 +533,7 @@ template <> struct HU<T_Q5_K> {
     }
     __device__ static __forceinline__ void epi(const Ctx& x, const float (&c)[4][4], float4 xm0, float4 xm1, int, int,
                                                float& y0, float& y1) {
-        const float tl0 = csum_g(c[0]) + csum_g(c[1]), th0 = csum_g(c[2]) + csum_g(c[3]);
-        const float tl1 = csum_g8(c[0]) + csum_g8(c[1]), th1 = csum_g8(c[2]) + csum_g8(c[3]);
-        y0 += fmaf(x.p0.ds_lo * xm0.y, tl0, -x.p0.r_lo * xm0.x) + fmaf(x.p0.ds_hi * xm1.y, th0, -x.p0.r_hi * xm1.x);
-        y1 += fmaf(x.p1.ds_lo * xm0.y, tl1, -x.p1.r_lo * xm0.x) + fmaf(x.p1.ds_hi * xm1.y, th1, -x.p1.r_hi * xm1.x);
+        HU<T_Q4_K>::epi_min(x.p0, x.p1, c, xm0, xm1, y0, y1);
     }
 };
 
