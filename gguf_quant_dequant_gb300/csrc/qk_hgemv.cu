@@ -42,6 +42,7 @@ using namespace hm;
 constexpr int kCW = 8;                      // consumer warps
 constexpr int kThreads = (kCW + 1) * 32;    // + one producer warp
 constexpr int kTileRows = 16;               // rows per MMA tile
+constexpr int kPartW = 4 * kTileRows;       // partial sums per (tile pass, token, warp): a row's four threads each
 constexpr int kUnitW = 256;                 // weights per unit (16 rows x 256 weights: one warp's work item)
 constexpr int kXBB = 128;                   // prepared bytes per x-block: 2 planes x 8 words x 8 bytes
 constexpr int kMaxGroup = QK_GEMV_BATCH_MAX;
@@ -145,7 +146,10 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     uint64_t* empty = full + p.stages;
     volatile int* abort = reinterpret_cast<volatile int*>(empty + p.stages);
-    float* part = reinterpret_cast<float*>(smem + p.off_red);   // [tile pass][token][kCW][16]
+    // Partial sums [tile pass][token][kCW][64]: per warp, row g's sums of the
+    // four threads of its group t at t * 8 + g, row g + 8's at 32 + t * 8 + g
+    // (32 consecutive words for a warp's 32 lanes).
+    float* part = reinterpret_cast<float*>(smem + p.off_red);
     uint8_t* xb = smem + p.off_xb;
     float4* xm = reinterpret_cast<float4*>(smem + p.off_xm);
     float* xst = reinterpret_cast<float*>(smem + p.off_xs);   // [warp][token][256] staged x
@@ -241,8 +245,8 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
     const int g = lane >> 2, t = lane & 3;
     // This warp's partial sums start at zero (only this warp adds into them
     // until the final barrier).
-    for (int i = lane; i < ntiles * npass * MT * kTileRows; i += 32)
-        part[((i >> 4) * kCW + warp) * kTileRows + (i & 15)] = 0.0f;
+    for (int i = lane; i < ntiles * npass * MT * kPartW; i += 32)
+        part[((i >> 6) * kCW + warp) * kPartW + (i & 63)] = 0.0f;
     // This warp's prepared x: its unit of the current chunk, per token.
     uint8_t* xbw = xb + warp * MT * (8 * kXBB);
     float4* xmw = xm + warp * MT * 8;
@@ -324,18 +328,14 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
                     s = 0;
                     ph ^= 1u;
                 }
-                // Row sums of this unit: the four threads of a row.
+                // Each thread keeps its own sums of rows g and g + 8 (the four
+                // threads of a row are added at the end).
+                if (act) {
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    float a = y0[m], b = y1[m];
-                    a += __shfl_xor_sync(0xffffffffu, a, 1);
-                    a += __shfl_xor_sync(0xffffffffu, a, 2);
-                    b += __shfl_xor_sync(0xffffffffu, b, 1);
-                    b += __shfl_xor_sync(0xffffffffu, b, 2);
-                    if (t == 0 && act) {
-                        float* pp = part + (((tile * npass + pass) * MT + m) * kCW + warp) * kTileRows;
-                        pp[g] += a;
-                        pp[g + 8] += b;
+                    for (int m = 0; m < MT; ++m) {
+                        float* pp = part + (((tile * npass + pass) * MT + m) * kCW + warp) * kPartW + t * 8 + g;
+                        pp[0] += y0[m];
+                        pp[32] += y1[m];
                     }
                 }
             }
@@ -346,14 +346,19 @@ __global__ void __launch_bounds__(kThreads, 2) hgemv_kernel(const Args p) {
     for (int i = ctid; i < nrows * MT; i += kCW * 32) {
         const int m = i / nrows, ri = i - m * nrows;
         const int tile = ri / kTileRows, r = ri % kTileRows;
-        const float* pp = part + ((tile * npass) * MT + m) * kCW * kTileRows + r;
+        const float* pp = part + ((tile * npass) * MT + m) * kCW * kPartW + (r < 8 ? r : 24 + r);
+        // Warps in order, the four threads of the row in order within each.
         float v = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kCW; ++w) v += pp[w * kTileRows];
+        for (int w = 0; w < kCW; ++w)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v += pp[w * kPartW + 8 * q];
         if (SWI) {   // h = SiLU(g) * u, SiLU(g) = g / (1 + e^-g)
             float uu = 0.0f;
 #pragma unroll
-            for (int w = 0; w < kCW; ++w) uu += pp[(kCW + w) * kTileRows];
+            for (int w = 0; w < kCW; ++w)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) uu += pp[(kCW + w) * kPartW + 8 * q];
             v = v / (1.0f + expf(-v)) * uu;
         }
         ym[(int64_t)m * p.ystride + r_begin + ri] = v;
@@ -420,12 +425,12 @@ PlanH planh(int type, int n, const int64_t* rows, int64_t cols, int sms, int mt,
     for (int i = n; i <= hg::kMaxGroup; ++i) p.cta0[i] = (int)g0;
     p.grid = (int)g0;
     // Layout: B fragments of each token, block sums of each token, partial
-    // sums [tile pass][token][8 warps][16], mbarriers + abort word, ring.
+    // sums [tile pass][token][8 warps][64], mbarriers + abort word, ring.
     const int64_t ntp = (per_cta + hg::kTileRows - 1) / hg::kTileRows * (swiglu ? 2 : 1);
     // Each consumer warp prepares its own unit of x, per token.
     const int64_t xbb = (int64_t)mt * hg::kCW * 8 * hg::kXBB;
     const int64_t xmb = (int64_t)mt * hg::kCW * 8 * 16;
-    const int64_t redb = ntp * mt * hg::kCW * hg::kTileRows * 4;
+    const int64_t redb = ntp * mt * hg::kCW * hg::kPartW * 4;
     const int64_t barb = 2 * hg::kMaxStages * 8 + 16;
     const int64_t xsb = (int64_t)mt * hg::kCW * 256 * 4;   // staged x, 32 bytes per lane per token
     p.off_xb = 0;
