@@ -227,16 +227,14 @@ template <> struct HU<T_Q4_K> {
         return r;
     }
     // y0, y1 += the unit's sums of rows g, g + 8 (low / high sub-block sums
-    // of group t in c[0] / c[2]): ds*2^e*t - r*X per sub-block, packed.
+    // of group t in c[0] / c[2], each the hi and lo columns): ds*2^e*t - r*X
+    // per sub-block.
     __device__ static __forceinline__ void epi_min(const Row& p0, const Row& p1, const float (&c)[4][4], float4 xm0,
                                                    float4 xm1, float& y0, float& y1) {
-        const float2 t0 = __fadd2_rn(make_float2(c[0][0], c[2][0]), make_float2(c[0][1], c[2][1]));   // row g
-        const float2 t1 = __fadd2_rn(make_float2(c[0][2], c[2][2]), make_float2(c[0][3], c[2][3]));   // row g + 8
-        const float2 e = make_float2(xm0.y, xm1.y), X = make_float2(xm0.x, xm1.x);
-        const float2 z0 = __ffma2_rn(__fmul2_rn(p0.ds, e), t0, __fmul2_rn(p0.nr, X));
-        const float2 z1 = __ffma2_rn(__fmul2_rn(p1.ds, e), t1, __fmul2_rn(p1.nr, X));
-        y0 += z0.x + z0.y;
-        y1 += z1.x + z1.y;
+        y0 += fmaf(p0.ds.x * xm0.y, c[0][0] + c[0][1], p0.nr.x * xm0.x) +
+              fmaf(p0.ds.y * xm1.y, c[2][0] + c[2][1], p0.nr.y * xm1.x);
+        y1 += fmaf(p1.ds.x * xm0.y, c[0][2] + c[0][3], p1.nr.x * xm0.x) +
+              fmaf(p1.ds.y * xm1.y, c[2][2] + c[2][3], p1.nr.y * xm1.x);
     }
     struct Ctx {
         uint32_t w0[8], w1[8];
