@@ -111,14 +111,19 @@ __device__ __forceinline__ void prep_unit_x(const float* xs, uint8_t* xb, float4
     // Words 2q and 2q+1: elements 8q + {0,2}, {1,3}, {4,6}, {5,7}; each pair
     // rounded to fp16 by one packed convert, its residual by another.
     constexpr int kPair[4][2] = {{0, 2}, {1, 3}, {4, 6}, {5, 7}};
+    // x' = x 2^-e on the loads' natural register pairs.
+    const float2 s01 = __fmul2_rn(make_float2(a.x, a.y), make_float2(down, down));
+    const float2 s23 = __fmul2_rn(make_float2(a.z, a.w), make_float2(down, down));
+    const float2 s45 = __fmul2_rn(make_float2(b.x, b.y), make_float2(down, down));
+    const float2 s67 = __fmul2_rn(make_float2(b.z, b.w), make_float2(down, down));
+    const float xs8[8] = {s01.x, s01.y, s23.x, s23.y, s45.x, s45.y, s67.x, s67.y};
     uint32_t hi[4], lo[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const float2 ab = __fmul2_rn(make_float2(v[kPair[k][0]], v[kPair[k][1]]), make_float2(down, down));
-        const __half2 h = __floats2half2_rn(ab.x, ab.y);
+        const float a0 = xs8[kPair[k][0]], b0 = xs8[kPair[k][1]];
+        const __half2 h = __floats2half2_rn(a0, b0);
         const float2 hf = __half22float2(h);
-        const float2 r = __ffma2_rn(hf, make_float2(-1.0f, -1.0f), ab);   // x' - hi, exact
-        const __half2 l = __floats2half2_rn(r.x, r.y);
+        const __half2 l = __floats2half2_rn(a0 - hf.x, b0 - hf.y);   // x' - hi, exact
         hi[k] = *reinterpret_cast<const uint32_t*>(&h);
         lo[k] = *reinterpret_cast<const uint32_t*>(&l);
     }

@@ -318,11 +318,25 @@ template <> struct HU<T_Q6_K> {
     }
     __device__ static __forceinline__ void epi(const Ctx& x, const float (&c)[4][4], float4 xm0, float4 xm1, int, int,
                                                float& y0, float& y1) {
-        auto sc = [](uint32_t s, int k) { return (float)(int8_t)((s >> (8 * k)) & 0xFFu); };
-        y0 += x.d0 * (xm0.y * fmaf(sc(x.s0, 0), csum_g(c[0]), sc(x.s0, 1) * csum_g(c[1])) +
-                      xm1.y * fmaf(sc(x.s0, 2), csum_g(c[2]), sc(x.s0, 3) * csum_g(c[3])));
-        y1 += x.d1 * (xm0.y * fmaf(sc(x.s1, 0), csum_g8(c[0]), sc(x.s1, 1) * csum_g8(c[1])) +
-                      xm1.y * fmaf(sc(x.s1, 2), csum_g8(c[2]), sc(x.s1, 3) * csum_g8(c[3])));
+        // The four int8 scales of a row as exact floats: each byte with its sign
+        // bit flipped (b + 128) in the mantissa of 2^23, less 2^23 + 128.
+        auto scales = [](uint32_t s, float (&f)[4]) {
+            const uint32_t u = s ^ 0x80808080u;
+            const float2 lo = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)),
+                                                     __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651))),
+                                         make_float2(-8388736.0f, -8388736.0f));
+            const float2 hi = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)),
+                                                     __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653))),
+                                         make_float2(-8388736.0f, -8388736.0f));
+            f[0] = lo.x; f[1] = lo.y; f[2] = hi.x; f[3] = hi.y;
+        };
+        float a[4], b[4];
+        scales(x.s0, a);
+        scales(x.s1, b);
+        y0 += x.d0 * (xm0.y * fmaf(a[0], csum_g(c[0]), a[1] * csum_g(c[1])) +
+                      xm1.y * fmaf(a[2], csum_g(c[2]), a[3] * csum_g(c[3])));
+        y1 += x.d1 * (xm0.y * fmaf(b[0], csum_g8(c[0]), b[1] * csum_g8(c[1])) +
+                      xm1.y * fmaf(b[2], csum_g8(c[2]), b[3] * csum_g8(c[3])));
     }
 };
 
