@@ -569,13 +569,22 @@ template <int T, int NB> struct SGeo {
 
 // Shared-memory map of the streaming kernel: ring (+16 bytes for word reads
 // past the last row), queries [G][D], p [warp][16][G], rescale factors
-// [warp][G], mbarriers and the abort word.
+// [warp][G], mbarriers and the abort word.  With the p V pass on the MMA
+// (kMmaV: Q8_0, d = 128, up to four query heads per kv head) the query area
+// is reused, once the queries are in registers, for a stage's B fragments
+// [4 blocks][8 position tiles][32 lanes][2 words] and the warps' tile maxima
+// [kSW][8] (four heads' scores, the V scales' magnitude), and there is no p
+// or rescale area.
 template <int T, int NB, int G> struct SMap {
     static constexpr int D = 32 * NB;
+    static constexpr bool kMmaV = T == T_Q8_0 && NB == 4 && G <= 4;
+    static constexpr int kBFrag = 4 * kSW * 32 * 2 * 4;   // B fragment bytes of a stage
+    static constexpr int QB = kMmaV ? kBFrag + kSW * 8 * 4 : G * D * 4;
+    static_assert(!kMmaV || QB >= G * D * 4, "the query area holds the queries first");
     __host__ __device__ static constexpr int off_q(int nstg) { return nstg * SGeo<T, NB>::STAGE + 16; }
-    __host__ __device__ static constexpr int off_p(int nstg) { return off_q(nstg) + G * D * 4; }
-    __host__ __device__ static constexpr int off_a(int nstg) { return off_p(nstg) + kSW * 16 * G * 4; }
-    __host__ __device__ static constexpr int off_bar(int nstg) { return (off_a(nstg) + kSW * G * 4 + 7) / 8 * 8; }
+    __host__ __device__ static constexpr int off_p(int nstg) { return off_q(nstg) + QB; }
+    __host__ __device__ static constexpr int off_a(int nstg) { return off_p(nstg) + (kMmaV ? 0 : kSW * 16 * G * 4); }
+    __host__ __device__ static constexpr int off_bar(int nstg) { return (off_a(nstg) + (kMmaV ? 0 : kSW * G * 4) + 7) / 8 * 8; }
     // + 128 bytes to align the ring.
     __host__ __device__ static constexpr int bytes(int nstg) { return off_bar(nstg) + 2 * kSMaxStages * 8 + 16 + 128; }
 };
@@ -664,190 +673,388 @@ __global__ void __launch_bounds__(kSThreads, 2) attn_stream_kernel(const __grid_
     for (int n = 0; n < NT; ++n)
 #pragma unroll
         for (int b = 0; b < NB; ++b) upr[n][b] = sup[4 * n + tq][b];
-    const int e0 = (lane * NB) & 31, eb = (lane * NB) >> 5;   // this lane's elements of V
-    const float kNegInf = -__int_as_float(0x7f800000);
-    float m_run[NT], l_part[NT];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-        m_run[n] = kNegInf;
-        l_part[n] = 0.0f;
-    }
-    // Sums of p V: heads in pairs (packed fp32 FMAs), this lane's elements.
-    constexpr int GP = (G + 1) / 2;
-    float2 acc[GP][NB];
-#pragma unroll
-    for (int h = 0; h < GP; ++h)
-#pragma unroll
-        for (int k = 0; k < NB; ++k) acc[h][k] = make_float2(0.0f, 0.0f);
-    float* spw = sp + warp * 16 * G;
-    float* saw = sa + warp * G;
-    int slot = 0;
-    uint32_t ph = 0;
-    bool dead = false;
-    for (int st = 0; st < nst; ++st) {
-        if (!dead && !mbar_wait_abortable(&full[slot], ph, status, abort)) dead = true;
-        const int jt = 16 * warp;
-        const int64_t tp0 = p0 + (int64_t)st * kSPos + jt;
-        const int nvalid = (int)max((int64_t)0, min((int64_t)16, p1 - tp0));
-        if (!dead && nvalid > 0) {
+    if constexpr (Mp::kMmaV) {
+        // p V on the fp16 MMA.  Per stage:
+        //  1. warp w scores its positions 16 w .. 16 w + 15 (as below);
+        //  2. the warps' tile maxima give the stage's maximum per head, the
+        //     same in every warp, so all warps' p share one reference;
+        //  3. thread (gq, tq) writes x = p d 2^E (d: the position's V block
+        //     scale) of its positions gq, gq + 8 and head tq for each V block,
+        //     as two fp16 terms hi = fp16(x), lo = fp16(x - hi), into the
+        //     stage's B fragments (k = position in the tile, column 2 h + term).
+        //     2^E brings the stage's largest |d| into [2^14, 2^15), so x stays
+        //     below the fp16 maximum and out of its subnormal range, where
+        //     hi + lo would keep fewer than 22 bits; the sums are rescaled when
+        //     E changes and divided by 2^E at the end;
+        //  4. warp w takes V block b = w & 3 as two 16-element MMA tiles
+        //     (rows g and g + 8 of tile j: elements 32 b + 4 g + 2 j and
+        //     32 b + 4 g + 2 j + 1) over position tiles 4 (w >> 2) .. + 3,
+        //     A = the codes transposed by byte permutes (exact in fp16),
+        //     accumulating in the MMA; an element's output is the sum of its
+        //     hi and lo columns.
+        // Warps w and w + 4 hold the same elements over different positions
+        // and are added at the end, as are the threads' softmax sums.
+        const float kNegInf = -__int_as_float(0x7f800000);
+        uint32_t* bfr = reinterpret_cast<uint32_t*>(base + Mp::off_q(nstg));
+        uint16_t* bfh = reinterpret_cast<uint16_t*>(bfr);
+        float* tmx = reinterpret_cast<float*>(base + Mp::off_q(nstg) + Mp::kBFrag);   // [kSW][8]
+        const int vb = warp & 3, pt0 = 4 * (warp >> 2);
+        const int voff = misg + vb * BB + 2 + 4 * gq;   // this thread's four codes of a V row
+        const bool hv = tq < G;
+        float m_run = kNegInf, l_part = 0.0f;
+        float cv[2][4] = {};
+        int e_run = 0;   // the sums cv are in units of 2^-e_run
+        int slot = 0;
+        uint32_t ph = 0;
+        bool dead = false;
+        for (int st = 0; st < nst; ++st) {
+            if (!dead && !mbar_wait_abortable(&full[slot], ph, status, abort)) dead = true;
+            const int jt = 16 * warp;
+            const int64_t sp0 = p0 + (int64_t)st * kSPos;
+            const int nvalid = (int)max((int64_t)0, min((int64_t)16, p1 - sp0 - jt));
+            const int svalid = (int)min((int64_t)kSPos, p1 - sp0);   // valid positions of the stage
             const uint8_t* kst = ring + slot * Gm::STAGE;
             const uint8_t* vst = kst + Gm::HALF;
-            // Scores of positions gq and gq + 8 of the tile.
-            const uint8_t* r0 = kst + (jt + gq) * Gm::SLOT + misg;
-            const uint8_t* r1 = r0 + 8 * Gm::SLOT;
-            const KAddr k0 = kaddr<T>(r0, tq), k1 = kaddr<T>(r1, tq);
-            float s0[NT], s1[NT];
+            const bool v0 = gq < nvalid, v1 = gq + 8 < nvalid;
+            float s0 = kNegInf, s1 = kNegInf;
+            if (!dead && nvalid > 0) {
+                const uint8_t* r0 = kst + (jt + gq) * Gm::SLOT + misg;
+                const uint8_t* r1 = r0 + 8 * Gm::SLOT;
+                const KAddr k0 = kaddr<T>(r0, tq), k1 = kaddr<T>(r1, tq);
+                float a0s = 0.0f, a1s = 0.0f;
 #pragma unroll
-            for (int n = 0; n < NT; ++n) s0[n] = s1[n] = 0.0f;
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                uint32_t a0[4], a1[4];
-                kcodes_at<T>(k0, b, a0);
-                kcodes_at<T>(k1, b, a1);
-                const float d0 = h2f(lds16(r0 + b * BB)), d1 = h2f(lds16(r1 + b * BB));
-#pragma unroll
-                for (int n = 0; n < NT; ++n) {
+                for (int b = 0; b < NB; ++b) {
+                    uint32_t a0[4], a1[4];
+                    kcodes_at<T>(k0, b, a0);
+                    kcodes_at<T>(k1, b, a1);
+                    const float d0 = h2f(lds16(r0 + b * BB)), d1 = h2f(lds16(r1 + b * BB));
                     float cc[4];
-                    hm::mma16816_z(cc, a0[0], a1[0], a0[1], a1[1], bq[b][0][n][0], bq[b][0][n][1]);
-                    hm::mma16816(cc, a0[2], a1[2], a0[3], a1[3], bq[b][1][n][0], bq[b][1][n][1]);
-                    s0[n] = fmaf(d0 * upr[n][b], cc[0] + cc[1], s0[n]);
-                    s1[n] = fmaf(d1 * upr[n][b], cc[2] + cc[3], s1[n]);
+                    hm::mma16816_z(cc, a0[0], a1[0], a0[1], a1[1], bq[b][0][0][0], bq[b][0][0][1]);
+                    hm::mma16816(cc, a0[2], a1[2], a0[3], a1[3], bq[b][1][0][0], bq[b][1][0][1]);
+                    a0s = fmaf(d0 * upr[0][b], cc[0] + cc[1], a0s);
+                    a1s = fmaf(d1 * upr[0][b], cc[2] + cc[3], a1s);
+                }
+                if (v0) s0 = scale * a0s;
+                if (v1) s1 = scale * a1s;
+            }
+            float mt = fmaxf(s0, s1);
+            // The largest |d| of V among the tile's rows (thread tq: block tq).
+            float dmx = fmaxf(fabsf(h2f(lds16(vst + (jt + gq) * Gm::SLOT + misg + tq * BB))),
+                              fabsf(h2f(lds16(vst + (jt + gq + 8) * Gm::SLOT + misg + tq * BB))));
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) dmx = fmaxf(dmx, __shfl_xor_sync(0xffffffffu, dmx, o));
+            if (gq == 0) tmx[warp * 8 + tq] = mt;
+            if (lane == 0) tmx[warp * 8 + 4] = dmx;
+            named_sync_stream_consumers();
+            float ms = tmx[tq], dm = tmx[4];
+#pragma unroll
+            for (int w = 1; w < kSW; ++w) {
+                ms = fmaxf(ms, tmx[w * 8 + tq]);
+                dm = fmaxf(dm, tmx[w * 8 + 4]);
+            }
+            const float mnew = fmaxf(m_run, ms);   // finite: the stage has a valid position
+            // 2^E with 2^14 <= dm 2^E < 2^15 (an all-zero stage keeps E).
+            const int e_st = dm > 0.0f ? 141 - (int)((__float_as_uint(dm) >> 23) & 255u) : e_run;
+            const float dsc = __uint_as_float((uint32_t)(127 + e_st) << 23);
+            const float alpha = expf(m_run - mnew);
+            const float calpha = alpha * __uint_as_float((uint32_t)(127 + e_st - e_run) << 23);   // x 2^(E - E_old)
+            m_run = mnew;
+            e_run = e_st;
+            const float pa = v0 ? expf(s0 - mnew) : 0.0f, pb = v1 ? expf(s1 - mnew) : 0.0f;
+            l_part = fmaf(l_part, alpha, pa + pb);
+            {
+                // (k = gq, column n) is half gq & 1 of word 0 of lane 4 n + gq / 2,
+                // k = gq + 8 the same half of word 1; columns 2 tq (hi) and
+                // 2 tq + 1 (lo) are lanes 8 tq + gq / 2 and 8 tq + 4 + gq / 2.
+                const uint8_t* rv0 = vst + (jt + gq) * Gm::SLOT + misg;
+                const uint8_t* rv1 = rv0 + 8 * Gm::SLOT;
+                const bool w0 = hv && v0 && !dead, w1 = hv && v1 && !dead;
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    const float x0 = w0 ? pa * (h2f(lds16(rv0 + b * BB)) * dsc) : 0.0f;
+                    const float x1 = w1 ? pb * (h2f(lds16(rv1 + b * BB)) * dsc) : 0.0f;
+                    const __half2 hi = __floats2half2_rn(x0, x1);
+                    const float2 hf = __half22float2(hi);
+                    const __half2 lo = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+                    uint16_t* q0 = bfh + (((b * kSW + warp) * 32 + 8 * tq + (gq >> 1)) * 2) * 2 + (gq & 1);
+                    q0[0] = __half_as_ushort(__low2half(hi));    // hi, k = gq
+                    q0[2] = __half_as_ushort(__high2half(hi));   // hi, k = gq + 8
+                    q0[16] = __half_as_ushort(__low2half(lo));   // lo (4 lanes on), k = gq
+                    q0[18] = __half_as_ushort(__high2half(lo));  // lo, k = gq + 8
                 }
             }
-            // Running softmax of head 4 n + tq over this warp's positions.
-            const bool v0 = gq < nvalid, v1 = gq + 8 < nvalid;
+            named_sync_stream_consumers();
+            if (!dead) {
 #pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                const float a0 = v0 ? scale * s0[n] : kNegInf, a1 = v1 ? scale * s1[n] : kNegInf;
-                float mt = fmaxf(a0, a1);
+                for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int o = 4; o < 32; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-                const float mnew = fmaxf(m_run[n], mt);   // finite: position 0 of the tile is valid
-                const float alpha = expf(m_run[n] - mnew);
-                const float pa = v0 ? expf(a0 - mnew) : 0.0f, pb = v1 ? expf(a1 - mnew) : 0.0f;
-                l_part[n] = fmaf(l_part[n], alpha, pa + pb);
-                m_run[n] = mnew;
-                const int h = 4 * n + tq;
-                if (h < G) {
-                    spw[gq * G + h] = pa;
-                    spw[(gq + 8) * G + h] = pb;
-                    if (gq == 0) saw[h] = alpha;
+                    for (int k = 0; k < 4; ++k) cv[j][k] *= calpha;   // columns 2 tq, 2 tq + 1: head tq
+                const uint8_t* vr = vst + (pt0 * 16 + 2 * tq) * Gm::SLOT + voff;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (16 * (pt0 + i) >= svalid) break;
+                    const uint8_t* vi = vr + i * 16 * Gm::SLOT;
+                    // Elements 4 gq .. 4 gq + 3 at positions 2 tq, 2 tq + 1, 2 tq + 8,
+                    // 2 tq + 9 of the tile (odd blocks' codes are 4-byte aligned).
+                    uint32_t cw4[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const uint8_t* a = vi + ((r & 1) + 8 * (r >> 1)) * Gm::SLOT;
+                        cw4[r] = (vb & 1) ? *reinterpret_cast<const uint32_t*>(a) : (lds16(a) | (lds16(a + 2) << 16));
+                    }
+                    const uint2 bf = *reinterpret_cast<const uint2*>(bfr + ((vb * kSW + pt0 + i) * 32 + lane) * 2);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        // Elements 2 j, 2 j + 1 of positions k, k + 1 as bytes [e@k, e'@k, e@k+1, e'@k+1].
+                        const uint32_t sel = j ? 0x7632u : 0x5410u;
+                        const uint32_t zl = __byte_perm(cw4[0], cw4[1], sel), zh = __byte_perm(cw4[2], cw4[3], sel);
+                        // 0x6480 ^ b = 1024 + 128 + (signed b); minus 1152.
+                        const uint32_t a0 = hm::hadd2(hm::and_xor(zl, 0x00FF00FFu, 0x64806480u), 0xE480E480u);
+                        const uint32_t a1 = hm::hadd2(hm::and_xor(zl >> 8, 0x00FF00FFu, 0x64806480u), 0xE480E480u);
+                        const uint32_t a2 = hm::hadd2(hm::and_xor(zh, 0x00FF00FFu, 0x64806480u), 0xE480E480u);
+                        const uint32_t a3 = hm::hadd2(hm::and_xor(zh >> 8, 0x00FF00FFu, 0x64806480u), 0xE480E480u);
+                        hm::mma16816(cv[j], a0, a1, a2, a3, bf.x, bf.y);
+                    }
                 }
             }
             __syncwarp();
-#pragma unroll
-            for (int h = 0; h < GP; ++h) {
-                const float2 al = make_float2(saw[2 * h], 2 * h + 1 < G ? saw[2 * h + 1] : 0.0f);
-#pragma unroll
-                for (int k = 0; k < NB; ++k) acc[h][k] = __fmul2_rn(acc[h][k], al);
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (++slot == nstg) {
+                slot = 0;
+                ph ^= 1u;
             }
-            // sum_j p_j d_j q_j: this lane's elements, every head (a full tile
-            // unrolled, so the loads of several positions are in flight).  The
-            // rows' alignment is the same in every position (misg; slots are
-            // 16-byte multiples), so the code reader is set up once.
-            const uint8_t* vt = vst + jt * Gm::SLOT + misg + eb * BB;
-            const Codes<T, (NB >= 4 ? NB / 4 : 1)> vc(vt, e0);
-            auto vrow = [&](int j) {
-                const uint8_t* vb = vt + j * Gm::SLOT;
-                const float dv = h2f(lds16(vb));
-                float vv[NB];
-                if constexpr (NB >= 4) {
-                    uint32_t cw[NB / 4];
-                    vc.load((uint32_t)(j * Gm::SLOT), cw);
-                    // Byte b as the fp32 2^23 + b (one byte permute), less
-                    // 2^23 and the code offset (Q8_0: bytes flipped to q + 128).
-                    constexpr float kOff = 8388608.0f + (T == T_Q8_0 ? 128.0f : (T == T_Q5_0 ? 16.0f : 8.0f));
+        }
+        // Softmax sums: the lanes of a head, then the warps in order; o: warps
+        // w and w + 4 in that order.
 #pragma unroll
-                    for (int w = 0; w < NB / 4; ++w) {
-                        const uint32_t u = T == T_Q8_0 ? cw[w] ^ 0x80808080u : cw[w];
-                        const float2 f01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)),
-                                                                  __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651))),
-                                                      make_float2(-kOff, -kOff));
-                        const float2 f23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)),
-                                                                  __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653))),
-                                                      make_float2(-kOff, -kOff));
-                        vv[4 * w] = f01.x; vv[4 * w + 1] = f01.y; vv[4 * w + 2] = f23.x; vv[4 * w + 3] = f23.y;
+        for (int o = 4; o < 32; o <<= 1) l_part += __shfl_xor_sync(0xffffffffu, l_part, o);
+        named_sync_stream_consumers();   // the ring is free
+        float* og = reinterpret_cast<float*>(ring);   // [G][D] o, [kSW][4] l, [4] m
+        float* lw = og + G * D;
+        float* mw = lw + kSW * 4;
+        if (gq == 0) {
+            lw[warp * 4 + tq] = l_part;
+            if (warp == 0) mw[tq] = m_run;
+        }
+        float* oh = og + tq * D + 32 * vb + 4 * gq;
+        const float unscale = __uint_as_float((uint32_t)(127 - e_run) << 23);   // 2^-E
+        if (warp < 4 && hv) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                oh[2 * j] = (cv[j][0] + cv[j][1]) * unscale;
+                oh[2 * j + 1] = (cv[j][2] + cv[j][3]) * unscale;
+            }
+        }
+        named_sync_stream_consumers();
+        if (warp >= 4 && hv) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                oh[2 * j] += (cv[j][0] + cv[j][1]) * unscale;
+                oh[2 * j + 1] += (cv[j][2] + cv[j][3]) * unscale;
+            }
+        }
+        named_sync_stream_consumers();
+        if (*abort) return;
+        for (int i = tid; i < G * D; i += kSW * 32) {
+            const int h = i / D, e = i - h * D;
+            float* dst = ws + ((int64_t)(g * G + h) * nsplit + c) * (D + 2);
+            dst[2 + e] = og[i];
+            if (e == 0) {
+                float L = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kSW; ++w) L += lw[w * 4 + h];
+                dst[0] = mw[h];
+                dst[1] = L;
+            }
+        }
+    } else {
+        const int e0 = (lane * NB) & 31, eb = (lane * NB) >> 5;   // this lane's elements of V
+        const float kNegInf = -__int_as_float(0x7f800000);
+        float m_run[NT], l_part[NT];
+    #pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            m_run[n] = kNegInf;
+            l_part[n] = 0.0f;
+        }
+        // Sums of p V: heads in pairs (packed fp32 FMAs), this lane's elements.
+        constexpr int GP = (G + 1) / 2;
+        float2 acc[GP][NB];
+    #pragma unroll
+        for (int h = 0; h < GP; ++h)
+    #pragma unroll
+            for (int k = 0; k < NB; ++k) acc[h][k] = make_float2(0.0f, 0.0f);
+        float* spw = sp + warp * 16 * G;
+        float* saw = sa + warp * G;
+        int slot = 0;
+        uint32_t ph = 0;
+        bool dead = false;
+        for (int st = 0; st < nst; ++st) {
+            if (!dead && !mbar_wait_abortable(&full[slot], ph, status, abort)) dead = true;
+            const int jt = 16 * warp;
+            const int64_t tp0 = p0 + (int64_t)st * kSPos + jt;
+            const int nvalid = (int)max((int64_t)0, min((int64_t)16, p1 - tp0));
+            if (!dead && nvalid > 0) {
+                const uint8_t* kst = ring + slot * Gm::STAGE;
+                const uint8_t* vst = kst + Gm::HALF;
+                // Scores of positions gq and gq + 8 of the tile.
+                const uint8_t* r0 = kst + (jt + gq) * Gm::SLOT + misg;
+                const uint8_t* r1 = r0 + 8 * Gm::SLOT;
+                const KAddr k0 = kaddr<T>(r0, tq), k1 = kaddr<T>(r1, tq);
+                float s0[NT], s1[NT];
+    #pragma unroll
+                for (int n = 0; n < NT; ++n) s0[n] = s1[n] = 0.0f;
+    #pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    uint32_t a0[4], a1[4];
+                    kcodes_at<T>(k0, b, a0);
+                    kcodes_at<T>(k1, b, a1);
+                    const float d0 = h2f(lds16(r0 + b * BB)), d1 = h2f(lds16(r1 + b * BB));
+    #pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        float cc[4];
+                        hm::mma16816_z(cc, a0[0], a1[0], a0[1], a1[1], bq[b][0][n][0], bq[b][0][n][1]);
+                        hm::mma16816(cc, a0[2], a1[2], a0[3], a1[3], bq[b][1][n][0], bq[b][1][n][1]);
+                        s0[n] = fmaf(d0 * upr[n][b], cc[0] + cc[1], s0[n]);
+                        s1[n] = fmaf(d1 * upr[n][b], cc[2] + cc[3], s1[n]);
                     }
-                } else {
-#pragma unroll
-                    for (int k = 0; k < NB; ++k) vv[k] = (float)code_at<T>(vb, e0 + k);
                 }
-                float pj[2 * GP];
-                if constexpr (G % 4 == 0) {
-#pragma unroll
-                    for (int h = 0; h < G; h += 4) {
-                        const float4 p4 = *reinterpret_cast<const float4*>(spw + j * G + h);
-                        pj[h] = p4.x; pj[h + 1] = p4.y; pj[h + 2] = p4.z; pj[h + 3] = p4.w;
+                // Running softmax of head 4 n + tq over this warp's positions.
+                const bool v0 = gq < nvalid, v1 = gq + 8 < nvalid;
+    #pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    const float a0 = v0 ? scale * s0[n] : kNegInf, a1 = v1 ? scale * s1[n] : kNegInf;
+                    float mt = fmaxf(a0, a1);
+    #pragma unroll
+                    for (int o = 4; o < 32; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+                    const float mnew = fmaxf(m_run[n], mt);   // finite: position 0 of the tile is valid
+                    const float alpha = expf(m_run[n] - mnew);
+                    const float pa = v0 ? expf(a0 - mnew) : 0.0f, pb = v1 ? expf(a1 - mnew) : 0.0f;
+                    l_part[n] = fmaf(l_part[n], alpha, pa + pb);
+                    m_run[n] = mnew;
+                    const int h = 4 * n + tq;
+                    if (h < G) {
+                        spw[gq * G + h] = pa;
+                        spw[(gq + 8) * G + h] = pb;
+                        if (gq == 0) saw[h] = alpha;
                     }
-                } else {
-#pragma unroll
-                    for (int h = 0; h < G; ++h) pj[h] = spw[j * G + h];
-                    if constexpr (G % 2) pj[G] = 0.0f;
                 }
-#pragma unroll
+                __syncwarp();
+    #pragma unroll
                 for (int h = 0; h < GP; ++h) {
-                    const float2 pd = __fmul2_rn(make_float2(pj[2 * h], pj[2 * h + 1]), make_float2(dv, dv));
-#pragma unroll
-                    for (int k = 0; k < NB; ++k) acc[h][k] = __ffma2_rn(pd, make_float2(vv[k], vv[k]), acc[h][k]);
+                    const float2 al = make_float2(saw[2 * h], 2 * h + 1 < G ? saw[2 * h + 1] : 0.0f);
+    #pragma unroll
+                    for (int k = 0; k < NB; ++k) acc[h][k] = __fmul2_rn(acc[h][k], al);
                 }
-            };
-            if (nvalid == 16) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) vrow(j);
-            } else {
-                for (int j = 0; j < nvalid; ++j) vrow(j);
+                // sum_j p_j d_j q_j: this lane's elements, every head (a full tile
+                // unrolled, so the loads of several positions are in flight).  The
+                // rows' alignment is the same in every position (misg; slots are
+                // 16-byte multiples), so the code reader is set up once.
+                const uint8_t* vt = vst + jt * Gm::SLOT + misg + eb * BB;
+                const Codes<T, (NB >= 4 ? NB / 4 : 1)> vc(vt, e0);
+                auto vrow = [&](int j) {
+                    const uint8_t* vb = vt + j * Gm::SLOT;
+                    const float dv = h2f(lds16(vb));
+                    float vv[NB];
+                    if constexpr (NB >= 4) {
+                        uint32_t cw[NB / 4];
+                        vc.load((uint32_t)(j * Gm::SLOT), cw);
+                        // Byte b as the fp32 2^23 + b (one byte permute), less
+                        // 2^23 and the code offset (Q8_0: bytes flipped to q + 128).
+                        constexpr float kOff = 8388608.0f + (T == T_Q8_0 ? 128.0f : (T == T_Q5_0 ? 16.0f : 8.0f));
+    #pragma unroll
+                        for (int w = 0; w < NB / 4; ++w) {
+                            const uint32_t u = T == T_Q8_0 ? cw[w] ^ 0x80808080u : cw[w];
+                            const float2 f01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)),
+                                                                      __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651))),
+                                                          make_float2(-kOff, -kOff));
+                            const float2 f23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)),
+                                                                      __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653))),
+                                                          make_float2(-kOff, -kOff));
+                            vv[4 * w] = f01.x; vv[4 * w + 1] = f01.y; vv[4 * w + 2] = f23.x; vv[4 * w + 3] = f23.y;
+                        }
+                    } else {
+    #pragma unroll
+                        for (int k = 0; k < NB; ++k) vv[k] = (float)code_at<T>(vb, e0 + k);
+                    }
+                    float pj[2 * GP];
+                    if constexpr (G % 4 == 0) {
+    #pragma unroll
+                        for (int h = 0; h < G; h += 4) {
+                            const float4 p4 = *reinterpret_cast<const float4*>(spw + j * G + h);
+                            pj[h] = p4.x; pj[h + 1] = p4.y; pj[h + 2] = p4.z; pj[h + 3] = p4.w;
+                        }
+                    } else {
+    #pragma unroll
+                        for (int h = 0; h < G; ++h) pj[h] = spw[j * G + h];
+                        if constexpr (G % 2) pj[G] = 0.0f;
+                    }
+    #pragma unroll
+                    for (int h = 0; h < GP; ++h) {
+                        const float2 pd = __fmul2_rn(make_float2(pj[2 * h], pj[2 * h + 1]), make_float2(dv, dv));
+    #pragma unroll
+                        for (int k = 0; k < NB; ++k) acc[h][k] = __ffma2_rn(pd, make_float2(vv[k], vv[k]), acc[h][k]);
+                    }
+                };
+                if (nvalid == 16) {
+    #pragma unroll
+                    for (int j = 0; j < 16; ++j) vrow(j);
+                } else {
+                    for (int j = 0; j < nvalid; ++j) vrow(j);
+                }
+                __syncwarp();   // spw and saw are rewritten by the next tile
             }
-            __syncwarp();   // spw and saw are rewritten by the next tile
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (++slot == nstg) {
+                slot = 0;
+                ph ^= 1u;
+            }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        if (++slot == nstg) {
-            slot = 0;
-            ph ^= 1u;
+        // The softmax sums of the warp's positions: the lanes of a head.
+    #pragma unroll
+        for (int n = 0; n < NT; ++n)
+    #pragma unroll
+            for (int o = 4; o < 32; o <<= 1) l_part[n] += __shfl_xor_sync(0xffffffffu, l_part[n], o);
+        // Merge the warps in order (the ring is free now): per warp and head,
+        // (m, l, o[D]) in shared memory, then per output element.
+        named_sync_stream_consumers();
+        float* mg = reinterpret_cast<float*>(ring);   // [kSW][G][D + 2]
+    #pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const int h = 4 * n + tq;
+            if (h < G && gq == 0) {
+                mg[(warp * G + h) * (D + 2)] = m_run[n];
+                mg[(warp * G + h) * (D + 2) + 1] = l_part[n];
+            }
         }
-    }
-    // The softmax sums of the warp's positions: the lanes of a head.
-#pragma unroll
-    for (int n = 0; n < NT; ++n)
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) l_part[n] += __shfl_xor_sync(0xffffffffu, l_part[n], o);
-    // Merge the warps in order (the ring is free now): per warp and head,
-    // (m, l, o[D]) in shared memory, then per output element.
-    named_sync_stream_consumers();
-    float* mg = reinterpret_cast<float*>(ring);   // [kSW][G][D + 2]
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-        const int h = 4 * n + tq;
-        if (h < G && gq == 0) {
-            mg[(warp * G + h) * (D + 2)] = m_run[n];
-            mg[(warp * G + h) * (D + 2) + 1] = l_part[n];
-        }
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int k = 0; k < NB; ++k)
-            mg[(warp * G + h) * (D + 2) + 2 + lane * NB + k] = (h & 1) ? acc[h >> 1][k].y : acc[h >> 1][k].x;
-    named_sync_stream_consumers();
-    if (*abort) return;
-    for (int i = tid; i < G * D; i += kSW * 32) {
-        const int h = i / D, e = i - h * D;
-        float M = kNegInf;
-#pragma unroll
-        for (int w = 0; w < kSW; ++w) M = fmaxf(M, mg[(w * G + h) * (D + 2)]);
-        float o = 0.0f, L = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kSW; ++w) {
-            const float* r = mg + (w * G + h) * (D + 2);
-            const float f = expf(r[0] - M);   // 0 for a warp with no position
-            o = fmaf(f, r[2 + e], o);
-            L = fmaf(f, r[1], L);
-        }
-        float* dst = ws + ((int64_t)(g * G + h) * nsplit + c) * (D + 2);
-        dst[2 + e] = o;
-        if (e == 0) {
-            dst[0] = M;
-            dst[1] = L;
+    #pragma unroll
+        for (int h = 0; h < G; ++h)
+    #pragma unroll
+            for (int k = 0; k < NB; ++k)
+                mg[(warp * G + h) * (D + 2) + 2 + lane * NB + k] = (h & 1) ? acc[h >> 1][k].y : acc[h >> 1][k].x;
+        named_sync_stream_consumers();
+        if (*abort) return;
+        for (int i = tid; i < G * D; i += kSW * 32) {
+            const int h = i / D, e = i - h * D;
+            float M = kNegInf;
+    #pragma unroll
+            for (int w = 0; w < kSW; ++w) M = fmaxf(M, mg[(w * G + h) * (D + 2)]);
+            float o = 0.0f, L = 0.0f;
+    #pragma unroll
+            for (int w = 0; w < kSW; ++w) {
+                const float* r = mg + (w * G + h) * (D + 2);
+                const float f = expf(r[0] - M);   // 0 for a warp with no position
+                o = fmaf(f, r[2 + e], o);
+                L = fmaf(f, r[1], L);
+            }
+            float* dst = ws + ((int64_t)(g * G + h) * nsplit + c) * (D + 2);
+            dst[2 + e] = o;
+            if (e == 0) {
+                dst[0] = M;
+                dst[1] = L;
+            }
         }
     }
 }
