@@ -572,13 +572,15 @@ template <int T, int NB> struct SGeo {
 // [warp][G], mbarriers and the abort word.  With the p V pass on the MMA
 // (kMmaV: Q8_0, d = 128, up to four query heads per kv head) the query area
 // is reused, once the queries are in registers, for a stage's B fragments
-// [4 blocks][8 position tiles][32 lanes][2 words] and the warps' tile maxima
+// [4 blocks][8 position tiles][36 lane slots][2 words] (lanes 16..31 four
+// slots on, so that a warp's 16-bit fragment stores meet distinct banks)
+// and the warps' tile maxima
 // [kSW][8] (four heads' scores, the V scales' magnitude), and there is no p
 // or rescale area.
 template <int T, int NB, int G> struct SMap {
     static constexpr int D = 32 * NB;
     static constexpr bool kMmaV = T == T_Q8_0 && NB == 4 && G <= 4;
-    static constexpr int kBFrag = 4 * kSW * 32 * 2 * 4;   // B fragment bytes of a stage
+    static constexpr int kBFrag = 4 * kSW * 36 * 2 * 4;   // B fragment bytes of a stage
     static constexpr int QB = kMmaV ? kBFrag + kSW * 8 * 4 : G * D * 4;
     static_assert(!kMmaV || QB >= G * D * 4, "the query area holds the queries first");
     __host__ __device__ static constexpr int off_q(int nstg) { return nstg * SGeo<T, NB>::STAGE + 16; }
@@ -767,7 +769,8 @@ __global__ void __launch_bounds__(kSThreads, 2) attn_stream_kernel(const __grid_
             {
                 // (k = gq, column n) is half gq & 1 of word 0 of lane 4 n + gq / 2,
                 // k = gq + 8 the same half of word 1; columns 2 tq (hi) and
-                // 2 tq + 1 (lo) are lanes 8 tq + gq / 2 and 8 tq + 4 + gq / 2.
+                // 2 tq + 1 (lo) are lanes 8 tq + gq / 2 and 8 tq + 4 + gq / 2
+                // (lane l in slot l + 4 (l >> 4)).
                 const uint8_t* rv0 = vst + (jt + gq) * Gm::SLOT + misg;
                 const uint8_t* rv1 = rv0 + 8 * Gm::SLOT;
                 const bool w0 = hv && v0 && !dead, w1 = hv && v1 && !dead;
@@ -778,7 +781,7 @@ __global__ void __launch_bounds__(kSThreads, 2) attn_stream_kernel(const __grid_
                     const __half2 hi = __floats2half2_rn(x0, x1);
                     const float2 hf = __half22float2(hi);
                     const __half2 lo = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
-                    uint16_t* q0 = bfh + (((b * kSW + warp) * 32 + 8 * tq + (gq >> 1)) * 2) * 2 + (gq & 1);
+                    uint16_t* q0 = bfh + (((b * kSW + warp) * 36 + 8 * tq + 4 * (tq >> 1) + (gq >> 1)) * 2) * 2 + (gq & 1);
                     q0[0] = __half_as_ushort(__low2half(hi));    // hi, k = gq
                     q0[2] = __half_as_ushort(__high2half(hi));   // hi, k = gq + 8
                     q0[16] = __half_as_ushort(__low2half(lo));   // lo (4 lanes on), k = gq
@@ -804,7 +807,7 @@ __global__ void __launch_bounds__(kSThreads, 2) attn_stream_kernel(const __grid_
                         const uint8_t* a = vi + ((r & 1) + 8 * (r >> 1)) * Gm::SLOT;
                         cw4[r] = (vb & 1) ? *reinterpret_cast<const uint32_t*>(a) : (lds16(a) | (lds16(a + 2) << 16));
                     }
-                    const uint2 bf = *reinterpret_cast<const uint2*>(bfr + ((vb * kSW + pt0 + i) * 32 + lane) * 2);
+                    const uint2 bf = *reinterpret_cast<const uint2*>(bfr + ((vb * kSW + pt0 + i) * 36 + lane + 4 * (lane >> 4)) * 2);
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         // Elements 2 j, 2 j + 1 of positions k, k + 1 as bytes [e@k, e'@k, e@k+1, e'@k+1].

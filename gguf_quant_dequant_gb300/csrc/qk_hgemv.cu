@@ -93,7 +93,6 @@ __device__ __forceinline__ void load_unit_x(const float* __restrict__ x, int nxb
 __device__ __forceinline__ void prep_unit_x(const float* xs, uint8_t* xb, float4* xm, int lane) {
     const int jl = lane >> 2, q = lane & 3;
     const float4 a = *reinterpret_cast<const float4*>(xs + 8 * lane), b = *reinterpret_cast<const float4*>(xs + 8 * lane + 4);
-    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     const float amax_a = fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w)));
     float amax = fmaxf(amax_a, fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
     // The eight elements' sum by packed pair adds (any order: an fp32 block sum).
