@@ -548,7 +548,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __
 // on the MMA as in the chunk kernel, then p = e^(s - m) rescales and feeds
 // its fp32 sums of p V (lane l owns d/32 elements of V for every head).  At
 // the end the eight warps' (m, l, o) are merged in warp order: the result
-// does not depend on timing.
+// does not depend on timing.  For Q8_0 with d = 128 and up to four query
+// heads per kv head, p V runs on the MMA too (the kMmaV form below): the
+// warps share each stage's softmax reference, and warp w sums one V block
+// over half the stage's positions.
 constexpr int kSW = 8;                      // consumer warps
 constexpr int kSThreads = (kSW + 1) * 32;   // + the producer warp
 constexpr int kSPos = 16 * kSW;             // positions per stage
