@@ -548,8 +548,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_chunk_kernel(const float* __
 // on the MMA as in the chunk kernel, then p = e^(s - m) rescales and feeds
 // its fp32 sums of p V (lane l owns d/32 elements of V for every head).  At
 // the end the eight warps' (m, l, o) are merged in warp order: the result
-// does not depend on timing.  For Q8_0 with d = 128 and up to four query
-// heads per kv head, p V runs on the MMA too (the kMmaV form below): the
+// does not depend on timing.  For Q8_0 and Q4_0 with d = 128 and up to four
+// query heads per kv head, p V runs on the MMA too (the kMmaV form below): the
 // warps share each stage's softmax reference, and warp w sums one V block
 // over half the stage's positions.
 constexpr int kSW = 8;                      // consumer warps
@@ -573,7 +573,7 @@ template <int T, int NB> struct SGeo {
 // Shared-memory map of the streaming kernel: ring (+16 bytes for word reads
 // past the last row), queries [G][D], p [warp][16][G], rescale factors
 // [warp][G], mbarriers and the abort word.  With the p V pass on the MMA
-// (kMmaV: Q8_0, d = 128, up to four query heads per kv head) the query area
+// (kMmaV: Q8_0 or Q4_0, d = 128, up to four query heads per kv head) the query area
 // is reused, once the queries are in registers, for a stage's B fragments
 // [4 blocks][8 position tiles][36 lane slots][2 words] (lanes 16..31 four
 // slots on, so that a warp's 16-bit fragment stores meet distinct banks)
@@ -582,7 +582,7 @@ template <int T, int NB> struct SGeo {
 // or rescale area.
 template <int T, int NB, int G> struct SMap {
     static constexpr int D = 32 * NB;
-    static constexpr bool kMmaV = T == T_Q8_0 && NB == 4 && G <= 4;
+    static constexpr bool kMmaV = (T == T_Q8_0 || T == T_Q4_0) && NB == 4 && G <= 4;
     static constexpr int kBFrag = 4 * kSW * 36 * 2 * 4;   // B fragment bytes of a stage
     static constexpr int QB = kMmaV ? kBFrag + kSW * 8 * 4 : G * D * 4;
     static_assert(!kMmaV || QB >= G * D * 4, "the query area holds the queries first");
@@ -694,7 +694,9 @@ __global__ void __launch_bounds__(kSThreads, 2) attn_stream_kernel(const __grid_
         //  4. warp w takes V block b = w & 3 as two 16-element MMA tiles
         //     (rows g and g + 8 of tile j: elements 32 b + 4 g + 2 j and
         //     32 b + 4 g + 2 j + 1) over position tiles 4 (w >> 2) .. + 3,
-        //     A = the codes transposed by byte permutes (exact in fp16),
+        //     A = the codes transposed by byte permutes (exact in fp16; a
+        //     Q4_0 lane takes the low nibbles of bytes 4 g .. 4 g + 3 for
+        //     g < 4, the high nibbles of the same bytes for g >= 4),
         //     accumulating in the MMA; an element's output is the sum of its
         //     hi and lo columns.
         // Warps w and w + 4 hold the same elements over different positions
@@ -704,7 +706,15 @@ __global__ void __launch_bounds__(kSThreads, 2) attn_stream_kernel(const __grid_
         uint16_t* bfh = reinterpret_cast<uint16_t*>(bfr);
         float* tmx = reinterpret_cast<float*>(base + Mp::off_q(nstg) + Mp::kBFrag);   // [kSW][8]
         const int vb = warp & 3, pt0 = 4 * (warp >> 2);
-        const int voff = misg + vb * BB + 2 + 4 * gq;   // this thread's four codes of a V row
+        // This thread's four codes of a V row (Q4_0: lanes gq and gq + 4 read
+        // the same bytes, low and high nibbles).
+        const int voff = misg + vb * BB + 2 + 4 * (T == T_Q4_0 ? (gq & 3) : gq);
+        // Code pairs to exact fp16 integers: (bytes & mask) | magic, then
+        // minus the magic and the type's offset.
+        const bool hin = T == T_Q4_0 && gq >= 4;
+        const uint32_t cmask = T == T_Q8_0 ? 0x00FF00FFu : (hin ? 0x00F000F0u : 0x000F000Fu);
+        const uint32_t cmag = T == T_Q8_0 ? 0x64806480u : (hin ? 0x54005400u : 0x64006400u);
+        const uint32_t cneg = T == T_Q8_0 ? 0xE480E480u : (hin ? 0xD480D480u : 0xE408E408u);
         const bool hv = tq < G;
         float m_run = kNegInf, l_part = 0.0f;
         float cv[2][4] = {};
@@ -816,11 +826,21 @@ __global__ void __launch_bounds__(kSThreads, 2) attn_stream_kernel(const __grid_
                         // Elements 2 j, 2 j + 1 of positions k, k + 1 as bytes [e@k, e'@k, e@k+1, e'@k+1].
                         const uint32_t sel = j ? 0x7632u : 0x5410u;
                         const uint32_t zl = __byte_perm(cw4[0], cw4[1], sel), zh = __byte_perm(cw4[2], cw4[3], sel);
-                        // 0x6480 ^ b = 1024 + 128 + (signed b); minus 1152.
-                        const uint32_t a0 = hm::hadd2(hm::and_xor(zl, 0x00FF00FFu, 0x64806480u), 0xE480E480u);
-                        const uint32_t a1 = hm::hadd2(hm::and_xor(zl >> 8, 0x00FF00FFu, 0x64806480u), 0xE480E480u);
-                        const uint32_t a2 = hm::hadd2(hm::and_xor(zh, 0x00FF00FFu, 0x64806480u), 0xE480E480u);
-                        const uint32_t a3 = hm::hadd2(hm::and_xor(zh >> 8, 0x00FF00FFu, 0x64806480u), 0xE480E480u);
+                        // Q8_0: 0x6480 ^ b = 1024 + 128 + (signed b), minus 1152.  Q4_0:
+                        // 1024 + q (low nibble) or 64 + q (high nibble, unit 1/16
+                        // there), minus that and 8.
+                        uint32_t a0, a1, a2, a3;
+                        if constexpr (T == T_Q8_0) {
+                            a0 = hm::hadd2(hm::and_xor(zl, cmask, cmag), cneg);
+                            a1 = hm::hadd2(hm::and_xor(zl >> 8, cmask, cmag), cneg);
+                            a2 = hm::hadd2(hm::and_xor(zh, cmask, cmag), cneg);
+                            a3 = hm::hadd2(hm::and_xor(zh >> 8, cmask, cmag), cneg);
+                        } else {
+                            a0 = hm::hadd2(hm::and_or(zl, cmask, cmag), cneg);
+                            a1 = hm::hadd2(hm::and_or(zl >> 8, cmask, cmag), cneg);
+                            a2 = hm::hadd2(hm::and_or(zh, cmask, cmag), cneg);
+                            a3 = hm::hadd2(hm::and_or(zh >> 8, cmask, cmag), cneg);
+                        }
                         hm::mma16816(cv[j], a0, a1, a2, a3, bf.x, bf.y);
                     }
                 }

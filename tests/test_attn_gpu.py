@@ -122,24 +122,25 @@ def test_attn_decode_maximum_positions(gpu):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("name", ["Q8_0", "Q4_0"])
 @pytest.mark.parametrize("v_scale", [1e-7, 1e-5, 1e-2, 50.0, "mixed"])
-def test_attn_decode_v_scale_range(gpu, v_scale):
-    # Q8_0, d = 128, four query heads per kv head (p V on the MMA with the
-    # stage's power-of-two scale): V block scales from fp16 subnormals
-    # (1e-7) to ~200, and a cache whose positions alternate between scales
-    # 2^20 apart inside every stage.
-    t, Tn, nh, nkv, d = qk.Q8_0, 1000, 16, 4, 128
-    K = synth.random_blocks("Q8_0", Tn * nkv, d, 1400)
+def test_attn_decode_v_scale_range(gpu, name, v_scale):
+    # d = 128, four query heads per kv head (p V on the MMA with the stage's
+    # power-of-two scale): V block scales from fp16 subnormals (1e-7) to
+    # ~200, and a cache whose positions mix scales 2^30 apart inside every
+    # stage.
+    t, Tn, nh, nkv, d = type_id(name), 1000, 16, 4, 128
+    K = synth.random_blocks(name, Tn * nkv, d, 1400)
     if v_scale == "mixed":
-        V = synth.random_blocks("Q8_0", Tn * nkv, d, 1401).copy()
-        blocks = V.reshape(-1, 34)
+        V = synth.random_blocks(name, Tn * nkv, d, 1401).copy()
+        blocks = V.reshape(-1, qk.block_bytes(t))
         dv = blocks[:, :2].copy().view(np.float16).astype(np.float32)
         pos = np.arange(blocks.shape[0]) // (nkv * d // 32)
         dv[pos % 3 == 1] *= 2.0 ** -20
         dv[pos % 7 == 2] *= 2.0 ** 10
         blocks[:, :2] = dv.astype(np.float16).view(np.uint8).reshape(-1, 2)
     else:
-        V = synth.random_blocks("Q8_0", Tn * nkv, d, 1401, d_scale=v_scale)
+        V = synth.random_blocks(name, Tn * nkv, d, 1401, d_scale=v_scale)
     q = synth.activations(nh, d, 1402)
     out = qk.attn_decode(t, torch.from_numpy(q).to(gpu), dev_u8(K, gpu), dev_u8(V, gpu), Tn, nh, nkv, d,
                          1.0 / np.sqrt(d)).cpu().numpy()
@@ -147,4 +148,4 @@ def test_attn_decode_v_scale_range(gpu, v_scale):
     ref, Sv = oracle.attn_decode(t, q, K, V, Tn, nh, nkv, d, 1.0 / np.sqrt(d))
     assert np.isfinite(out).all()
     err = np.abs(out - ref) - (RTOL * Sv + 1e-6)
-    assert (err <= 0).all(), f"V scale {v_scale}: worst excess {err.max():.3e}"
+    assert (err <= 0).all(), f"{name} V scale {v_scale}: worst excess {err.max():.3e}"
