@@ -164,11 +164,17 @@ qk_status qk_quantize(int type, const float* w, int64_t rows, int64_t cols, void
  *   d      32, 64, 128 or 256; n_heads a multiple of n_kv, at most 8 query
  *          heads per kv head; 1 <= T <= 65535 * 256.
  *   out    fp32 [n_heads, d]; ws at least qk_attn_decode_workspace bytes.
- * Positions are split in chunks of 192 (Q8_0) or 256 (Q5_0, Q4_0) (one CTA
- * per kv head and chunk, the cache streamed once); each chunk keeps its max
- * score, sum of exponentials and weighted value sum, and a second launch
- * combines the chunks (log-sum-exp) in a fixed order: deterministic.  fp32
- * arithmetic.
+ * Positions are split over CTAs (one CTA per kv head and range of
+ * positions, about T / (2 SMs / n_kv) of them; shapes whose per-thread state
+ * does not fit take chunks of 192 or 256), the cache streamed once; each
+ * range keeps its max score, sum of exponentials and weighted value sum, and
+ * a second launch combines the ranges (log-sum-exp) in a fixed order:
+ * deterministic.  Scores on the fp16 tensor-core MMA (exact codes, each
+ * query element as two fp16 terms after a power-of-two scale per 32-block),
+ * fp32 softmax; the p V sums in fp32, or for Q8_0 / Q4_0 with d = 128 and
+ * up to four query heads per kv head on the MMA with p d as two fp16 terms
+ * after a power-of-two scale per 128 positions.  Accuracy: |out - out_exact|
+ * <= 2e-4 * sum_t p_t |V[t, g, i]| + 1e-6.
  * Errors: QK_ERR_TYPE, QK_ERR_SHAPE, QK_ERR_NULL, QK_ERR_ALIGN,
  * QK_ERR_WORKSPACE. */
 size_t qk_attn_decode_workspace(int type, int64_t T, int n_heads, int n_kv, int d);
