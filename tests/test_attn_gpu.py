@@ -98,6 +98,8 @@ def test_attn_decode_deterministic(gpu):
     ("Q8_0", 290, 8, 1, 32),     # eight heads, d = 32 (whole blocks per lane)
     ("Q5_0", 700, 32, 4, 256),   # eight heads, d = 256: the runtime-group path
     ("Q4_0", 100, 2, 1, 32),     # two heads, d = 32: the runtime-group path
+    ("Q8_0", 333, 8, 4, 128),    # two heads, d = 128: p V on the MMA, half its columns
+    ("Q4_0", 257, 4, 2, 128),    # the same for Q4_0, a ragged last stage
 ])
 def test_attn_decode_every_group_path(gpu, name, Tn, nh, nkv, d):
     out, ref, Sv = run(gpu, name, Tn, nh, nkv, d, 1100 + Tn + d)
